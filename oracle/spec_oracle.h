@@ -1,0 +1,101 @@
+/*
+ * spec_oracle.h -- float64 CPU oracle for batched speculative-sampling
+ * verification.  TEST INFRASTRUCTURE: only the tests, the smoke check and the
+ * benchmark's CPU-baseline leg may call it.  It shares no code, header, table
+ * or helper with the CUDA library.
+ *
+ * Source pages (cited by name below):
+ *   [SD-survey]  "大模型投机解码：Medusa、MTP、EAGLE、DFlash、DDTree 与 DSpark"
+ *                (Speculative decoding for LLMs: Medusa, MTP, EAGLE, DFlash,
+ *                DDTree and DSpark), chzhyang.github.io.
+ *
+ * Conventions shared by every function here:
+ *   - logits rows are fp32 (ldt = 0) or bf16 given as raw uint16 bits (ldt = 1);
+ *     every value is converted exactly to double before any arithmetic.
+ *   - dense addressing: row (b, i) starts at b*batch_stride + i*row_stride
+ *     elements; ragged addressing (k_per_req != NULL): row (b, i) starts at
+ *     (row_off[b] + i) * row_stride.
+ *   - "row invalid": the row holds a NaN or +Inf, or every entry is -Inf.
+ */
+#ifndef SPEC_ORACLE_H
+#define SPEC_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status bits written per request */
+#define ORC_ST_BAD_ROW      1   /* a read row was invalid: walk stopped          */
+#define ORC_ST_Q_ZERO       2   /* q(y) == 0 for a drafted token                  */
+#define ORC_ST_R_ZERO       4   /* residual mass <= 0: sampled from p instead     */
+#define ORC_ST_BAD_TOKEN    8   /* drafted token id outside [0, V)                */
+#define ORC_ST_BAD_K       16   /* per-request draft length outside [0, K]        */
+
+/* near-tie window (absolute on the ratio, relative to the mass on the CDF) */
+#define ORC_NEAR_TIE 1e-6
+
+/* Chain speculative sampling ([SD-survey] §1).  near_tie[b]: bit i set when
+ * |u_i - p_i(y_i)/q_i(y_i)| <= 1e-6 at an examined position i (i < 31);
+ * bit 31 set when the final sample's target lies within 1e-6 (normalised) of
+ * either boundary of the chosen token's CDF interval.  rows_read[b] = number
+ * of logits rows examined.  diag[b, i, 0..3] = p_i(y_i), q_i(y_i), Z_i, R_i
+ * for examined draft rows; for the bonus row p_k(x*), 0, Z_k, 0. */
+void oracle_verify_chain(
+    const void* logits, int ldt, int64_t l_bstride, int64_t l_rstride,
+    const float* q, int64_t q_bstride, int64_t q_rstride,
+    const int32_t* draft, const float* uniforms,
+    int B, int K, int V, float temperature, int top_k,
+    const int32_t* k_per_req, const int32_t* l_row_off, const int32_t* q_row_off,
+    int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
+    double* diag, int32_t* near_tie, int32_t* rows_read);
+
+/* Greedy argmax-match verification ([SD-survey] §1, greedy consistency). */
+void oracle_verify_greedy(
+    const void* logits, int ldt, int64_t l_bstride, int64_t l_rstride,
+    const int32_t* draft, int B, int K, int V,
+    const int32_t* k_per_req, const int32_t* l_row_off,
+    int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
+    int32_t* rows_read);
+
+/* DDTree best-first tree ([SD-survey] §5 "DDTree", Q(u) equation).
+ * q: [B, L, V] probabilities, row (b, d-1) is the marginal of depth d.
+ * budget N includes the root.  anc_mask has W = ceil(N/64) words per node.
+ * rows_needed[b] = deepest per-depth list the best-first order consulted. */
+void oracle_tree_build(
+    const float* q, int64_t q_bstride, int64_t q_rstride,
+    int B, int L, int V, int budget,
+    int32_t* token, int32_t* parent, int32_t* depth, double* score,
+    uint64_t* anc_mask, int32_t* num_nodes, int32_t* status,
+    int32_t* rows_needed);
+
+/* Brute force for tiny V and L: every prefix of length <= L over the
+ * per-depth candidate lists, sorted by (Q desc, depth asc, rank path asc),
+ * first N kept.  Same outputs as oracle_tree_build.  Returns -1 when the
+ * prefix count exceeds max_prefixes. */
+int oracle_tree_build_bruteforce(
+    const float* q, int64_t q_bstride, int64_t q_rstride,
+    int B, int L, int V, int budget, int64_t max_prefixes,
+    int32_t* token, int32_t* parent, int32_t* depth, double* score,
+    uint64_t* anc_mask, int32_t* num_nodes);
+
+/* Tree-walk verification ([SD-survey] §5 "DDTree", verification walk). */
+void oracle_verify_tree(
+    const void* logits, int ldt, int64_t l_bstride, int64_t l_rstride,
+    const int32_t* token, const int32_t* parent, const int32_t* num_nodes,
+    int B, int N, int V, int max_depth,
+    int32_t* path_nodes, int32_t* out_tokens, int32_t* num_accepted,
+    int32_t* status);
+
+/* DSpark prefix survival and adaptive verify length ([SD-survey] §5
+ * "DSpark", s_j equation and expected advance).  near_tie[b] = 1 when the
+ * best and second-best E(k)/(a+b*k) differ by <= 1e-6 relative. */
+void oracle_adaptive_len(
+    const float* conf, int B, int Kmax, float a, float b,
+    int32_t* k_out, double* surv, double* exp_adv,
+    int32_t* l_row_off, int32_t* q_row_off, int32_t* near_tie);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
