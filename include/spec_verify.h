@@ -1,0 +1,215 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify, batched verification of
+ * speculative-decoding drafts on one NVIDIA GB300 (sm_103a).
+ *
+ * Source page for every operation below:
+ *   [SD-survey] "大模型投机解码：Medusa、MTP、EAGLE、DFlash、DDTree 与 DSpark"
+ *               (Speculative decoding for LLMs: Medusa, MTP, EAGLE, DFlash,
+ *               DDTree and DSpark), chzhyang.github.io.
+ *
+ * Conventions for every call
+ *   - All array pointers are DEVICE pointers owned by the caller.  The
+ *     library never allocates device memory; scratch space comes from the
+ *     caller's `ws` buffer, sized by the matching *_workspace_size() query.
+ *     The workspace must not be shared by two calls in flight at once.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls enqueue work and return without synchronising; they are
+ *     free of host-device synchronisation and of allocation.
+ *   - The return value reports only synchronous problems: argument checks
+ *     (SPEC_INVALID_ARG), unsupported shapes (SPEC_UNSUPPORTED) and launch
+ *     errors (SPEC_CUDA_ERROR).  spec_last_error() returns a thread-local
+ *     description of the last non-OK status.
+ *   - Problems found on the device are reported per request in `status`
+ *     (bits SPEC_ST_*), and device-wide ones (a bounded wait that gave up)
+ *     in the workspace error word, read with spec_workspace_error().
+ *   - Row strides are in elements.  Rows whose start address is 16-byte
+ *     aligned are streamed by the Tensor Memory Accelerator; other layouts
+ *     are accepted and read with plain loads (slower).
+ *   - Token ids are int32 in [0, V).  Output token rows are padded with -1.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_INVALID_ARG = 1,
+    SPEC_UNSUPPORTED = 2,
+    SPEC_CUDA_ERROR = 3
+} spec_status;
+
+typedef enum {
+    SPEC_F32 = 0,   /* IEEE binary32 */
+    SPEC_BF16 = 1   /* bfloat16 */
+} spec_dtype;
+
+/* per-request status bits */
+#define SPEC_ST_BAD_ROW   1   /* a read logits row held NaN/+Inf or only -Inf: the walk
+                                 stopped there, no correction/bonus token */
+#define SPEC_ST_Q_ZERO    2   /* q(y) == 0 for a drafted token: ratio taken as +inf
+                                 when p(y) > 0, else 0 */
+#define SPEC_ST_R_ZERO    4   /* residual mass <= 0 after a rejection: the correction
+                                 token was sampled from p instead */
+#define SPEC_ST_BAD_TOKEN 8   /* a drafted or tree token id outside [0, V) */
+#define SPEC_ST_BAD_K    16   /* per-request draft length outside [0, K] */
+
+/* workspace error bits */
+#define SPEC_WS_ERR_WAIT     1u   /* a bounded device wait gave up; outputs invalid */
+#define SPEC_WS_ERR_QUEUE    2u   /* the device task queue overflowed; outputs invalid */
+
+const char* spec_last_error(void);
+int spec_version(void);
+
+/*
+ * Optional tuning, for benchmarking sweeps.  slices_per_row: how many CTAs
+ * share one vocabulary row (0 = automatic).  ctas_per_sm: resident CTAs per
+ * SM of the persistent grid (0 = automatic, i.e. as many as fit).  Affects
+ * later calls of this process and later workspace-size queries.
+ */
+spec_status spec_set_tuning(int slices_per_row, int ctas_per_sm);
+
+/*
+ * Reads the device error word of a workspace after the stream is drained
+ * (synchronises `stream`).  For diagnostics and tests; not for hot loops.
+ */
+spec_status spec_workspace_error(const void* ws, void* stream, uint32_t* err_out);
+
+/* ------------------------------------------------------------------------
+ * spec_verify_chain -- batched chain speculative sampling
+ * [SD-survey] §1 "what speculative decoding guarantees": acceptance
+ * alpha_i(y_i) = min(1, p_i(y_i)/q_i(y_i)); at the first rejection the
+ * correction token is drawn from the normalised residual [p_i - q_i]_+;
+ * if every draft passes, a bonus token is drawn from p_{K+1}.  Temperature
+ * and top-k truncation are folded into p (same section).
+ *
+ *   logits   target logits, dtype `ldt`.  Dense mode (k_per_req == NULL):
+ *            row (b, i), i = 0..K, starts at b*l_batch_stride + i*l_row_stride.
+ *            Ragged mode: row (b, i), i = 0..k_b, starts at
+ *            (l_row_off[b] + i) * l_row_stride; l_batch_stride is ignored.
+ *   q        draft proposal probabilities, fp32, used as given (not
+ *            truncated or renormalised).  Row (b, i), i = 0..k-1, addressed
+ *            like logits with q_batch_stride / q_row_stride / q_row_off.
+ *   draft    [B, K] int32 drafted tokens (ragged: the first k_b of each row).
+ *   uniforms [B, K+1] fp32 in [0, 1): u[b, i] decides position i (accept iff
+ *            u < p/q), u[b, k] drives the single inverse-CDF sample (ascending
+ *            token id, smallest x with C(x) > u * total).
+ *   temperature > 0.  top_k <= 0 or >= V disables truncation; otherwise
+ *            S = {x : l_x >= tau}, tau = top_k-th largest raw logit, ties kept.
+ *   k_per_req, l_row_off, q_row_off  NULL for dense mode; else [B], [B+1],
+ *            [B+1] (from spec_adaptive_len or the caller).
+ * Outputs:
+ *   out_tokens   [B, K+1]: accepted drafts, then the correction or bonus token, then -1.
+ *   num_accepted [B]: accepted draft tokens (excludes the correction/bonus token).
+ *   status       [B]: SPEC_ST_* bits.
+ *   diag         NULL or [B, K+1, 4] fp32: for each examined draft row
+ *                {p(y), q(y), Z, R} (R = residual mass at the rejection row,
+ *                else 0); for the bonus row {p(x), 0, Z, 0}.  Z is
+ *                sum over S of exp((l_x - max l)/T).  Rows not examined are
+ *                left untouched.
+ * Rows past the first rejection are never read.
+ * ---------------------------------------------------------------------- */
+size_t spec_verify_chain_workspace_size(int B, int K, int V, int top_k);
+spec_status spec_verify_chain(
+    const void* logits, spec_dtype ldt, int64_t l_batch_stride, int64_t l_row_stride,
+    const float* q, int64_t q_batch_stride, int64_t q_row_stride,
+    const int32_t* draft, const float* uniforms,
+    int B, int K, int V, float temperature, int top_k,
+    const int32_t* k_per_req, const int32_t* l_row_off, const int32_t* q_row_off,
+    int32_t* out_tokens, int32_t* num_accepted, int32_t* status, float* diag,
+    void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * spec_verify_greedy -- greedy argmax-match verification
+ * [SD-survey] §1, "greedy-consistent" results: accept while the drafted
+ * token equals the target argmax (raw logits, lowest id on ties); the first
+ * mismatch commits the argmax; if all K match, the bonus is the argmax of
+ * row K.  Layout of logits, draft, k_per_req, l_row_off and the outputs as in
+ * spec_verify_chain; no q, no uniforms.
+ * ---------------------------------------------------------------------- */
+size_t spec_verify_greedy_workspace_size(int B, int K, int V);
+spec_status spec_verify_greedy(
+    const void* logits, spec_dtype ldt, int64_t l_batch_stride, int64_t l_row_stride,
+    const int32_t* draft, int B, int K, int V,
+    const int32_t* k_per_req, const int32_t* l_row_off,
+    int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
+    void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * spec_tree_build -- DDTree best-first draft tree
+ * [SD-survey] §5 "DDTree": prefixes u scored by the factorised proxy
+ * Q(u) = prod_{i=1}^{|u|} q_i(u_i) over the block drafter's per-position
+ * marginals; a best-first heap picks prefixes under a node budget; nodes take
+ * position id = depth and see only themselves and their ancestors.
+ *
+ *   q        [B, L, V] fp32 marginals: row (b, d-1) at b*q_batch_stride +
+ *            (d-1)*q_row_stride is depth d's distribution.  Depth d uses its
+ *            budget-1 most probable tokens (ties to the lower id).
+ *   budget   N nodes including the root (node 0, depth 0, Q = 1, token -1),
+ *            1 <= N <= 256; L <= 16.
+ * Outputs ([B, N], node order = pop order, so parents precede children;
+ * slots >= num_nodes[b] hold -1 / 0):
+ *   token, parent (-1 for the root), depth (position id), score (Q, fp64),
+ *   anc_mask [B, N, ceil(N/64)] uint64: bit m of node n set iff m is n or an
+ *   ancestor of n; num_nodes [B]; status [B].
+ * Pop order: higher Q, then smaller depth, then lexicographically smaller
+ * path of per-depth ranks.  Depth rows are read in order and reading stops as
+ * soon as the best-first order no longer needs a deeper row.
+ * ---------------------------------------------------------------------- */
+size_t spec_tree_build_workspace_size(int B, int L, int V, int budget);
+spec_status spec_tree_build(
+    const float* q, int64_t q_batch_stride, int64_t q_row_stride,
+    int B, int L, int V, int budget,
+    int32_t* token, int32_t* parent, int32_t* depth, double* score,
+    uint64_t* anc_mask, int32_t* num_nodes, int32_t* status,
+    void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * spec_verify_tree -- greedy tree-walk verification
+ * [SD-survey] §5 "DDTree": verification walks the target-selected token;
+ * when no child of the current node carries it, that token becomes the
+ * bonus token; only the accepted path is kept.
+ *
+ *   logits   [B, N, V]: row (b, n) at b*l_batch_stride + n*l_row_stride is
+ *            the target's distribution after node n.
+ *   token, parent, num_nodes   the tree (as produced by spec_tree_build).
+ *   max_depth  the tree's depth limit L (output width L+1).
+ * Outputs: path_nodes [B, L+1] (root 0, then accepted nodes, then -1),
+ *   out_tokens [B, L+1] (accepted tokens, then the bonus, then -1),
+ *   num_accepted [B], status [B].  Only rows on the walked path are read.
+ * ---------------------------------------------------------------------- */
+size_t spec_verify_tree_workspace_size(int B, int N, int V);
+spec_status spec_verify_tree(
+    const void* logits, spec_dtype ldt, int64_t l_batch_stride, int64_t l_row_stride,
+    const int32_t* token, const int32_t* parent, const int32_t* num_nodes,
+    int B, int N, int V, int max_depth,
+    int32_t* path_nodes, int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
+    void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * spec_adaptive_len -- DSpark verify length
+ * [SD-survey] §5 "DSpark": prefix survival s_j = prod_{i<=j} c_i, expected
+ * advance 1 + sum_{j<=k} s_j; each request verifies the k in [0, Kmax] that
+ * maximises (1 + sum_{j<=k} s_j) / (a + b*k), ties to the smaller k.
+ * Computed in fp64 without fused multiply-add.
+ *
+ *   conf   [B, Kmax] fp32 conditional confidences c_i.   a > 0, b >= 0.
+ * Outputs: k_out [B]; surv NULL or [B, Kmax] fp64; exp_adv NULL or [B] fp64
+ *   (the advance at the chosen k); l_row_off [B+1] = exclusive scan of
+ *   k_b + 1; q_row_off [B+1] = exclusive scan of k_b (the ragged layout of
+ *   spec_verify_chain, SGLang's "compact" mode, [SD-survey] §9).
+ * ---------------------------------------------------------------------- */
+spec_status spec_adaptive_len(
+    const float* conf, int B, int Kmax, float a, float b,
+    int32_t* k_out, double* surv, double* exp_adv,
+    int32_t* l_row_off, int32_t* q_row_off, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,385 @@
+"""Batched verification of speculative-decoding drafts on an NVIDIA GB300.
+
+Thin Python binding over the C ABI of ``libspecverify.so`` (declared in
+``include/spec_verify.h``).  Every function here only marshals arguments:
+it checks tensor devices, dtypes and layouts, allocates the outputs and the
+workspace with PyTorch (device memory only), and calls the library on the
+current CUDA stream.  All computation runs in the library's sm_103a
+kernels; there is no CPU or PyTorch fallback.  Importing the package does
+not load the library; the first call does, and raises if it is missing.
+
+Functions (same names as the C entry points, without the ``spec_`` prefix):
+  verify_chain   chain speculative sampling (accept min(1,p/q), residual, bonus)
+  verify_greedy  greedy argmax-match verification
+  tree_build     DDTree best-first tree under a node budget
+  verify_tree    greedy tree-walk verification
+  adaptive_len   DSpark survival, expected advance and verify length
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libspecverify.so")
+
+SPEC_F32, SPEC_BF16 = 0, 1
+ST_BAD_ROW, ST_Q_ZERO, ST_R_ZERO, ST_BAD_TOKEN, ST_BAD_K = 1, 2, 4, 8, 16
+WS_ERR_WAIT, WS_ERR_QUEUE = 1, 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SpecError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile libspecverify.so in-tree (nvcc, sm_103a)."""
+    from . import _build
+    return _build.build(force=force)
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise SpecError(f"{LIB_PATH} is missing: build it with "
+                            "speculative_decoding_draft_sampling_gb300.build() first")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        lib.spec_last_error.restype = ctypes.c_char_p
+        lib.spec_version.restype = ctypes.c_int
+        lib.spec_set_tuning.argtypes = [i32, i32]
+        lib.spec_workspace_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
+        lib.spec_verify_chain_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.spec_verify_chain_workspace_size.restype = sz
+        lib.spec_verify_chain.argtypes = [P, i32, i64, i64, P, i64, i64, P, P, i32, i32, i32, f32, i32,
+                                          P, P, P, P, P, P, P, P, sz, P]
+        lib.spec_verify_greedy_workspace_size.argtypes = [i32, i32, i32]
+        lib.spec_verify_greedy_workspace_size.restype = sz
+        lib.spec_verify_greedy.argtypes = [P, i32, i64, i64, P, i32, i32, i32, P, P, P, P, P, P, sz, P]
+        lib.spec_tree_build_workspace_size.argtypes = [i32, i32, i32, i32]
+        lib.spec_tree_build_workspace_size.restype = sz
+        lib.spec_tree_build.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, P, P, P, P, P, P, sz, P]
+        lib.spec_verify_tree_workspace_size.argtypes = [i32, i32, i32]
+        lib.spec_verify_tree_workspace_size.restype = sz
+        lib.spec_verify_tree.argtypes = [P, i32, i64, i64, P, P, P, i32, i32, i32, i32, P, P, P, P, P, sz, P]
+        lib.spec_adaptive_len.argtypes = [P, i32, i32, f32, f32, P, P, P, P, P, P]
+        for name in ("spec_set_tuning", "spec_workspace_error", "spec_verify_chain", "spec_verify_greedy",
+                     "spec_tree_build", "spec_verify_tree", "spec_adaptive_len"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def lib():
+    """The loaded ctypes library (loads it on first use)."""
+    return _load()
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        msg = _load().spec_last_error().decode(errors="replace")
+        raise SpecError(f"{what} failed (status {rc}): {msg}")
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cuda(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise SpecError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise SpecError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _ldt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise SpecError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+_ws_cache: dict = {}
+
+
+def workspace(nbytes: int, device) -> torch.Tensor:
+    """A cached device scratch buffer of at least ``nbytes`` bytes (one per
+    device); calls on one stream may share it, concurrent calls must not."""
+    key = torch.device(device).index if torch.device(device).index is not None else torch.cuda.current_device()
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1 << 12), dtype=torch.uint8, device=torch.device("cuda", key))
+        _ws_cache[key] = buf
+    return buf
+
+
+def set_tuning(slices_per_row: int = 0, ctas_per_sm: int = 0):
+    _check(_load().spec_set_tuning(int(slices_per_row), int(ctas_per_sm)), "spec_set_tuning")
+
+
+def workspace_error(ws: torch.Tensor, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check(_load().spec_workspace_error(_p(ws), _stream(stream), ctypes.byref(v)), "spec_workspace_error")
+    return int(v.value)
+
+
+def version() -> int:
+    return int(_load().spec_version())
+
+
+# ---------------------------------------------------------------------------
+# chain speculative sampling
+# ---------------------------------------------------------------------------
+@dataclass
+class ChainResult:
+    tokens: torch.Tensor        # [B, K+1] int32
+    num_accepted: torch.Tensor  # [B] int32
+    status: torch.Tensor        # [B] int32
+    diag: Optional[torch.Tensor]
+    ws: torch.Tensor
+
+
+def verify_chain(logits, q, draft, uniforms, temperature: float, top_k: int = 0, *,
+                 k_per_req=None, l_row_off=None, q_row_off=None, diag: bool = False,
+                 out: Optional[ChainResult] = None, ws: Optional[torch.Tensor] = None,
+                 stream=None) -> ChainResult:
+    """Chain speculative sampling.
+
+    Dense: logits [B, K+1, V], q [B, K, V] (any batch/row strides, unit
+    element stride).  Ragged (k_per_req given): logits [rows, V] packed by
+    l_row_off, q [rows, V] packed by q_row_off.  draft [B, K] int32,
+    uniforms [B, K+1] fp32.
+    """
+    L = _load()
+    _cuda(logits, "logits")
+    ldt = _ldt(logits)
+    _cuda(q, "q", torch.float32)
+    _cuda(draft, "draft", torch.int32)
+    _cuda(uniforms, "uniforms", torch.float32)
+    if draft.dim() != 2 or not draft.is_contiguous() or not uniforms.is_contiguous():
+        raise SpecError("draft [B, K] and uniforms [B, K+1] must be contiguous")
+    B, K = draft.shape
+    V = logits.shape[-1]
+    if uniforms.shape != (B, K + 1):
+        raise SpecError("uniforms must be [B, K+1]")
+    if logits.stride(-1) != 1 or q.stride(-1) != 1:
+        raise SpecError("logits and q need unit element stride")
+    ragged = k_per_req is not None
+    if ragged:
+        for t, n in ((k_per_req, "k_per_req"), (l_row_off, "l_row_off"), (q_row_off, "q_row_off")):
+            _cuda(t, n, torch.int32)
+        if logits.dim() != 2 or q.dim() != 2:
+            raise SpecError("ragged mode takes packed 2-D logits and q")
+        lbs, lrs = 0, logits.stride(0)
+        qbs, qrs = 0, q.stride(0)
+    else:
+        if logits.dim() != 3 or logits.shape[:2] != (B, K + 1):
+            raise SpecError("dense logits must be [B, K+1, V]")
+        if q.dim() != 3 or q.shape[0] != B or q.shape[1] < K or q.shape[2] != V:
+            raise SpecError("dense q must be [B, K, V]")
+        lbs, lrs = logits.stride(0), logits.stride(1)
+        qbs, qrs = q.stride(0), q.stride(1)
+    dev = logits.device
+    if out is None:
+        out = ChainResult(torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+                          torch.empty(B, dtype=torch.int32, device=dev),
+                          torch.empty(B, dtype=torch.int32, device=dev),
+                          torch.full((B, K + 1, 4), float("nan"), dtype=torch.float32, device=dev) if diag else None,
+                          None)
+    need = L.spec_verify_chain_workspace_size(B, K, V, int(top_k))
+    if ws is None:
+        ws = workspace(need, dev)
+    out.ws = ws
+    rc = L.spec_verify_chain(_p(logits), ldt, lbs, lrs, _p(q), qbs, qrs, _p(draft), _p(uniforms),
+                             B, K, V, float(temperature), int(top_k),
+                             _p(k_per_req), _p(l_row_off), _p(q_row_off),
+                             _p(out.tokens), _p(out.num_accepted), _p(out.status), _p(out.diag),
+                             _p(ws), ws.numel(), _stream(stream))
+    _check(rc, "spec_verify_chain")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# greedy
+# ---------------------------------------------------------------------------
+@dataclass
+class GreedyResult:
+    tokens: torch.Tensor
+    num_accepted: torch.Tensor
+    status: torch.Tensor
+    ws: torch.Tensor
+
+
+def verify_greedy(logits, draft, *, k_per_req=None, l_row_off=None, out: Optional[GreedyResult] = None,
+                  ws: Optional[torch.Tensor] = None, stream=None) -> GreedyResult:
+    """Greedy argmax-match verification.  Layouts as in verify_chain."""
+    L = _load()
+    _cuda(logits, "logits")
+    ldt = _ldt(logits)
+    _cuda(draft, "draft", torch.int32)
+    if draft.dim() != 2 or not draft.is_contiguous():
+        raise SpecError("draft must be a contiguous [B, K] tensor")
+    B, K = draft.shape
+    V = logits.shape[-1]
+    if logits.stride(-1) != 1:
+        raise SpecError("logits need unit element stride")
+    if k_per_req is not None:
+        _cuda(k_per_req, "k_per_req", torch.int32)
+        _cuda(l_row_off, "l_row_off", torch.int32)
+        lbs, lrs = 0, logits.stride(0)
+    else:
+        if logits.dim() != 3 or logits.shape[:2] != (B, K + 1):
+            raise SpecError("dense logits must be [B, K+1, V]")
+        lbs, lrs = logits.stride(0), logits.stride(1)
+    dev = logits.device
+    if out is None:
+        out = GreedyResult(torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+                           torch.empty(B, dtype=torch.int32, device=dev),
+                           torch.empty(B, dtype=torch.int32, device=dev), None)
+    need = L.spec_verify_greedy_workspace_size(B, K, V)
+    if ws is None:
+        ws = workspace(need, dev)
+    out.ws = ws
+    rc = L.spec_verify_greedy(_p(logits), ldt, lbs, lrs, _p(draft), B, K, V, _p(k_per_req), _p(l_row_off),
+                              _p(out.tokens), _p(out.num_accepted), _p(out.status), _p(ws), ws.numel(),
+                              _stream(stream))
+    _check(rc, "spec_verify_greedy")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# DDTree
+# ---------------------------------------------------------------------------
+@dataclass
+class Tree:
+    token: torch.Tensor      # [B, N] int32
+    parent: torch.Tensor     # [B, N] int32
+    depth: torch.Tensor      # [B, N] int32
+    score: torch.Tensor      # [B, N] float64
+    anc_mask: torch.Tensor   # [B, N, ceil(N/64)] int64 (bit patterns of uint64)
+    num_nodes: torch.Tensor  # [B] int32
+    status: torch.Tensor     # [B] int32
+    ws: torch.Tensor
+
+
+def tree_build(q, budget: int, *, out: Optional[Tree] = None, ws: Optional[torch.Tensor] = None,
+               stream=None) -> Tree:
+    """DDTree best-first tree over per-depth marginals q [B, L, V] fp32."""
+    Lb = _load()
+    _cuda(q, "q", torch.float32)
+    if q.dim() != 3 or q.stride(-1) != 1:
+        raise SpecError("q must be [B, L, V] with unit element stride")
+    B, L, V = q.shape
+    N = int(budget)
+    W = (N + 63) // 64
+    dev = q.device
+    if out is None:
+        out = Tree(torch.empty((B, N), dtype=torch.int32, device=dev),
+                   torch.empty((B, N), dtype=torch.int32, device=dev),
+                   torch.empty((B, N), dtype=torch.int32, device=dev),
+                   torch.empty((B, N), dtype=torch.float64, device=dev),
+                   torch.empty((B, N, W), dtype=torch.int64, device=dev),
+                   torch.empty(B, dtype=torch.int32, device=dev),
+                   torch.empty(B, dtype=torch.int32, device=dev), None)
+    need = Lb.spec_tree_build_workspace_size(B, L, V, N)
+    if need == 0 and B > 0:
+        raise SpecError("unsupported tree shape (L <= 16, 1 <= budget <= 256)")
+    if ws is None:
+        ws = workspace(need, dev)
+    out.ws = ws
+    rc = Lb.spec_tree_build(_p(q), q.stride(0), q.stride(1), B, L, V, N,
+                            _p(out.token), _p(out.parent), _p(out.depth), _p(out.score), _p(out.anc_mask),
+                            _p(out.num_nodes), _p(out.status), _p(ws), ws.numel(), _stream(stream))
+    _check(rc, "spec_tree_build")
+    return out
+
+
+@dataclass
+class TreeWalk:
+    path_nodes: torch.Tensor   # [B, L+1]
+    tokens: torch.Tensor       # [B, L+1]
+    num_accepted: torch.Tensor
+    status: torch.Tensor
+    ws: torch.Tensor
+
+
+def verify_tree(logits, token, parent, num_nodes, max_depth: int, *, out: Optional[TreeWalk] = None,
+                ws: Optional[torch.Tensor] = None, stream=None) -> TreeWalk:
+    """Greedy tree walk over target logits [B, N, V] (fp32 or bf16)."""
+    Lb = _load()
+    _cuda(logits, "logits")
+    ldt = _ldt(logits)
+    for t, n in ((token, "token"), (parent, "parent"), (num_nodes, "num_nodes")):
+        _cuda(t, n, torch.int32)
+        if not t.is_contiguous():
+            raise SpecError(f"{n} must be contiguous")
+    if logits.dim() != 3 or logits.stride(-1) != 1:
+        raise SpecError("logits must be [B, N, V] with unit element stride")
+    B, N = token.shape
+    V = logits.shape[-1]
+    Ld = int(max_depth)
+    dev = logits.device
+    if out is None:
+        out = TreeWalk(torch.empty((B, Ld + 1), dtype=torch.int32, device=dev),
+                       torch.empty((B, Ld + 1), dtype=torch.int32, device=dev),
+                       torch.empty(B, dtype=torch.int32, device=dev),
+                       torch.empty(B, dtype=torch.int32, device=dev), None)
+    need = Lb.spec_verify_tree_workspace_size(B, N, V)
+    if ws is None:
+        ws = workspace(need, dev)
+    out.ws = ws
+    rc = Lb.spec_verify_tree(_p(logits), ldt, logits.stride(0), logits.stride(1), _p(token), _p(parent),
+                             _p(num_nodes), B, N, V, Ld, _p(out.path_nodes), _p(out.tokens),
+                             _p(out.num_accepted), _p(out.status), _p(ws), ws.numel(), _stream(stream))
+    _check(rc, "spec_verify_tree")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# DSpark
+# ---------------------------------------------------------------------------
+@dataclass
+class AdaptiveLen:
+    k: torch.Tensor          # [B] int32
+    surv: torch.Tensor       # [B, Kmax] float64
+    exp_adv: torch.Tensor    # [B] float64
+    l_row_off: torch.Tensor  # [B+1] int32
+    q_row_off: torch.Tensor  # [B+1] int32
+
+
+def adaptive_len(conf, a: float, b: float, *, out: Optional[AdaptiveLen] = None, stream=None) -> AdaptiveLen:
+    """DSpark verify length from conditional confidences conf [B, Kmax] fp32."""
+    Lb = _load()
+    _cuda(conf, "conf", torch.float32)
+    if conf.dim() != 2 or not conf.is_contiguous():
+        raise SpecError("conf must be a contiguous [B, Kmax] tensor")
+    B, Kmax = conf.shape
+    dev = conf.device
+    if out is None:
+        out = AdaptiveLen(torch.empty(B, dtype=torch.int32, device=dev),
+                          torch.empty((B, Kmax), dtype=torch.float64, device=dev),
+                          torch.empty(B, dtype=torch.float64, device=dev),
+                          torch.empty(B + 1, dtype=torch.int32, device=dev),
+                          torch.empty(B + 1, dtype=torch.int32, device=dev))
+    rc = Lb.spec_adaptive_len(_p(conf), B, Kmax, float(a), float(b), _p(out.k), _p(out.surv), _p(out.exp_adv),
+                              _p(out.l_row_off), _p(out.q_row_off), _stream(stream))
+    _check(rc, "spec_adaptive_len")
+    return out

@@ -1,0 +1,84 @@
+// spec_chain.cuh -- argument blocks of the engine kernels and the host-side
+// launch functions each translation unit provides.
+#pragma once
+
+#include "spec_engine.cuh"
+
+namespace spec {
+
+struct ChainArgs {
+    const void* logits;
+    long long l_bs, l_rs;          // element strides
+    const float* q;
+    long long q_bs, q_rs;
+    const int* draft;
+    const float* uniforms;
+    int B, K, V, ldt;
+    float c2;                      // log2(e) / T, fp32
+    double Td;                     // T
+    int top_k;
+    const int* k_per_req;
+    const int* l_row_off;
+    const int* q_row_off;
+    int* out_tokens;
+    int* num_accepted;
+    int* status;
+    float* diag;
+    Workspace W;
+    int S, SL, cap_p;
+    int tma_l, tma_q;
+};
+
+struct WalkArgs {                  // greedy verify and tree walk
+    const void* logits;
+    long long l_bs, l_rs;
+    int B, K, V, ldt;
+    const int* draft;              // greedy
+    const int* k_per_req;
+    const int* l_row_off;
+    const int* token;              // tree
+    const int* parent;
+    const int* num_nodes;
+    int N, L;
+    int* path_nodes;
+    int* out_tokens;
+    int* num_accepted;
+    int* status;
+    Workspace W;
+    int S, SL;
+    int tma_l;
+};
+
+struct BuildArgs {
+    const float* q;
+    long long q_bs, q_rs;
+    int B, L, V, N, M;
+    int* token;
+    int* parent;
+    int* depth;
+    double* score;
+    unsigned long long* anc_mask;
+    int* num_nodes;
+    int* status;
+    Workspace W;
+    int S, SL, cap_p;
+    int tma_q;
+};
+
+// chain
+cudaError_t chain_run(const ChainArgs& A, int grid, cudaStream_t st);
+size_t chain_smem(int ldt, bool topk);
+int chain_occupancy(int ldt, bool topk);
+// greedy / tree walk
+cudaError_t walk_run(const WalkArgs& A, bool tree, int grid, cudaStream_t st);
+int walk_occupancy(int ldt, bool tree);
+// tree build
+cudaError_t build_run(const BuildArgs& A, int grid, cudaStream_t st);
+int build_occupancy(int N, int L);
+size_t build_extra_bytes(int N, int L);
+int build_max_slices(int N, int L);
+// adaptive length
+cudaError_t adaptive_run(const float* conf, int B, int Kmax, float a, float b, int* k_out, double* surv,
+                         double* exp_adv, int* l_off, int* q_off, cudaStream_t st);
+
+}  // namespace spec

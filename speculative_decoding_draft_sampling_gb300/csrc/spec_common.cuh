@@ -1,0 +1,232 @@
+// spec_common.cuh -- device helpers shared by the verification kernels:
+// inline-PTX wrappers for mbarriers and 1-D TMA bulk copies (sm_90+ / sm_103a),
+// bounded waits, order-preserving sort keys, warp and block reductions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace spec {
+
+constexpr int kThreads = 256;                 // every engine CTA
+constexpr int kWarps = kThreads / 32;
+constexpr uint32_t kWaitLimit = 1u << 22;     // queue-wait polls (with backoff): ~seconds, never forever
+constexpr uint32_t kMbarLimit = 1u << 20;     // mbarrier try_wait polls: ~1 s
+constexpr float kInf = __builtin_huge_valf();
+
+// ---------------------------------------------------------------------------
+// element types
+// ---------------------------------------------------------------------------
+struct F32 {
+    using T = float;
+    static constexpr int kBytes = 4;
+    static constexpr int kVec = 4;            // elements per 16-byte vector
+    __device__ static __forceinline__ void unpack(const uint4& w, float (&v)[4]) {
+        v[0] = __uint_as_float(w.x); v[1] = __uint_as_float(w.y);
+        v[2] = __uint_as_float(w.z); v[3] = __uint_as_float(w.w);
+    }
+    __device__ static __forceinline__ float load(const void* base, long long i) {
+        return static_cast<const float*>(base)[i];
+    }
+};
+struct BF16 {
+    using T = __nv_bfloat16;
+    static constexpr int kBytes = 2;
+    static constexpr int kVec = 8;
+    __device__ static __forceinline__ void unpack(const uint4& w, float (&v)[8]) {
+        v[0] = __uint_as_float(w.x << 16); v[1] = __uint_as_float(w.x & 0xffff0000u);
+        v[2] = __uint_as_float(w.y << 16); v[3] = __uint_as_float(w.y & 0xffff0000u);
+        v[4] = __uint_as_float(w.z << 16); v[5] = __uint_as_float(w.z & 0xffff0000u);
+        v[6] = __uint_as_float(w.w << 16); v[7] = __uint_as_float(w.w & 0xffff0000u);
+    }
+    __device__ static __forceinline__ float load(const void* base, long long i) {
+        uint32_t h = static_cast<const uint16_t*>(base)[i];
+        return __uint_as_float(h << 16);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// memory-model helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void nanosleep_ns(uint32_t ns) {
+    asm volatile("nanosleep.u32 %0;" :: "r"(ns));
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + 1-D bulk copy (TMA), global -> shared
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+// copy `bytes` (multiple of 16, both addresses 16-byte aligned) and count the
+// bytes on `bar`
+__device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+// bounded wait for the phase with the given parity; false when it gave up
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    for (uint32_t it = 0; it < kMbarLimit; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok) : "r"(a), "r"(parity) : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+// ---------------------------------------------------------------------------
+// keys: order-preserving uint32 of a float (-0 folded onto +0), and a 64-bit
+// composite key ordering by value descending then index ascending (larger
+// key = earlier in that order)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t fkey(float v) {
+    uint32_t u = __float_as_uint(v + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_inv(uint32_t k) {
+    uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+    return __uint_as_float(u);
+}
+__device__ __forceinline__ uint64_t ckey(float v, int x) {
+    return (static_cast<uint64_t>(fkey(v)) << 32) | static_cast<uint32_t>(0x7fffffff - x);
+}
+__device__ __forceinline__ float ckey_val(uint64_t k) { return fkey_inv(static_cast<uint32_t>(k >> 32)); }
+__device__ __forceinline__ int ckey_idx(uint64_t k) { return 0x7fffffff - static_cast<int>(static_cast<uint32_t>(k)); }
+
+// ---------------------------------------------------------------------------
+// reductions
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        uint64_t w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ uint32_t warp_or(uint32_t v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v |= __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Block-wide reductions over kThreads threads; `red` is shared scratch of at
+// least kWarps 8-byte slots.  Every thread receives the result.
+__device__ __forceinline__ uint64_t block_max_u64(uint64_t v, uint64_t* red) {
+    v = warp_max_u64(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    uint64_t r = red[0];
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) r = red[i] > r ? red[i] : r;
+    return r;
+}
+__device__ __forceinline__ double block_sum_d(double v, double* red) {
+    v = warp_sum_d(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    double r = 0.0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) r += red[i];
+    return r;
+}
+__device__ __forceinline__ int block_sum_i(int v, int* red) {
+    v = warp_sum_i(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    int r = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) r += red[i];
+    return r;
+}
+__device__ __forceinline__ uint32_t block_or(uint32_t v, uint32_t* red) {
+    v = warp_or(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    uint32_t r = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) r |= red[i];
+    return r;
+}
+// exclusive prefix sum (fp64) of one value per thread, in thread order; also
+// returns the block total.
+__device__ __forceinline__ double block_exscan_d(double v, double* red, double& total) {
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    double inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        double t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (l >= o) inc += t;
+    }
+    __syncthreads();
+    if (l == 31) red[w] = inc;
+    __syncthreads();
+    double base = 0.0, tot = 0.0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) {
+        if (i < w) base += red[i];
+        tot += red[i];
+    }
+    total = tot;
+    return base + inc - v;
+}
+
+// fast 2^x on the special-function unit (PTX ex2.approx.ftz.f32)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+}  // namespace spec

@@ -1,0 +1,192 @@
+// spec_walk.cu -- argmax walks on the row-task engine.
+//
+// [SD-survey] = "大模型投机解码：Medusa、MTP、EAGLE、DFlash、DDTree 与 DSpark"
+// (Speculative decoding for LLMs: Medusa, MTP, EAGLE, DFlash, DDTree and
+// DSpark), chzhyang.github.io.
+//
+// Greedy verification (§1, greedy-consistent results): row i's argmax (raw
+// logits, lowest id on ties) is compared with draft y_i; a match reads row
+// i+1, a mismatch commits the argmax; row k's argmax is the bonus token.
+//
+// Tree walk (§5 "DDTree"): from the root, the argmax of the current node's
+// row is looked up among the node's children; a matching child is accepted
+// and becomes the current node; otherwise the argmax is the bonus token.
+// Only rows on the walked path are read.
+#include "spec_chain.cuh"
+#include "spec_select.cuh"
+
+namespace spec {
+
+struct __align__(16) WalkSmem {
+    uint64_t bars[kStages];
+    Claimed claimed;
+    int last;
+    uint64_t red[kWarps];
+    int ish[4];
+};
+
+template <class E>
+__device__ __forceinline__ const void* walk_row(const WalkArgs& A, int b, int i, bool tree) {
+    long long r;
+    if (!tree && A.k_per_req) r = static_cast<long long>(A.l_row_off[b] + i) * A.l_rs;
+    else r = static_cast<long long>(b) * A.l_bs + static_cast<long long>(i) * A.l_rs;
+    return static_cast<const unsigned char*>(A.logits) + r * E::kBytes;
+}
+
+__device__ void greedy_finish(const WalkArgs& A, int b, int n, int last, int st) {
+    const int W = A.K + 1;
+    int* out = A.out_tokens + static_cast<long long>(b) * W;
+    for (int i = threadIdx.x; i < W; i += kThreads) {
+        int v = -1;
+        if (i < n) v = A.draft[static_cast<long long>(b) * A.K + i];
+        else if (i == n) v = last;
+        out[i] = v;
+    }
+    if (threadIdx.x == 0) {
+        A.num_accepted[b] = n;
+        A.status[b] = st;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) finish_request(A.W);
+}
+
+// path_nodes[b][0..acc] and out_tokens[b][0..acc-1] were written on the way
+__device__ void tree_finish(const WalkArgs& A, int b, int acc, int last, int st) {
+    const int W = A.L + 1;
+    int* pn = A.path_nodes + static_cast<long long>(b) * W;
+    int* ot = A.out_tokens + static_cast<long long>(b) * W;
+    for (int i = threadIdx.x; i < W; i += kThreads) {
+        if (i > acc) { pn[i] = -1; ot[i] = -1; }
+        if (i == acc) ot[i] = last;
+    }
+    if (threadIdx.x == 0) {
+        pn[0] = 0;
+        A.num_accepted[b] = acc;
+        A.status[b] = st;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) finish_request(A.W);
+}
+
+template <class E, bool kTree>
+__global__ void __launch_bounds__(kThreads) walk_kernel(const WalkArgs A) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    auto& sh = *reinterpret_cast<WalkSmem*>(smem + kStages * kChunkBytes);
+    Ring R;
+    R.init(smem, sh.bars);
+    for (;;) {
+        Task t;
+        int s;
+        if (!claim(A.W, A.B, A.S, t, s, &sh.claimed)) break;
+        const int b = t.b;
+        const bool initial = t.kind < 0;
+        const int row = t.row;              // greedy: position; tree: node id
+        const int acc = initial ? 0 : t.aux;
+        bool invalid = false;
+        if (!kTree && initial) {
+            const int kb = A.k_per_req ? A.k_per_req[b] : A.K;
+            invalid = kb < 0 || kb > A.K;
+        }
+        PartHdr* ph = part_hdr(A.W, b, s, A.S);
+        if (!invalid) {
+            const int x0 = s * A.SL, x1 = min(A.V, x0 + A.SL);
+            ArgmaxFn<E> fn;
+            stream_row<E>(R, walk_row<E>(A, b, row, kTree), A.tma_l != 0, x0, x1, fn);
+            const uint64_t best = block_max_u64(fn.best, sh.red);
+            const uint32_t bad = block_or(fn.bad, reinterpret_cast<uint32_t*>(sh.red));
+            if (threadIdx.x == 0) {
+                ph->flags = bad ? kPfBad : 0u;
+                ph->kth = best;
+            }
+        }
+        if (!arrive(A.W, b, A.S, &sh.last)) continue;
+        int st = initial ? 0 : __ldcg(&A.W.req[b].status);
+        if (invalid) {
+            greedy_finish(A, b, 0, -1, 16);
+            continue;
+        }
+        uint32_t flags = 0;
+        uint64_t best = 0;
+        for (int j = threadIdx.x; j < A.S; j += kThreads) {
+            const PartHdr* h = part_hdr(A.W, b, j, A.S);
+            flags |= __ldcg(&h->flags);
+            const uint64_t k = __ldcg(&h->kth);
+            best = k > best ? k : best;
+        }
+        flags = block_or(flags, reinterpret_cast<uint32_t*>(sh.red));
+        best = block_max_u64(best, sh.red);
+        const bool bad_row = (flags & kPfBad) || !(ckey_val(best) > -kInf);
+        const int am = ckey_idx(best);
+        if constexpr (!kTree) {
+            const int kb = A.k_per_req ? A.k_per_req[b] : A.K;
+            if (bad_row) { greedy_finish(A, b, row, -1, st | 1); continue; }
+            if (row == kb) { greedy_finish(A, b, row, am, st); continue; }
+            const int y = A.draft[static_cast<long long>(b) * A.K + row];
+            if (y < 0 || y >= A.V) st |= 8;
+            if (y != am) { greedy_finish(A, b, row, am, st); continue; }
+            if (threadIdx.x == 0) {
+                __stcg(&A.W.req[b].status, st);
+                Task nt;
+                nt.b = b; nt.row = row + 1; nt.kind = 0; nt.aux = 0;
+                push_task(A.W, nt);
+            }
+        } else {
+            if (bad_row) { tree_finish(A, b, acc, -1, st | 1); continue; }
+            // lowest child of `row` carrying the argmax token
+            int child = 0x7fffffff;
+            int nn = A.num_nodes[b];
+            nn = nn < A.N ? nn : A.N;
+            const int* par = A.parent + static_cast<long long>(b) * A.N;
+            const int* tok = A.token + static_cast<long long>(b) * A.N;
+            for (int c = threadIdx.x; c < nn; c += kThreads)
+                if (par[c] == row && tok[c] == am) child = min(child, c);
+            child = static_cast<int>(block_max_u64(~static_cast<uint64_t>(static_cast<uint32_t>(child)) & 0xffffffffull,
+                                                   sh.red) ^ 0xffffffffull);
+            if (child == 0x7fffffff || acc >= A.L) { tree_finish(A, b, acc, am, st); continue; }
+            if (threadIdx.x == 0) {
+                const int W = A.L + 1;
+                A.out_tokens[static_cast<long long>(b) * W + acc] = am;
+                A.path_nodes[static_cast<long long>(b) * W + acc + 1] = child;
+                __stcg(&A.W.req[b].status, st);
+                Task nt;
+                nt.b = b; nt.row = child; nt.kind = 0; nt.aux = acc + 1;
+                push_task(A.W, nt);
+            }
+        }
+        __syncthreads();
+    }
+    if (R.err) atomicOr(&A.W.ctrl->error, kErrWait);
+}
+
+static size_t walk_smem() { return kStages * kChunkBytes + sizeof(WalkSmem); }
+
+template <class E, bool kTree>
+static cudaError_t walk_launch(const WalkArgs& A, int grid, cudaStream_t st) {
+    const size_t smem = walk_smem();
+    cudaError_t e = cudaFuncSetAttribute(walk_kernel<E, kTree>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    walk_kernel<E, kTree><<<grid, kThreads, smem, st>>>(A);
+    return cudaGetLastError();
+}
+
+template <class E, bool kTree>
+static int walk_occ() {
+    const int smem = static_cast<int>(walk_smem());
+    int n = 0;
+    cudaFuncSetAttribute(walk_kernel<E, kTree>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, walk_kernel<E, kTree>, kThreads, smem);
+    return n;
+}
+
+int walk_occupancy(int ldt, bool tree) {
+    if (ldt == 0) return tree ? walk_occ<F32, true>() : walk_occ<F32, false>();
+    return tree ? walk_occ<BF16, true>() : walk_occ<BF16, false>();
+}
+
+cudaError_t walk_run(const WalkArgs& A, bool tree, int grid, cudaStream_t st) {
+    if (A.ldt == 0) return tree ? walk_launch<F32, true>(A, grid, st) : walk_launch<F32, false>(A, grid, st);
+    return tree ? walk_launch<BF16, true>(A, grid, st) : walk_launch<BF16, false>(A, grid, st);
+}
+
+}  // namespace spec

@@ -1,0 +1,217 @@
+"""GPU parity: DDTree build and tree walk, DSpark verify length and the
+ragged (compact) chain verify it feeds, against the float64 oracle through
+the C ABI.
+
+Source page: "大模型投机解码：Medusa、MTP、EAGLE、DFlash、DDTree 与 DSpark"
+(chzhyang.github.io), §5 (DDTree, DSpark) and §9 (compact ragged verify).
+Tree outputs and verify lengths are compared bit for bit: the GPU forms
+Q(u) and the DSpark ratios with the same fp64 operations in the same order.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_draft_sampling_gb300 as sv
+import workloads
+from gpu_util import compare_chain, compare_exact, host
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+TREE_KEYS = ("token", "parent", "depth", "score", "anc_mask", "num_nodes", "status")
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _built():
+    sv.build()
+    sv.set_tuning(0, 0)
+    yield
+    sv.set_tuning(0, 0)
+
+
+def _tree_np(t):
+    out = {k: getattr(t, k).cpu().numpy() for k in TREE_KEYS}
+    out["anc_mask"] = out["anc_mask"].view(np.uint64)
+    return out
+
+
+def _assert_tree_equal(gpu, ref, rows=None):
+    for k in TREE_KEYS:
+        a, b = gpu[k], ref[k]
+        if rows is not None:
+            a = a[rows]
+        assert np.array_equal(a, b), k
+
+
+# ---------------------------------------------------------------------------
+# DDTree build
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("B,L,V,N", [(4, 6, 3000, 24), (8, 16, 20011, 64), (3, 4, 777, 2), (5, 3, 500, 1),
+                                     (4, 16, 10007, 200), (2, 5, 64, 40)])
+@pytest.mark.parametrize("slices", [0, 2])
+def test_tree_build_parity(B, L, V, N, slices):
+    sv.set_tuning(slices, 0)
+    t = workloads.make_tree("ddtree", device=DEV, B=B, L=L, V=V, N=N, seed=B * 1000 + V)
+    g = sv.tree_build(t.q, t.budget)
+    ref = oracle.tree_build(host(t.q), t.budget)
+    _assert_tree_equal(_tree_np(g), ref)
+    assert sv.workspace_error(g.ws) == 0
+    sv.set_tuning(0, 0)
+
+
+def test_tree_build_ties_and_uniform_rows():
+    B, L, V, N = 4, 5, 300, 30
+    q = torch.randint(1, 4, (B, L, V), device=DEV).float()
+    q[0] = 1.0
+    q = (q / q.sum(-1, keepdim=True)).contiguous()
+    g = sv.tree_build(q, N)
+    ref = oracle.tree_build(host(q), N)
+    _assert_tree_equal(_tree_np(g), ref)
+
+
+def test_tree_build_never_reads_past_needed_rows():
+    t = workloads.make_tree("ddtree", device=DEV, B=8, L=16, V=20000, N=64)
+    ref = oracle.tree_build(host(t.q), 64)
+    q = t.q.clone()
+    for b in range(8):
+        q[b, ref["rows_needed"][b]:] = float("nan")
+    g = sv.tree_build(q, 64)
+    _assert_tree_equal(_tree_np(g), ref)
+
+
+def test_tree_build_full_size_sampled():
+    t = workloads.make_tree("ddtree", device=DEV)
+    g = _tree_np(sv.tree_build(t.q, t.budget))
+    rows = [0, 13, 31]
+    ref = oracle.tree_build(host(t.q[rows]), t.budget)
+    _assert_tree_equal(g, ref, rows)
+    assert (g["num_nodes"] == t.budget).all()
+
+
+# ---------------------------------------------------------------------------
+# tree walk
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("B,L,V,N", [(6, 6, 3000, 24), (8, 16, 20011, 64)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_tree_walk_parity(B, L, V, N, dtype):
+    t = workloads.make_tree("ddtree", device=DEV, B=B, L=L, V=V, N=N)
+    g = sv.tree_build(t.q, t.budget)
+    ref_t = oracle.tree_build(host(t.q), t.budget)
+    tl = workloads.tree_target_logits(t, g.depth, dtype=dtype)
+    w = sv.verify_tree(tl, g.token, g.parent, g.num_nodes, L)
+    ref = oracle.verify_tree(host(tl), ref_t["token"], ref_t["parent"], ref_t["num_nodes"], L)
+    for k in ("path_nodes", "tokens", "num_accepted", "status"):
+        assert np.array_equal(getattr(w, k).cpu().numpy(), ref[k]), k
+    assert sv.workspace_error(w.ws) == 0
+
+
+def test_tree_walk_full_size():
+    t = workloads.make_tree("ddtree", device=DEV)
+    g = sv.tree_build(t.q, t.budget)
+    tl = workloads.tree_target_logits(t, g.depth)
+    w = sv.verify_tree(tl, g.token, g.parent, g.num_nodes, 16)
+    rows = [0, 7, 19, 31]
+    ref_t = oracle.tree_build(host(t.q[rows]), t.budget)
+    ref = oracle.verify_tree(host(tl[rows]), ref_t["token"], ref_t["parent"], ref_t["num_nodes"], 16)
+    for k in ("path_nodes", "tokens", "num_accepted"):
+        assert np.array_equal(getattr(w, k).cpu().numpy()[rows], ref[k]), k
+    assert (w.num_accepted.cpu().numpy() >= 1).mean() > 0.5     # the walk gets somewhere
+
+
+def test_tree_walk_rows_off_path_never_read():
+    t = workloads.make_tree("ddtree", device=DEV, B=6, L=6, V=3000, N=24)
+    g = sv.tree_build(t.q, t.budget)
+    tl = workloads.tree_target_logits(t, g.depth)
+    w = sv.verify_tree(tl, g.token, g.parent, g.num_nodes, 6)
+    keep = torch.zeros(tl.shape[:2], dtype=torch.bool, device=DEV)
+    pn = w.path_nodes.cpu().numpy()
+    for b in range(6):
+        for n in pn[b]:
+            if n >= 0:
+                keep[b, n] = True
+    tl2 = tl.clone()
+    tl2[~keep] = float("nan")
+    w2 = sv.verify_tree(tl2, g.token, g.parent, g.num_nodes, 6)
+    assert torch.equal(w.tokens, w2.tokens) and torch.equal(w.status, w2.status)
+
+
+# ---------------------------------------------------------------------------
+# DSpark verify length + ragged chain verify
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("B,Kmax", [(512, 8), (3, 1), (1000, 16), (7, 0)])
+def test_adaptive_len_bit_exact(B, Kmax):
+    g = torch.Generator(device="cpu")
+    g.manual_seed(B + Kmax)
+    c = torch.distributions.Beta(8.0, 2.0).sample((B, Kmax)).float()
+    if B > 3:
+        c[0] = 1.0
+        c[1] = 0.0
+    cg = c.to(DEV)
+    a = sv.adaptive_len(cg, 1.0, 0.15)
+    ref = oracle.adaptive_len(c.numpy(), 1.0, 0.15)
+    assert np.array_equal(a.k.cpu().numpy(), ref["k"])
+    assert np.array_equal(a.surv.cpu().numpy(), ref["surv"])
+    assert np.array_equal(a.exp_adv.cpu().numpy(), ref["exp_adv"])
+    assert np.array_equal(a.l_row_off.cpu().numpy(), ref["l_row_off"])
+    assert np.array_equal(a.q_row_off.cpu().numpy(), ref["q_row_off"])
+
+
+def _ragged(w, a):
+    pl, pq = workloads.pack_ragged(w.logits, w.q, a.k, a.l_row_off, a.q_row_off)
+    return pl, pq
+
+
+@pytest.mark.parametrize("over", [dict(B=48, V=30011), dict(B=512, V=128256)])
+def test_ragged_verify_parity(over):
+    w = workloads.make_chain("dspark", device=DEV, **over)
+    a = sv.adaptive_len(w.conf, 1.0, 0.15)
+    pl, pq = _ragged(w, a)
+    r = sv.verify_chain(pl, pq, w.draft, w.uniforms, w.temperature, w.top_k,
+                        k_per_req=a.k, l_row_off=a.l_row_off, q_row_off=a.q_row_off, diag=True)
+    torch.cuda.synchronize()
+    full = over["B"] <= 64
+    idx = list(range(w.B)) if full else list(range(0, w.B, 64))
+    aref = oracle.adaptive_len(host(w.conf), 1.0, 0.15)
+    k = aref["k"]
+    # the oracle packs its own rows with its own offsets
+    sel_k = k[idx]
+    lo = np.concatenate([[0], np.cumsum(sel_k + 1)]).astype(np.int32)
+    qo = np.concatenate([[0], np.cumsum(sel_k)]).astype(np.int32)
+    lh = host(w.logits[idx])
+    qh = host(w.q[idx])
+    pl_h = np.concatenate([lh[j, :sel_k[j] + 1] for j in range(len(idx))])
+    pq_h = np.concatenate([qh[j, :sel_k[j]] for j in range(len(idx))] + [np.zeros((1, w.V), np.float32)])
+    ref = oracle.verify_chain(pl_h, pq_h, host(w.draft[idx]), host(w.uniforms[idx]), w.temperature, w.top_k,
+                              K=w.K, V=w.V, k_per_req=sel_k, l_row_off=lo, q_row_off=qo)
+
+    class Sub:
+        pass
+    sub = Sub()
+    sub.tokens, sub.num_accepted, sub.status, sub.diag = r.tokens[idx], r.num_accepted[idx], r.status[idx], r.diag[idx]
+    bad, near = compare_chain(sub, ref, w.K)
+    assert not bad, bad[:5]
+
+
+def test_ragged_greedy_and_bad_lengths():
+    w = workloads.make_chain("dspark", device=DEV, B=20, V=4099)
+    k = torch.randint(0, w.K + 1, (w.B,), dtype=torch.int32)
+    k[3] = w.K + 1                        # out of range
+    k[4] = -2
+    kk = k.clamp(0, w.K)
+    lo = torch.zeros(w.B + 1, dtype=torch.int32)
+    qo = torch.zeros(w.B + 1, dtype=torch.int32)
+    lo[1:] = torch.cumsum(kk + 1, 0)
+    qo[1:] = torch.cumsum(kk, 0)
+    pl, pq = workloads.pack_ragged(w.logits, w.q, kk, lo, qo)
+    kg, log, qog = k.to(DEV), lo.to(DEV), qo.to(DEV)
+    r = sv.verify_chain(pl, pq, w.draft, w.uniforms, w.temperature, w.top_k, k_per_req=kg, l_row_off=log,
+                        q_row_off=qog)
+    ref = oracle.verify_chain(host(pl), host(pq), host(w.draft), host(w.uniforms), w.temperature, w.top_k,
+                              K=w.K, V=w.V, k_per_req=k.numpy(), l_row_off=lo.numpy(), q_row_off=qo.numpy())
+    bad, _ = compare_chain(r, ref, w.K, check_diag=False)
+    assert not bad, bad
+    assert r.status[3].item() == 16 and r.status[4].item() == 16
+    g = sv.verify_greedy(pl, w.draft, k_per_req=kg, l_row_off=log)
+    gref = oracle.verify_greedy(host(pl), host(w.draft), K=w.K, V=w.V, k_per_req=k.numpy(), l_row_off=lo.numpy())
+    compare_exact(g.tokens, g.num_accepted, gref)
