@@ -319,9 +319,11 @@ __device__ void chain_fallback(const ChainArgs& A, ChainSmem<kCap>& sh, int b, i
     const void* lrow = chain_lrow<E>(A, b, row);
     const int V = A.V, k = A.top_k;
     // largest key t with #{x : key(l_x) >= t} >= k
+    // invariant: count(lo) >= k (count(0) = V > k); the range halves every
+    // step (64-bit midpoint: hi - lo + 1 can be 2^32), so 32 steps suffice
     uint32_t lo = 0, hi = 0xffffffffu;
-    while (lo < hi) {
-        const uint32_t mid = lo + (hi - lo + 1) / 2;
+    for (int it = 0; it < 33 && lo < hi; ++it) {
+        const uint32_t mid = lo + static_cast<uint32_t>((static_cast<uint64_t>(hi) - lo + 1) >> 1);
         int c = 0;
         for (int x = threadIdx.x; x < V; x += kThreads) c += fkey(E::load(lrow, x)) >= mid;
         c = block_sum_i(c, sh.ired);

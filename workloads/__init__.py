@@ -58,6 +58,8 @@ def _gen(device, seed):
 
 def _sample_rows(q2d: torch.Tensor, g: torch.Generator) -> torch.Tensor:
     """One token per row of the probability matrix q2d (the draft's sample)."""
+    if q2d.shape[0] == 0:
+        return torch.empty(0, dtype=torch.int32, device=q2d.device)
     out = []
     step = 4096
     for s in range(0, q2d.shape[0], step):
