@@ -141,6 +141,30 @@ spec_status spec_verify_greedy(
     void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * spec_verify_greedy_static -- spec_verify_greedy without a caller workspace
+ * No counterpart on the source pages: this is a library convenience.
+ *
+ * For callers that cannot allocate device memory when they verify (code in
+ * host callbacks or allocator-free runtimes, plugins handed raw buffers by an
+ * engine that owns every allocation, loops that forbid allocation after
+ * start-up).  Same arguments and results as spec_verify_greedy, minus `ws`
+ * and `ws_bytes`: the scratch space is an 8 MiB array in device memory that
+ * the library reserves on every GPU it is loaded on, until the process exits.
+ * Batches whose spec_verify_greedy_workspace_size() exceeds 8 MiB are
+ * rejected with SPEC_INVALID_ARG.  Nothing is allocated.
+ * The first call on a device, with that device current, looks up the array's
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  Every call on a device shares the array: calls whose GPU
+ * work overlaps (different streams or host threads) race and must be
+ * serialised by the caller.
+ * ---------------------------------------------------------------------- */
+spec_status spec_verify_greedy_static(
+    const void* logits, spec_dtype ldt, int64_t l_batch_stride, int64_t l_row_stride,
+    const int32_t* draft, int B, int K, int V,
+    const int32_t* k_per_req, const int32_t* l_row_off,
+    int32_t* out_tokens, int32_t* num_accepted, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
  * spec_tree_build -- DDTree best-first draft tree
  * [SD-survey] §5 "DDTree": prefixes u scored by the factorised proxy
  * Q(u) = prod_{i=1}^{|u|} q_i(u_i) over the block drafter's per-position

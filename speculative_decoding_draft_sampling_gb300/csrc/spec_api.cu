@@ -135,6 +135,11 @@ int esize_of(spec_dtype d) { return d == SPEC_F32 ? 4 : 2; }
 
 }  // namespace
 
+namespace spec {
+// lets other translation units of the library report an argument error
+void set_last_error(const char* msg) { g_err = msg; }
+}  // namespace spec
+
 extern "C" {
 
 const char* spec_last_error(void) { return g_err.c_str(); }

@@ -77,6 +77,8 @@ cudaError_t build_run(const BuildArgs& A, int grid, cudaStream_t st);
 int build_occupancy(int N, int L);
 size_t build_extra_bytes(int N, int L);
 int build_max_slices(int N, int L);
+// error text for spec_last_error() from outside the API file
+void set_last_error(const char* msg);
 // adaptive length
 cudaError_t adaptive_run(const float* conf, int B, int Kmax, float a, float b, int* k_out, double* surv,
                          double* exp_adv, int* l_off, int* q_off, cudaStream_t st);
