@@ -129,10 +129,11 @@ def chain_bytes(w, res):
     return int(rows.sum() * V * es + q_pts.sum() * 32 + rej.sum() * per_rej + small)
 
 
-def make_chain_case(name, dev, copies, greedy=False):
+def make_chain_case(name, dev, copies, greedy=False, over=None):
     import workloads
     import speculative_decoding_draft_sampling_gb300 as sv
-    ws = [workloads.make_chain(name, device=dev, seed=workloads.seed_of(name) + 100 * i) for i in range(copies)]
+    ws = [workloads.make_chain(name, device=dev, seed=workloads.seed_of(name) + 100 * i, **(over or {}))
+          for i in range(copies)]
     outs = []
     for w in ws:
         if greedy:
@@ -227,14 +228,16 @@ def make_dspark_case(dev, copies):
     return dict(step=step, positions=pos, bytes=nbytes, cfg=cfg, inputs=ws, outs=outs, dtype="bf16")
 
 
-def make_case(name, dev, copies):
+def make_case(name, dev, copies, over=None):
+    """`over` shrinks or reshapes a chain workload (e.g. {"B": 64}) for sweeps;
+    the default bench line always uses the workload's own sizes."""
     if name == "ddtree":
         return make_tree_case(dev, copies)
     if name == "dspark":
         return make_dspark_case(dev, copies)
     if name == "eagle3_greedy":
-        return make_chain_case("eagle3", dev, copies, greedy=True)
-    return make_chain_case(name, dev, copies)
+        return make_chain_case("eagle3", dev, copies, greedy=True, over=over)
+    return make_chain_case(name, dev, copies, over=over)
 
 
 # ---------------------------------------------------------------------------
@@ -351,6 +354,9 @@ def main():
     ap.add_argument("--copies", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--B", type=int, default=0, help="override the batch size of a chain workload (sweeps)")
+    ap.add_argument("--slices", type=int, default=0, help="slices per row (0 = automatic)")
+    ap.add_argument("--ctas-per-sm", type=int, default=0, help="resident CTAs per SM (0 = occupancy limit)")
     args = ap.parse_args()
     rank, world, local = dist_setup()
     if torch.cuda.is_available():
@@ -364,7 +370,8 @@ def main():
     barrier(world)
     sv.build()
     dev = torch.device("cuda", local)
-    case = make_case(args.workload, dev, args.copies)
+    sv.set_tuning(args.slices, args.ctas_per_sm)
+    case = make_case(args.workload, dev, args.copies, over={"B": args.B} if args.B > 0 else None)
     step = case["step"]
     stream = torch.cuda.current_stream()
     for i in range(args.warmup):

@@ -50,6 +50,7 @@ struct Layout {
     size_t off_ready, off_counter, zero_bytes, off_tasks, off_req, off_part, off_extra, total;
     uint32_t maxt, part_stride;
     uint64_t extra_stride;
+    int smax;
 };
 
 // slices per row never exceed kMaxSlices nor ceil(V / 64) (slices are >= 64 elements)
@@ -61,6 +62,7 @@ int max_slices_for(int V) {
 Layout make_layout(int B, long long maxt, int cap_p, size_t extra_per_req, int smax) {
     Layout L{};
     L.maxt = static_cast<uint32_t>(maxt);
+    L.smax = smax;
     L.off_ready = sizeof(spec::Ctrl);
     L.off_counter = align_up(L.off_ready + 4ull * maxt, 16);
     L.zero_bytes = align_up(L.off_counter + 4ull * B, 256);
@@ -87,6 +89,7 @@ spec::Workspace make_ws(void* ws, const Layout& L) {
     W.part_stride = L.part_stride;
     W.maxt = L.maxt;
     W.extra_stride = L.extra_stride;
+    W.smax = L.smax;
     return W;
 }
 
@@ -169,7 +172,8 @@ spec_status spec_workspace_error(const void* ws, void* stream, uint32_t* err_out
 // chain
 // ---------------------------------------------------------------------------
 static Layout chain_layout(int B, int K, int V, int top_k) {
-    return make_layout(B, static_cast<long long>(B) * (K + 2), chain_cap_p(B, K, V, top_k), 0, max_slices_for(V));
+    // per request: every row at most twice (a hinted pass and its retry) plus a residual pass
+    return make_layout(B, static_cast<long long>(B) * (2 * K + 4), chain_cap_p(B, K, V, top_k), 0, max_slices_for(V));
 }
 
 size_t spec_verify_chain_workspace_size(int B, int K, int V, int top_k) {

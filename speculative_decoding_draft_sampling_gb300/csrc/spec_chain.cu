@@ -23,22 +23,28 @@
 namespace spec {
 
 enum ChainKind : int { kVerify = 0, kBonus = 1, kResid = 2, kInvalid = 3 };
+constexpr int kKindMask = 7;
+constexpr int kNoHint = 8;        // kind bit: stream the row without a filter hint (a retry)
 
-template <int kCap>
-struct __align__(16) ChainSmem {
+template <bool kTopk> struct ChainTopkPart {};
+template <> struct ChainTopkPart<true> { TopkSmem tk; };
+
+template <bool kTopk>
+struct __align__(16) ChainSmem : ChainTopkPart<kTopk> {
     uint64_t bars[kStages];
     Claimed claimed;
     int last;
-    int cnt;
-    int oflow;
     int lcnt;
+    int oflow;
     uint64_t sh64[4];
     double red[kWarps];
     int ired[kWarps + 4];
-    uint64_t pool[kThreads];
+    int hist[64];
+    uint32_t scratch[kWarps + 2];
     double dsh[8];
     int ish[8];
-    uint64_t cand[kCap];
+    float fsh[8];
+    SliceHdrs hdrs;
 };
 
 __device__ __forceinline__ int chain_k(const ChainArgs& A, int b) {
@@ -54,6 +60,9 @@ __device__ __forceinline__ const float* chain_qrow(const ChainArgs& A, int b, in
     const long long r = A.k_per_req ? static_cast<long long>(A.q_row_off[b] + i) * A.q_rs
                                     : static_cast<long long>(b) * A.q_bs + static_cast<long long>(i) * A.q_rs;
     return A.q + r;
+}
+__device__ __forceinline__ float chain_u(const ChainArgs& A, int b, int i) {
+    return A.uniforms[static_cast<long long>(b) * (A.K + 1) + i];
 }
 
 // Commit the request: accepted drafts, then `last` (correction/bonus, or -1),
@@ -81,37 +90,30 @@ __device__ __forceinline__ void chain_diag(const ChainArgs& A, int b, int i, flo
     d[0] = py; d[1] = qy; d[2] = Z; d[3] = R;
 }
 
-// push the request's next task after an accepted position
-__device__ void chain_advance(const ChainArgs& A, int b, int row, int kb, int st) {
-    if (threadIdx.x == 0) {
-        ReqState* rs = &A.W.req[b];
-        __stcg(&rs->status, st);
-        Task t;
-        t.b = b;
-        t.row = row + 1;
-        t.kind = (row + 1 < kb) ? kVerify : kBonus;
-        t.aux = 0;
-        push_task(A.W, t);
-    }
+// thread 0: push the request's next task after an accepted position
+__device__ void chain_advance(const ChainArgs& A, int b, int row, int kb, int st, uint32_t hint) {
+    ReqState* rs = &A.W.req[b];
+    __stcg(&rs->status, st);
+    Task t;
+    t.b = b;
+    t.row = row + 1;
+    t.kind = (row + 1 < kb) ? kVerify : kBonus;
+    t.aux = static_cast<int>(hint);
+    push_task(A.W, t);
 }
 
-// acceptance of drafted y at one row, given p(y) (fp64): returns accept
-__device__ bool chain_accept(const ChainArgs& A, int b, int row, int y, double py, double& qy, int& st) {
+// acceptance of drafted y given p(y) and q(y): u < p/q (fp64)
+__device__ __forceinline__ bool chain_accept(const ChainArgs& A, int y, double py, double qy, double u, int& st) {
     double ratio;
     if (y < 0 || y >= A.V) {
         st |= 8;
-        qy = 0.0;
         ratio = 0.0;
+    } else if (qy == 0.0) {
+        st |= 2;
+        ratio = py > 0.0 ? __longlong_as_double(0x7ff0000000000000LL) : 0.0;
     } else {
-        qy = static_cast<double>(chain_qrow(A, b, row)[y]);
-        if (qy == 0.0) {
-            st |= 2;
-            ratio = py > 0.0 ? __longlong_as_double(0x7ff0000000000000LL) : 0.0;
-        } else {
-            ratio = py / qy;
-        }
+        ratio = py / qy;
     }
-    const double u = static_cast<double>(A.uniforms[static_cast<long long>(b) * (A.K + 1) + row]);
     return u < ratio;
 }
 
@@ -147,101 +149,100 @@ __device__ int warp_icdf_pairs(const int* tok, const double* w, int n, double t)
     return n > 0 ? tok[pick] : -1;
 }
 
+// Filter hint for the next row from this row's top-k threshold tau and max
+// m: half the gap below tau (rows of one target differ little in tau).
+__device__ __forceinline__ uint32_t next_hint(float tau, float m) {
+    const float h = tau - 0.5f * (m - tau);
+    return (h == h && h > -kInf) ? fkey(h) : 0u;
+}
+
 // ---------------------------------------------------------------------------
 // combine with top-k: the candidate lists of all slices hold S exactly
 // ---------------------------------------------------------------------------
-template <class E, int kCap>
-__device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<kCap>& sh, int b, int row,
-                             int kind, int st);
-
-template <class E, int kCap>
-__device__ void chain_fallback(const ChainArgs& A, ChainSmem<kCap>& sh, int b, int row, int kind,
+template <class E>
+__device__ void chain_fallback(const ChainArgs& A, ChainSmem<true>& sh, int b, int row, int kind,
                                int st, float vmax);
 
-template <class E, int kCap>
-__device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<kCap>& sh, int b, int row,
+template <class E>
+__device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<true>& sh, int b, int row,
                              int kind, int st) {
     const int S = A.S;
     const int k = A.top_k;
-    uint32_t flags = 0;
-    uint64_t vkey = 0, theta = 0;
-    for (int s = threadIdx.x; s < S; s += kThreads) {
-        const PartHdr* h = part_hdr(A.W, b, s, S);
-        flags |= __ldcg(&h->flags);
-        const int c = __ldcg(&h->cnt);
-        if (c > 0) {
-            const uint64_t k0 = __ldcg(part_keys(A.W, b, s, S));
-            vkey = k0 > vkey ? k0 : vkey;
-        }
-        const uint64_t kk = __ldcg(&h->kth);
-        if (c >= k) theta = kk > theta ? kk : theta;
-    }
-    flags = block_or(flags, reinterpret_cast<uint32_t*>(sh.red));
-    vkey = block_max_u64(vkey, reinterpret_cast<uint64_t*>(sh.red));
-    theta = block_max_u64(theta, reinterpret_cast<uint64_t*>(sh.red));
-    const float vmax = vkey ? ckey_val(vkey) : -kInf;
     const int kb = chain_k(A, b);
+    // independent loads first: they overlap the header loads
+    const double uk = static_cast<double>(chain_u(A, b, kb));
+    const double ur = kind == kVerify ? static_cast<double>(chain_u(A, b, row)) : 0.0;
+    const int y = kind == kVerify ? A.draft[static_cast<long long>(b) * A.K + row] : -1;
+    SliceHdrs& H = sh.hdrs;
+    load_hdrs(A.W, b, S, H);
+    uint32_t flags = 0;
+    float vmax = -kInf;
+    uint64_t theta = 0;
+    for (int s = 0; s < S; ++s) {
+        flags |= H.flags[s];
+        vmax = max_nan(vmax, H.vmax[s]);
+        theta = H.kth[s] > theta ? H.kth[s] : theta;
+    }
     if ((flags & kPfBad) || !(vmax > -kInf)) {
         chain_finish(A, b, row, -1, st | 1);
         return;
     }
     if (flags & kPfOverflow) {
-        chain_fallback<E, kCap>(A, sh, b, row, kind, st, vmax);
+        chain_fallback<E>(A, sh, b, row, kind, st, vmax);
         return;
     }
-    // gather every candidate whose value reaches the largest slice threshold
-    constexpr int kList = 4096;                      // keys in the ring (32 KiB)
+    const bool hinted = (flags & kPfHinted) != 0;
+    // gather every candidate at or above the largest slice filter
+    constexpr int kList = 4096;                      // keys at the front of the ring (32 KiB)
     uint64_t* list = reinterpret_cast<uint64_t*>(R.buf);
     int* rank = reinterpret_cast<int*>(R.buf + kList * 8);
-    const uint32_t th = static_cast<uint32_t>(theta >> 32);
-    if (threadIdx.x == 0) { sh.lcnt = 0; sh.oflow = 0; }
-    __syncthreads();
-    for (int s = 0; s < S; ++s) {
-        const int c = __ldcg(&part_hdr(A.W, b, s, S)->cnt);
-        const uint64_t* keys = part_keys(A.W, b, s, S);
-        for (int i0 = 0; i0 < c; i0 += kThreads) {
-            const int i = i0 + threadIdx.x;
-            uint64_t key = 0;
-            bool p = false;
-            if (i < c) {
-                key = __ldcg(keys + i);
-                p = static_cast<uint32_t>(key >> 32) >= th;
-            }
-            const uint32_t bal = __ballot_sync(0xffffffffu, p);
-            int base = 0;
-            const int lane = threadIdx.x & 31;
-            if (lane == 0 && bal) base = atomicAdd(&sh.lcnt, __popc(bal));
-            base = __shfl_sync(0xffffffffu, base, 0);
-            if (p) {
-                const int pos = base + __popc(bal & ((1u << lane) - 1u));
-                if (pos < kList) list[pos] = key;
-                else sh.oflow = 1;
-            }
-        }
-    }
-    __syncthreads();
+    gather_keys(A.W, b, S, H, [&](uint64_t key) { return key >= theta; }, list, kList, &sh.lcnt, &sh.oflow);
     int n = sh.lcnt;
     if (sh.oflow || n > kList) {
         __syncthreads();
-        chain_fallback<E, kCap>(A, sh, b, row, kind, st, vmax);
+        chain_fallback<E>(A, sh, b, row, kind, st, vmax);
         return;
+    }
+    if (n < k) {
+        __syncthreads();
+        if (hinted) {
+            // the hint was above the row's k-th value: stream the row again without it
+            if (threadIdx.x == 0) {
+                __stcg(&A.W.req[b].status, st);
+                Task t;
+                t.b = b; t.row = row; t.kind = kind | kNoHint; t.aux = 0;
+                push_task(A.W, t);
+            }
+            return;
+        }
+        chain_fallback<E>(A, sh, b, row, kind, st, vmax);
+        return;
+    }
+    if (n > 2 * k + 64) {
+        // certified pre-reduction: fewer keys for the quadratic selection
+        bool cert;
+        const uint32_t F = hist_bound_list(list, n, k, hkey(theta), sh.hist, sh.scratch, cert);
+        if (cert && F > hkey(theta)) n = compact_list(list, n, F, sh.ired);
     }
     uint64_t kth;
     bool of = false;
-    const int keep = select_to(list, n, k, true, rank, sh.cand, kCap, kth, of, sh.sh64, sh.ired);
+    uint64_t* cand = sh.tk.cand;
+    constexpr int kCandCap = kWarps * TopkSmem::kRegion;
+    const int keep = select_to(list, n, k, true, rank, cand, kCandCap, kth, of, sh.sh64, sh.ired);
     if (of) {
-        chain_fallback<E, kCap>(A, sh, b, row, kind, st, vmax);
+        chain_fallback<E>(A, sh, b, row, kind, st, vmax);
         return;
     }
-    // S = sh.cand[0 .. keep): values >= tau, sorted by value descending
-    const uint32_t tau_key = static_cast<uint32_t>(sh.cand[keep - 1] >> 32);
-    const double m = static_cast<double>(vmax);
-    const double T = A.Td;
+    // S = cand[0 .. keep): values >= tau, sorted by value descending
+    const uint32_t tau_key = hkey(cand[keep - 1]);
+    const float tau = ckey_val(cand[keep - 1]);
+    const float m = vmax, c2 = A.c2;
     double zpart = 0.0;
     for (int i = threadIdx.x; i < keep; i += kThreads)
-        zpart += exp((static_cast<double>(ckey_val(sh.cand[i])) - m) / T);
+        zpart += static_cast<double>(ex2((ckey_val(cand[i]) - m) * c2));
     const double Z = block_sum_d(zpart, sh.red);
-    const double uk = static_cast<double>(A.uniforms[static_cast<long long>(b) * (A.K + 1) + kb]);
+    const uint32_t hint = next_hint(tau, m);
+    if (threadIdx.x == 0) __stcg(&A.W.ctrl->hint0, hint);
 
     // weights of S sorted by token id (ascending): pairs in the ring
     int* tok = reinterpret_cast<int*>(R.buf);
@@ -249,10 +250,10 @@ __device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<kCap>& sh, i
     auto sort_by_token = [&](bool residual, const float* qrow, double& total) {
         double part = 0.0;
         for (int i = threadIdx.x; i < keep; i += kThreads) {
-            const int x = ckey_idx(sh.cand[i]);
+            const int x = ckey_idx(cand[i]);
             int r = 0;
-            for (int j = 0; j < keep; ++j) r += ckey_idx(sh.cand[j]) < x;
-            const double p = exp((static_cast<double>(ckey_val(sh.cand[i])) - m) / T) / Z;
+            for (int j = 0; j < keep; ++j) r += ckey_idx(cand[j]) < x;
+            const double p = static_cast<double>(ex2((ckey_val(cand[i]) - m) * c2)) / Z;
             double w = p;
             if (residual) {
                 const double d = p - static_cast<double>(qrow[x]);
@@ -266,17 +267,19 @@ __device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<kCap>& sh, i
     };
 
     if (kind == kVerify) {
-        const int y = A.draft[static_cast<long long>(b) * A.K + row];
-        double py = 0.0;
+        double py = 0.0, qy = 0.0;
         if (y >= 0 && y < A.V) {
-            const float vy = E::load(chain_lrow<E>(A, b, row), y);
-            if (fkey(vy) >= tau_key) py = exp((static_cast<double>(vy) - m) / T) / Z;
+            const int sy = y / A.SL;
+            const float ly = H.ly[sy];
+            qy = static_cast<double>(H.qy[sy]);
+            if (fkey(ly) >= tau_key) py = static_cast<double>(ex2((ly - m) * c2)) / Z;
         }
-        double qy;
-        const bool acc = chain_accept(A, b, row, y, py, qy, st);
+        const bool acc = chain_accept(A, y, py, qy, ur, st);
         if (acc) {
-            if (threadIdx.x == 0) chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
-            chain_advance(A, b, row, kb, st);
+            if (threadIdx.x == 0) {
+                chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
+                chain_advance(A, b, row, kb, st, hint);
+            }
             return;
         }
         // residual [p - q]_+ lives on S (p = 0 outside it)
@@ -305,16 +308,16 @@ __device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<kCap>& sh, i
     __syncthreads();
     x = sh.ish[0];
     if (threadIdx.x == 0 && x >= 0)
-        chain_diag(A, b, row, (float)(exp((static_cast<double>(E::load(chain_lrow<E>(A, b, row), x)) - m) / T) / Z),
+        chain_diag(A, b, row, (float)(static_cast<double>(ex2((E::load(chain_lrow<E>(A, b, row), x) - m) * c2)) / Z),
                    0.f, (float)Z, 0.f);
     chain_finish(A, b, row, x, st);
 }
 
 // Exact single-CTA path for rows whose top-k set did not fit the candidate
-// buffers (massive ties): tau by bisection over order-preserving keys, then
-// full-row passes.  Slow; correctness only.
-template <class E, int kCap>
-__device__ void chain_fallback(const ChainArgs& A, ChainSmem<kCap>& sh, int b, int row, int kind,
+// buffers (massive ties, adversarial order): tau by bisection over
+// order-preserving keys, then full-row passes.  Slow; correctness only.
+template <class E>
+__device__ void chain_fallback(const ChainArgs& A, ChainSmem<true>& sh, int b, int row, int kind,
                                int st, float vmax) {
     const void* lrow = chain_lrow<E>(A, b, row);
     const int V = A.V, k = A.top_k;
@@ -337,18 +340,19 @@ __device__ void chain_fallback(const ChainArgs& A, ChainSmem<kCap>& sh, int b, i
     };
     const double Z = cta_sum(0, V, wp, sh.red);
     const int kb = chain_k(A, b);
-    const double uk = static_cast<double>(A.uniforms[static_cast<long long>(b) * (A.K + 1) + kb]);
+    const double uk = static_cast<double>(chain_u(A, b, kb));
     if (kind == kVerify) {
         const int y = A.draft[static_cast<long long>(b) * A.K + row];
-        double py = 0.0;
+        double py = 0.0, qy = 0.0;
         if (y >= 0 && y < V) {
-            const float vy = E::load(lrow, y);
-            if (fkey(vy) >= tau) py = exp((static_cast<double>(vy) - m) / A.Td) / Z;
+            py = static_cast<double>(wp(y)) / Z;
+            qy = static_cast<double>(chain_qrow(A, b, row)[y]);
         }
-        double qy;
-        if (chain_accept(A, b, row, y, py, qy, st)) {
-            if (threadIdx.x == 0) chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
-            chain_advance(A, b, row, kb, st);
+        if (chain_accept(A, y, py, qy, static_cast<double>(chain_u(A, b, row)), st)) {
+            if (threadIdx.x == 0) {
+                chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
+                chain_advance(A, b, row, kb, st, 0u);
+            }
             return;
         }
         const float* qrow = chain_qrow(A, b, row);
@@ -406,33 +410,33 @@ __device__ int find_slice(int S, double t, F val, double& before, double* dsh, i
     return s;
 }
 
-template <class E, int kCap>
-__device__ void combine_full(const ChainArgs& A, ChainSmem<kCap>& sh, int b, int row, int kind, int st) {
+template <class E>
+__device__ void combine_full(const ChainArgs& A, ChainSmem<false>& sh, int b, int row, int kind, int st) {
     const int S = A.S;
     const int kb = chain_k(A, b);
     const double cd = static_cast<double>(A.c2);
-    const double uk = static_cast<double>(A.uniforms[static_cast<long long>(b) * (A.K + 1) + kb]);
+    const double uk = static_cast<double>(chain_u(A, b, kb));
+    const double ur = kind == kVerify ? static_cast<double>(chain_u(A, b, row)) : 0.0;
+    const int y = kind == kVerify ? A.draft[static_cast<long long>(b) * A.K + row] : -1;
     const void* lrow = chain_lrow<E>(A, b, row);
+    SliceHdrs& H = sh.hdrs;
+    load_hdrs(A.W, b, S, H);
     if (kind == kResid) {
         const ReqState* rs = &A.W.req[b];
         const float m = static_cast<float>(__ldcg(&rs->m));
         const double Z = __ldcg(&rs->Z);
-        double rp = 0.0, pp = 0.0;
-        for (int s = threadIdx.x; s < S; s += kThreads) {
-            const PartHdr* h = part_hdr(A.W, b, s, S);
-            rp += __ldcg(&h->sum);
-            pp += __ldcg(&h->sum2);
+        double R_mass = 0.0, P_mass = 0.0;
+        for (int s = 0; s < S; ++s) {
+            R_mass += H.sum[s];
+            P_mass += H.sum2[s];
         }
-        const double R_mass = block_sum_d(rp, sh.red);
-        const double P_mass = block_sum_d(pp, sh.red);
         const float* qrow = chain_qrow(A, b, row);
         const float c2 = A.c2, invZ = static_cast<float>(1.0 / Z);
         int x;
         double before;
         if (R_mass > 0.0) {
             const double t = uk * R_mass;
-            const int s = find_slice(S, t, [&](int j) { return __ldcg(&part_hdr(A.W, b, j, S)->sum); },
-                                     before, sh.dsh, sh.ish);
+            const int s = find_slice(S, t, [&](int j) { return H.sum[j]; }, before, sh.dsh, sh.ish);
             auto wr = [&](int xx) -> float {
                 const float d = ex2((E::load(lrow, xx) - m) * c2) * invZ - qrow[xx];
                 return d > 0.f ? d : 0.f;
@@ -442,8 +446,7 @@ __device__ void combine_full(const ChainArgs& A, ChainSmem<kCap>& sh, int b, int
         } else {
             st |= 4;
             const double t = uk * P_mass;
-            const int s = find_slice(S, t, [&](int j) { return __ldcg(&part_hdr(A.W, b, j, S)->sum2); },
-                                     before, sh.dsh, sh.ish);
+            const int s = find_slice(S, t, [&](int j) { return H.sum2[j]; }, before, sh.dsh, sh.ish);
             auto wp = [&](int xx) -> float { return ex2((E::load(lrow, xx) - m) * c2); };
             const int x0 = s * A.SL, x1 = min(A.V, x0 + A.SL);
             x = cta_icdf(x0, x1, t - before, wp, sh.red, sh.ired);
@@ -455,38 +458,34 @@ __device__ void combine_full(const ChainArgs& A, ChainSmem<kCap>& sh, int b, int
     }
     // VERIFY or BONUS: max and normaliser from the slice partials
     uint32_t flags = 0;
-    float vm = -kInf;
-    for (int s = threadIdx.x; s < S; s += kThreads) {
-        const PartHdr* h = part_hdr(A.W, b, s, S);
-        flags |= __ldcg(&h->flags);
-        vm = fmaxf(vm, __ldcg(&h->vmax));
+    float vmax = -kInf;
+    for (int s = 0; s < S; ++s) {
+        flags |= H.flags[s];
+        vmax = max_nan(vmax, H.vmax[s]);
     }
-    flags = block_or(flags, reinterpret_cast<uint32_t*>(sh.red));
-    const uint64_t vk = block_max_u64(static_cast<uint64_t>(fkey(vm)), reinterpret_cast<uint64_t*>(sh.red));
-    const float vmax = fkey_inv(static_cast<uint32_t>(vk));
     if ((flags & kPfBad) || !(vmax > -kInf)) {
         chain_finish(A, b, row, -1, st | 1);
         return;
     }
     const double m = static_cast<double>(vmax);
     auto scaled = [&](int s) -> double {
-        const PartHdr* h = part_hdr(A.W, b, s, S);
-        const double ms = static_cast<double>(__ldcg(&h->vmax));
-        const double sm = __ldcg(&h->sum);
-        return sm > 0.0 ? sm * exp2((ms - m) * cd) : 0.0;
+        const double sm = H.sum[s];
+        return sm > 0.0 ? sm * exp2((static_cast<double>(H.vmax[s]) - m) * cd) : 0.0;
     };
     double zp = 0.0;
     for (int s = threadIdx.x; s < S; s += kThreads) zp += scaled(s);
     const double Z = block_sum_d(zp, sh.red);
     if (kind == kVerify) {
-        const int y = A.draft[static_cast<long long>(b) * A.K + row];
-        double py = 0.0;
-        if (y >= 0 && y < A.V) py = exp((static_cast<double>(E::load(lrow, y)) - m) / A.Td) / Z;
-        double qy;
-        const bool acc = chain_accept(A, b, row, y, py, qy, st);
+        double py = 0.0, qy = 0.0;
+        if (y >= 0 && y < A.V) {
+            const int sy = y / A.SL;
+            py = exp((static_cast<double>(H.ly[sy]) - m) / A.Td) / Z;
+            qy = static_cast<double>(H.qy[sy]);
+        }
+        const bool acc = chain_accept(A, y, py, qy, ur, st);
         if (threadIdx.x == 0) chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
         if (acc) {
-            chain_advance(A, b, row, kb, st);
+            if (threadIdx.x == 0) chain_advance(A, b, row, kb, st, 0u);
             return;
         }
         if (threadIdx.x == 0) {
@@ -518,10 +517,9 @@ __device__ void combine_full(const ChainArgs& A, ChainSmem<kCap>& sh, int b, int
 // the kernel
 // ---------------------------------------------------------------------------
 template <class E, bool kTopk>
-__global__ void __launch_bounds__(kThreads) chain_kernel(const ChainArgs A) {
-    constexpr int kCap = kThreads * E::kVec + 512;
+__global__ void __launch_bounds__(kThreads, 2) chain_kernel(const ChainArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
-    auto& sh = *reinterpret_cast<ChainSmem<kCap>*>(smem + kStages * kChunkBytes);
+    auto& sh = *reinterpret_cast<ChainSmem<kTopk>*>(smem + kStages * kChunkBytes);
     Ring R;
     R.init(smem, sh.bars);
     for (;;) {
@@ -529,8 +527,9 @@ __global__ void __launch_bounds__(kThreads) chain_kernel(const ChainArgs A) {
         int s;
         if (!claim(A.W, A.B, A.S, t, s, &sh.claimed)) break;
         const int b = t.b;
-        int kind = t.kind, row = t.row;
-        const bool initial = kind < 0;
+        int kind = t.kind & kKindMask, row = t.row;
+        const bool initial = t.kind < 0;
+        const bool nohint = !initial && (t.kind & kNoHint);
         if (initial) {
             const int kb = chain_k(A, b);
             kind = (kb < 0 || kb > A.K) ? kInvalid : (kb == 0 ? kBonus : kVerify);
@@ -538,31 +537,65 @@ __global__ void __launch_bounds__(kThreads) chain_kernel(const ChainArgs A) {
         PartHdr* ph = part_hdr(A.W, b, s, A.S);
         uint64_t* pk = part_keys(A.W, b, s, A.S);
         const int x0 = s * A.SL, x1 = min(A.V, x0 + A.SL);
+        uint32_t hint = 0;
         if (kind == kVerify || kind == kBonus) {
             const void* lrow = chain_lrow<E>(A, b, row);
+            // the drafted token: its logit is recorded as the slice streams,
+            // its q fetched early by the slice that holds it
+            DraftWatch dw;
+            dw.x0 = x0; dw.x1 = x1;
+            if (kind == kVerify) {
+                dw.y = A.draft[static_cast<long long>(b) * A.K + row];
+                dw.qrow = chain_qrow(A, b, row);
+            }
+            float* wsl = sh.fsh;
             if constexpr (kTopk) {
-                if (threadIdx.x == 0) { sh.cnt = 0; sh.oflow = 0; }
-                __syncthreads();
-                TopkFn<E, true, kCap> fn;
-                fn.cand = sh.cand; fn.cnt = &sh.cnt; fn.oflow = &sh.oflow; fn.pool = sh.pool;
-                fn.sh64 = sh.sh64; fn.ired = sh.ired; fn.k = A.top_k;
+                if (!nohint) hint = initial ? __ldcg(&A.W.ctrl->hint0) : static_cast<uint32_t>(t.aux);
+                TopkHistFn<E, true> fn;
+                fn.init(&sh.tk, A.top_k, hint);
+                fn.dw = dw;
                 stream_row<E>(R, lrow, A.tma_l != 0, x0, x1, fn);
-                uint64_t kth;
-                const int keep = fn.finish(kth);
-                const uint32_t bad = block_or(fn.bad, reinterpret_cast<uint32_t*>(sh.red));
-                const int wr = keep < A.cap_p ? keep : A.cap_p;
-                for (int i = threadIdx.x; i < wr; i += kThreads) __stcg(pk + i, sh.cand[i]);
+                uint64_t* list = reinterpret_cast<uint64_t*>(R.buf);
+                uint64_t F;
+                uint32_t oflow, bad;
+                int n = fn.finish(list, F, oflow, bad);
+                const float vm = block_max_nan(fn.vmx, reinterpret_cast<float*>(sh.red));
+                if (fn.dw.seen) wsl[0] = fn.dw.ly;
+                if (n > A.cap_p && !oflow && !bad) {
+                    // certified bound first, then the exact top-k (ties kept)
+                    bool cert;
+                    const uint32_t F2 = hist_bound_list(list, n, A.top_k, hkey(F), sh.hist, sh.scratch, cert);
+                    if (cert && F2 > hkey(F)) {
+                        n = compact_list(list, n, F2, sh.ired);
+                        F = static_cast<uint64_t>(F2) << 32;
+                    }
+                    if (n > A.cap_p) {
+                        uint64_t* dst = list + kWarps * TopkSmem::kRegion;
+                        int* rank = reinterpret_cast<int*>(dst + kWarps * TopkSmem::kRegion);
+                        uint64_t kth;
+                        bool of2;
+                        const int keep = select_to(list, n, A.top_k, true, rank, dst, A.cap_p, kth, of2,
+                                                   sh.sh64, sh.ired);
+                        if (of2) oflow = 1;
+                        else F = static_cast<uint64_t>(hkey(kth)) << 32;
+                        n = keep;
+                        list = dst;
+                    }
+                }
+                if (oflow || bad) n = 0;   // the combine does not read the keys then
+                __syncthreads();
+                for (int i = threadIdx.x; i < n; i += kThreads) __stcg(pk + i, list[i]);
                 if (threadIdx.x == 0) {
-                    uint32_t f = bad ? kPfBad : 0u;
-                    if (sh.oflow || keep > A.cap_p) f |= kPfOverflow;
-                    ph->flags = f;
-                    ph->cnt = wr;
-                    ph->kth = kth;
-                    ph->vmax = keep ? ckey_val(sh.cand[0]) : -kInf;
+                    ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u) | (hint ? kPfHinted : 0u);
+                    ph->cnt = n;
+                    ph->kth = F;
+                    ph->vmax = vm;
+                    if (fn.dw.owns()) { ph->ly = wsl[0]; ph->qy = fn.dw.qy; }
                 }
             } else {
                 SumExpFn<E> fn;
                 fn.c = A.c2;
+                fn.dw = dw;
                 stream_row<E>(R, lrow, A.tma_l != 0, x0, x1, fn);
                 // fold per-thread (m_t, s_t) into the slice max and sum
                 const uint64_t mk = block_max_u64(static_cast<uint64_t>(fkey(fn.m)), reinterpret_cast<uint64_t*>(sh.red));
@@ -570,12 +603,15 @@ __global__ void __launch_bounds__(kThreads) chain_kernel(const ChainArgs A) {
                 float sc = 0.f;
                 if (fn.s > 0.f) sc = fn.s * ex2((fn.m - ms) * A.c2);
                 const double tot = block_sum_d(static_cast<double>(sc), sh.red);
-                const uint32_t bad = block_or(fn.bad, reinterpret_cast<uint32_t*>(sh.red));
+                const uint32_t bad = block_or(fn.bad_flag(), reinterpret_cast<uint32_t*>(sh.red));
+                if (fn.dw.seen) wsl[0] = fn.dw.ly;
+                __syncthreads();
                 if (threadIdx.x == 0) {
                     ph->flags = bad ? kPfBad : 0u;
                     ph->cnt = 0;
                     ph->vmax = ms;
                     ph->sum = tot;
+                    if (fn.dw.owns()) { ph->ly = wsl[0]; ph->qy = fn.dw.qy; }
                 }
             }
         } else if (kind == kResid) {
@@ -599,9 +635,9 @@ __global__ void __launch_bounds__(kThreads) chain_kernel(const ChainArgs A) {
             if (kind == kInvalid) {
                 chain_finish(A, b, 0, -1, 16);
             } else if constexpr (kTopk) {
-                combine_topk<E, kCap>(A, R, sh, b, row, kind, st);
+                combine_topk<E>(A, R, sh, b, row, kind, st);
             } else {
-                combine_full<E, kCap>(A, sh, b, row, kind, st);
+                combine_full<E>(A, sh, b, row, kind, st);
             }
             __syncthreads();
         }
@@ -611,8 +647,7 @@ __global__ void __launch_bounds__(kThreads) chain_kernel(const ChainArgs A) {
 
 template <class E, bool kTopk>
 static size_t chain_smem_bytes() {
-    constexpr int kCap = kThreads * E::kVec + 512;
-    return kStages * kChunkBytes + sizeof(ChainSmem<kCap>);
+    return kStages * kChunkBytes + sizeof(ChainSmem<kTopk>);
 }
 
 template <class E, bool kTopk>

@@ -57,6 +57,11 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
 __device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
+// release/acquire fence at GPU scope (orders this thread's, and by
+// cumulativity the CTA's barrier-ordered, memory operations)
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
 __device__ __forceinline__ void nanosleep_ns(uint32_t ns) {
     asm volatile("nanosleep.u32 %0;" :: "r"(ns));
 }
@@ -220,6 +225,20 @@ __device__ __forceinline__ double block_exscan_d(double v, double* red, double& 
     }
     total = tot;
     return base + inc - v;
+}
+
+// max with NaN propagation (PTX max.NaN.f32): a NaN anywhere survives
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+template <int N>
+__device__ __forceinline__ float vmax_nan(const float (&v)[N]) {
+    float m = v[0];
+#pragma unroll
+    for (int j = 1; j < N; ++j) m = max_nan(m, v[j]);
+    return m;
 }
 
 // fast 2^x on the special-function unit (PTX ex2.approx.ftz.f32)

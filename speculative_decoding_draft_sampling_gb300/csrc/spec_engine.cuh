@@ -25,20 +25,43 @@
 
 namespace spec {
 
+// Optional phase timers for development builds (-DSPEC_PROFILE): thread 0
+// adds clock64() deltas per phase to g_prof[2*i] and counts to g_prof[2*i+1].
+#ifdef SPEC_PROFILE
+static __device__ unsigned long long g_prof[64];
+#define SPEC_PROF_T(v) const long long v = clock64()
+#define SPEC_PROF_ADD(i, v)                                                                   \
+    do {                                                                                      \
+        if (threadIdx.x == 0) {                                                               \
+            atomicAdd(&g_prof[2 * (i)], static_cast<unsigned long long>(clock64() - (v)));    \
+            atomicAdd(&g_prof[2 * (i) + 1], 1ull);                                            \
+        }                                                                                     \
+    } while (0)
+#else
+#define SPEC_PROF_T(v)
+#define SPEC_PROF_ADD(i, v)
+#endif
+
 constexpr int kChunkBytes = 12288;   // one ring stage
 constexpr int kStages = 4;           // ring depth: 48 KiB in flight per CTA
 constexpr int kMaxSlices = 32;
 
 enum : uint32_t { kErrWait = 1u, kErrQueue = 2u };
 
+// Queue control words, one 128-byte line per group so that the atomics on
+// `head` and `tail` do not serialise with the polling of `done` / `error`.
 struct Ctrl {
     uint32_t head;     // next unit index to claim
+    uint32_t pad0[31];
     uint32_t tail;     // pushed tasks
+    uint32_t pad1[31];
     uint32_t done;     // finished requests
     uint32_t error;    // kErr* bits
-    uint32_t pad[60];
+    uint32_t pad2[30];
+    uint32_t hint0;    // top-k filter hint (value key) for first rows, from the latest finished row
+    uint32_t pad3[31];
 };
-static_assert(sizeof(Ctrl) == 256, "Ctrl is one 256-byte block");
+static_assert(sizeof(Ctrl) == 512, "Ctrl is four 128-byte lines");
 
 struct Task {
     int32_t b, row, kind, aux;
@@ -55,17 +78,19 @@ static_assert(sizeof(ReqState) == 64, "ReqState is 64 bytes");
 
 // Slice partial written to global scratch; `keys` follow the header.
 struct PartHdr {
-    float vmax;        // slice maximum
+    float vmax;        // slice maximum (over every element, NaN-propagating)
     int32_t cnt;       // number of keys written
     uint32_t flags;    // kPf* bits
     int32_t pad0;
-    uint64_t kth;      // slice-local threshold key (top-k) / best key (argmax)
+    uint64_t kth;      // top-k: the slice's filter as a composite key / argmax: best key
     double sum;        // slice sum (meaning depends on the op)
     double sum2;
-    uint64_t pad1[3];
+    float ly;          // chain: logit of the drafted token (slice holding it)
+    float qy;          // chain: q of the drafted token (slice holding it)
+    uint64_t pad1[2];
 };
 static_assert(sizeof(PartHdr) == 64, "PartHdr is 64 bytes");
-enum : uint32_t { kPfBad = 1u, kPfOverflow = 2u };
+enum : uint32_t { kPfBad = 1u, kPfOverflow = 2u, kPfHinted = 4u };
 
 // Device view of the caller's workspace; offsets computed on the host.
 struct Workspace {
@@ -79,10 +104,11 @@ struct Workspace {
     uint32_t part_stride;
     uint32_t maxt;
     uint64_t extra_stride;
+    int smax;             // partial slots per request
 };
 
-__device__ __forceinline__ PartHdr* part_hdr(const Workspace& W, int b, int s, int S) {
-    return reinterpret_cast<PartHdr*>(W.part + (static_cast<size_t>(b) * S + s) * W.part_stride);
+__device__ __forceinline__ PartHdr* part_hdr(const Workspace& W, int b, int s, int /*S*/) {
+    return reinterpret_cast<PartHdr*>(W.part + (static_cast<size_t>(b) * W.smax + s) * W.part_stride);
 }
 __device__ __forceinline__ uint64_t* part_keys(const Workspace& W, int b, int s, int S) {
     return reinterpret_cast<uint64_t*>(part_hdr(W, b, s, S) + 1);
@@ -130,7 +156,7 @@ __device__ __forceinline__ bool claim(const Workspace& W, int B, int S, Task& t,
                     if (ld_acquire(&W.ctrl->error) != 0) { c.ok = 0; break; }   // another CTA gave up
                     if (it >= kWaitLimit) { atomicOr(&W.ctrl->error, kErrWait); c.ok = 0; break; }
                     nanosleep_ns(ns);
-                    if (ns < 1024) ns <<= 1;
+                    if (ns < 256) ns <<= 1;
                 }
             }
         }
@@ -149,11 +175,11 @@ __device__ __forceinline__ bool claim(const Workspace& W, int B, int S, Task& t,
 __device__ __forceinline__ bool arrive(const Workspace& W, int b, int S, int* sh) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
+        fence_acq_rel_gpu();   // release this CTA's partial
         const uint32_t prev = atomicAdd(&W.counter[b], 1u);
         int last = (prev == static_cast<uint32_t>(S - 1));
         if (last) {
-            __threadfence();
+            fence_acq_rel_gpu();   // acquire the other slices' partials
             W.counter[b] = 0;   // ready for the request's next task
         }
         *sh = last;
@@ -166,21 +192,20 @@ __device__ __forceinline__ bool arrive(const Workspace& W, int b, int S, int* sh
 
 // Thread 0 of the combining CTA: enqueue the request's next task.
 __device__ __forceinline__ void push_task(const Workspace& W, Task t) {
-    __threadfence();
+    fence_acq_rel_gpu();
     const uint32_t ti = atomicAdd(&W.ctrl->tail, 1u);
     if (ti >= W.maxt) { atomicOr(&W.ctrl->error, kErrQueue); return; }
     __stcg(&W.tasks[ti].b, t.b);
     __stcg(&W.tasks[ti].row, t.row);
     __stcg(&W.tasks[ti].kind, t.kind);
     __stcg(&W.tasks[ti].aux, t.aux);
-    __threadfence();
     st_release(&W.ready[ti], 1u);
 }
 
 // Thread 0 of the combining CTA, after the request's outputs are written by
 // the whole CTA (call after a __syncthreads()).
 __device__ __forceinline__ void finish_request(const Workspace& W) {
-    __threadfence();
+    fence_acq_rel_gpu();
     atomicAdd(&W.ctrl->done, 1u);
 }
 
@@ -221,12 +246,32 @@ struct Ring {
 };
 
 // Stream elements [x0, x1) of one row (16-byte aligned start when `tma`)
-// through the ring.  Calls, on every thread:
-//   fn.pre_vec(active, vals, x) / fn.pre_end()   -- first chunk only, if Fn::kPrepass
-//   fn.vec(active, vals, x)                      -- one 16-byte vector per thread
-//   fn.round_end()                               -- after each round of vectors
-// Tail elements that do not fill a 16-byte vector go through fn.vec with
-// only vals[0] meaningful and `n` = 1 via fn.scalar(active, v, x).
+// through the ring.  Calls, on every thread, per chunk c:
+//   fn.chunk_begin(c)                              -- chunk c is in shared memory
+//   fn.pre_vec(active, vals, x) / fn.pre_scalar / fn.pre_end()
+//                                                  -- chunk 0 only, if Fn::kPrepass
+//                                                     and fn.use_prepass()
+//   fn.vec(active, vals, x)                        -- one 16-byte vector per thread
+//   fn.round_end()                                 -- after each round of vectors
+//   fn.scalar(active, v, x)                        -- tail elements that do not fill
+//                                                     a vector, one per thread
+//   fn.chunk_end(c)                                -- before the CTA barrier that
+//                                                     releases the stage
+//   fn.after_release(c)                            -- after that barrier (uniform
+//                                                     control flow: may synchronise)
+// Functors derive from FnHooks for the hooks they do not use.
+struct FnHooks {
+    static constexpr bool kPrepass = false;
+    __device__ __forceinline__ bool use_prepass() const { return false; }
+    template <int N> __device__ __forceinline__ void pre_vec(bool, const float (&)[N], int) {}
+    __device__ __forceinline__ void pre_scalar(bool, float, int) {}
+    __device__ __forceinline__ void pre_end() {}
+    __device__ __forceinline__ void chunk_begin(int) {}
+    __device__ __forceinline__ void round_end() {}
+    __device__ __forceinline__ void chunk_end(int) {}
+    __device__ __forceinline__ void after_release(int) {}
+};
+
 template <class E, class Fn>
 __device__ void stream_row(Ring& R, const void* row, bool tma, int x0, int x1, Fn& fn) {
     constexpr int CE = kChunkBytes / E::kBytes;
@@ -257,7 +302,8 @@ __device__ void stream_row(Ring& R, const void* row, bool tma, int x0, int x1, F
         }
         const int nv = (ne * E::kBytes) >> 4;
         const int rounds = (nv + kThreads - 1) / kThreads;
-        if (Fn::kPrepass && c == 0) {
+        fn.chunk_begin(c);
+        if (Fn::kPrepass && c == 0 && fn.use_prepass()) {
             for (int r = 0; r < rounds; ++r) {
                 const int v = r * kThreads + threadIdx.x;
                 float vals[VEC];
@@ -293,12 +339,14 @@ __device__ void stream_row(Ring& R, const void* row, bool tma, int x0, int x1, F
             fn.scalar(act, v, cx0 + i);
             fn.round_end();
         }
+        fn.chunk_end(c);
         __syncthreads();   // every thread is done with stage s
         if (tma && threadIdx.x == 0 && c + kStages < nch) {
             const int c2 = c + kStages;
             const int ne2 = min(CE, n - c2 * CE);
             R.issue(s, base + static_cast<long long>(c2) * kChunkBytes, (ne2 * E::kBytes) & ~15);
         }
+        fn.after_release(c);
     }
 }
 
@@ -392,40 +440,41 @@ __device__ double cta_sum(int x0, int x1, W& w, double* red) {
 }
 
 // Inverse CDF over non-negative weights w(x), x ascending in [x0, x1): the
-// smallest x with C(x) > t.  Blocks of kThreads*4 consecutive elements; each
-// thread owns 4 consecutive elements (fp32 prefix inside, fp64 across).
-// If rounding leaves no crossing, returns the last x with w(x) > 0 (or x0).
+// smallest x with C(x) > t.  Blocks of kThreads*16 consecutive elements; each
+// thread owns 16 consecutive elements (fp32 prefix inside, fp64 across), so
+// every thread has 16 independent loads in flight per block.  If rounding
+// leaves no crossing, returns the last x with w(x) > 0 (or x0).
 template <class W>
 __device__ int cta_icdf(int x0, int x1, double t, W& w, double* red, int* ired) {
+    constexpr int PER = 16;
     double base = 0.0;
     int last_pos = -1;
-    for (int b0 = x0; b0 < x1; b0 += kThreads * 4) {
-        const int xs = b0 + threadIdx.x * 4;
-        float wv[4];
+    for (int b0 = x0; b0 < x1; b0 += kThreads * PER) {
+        const int xs = b0 + threadIdx.x * PER;
+        float wv[PER];
         float loc = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < PER; ++j) {
             const int x = xs + j;
             wv[j] = (x < x1) ? w(x) : 0.f;
-            loc += wv[j];
         }
         int lp = -1;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < PER; ++j) {
+            loc += wv[j];
             if (wv[j] > 0.f) lp = xs + j;
+        }
         double tot;
         const double ex = block_exscan_d(static_cast<double>(loc), red, tot);
-        // crossing thread: base+ex <= t < base+ex+loc
         int found = 0x7fffffff;
         if (loc > 0.f && base + ex + static_cast<double>(loc) > t) {
             double c = base + ex;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < PER; ++j) {
                 c += static_cast<double>(wv[j]);
-                if (wv[j] > 0.f && c > t) { found = xs + j; break; }
+                if (found == 0x7fffffff && wv[j] > 0.f && c > t) found = xs + j;
             }
         }
-        // lowest crossing index across the block; also the last positive x
         __syncthreads();
         if (threadIdx.x == 0) { ired[0] = 0x7fffffff; ired[1] = -1; }
         __syncthreads();
@@ -439,6 +488,79 @@ __device__ int cta_icdf(int x0, int x1, double t, W& w, double* red, int* ired) 
         base += tot;
     }
     return last_pos >= 0 ? last_pos : x0;
+}
+
+// Every slice header of a task, in shared memory (loaded in parallel).
+struct SliceHdrs {
+    int cnt[kMaxSlices];
+    int off[kMaxSlices + 1];     // exclusive prefix of cnt
+    uint32_t flags[kMaxSlices];
+    float vmax[kMaxSlices];
+    uint64_t kth[kMaxSlices];
+    double sum[kMaxSlices];
+    double sum2[kMaxSlices];
+    float ly[kMaxSlices];
+    float qy[kMaxSlices];
+};
+
+__device__ inline void load_hdrs(const Workspace& W, int b, int S, SliceHdrs& H) {
+    for (int s = threadIdx.x; s < S; s += kThreads) {
+        const PartHdr* h = part_hdr(W, b, s, S);
+        H.cnt[s] = __ldcg(&h->cnt);
+        H.flags[s] = __ldcg(&h->flags);
+        H.vmax[s] = __ldcg(&h->vmax);
+        H.kth[s] = __ldcg(&h->kth);
+        H.sum[s] = __ldcg(&h->sum);
+        H.sum2[s] = __ldcg(&h->sum2);
+        H.ly[s] = __ldcg(&h->ly);
+        H.qy[s] = __ldcg(&h->qy);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int a = 0;
+        for (int s = 0; s < S; ++s) { H.off[s] = a; a += H.cnt[s]; }
+        H.off[S] = a;
+    }
+    __syncthreads();
+}
+
+// Gather every slice key that `keep(key)` accepts into list[0..*lcnt)
+// (order arbitrary); keys beyond `cap` set *oflow.  All loads independent.
+template <class F>
+__device__ inline void gather_keys(const Workspace& W, int b, int S, const SliceHdrs& H, F keep,
+                                   uint64_t* list, int cap, int* lcnt, int* oflow) {
+    if (threadIdx.x == 0) { *lcnt = 0; *oflow = 0; }
+    __syncthreads();
+    const int total = H.off[S];
+    const int lane = threadIdx.x & 31;
+    for (int f0 = 0; f0 < total; f0 += kThreads * 4) {
+        uint64_t key[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int f = f0 + j * kThreads + threadIdx.x;
+            key[j] = 0;
+            if (f < total) {
+                int s = 0;
+                while (s + 1 < S && H.off[s + 1] <= f) ++s;
+                key[j] = __ldcg(part_keys(W, b, s, S) + (f - H.off[s]));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int f = f0 + j * kThreads + threadIdx.x;
+            const bool p = f < total && keep(key[j]);
+            const uint32_t bal = __ballot_sync(0xffffffffu, p);
+            int base = 0;
+            if (lane == 0 && bal) base = atomicAdd(lcnt, __popc(bal));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (p) {
+                const int pos = base + __popc(bal & ((1u << lane) - 1u));
+                if (pos < cap) list[pos] = key[j];
+                else *oflow = 1;
+            }
+        }
+    }
+    __syncthreads();
 }
 
 }  // namespace spec

@@ -1,15 +1,27 @@
 // spec_select.cuh -- per-slice pass functors for stream_row():
-//   ArgmaxFn   max value with the lowest index (greedy, tree walk)
-//   SumExpFn   max and sum of 2^((l - m) c), c = log2(e)/T (untruncated p)
-//   TopkFn     all elements that can belong to the slice's top-k, found in one
-//              pass with a running lower bound, then an exact selection
-//   ResidFn    sum of [p - q]_+ and of the p weights (two streams)
-// and the exact rank-based selections they and the combines use.
+//   ArgmaxFn    max value with the lowest index (greedy, tree walk)
+//   SumExpFn    max and sum of 2^((l - m) c), c = log2(e)/T (untruncated p)
+//   TopkHistFn  every element that can belong to the row's top-k, found in
+//               one pass behind a certified (or hinted) value threshold
+//   ResidFn     sum of [p - q]_+ and of the p weights (two streams)
+// and the exact rank-based selection and histogram bounds the functors and
+// the combines use.
 #pragma once
 
 #include "spec_engine.cuh"
 
 namespace spec {
+
+// value key of a composite key
+__device__ __forceinline__ uint32_t hkey(uint64_t k) { return static_cast<uint32_t>(k >> 32); }
+
+// Float threshold equivalent to a value-key threshold: for every non-NaN x,
+// x >= key_to_thr(t)  <=>  fkey(x) >= t.
+__device__ __forceinline__ float key_to_thr(uint32_t t) {
+    if (t <= fkey(-kInf)) return -kInf;
+    if (t >= fkey(kInf)) return kInf;
+    return fkey_inv(t);
+}
 
 // ---------------------------------------------------------------------------
 // warp bitonic sort, descending, one 64-bit key per lane
@@ -33,65 +45,33 @@ __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
 // ---------------------------------------------------------------------------
 // exact selection from a shared-memory key array (keys unique)
 // ---------------------------------------------------------------------------
-// Ranks live in registers: kPer keys per thread (n <= kPer * kThreads).
-// Keeps min(n, k) keys, or -- with `ties` -- every key whose value (high 32
-// bits) is >= that of the k-th; writes them back sorted descending to
-// cand[0 .. keep).  Returns keep; `kth` = key of rank k-1 (0 when n < k).
-template <int kPer>
-__device__ int select_inplace(uint64_t* cand, int n, int k, bool ties, uint64_t& kth,
-                              uint64_t* sh64, int* ired) {
-    uint64_t key[kPer];
-    int rank[kPer];
-    if (threadIdx.x == 0) sh64[0] = 0;
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int i = threadIdx.x + j * kThreads;
-        rank[j] = 0x7fffffff;
-        key[j] = 0;
-        if (i < n) {
-            key[j] = cand[i];
-            int r = 0;
-            for (int t = 0; t < n; ++t) r += (cand[t] > key[j]);
-            rank[j] = r;
-            if (r == k - 1) sh64[0] = key[j];
-        }
+// number of keys in src[0..n) greater than `me`; src 16-byte aligned (two
+// keys per shared load, every thread reading the same address)
+__device__ __forceinline__ int count_greater(const uint64_t* src, int n, uint64_t me) {
+    const ulonglong2* s2 = reinterpret_cast<const ulonglong2*>(src);
+    int r = 0;
+    const int n2 = n >> 1;
+    for (int t = 0; t < n2; ++t) {
+        const ulonglong2 p = s2[t];
+        r += (p.x > me) + (p.y > me);
     }
-    __syncthreads();
-    kth = sh64[0];
-    int keep;
-    if (n < k) {
-        keep = n;
-    } else if (!ties) {
-        keep = k;
-    } else {
-        const uint32_t th = static_cast<uint32_t>(kth >> 32);
-        int c = 0;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j)
-            if (rank[j] != 0x7fffffff && static_cast<uint32_t>(key[j] >> 32) >= th) ++c;
-        keep = block_sum_i(c, ired);
-    }
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < kPer; ++j)
-        if (rank[j] < keep) cand[rank[j]] = key[j];
-    __syncthreads();
-    return keep;
+    if (n & 1) r += src[n - 1] > me;
+    return r;
 }
 
-// Same selection with ranks in shared memory (large n, e.g. a combine over
-// many slices): src[0..n) -> dst[0..keep) sorted descending.  keep is capped
-// at dst_cap; *overflow set when the ties rule wanted more.
+// src[0..n) (16-byte aligned) -> dst[0..keep) sorted descending.  Keeps
+// min(n, k) keys or -- with `ties` -- every key whose value (high 32 bits)
+// reaches that of the k-th.  keep is capped at dst_cap; `overflow` is set
+// when the ties rule wanted more.  `kth` = key of rank k-1 (0 when n < k).
+// `rank` is shared scratch of n ints.
 __device__ inline int select_to(const uint64_t* src, int n, int k, bool ties, int* rank,
-                         uint64_t* dst, int dst_cap, uint64_t& kth, bool& overflow,
-                         uint64_t* sh64, int* ired) {
+                                uint64_t* dst, int dst_cap, uint64_t& kth, bool& overflow,
+                                uint64_t* sh64, int* ired) {
     if (threadIdx.x == 0) sh64[0] = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < n; i += kThreads) {
         const uint64_t me = src[i];
-        int r = 0;
-        for (int t = 0; t < n; ++t) r += (src[t] > me);
+        const int r = count_greater(src, n, me);
         rank[i] = r;
         if (r == k - 1) sh64[0] = me;
     }
@@ -103,9 +83,9 @@ __device__ inline int select_to(const uint64_t* src, int n, int k, bool ties, in
     } else if (!ties) {
         keep = k;
     } else {
-        const uint32_t th = static_cast<uint32_t>(kth >> 32);
+        const uint32_t th = hkey(kth);
         int c = 0;
-        for (int i = threadIdx.x; i < n; i += kThreads) c += (static_cast<uint32_t>(src[i] >> 32) >= th);
+        for (int i = threadIdx.x; i < n; i += kThreads) c += hkey(src[i]) >= th;
         keep = block_sum_i(c, ired);
     }
     overflow = keep > dst_cap;
@@ -117,206 +97,461 @@ __device__ inline int select_to(const uint64_t* src, int n, int k, bool ties, in
 }
 
 // ---------------------------------------------------------------------------
-// functors
+// certified histogram bound
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t bad_value(float v) {
-    return (v != v) || (v == kInf);
+// A lower bound B >= lo on the value key of the k-th largest key such that at
+// least k keys have value key >= B: the lower edge of the highest bin of a
+// 64-bin histogram over [lo, max] whose suffix count reaches k; a bottom bin
+// holding the k-th is split again until it is one key wide.  `each(f)` calls
+// f(value key) for every key this thread owns.  `certified` is set when at
+// least k keys reach lo (then B is a bound for any superset of the keys).
+// All threads; hist[64], scratch[kWarps + 1] shared.
+template <class Each>
+__device__ uint32_t hist_bound(Each each, int k, uint32_t lo, int* hist, uint32_t* scratch, bool& certified) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint32_t mk = 0;
+    each([&](uint32_t h) { mk = max(mk, h); });
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+    __syncthreads();
+    if (lane == 0) scratch[w] = mk;
+    __syncthreads();
+    uint32_t top = scratch[0];
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) top = max(top, scratch[i]);
+    const uint32_t d = top > lo ? top - lo : 0u;
+    const int bits = 32 - __clz(d);
+    uint32_t sh = bits > 6 ? static_cast<uint32_t>(bits - 6) : 0u;
+    uint32_t bound = lo;
+    certified = false;
+    for (int round = 0; round < 6; ++round) {
+        for (int i = threadIdx.x; i < 64; i += kThreads) hist[i] = 0;
+        __syncthreads();
+        each([&](uint32_t h) {
+            if (h >= lo) {
+                const uint32_t bb = (h - lo) >> sh;
+                atomicAdd(&hist[bb < 64 ? bb : 63], 1);
+            }
+        });
+        __syncthreads();
+        if (w == 0) {
+            const int h0 = hist[2 * lane], h1 = hist[2 * lane + 1];
+            int suf = h0 + h1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_down_sync(0xffffffffu, suf, o);
+                if (lane + o < 32) suf += t;
+            }
+            const int above = suf - h0 - h1;
+            int best = -1;
+            if (above + h1 >= k) best = 2 * lane + 1;
+            else if (above + h1 + h0 >= k) best = 2 * lane;
+            const uint32_t ql = __ballot_sync(0xffffffffu, best >= 0);
+            const int bl = ql ? 31 - __clz(ql) : -1;
+            const int bb = __shfl_sync(0xffffffffu, best, bl >= 0 ? bl : 0);
+            if (lane == 0) scratch[kWarps] = static_cast<uint32_t>(bl >= 0 ? bb : -1);
+        }
+        __syncthreads();
+        const int bb = static_cast<int>(scratch[kWarps]);
+        __syncthreads();
+        if (bb < 0) break;                 // fewer than k keys reach lo
+        certified = true;
+        if (bb > 0) {
+            const uint64_t e = static_cast<uint64_t>(lo) + (static_cast<uint64_t>(bb) << sh);
+            if (e <= 0xffffffffull) bound = static_cast<uint32_t>(e);
+            break;
+        }
+        if (sh == 0) break;
+        sh = sh >= 6 ? sh - 6 : 0u;
+    }
+    return bound;
 }
 
+// The largest composite key t >= lo64 with at least k keys >= t, when the
+// k-th largest key has value key hkey(lo64) (so t differs from lo64 only in
+// the index bits): bisection over the low 32 bits.  `each(f)` calls f(key)
+// for every key this thread owns.  All threads; ired[kWarps] shared.
+template <class Each>
+__device__ uint64_t composite_bound(Each each, int k, uint64_t lo64, int* ired) {
+    uint64_t lo = lo64, hi = lo64 | 0xffffffffull;
+    for (int it = 0; it < 34 && lo < hi; ++it) {
+        const uint64_t mid = lo + ((hi - lo + 1) >> 1);
+        int c = 0;
+        each([&](uint64_t key) { c += key >= mid; });
+        c = block_sum_i(c, ired);
+        if (c >= k) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// the same over a contiguous shared list
+__device__ inline uint32_t hist_bound_list(const uint64_t* list, int n, int k, uint32_t lo, int* hist,
+                                           uint32_t* scratch, bool& certified) {
+    return hist_bound([&](auto f) { for (int i = threadIdx.x; i < n; i += kThreads) f(hkey(list[i])); },
+                      k, lo, hist, scratch, certified);
+}
+
+// Keep the keys of list[0..n) with value key >= t, in place (order kept).
+// All threads; returns the new count.  ired[kWarps + 1] shared.
+__device__ inline int compact_list(uint64_t* list, int n, uint32_t t, int* ired) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int out = 0;
+    for (int i0 = 0; i0 < n; i0 += kThreads) {
+        const int i = i0 + threadIdx.x;
+        uint64_t key = 0;
+        bool p = false;
+        if (i < n) { key = list[i]; p = hkey(key) >= t; }
+        const uint32_t bal = __ballot_sync(0xffffffffu, p);
+        if (lane == 0) ired[w] = __popc(bal);
+        __syncthreads();
+        int base = out;
+        int tot = 0;
+#pragma unroll
+        for (int j = 0; j < kWarps; ++j) {
+            const int c = ired[j];
+            if (j < w) base += c;
+            tot += c;
+        }
+        __syncthreads();   // every thread read its block before anyone writes
+        if (p) list[base + __popc(bal & ((1u << lane) - 1u))] = key;
+        out += tot;
+        __syncthreads();
+    }
+    return out;
+}
+
+// ---------------------------------------------------------------------------
+// functors
+// ---------------------------------------------------------------------------
+// Watches one element (the drafted token y) as the slice streams by: records
+// its logit from the chunk in shared memory, and thread 0 of the slice that
+// holds y fetches q(y) at the first chunk so that the load overlaps the
+// stream.  The slice reports both with its partial.
+struct DraftWatch {
+    int y = -1;                 // watched index (-1: none)
+    int x0 = 0, x1 = 0;         // the slice
+    const float* qrow = nullptr;
+    float ly = 0.f, qy = 0.f;
+    bool seen = false;
+    __device__ __forceinline__ bool owns() const { return y >= x0 && y < x1; }
+    __device__ __forceinline__ void begin(int c) {
+        if (c == 0 && threadIdx.x == 0 && qrow && owns()) qy = qrow[y];
+    }
+    template <int N>
+    __device__ __forceinline__ void see(const float (&v)[N], int x) {
+        const unsigned d = static_cast<unsigned>(y - x);
+        if (d < static_cast<unsigned>(N)) {
+#pragma unroll
+            for (int j = 0; j < N; ++j)
+                if (static_cast<unsigned>(j) == d) ly = v[j];
+            seen = true;
+        }
+    }
+    __device__ __forceinline__ void see1(float v, int x) {
+        if (x == y) { ly = v; seen = true; }
+    }
+};
+
+// a value that poisons a row: NaN or +inf (a running max_nan sees both)
+__device__ __forceinline__ uint32_t bad_max(float vmx) { return !(vmx < kInf); }
+
+// Max value, lowest index.  Per vector, a NaN-propagating max decides
+// whether any element can beat the thread's best; only then are the elements
+// examined.  Each thread sees its elements in increasing index order, so a
+// strict > keeps the lowest index among equal values.
 template <class E>
-struct ArgmaxFn {
-    static constexpr bool kPrepass = false;
-    uint64_t best = 0;
-    uint32_t bad = 0;
-    __device__ __forceinline__ void pre_vec(bool, const float (&)[E::kVec], int) {}
-    __device__ __forceinline__ void pre_scalar(bool, float, int) {}
-    __device__ __forceinline__ void pre_end() {}
+struct ArgmaxFn : FnHooks {
+    float bv = -kInf;   // best value
+    int bx = -1;        // its index
+    float vmx = -kInf;  // running max with NaN propagation (bad-value test)
     __device__ __forceinline__ void vec(bool act, const float (&v)[E::kVec], int x) {
         if (!act) return;
+        const float m4 = vmax_nan(v);
+        vmx = max_nan(vmx, m4);
+        if (!(m4 <= bv)) {
 #pragma unroll
-        for (int j = 0; j < E::kVec; ++j) {
-            bad |= bad_value(v[j]);
-            const uint64_t k = ckey(v[j], x + j);
-            best = k > best ? k : best;
+            for (int j = 0; j < E::kVec; ++j)
+                if (v[j] > bv) { bv = v[j]; bx = x + j; }
         }
     }
     __device__ __forceinline__ void scalar(bool act, float v, int x) {
         if (!act) return;
-        bad |= bad_value(v);
-        const uint64_t k = ckey(v, x);
-        best = k > best ? k : best;
+        vmx = max_nan(vmx, v);
+        if (v > bv) { bv = v; bx = x; }
     }
-    __device__ __forceinline__ void round_end() {}
+    // composite key of the thread's best (0 when it saw no value above -inf)
+    __device__ __forceinline__ uint64_t key() const { return bx >= 0 ? ckey(bv, bx) : 0ull; }
+    __device__ __forceinline__ uint32_t bad_flag() const { return bad_max(vmx); }
 };
 
 // max and sum of 2^((l - m_t) c) with a per-thread running max m_t
 template <class E>
-struct SumExpFn {
-    static constexpr bool kPrepass = false;
+struct SumExpFn : FnHooks {
     float c;
     float m = -kInf;
     float s = 0.f;
-    uint32_t bad = 0;
-    __device__ __forceinline__ void pre_vec(bool, const float (&)[E::kVec], int) {}
-    __device__ __forceinline__ void pre_scalar(bool, float, int) {}
-    __device__ __forceinline__ void pre_end() {}
-    __device__ __forceinline__ void add(float lm, const float* v, int n) {
+    float vmx = -kInf;
+    DraftWatch dw;
+    __device__ __forceinline__ void chunk_begin(int ci) { dw.begin(ci); }
+    __device__ __forceinline__ void vec(bool act, const float (&v)[E::kVec], int x) {
+        if (!act) return;
+        dw.see(v, x);
+        const float lm = vmax_nan(v);
+        vmx = max_nan(vmx, lm);
         if (lm > m) {
             s *= ex2((m - lm) * c);
             m = lm;
         }
         if (m == -kInf) return;   // every value so far is -inf
-        for (int j = 0; j < n; ++j) s += ex2((v[j] - m) * c);
-    }
-    __device__ __forceinline__ void vec(bool act, const float (&v)[E::kVec], int) {
-        if (!act) return;
-        float lm = v[0];
-        bad |= bad_value(v[0]);
-#pragma unroll
-        for (int j = 1; j < E::kVec; ++j) {
-            lm = fmaxf(lm, v[j]);
-            bad |= bad_value(v[j]);
-        }
-        if (lm > m) {
-            s *= ex2((m - lm) * c);
-            m = lm;
-        }
-        if (m == -kInf) return;
 #pragma unroll
         for (int j = 0; j < E::kVec; ++j) s += ex2((v[j] - m) * c);
     }
-    __device__ __forceinline__ void scalar(bool act, float v, int) {
+    __device__ __forceinline__ void scalar(bool act, float v, int x) {
         if (!act) return;
-        bad |= bad_value(v);
-        add(v, &v, 1);
+        dw.see1(v, x);
+        vmx = max_nan(vmx, v);
+        if (v > m) {
+            s *= ex2((m - v) * c);
+            m = v;
+        }
+        if (m == -kInf) return;
+        s += ex2((v - m) * c);
     }
-    __device__ __forceinline__ void round_end() {}
+    __device__ __forceinline__ uint32_t bad_flag() const { return bad_max(vmx); }
 };
 
-// Elements that can belong to the slice's top-k: a running lower bound
-// `theta` on the slice's k-th largest key filters the stream; survivors go to
-// a shared candidate buffer.  The bound starts as the k-th largest of the
-// per-warp top-8 (or top-32) thread maxima of the first chunk -- each of those
-// is a real element, so at least k elements reach it -- and is raised to the
-// exact k-th largest candidate whenever the buffer fills up.
-//   kTies = true : keep every element whose value equals the k-th value
-//                  (the top-k set S of a target distribution)
-//   kTies = false: keep exactly k by (value desc, index asc) (DDTree lists)
-template <class E, bool kTies, int kCap>
-struct TopkFn {
+// Shared state of TopkHistFn: one candidate region per warp, so a warp
+// appends with ballots and a register counter and never contends with the
+// other warps.
+struct TopkSmem {
+    static constexpr int kRegion = 256;                 // keys per warp
+    alignas(16) uint64_t cand[kWarps * kRegion];
+    uint64_t pool[kThreads];
+    int wcnt[2][kWarps];
+    uint64_t wthr[kWarps];
+    int hist[64];
+    uint32_t scratch[kWarps + 2];
+    uint64_t sh64[2];
+    int ired[kWarps + 4];
+};
+
+// Every element of a slice that can belong to the row's top-k: composite
+// key >= the filter `theta`.  The filter is only ever raised to a certified
+// lower bound on the row's k-th largest key (at least k elements of the row
+// reach it), or set from a hint.  With kTies the filter is a value bound
+// (low 32 bits zero: every element of the k-th value is kept); without, the
+// k-th key is the exact (value desc, index asc) order statistic.
+//
+// Hints are not certified: the combine verifies them (at least k gathered
+// keys reach the filter) and retries the row without a hint otherwise.
+// Without a hint, the first chunk's per-thread maxima give the first
+// certified bound (they are distinct elements, so the k-th largest of them
+// is at most the row's k-th largest).  Whenever a warp region fills past a
+// quarter, the CTA raises the filter to a certified histogram bound over all
+// candidates (kTies = false: an exact composite bound when the values tie)
+// and compacts the regions.  A region that overflows anyway (massive ties
+// with kTies, adversarial order) is reported; the combine then takes its
+// exact fallback.
+template <class E, bool kTies>
+struct TopkHistFn : FnHooks {
     static constexpr bool kPrepass = true;
     static constexpr int VEC = E::kVec;
-    static constexpr int kPer = (kCap + kThreads - 1) / kThreads;
-    uint64_t* cand;     // [kCap] shared
-    int* cnt;           // shared counter
-    int* oflow;         // shared flag
-    uint64_t* pool;     // [kThreads] shared scratch
-    uint64_t* sh64;
-    int* ired;
+    static constexpr int kRegion = TopkSmem::kRegion;
+    static constexpr int kRefineAt = kRegion / 4;
+    TopkSmem* S;
     int k;
-    uint64_t theta = 0;
-    uint64_t tmax = 0;
-    uint32_t bad = 0;
+    uint64_t theta;     // composite filter, CTA-uniform
+    float thr_f;        // float prefilter: v >= thr_f  <=>  value key >= hkey(theta)
+    float vmx;          // running max with NaN propagation (every element)
+    int nw;             // candidates appended by this warp (warp-uniform; may exceed kRegion)
+    uint32_t lost;      // this warp's region overflowed
+    uint32_t tmax;      // prepass: this thread's max value key
+    DraftWatch dw;
 
-    __device__ __forceinline__ bool passes(uint64_t key) const {
-        if (kTies) return static_cast<uint32_t>(key >> 32) >= static_cast<uint32_t>(theta >> 32);
-        return key >= theta;
+    __device__ __forceinline__ void set_theta(uint64_t t) { theta = t; thr_f = key_to_thr(hkey(t)); }
+    __device__ __forceinline__ void init(TopkSmem* s, int kk, uint32_t hint) {
+        S = s; k = kk;
+        set_theta(static_cast<uint64_t>(hint) << 32);
+        vmx = -kInf; nw = 0; lost = 0; tmax = 0;
     }
-    __device__ __forceinline__ void pre_vec(bool act, const float (&v)[VEC], int x) {
+    __device__ __forceinline__ void chunk_begin(int c) { dw.begin(c); }
+    __device__ __forceinline__ bool use_prepass() const { return theta == 0; }
+    __device__ __forceinline__ void pre_vec(bool act, const float (&v)[VEC], int) {
         if (!act) return;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-            const uint64_t key = ckey(v[j], x + j);
-            tmax = key > tmax ? key : tmax;
-        }
+        const float m4 = vmax_nan(v);
+        if (m4 == m4) tmax = max(tmax, fkey(m4));
     }
-    __device__ __forceinline__ void pre_scalar(bool act, float v, int x) {
-        if (!act) return;
-        const uint64_t key = ckey(v, x);
-        tmax = key > tmax ? key : tmax;
+    __device__ __forceinline__ void pre_scalar(bool act, float v, int) {
+        if (act && v == v) tmax = max(tmax, fkey(v));
     }
+    // k-th largest of the warps' top-8 (k <= 64) or top-32 thread maxima
     __device__ void pre_end() {
-        const int per = (k <= 64) ? 8 : 32;
+        const int per = (k <= 8 * kWarps) ? 8 : 32;
         const int P = per * kWarps;
         const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-        const uint64_t s = warp_sort_desc(tmax);
-        if (lane < per) pool[w * per + lane] = s;
-        if (threadIdx.x == 0) sh64[1] = 0;
+        const uint64_t srt = warp_sort_desc(static_cast<uint64_t>(tmax));
+        if (lane < per) S->pool[w * per + lane] = srt;
+        if (threadIdx.x == 0) S->sh64[1] = 0;
         __syncthreads();
         if (k <= P && threadIdx.x < P) {
-            const uint64_t me = pool[threadIdx.x];
-            int r = 0;
-            for (int t = 0; t < P; ++t) r += (pool[t] > me);
-            if (r == k - 1 && me != 0) sh64[1] = me;
+            const uint64_t me = S->pool[threadIdx.x];
+            int r = 0, eq = 0;
+            for (int t = 0; t < P; ++t) {
+                const uint64_t o = S->pool[t];
+                r += o > me;
+                eq += (o == me) & (t < static_cast<int>(threadIdx.x));
+            }
+            // the k-th largest value (ties resolved by position)
+            if (r + eq == k - 1) S->sh64[1] = me;
         }
         __syncthreads();
-        theta = sh64[1];
+        const uint64_t b = S->sh64[1] << 32;
+        if (b > theta) set_theta(b);
         __syncthreads();
     }
-    __device__ __forceinline__ void append(uint32_t m, const uint64_t* keys, int nk) {
-        const int c = __popc(m);
-        if (__ballot_sync(0xffffffffu, c != 0) == 0) return;
+    __device__ __forceinline__ void append(uint32_t m, const float* v, int x) {
         const int lane = threadIdx.x & 31;
+        const int c = __popc(m);
         int incl = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int t = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += t;
         }
-        int base = 0;
-        if (lane == 31) base = atomicAdd(cnt, incl);
-        base = __shfl_sync(0xffffffffu, base, 31);
-        int pos = base + incl - c;
-        for (int j = 0; j < nk; ++j) {
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        uint64_t* reg = S->cand + (threadIdx.x >> 5) * kRegion;
+        int pos = nw + incl - c;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
             if ((m >> j) & 1u) {
-                if (pos < kCap) cand[pos] = keys[j];
-                else *oflow = 1;
+                if (pos < kRegion) reg[pos] = ckey(v[j], x + j);
                 ++pos;
             }
         }
+        nw += total;
+    }
+    __device__ __forceinline__ bool passes(float v, int x) const {
+        return v >= thr_f && (kTies || ckey(v, x) >= theta);
     }
     __device__ __forceinline__ void vec(bool act, const float (&v)[VEC], int x) {
-        uint64_t keys[VEC];
-        uint32_t m = 0;
+        bool any = false;
         if (act) {
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) {
-                bad |= bad_value(v[j]);
-                keys[j] = ckey(v[j], x + j);
-                if (passes(keys[j])) m |= 1u << j;
-            }
+            dw.see(v, x);
+            const float m4 = vmax_nan(v);
+            vmx = max_nan(vmx, m4);
+            any = !(m4 < thr_f);            // NaN lands here too; it is not appended
         }
-        append(m, keys, VEC);
+        if (__any_sync(0xffffffffu, any)) {
+            uint32_t m = 0;
+            if (any) {
+#pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    if (passes(v[j], x + j)) m |= 1u << j;
+            }
+            append(m, v, x);
+        }
     }
     __device__ __forceinline__ void scalar(bool act, float v, int x) {
-        uint64_t key[1] = {0};
-        uint32_t m = 0;
+        bool any = false;
         if (act) {
-            bad |= bad_value(v);
-            key[0] = ckey(v, x);
-            if (passes(key[0])) m = 1;
+            dw.see1(v, x);
+            vmx = max_nan(vmx, v);
+            any = passes(v, x);
         }
-        append(m, key, 1);
-    }
-    // raise theta to the exact k-th candidate when the next round could overflow
-    __device__ void round_end() {
-        __syncthreads();
-        const int n = *cnt;
-        __syncthreads();   // every thread has read cnt before the next round appends
-        if (n > kCap - kThreads * VEC && n <= kCap) {
-            uint64_t kth;
-            const int keep = select_inplace<kPer>(cand, n, k, kTies, kth, sh64, ired);
-            if (threadIdx.x == 0) *cnt = keep;
-            if (n >= k) theta = kth;
-            __syncthreads();
+        if (__any_sync(0xffffffffu, any)) {
+            float vv[VEC] = {};
+            vv[0] = v;
+            append(any ? 1u : 0u, vv, x);
         }
     }
-    // final exact selection; returns keep (keys sorted descending in cand)
-    __device__ int finish(uint64_t& kth) {
+    __device__ __forceinline__ void chunk_end(int c) {
+        if ((threadIdx.x & 31) == 0) S->wcnt[c & 1][threadIdx.x >> 5] = nw;
+    }
+    __device__ __forceinline__ void after_release(int c) {
+        bool need = false;
+#pragma unroll
+        for (int j = 0; j < kWarps; ++j) need |= S->wcnt[c & 1][j] > kRefineAt;
+        if (need) refine();
+    }
+    // raise theta to a certified bound over every candidate, compact the regions
+    __device__ void refine() {
+        const int lane = threadIdx.x & 31;
+        uint64_t* reg = S->cand + (threadIdx.x >> 5) * kRegion;
+        const int n = nw < kRegion ? nw : kRegion;
+        lost |= nw > kRegion;
+        auto each = [&](auto f) { for (int j = lane; j < n; j += 32) f(reg[j]); };
+        bool cert;
+        const uint32_t lo = hkey(theta);
+        const uint32_t b = hist_bound([&](auto f) { each([&](uint64_t key) { f(hkey(key)); }); },
+                                      k, lo, S->hist, S->scratch, cert);
+        if (!cert) return;
+        uint64_t nt = static_cast<uint64_t>(b) << 32;
+        if (!kTies && b == lo) {
+            // the k-th value is lo itself: the exact composite bound among the keys of value lo
+            nt = composite_bound(each, k, theta, S->ired);
+        }
+        if (nt <= theta) return;
+        set_theta(nt);
+        int out = 0;
+        for (int j0 = 0; j0 < n; j0 += 32) {
+            const int j = j0 + lane;
+            uint64_t key = 0;
+            bool p = false;
+            if (j < n) { key = reg[j]; p = key >= nt; }
+            const uint32_t bal = __ballot_sync(0xffffffffu, p);
+            if (p) reg[out + __popc(bal & ((1u << lane) - 1u))] = key;
+            out += __popc(bal);
+        }
+        nw = out;
+        __syncwarp();
+    }
+    // After stream_row: the candidates with key >= the final filter F,
+    // contiguous in list[0..return) (shared, 16-byte aligned, room for
+    // kWarps * kRegion keys).  `oflow` when a region lost keys, `bad` when
+    // the slice holds a NaN or +inf.
+    __device__ int finish(uint64_t* list, uint64_t& F, uint32_t& oflow, uint32_t& bad) {
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+        if (lane == 0) S->wthr[w] = theta;
+        lost |= nw > kRegion;
         __syncthreads();
-        int n = *cnt;
-        if (n > kCap) n = kCap;   // overflow already flagged
-        return select_inplace<kPer>(cand, n, k, kTies, kth, sh64, ired);
+        F = S->wthr[0];
+#pragma unroll
+        for (int j = 1; j < kWarps; ++j) F = S->wthr[j] > F ? S->wthr[j] : F;
+        const uint64_t* reg = S->cand + w * kRegion;
+        const int n = nw < kRegion ? nw : kRegion;
+        int cnt = 0;
+        for (int j0 = 0; j0 < n; j0 += 32) {
+            const int j = j0 + lane;
+            cnt += __popc(__ballot_sync(0xffffffffu, j < n && reg[j] >= F));
+        }
+        const uint32_t lw = __ballot_sync(0xffffffffu, lost) != 0;
+        const uint32_t bw = __ballot_sync(0xffffffffu, bad_max(vmx)) != 0;
+        if (lane == 0) {
+            S->ired[w] = cnt;
+            S->scratch[w] = lw | (bw << 1);
+        }
+        __syncthreads();
+        int base = 0, tot = 0;
+        uint32_t fl = 0;
+#pragma unroll
+        for (int j = 0; j < kWarps; ++j) {
+            if (j < w) base += S->ired[j];
+            tot += S->ired[j];
+            fl |= S->scratch[j];
+        }
+        oflow = fl & 1u;
+        bad = (fl >> 1) & 1u;
+        for (int j0 = 0; j0 < n; j0 += 32) {
+            const int j = j0 + lane;
+            uint64_t key = 0;
+            bool p = false;
+            if (j < n) { key = reg[j]; p = key >= F; }
+            const uint32_t bal = __ballot_sync(0xffffffffu, p);
+            if (p) list[base + __popc(bal & ((1u << lane) - 1u))] = key;
+            base += __popc(bal);
+        }
+        __syncthreads();
+        return tot;
     }
 };
 
@@ -343,5 +578,19 @@ struct ResidFn {
         pw += w;
     }
 };
+
+// block max of a float with NaN propagation; every thread receives it
+__device__ __forceinline__ float block_max_nan(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) r = max_nan(r, red[i]);
+    return r;
+}
 
 }  // namespace spec

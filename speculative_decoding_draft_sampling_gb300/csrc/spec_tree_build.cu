@@ -23,7 +23,7 @@
 
 namespace spec {
 
-constexpr int kBuildCap = kThreads * F32::kVec + 512;   // candidate buffer (keys)
+constexpr int kBuildCap = kWarps * TopkSmem::kRegion;   // selected-list buffer (keys)
 
 struct Ent {                 // a frontier entry or an emitted node
     double Q;
@@ -39,18 +39,19 @@ struct EnumHdr {
 };
 
 struct __align__(16) BuildSmem {
+    TopkSmem tk;             // slice candidates; later the merged list and mask scratch
     uint64_t bars[kStages];
     Claimed claimed;
     int last;
-    int cnt;
-    int oflow;
     int lcnt;
+    int oflow;
     uint64_t sh64[4];
     double red[kWarps];
     int ired[kWarps + 4];
-    uint64_t pool[kThreads];
+    int hist[64];
+    uint32_t scratch[kWarps + 2];
     EnumHdr eh;
-    uint64_t cand[kBuildCap];
+    SliceHdrs hdrs;
 };
 
 // per-request extra scratch: [EnumHdr][lists L*M (tok,int) + (prob,float)][nodes N][pending 2N+2]
@@ -84,6 +85,38 @@ __device__ __forceinline__ void path_set(Ent& e, int d, int r) {
     }
 }
 
+// Exact top-M (value desc, index asc) of one q row, single CTA, by
+// bisection over composite keys; for rows whose slice candidate buffers
+// overflowed (adversarial value order).  Writes the keys (unordered) to
+// list[0..return).
+__device__ int build_fallback(const float* qrow, int V, int M, uint64_t* list, int* ired, int* lcnt) {
+    uint64_t lo = 0, hi = ~0ull;
+    if (V > M) {
+        // invariant: count(key >= lo) >= M; the range halves every step
+        for (int it = 0; it < 66 && lo < hi; ++it) {
+            const uint64_t d = hi - lo;
+            const uint64_t mid = lo + (d >> 1) + (d & 1ull);
+            int c = 0;
+            for (int x = threadIdx.x; x < V; x += kThreads) c += ckey(qrow[x], x) >= mid;
+            c = block_sum_i(c, ired);
+            if (c >= M) lo = mid; else hi = mid - 1;
+        }
+    }
+    if (threadIdx.x == 0) *lcnt = 0;
+    __syncthreads();
+    for (int x = threadIdx.x; x < V; x += kThreads) {
+        const uint64_t key = ckey(qrow[x], x);
+        if (key >= lo) {
+            const int pos = atomicAdd(lcnt, 1);
+            if (pos < M) list[pos] = key;
+        }
+    }
+    __syncthreads();
+    const int n = *lcnt;
+    __syncthreads();
+    return n < M ? n : M;
+}
+
 // Write the final tree of request b from shared memory (all threads).
 __device__ void build_finalize(const BuildArgs& A, BuildSmem& sh, const Ent* nodes, const int* ltok,
                                int b, int count, int st) {
@@ -106,7 +139,7 @@ __device__ void build_finalize(const BuildArgs& A, BuildSmem& sh, const Ent* nod
     }
     // ancestor masks: mask[n] = mask[parent[n]] | bit n, parents first
     unsigned long long* mk = A.anc_mask + static_cast<long long>(b) * N * W;
-    unsigned long long* sm = reinterpret_cast<unsigned long long*>(sh.cand);   // N*W <= 1024 words
+    unsigned long long* sm = reinterpret_cast<unsigned long long*>(sh.tk.cand);   // N*W <= 1024 words
     if (threadIdx.x == 0) {
         for (int n = 0; n < N; ++n) {
             for (int w = 0; w < W; ++w) {
@@ -147,21 +180,31 @@ __global__ void __launch_bounds__(kThreads) build_kernel(const BuildArgs A) {
         uint64_t* pk = part_keys(A.W, b, s, A.S);
         if (!trivial) {
             const int x0 = s * A.SL, x1 = min(A.V, x0 + A.SL);
-            if (threadIdx.x == 0) { sh.cnt = 0; sh.oflow = 0; }
-            __syncthreads();
-            TopkFn<F32, false, kBuildCap> fn;
-            fn.cand = sh.cand; fn.cnt = &sh.cnt; fn.oflow = &sh.oflow; fn.pool = sh.pool;
-            fn.sh64 = sh.sh64; fn.ired = sh.ired; fn.k = M;
+            TopkHistFn<F32, false> fn;
+            fn.init(&sh.tk, M, 0u);
             const float* qrow = A.q + static_cast<long long>(b) * A.q_bs + static_cast<long long>(d - 1) * A.q_rs;
             stream_row<F32>(R, qrow, A.tma_q != 0, x0, x1, fn);
-            uint64_t kth;
-            const int keep = fn.finish(kth);
-            const uint32_t bad = block_or(fn.bad, reinterpret_cast<uint32_t*>(sh.red));
-            for (int i = threadIdx.x; i < keep; i += kThreads) __stcg(pk + i, sh.cand[i]);
+            uint64_t* list = reinterpret_cast<uint64_t*>(R.buf);
+            uint64_t F;
+            uint32_t oflow, bad;
+            int n = fn.finish(list, F, oflow, bad);
+            if (n > A.cap_p && !bad) {
+                // the slice's exact top-M (value desc, index asc); its M-th key is the filter
+                uint64_t* dst = list + kWarps * TopkSmem::kRegion;
+                int* rank = reinterpret_cast<int*>(dst + kWarps * TopkSmem::kRegion);
+                uint64_t kth;
+                bool of2;
+                n = select_to(list, n, M, false, rank, dst, A.cap_p, kth, of2, sh.sh64, sh.ired);
+                F = kth;
+                list = dst;
+            }
+            if (bad) n = 0;
+            __syncthreads();
+            for (int i = threadIdx.x; i < n; i += kThreads) __stcg(pk + i, list[i]);
             if (threadIdx.x == 0) {
-                ph->flags = bad ? kPfBad : 0u;
-                ph->cnt = keep;
-                ph->kth = kth;
+                ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u);
+                ph->cnt = n;
+                ph->kth = F;
             }
         }
         if (!arrive(A.W, b, A.S, &sh.last)) continue;
@@ -207,54 +250,37 @@ __global__ void __launch_bounds__(kThreads) build_kernel(const BuildArgs A) {
         }
         __syncthreads();
         if (!trivial) {
+            load_hdrs(A.W, b, A.S, sh.hdrs);
             uint32_t flags = 0;
             uint64_t theta = 0;
-            for (int j = threadIdx.x; j < A.S; j += kThreads) {
-                const PartHdr* h = part_hdr(A.W, b, j, A.S);
-                flags |= __ldcg(&h->flags);
-                if (__ldcg(&h->cnt) >= M) {
-                    const uint64_t kk = __ldcg(&h->kth);
-                    theta = kk > theta ? kk : theta;
-                }
+            for (int j = 0; j < A.S; ++j) {
+                flags |= sh.hdrs.flags[j];
+                theta = sh.hdrs.kth[j] > theta ? sh.hdrs.kth[j] : theta;
             }
-            flags = block_or(flags, reinterpret_cast<uint32_t*>(sh.red));
-            theta = block_max_u64(theta, reinterpret_cast<uint64_t*>(sh.red));
-            // gather keys >= theta into the candidate buffer, select the top M
-            if (threadIdx.x == 0) sh.lcnt = 0;
-            __syncthreads();
             // gathered keys and their ranks in the rest of the ring
             const size_t used = (static_cast<size_t>(LM) * 8 + 15) & ~static_cast<size_t>(15);
             uint64_t* list = reinterpret_cast<uint64_t*>(R.buf + used);
             const int kList = static_cast<int>((kStages * kChunkBytes - used) / 12);
             int* rank = reinterpret_cast<int*>(list + kList);
-            for (int j = 0; j < A.S; ++j) {
-                const int c = __ldcg(&part_hdr(A.W, b, j, A.S)->cnt);
-                const uint64_t* keys = part_keys(A.W, b, j, A.S);
-                for (int i0 = 0; i0 < c; i0 += kThreads) {
-                    const int i = i0 + threadIdx.x;
-                    uint64_t key = 0;
-                    bool p = false;
-                    if (i < c) { key = __ldcg(keys + i); p = key >= theta; }
-                    const uint32_t bal = __ballot_sync(0xffffffffu, p);
-                    const int lane = threadIdx.x & 31;
-                    int base = 0;
-                    if (lane == 0 && bal) base = atomicAdd(&sh.lcnt, __popc(bal));
-                    base = __shfl_sync(0xffffffffu, base, 0);
-                    if (p) {
-                        const int pos = base + __popc(bal & ((1u << lane) - 1u));
-                        if (pos < kList) list[pos] = key;
-                    }
-                }
+            int n = 0;
+            if (flags & kPfBad) {
+                n = 0;
+            } else if (flags & kPfOverflow) {
+                const float* qrow = A.q + static_cast<long long>(b) * A.q_bs + static_cast<long long>(d - 1) * A.q_rs;
+                n = build_fallback(qrow, A.V, M, list, sh.ired, &sh.lcnt);
+            } else {
+                // every slice key at or above the largest slice filter, then the top M
+                gather_keys(A.W, b, A.S, sh.hdrs, [&](uint64_t key) { return key >= theta; }, list, kList,
+                            &sh.lcnt, &sh.oflow);
+                n = min(sh.lcnt, kList);
             }
-            __syncthreads();
-            const int n = min(sh.lcnt, kList);
             uint64_t kth;
             bool of;
             const int keep = (flags & kPfBad) ? 0
-                             : select_to(list, n, M, false, rank, sh.cand, kBuildCap, kth, of, sh.sh64, sh.ired);
+                             : select_to(list, n, M, false, rank, sh.tk.cand, kBuildCap, kth, of, sh.sh64, sh.ired);
             __syncthreads();
             for (int i = threadIdx.x; i < keep; i += kThreads) {
-                const uint64_t key = sh.cand[i];
+                const uint64_t key = sh.tk.cand[i];
                 ltok[(d - 1) * M + i] = ckey_idx(key);
                 lprob[(d - 1) * M + i] = ckey_val(key);
                 __stcg(gl + 2 * ((d - 1) * M + i), ckey_idx(key));

@@ -92,8 +92,8 @@ __global__ void __launch_bounds__(kThreads) walk_kernel(const WalkArgs A) {
             const int x0 = s * A.SL, x1 = min(A.V, x0 + A.SL);
             ArgmaxFn<E> fn;
             stream_row<E>(R, walk_row<E>(A, b, row, kTree), A.tma_l != 0, x0, x1, fn);
-            const uint64_t best = block_max_u64(fn.best, sh.red);
-            const uint32_t bad = block_or(fn.bad, reinterpret_cast<uint32_t*>(sh.red));
+            const uint64_t best = block_max_u64(fn.key(), sh.red);
+            const uint32_t bad = block_or(fn.bad_flag(), reinterpret_cast<uint32_t*>(sh.red));
             if (threadIdx.x == 0) {
                 ph->flags = bad ? kPfBad : 0u;
                 ph->kth = best;
