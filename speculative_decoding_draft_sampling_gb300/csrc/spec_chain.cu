@@ -26,13 +26,18 @@ enum ChainKind : int { kVerify = 0, kBonus = 1, kResid = 2, kInvalid = 3 };
 constexpr int kKindMask = 7;
 constexpr int kNoHint = 8;        // kind bit: stream the row without a filter hint (a retry)
 
+// combine / slice-reduction scratch (the ring belongs to the producer):
+// up to kScrKeys keys and as many ints
+constexpr int kScrKeys = 2560;
 template <bool kTopk> struct ChainTopkPart {};
-template <> struct ChainTopkPart<true> { TopkSmem tk; };
+template <> struct ChainTopkPart<true> {
+    TopkSmem tk;
+    alignas(16) unsigned char scr[kScrKeys * 12];
+};
 
 template <bool kTopk>
 struct __align__(16) ChainSmem : ChainTopkPart<kTopk> {
-    uint64_t bars[kStages];
-    Claimed claimed;
+    PipeSmem pipe;
     int last;
     int lcnt;
     int oflow;
@@ -80,7 +85,7 @@ __device__ void chain_finish(const ChainArgs& A, int b, int n, int last, int st)
         A.num_accepted[b] = n;
         A.status[b] = st;
     }
-    __syncthreads();
+    csync();
     if (threadIdx.x == 0) finish_request(A.W);
 }
 
@@ -149,6 +154,8 @@ __device__ int warp_icdf_pairs(const int* tok, const double* w, int n, double t)
     return n > 0 ? tok[pick] : -1;
 }
 
+__device__ __forceinline__ int n_slices_dbg(int S) { return S; }
+
 // Filter hint for the next row from this row's top-k threshold tau and max
 // m: half the gap below tau (rows of one target differ little in tau).
 __device__ __forceinline__ uint32_t next_hint(float tau, float m) {
@@ -164,7 +171,7 @@ __device__ void chain_fallback(const ChainArgs& A, ChainSmem<true>& sh, int b, i
                                int st, float vmax);
 
 template <class E>
-__device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<true>& sh, int b, int row,
+__device__ void combine_topk(const ChainArgs& A, ChainSmem<true>& sh, int b, int row,
                              int kind, int st) {
     const int S = A.S;
     const int k = A.top_k;
@@ -175,6 +182,7 @@ __device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<true>& sh, i
     const int y = kind == kVerify ? A.draft[static_cast<long long>(b) * A.K + row] : -1;
     SliceHdrs& H = sh.hdrs;
     load_hdrs(A.W, b, S, H);
+    SPEC_TRACE_EV(5, b, row, n_slices_dbg(S), kind);
     uint32_t flags = 0;
     float vmax = -kInf;
     uint64_t theta = 0;
@@ -193,18 +201,19 @@ __device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<true>& sh, i
     }
     const bool hinted = (flags & kPfHinted) != 0;
     // gather every candidate at or above the largest slice filter
-    constexpr int kList = 4096;                      // keys at the front of the ring (32 KiB)
-    uint64_t* list = reinterpret_cast<uint64_t*>(R.buf);
-    int* rank = reinterpret_cast<int*>(R.buf + kList * 8);
+    constexpr int kList = kScrKeys;
+    uint64_t* list = reinterpret_cast<uint64_t*>(sh.scr);
+    int* rank = reinterpret_cast<int*>(sh.scr + kList * 8);
     gather_keys(A.W, b, S, H, [&](uint64_t key) { return key >= theta; }, list, kList, &sh.lcnt, &sh.oflow);
     int n = sh.lcnt;
+    SPEC_TRACE_EV(6, b, row, n, kind);
     if (sh.oflow || n > kList) {
-        __syncthreads();
+        csync();
         chain_fallback<E>(A, sh, b, row, kind, st, vmax);
         return;
     }
     if (n < k) {
-        __syncthreads();
+        csync();
         if (hinted) {
             // the hint was above the row's k-th value: stream the row again without it
             if (threadIdx.x == 0) {
@@ -229,6 +238,7 @@ __device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<true>& sh, i
     uint64_t* cand = sh.tk.cand;
     constexpr int kCandCap = kWarps * TopkSmem::kRegion;
     const int keep = select_to(list, n, k, true, rank, cand, kCandCap, kth, of, sh.sh64, sh.ired);
+    SPEC_TRACE_EV(7, b, row, n, kind);
     if (of) {
         chain_fallback<E>(A, sh, b, row, kind, st, vmax);
         return;
@@ -245,8 +255,8 @@ __device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<true>& sh, i
     if (threadIdx.x == 0) __stcg(&A.W.ctrl->hint0, hint);
 
     // weights of S sorted by token id (ascending): pairs in the ring
-    int* tok = reinterpret_cast<int*>(R.buf);
-    double* wgt = reinterpret_cast<double*>(R.buf + 16384);
+    int* tok = reinterpret_cast<int*>(sh.scr);
+    double* wgt = reinterpret_cast<double*>(sh.scr + kScrKeys * 4);
     auto sort_by_token = [&](bool residual, const float* qrow, double& total) {
         double part = 0.0;
         for (int i = threadIdx.x; i < keep; i += kThreads) {
@@ -256,7 +266,8 @@ __device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<true>& sh, i
             const double p = static_cast<double>(ex2((ckey_val(cand[i]) - m) * c2)) / Z;
             double w = p;
             if (residual) {
-                const double d = p - static_cast<double>(qrow[x]);
+                const float qx = (x >= 0 && x < A.V) ? qrow[x] : 0.f;   // keys always hold in-range ids
+                const double d = p - static_cast<double>(qx);
                 w = d > 0.0 ? d : 0.0;
             }
             tok[r] = x;
@@ -295,7 +306,7 @@ __device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<true>& sh, i
             sh.ish[0] = x;
             chain_diag(A, b, row, (float)py, (float)qy, (float)Z, (st & 4) ? 0.f : (float)R_mass);
         }
-        __syncthreads();
+        csync();
         chain_finish(A, b, row, sh.ish[0], st);
         return;
     }
@@ -305,9 +316,9 @@ __device__ void combine_topk(const ChainArgs& A, Ring& R, ChainSmem<true>& sh, i
     int x = -1;
     if (threadIdx.x < 32) x = warp_icdf_pairs(tok, wgt, keep, uk * tot);
     if (threadIdx.x == 0) sh.ish[0] = x;
-    __syncthreads();
+    csync();
     x = sh.ish[0];
-    if (threadIdx.x == 0 && x >= 0)
+    if (threadIdx.x == 0 && x >= 0 && x < A.V)
         chain_diag(A, b, row, (float)(static_cast<double>(ex2((E::load(chain_lrow<E>(A, b, row), x) - m) * c2)) / Z),
                    0.f, (float)Z, 0.f);
     chain_finish(A, b, row, x, st);
@@ -403,10 +414,10 @@ __device__ int find_slice(int S, double t, F val, double& before, double* dsh, i
         ish[0] = pick;
         dsh[0] = acc;
     }
-    __syncthreads();
+    csync();
     const int s = ish[0];
     before = dsh[0];
-    __syncthreads();
+    csync();
     return s;
 }
 
@@ -421,6 +432,7 @@ __device__ void combine_full(const ChainArgs& A, ChainSmem<false>& sh, int b, in
     const void* lrow = chain_lrow<E>(A, b, row);
     SliceHdrs& H = sh.hdrs;
     load_hdrs(A.W, b, S, H);
+    SPEC_TRACE_EV(5, b, row, S, kind);
     if (kind == kResid) {
         const ReqState* rs = &A.W.req[b];
         const float m = static_cast<float>(__ldcg(&rs->m));
@@ -475,6 +487,7 @@ __device__ void combine_full(const ChainArgs& A, ChainSmem<false>& sh, int b, in
     double zp = 0.0;
     for (int s = threadIdx.x; s < S; s += kThreads) zp += scaled(s);
     const double Z = block_sum_d(zp, sh.red);
+    SPEC_TRACE_EV(6, b, row, S, kind);
     if (kind == kVerify) {
         double py = 0.0, qy = 0.0;
         if (y >= 0 && y < A.V) {
@@ -483,6 +496,7 @@ __device__ void combine_full(const ChainArgs& A, ChainSmem<false>& sh, int b, in
             qy = static_cast<double>(H.qy[sy]);
         }
         const bool acc = chain_accept(A, y, py, qy, ur, st);
+        SPEC_TRACE_EV(7, b, row, S, kind);
         if (threadIdx.x == 0) chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
         if (acc) {
             if (threadIdx.x == 0) chain_advance(A, b, row, kb, st, 0u);
@@ -516,30 +530,59 @@ __device__ void combine_full(const ChainArgs& A, ChainSmem<false>& sh, int b, in
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
+// what a unit streams: logits row range (VERIFY/BONUS), logits and q
+// (RESID), nothing (invalid k)
+template <class E>
+__device__ __forceinline__ int chain_unit_kind(const ChainArgs& A, const Task& t) {
+    if (t.kind >= 0) return t.kind & kKindMask;
+    const int kb = chain_k(A, t.b);
+    return (kb < 0 || kb > A.K) ? kInvalid : (kb == 0 ? kBonus : kVerify);
+}
+template <class E>
+__device__ __forceinline__ StreamPlan chain_plan(const ChainArgs& A, const Task& t, int kind, int slice) {
+    const int x0 = slice * A.SL, x1 = min(A.V, x0 + A.SL);
+    if (kind == kVerify || kind == kBonus) return plan_single(chain_lrow<E>(A, t.b, t.row), E::kBytes, x0, x1);
+    if (kind == kResid) return plan_dual(chain_lrow<E>(A, t.b, t.row), E::kBytes, chain_qrow(A, t.b, t.row), x0, x1);
+    return plan_none();
+}
+
 template <class E, bool kTopk>
-__global__ void __launch_bounds__(kThreads, 2) chain_kernel(const ChainArgs A) {
+__global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     auto& sh = *reinterpret_cast<ChainSmem<kTopk>*>(smem + kStages * kChunkBytes);
-    Ring R;
-    R.init(smem, sh.bars);
-    for (;;) {
-        Task t;
-        int s;
-        if (!claim(A.W, A.B, A.S, t, s, &sh.claimed)) break;
-        const int b = t.b;
-        int kind = t.kind & kKindMask, row = t.row;
-        const bool initial = t.kind < 0;
-        const bool nohint = !initial && (t.kind & kNoHint);
-        if (initial) {
-            const int kb = chain_k(A, b);
-            kind = (kb < 0 || kb > A.K) ? kInvalid : (kb == 0 ? kBonus : kVerify);
+    const Pipe P = pipe_init(smem, sh.pipe);
+    // the residual pass streams q beside the logits; without q rows (K = 0)
+    // there is no residual pass
+    const bool tma = A.tma_l && (kTopk || A.K == 0 || A.tma_q);
+    if (threadIdx.x >= kThreads) {
+        if (threadIdx.x == kThreads) {
+            producer_loop(A.W, A.B, A.S, P, tma,
+                          [&](Claimed& c) {
+                              if (kTopk && c.task.kind < 0) c.hint = __ldcg(&A.W.ctrl->hint0);
+                          },
+                          [&](const Claimed& c) {
+                              return chain_plan<E>(A, c.task, chain_unit_kind<E>(A, c.task), c.slice);
+                          });
         }
+        return;
+    }
+    uint32_t seq = 0;
+    for (uint32_t u = 0;; ++u) {
+        const Claimed cl = next_unit(P, u);
+        if (!cl.ok) break;
+        const Task t = cl.task;
+        const int s = cl.slice;
+        SPEC_TRACE_EV(0, t.b, t.row, s, t.kind);
+        const int b = t.b;
+        const int row = t.row;
+        const bool initial = t.kind < 0;
+        const int kind = chain_unit_kind<E>(A, t);
+        const bool nohint = !initial && (t.kind & kNoHint);
         PartHdr* ph = part_hdr(A.W, b, s, A.S);
         uint64_t* pk = part_keys(A.W, b, s, A.S);
         const int x0 = s * A.SL, x1 = min(A.V, x0 + A.SL);
-        uint32_t hint = 0;
+        const StreamPlan plan = chain_plan<E>(A, t, kind, s);
         if (kind == kVerify || kind == kBonus) {
-            const void* lrow = chain_lrow<E>(A, b, row);
             // the drafted token: its logit is recorded as the slice streams,
             // its q fetched early by the slice that holds it
             DraftWatch dw;
@@ -550,15 +593,16 @@ __global__ void __launch_bounds__(kThreads, 2) chain_kernel(const ChainArgs A) {
             }
             float* wsl = sh.fsh;
             if constexpr (kTopk) {
-                if (!nohint) hint = initial ? __ldcg(&A.W.ctrl->hint0) : static_cast<uint32_t>(t.aux);
+                const uint32_t hint = nohint ? 0u : (initial ? cl.hint : static_cast<uint32_t>(t.aux));
                 TopkHistFn<E, true> fn;
                 fn.init(&sh.tk, A.top_k, hint);
                 fn.dw = dw;
-                stream_row<E>(R, lrow, A.tma_l != 0, x0, x1, fn);
-                uint64_t* list = reinterpret_cast<uint64_t*>(R.buf);
+                if (!consume_row<E>(P, seq, plan, tma, x0, fn)) break;
+                SPEC_TRACE_EV(4, b, row, s, kind);
                 uint64_t F;
                 uint32_t oflow, bad;
-                int n = fn.finish(list, F, oflow, bad);
+                int n = fn.finish(F, oflow, bad);
+                uint64_t* list = sh.tk.cand;
                 const float vm = block_max_nan(fn.vmx, reinterpret_cast<float*>(sh.red));
                 if (fn.dw.seen) wsl[0] = fn.dw.ly;
                 if (n > A.cap_p && !oflow && !bad) {
@@ -570,12 +614,12 @@ __global__ void __launch_bounds__(kThreads, 2) chain_kernel(const ChainArgs A) {
                         F = static_cast<uint64_t>(F2) << 32;
                     }
                     if (n > A.cap_p) {
-                        uint64_t* dst = list + kWarps * TopkSmem::kRegion;
-                        int* rank = reinterpret_cast<int*>(dst + kWarps * TopkSmem::kRegion);
+                        uint64_t* dst = reinterpret_cast<uint64_t*>(sh.scr);
+                        int* rank = reinterpret_cast<int*>(sh.scr + kScrKeys * 8);
                         uint64_t kth;
                         bool of2;
-                        const int keep = select_to(list, n, A.top_k, true, rank, dst, A.cap_p, kth, of2,
-                                                   sh.sh64, sh.ired);
+                        const int keep = select_to(list, n, A.top_k, true, rank, dst, min(A.cap_p, kScrKeys), kth,
+                                                   of2, sh.sh64, sh.ired);
                         if (of2) oflow = 1;
                         else F = static_cast<uint64_t>(hkey(kth)) << 32;
                         n = keep;
@@ -583,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 2) chain_kernel(const ChainArgs A) {
                     }
                 }
                 if (oflow || bad) n = 0;   // the combine does not read the keys then
-                __syncthreads();
+                csync();
                 for (int i = threadIdx.x; i < n; i += kThreads) __stcg(pk + i, list[i]);
                 if (threadIdx.x == 0) {
                     ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u) | (hint ? kPfHinted : 0u);
@@ -596,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 2) chain_kernel(const ChainArgs A) {
                 SumExpFn<E> fn;
                 fn.c = A.c2;
                 fn.dw = dw;
-                stream_row<E>(R, lrow, A.tma_l != 0, x0, x1, fn);
+                if (!consume_row<E>(P, seq, plan, tma, x0, fn)) break;
                 // fold per-thread (m_t, s_t) into the slice max and sum
                 const uint64_t mk = block_max_u64(static_cast<uint64_t>(fkey(fn.m)), reinterpret_cast<uint64_t*>(sh.red));
                 const float ms = fkey_inv(static_cast<uint32_t>(mk));
@@ -605,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 2) chain_kernel(const ChainArgs A) {
                 const double tot = block_sum_d(static_cast<double>(sc), sh.red);
                 const uint32_t bad = block_or(fn.bad_flag(), reinterpret_cast<uint32_t*>(sh.red));
                 if (fn.dw.seen) wsl[0] = fn.dw.ly;
-                __syncthreads();
+                csync();
                 if (threadIdx.x == 0) {
                     ph->flags = bad ? kPfBad : 0u;
                     ph->cnt = 0;
@@ -620,8 +664,7 @@ __global__ void __launch_bounds__(kThreads, 2) chain_kernel(const ChainArgs A) {
             fn.m = static_cast<float>(__ldcg(&rs->m));
             fn.c = A.c2;
             fn.invZ = static_cast<float>(1.0 / __ldcg(&rs->Z));
-            stream_row2<E>(R, chain_lrow<E>(A, b, row), chain_qrow(A, b, row),
-                           (A.tma_l && A.tma_q), x0, x1, fn);
+            if (!consume_row2<E>(P, seq, plan, tma, x0, fn)) break;
             const double rsum = block_sum_d(static_cast<double>(fn.r), sh.red);
             const double psum = block_sum_d(static_cast<double>(fn.pw), sh.red);
             if (threadIdx.x == 0) {
@@ -630,19 +673,21 @@ __global__ void __launch_bounds__(kThreads, 2) chain_kernel(const ChainArgs A) {
                 ph->sum2 = psum;
             }
         }
+        SPEC_TRACE_EV(1, b, row, s, kind);
         if (arrive(A.W, b, A.S, &sh.last)) {
+            SPEC_TRACE_EV(2, b, row, s, kind);
             const int st = initial ? 0 : __ldcg(&A.W.req[b].status);
             if (kind == kInvalid) {
                 chain_finish(A, b, 0, -1, 16);
             } else if constexpr (kTopk) {
-                combine_topk<E>(A, R, sh, b, row, kind, st);
+                combine_topk<E>(A, sh, b, row, kind, st);
             } else {
                 combine_full<E>(A, sh, b, row, kind, st);
             }
-            __syncthreads();
+            csync();
+            SPEC_TRACE_EV(3, b, row, s, kind);
         }
     }
-    if (R.err) atomicOr(&A.W.ctrl->error, kErrWait);
 }
 
 template <class E, bool kTopk>
@@ -656,7 +701,7 @@ static cudaError_t chain_launch(const ChainArgs& A, int grid, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(chain_kernel<E, kTopk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    chain_kernel<E, kTopk><<<grid, kThreads, smem, st>>>(A);
+    chain_kernel<E, kTopk><<<grid, kBlockThreads, smem, st>>>(A);
     return cudaGetLastError();
 }
 
@@ -670,14 +715,14 @@ int chain_occupancy(int ldt, bool topk) {
     const int smem = static_cast<int>(chain_smem(ldt, topk));
     if (ldt == 0) {
         if (topk) { cudaFuncSetAttribute(chain_kernel<F32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, chain_kernel<F32, true>, kThreads, smem); }
+                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, chain_kernel<F32, true>, kBlockThreads, smem); }
         else { cudaFuncSetAttribute(chain_kernel<F32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-               cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, chain_kernel<F32, false>, kThreads, smem); }
+               cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, chain_kernel<F32, false>, kBlockThreads, smem); }
     } else {
         if (topk) { cudaFuncSetAttribute(chain_kernel<BF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, chain_kernel<BF16, true>, kThreads, smem); }
+                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, chain_kernel<BF16, true>, kBlockThreads, smem); }
         else { cudaFuncSetAttribute(chain_kernel<BF16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-               cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, chain_kernel<BF16, false>, kThreads, smem); }
+               cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, chain_kernel<BF16, false>, kBlockThreads, smem); }
     }
     return n;
 }
@@ -689,3 +734,5 @@ cudaError_t chain_run(const ChainArgs& A, int grid, cudaStream_t st) {
 }
 
 }  // namespace spec
+
+SPEC_TRACE_EXPORT(chain)

@@ -9,10 +9,29 @@
 
 namespace spec {
 
-constexpr int kThreads = 256;                 // every engine CTA
-constexpr int kWarps = kThreads / 32;
+constexpr int kThreads = 256;                 // consumer threads of every engine CTA
+constexpr int kWarps = kThreads / 32;         // consumer warps
+constexpr int kBlockThreads = kThreads + 32;  // + one producer warp (warp kWarps)
+
+// Barrier among the consumer threads only (named barrier 1; the producer
+// warp never takes part), with the memory ordering of __syncthreads().
+__device__ __forceinline__ void csync() {
+    asm volatile("bar.sync 1, %0;" :: "n"(kThreads) : "memory");
+}
+// the same, returning whether any consumer thread passed a non-zero value
+__device__ __forceinline__ int csync_or(int p) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred a, b;\n\t"
+        "setp.ne.s32 a, %1, 0;\n\t"
+        "bar.red.or.pred b, 1, %2, a;\n\t"
+        "selp.s32 %0, 1, 0, b;\n\t}"
+        : "=r"(r) : "r"(p), "n"(kThreads) : "memory");
+    return r;
+}
 constexpr uint32_t kWaitLimit = 1u << 22;     // queue-wait polls (with backoff): ~seconds, never forever
-constexpr uint32_t kMbarLimit = 1u << 20;     // mbarrier try_wait polls: ~1 s
+constexpr unsigned long long kMbarLimitNs = 2000000000ull;   // an mbarrier wait gives up after 2 s
+constexpr uint32_t kMbarPollLimit = 1u << 26;                  // ... or after this many polls
 constexpr float kInf = __builtin_huge_valf();
 
 // ---------------------------------------------------------------------------
@@ -81,6 +100,10 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// plain arrive (release at CTA scope)
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
                  :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
@@ -92,10 +115,17 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
-// bounded wait for the phase with the given parity; false when it gave up
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// bounded wait for the phase with the given parity (2 s of wall time or
+// kMbarPollLimit polls, whichever comes first); false when it gave up
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     const uint32_t a = smem_u32(bar);
-    for (uint32_t it = 0; it < kMbarLimit; ++it) {
+    unsigned long long t0 = 0;
+    for (uint32_t it = 0; it < kMbarPollLimit; ++it) {
         uint32_t ok;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
@@ -103,6 +133,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(ok) : "r"(a), "r"(parity) : "memory");
         if (ok) return true;
+        if ((it & 255u) == 255u) {
+            const unsigned long long now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kMbarLimitNs) return false;
+        }
     }
     return false;
 }
@@ -158,14 +193,14 @@ __device__ __forceinline__ uint32_t warp_or(uint32_t v) {
     return v;
 }
 
-// Block-wide reductions over kThreads threads; `red` is shared scratch of at
-// least kWarps 8-byte slots.  Every thread receives the result.
+// Reductions over the kThreads consumer threads; `red` is shared scratch of
+// at least kWarps 8-byte slots.  Every consumer thread receives the result.
 __device__ __forceinline__ uint64_t block_max_u64(uint64_t v, uint64_t* red) {
     v = warp_max_u64(v);
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
+    csync();
     if (l == 0) red[w] = v;
-    __syncthreads();
+    csync();
     uint64_t r = red[0];
 #pragma unroll
     for (int i = 1; i < kWarps; ++i) r = red[i] > r ? red[i] : r;
@@ -174,9 +209,9 @@ __device__ __forceinline__ uint64_t block_max_u64(uint64_t v, uint64_t* red) {
 __device__ __forceinline__ double block_sum_d(double v, double* red) {
     v = warp_sum_d(v);
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
+    csync();
     if (l == 0) red[w] = v;
-    __syncthreads();
+    csync();
     double r = 0.0;
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) r += red[i];
@@ -185,9 +220,9 @@ __device__ __forceinline__ double block_sum_d(double v, double* red) {
 __device__ __forceinline__ int block_sum_i(int v, int* red) {
     v = warp_sum_i(v);
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
+    csync();
     if (l == 0) red[w] = v;
-    __syncthreads();
+    csync();
     int r = 0;
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) r += red[i];
@@ -196,9 +231,9 @@ __device__ __forceinline__ int block_sum_i(int v, int* red) {
 __device__ __forceinline__ uint32_t block_or(uint32_t v, uint32_t* red) {
     v = warp_or(v);
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
+    csync();
     if (l == 0) red[w] = v;
-    __syncthreads();
+    csync();
     uint32_t r = 0;
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) r |= red[i];
@@ -214,9 +249,9 @@ __device__ __forceinline__ double block_exscan_d(double v, double* red, double& 
         double t = __shfl_up_sync(0xffffffffu, inc, o);
         if (l >= o) inc += t;
     }
-    __syncthreads();
+    csync();
     if (l == 31) red[w] = inc;
-    __syncthreads();
+    csync();
     double base = 0.0, tot = 0.0;
 #pragma unroll
     for (int i = 0; i < kWarps; ++i) {

@@ -6,9 +6,10 @@
 // says so (early exit).  A *task* is "process row r of request b"; it is cut
 // into S contiguous *slices* of the vocabulary, and each (task, slice) pair
 // is a *unit*.  A persistent grid of CTAs claims units from one global FIFO
-// counter; each unit streams its slice HBM -> shared memory with 1-D TMA
-// bulk copies through a 4-stage mbarrier ring and writes a small partial
-// result.  The CTA that completes the last slice of a task (atomic arrival
+// counter.  Inside a CTA a producer warp claims units and streams each
+// unit's slice HBM -> shared memory with 1-D TMA bulk copies through a
+// kStages mbarrier ring, while eight consumer warps process the chunks and
+// write a small partial result per unit.  The CTA that completes the last slice of a task (atomic arrival
 // counter, last-arriver pattern) combines the partials, takes the decision,
 // and pushes the request's next task, if any, onto the queue.  Tasks of
 // different requests and depths interleave freely: there is no grid-wide
@@ -42,8 +43,58 @@ static __device__ unsigned long long g_prof[64];
 #define SPEC_PROF_ADD(i, v)
 #endif
 
-constexpr int kChunkBytes = 12288;   // one ring stage
-constexpr int kStages = 4;           // ring depth: 48 KiB in flight per CTA
+// Optional event trace for development builds (-DSPEC_TRACE): thread 0
+// appends (globaltimer, SM, event, request, row, slice, aux) records to a
+// buffer installed by the translation unit's spec_trace_setup_<name>().
+#ifdef SPEC_TRACE
+struct TraceRec {
+    unsigned long long t;
+    int sm, ev, b, row, slice, aux;
+};
+static __device__ TraceRec* g_trace;
+static __device__ unsigned g_trace_cap;
+static __device__ unsigned g_trace_n;
+__device__ __forceinline__ void trace_ev(int ev, int b, int row, int slice, int aux) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    int sm;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+    const unsigned i = atomicAdd(&g_trace_n, 1u);
+    if (g_trace && i < g_trace_cap) {
+        TraceRec r;
+        r.t = t; r.sm = sm | (blockIdx.x << 8); r.ev = ev; r.b = b; r.row = row; r.slice = slice; r.aux = aux;
+        g_trace[i] = r;
+    }
+}
+#define SPEC_TRACE_EV(ev, b, row, slice, aux) \
+    do { if (threadIdx.x == 0) ::spec::trace_ev((ev), (b), (row), (slice), (aux)); } while (0)
+#define SPEC_TRACE_EXPORT(name)                                                              \
+    extern "C" int spec_trace_setup_##name(void* buf, unsigned cap) {                        \
+        unsigned z = 0;                                                                      \
+        if (cudaMemcpyToSymbol(::spec::g_trace, &buf, sizeof(buf)) != cudaSuccess) return 1; \
+        if (cudaMemcpyToSymbol(::spec::g_trace_cap, &cap, sizeof(cap)) != cudaSuccess) return 1; \
+        return cudaMemcpyToSymbol(::spec::g_trace_n, &z, sizeof(z)) != cudaSuccess;          \
+    }                                                                                        \
+    extern "C" unsigned spec_trace_count_##name(void) {                                      \
+        unsigned n = 0;                                                                      \
+        cudaMemcpyFromSymbol(&n, ::spec::g_trace_n, sizeof(n));                               \
+        return n;                                                                            \
+    }
+#else
+#define SPEC_TRACE_EV(ev, b, row, slice, aux)
+#define SPEC_TRACE_EXPORT(name)
+#endif
+
+// Ring geometry (development builds may override it).
+#ifndef SPEC_CHUNK_BYTES
+#define SPEC_CHUNK_BYTES 12288
+#endif
+#ifndef SPEC_STAGES
+#define SPEC_STAGES 4
+#endif
+constexpr int kChunkBytes = SPEC_CHUNK_BYTES;   // one ring stage
+constexpr int kStages = SPEC_STAGES;            // ring depth: 48 KiB in flight per CTA by default
+static_assert(kChunkBytes % 4096 == 0 && kStages >= 2, "ring geometry");
 constexpr int kMaxSlices = 32;
 
 enum : uint32_t { kErrWait = 1u, kErrQueue = 2u };
@@ -121,59 +172,51 @@ struct Claimed {
     Task task;
     int slice;
     int ok;
+    uint32_t hint;     // a kernel-specific word the producer fetched with the claim
+    int pad;
 };
 
-// Claim the next unit.  Units [0, B*S) are the initial tasks (kind = -1,
-// row 0, one per request); unit u >= B*S belongs to pushed task (u/S - B).
-__device__ __forceinline__ bool claim(const Workspace& W, int B, int S, Task& t, int& slice,
-                                      Claimed* sh) {
-    if (threadIdx.x == 0) {
-        Claimed c;
-        c.ok = 1;
-        const uint32_t u = atomicAdd(&W.ctrl->head, 1u);
-        const uint32_t slot = u / static_cast<uint32_t>(S);
-        c.slice = static_cast<int>(u % static_cast<uint32_t>(S));
-        if (slot < static_cast<uint32_t>(B)) {
-            c.task.b = static_cast<int>(slot);
-            c.task.row = 0;
-            c.task.kind = -1;
-            c.task.aux = 0;
-        } else {
-            const uint32_t ti = slot - static_cast<uint32_t>(B);
-            if (ti >= W.maxt) {
-                c.ok = 0;
-            } else {
-                uint32_t ns = 32;
-                for (uint32_t it = 0;; ++it) {
-                    if (ld_acquire(&W.ready[ti])) {
-                        c.task.b = __ldcg(&W.tasks[ti].b);
-                        c.task.row = __ldcg(&W.tasks[ti].row);
-                        c.task.kind = __ldcg(&W.tasks[ti].kind);
-                        c.task.aux = __ldcg(&W.tasks[ti].aux);
-                        break;
-                    }
-                    if (ld_acquire(&W.ctrl->done) >= static_cast<uint32_t>(B)) { c.ok = 0; break; }
-                    if (ld_acquire(&W.ctrl->error) != 0) { c.ok = 0; break; }   // another CTA gave up
-                    if (it >= kWaitLimit) { atomicOr(&W.ctrl->error, kErrWait); c.ok = 0; break; }
-                    nanosleep_ns(ns);
-                    if (ns < 256) ns <<= 1;
-                }
-            }
-        }
-        *sh = c;
+// The producer's claim of the next unit (one thread).  Units [0, B*S) are
+// the initial tasks (kind = -1, row 0, one per request); unit u >= B*S
+// belongs to pushed task (u/S - B), whose ready flag it waits for, bounded.
+__device__ inline Claimed claim_unit(const Workspace& W, int B, int S) {
+    Claimed c;
+    c.ok = 1;
+    c.hint = 0;
+    c.pad = 0;
+    const uint32_t u = atomicAdd(&W.ctrl->head, 1u);
+    const uint32_t slot = u / static_cast<uint32_t>(S);
+    c.slice = static_cast<int>(u % static_cast<uint32_t>(S));
+    c.task.b = 0; c.task.row = 0; c.task.kind = -1; c.task.aux = 0;
+    if (slot < static_cast<uint32_t>(B)) {
+        c.task.b = static_cast<int>(slot);
+        return c;
     }
-    __syncthreads();
-    const Claimed c = *sh;
-    t = c.task;
-    slice = c.slice;
-    __syncthreads();
-    return c.ok != 0;
+    const uint32_t ti = slot - static_cast<uint32_t>(B);
+    if (ti >= W.maxt) { c.ok = 0; return c; }
+    uint32_t ns = 32;
+    SPEC_TRACE_EV(10, -1, -1, -1, static_cast<int>(ti));
+    for (uint32_t it = 0;; ++it) {
+        if (ld_acquire(&W.ready[ti])) {
+            c.task.b = __ldcg(&W.tasks[ti].b);
+            c.task.row = __ldcg(&W.tasks[ti].row);
+            c.task.kind = __ldcg(&W.tasks[ti].kind);
+            c.task.aux = __ldcg(&W.tasks[ti].aux);
+            return c;
+        }
+        if (ld_acquire(&W.ctrl->done) >= static_cast<uint32_t>(B)) { c.ok = 0; return c; }
+        if (ld_acquire(&W.ctrl->error) != 0) { c.ok = 0; return c; }   // another CTA gave up
+        if (it >= kWaitLimit) { atomicOr(&W.ctrl->error, kErrWait); c.ok = 0; return c; }
+        nanosleep_ns(ns);
+        if (ns < 256) ns <<= 1;
+    }
 }
 
-// All threads: after the unit's partial is written.  Returns true in the CTA
-// that completed the task's last slice; that CTA owns the combine.
+// Consumers: after the unit's partial is written.  Returns true (in every
+// consumer thread) in the CTA that completed the task's last slice; that CTA
+// owns the combine.
 __device__ __forceinline__ bool arrive(const Workspace& W, int b, int S, int* sh) {
-    __syncthreads();
+    csync();
     if (threadIdx.x == 0) {
         fence_acq_rel_gpu();   // release this CTA's partial
         const uint32_t prev = atomicAdd(&W.counter[b], 1u);
@@ -184,13 +227,11 @@ __device__ __forceinline__ bool arrive(const Workspace& W, int b, int S, int* sh
         }
         *sh = last;
     }
-    __syncthreads();
-    const int last = *sh;
-    __syncthreads();
-    return last != 0;
+    csync();
+    return *sh != 0;
 }
 
-// Thread 0 of the combining CTA: enqueue the request's next task.
+// Consumer thread 0 of the combining CTA: enqueue the request's next task.
 __device__ __forceinline__ void push_task(const Workspace& W, Task t) {
     fence_acq_rel_gpu();
     const uint32_t ti = atomicAdd(&W.ctrl->tail, 1u);
@@ -202,64 +243,196 @@ __device__ __forceinline__ void push_task(const Workspace& W, Task t) {
     st_release(&W.ready[ti], 1u);
 }
 
-// Thread 0 of the combining CTA, after the request's outputs are written by
-// the whole CTA (call after a __syncthreads()).
+// Consumer thread 0 of the combining CTA, after the request's outputs are
+// written by all consumers (call after a csync()).
 __device__ __forceinline__ void finish_request(const Workspace& W) {
     fence_acq_rel_gpu();
     atomicAdd(&W.ctrl->done, 1u);
 }
 
 // ---------------------------------------------------------------------------
-// shared-memory ring fed by TMA bulk copies
+// the producer / consumer pipeline of one CTA
 // ---------------------------------------------------------------------------
-struct Ring {
-    unsigned char* buf;   // kStages * kChunkBytes, 128-byte aligned
-    uint64_t* bar;        // kStages mbarriers
-    uint32_t phase;       // bit s: parity of the next completion of stage s
-    uint32_t err;
-
-    __device__ void init(unsigned char* b, uint64_t* bars) {
-        buf = b;
-        bar = bars;
-        phase = 0;
-        err = 0;
-        if (threadIdx.x == 0) {
-            for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
-            fence_mbar_init();
-        }
-        __syncthreads();
-    }
+// Warp kWarps (the producer) claims units, publishes each unit's descriptor
+// through a two-slot queue, and streams the unit's chunks HBM -> shared
+// memory with 1-D TMA bulk copies into a kStages ring.  The kWarps consumer
+// warps take descriptors in order, wait for each chunk's `full` barrier,
+// process it, and release the stage with one arrive per warp on its `empty`
+// barrier; no consumer ever waits for another consumer while streaming.  The
+// producer runs ahead by up to one unit, so a unit's claim and first bytes
+// overlap the previous unit's tail, finish and combine.  Every wait is
+// bounded; a timeout raises the CTA's abort flag and the workspace error.
+struct Pipe {
+    unsigned char* buf;    // kStages * kChunkBytes, 128-byte aligned
+    uint64_t* full;        // [kStages] count 1: producer's expect_tx + the copies' bytes
+    uint64_t* empty;       // [kStages] count kWarps: one arrive per consumer warp
+    uint64_t* ufull;       // [2] count 1: descriptor published
+    uint64_t* uempty;      // [2] count kWarps: descriptor read
+    Claimed* desc;         // [2]
+    volatile int* abort;   // a wait timed out in this CTA
     __device__ __forceinline__ unsigned char* slot(int s) const { return buf + s * kChunkBytes; }
-    // thread 0: start the copies of one stage (sizes multiple of 16 bytes)
-    __device__ __forceinline__ void issue(int s, const void* src0, uint32_t b0,
-                                          const void* src1 = nullptr, uint32_t b1 = 0,
-                                          uint32_t off1 = 0) {
-        fence_proxy_async_smem();
-        mbar_expect_tx(&bar[s], b0 + b1);
-        if (b0) tma_load_1d(slot(s), src0, b0, &bar[s]);
-        if (b1) tma_load_1d(slot(s) + off1, src1, b1, &bar[s]);
-    }
-    __device__ __forceinline__ void wait(int s) {
-        if (!err && !mbar_wait(&bar[s], (phase >> s) & 1u)) err = 1;   // after one timeout, stop waiting
-        phase ^= 1u << s;
-    }
 };
 
-// Stream elements [x0, x1) of one row (16-byte aligned start when `tma`)
-// through the ring.  Calls, on every thread, per chunk c:
+// shared-memory control block of the pipe (part of every kernel's smem)
+struct PipeSmem {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t ufull[2];
+    uint64_t uempty[2];
+    Claimed desc[2];
+    int abort;
+    int pad[3];
+};
+
+// all kBlockThreads threads, once at kernel start
+__device__ inline Pipe pipe_init(unsigned char* ring, PipeSmem& ps) {
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&ps.full[s], 1);
+            mbar_init(&ps.empty[s], kWarps);
+        }
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(&ps.ufull[j], 1);
+            mbar_init(&ps.uempty[j], kWarps);
+        }
+        ps.abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    Pipe P;
+    P.buf = ring;
+    P.full = ps.full; P.empty = ps.empty; P.ufull = ps.ufull; P.uempty = ps.uempty;
+    P.desc = ps.desc;
+    P.abort = &ps.abort;
+    return P;
+}
+
+// What one unit streams: one row range (logits or q), or a logits range and
+// the fp32 q range beside it in the same stages (the residual pass).
+struct StreamPlan {
+    const unsigned char* src0;   // element x0 of stream 0
+    const unsigned char* src1;   // element x0 of stream 1 (fp32), or null
+    int es0;                     // element bytes of stream 0
+    int n;                       // elements
+    int ce;                      // elements per chunk
+    int nch;                     // chunks (0: the unit streams nothing)
+};
+__device__ __forceinline__ StreamPlan plan_none() {
+    StreamPlan p;
+    p.src0 = nullptr; p.src1 = nullptr; p.es0 = 4; p.n = 0; p.ce = 1; p.nch = 0;
+    return p;
+}
+__device__ __forceinline__ StreamPlan plan_single(const void* row, int es, int x0, int x1) {
+    StreamPlan p;
+    p.src0 = static_cast<const unsigned char*>(row) + static_cast<long long>(x0) * es;
+    p.src1 = nullptr;
+    p.es0 = es;
+    p.n = x1 > x0 ? x1 - x0 : 0;
+    p.ce = kChunkBytes / es;
+    p.nch = (p.n + p.ce - 1) / p.ce;
+    return p;
+}
+template <int kEs>
+__device__ __forceinline__ constexpr int dual_chunk_elems() { return (kChunkBytes / (kEs + 4)) & ~63; }
+__device__ __forceinline__ StreamPlan plan_dual(const void* lrow, int es, const float* qrow, int x0, int x1) {
+    StreamPlan p;
+    p.src0 = static_cast<const unsigned char*>(lrow) + static_cast<long long>(x0) * es;
+    p.src1 = reinterpret_cast<const unsigned char*>(qrow + x0);
+    p.es0 = es;
+    p.n = x1 > x0 ? x1 - x0 : 0;
+    p.ce = es == 4 ? dual_chunk_elems<4>() : dual_chunk_elems<2>();
+    p.nch = (p.n + p.ce - 1) / p.ce;
+    return p;
+}
+
+// Producer lane: issue chunk c of plan p into stage s.  Bytes past the
+// largest 16-byte multiple of each range are not copied (the consumers read
+// them from global memory).
+__device__ __forceinline__ void issue_chunk(const Pipe& P, const StreamPlan& p, int c, int s) {
+    const int ne = min(p.ce, p.n - c * p.ce);
+    const uint32_t b0 = static_cast<uint32_t>(ne * p.es0) & ~15u;
+    const uint32_t b1 = p.src1 ? (static_cast<uint32_t>(ne * 4) & ~15u) : 0u;
+    mbar_expect_tx(&P.full[s], b0 + b1);
+    unsigned char* dst = P.slot(s);
+    if (b0) tma_load_1d(dst, p.src0 + static_cast<long long>(c) * p.ce * p.es0, b0, &P.full[s]);
+    if (b1) tma_load_1d(dst + p.ce * p.es0, p.src1 + static_cast<long long>(c) * p.ce * 4, b1, &P.full[s]);
+}
+
+// The producer warp's loop (lane 0 only).  `fetch(c)` may fill c.hint;
+// `plan(c)` returns the unit's StreamPlan (tma: issue the chunks; otherwise
+// the consumers copy them themselves).
+template <class Fetch, class PlanF>
+__device__ void producer_loop(const Workspace& W, int B, int S, const Pipe& P, bool tma, Fetch fetch, PlanF plan) {
+    uint32_t seq = 0;          // chunks issued so far (ring sequence number)
+    bool dead = false;
+    for (uint32_t u = 0;; ++u) {
+        const int j = u & 1;
+        if (u >= 2 && !mbar_wait(&P.uempty[j], ((u >> 1) - 1) & 1u)) dead = true;
+        Claimed c;
+        if (dead || *P.abort) {
+            c.ok = 0; c.slice = 0; c.hint = 0; c.pad = 0;
+            c.task.b = 0; c.task.row = 0; c.task.kind = 0; c.task.aux = 0;
+        } else {
+            c = claim_unit(W, B, S);
+            if (c.ok) fetch(c);
+        }
+        P.desc[j] = c;
+        mbar_arrive(&P.ufull[j]);
+        if (!c.ok) break;
+        if (!tma) continue;
+        const StreamPlan p = plan(c);
+        for (int ci = 0; ci < p.nch; ++ci, ++seq) {
+            const int s = static_cast<int>(seq % kStages);
+            if (seq >= static_cast<uint32_t>(kStages) && !mbar_wait(&P.empty[s], ((seq / kStages) - 1) & 1u)) {
+                dead = true;
+                break;
+            }
+            if (*P.abort) { dead = true; break; }
+            issue_chunk(P, p, ci, s);
+        }
+        if (dead) {
+            // unblock consumers waiting for a descriptor, then stop
+            *P.abort = 1;
+            atomicOr(&W.ctrl->error, kErrWait);
+        }
+    }
+    if (dead || *P.abort) {
+        // wait (bounded) for the copies still in flight before the CTA can end
+        const uint32_t first = seq > static_cast<uint32_t>(kStages) ? seq - kStages : 0u;
+        for (uint32_t q = first; q < seq; ++q) mbar_wait(&P.full[q % kStages], (q / kStages) & 1u);
+    }
+}
+
+// Consumers: the next unit's descriptor.  ok = 0 ends the consumer loop
+// (every request finished, the queue closed, or an abort).
+__device__ __forceinline__ Claimed next_unit(const Pipe& P, uint32_t u) {
+    const int j = u & 1;
+    const bool got = mbar_wait(&P.ufull[j], (u >> 1) & 1u);
+    Claimed c = P.desc[j];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&P.uempty[j]);
+    if (!got) *P.abort = 1;
+    if (csync_or(!got || *P.abort)) c.ok = 0;
+    return c;
+}
+
+// ---------------------------------------------------------------------------
+// consumer side of a stream
+// ---------------------------------------------------------------------------
+// Calls, on every consumer thread, per chunk c:
 //   fn.chunk_begin(c)                              -- chunk c is in shared memory
 //   fn.pre_vec(active, vals, x) / fn.pre_scalar / fn.pre_end()
 //                                                  -- chunk 0 only, if Fn::kPrepass
-//                                                     and fn.use_prepass()
-//   fn.vec(active, vals, x)                        -- one 16-byte vector per thread
-//   fn.round_end()                                 -- after each round of vectors
+//                                                     and fn.use_prepass() (pre_end
+//                                                     may csync())
+//   fn.vec(active, vals, x)                        -- one 16-byte vector per thread and round
 //   fn.scalar(active, v, x)                        -- tail elements that do not fill
 //                                                     a vector, one per thread
-//   fn.chunk_end(c)                                -- before the CTA barrier that
-//                                                     releases the stage
-//   fn.after_release(c)                            -- after that barrier (uniform
-//                                                     control flow: may synchronise)
-// Functors derive from FnHooks for the hooks they do not use.
+//   fn.chunk_end(c, sm, cx0, nv)                   -- the chunk is still readable: sm
+//                                                     holds nv full vectors from element cx0
+//   fn.after_release(c)                            -- after the warp released the stage
+// chunk_end and after_release run per warp (no consumer barrier).  Functors
+// derive from FnHooks for the hooks they do not use.
 struct FnHooks {
     static constexpr bool kPrepass = false;
     __device__ __forceinline__ bool use_prepass() const { return false; }
@@ -267,164 +440,166 @@ struct FnHooks {
     __device__ __forceinline__ void pre_scalar(bool, float, int) {}
     __device__ __forceinline__ void pre_end() {}
     __device__ __forceinline__ void chunk_begin(int) {}
-    __device__ __forceinline__ void round_end() {}
-    __device__ __forceinline__ void chunk_end(int) {}
+    __device__ __forceinline__ void chunk_end(int, const unsigned char*, int, int) {}
     __device__ __forceinline__ void after_release(int) {}
 };
 
-template <class E, class Fn>
-__device__ void stream_row(Ring& R, const void* row, bool tma, int x0, int x1, Fn& fn) {
-    constexpr int CE = kChunkBytes / E::kBytes;
-    constexpr int VEC = E::kVec;
-    const int n = x1 - x0;
-    if (n <= 0) return;
-    const int nch = (n + CE - 1) / CE;
-    const unsigned char* base = static_cast<const unsigned char*>(row) + static_cast<long long>(x0) * E::kBytes;
-    if (tma && threadIdx.x == 0) {
-        const int pre = nch < kStages ? nch : kStages;
-        for (int c = 0; c < pre; ++c) {
-            const int ne = min(CE, n - c * CE);
-            R.issue(c, base + static_cast<long long>(c) * kChunkBytes, (ne * E::kBytes) & ~15);
-        }
+constexpr int kChunkVecs = kChunkBytes / 16;                  // vectors in a full chunk
+constexpr int kFullRounds = (kChunkVecs + kThreads - 1) / kThreads;
+static_assert(kChunkVecs % kThreads == 0, "a full chunk is a whole number of rounds");
+
+// Wait for chunk `seq` (every consumer thread).  With tma = false the
+// consumers copy it from global memory themselves (the producer issues
+// nothing in that mode).
+__device__ __forceinline__ bool take_chunk(const Pipe& P, uint32_t seq, bool tma, bool& dead,
+                                           const StreamPlan& p, int c) {
+    const int s = static_cast<int>(seq % kStages);
+    if (tma) {
+        const bool ok = !dead && mbar_wait(&P.full[s], (seq / kStages) & 1u);
+        dead = !__all_sync(0xffffffffu, ok);   // warp-uniform from here on
+        if (dead) *P.abort = 1;
+        return !dead;
     }
-    for (int c = 0; c < nch; ++c) {
-        const int s = c % kStages;
-        const int ne = min(CE, n - c * CE);
-        const int cx0 = x0 + c * CE;
-        unsigned char* sm = R.slot(s);
-        if (tma) {
-            R.wait(s);
-        } else {
-            const typename E::T* g = reinterpret_cast<const typename E::T*>(base) + static_cast<long long>(c) * CE;
-            typename E::T* d = reinterpret_cast<typename E::T*>(sm);
-            for (int i = threadIdx.x; i < ne; i += kThreads) d[i] = g[i];
-            __syncthreads();
-        }
+    const int ne = min(p.ce, p.n - c * p.ce);
+    unsigned char* sm = P.slot(s);
+    csync();   // every consumer is done with this stage's previous chunk
+    const unsigned char* g0 = p.src0 + static_cast<long long>(c) * p.ce * p.es0;
+    if (p.es0 == 4) {
+        for (int i = threadIdx.x; i < ne; i += kThreads)
+            reinterpret_cast<uint32_t*>(sm)[i] = reinterpret_cast<const uint32_t*>(g0)[i];
+    } else {
+        for (int i = threadIdx.x; i < ne; i += kThreads)
+            reinterpret_cast<uint16_t*>(sm)[i] = reinterpret_cast<const uint16_t*>(g0)[i];
+    }
+    if (p.src1) {
+        const float* g1 = reinterpret_cast<const float*>(p.src1) + static_cast<long long>(c) * p.ce;
+        float* d1 = reinterpret_cast<float*>(sm + p.ce * p.es0);
+        for (int i = threadIdx.x; i < ne; i += kThreads) d1[i] = g1[i];
+    }
+    csync();
+    return true;
+}
+
+// release chunk `seq` (per warp)
+__device__ __forceinline__ void release_chunk(const Pipe& P, uint32_t seq, bool tma, bool dead) {
+    if (!tma || dead) return;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&P.empty[seq % kStages]);
+}
+
+// Stream one row range (plan from plan_single) through fn.  Returns false
+// (in every consumer thread) when a chunk wait timed out; the caller then
+// leaves the kernel.  `seq` is the consumer's ring sequence number.
+template <class E, class Fn>
+__device__ bool consume_row(const Pipe& P, uint32_t& seq, const StreamPlan& p, bool tma, int x0, Fn& fn) {
+    constexpr int VEC = E::kVec;
+    bool dead = false;
+    for (int c = 0; c < p.nch; ++c, ++seq) {
+        const bool have = take_chunk(P, seq, tma, dead, p, c);
+        const unsigned char* sm = P.slot(static_cast<int>(seq % kStages));
+        const int ne = min(p.ce, p.n - c * p.ce);
+        const int cx0 = x0 + c * p.ce;
         const int nv = (ne * E::kBytes) >> 4;
-        const int rounds = (nv + kThreads - 1) / kThreads;
+        const uint4* sv = reinterpret_cast<const uint4*>(sm);
         fn.chunk_begin(c);
         if (Fn::kPrepass && c == 0 && fn.use_prepass()) {
-            for (int r = 0; r < rounds; ++r) {
-                const int v = r * kThreads + threadIdx.x;
+            for (int v = threadIdx.x; v < (have ? nv : 0); v += kThreads) {
                 float vals[VEC];
-                const bool act = v < nv;
-                if (act) E::unpack(reinterpret_cast<const uint4*>(sm)[v], vals);
-                fn.pre_vec(act, vals, cx0 + v * VEC);
+                E::unpack(sv[v], vals);
+                fn.pre_vec(true, vals, cx0 + v * VEC);
             }
-            const int t0 = (nv << 4) / E::kBytes;
-            if (t0 < ne) {
+            const int t0 = nv * VEC;
+            if (have && t0 + static_cast<int>(threadIdx.x) < ne) {
                 const int i = t0 + threadIdx.x;
-                const bool act = i < ne;
-                float v = 0.f;
-                if (act) v = tma ? E::load(base, static_cast<long long>(c) * CE + i)
-                                 : E::load(sm, i);
-                fn.pre_scalar(act, v, cx0 + i);
+                fn.pre_scalar(true, tma ? E::load(p.src0, static_cast<long long>(c) * p.ce + i) : E::load(sm, i),
+                              cx0 + i);
             }
             fn.pre_end();
         }
-        for (int r = 0; r < rounds; ++r) {
-            const int v = r * kThreads + threadIdx.x;
-            float vals[VEC];
-            const bool act = v < nv;
-            if (act) E::unpack(reinterpret_cast<const uint4*>(sm)[v], vals);
-            fn.vec(act, vals, cx0 + v * VEC);
-            fn.round_end();
-        }
-        const int t0 = (nv << 4) / E::kBytes;
-        if (t0 < ne) {   // fewer than VEC elements left: at most one per thread
-            const int i = t0 + threadIdx.x;
-            const bool act = i < ne;
-            float v = 0.f;
-            if (act) v = tma ? E::load(base, static_cast<long long>(c) * CE + i) : E::load(sm, i);
-            fn.scalar(act, v, cx0 + i);
-            fn.round_end();
-        }
-        fn.chunk_end(c);
-        __syncthreads();   // every thread is done with stage s
-        if (tma && threadIdx.x == 0 && c + kStages < nch) {
-            const int c2 = c + kStages;
-            const int ne2 = min(CE, n - c2 * CE);
-            R.issue(s, base + static_cast<long long>(c2) * kChunkBytes, (ne2 * E::kBytes) & ~15);
-        }
-        fn.after_release(c);
-    }
-}
-
-// Two rows streamed together: logits (E) and fp32 q over the same element
-// range.  fn.vec2(active, lv[VEC], qv[VEC], x), fn.scalar2(active, l, q, x).
-template <class E, class Fn>
-__device__ void stream_row2(Ring& R, const void* lrow, const float* qrow, bool tma,
-                            int x0, int x1, Fn& fn) {
-    constexpr int CE = (kChunkBytes / (E::kBytes + 4)) & ~63;
-    constexpr int VEC = E::kVec;
-    constexpr int LOFF = 0;
-    constexpr int QOFF = CE * E::kBytes;
-    const int n = x1 - x0;
-    if (n <= 0) return;
-    const int nch = (n + CE - 1) / CE;
-    const unsigned char* lb = static_cast<const unsigned char*>(lrow) + static_cast<long long>(x0) * E::kBytes;
-    const float* qb = qrow + x0;
-    auto issue = [&](int c, int s) {
-        const int ne = min(CE, n - c * CE);
-        R.issue(s, lb + static_cast<long long>(c) * CE * E::kBytes, (ne * E::kBytes) & ~15,
-                qb + static_cast<long long>(c) * CE, (ne * 4) & ~15, QOFF);
-    };
-    if (tma && threadIdx.x == 0) {
-        const int pre = nch < kStages ? nch : kStages;
-        for (int c = 0; c < pre; ++c) issue(c, c);
-    }
-    for (int c = 0; c < nch; ++c) {
-        const int s = c % kStages;
-        const int ne = min(CE, n - c * CE);
-        const int cx0 = x0 + c * CE;
-        unsigned char* sm = R.slot(s);
-        if (tma) {
-            R.wait(s);
-        } else {
-            const typename E::T* g = reinterpret_cast<const typename E::T*>(lb) + static_cast<long long>(c) * CE;
-            typename E::T* d = reinterpret_cast<typename E::T*>(sm + LOFF);
-            float* dq = reinterpret_cast<float*>(sm + QOFF);
-            for (int i = threadIdx.x; i < ne; i += kThreads) {
-                d[i] = g[i];
-                dq[i] = qb[static_cast<long long>(c) * CE + i];
-            }
-            __syncthreads();
-        }
-        // vectors of VEC logits (16 bytes) and VEC q values (VEC*4 bytes)
-        const int nv = ne / VEC;
-        const int rounds = (nv + kThreads - 1) / kThreads;
-        for (int r = 0; r < rounds; ++r) {
-            const int v = r * kThreads + threadIdx.x;
-            const bool act = v < nv;
-            float lv[VEC], qv[VEC];
-            if (act) {
-                E::unpack(reinterpret_cast<const uint4*>(sm + LOFF)[v], lv);
-                const float4* q4 = reinterpret_cast<const float4*>(sm + QOFF) + v * (VEC / 4);
+        if (have) {
+            if (nv == kChunkVecs) {
+                // full chunk: every round's vector loaded first (independent loads)
+                float vals[kFullRounds][VEC];
 #pragma unroll
-                for (int j = 0; j < VEC / 4; ++j) {
-                    const float4 f = q4[j];
-                    qv[4 * j] = f.x; qv[4 * j + 1] = f.y; qv[4 * j + 2] = f.z; qv[4 * j + 3] = f.w;
+                for (int r = 0; r < kFullRounds; ++r) E::unpack(sv[r * kThreads + threadIdx.x], vals[r]);
+#pragma unroll
+                for (int r = 0; r < kFullRounds; ++r) fn.vec(true, vals[r], cx0 + (r * kThreads + threadIdx.x) * VEC);
+            } else {
+                const int rounds = (nv + kThreads - 1) / kThreads;
+                for (int r = 0; r < rounds; ++r) {
+                    const int v = r * kThreads + threadIdx.x;
+                    float vals[VEC];
+                    const bool act = v < nv;
+                    if (act) E::unpack(sv[v], vals);
+                    fn.vec(act, vals, cx0 + v * VEC);
+                }
+                const int t0 = nv * VEC;
+                if (t0 < ne) {   // fewer than VEC elements left: at most one per thread
+                    const int i = t0 + threadIdx.x;
+                    const bool act = i < ne;
+                    float v = 0.f;
+                    if (act) v = tma ? E::load(p.src0, static_cast<long long>(c) * p.ce + i) : E::load(sm, i);
+                    fn.scalar(act, v, cx0 + i);
                 }
             }
-            fn.vec2(act, lv, qv, cx0 + v * VEC);
+            fn.chunk_end(c, sm, cx0, nv);
         }
-        const int t0 = nv * VEC;
-        if (t0 < ne) {
-            const int i = t0 + threadIdx.x;
-            const bool act = i < ne;
-            float l = 0.f, qq = 0.f;
-            if (act) {
-                // bytes past the 16-byte-multiple prefix were not copied by TMA
-                const bool l_in = tma ? ((i * E::kBytes + E::kBytes) <= ((ne * E::kBytes) & ~15)) : true;
-                const bool q_in = tma ? ((i * 4 + 4) <= ((ne * 4) & ~15)) : true;
-                l = l_in ? E::load(sm + LOFF, i) : E::load(lb, static_cast<long long>(c) * CE + i);
-                qq = q_in ? reinterpret_cast<const float*>(sm + QOFF)[i] : qb[static_cast<long long>(c) * CE + i];
-            }
-            fn.scalar2(act, l, qq, cx0 + i);
-        }
-        __syncthreads();
-        if (tma && threadIdx.x == 0 && c + kStages < nch) issue(c + kStages, s);
+        release_chunk(P, seq, tma, dead);
+        if (have) fn.after_release(c);
     }
+    return !csync_or(dead);
+}
+
+// Two ranges streamed together (plan from plan_dual): logits (E) and fp32 q
+// over the same elements.  fn.vec2(active, lv[VEC], qv[VEC], x),
+// fn.scalar2(active, l, q, x).
+template <class E, class Fn>
+__device__ bool consume_row2(const Pipe& P, uint32_t& seq, const StreamPlan& p, bool tma, int x0, Fn& fn) {
+    constexpr int VEC = E::kVec;
+    bool dead = false;
+    for (int c = 0; c < p.nch; ++c, ++seq) {
+        const bool have = take_chunk(P, seq, tma, dead, p, c);
+        const unsigned char* sm = P.slot(static_cast<int>(seq % kStages));
+        const int ne = min(p.ce, p.n - c * p.ce);
+        const int cx0 = x0 + c * p.ce;
+        const int qoff = p.ce * E::kBytes;
+        if (have) {
+            const int nv = ne / VEC;
+            const int rounds = (nv + kThreads - 1) / kThreads;
+            for (int r = 0; r < rounds; ++r) {
+                const int v = r * kThreads + threadIdx.x;
+                const bool act = v < nv;
+                float lv[VEC], qv[VEC];
+                if (act) {
+                    E::unpack(reinterpret_cast<const uint4*>(sm)[v], lv);
+                    const float4* q4 = reinterpret_cast<const float4*>(sm + qoff) + v * (VEC / 4);
+#pragma unroll
+                    for (int j = 0; j < VEC / 4; ++j) {
+                        const float4 f = q4[j];
+                        qv[4 * j] = f.x; qv[4 * j + 1] = f.y; qv[4 * j + 2] = f.z; qv[4 * j + 3] = f.w;
+                    }
+                }
+                fn.vec2(act, lv, qv, cx0 + v * VEC);
+            }
+            const int t0 = nv * VEC;
+            if (t0 < ne) {
+                const int i = t0 + threadIdx.x;
+                const bool act = i < ne;
+                float l = 0.f, qq = 0.f;
+                if (act) {
+                    // bytes past the 16-byte-multiple prefix were not copied by TMA
+                    const bool l_in = tma ? ((i * E::kBytes + E::kBytes) <= ((ne * E::kBytes) & ~15)) : true;
+                    const bool q_in = tma ? ((i * 4 + 4) <= ((ne * 4) & ~15)) : true;
+                    l = l_in ? E::load(sm, i) : E::load(p.src0, static_cast<long long>(c) * p.ce + i);
+                    qq = q_in ? reinterpret_cast<const float*>(sm + qoff)[i]
+                              : reinterpret_cast<const float*>(p.src1)[static_cast<long long>(c) * p.ce + i];
+                }
+                fn.scalar2(act, l, qq, cx0 + i);
+            }
+        }
+        release_chunk(P, seq, tma, dead);
+    }
+    return !csync_or(dead);
 }
 
 // ---------------------------------------------------------------------------
@@ -475,15 +650,15 @@ __device__ int cta_icdf(int x0, int x1, double t, W& w, double* red, int* ired) 
                 if (found == 0x7fffffff && wv[j] > 0.f && c > t) found = xs + j;
             }
         }
-        __syncthreads();
+        csync();
         if (threadIdx.x == 0) { ired[0] = 0x7fffffff; ired[1] = -1; }
-        __syncthreads();
+        csync();
         if (found != 0x7fffffff) atomicMin(&ired[0], found);
         if (lp >= 0) atomicMax(&ired[1], lp);
-        __syncthreads();
+        csync();
         const int fb = ired[0];
         if (ired[1] > last_pos) last_pos = ired[1];
-        __syncthreads();
+        csync();
         if (fb != 0x7fffffff) return fb;
         base += tot;
     }
@@ -515,13 +690,13 @@ __device__ inline void load_hdrs(const Workspace& W, int b, int S, SliceHdrs& H)
         H.ly[s] = __ldcg(&h->ly);
         H.qy[s] = __ldcg(&h->qy);
     }
-    __syncthreads();
+    csync();
     if (threadIdx.x == 0) {
         int a = 0;
         for (int s = 0; s < S; ++s) { H.off[s] = a; a += H.cnt[s]; }
         H.off[S] = a;
     }
-    __syncthreads();
+    csync();
 }
 
 // Gather every slice key that `keep(key)` accepts into list[0..*lcnt)
@@ -530,7 +705,7 @@ template <class F>
 __device__ inline void gather_keys(const Workspace& W, int b, int S, const SliceHdrs& H, F keep,
                                    uint64_t* list, int cap, int* lcnt, int* oflow) {
     if (threadIdx.x == 0) { *lcnt = 0; *oflow = 0; }
-    __syncthreads();
+    csync();
     const int total = H.off[S];
     const int lane = threadIdx.x & 31;
     for (int f0 = 0; f0 < total; f0 += kThreads * 4) {
@@ -560,7 +735,7 @@ __device__ inline void gather_keys(const Workspace& W, int b, int S, const Slice
             }
         }
     }
-    __syncthreads();
+    csync();
 }
 
 }  // namespace spec

@@ -68,14 +68,14 @@ __device__ inline int select_to(const uint64_t* src, int n, int k, bool ties, in
                                 uint64_t* dst, int dst_cap, uint64_t& kth, bool& overflow,
                                 uint64_t* sh64, int* ired) {
     if (threadIdx.x == 0) sh64[0] = 0;
-    __syncthreads();
+    csync();
     for (int i = threadIdx.x; i < n; i += kThreads) {
         const uint64_t me = src[i];
         const int r = count_greater(src, n, me);
         rank[i] = r;
         if (r == k - 1) sh64[0] = me;
     }
-    __syncthreads();
+    csync();
     kth = sh64[0];
     int keep;
     if (n < k) {
@@ -92,7 +92,7 @@ __device__ inline int select_to(const uint64_t* src, int n, int k, bool ties, in
     if (overflow) keep = dst_cap;
     for (int i = threadIdx.x; i < n; i += kThreads)
         if (rank[i] < keep) dst[rank[i]] = src[i];
-    __syncthreads();
+    csync();
     return keep;
 }
 
@@ -113,9 +113,9 @@ __device__ uint32_t hist_bound(Each each, int k, uint32_t lo, int* hist, uint32_
     each([&](uint32_t h) { mk = max(mk, h); });
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mk = max(mk, __shfl_xor_sync(0xffffffffu, mk, o));
-    __syncthreads();
+    csync();
     if (lane == 0) scratch[w] = mk;
-    __syncthreads();
+    csync();
     uint32_t top = scratch[0];
 #pragma unroll
     for (int i = 1; i < kWarps; ++i) top = max(top, scratch[i]);
@@ -126,14 +126,14 @@ __device__ uint32_t hist_bound(Each each, int k, uint32_t lo, int* hist, uint32_
     certified = false;
     for (int round = 0; round < 6; ++round) {
         for (int i = threadIdx.x; i < 64; i += kThreads) hist[i] = 0;
-        __syncthreads();
+        csync();
         each([&](uint32_t h) {
             if (h >= lo) {
                 const uint32_t bb = (h - lo) >> sh;
                 atomicAdd(&hist[bb < 64 ? bb : 63], 1);
             }
         });
-        __syncthreads();
+        csync();
         if (w == 0) {
             const int h0 = hist[2 * lane], h1 = hist[2 * lane + 1];
             int suf = h0 + h1;
@@ -151,9 +151,9 @@ __device__ uint32_t hist_bound(Each each, int k, uint32_t lo, int* hist, uint32_
             const int bb = __shfl_sync(0xffffffffu, best, bl >= 0 ? bl : 0);
             if (lane == 0) scratch[kWarps] = static_cast<uint32_t>(bl >= 0 ? bb : -1);
         }
-        __syncthreads();
+        csync();
         const int bb = static_cast<int>(scratch[kWarps]);
-        __syncthreads();
+        csync();
         if (bb < 0) break;                 // fewer than k keys reach lo
         certified = true;
         if (bb > 0) {
@@ -203,7 +203,7 @@ __device__ inline int compact_list(uint64_t* list, int n, uint32_t t, int* ired)
         if (i < n) { key = list[i]; p = hkey(key) >= t; }
         const uint32_t bal = __ballot_sync(0xffffffffu, p);
         if (lane == 0) ired[w] = __popc(bal);
-        __syncthreads();
+        csync();
         int base = out;
         int tot = 0;
 #pragma unroll
@@ -212,10 +212,10 @@ __device__ inline int compact_list(uint64_t* list, int n, uint32_t t, int* ired)
             if (j < w) base += c;
             tot += c;
         }
-        __syncthreads();   // every thread read its block before anyone writes
+        csync();   // every thread read its block before anyone writes
         if (p) list[base + __popc(bal & ((1u << lane) - 1u))] = key;
         out += tot;
-        __syncthreads();
+        csync();
     }
     return out;
 }
@@ -321,13 +321,14 @@ struct SumExpFn : FnHooks {
 };
 
 // Shared state of TopkHistFn: one candidate region per warp, so a warp
-// appends with ballots and a register counter and never contends with the
-// other warps.
+// appends with ballots and a register counter and never waits for the other
+// warps.
 struct TopkSmem {
     static constexpr int kRegion = 256;                 // keys per warp
+    static constexpr int kSlots = 4;                    // per-thread keys within a chunk
     alignas(16) uint64_t cand[kWarps * kRegion];
+    uint64_t slot[kSlots][kThreads];
     uint64_t pool[kThreads];
-    int wcnt[2][kWarps];
     uint64_t wthr[kWarps];
     int hist[64];
     uint32_t scratch[kWarps + 2];
@@ -346,33 +347,42 @@ struct TopkSmem {
 // keys reach the filter) and retries the row without a hint otherwise.
 // Without a hint, the first chunk's per-thread maxima give the first
 // certified bound (they are distinct elements, so the k-th largest of them
-// is at most the row's k-th largest).  Whenever a warp region fills past a
-// quarter, the CTA raises the filter to a certified histogram bound over all
-// candidates (kTies = false: an exact composite bound when the values tie)
-// and compacts the regions.  A region that overflows anyway (massive ties
-// with kTies, adversarial order) is reported; the combine then takes its
-// exact fallback.
+// is at most the row's k-th largest).
+//
+// Candidates are rare, so the hot loop keeps them per thread: a vector
+// whose max reaches the filter stores its passing elements in the thread's
+// own kSlots slots (no warp synchronisation); a vector that does not fit is
+// flagged and re-read at chunk_end(), which also moves the warp's slots into
+// the warp's region with one ballot per slot.  A warp whose region fills past half
+// raises its own filter to the exact k-th largest of its own candidates
+// (again certified) and compacts its region; warps keep their own filters
+// and the slice's filter is their maximum.  A region that overflows anyway
+// (massive ties with kTies, adversarial order, k above half a region) is
+// reported; the combine then takes its exact fallback.
 template <class E, bool kTies>
 struct TopkHistFn : FnHooks {
     static constexpr bool kPrepass = true;
     static constexpr int VEC = E::kVec;
     static constexpr int kRegion = TopkSmem::kRegion;
-    static constexpr int kRefineAt = kRegion / 4;
+    static constexpr int kRefineAt = kRegion / 2;
     TopkSmem* S;
     int k;
-    uint64_t theta;     // composite filter, CTA-uniform
+    uint64_t theta;     // composite filter, warp-uniform (CTA-uniform until a warp refines)
     float thr_f;        // float prefilter: v >= thr_f  <=>  value key >= hkey(theta)
     float vmx;          // running max with NaN propagation (every element)
     int nw;             // candidates appended by this warp (warp-uniform; may exceed kRegion)
     uint32_t lost;      // this warp's region overflowed
     uint32_t tmax;      // prepass: this thread's max value key
+    uint32_t cmask;     // rounds of the current chunk deferred to chunk_end()
+    int rr;             // rounds seen in the current chunk
+    int tcnt;           // keys in this thread's slots
     DraftWatch dw;
 
     __device__ __forceinline__ void set_theta(uint64_t t) { theta = t; thr_f = key_to_thr(hkey(t)); }
     __device__ __forceinline__ void init(TopkSmem* s, int kk, uint32_t hint) {
         S = s; k = kk;
         set_theta(static_cast<uint64_t>(hint) << 32);
-        vmx = -kInf; nw = 0; lost = 0; tmax = 0;
+        vmx = -kInf; nw = 0; lost = 0; tmax = 0; cmask = 0; rr = 0; tcnt = 0;
     }
     __device__ __forceinline__ void chunk_begin(int c) { dw.begin(c); }
     __device__ __forceinline__ bool use_prepass() const { return theta == 0; }
@@ -384,7 +394,7 @@ struct TopkHistFn : FnHooks {
     __device__ __forceinline__ void pre_scalar(bool act, float v, int) {
         if (act && v == v) tmax = max(tmax, fkey(v));
     }
-    // k-th largest of the warps' top-8 (k <= 64) or top-32 thread maxima
+    // k-th largest of the warps' top-8 (k <= 64) or top-32 thread maxima (all consumers)
     __device__ void pre_end() {
         const int per = (k <= 8 * kWarps) ? 8 : 32;
         const int P = per * kWarps;
@@ -392,8 +402,8 @@ struct TopkHistFn : FnHooks {
         const uint64_t srt = warp_sort_desc(static_cast<uint64_t>(tmax));
         if (lane < per) S->pool[w * per + lane] = srt;
         if (threadIdx.x == 0) S->sh64[1] = 0;
-        __syncthreads();
-        if (k <= P && threadIdx.x < P) {
+        csync();
+        if (k <= P && static_cast<int>(threadIdx.x) < P) {
             const uint64_t me = S->pool[threadIdx.x];
             int r = 0, eq = 0;
             for (int t = 0; t < P; ++t) {
@@ -404,52 +414,60 @@ struct TopkHistFn : FnHooks {
             // the k-th largest value (ties resolved by position)
             if (r + eq == k - 1) S->sh64[1] = me;
         }
-        __syncthreads();
+        csync();
         const uint64_t b = S->sh64[1] << 32;
         if (b > theta) set_theta(b);
-        __syncthreads();
+        csync();
     }
+    // Append the lanes' candidates (bit j of m: element x + j) to the warp's
+    // region: one ballot per element slot, so the positions need no scan.
     __device__ __forceinline__ void append(uint32_t m, const float* v, int x) {
-        const int lane = threadIdx.x & 31;
-        const int c = __popc(m);
-        int incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        const uint32_t lt = (1u << (threadIdx.x & 31)) - 1u;
         uint64_t* reg = S->cand + (threadIdx.x >> 5) * kRegion;
-        int pos = nw + incl - c;
+        int base = nw;
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
-            if ((m >> j) & 1u) {
+            const bool p = (m >> j) & 1u;
+            const uint32_t bj = __ballot_sync(0xffffffffu, p);
+            if (p) {
+                const int pos = base + __popc(bj & lt);
                 if (pos < kRegion) reg[pos] = ckey(v[j], x + j);
-                ++pos;
             }
+            base += __popc(bj);
         }
-        nw += total;
+        nw = base;
     }
     __device__ __forceinline__ bool passes(float v, int x) const {
         return v >= thr_f && (kTies || ckey(v, x) >= theta);
     }
+    // Hot loop: the vector max decides whether any element reaches the
+    // filter (NaN lands there too; it is never stored).  Passing elements go
+    // to the thread's slots, or the round is deferred to chunk_end().
     __device__ __forceinline__ void vec(bool act, const float (&v)[VEC], int x) {
-        bool any = false;
         if (act) {
             dw.see(v, x);
             const float m4 = vmax_nan(v);
             vmx = max_nan(vmx, m4);
-            any = !(m4 < thr_f);            // NaN lands here too; it is not appended
-        }
-        if (__any_sync(0xffffffffu, any)) {
-            uint32_t m = 0;
-            if (any) {
+            if (!(m4 < thr_f)) {
+                uint32_t m = 0;
 #pragma unroll
                 for (int j = 0; j < VEC; ++j)
                     if (passes(v[j], x + j)) m |= 1u << j;
+                const int c = __popc(m);
+                if (tcnt + c <= TopkSmem::kSlots) {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) {
+                        if ((m >> j) & 1u) {
+                            S->slot[tcnt][threadIdx.x] = ckey(v[j], x + j);
+                            ++tcnt;
+                        }
+                    }
+                } else {
+                    cmask |= 1u << rr;
+                }
             }
-            append(m, v, x);
         }
+        ++rr;
     }
     __device__ __forceinline__ void scalar(bool act, float v, int x) {
         bool any = false;
@@ -464,34 +482,85 @@ struct TopkHistFn : FnHooks {
             append(any ? 1u : 0u, vv, x);
         }
     }
-    __device__ __forceinline__ void chunk_end(int c) {
-        if ((threadIdx.x & 31) == 0) S->wcnt[c & 1][threadIdx.x >> 5] = nw;
-    }
-    __device__ __forceinline__ void after_release(int c) {
-        bool need = false;
+    __device__ __forceinline__ void chunk_end(int, const unsigned char* sm, int cx0, int nv) {
+        if (__any_sync(0xffffffffu, tcnt != 0)) {
+            // the warp's slots into its region, one ballot per slot
+            const uint32_t lt = (1u << (threadIdx.x & 31)) - 1u;
+            uint64_t* reg = S->cand + (threadIdx.x >> 5) * kRegion;
+            int base = nw;
 #pragma unroll
-        for (int j = 0; j < kWarps; ++j) need |= S->wcnt[c & 1][j] > kRefineAt;
-        if (need) refine();
+            for (int i = 0; i < TopkSmem::kSlots; ++i) {
+                const bool p = i < tcnt;
+                const uint32_t bal = __ballot_sync(0xffffffffu, p);
+                if (p) {
+                    const int pos = base + __popc(bal & lt);
+                    if (pos < kRegion) reg[pos] = S->slot[i][threadIdx.x];
+                }
+                base += __popc(bal);
+            }
+            nw = base;
+            tcnt = 0;
+        }
+        if (__any_sync(0xffffffffu, cmask != 0)) {
+            for (int r = 0; r < rr; ++r) {
+                const bool mine = (cmask >> r) & 1u;
+                if (!__any_sync(0xffffffffu, mine)) continue;
+                const int vi = r * kThreads + static_cast<int>(threadIdx.x);
+                float vals[VEC] = {};
+                uint32_t m = 0;
+                if (mine && vi < nv) {
+                    E::unpack(reinterpret_cast<const uint4*>(sm)[vi], vals);
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        if (passes(vals[j], cx0 + vi * VEC + j)) m |= 1u << j;
+                }
+                append(m, vals, cx0 + vi * VEC);
+            }
+        }
+        cmask = 0;
+        rr = 0;
     }
-    // raise theta to a certified bound over every candidate, compact the regions
-    __device__ void refine() {
+    // per warp: past half a region, refine this warp's filter
+    __device__ __forceinline__ void after_release(int) {
+        if (nw > kRefineAt) refine_warp();
+    }
+    // The exact k-th largest key of this warp's candidates by bisection
+    // (value key; then the index bits without kTies), and compaction.
+    __device__ void refine_warp() {
         const int lane = threadIdx.x & 31;
         uint64_t* reg = S->cand + (threadIdx.x >> 5) * kRegion;
         const int n = nw < kRegion ? nw : kRegion;
         lost |= nw > kRegion;
-        auto each = [&](auto f) { for (int j = lane; j < n; j += 32) f(reg[j]); };
-        bool cert;
-        const uint32_t lo = hkey(theta);
-        const uint32_t b = hist_bound([&](auto f) { each([&](uint64_t key) { f(hkey(key)); }); },
-                                      k, lo, S->hist, S->scratch, cert);
-        if (!cert) return;
-        uint64_t nt = static_cast<uint64_t>(b) << 32;
-        if (!kTies && b == lo) {
-            // the k-th value is lo itself: the exact composite bound among the keys of value lo
-            nt = composite_bound(each, k, theta, S->ired);
+        if (n < k) return;                  // not certifiable from this warp alone
+        auto count_ge = [&](uint64_t t, bool value_only) {
+            int c = 0;
+            for (int j0 = 0; j0 < n; j0 += 32) {
+                const int j = j0 + lane;
+                bool p = false;
+                if (j < n) p = value_only ? (hkey(reg[j]) >= static_cast<uint32_t>(t)) : (reg[j] >= t);
+                c += __popc(__ballot_sync(0xffffffffu, p));
+            }
+            return c;
+        };
+        // every stored key reaches theta, so count(value >= hkey(theta)) = n >= k
+        uint32_t lo = hkey(theta), hi = 0xffffffffu;
+        while (lo < hi) {
+            const uint32_t mid = lo + static_cast<uint32_t>((static_cast<uint64_t>(hi) - lo + 1) >> 1);
+            if (count_ge(mid, true) >= k) lo = mid; else hi = mid - 1;
+        }
+        uint64_t nt = static_cast<uint64_t>(lo) << 32;
+        if (!kTies) {
+            uint64_t clo = nt > theta ? nt : theta, chi = nt | 0xffffffffull;
+            while (clo < chi) {
+                const uint64_t d = chi - clo;
+                const uint64_t mid = clo + (d >> 1) + (d & 1ull);
+                if (count_ge(mid, false) >= k) clo = mid; else chi = mid - 1;
+            }
+            nt = clo;
         }
         if (nt <= theta) return;
         set_theta(nt);
+        const uint32_t lt = (1u << lane) - 1u;
         int out = 0;
         for (int j0 = 0; j0 < n; j0 += 32) {
             const int j = j0 + lane;
@@ -499,58 +568,63 @@ struct TopkHistFn : FnHooks {
             bool p = false;
             if (j < n) { key = reg[j]; p = key >= nt; }
             const uint32_t bal = __ballot_sync(0xffffffffu, p);
-            if (p) reg[out + __popc(bal & ((1u << lane) - 1u))] = key;
+            if (p) reg[out + __popc(bal & lt)] = key;
             out += __popc(bal);
         }
         nw = out;
         __syncwarp();
     }
-    // After stream_row: the candidates with key >= the final filter F,
-    // contiguous in list[0..return) (shared, 16-byte aligned, room for
-    // kWarps * kRegion keys).  `oflow` when a region lost keys, `bad` when
-    // the slice holds a NaN or +inf.
-    __device__ int finish(uint64_t* list, uint64_t& F, uint32_t& oflow, uint32_t& bad) {
+    // After the stream (all consumers): the candidates with key >= F (the
+    // largest warp filter), compacted to S->cand[0..return).  `oflow` when a
+    // region lost keys, `bad` when the slice holds a NaN or +inf.
+    __device__ int finish(uint64_t& F, uint32_t& oflow, uint32_t& bad) {
+        constexpr int kPer = kRegion / 32;
         const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-        if (lane == 0) S->wthr[w] = theta;
+        const uint32_t lt = (1u << lane) - 1u;
         lost |= nw > kRegion;
-        __syncthreads();
+        const uint32_t fl = (lost ? 1u : 0u) | (bad_max(vmx) ? 2u : 0u);
+        const uint32_t flw = __reduce_or_sync(0xffffffffu, fl);
+        if (lane == 0) { S->wthr[w] = theta; S->scratch[w] = flw; }
+        csync();
         F = S->wthr[0];
+        uint32_t fa = S->scratch[0];
 #pragma unroll
-        for (int j = 1; j < kWarps; ++j) F = S->wthr[j] > F ? S->wthr[j] : F;
+        for (int j = 1; j < kWarps; ++j) {
+            F = S->wthr[j] > F ? S->wthr[j] : F;
+            fa |= S->scratch[j];
+        }
+        oflow = fa & 1u;
+        bad = (fa >> 1) & 1u;
         const uint64_t* reg = S->cand + w * kRegion;
         const int n = nw < kRegion ? nw : kRegion;
+        uint64_t key[kPer];
+        uint32_t pm = 0;
         int cnt = 0;
-        for (int j0 = 0; j0 < n; j0 += 32) {
-            const int j = j0 + lane;
-            cnt += __popc(__ballot_sync(0xffffffffu, j < n && reg[j] >= F));
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int j = i * 32 + lane;
+            key[i] = j < n ? reg[j] : 0ull;
+            const bool p = j < n && key[i] >= F;
+            pm |= static_cast<uint32_t>(p) << i;
+            cnt += __popc(__ballot_sync(0xffffffffu, p));
         }
-        const uint32_t lw = __ballot_sync(0xffffffffu, lost) != 0;
-        const uint32_t bw = __ballot_sync(0xffffffffu, bad_max(vmx)) != 0;
-        if (lane == 0) {
-            S->ired[w] = cnt;
-            S->scratch[w] = lw | (bw << 1);
-        }
-        __syncthreads();
+        if (lane == 0) S->ired[w] = cnt;
+        csync();   // every warp holds its keys in registers: the regions may be overwritten
         int base = 0, tot = 0;
-        uint32_t fl = 0;
 #pragma unroll
         for (int j = 0; j < kWarps; ++j) {
-            if (j < w) base += S->ired[j];
-            tot += S->ired[j];
-            fl |= S->scratch[j];
+            const int c = S->ired[j];
+            if (j < w) base += c;
+            tot += c;
         }
-        oflow = fl & 1u;
-        bad = (fl >> 1) & 1u;
-        for (int j0 = 0; j0 < n; j0 += 32) {
-            const int j = j0 + lane;
-            uint64_t key = 0;
-            bool p = false;
-            if (j < n) { key = reg[j]; p = key >= F; }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const bool p = (pm >> i) & 1u;
             const uint32_t bal = __ballot_sync(0xffffffffu, p);
-            if (p) list[base + __popc(bal & ((1u << lane) - 1u))] = key;
+            if (p) S->cand[base + __popc(bal & lt)] = key[i];
             base += __popc(bal);
         }
-        __syncthreads();
+        csync();
         return tot;
     }
 };
@@ -584,9 +658,9 @@ __device__ __forceinline__ float block_max_nan(float v, float* red) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
+    csync();
     if (l == 0) red[w] = v;
-    __syncthreads();
+    csync();
     float r = red[0];
 #pragma unroll
     for (int i = 1; i < kWarps; ++i) r = max_nan(r, red[i]);

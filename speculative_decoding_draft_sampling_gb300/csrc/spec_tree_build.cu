@@ -40,8 +40,7 @@ struct EnumHdr {
 
 struct __align__(16) BuildSmem {
     TopkSmem tk;             // slice candidates; later the merged list and mask scratch
-    uint64_t bars[kStages];
-    Claimed claimed;
+    PipeSmem pipe;
     int last;
     int lcnt;
     int oflow;
@@ -65,8 +64,18 @@ __host__ __device__ inline size_t build_pend_off(int N, int L) {
 size_t build_extra_bytes(int N, int L) {
     return (build_pend_off(N, L) + static_cast<size_t>(2 * N + 2) * sizeof(Ent) + 127) & ~static_cast<size_t>(127);
 }
-// dynamic shared memory beyond the ring and BuildSmem: nodes + pending
-static size_t build_enum_smem(int N) { return static_cast<size_t>(3 * N + 2) * sizeof(Ent); }
+// dynamic shared memory beyond the ring and BuildSmem: scratch (depth lists,
+// gathered keys and their ranks) + nodes + pending
+constexpr int kBuildList = 2048;         // gathered keys in a combine
+__host__ __device__ inline size_t build_lists_bytes(int N, int L) {
+    return (static_cast<size_t>(L) * (N - 1) * 8 + 15) & ~static_cast<size_t>(15);
+}
+__host__ __device__ inline size_t build_scr_bytes(int N, int L) {
+    return build_lists_bytes(N, L) + static_cast<size_t>(kBuildList) * 12;
+}
+static size_t build_enum_smem(int N, int L) {
+    return build_scr_bytes(N, L) + static_cast<size_t>(3 * N + 2) * sizeof(Ent);
+}
 
 __device__ __forceinline__ bool ent_before(const Ent& a, const Ent& b) {
     if (a.Q != b.Q) return a.Q > b.Q;
@@ -103,7 +112,7 @@ __device__ int build_fallback(const float* qrow, int V, int M, uint64_t* list, i
         }
     }
     if (threadIdx.x == 0) *lcnt = 0;
-    __syncthreads();
+    csync();
     for (int x = threadIdx.x; x < V; x += kThreads) {
         const uint64_t key = ckey(qrow[x], x);
         if (key >= lo) {
@@ -111,9 +120,9 @@ __device__ int build_fallback(const float* qrow, int V, int M, uint64_t* list, i
             if (pos < M) list[pos] = key;
         }
     }
-    __syncthreads();
+    csync();
     const int n = *lcnt;
-    __syncthreads();
+    csync();
     return n < M ? n : M;
 }
 
@@ -150,48 +159,63 @@ __device__ void build_finalize(const BuildArgs& A, BuildSmem& sh, const Ent* nod
             }
         }
     }
-    __syncthreads();
+    csync();
     for (int i = threadIdx.x; i < N * W; i += kThreads) mk[i] = sm[i];
     if (threadIdx.x == 0) {
         A.num_nodes[b] = count;
         A.status[b] = st;
     }
-    __syncthreads();
+    csync();
     if (threadIdx.x == 0) finish_request(A.W);
 }
 
-__global__ void __launch_bounds__(kThreads) build_kernel(const BuildArgs A) {
+__global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     auto& sh = *reinterpret_cast<BuildSmem*>(smem + kStages * kChunkBytes);
-    Ent* nodes = reinterpret_cast<Ent*>(smem + kStages * kChunkBytes + sizeof(BuildSmem));
+    unsigned char* scr = smem + kStages * kChunkBytes + sizeof(BuildSmem);
+    Ent* nodes = reinterpret_cast<Ent*>(scr + build_scr_bytes(A.N, A.L));
     Ent* pend = nodes + A.N;
-    Ring R;
-    R.init(smem, sh.bars);
+    const Pipe P = pipe_init(smem, sh.pipe);
     const int N = A.N, M = A.M, L = A.L;
-    for (;;) {
-        Task t;
-        int s;
-        if (!claim(A.W, A.B, A.S, t, s, &sh.claimed)) break;
+    const bool tma = A.tma_q != 0;
+    auto trivial_of = [&](const Task& t) { return t.kind < 0 && (N <= 1 || L <= 0); };
+    auto plan = [&](const Task& t, int slice) {
+        if (trivial_of(t)) return plan_none();
+        const int x0 = slice * A.SL, x1 = min(A.V, x0 + A.SL);
+        const float* qrow = A.q + static_cast<long long>(t.b) * A.q_bs + static_cast<long long>(t.row) * A.q_rs;
+        return plan_single(qrow, 4, x0, x1);
+    };
+    if (threadIdx.x >= kThreads) {
+        if (threadIdx.x == kThreads)
+            producer_loop(A.W, A.B, A.S, P, tma, [](Claimed&) {},
+                          [&](const Claimed& c) { return plan(c.task, c.slice); });
+        return;
+    }
+    uint32_t seq = 0;
+    for (uint32_t u = 0;; ++u) {
+        const Claimed cl = next_unit(P, u);
+        if (!cl.ok) break;
+        const Task t = cl.task;
+        const int s = cl.slice;
         const int b = t.b;
         const bool initial = t.kind < 0;
         const int d = t.row + 1;                 // depth of this row
-        const bool trivial = initial && (N <= 1 || L <= 0);
+        const bool trivial = trivial_of(t);
         PartHdr* ph = part_hdr(A.W, b, s, A.S);
         uint64_t* pk = part_keys(A.W, b, s, A.S);
         if (!trivial) {
-            const int x0 = s * A.SL, x1 = min(A.V, x0 + A.SL);
+            const int x0 = s * A.SL;
             TopkHistFn<F32, false> fn;
             fn.init(&sh.tk, M, 0u);
-            const float* qrow = A.q + static_cast<long long>(b) * A.q_bs + static_cast<long long>(d - 1) * A.q_rs;
-            stream_row<F32>(R, qrow, A.tma_q != 0, x0, x1, fn);
-            uint64_t* list = reinterpret_cast<uint64_t*>(R.buf);
+            if (!consume_row<F32>(P, seq, plan(t, s), tma, x0, fn)) break;
             uint64_t F;
             uint32_t oflow, bad;
-            int n = fn.finish(list, F, oflow, bad);
+            int n = fn.finish(F, oflow, bad);
+            uint64_t* list = sh.tk.cand;
             if (n > A.cap_p && !bad) {
                 // the slice's exact top-M (value desc, index asc); its M-th key is the filter
-                uint64_t* dst = list + kWarps * TopkSmem::kRegion;
-                int* rank = reinterpret_cast<int*>(dst + kWarps * TopkSmem::kRegion);
+                uint64_t* dst = reinterpret_cast<uint64_t*>(scr);
+                int* rank = reinterpret_cast<int*>(scr + static_cast<size_t>(A.cap_p) * 8);
                 uint64_t kth;
                 bool of2;
                 n = select_to(list, n, M, false, rank, dst, A.cap_p, kth, of2, sh.sh64, sh.ired);
@@ -199,7 +223,7 @@ __global__ void __launch_bounds__(kThreads) build_kernel(const BuildArgs A) {
                 list = dst;
             }
             if (bad) n = 0;
-            __syncthreads();
+            csync();
             for (int i = threadIdx.x; i < n; i += kThreads) __stcg(pk + i, list[i]);
             if (threadIdx.x == 0) {
                 ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u);
@@ -217,8 +241,8 @@ __global__ void __launch_bounds__(kThreads) build_kernel(const BuildArgs A) {
         Ent* gpend = reinterpret_cast<Ent*>(ex + build_pend_off(N, L));
         // depth lists at the front of the ring: tokens [L*M] then probabilities [L*M]
         const int LM = L * M;
-        int* ltok = reinterpret_cast<int*>(R.buf);
-        float* lprob = reinterpret_cast<float*>(R.buf + static_cast<size_t>(LM) * 4);
+        int* ltok = reinterpret_cast<int*>(scr);
+        float* lprob = reinterpret_cast<float*>(scr + static_cast<size_t>(LM) * 4);
         if (initial) {
             if (threadIdx.x == 0) {
                 EnumHdr h{};
@@ -229,7 +253,7 @@ __global__ void __launch_bounds__(kThreads) build_kernel(const BuildArgs A) {
             for (int i = threadIdx.x; i < static_cast<int>(sizeof(EnumHdr) / 4); i += kThreads)
                 reinterpret_cast<int*>(&sh.eh)[i] = __ldcg(reinterpret_cast<const int*>(gh) + i);
         }
-        __syncthreads();
+        csync();
         EnumHdr& eh = sh.eh;
         if (initial) {
             if (threadIdx.x == 0) {
@@ -248,7 +272,7 @@ __global__ void __launch_bounds__(kThreads) build_kernel(const BuildArgs A) {
                 lprob[i] = __int_as_float(__ldcg(gl + 2 * i + 1));
             }
         }
-        __syncthreads();
+        csync();
         if (!trivial) {
             load_hdrs(A.W, b, A.S, sh.hdrs);
             uint32_t flags = 0;
@@ -258,9 +282,8 @@ __global__ void __launch_bounds__(kThreads) build_kernel(const BuildArgs A) {
                 theta = sh.hdrs.kth[j] > theta ? sh.hdrs.kth[j] : theta;
             }
             // gathered keys and their ranks in the rest of the ring
-            const size_t used = (static_cast<size_t>(LM) * 8 + 15) & ~static_cast<size_t>(15);
-            uint64_t* list = reinterpret_cast<uint64_t*>(R.buf + used);
-            const int kList = static_cast<int>((kStages * kChunkBytes - used) / 12);
+            uint64_t* list = reinterpret_cast<uint64_t*>(scr + build_lists_bytes(N, L));
+            const int kList = kBuildList;
             int* rank = reinterpret_cast<int*>(list + kList);
             int n = 0;
             if (flags & kPfBad) {
@@ -278,7 +301,7 @@ __global__ void __launch_bounds__(kThreads) build_kernel(const BuildArgs A) {
             bool of;
             const int keep = (flags & kPfBad) ? 0
                              : select_to(list, n, M, false, rank, sh.tk.cand, kBuildCap, kth, of, sh.sh64, sh.ired);
-            __syncthreads();
+            csync();
             for (int i = threadIdx.x; i < keep; i += kThreads) {
                 const uint64_t key = sh.tk.cand[i];
                 ltok[(d - 1) * M + i] = ckey_idx(key);
@@ -291,7 +314,7 @@ __global__ void __launch_bounds__(kThreads) build_kernel(const BuildArgs A) {
                 eh.avail = d;
                 if (flags & kPfBad) eh.status |= 1;
             }
-            __syncthreads();
+            csync();
         }
         // ---- best-first enumeration (thread 0), resumable ----
         if (threadIdx.x == 0) {
@@ -332,7 +355,7 @@ __global__ void __launch_bounds__(kThreads) build_kernel(const BuildArgs A) {
             eh.count = count; eh.npend = np; eh.want = want;
             sh.ired[0] = need;
         }
-        __syncthreads();
+        csync();
         const int need = sh.ired[0];
         if (need == 0) {
             build_finalize(A, sh, nodes, ltok, b, eh.count, eh.status);
@@ -345,44 +368,41 @@ __global__ void __launch_bounds__(kThreads) build_kernel(const BuildArgs A) {
                 __stcg(reinterpret_cast<unsigned long long*>(gpend) + i, reinterpret_cast<const unsigned long long*>(pend)[i]);
             for (int i = threadIdx.x; i < static_cast<int>(sizeof(EnumHdr) / 4); i += kThreads)
                 __stcg(reinterpret_cast<int*>(gh) + i, reinterpret_cast<const int*>(&eh)[i]);
-            __syncthreads();
+            csync();
             if (threadIdx.x == 0) {
                 Task nt;
                 nt.b = b; nt.row = need - 1; nt.kind = 0; nt.aux = 0;
                 push_task(A.W, nt);
             }
         }
-        __syncthreads();
+        csync();
     }
-    if (R.err) atomicOr(&A.W.ctrl->error, kErrWait);
 }
 
 // largest slice count whose candidate lists fit the combine's gather buffer
 int build_max_slices(int N, int L) {
+    (void)L;
     const int M = N - 1;
-    const size_t used = (static_cast<size_t>(L) * M * 8 + 15) & ~static_cast<size_t>(15);
-    const int kList = static_cast<int>((kStages * kChunkBytes - used) / 12);
-    const int s = M > 0 ? kList / M : kMaxSlices;
+    const int s = M > 0 ? kBuildList / M : kMaxSlices;
     return s < 1 ? 1 : (s > kMaxSlices ? kMaxSlices : s);
 }
 
-static size_t build_smem(int N) { return kStages * kChunkBytes + sizeof(BuildSmem) + build_enum_smem(N); }
+static size_t build_smem(int N, int L) { return kStages * kChunkBytes + sizeof(BuildSmem) + build_enum_smem(N, L); }
 
 int build_occupancy(int N, int L) {
-    (void)L;
-    const int smem = static_cast<int>(build_smem(N));
+    const int smem = static_cast<int>(build_smem(N, L));
     int n = 0;
     cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, build_kernel, kThreads, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, build_kernel, kBlockThreads, smem);
     return n;
 }
 
 cudaError_t build_run(const BuildArgs& A, int grid, cudaStream_t st) {
-    const size_t smem = build_smem(A.N);
+    const size_t smem = build_smem(A.N, A.L);
     cudaError_t e = cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    build_kernel<<<grid, kThreads, smem, st>>>(A);
+    build_kernel<<<grid, kBlockThreads, smem, st>>>(A);
     return cudaGetLastError();
 }
 

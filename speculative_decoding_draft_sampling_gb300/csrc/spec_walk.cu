@@ -18,8 +18,7 @@
 namespace spec {
 
 struct __align__(16) WalkSmem {
-    uint64_t bars[kStages];
-    Claimed claimed;
+    PipeSmem pipe;
     int last;
     uint64_t red[kWarps];
     int ish[4];
@@ -46,7 +45,7 @@ __device__ void greedy_finish(const WalkArgs& A, int b, int n, int last, int st)
         A.num_accepted[b] = n;
         A.status[b] = st;
     }
-    __syncthreads();
+    csync();
     if (threadIdx.x == 0) finish_request(A.W);
 }
 
@@ -64,34 +63,50 @@ __device__ void tree_finish(const WalkArgs& A, int b, int acc, int last, int st)
         A.num_accepted[b] = acc;
         A.status[b] = st;
     }
-    __syncthreads();
+    csync();
     if (threadIdx.x == 0) finish_request(A.W);
 }
 
 template <class E, bool kTree>
-__global__ void __launch_bounds__(kThreads) walk_kernel(const WalkArgs A) {
+__device__ __forceinline__ bool walk_invalid(const WalkArgs& A, const Task& t) {
+    if (kTree || t.kind >= 0) return false;
+    const int kb = A.k_per_req ? A.k_per_req[t.b] : A.K;
+    return kb < 0 || kb > A.K;
+}
+
+template <class E, bool kTree>
+__global__ void __launch_bounds__(kBlockThreads, 2) walk_kernel(const WalkArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     auto& sh = *reinterpret_cast<WalkSmem*>(smem + kStages * kChunkBytes);
-    Ring R;
-    R.init(smem, sh.bars);
-    for (;;) {
-        Task t;
-        int s;
-        if (!claim(A.W, A.B, A.S, t, s, &sh.claimed)) break;
+    const Pipe P = pipe_init(smem, sh.pipe);
+    const bool tma = A.tma_l != 0;
+    auto plan = [&](const Task& t, int slice) {
+        if (walk_invalid<E, kTree>(A, t)) return plan_none();
+        const int x0 = slice * A.SL, x1 = min(A.V, x0 + A.SL);
+        return plan_single(walk_row<E>(A, t.b, t.row, kTree), E::kBytes, x0, x1);
+    };
+    if (threadIdx.x >= kThreads) {
+        if (threadIdx.x == kThreads)
+            producer_loop(A.W, A.B, A.S, P, tma, [](Claimed&) {},
+                          [&](const Claimed& c) { return plan(c.task, c.slice); });
+        return;
+    }
+    uint32_t seq = 0;
+    for (uint32_t u = 0;; ++u) {
+        const Claimed cl = next_unit(P, u);
+        if (!cl.ok) break;
+        const Task t = cl.task;
+        const int s = cl.slice;
         const int b = t.b;
         const bool initial = t.kind < 0;
         const int row = t.row;              // greedy: position; tree: node id
         const int acc = initial ? 0 : t.aux;
-        bool invalid = false;
-        if (!kTree && initial) {
-            const int kb = A.k_per_req ? A.k_per_req[b] : A.K;
-            invalid = kb < 0 || kb > A.K;
-        }
+        const bool invalid = walk_invalid<E, kTree>(A, t);
         PartHdr* ph = part_hdr(A.W, b, s, A.S);
         if (!invalid) {
-            const int x0 = s * A.SL, x1 = min(A.V, x0 + A.SL);
+            const int x0 = s * A.SL;
             ArgmaxFn<E> fn;
-            stream_row<E>(R, walk_row<E>(A, b, row, kTree), A.tma_l != 0, x0, x1, fn);
+            if (!consume_row<E>(P, seq, plan(t, s), tma, x0, fn)) break;
             const uint64_t best = block_max_u64(fn.key(), sh.red);
             const uint32_t bad = block_or(fn.bad_flag(), reinterpret_cast<uint32_t*>(sh.red));
             if (threadIdx.x == 0) {
@@ -153,9 +168,8 @@ __global__ void __launch_bounds__(kThreads) walk_kernel(const WalkArgs A) {
                 push_task(A.W, nt);
             }
         }
-        __syncthreads();
+        csync();
     }
-    if (R.err) atomicOr(&A.W.ctrl->error, kErrWait);
 }
 
 static size_t walk_smem() { return kStages * kChunkBytes + sizeof(WalkSmem); }
@@ -166,7 +180,7 @@ static cudaError_t walk_launch(const WalkArgs& A, int grid, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(walk_kernel<E, kTree>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    walk_kernel<E, kTree><<<grid, kThreads, smem, st>>>(A);
+    walk_kernel<E, kTree><<<grid, kBlockThreads, smem, st>>>(A);
     return cudaGetLastError();
 }
 
@@ -175,7 +189,7 @@ static int walk_occ() {
     const int smem = static_cast<int>(walk_smem());
     int n = 0;
     cudaFuncSetAttribute(walk_kernel<E, kTree>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, walk_kernel<E, kTree>, kThreads, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, walk_kernel<E, kTree>, kBlockThreads, smem);
     return n;
 }
 
