@@ -96,7 +96,8 @@ spec::Workspace make_ws(void* ws, const Layout& L) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Slices per row: enough units to give every CTA several at the start, each
-// slice at least 16 KiB of row, at most `max_s`.
+// slice at least 32 KiB of row (a unit's fixed costs stay small next to its
+// stream), at most `max_s`.
 void choose_slices(int B, int V, int esize, int grid, int max_s, int& S, int& SL) {
     int s;
     if (g_tune_slices > 0) {
@@ -104,7 +105,7 @@ void choose_slices(int B, int V, int esize, int grid, int max_s, int& S, int& SL
     } else {
         s = static_cast<int>((4ll * grid + B - 1) / (B > 0 ? B : 1));
         const long long row_bytes = static_cast<long long>(V) * esize;
-        const int by_size = static_cast<int>((row_bytes + 16383) / 16384);
+        const int by_size = static_cast<int>((row_bytes + 32767) / 32768);
         if (s > by_size) s = by_size;
     }
     if (s > max_s) s = max_s;

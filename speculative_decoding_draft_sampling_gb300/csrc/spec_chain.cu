@@ -26,30 +26,54 @@ enum ChainKind : int { kVerify = 0, kBonus = 1, kResid = 2, kInvalid = 3 };
 constexpr int kKindMask = 7;
 constexpr int kNoHint = 8;        // kind bit: stream the row without a filter hint (a retry)
 
-// combine / slice-reduction scratch (the ring belongs to the producer):
-// up to kScrKeys keys and as many ints
-constexpr int kScrKeys = 2560;
-template <bool kTopk> struct ChainTopkPart {};
-template <> struct ChainTopkPart<true> {
-    TopkSmem tk;
-    alignas(16) unsigned char scr[kScrKeys * 12];
+// Combiner scratch: the gathered candidate keys, then the top-k set sorted by
+// token (ids and fp64 weights; a larger tied set takes the exact fallback).
+constexpr int kCombKeys = 2048;
+constexpr int kCombSet = 512;
+// A top-k combine as the combiner warp prepared it for the consumers: the
+// gathered keys are in CombSmem::list.
+struct CombPrep {
+    int b, row, kind, st;
+    int n;            // gathered keys
+    int y;            // drafted token (VERIFY)
+    int fallback;     // 1: a slice overflowed; take the exact path
+    int hinted;       // a slice streamed behind a hint
+    float vmax;
+    float pad;
+    uint64_t theta;   // largest slice filter
+    double uk, ur;    // uniforms: sample, accept
+    // an untruncated draw: rescan slice [x0, x1) for the CDF crossing t
+    int x0, x1, wmode;  // wmode 0: p weights 2^((l-m)c); 1: [p - q]_+
+    float m, invZf;
+    double t, Z, R;
 };
+struct CombSmem {
+    SliceHdrs hdrs;
+    CombPrep prep;
+    alignas(16) uint64_t list[kCombKeys];
+    int rank[kCombKeys];
+    int tok[kCombSet];
+    double wgt[kCombSet];
+};
+
+template <bool kTopk> struct ChainTopkPart {};
+template <> struct ChainTopkPart<true> { TopkSmem tk; };
 
 template <bool kTopk>
 struct __align__(16) ChainSmem : ChainTopkPart<kTopk> {
     PipeSmem pipe;
-    int last;
-    int lcnt;
-    int oflow;
+    CombSmem comb;
     uint64_t sh64[4];
+    int ish[4];
     double red[kWarps];
     int ired[kWarps + 4];
     int hist[64];
     uint32_t scratch[kWarps + 2];
-    double dsh[8];
-    int ish[8];
     float fsh[8];
-    SliceHdrs hdrs;
+    float wm[kWarps];        // per-warp partials of the one-barrier finishes
+    double ws[kWarps];
+    double ws2[kWarps];
+    uint32_t wb[kWarps];
 };
 
 __device__ __forceinline__ int chain_k(const ChainArgs& A, int b) {
@@ -70,9 +94,30 @@ __device__ __forceinline__ float chain_u(const ChainArgs& A, int b, int i) {
     return A.uniforms[static_cast<long long>(b) * (A.K + 1) + i];
 }
 
+// ---------------------------------------------------------------------------
+// combiner-warp steps (all 32 lanes unless stated)
+// ---------------------------------------------------------------------------
 // Commit the request: accepted drafts, then `last` (correction/bonus, or -1),
-// then -1 padding.  All threads call; thread 0 publishes completion.
+// then -1 padding; lane 0 publishes completion.
 __device__ void chain_finish(const ChainArgs& A, int b, int n, int last, int st) {
+    const int W = A.K + 1;
+    int* out = A.out_tokens + static_cast<long long>(b) * W;
+    for (int i = threadIdx.x & 31; i < W; i += 32) {
+        int v = -1;
+        if (i < n) v = A.draft[static_cast<long long>(b) * A.K + i];
+        else if (i == n) v = last;
+        out[i] = v;
+    }
+    if ((threadIdx.x & 31) == 0) {
+        A.num_accepted[b] = n;
+        A.status[b] = st;
+    }
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) finish_request(A.W);
+}
+
+// The same on every consumer thread (a combine the consumers run).
+__device__ void chain_finish_cta(const ChainArgs& A, int b, int n, int last, int st) {
     const int W = A.K + 1;
     int* out = A.out_tokens + static_cast<long long>(b) * W;
     for (int i = threadIdx.x; i < W; i += kThreads) {
@@ -95,7 +140,7 @@ __device__ __forceinline__ void chain_diag(const ChainArgs& A, int b, int i, flo
     d[0] = py; d[1] = qy; d[2] = Z; d[3] = R;
 }
 
-// thread 0: push the request's next task after an accepted position
+// lane 0: push the request's next task after an accepted position
 __device__ void chain_advance(const ChainArgs& A, int b, int row, int kb, int st, uint32_t hint) {
     ReqState* rs = &A.W.req[b];
     __stcg(&rs->status, st);
@@ -117,26 +162,23 @@ __device__ __forceinline__ bool chain_accept(const ChainArgs& A, int y, double p
         st |= 2;
         ratio = py > 0.0 ? __longlong_as_double(0x7ff0000000000000LL) : 0.0;
     } else {
-        ratio = py / qy;
+        // u < p/q as u*q < p: the two differ only within rounding of p/q,
+        // inside the near-tie band
+        return u * qy < py;
     }
     return u < ratio;
 }
 
-// One warp: inverse CDF over n (token, weight) pairs sorted by token; the
-// smallest token with prefix > t.  Result broadcast to the whole warp.
+// Inverse CDF over n (token, weight) pairs sorted by token; the smallest
+// token with prefix > t.  Result in every lane.
 __device__ int warp_icdf_pairs(const int* tok, const double* w, int n, double t) {
     const int lane = threadIdx.x & 31;
     const int per = (n + 31) / 32;
     const int i0 = lane * per, i1 = min(n, i0 + per);
     double loc = 0.0;
     for (int i = i0; i < i1; ++i) loc += w[i];
-    double inc = loc;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double v = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += v;
-    }
-    double c = inc - loc;
+    double tot;
+    double c = warp_exscan_d(loc, tot);
     int found = 0x7fffffff, lastpos = -1;
     for (int i = i0; i < i1; ++i) {
         if (w[i] > 0.0) {
@@ -154,67 +196,88 @@ __device__ int warp_icdf_pairs(const int* tok, const double* w, int n, double t)
     return n > 0 ? tok[pick] : -1;
 }
 
-__device__ __forceinline__ int n_slices_dbg(int S) { return S; }
-
 // Filter hint for the next row from this row's top-k threshold tau and max
-// m: half the gap below tau (rows of one target differ little in tau).
+// m: 0.15 of the gap below tau (rows of one target differ little in tau; a
+// hint above the next row's tau only costs a re-read of that row).
 __device__ __forceinline__ uint32_t next_hint(float tau, float m) {
-    const float h = tau - 0.5f * (m - tau);
+    const float h = tau - 0.15f * (m - tau);
     return (h == h && h > -kInf) ? fkey(h) : 0u;
 }
 
 // ---------------------------------------------------------------------------
 // combine with top-k: the candidate lists of all slices hold S exactly
 // ---------------------------------------------------------------------------
+// Combiner warp, last arrival of a top-k row: everything that waits on
+// global memory -- the slice headers, the drafted token, the uniforms, every
+// slice key -- into shared memory for the consumers.  Returns false when the
+// combine ended here (a bad row).
 template <class E>
-__device__ void chain_fallback(const ChainArgs& A, ChainSmem<true>& sh, int b, int row, int kind,
-                               int st, float vmax);
-
-template <class E>
-__device__ void combine_topk(const ChainArgs& A, ChainSmem<true>& sh, int b, int row,
-                             int kind, int st) {
+__device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st) {
+    const int l = threadIdx.x & 31;
     const int S = A.S;
-    const int k = A.top_k;
     const int kb = chain_k(A, b);
-    // independent loads first: they overlap the header loads
     const double uk = static_cast<double>(chain_u(A, b, kb));
     const double ur = kind == kVerify ? static_cast<double>(chain_u(A, b, row)) : 0.0;
     const int y = kind == kVerify ? A.draft[static_cast<long long>(b) * A.K + row] : -1;
-    SliceHdrs& H = sh.hdrs;
-    load_hdrs(A.W, b, S, H);
-    SPEC_TRACE_EV(5, b, row, n_slices_dbg(S), kind);
+    SliceHdrs& H = cs.hdrs;
+    load_hdrs_w(A.W, b, S, H);
+    SPEC_TRACE_EVW(5, b, row, S, kind);
     uint32_t flags = 0;
     float vmax = -kInf;
     uint64_t theta = 0;
-    for (int s = 0; s < S; ++s) {
-        flags |= H.flags[s];
-        vmax = max_nan(vmax, H.vmax[s]);
-        theta = H.kth[s] > theta ? H.kth[s] : theta;
+    if (l < S) { flags = H.flags[l]; vmax = H.vmax[l]; theta = H.kth[l]; }
+    flags = __reduce_or_sync(0xffffffffu, flags);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        vmax = max_nan(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+        const uint64_t t2 = __shfl_xor_sync(0xffffffffu, theta, o);
+        theta = t2 > theta ? t2 : theta;
     }
     if ((flags & kPfBad) || !(vmax > -kInf)) {
         chain_finish(A, b, row, -1, st | 1);
+        return false;
+    }
+    int n = 0, fb = (flags & kPfOverflow) ? 1 : 0;
+    if (!fb) {
+        bool oflow;
+        n = gather_all_w(A.W, b, S, H, cs.list, kCombKeys, oflow);
+        if (oflow) fb = 1;
+    }
+    SPEC_TRACE_EVW(6, b, row, n, kind);
+    if (l == 0) {
+        CombPrep& p = cs.prep;
+        p.b = b; p.row = row; p.kind = kind; p.st = st; p.n = n; p.y = y; p.fallback = fb;
+        p.hinted = (flags & kPfHinted) ? 1 : 0;
+        p.vmax = vmax; p.theta = theta; p.uk = uk; p.ur = ur;
+    }
+    return true;
+}
+
+template <class E>
+__device__ void chain_fallback_cta(const ChainArgs& A, ChainSmem<true>& sh, int b, int row, int kind,
+                                   int st, float vmax);
+
+// Consumers: the compute of a prepared top-k combine.  The set S of the
+// row's k largest values (ties kept) from the gathered keys, its normaliser
+// Z, then the accept test at the drafted token, or a draw from the residual
+// [p - q]_+ on S (rejection) or from p (bonus row).
+template <class E>
+__device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
+    CombSmem& cs = sh.comb;
+    const CombPrep p = cs.prep;
+    const int b = p.b, row = p.row, kind = p.kind, k = A.top_k;
+    int st = p.st;
+    const int kb = chain_k(A, b);
+    if (p.fallback) {
+        chain_fallback_cta<E>(A, sh, b, row, kind, st, p.vmax);
         return;
     }
-    if (flags & kPfOverflow) {
-        chain_fallback<E>(A, sh, b, row, kind, st, vmax);
-        return;
-    }
-    const bool hinted = (flags & kPfHinted) != 0;
-    // gather every candidate at or above the largest slice filter
-    constexpr int kList = kScrKeys;
-    uint64_t* list = reinterpret_cast<uint64_t*>(sh.scr);
-    int* rank = reinterpret_cast<int*>(sh.scr + kList * 8);
-    gather_keys(A.W, b, S, H, [&](uint64_t key) { return key >= theta; }, list, kList, &sh.lcnt, &sh.oflow);
-    int n = sh.lcnt;
-    SPEC_TRACE_EV(6, b, row, n, kind);
-    if (sh.oflow || n > kList) {
-        csync();
-        chain_fallback<E>(A, sh, b, row, kind, st, vmax);
-        return;
-    }
+    uint64_t* list = cs.list;
+    const uint32_t th = hkey(p.theta);
+    // keys at or above the largest slice filter: enough for the k-th?
+    int n = compact_list(list, p.n, th, sh.ired);
     if (n < k) {
-        csync();
-        if (hinted) {
+        if (p.hinted) {
             // the hint was above the row's k-th value: stream the row again without it
             if (threadIdx.x == 0) {
                 __stcg(&A.W.req[b].status, st);
@@ -224,68 +287,62 @@ __device__ void combine_topk(const ChainArgs& A, ChainSmem<true>& sh, int b, int
             }
             return;
         }
-        chain_fallback<E>(A, sh, b, row, kind, st, vmax);
+        chain_fallback_cta<E>(A, sh, b, row, kind, st, p.vmax);
         return;
-    }
-    if (n > 2 * k + 64) {
-        // certified pre-reduction: fewer keys for the quadratic selection
-        bool cert;
-        const uint32_t F = hist_bound_list(list, n, k, hkey(theta), sh.hist, sh.scratch, cert);
-        if (cert && F > hkey(theta)) n = compact_list(list, n, F, sh.ired);
     }
     uint64_t kth;
     bool of = false;
     uint64_t* cand = sh.tk.cand;
     constexpr int kCandCap = kWarps * TopkSmem::kRegion;
-    const int keep = select_to(list, n, k, true, rank, cand, kCandCap, kth, of, sh.sh64, sh.ired);
+    const int keep = select_to(list, n, k, true, cs.rank, cand, kCandCap, kth, of, sh.sh64, sh.ired);
     SPEC_TRACE_EV(7, b, row, n, kind);
-    if (of) {
-        chain_fallback<E>(A, sh, b, row, kind, st, vmax);
+    if (of || keep > kCombSet) {
+        chain_fallback_cta<E>(A, sh, b, row, kind, st, p.vmax);
         return;
     }
     // S = cand[0 .. keep): values >= tau, sorted by value descending
     const uint32_t tau_key = hkey(cand[keep - 1]);
     const float tau = ckey_val(cand[keep - 1]);
-    const float m = vmax, c2 = A.c2;
+    const float m = p.vmax, c2 = A.c2;
     double zpart = 0.0;
     for (int i = threadIdx.x; i < keep; i += kThreads)
         zpart += static_cast<double>(ex2((ckey_val(cand[i]) - m) * c2));
     const double Z = block_sum_d(zpart, sh.red);
+    const double invZ = 1.0 / Z;
     const uint32_t hint = next_hint(tau, m);
     if (threadIdx.x == 0) __stcg(&A.W.ctrl->hint0, hint);
 
-    // weights of S sorted by token id (ascending): pairs in the ring
-    int* tok = reinterpret_cast<int*>(sh.scr);
-    double* wgt = reinterpret_cast<double*>(sh.scr + kScrKeys * 4);
+    // weights of S sorted by token id (ascending)
     auto sort_by_token = [&](bool residual, const float* qrow, double& total) {
         double part = 0.0;
         for (int i = threadIdx.x; i < keep; i += kThreads) {
             const int x = ckey_idx(cand[i]);
             int r = 0;
             for (int j = 0; j < keep; ++j) r += ckey_idx(cand[j]) < x;
-            const double p = static_cast<double>(ex2((ckey_val(cand[i]) - m) * c2)) / Z;
-            double w = p;
+            const double pw = static_cast<double>(ex2((ckey_val(cand[i]) - m) * c2)) * invZ;
+            double w = pw;
             if (residual) {
                 const float qx = (x >= 0 && x < A.V) ? qrow[x] : 0.f;   // keys always hold in-range ids
-                const double d = p - static_cast<double>(qx);
+                const double d = pw - static_cast<double>(qx);
                 w = d > 0.0 ? d : 0.0;
             }
-            tok[r] = x;
-            wgt[r] = w;
+            cs.tok[r] = x;
+            cs.wgt[r] = w;
             part += w;
         }
         total = block_sum_d(part, sh.red);
     };
 
     if (kind == kVerify) {
+        const int y = p.y;
         double py = 0.0, qy = 0.0;
         if (y >= 0 && y < A.V) {
             const int sy = y / A.SL;
-            const float ly = H.ly[sy];
-            qy = static_cast<double>(H.qy[sy]);
-            if (fkey(ly) >= tau_key) py = static_cast<double>(ex2((ly - m) * c2)) / Z;
+            const float ly = cs.hdrs.ly[sy];
+            qy = static_cast<double>(cs.hdrs.qy[sy]);
+            if (fkey(ly) >= tau_key) py = static_cast<double>(ex2((ly - m) * c2)) * invZ;
         }
-        const bool acc = chain_accept(A, y, py, qy, ur, st);
+        const bool acc = chain_accept(A, y, py, qy, p.ur, st);
         if (acc) {
             if (threadIdx.x == 0) {
                 chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
@@ -301,35 +358,35 @@ __device__ void combine_topk(const ChainArgs& A, ChainSmem<true>& sh, int b, int
             sort_by_token(false, nullptr, R_mass);
         }
         int x = -1;
-        if (threadIdx.x < 32) x = warp_icdf_pairs(tok, wgt, keep, uk * R_mass);
+        if (threadIdx.x < 32) x = warp_icdf_pairs(cs.tok, cs.wgt, keep, p.uk * R_mass);
         if (threadIdx.x == 0) {
             sh.ish[0] = x;
             chain_diag(A, b, row, (float)py, (float)qy, (float)Z, (st & 4) ? 0.f : (float)R_mass);
         }
         csync();
-        chain_finish(A, b, row, sh.ish[0], st);
+        chain_finish_cta(A, b, row, sh.ish[0], st);
         return;
     }
     // bonus row: draw from p
     double tot;
     sort_by_token(false, nullptr, tot);
     int x = -1;
-    if (threadIdx.x < 32) x = warp_icdf_pairs(tok, wgt, keep, uk * tot);
+    if (threadIdx.x < 32) x = warp_icdf_pairs(cs.tok, cs.wgt, keep, p.uk * tot);
     if (threadIdx.x == 0) sh.ish[0] = x;
     csync();
     x = sh.ish[0];
     if (threadIdx.x == 0 && x >= 0 && x < A.V)
-        chain_diag(A, b, row, (float)(static_cast<double>(ex2((E::load(chain_lrow<E>(A, b, row), x) - m) * c2)) / Z),
+        chain_diag(A, b, row, (float)(static_cast<double>(ex2((E::load(chain_lrow<E>(A, b, row), x) - m) * c2)) * invZ),
                    0.f, (float)Z, 0.f);
-    chain_finish(A, b, row, x, st);
+    chain_finish_cta(A, b, row, x, st);
 }
 
-// Exact single-CTA path for rows whose top-k set did not fit the candidate
-// buffers (massive ties, adversarial order): tau by bisection over
+// Exact path for rows whose top-k set did not fit the candidate buffers
+// (massive ties, adversarial order), on the consumers: tau by bisection over
 // order-preserving keys, then full-row passes.  Slow; correctness only.
 template <class E>
-__device__ void chain_fallback(const ChainArgs& A, ChainSmem<true>& sh, int b, int row, int kind,
-                               int st, float vmax) {
+__device__ void chain_fallback_cta(const ChainArgs& A, ChainSmem<true>& sh, int b, int row, int kind,
+                                   int st, float vmax) {
     const void* lrow = chain_lrow<E>(A, b, row);
     const int V = A.V, k = A.top_k;
     // largest key t with #{x : key(l_x) >= t} >= k
@@ -381,48 +438,42 @@ __device__ void chain_fallback(const ChainArgs& A, ChainSmem<true>& sh, int b, i
             x = cta_icdf(0, V, uk * Z, wp, sh.red, sh.ired);
         }
         if (threadIdx.x == 0) chain_diag(A, b, row, (float)py, (float)qy, (float)Z, (float)R_mass);
-        chain_finish(A, b, row, x, st);
+        chain_finish_cta(A, b, row, x, st);
         return;
     }
     const int x = cta_icdf(0, V, uk * Z, wp, sh.red, sh.ired);
     if (threadIdx.x == 0)
         chain_diag(A, b, row, (float)(static_cast<double>(wp(x)) / Z), 0.f, (float)Z, 0.f);
-    chain_finish(A, b, row, x, st);
+    chain_finish_cta(A, b, row, x, st);
 }
 
 // ---------------------------------------------------------------------------
 // combine without truncation: per-slice (max, sum of 2^((l-m_s)c))
 // ---------------------------------------------------------------------------
-// index of the slice whose running prefix of `val(s)` crosses t; *before* =
-// prefix before it.  Thread 0 computes, result broadcast.
-template <class F>
-__device__ int find_slice(int S, double t, F val, double& before, double* dsh, int* ish) {
-    if (threadIdx.x == 0) {
-        double acc = 0.0;
-        int pick = -1, lastpos = -1;
-        double lastbefore = 0.0;
-        for (int s = 0; s < S; ++s) {
-            const double v = val(s);
-            if (v > 0.0) {
-                if (acc + v > t) { pick = s; break; }
-                lastpos = s;
-                lastbefore = acc;
-            }
-            acc += v;
-        }
-        if (pick < 0) { pick = lastpos >= 0 ? lastpos : 0; acc = lastbefore; }
-        ish[0] = pick;
-        dsh[0] = acc;
+// the slice whose running prefix of v (lane s holds slice s's value) crosses
+// t, and the prefix before it
+__device__ __forceinline__ int find_slice_w(int S, double v, double t, double& before) {
+    const int l = threadIdx.x & 31;
+    if (l >= S) v = 0.0;
+    double tot;
+    const double ex = warp_exscan_d(v, tot);
+    const uint32_t bal = __ballot_sync(0xffffffffu, v > 0.0 && ex + v > t);
+    int pick;
+    if (bal) {
+        pick = __ffs(bal) - 1;
+    } else {
+        const uint32_t pos = __ballot_sync(0xffffffffu, v > 0.0);
+        pick = pos ? 31 - __clz(pos) : 0;
     }
-    csync();
-    const int s = ish[0];
-    before = dsh[0];
-    csync();
-    return s;
+    before = __shfl_sync(0xffffffffu, ex, pick);
+    return pick;
 }
 
+// Combiner warp: the combine of an untruncated row.  Returns true when a draw
+// needs a slice rescan, prepared in cs.prep for the consumers.
 template <class E>
-__device__ void combine_full(const ChainArgs& A, ChainSmem<false>& sh, int b, int row, int kind, int st) {
+__device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st) {
+    const int l = threadIdx.x & 31;
     const int S = A.S;
     const int kb = chain_k(A, b);
     const double cd = static_cast<double>(A.c2);
@@ -430,64 +481,51 @@ __device__ void combine_full(const ChainArgs& A, ChainSmem<false>& sh, int b, in
     const double ur = kind == kVerify ? static_cast<double>(chain_u(A, b, row)) : 0.0;
     const int y = kind == kVerify ? A.draft[static_cast<long long>(b) * A.K + row] : -1;
     const void* lrow = chain_lrow<E>(A, b, row);
-    SliceHdrs& H = sh.hdrs;
-    load_hdrs(A.W, b, S, H);
-    SPEC_TRACE_EV(5, b, row, S, kind);
+    SliceHdrs& H = cs.hdrs;
+    load_hdrs_w(A.W, b, S, H);
+    SPEC_TRACE_EVW(5, b, row, S, kind);
     if (kind == kResid) {
         const ReqState* rs = &A.W.req[b];
         const float m = static_cast<float>(__ldcg(&rs->m));
         const double Z = __ldcg(&rs->Z);
-        double R_mass = 0.0, P_mass = 0.0;
-        for (int s = 0; s < S; ++s) {
-            R_mass += H.sum[s];
-            P_mass += H.sum2[s];
-        }
-        const float* qrow = chain_qrow(A, b, row);
-        const float c2 = A.c2, invZ = static_cast<float>(1.0 / Z);
-        int x;
-        double before;
+        const double rv = l < S ? H.sum[l] : 0.0, pv = l < S ? H.sum2[l] : 0.0;
+        const double R_mass = warp_sum_d(rv);
+        const double P_mass = warp_sum_d(pv);
+        double before, t;
+        int s, wmode;
         if (R_mass > 0.0) {
-            const double t = uk * R_mass;
-            const int s = find_slice(S, t, [&](int j) { return H.sum[j]; }, before, sh.dsh, sh.ish);
-            auto wr = [&](int xx) -> float {
-                const float d = ex2((E::load(lrow, xx) - m) * c2) * invZ - qrow[xx];
-                return d > 0.f ? d : 0.f;
-            };
-            const int x0 = s * A.SL, x1 = min(A.V, x0 + A.SL);
-            x = cta_icdf(x0, x1, t - before, wr, sh.red, sh.ired);
+            t = uk * R_mass;
+            s = find_slice_w(S, rv, t, before);
+            wmode = 1;
         } else {
             st |= 4;
-            const double t = uk * P_mass;
-            const int s = find_slice(S, t, [&](int j) { return H.sum2[j]; }, before, sh.dsh, sh.ish);
-            auto wp = [&](int xx) -> float { return ex2((E::load(lrow, xx) - m) * c2); };
-            const int x0 = s * A.SL, x1 = min(A.V, x0 + A.SL);
-            x = cta_icdf(x0, x1, t - before, wp, sh.red, sh.ired);
+            t = uk * P_mass;
+            s = find_slice_w(S, pv, t, before);
+            wmode = 0;
         }
-        if (threadIdx.x == 0 && A.diag)
-            A.diag[(static_cast<long long>(b) * (A.K + 1) + row) * 4 + 3] = (st & 4) ? 0.f : (float)R_mass;
-        chain_finish(A, b, row, x, st);
-        return;
+        if (l == 0) {
+            CombPrep& p = cs.prep;
+            p.b = b; p.row = row; p.kind = kind; p.st = st;
+            p.x0 = s * A.SL; p.x1 = min(A.V, p.x0 + A.SL); p.wmode = wmode;
+            p.m = m; p.invZf = static_cast<float>(1.0 / Z);
+            p.t = t - before; p.Z = Z; p.R = R_mass;
+        }
+        return true;   // the consumers rescan the slice
     }
     // VERIFY or BONUS: max and normaliser from the slice partials
-    uint32_t flags = 0;
-    float vmax = -kInf;
-    for (int s = 0; s < S; ++s) {
-        flags |= H.flags[s];
-        vmax = max_nan(vmax, H.vmax[s]);
-    }
+    uint32_t flags = l < S ? H.flags[l] : 0u;
+    float vmax = l < S ? H.vmax[l] : -kInf;
+    flags = __reduce_or_sync(0xffffffffu, flags);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) vmax = max_nan(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
     if ((flags & kPfBad) || !(vmax > -kInf)) {
         chain_finish(A, b, row, -1, st | 1);
-        return;
+        return false;
     }
     const double m = static_cast<double>(vmax);
-    auto scaled = [&](int s) -> double {
-        const double sm = H.sum[s];
-        return sm > 0.0 ? sm * exp2((static_cast<double>(H.vmax[s]) - m) * cd) : 0.0;
-    };
-    double zp = 0.0;
-    for (int s = threadIdx.x; s < S; s += kThreads) zp += scaled(s);
-    const double Z = block_sum_d(zp, sh.red);
-    SPEC_TRACE_EV(6, b, row, S, kind);
+    double zv = 0.0;
+    if (l < S && H.sum[l] > 0.0) zv = H.sum[l] * exp2((static_cast<double>(H.vmax[l]) - m) * cd);
+    const double Z = warp_sum_d(zv);
     if (kind == kVerify) {
         double py = 0.0, qy = 0.0;
         if (y >= 0 && y < A.V) {
@@ -496,13 +534,12 @@ __device__ void combine_full(const ChainArgs& A, ChainSmem<false>& sh, int b, in
             qy = static_cast<double>(H.qy[sy]);
         }
         const bool acc = chain_accept(A, y, py, qy, ur, st);
-        SPEC_TRACE_EV(7, b, row, S, kind);
-        if (threadIdx.x == 0) chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
+        if (l == 0) chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
         if (acc) {
-            if (threadIdx.x == 0) chain_advance(A, b, row, kb, st, 0u);
-            return;
+            if (l == 0) chain_advance(A, b, row, kb, st, 0u);
+            return false;
         }
-        if (threadIdx.x == 0) {
+        if (l == 0) {
             ReqState* rs = &A.W.req[b];
             __stcg(&rs->m, m);
             __stcg(&rs->Z, Z);
@@ -511,20 +548,52 @@ __device__ void combine_full(const ChainArgs& A, ChainSmem<false>& sh, int b, in
             t.b = b; t.row = row; t.kind = kResid; t.aux = 0;
             push_task(A.W, t);
         }
-        return;
+        return false;
     }
-    // BONUS: inverse CDF of p; find the slice, then rescan it
+    // BONUS: inverse CDF of p; find the slice, the consumers rescan it
     const double t = uk * Z;
     double before;
-    const int s = find_slice(S, t, scaled, before, sh.dsh, sh.ish);
-    const float mf = vmax, c2 = A.c2;
-    auto wp = [&](int xx) -> float { return ex2((E::load(lrow, xx) - mf) * c2); };
-    const int x0 = s * A.SL, x1 = min(A.V, x0 + A.SL);
-    const int x = cta_icdf(x0, x1, t - before, wp, sh.red, sh.ired);
-    if (threadIdx.x == 0)
-        chain_diag(A, b, row, (float)(exp((static_cast<double>(E::load(lrow, x)) - m) / A.Td) / Z), 0.f,
-                   (float)Z, 0.f);
-    chain_finish(A, b, row, x, st);
+    const int s = find_slice_w(S, zv, t, before);
+    if (l == 0) {
+        CombPrep& p = cs.prep;
+        p.b = b; p.row = row; p.kind = kind; p.st = st;
+        p.x0 = s * A.SL; p.x1 = min(A.V, p.x0 + A.SL); p.wmode = 0;
+        p.m = vmax; p.invZf = static_cast<float>(1.0 / Z);
+        p.t = t - before; p.Z = Z; p.R = 0.0;
+    }
+    return true;
+}
+
+// Consumers: the rescan of an untruncated draw prepared by combine_full --
+// the inverse CDF over one slice -- then the commit.
+template <class E>
+__device__ void rescan_cta(const ChainArgs& A, ChainSmem<false>& sh) {
+    const CombPrep p = sh.comb.prep;
+    const int b = p.b, row = p.row;
+    const void* lrow = chain_lrow<E>(A, b, row);
+    const float m = p.m, c2 = A.c2, invZ = p.invZf;
+    int x;
+    if (p.wmode == 1) {
+        const float* qrow = chain_qrow(A, b, row);
+        auto wr = [&](int xx) -> float {
+            const float d = ex2((E::load(lrow, xx) - m) * c2) * invZ - qrow[xx];
+            return d > 0.f ? d : 0.f;
+        };
+        x = cta_icdf(p.x0, p.x1, p.t, wr, sh.red, sh.ired);
+    } else {
+        auto wp = [&](int xx) -> float { return ex2((E::load(lrow, xx) - m) * c2); };
+        x = cta_icdf(p.x0, p.x1, p.t, wp, sh.red, sh.ired);
+    }
+    if (threadIdx.x == 0) {
+        if (p.kind == kResid) {
+            if (A.diag) A.diag[(static_cast<long long>(b) * (A.K + 1) + row) * 4 + 3] = (p.st & 4) ? 0.f : (float)p.R;
+        } else if (x >= 0 && x < A.V) {
+            chain_diag(A, b, row,
+                       (float)(exp((static_cast<double>(E::load(lrow, x)) - static_cast<double>(m)) / A.Td) / p.Z), 0.f,
+                       (float)p.Z, 0.f);
+        }
+    }
+    chain_finish_cta(A, b, row, x, p.st);
 }
 
 // ---------------------------------------------------------------------------
@@ -554,8 +623,29 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
     // the residual pass streams q beside the logits; without q rows (K = 0)
     // there is no residual pass
     const bool tma = A.tma_l && (kTopk || A.K == 0 || A.tma_q);
+    if (threadIdx.x >= kCombiner0) {
+        // combiner warp: arrivals, combines (top-k: prepared here, computed by
+        // the consumers at their next wait)
+        uint32_t cpub = 0;
+        combiner_loop(P, [&](const Job& job) {
+            const int b = job.task.b;
+            if (!comb_arrive(A.W, b, A.S)) return;
+            SPEC_TRACE_EVW(2, b, job.task.row, job.slice, job.kind);
+            const int st = job.task.kind < 0 ? 0 : __ldcg(&A.W.req[b].status);
+            if (job.kind == kInvalid) {
+                chain_finish(A, b, 0, -1, 16);
+            } else if constexpr (kTopk) {
+                if (prepare_topk<E>(A, sh.comb, b, job.task.row, job.kind, st)) publish_combine(P, cpub);
+            } else {
+                if (combine_full<E>(A, sh.comb, b, job.task.row, job.kind, st)) publish_combine(P, cpub);
+            }
+            __syncwarp();
+            SPEC_TRACE_EVW(3, b, job.task.row, job.slice, job.kind);
+        });
+        return;
+    }
     if (threadIdx.x >= kThreads) {
-        if (threadIdx.x == kThreads) {
+        if (threadIdx.x == kProducer) {
             producer_loop(A.W, A.B, A.S, P, tma,
                           [&](Claimed& c) {
                               if (kTopk && c.task.kind < 0) c.hint = __ldcg(&A.W.ctrl->hint0);
@@ -566,9 +656,13 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
         }
         return;
     }
-    uint32_t seq = 0;
+    uint32_t seq = 0, jseq = 0, cseq = 0;
+    auto serve = [&]() {
+        if constexpr (kTopk) combine_topk_cta<E>(A, sh);
+        else rescan_cta<E>(A, sh);
+    };
     for (uint32_t u = 0;; ++u) {
-        const Claimed cl = next_unit(P, u);
+        const Claimed cl = next_unit(P, u, cseq, serve);
         if (!cl.ok) break;
         const Task t = cl.task;
         const int s = cl.slice;
@@ -582,6 +676,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
         uint64_t* pk = part_keys(A.W, b, s, A.S);
         const int x0 = s * A.SL, x1 = min(A.V, x0 + A.SL);
         const StreamPlan plan = chain_plan<E>(A, t, kind, s);
+        bool ok = true;
         if (kind == kVerify || kind == kBonus) {
             // the drafted token: its logit is recorded as the slice streams,
             // its q fetched early by the slice that holds it
@@ -597,65 +692,79 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
                 TopkHistFn<E, true> fn;
                 fn.init(&sh.tk, A.top_k, hint);
                 fn.dw = dw;
-                if (!consume_row<E>(P, seq, plan, tma, x0, fn)) break;
-                SPEC_TRACE_EV(4, b, row, s, kind);
-                uint64_t F;
-                uint32_t oflow, bad;
-                int n = fn.finish(F, oflow, bad);
-                uint64_t* list = sh.tk.cand;
-                const float vm = block_max_nan(fn.vmx, reinterpret_cast<float*>(sh.red));
-                if (fn.dw.seen) wsl[0] = fn.dw.ly;
-                if (n > A.cap_p && !oflow && !bad) {
-                    // certified bound first, then the exact top-k (ties kept)
-                    bool cert;
-                    const uint32_t F2 = hist_bound_list(list, n, A.top_k, hkey(F), sh.hist, sh.scratch, cert);
-                    if (cert && F2 > hkey(F)) {
-                        n = compact_list(list, n, F2, sh.ired);
-                        F = static_cast<uint64_t>(F2) << 32;
+                ok = consume_row<E>(P, seq, plan, tma, x0, fn);
+                if (ok) {
+                    SPEC_TRACE_EV(4, b, row, s, kind);
+                    fn.publish();
+                    if (fn.dw.seen) wsl[0] = fn.dw.ly;
+                    csync();
+                    int tot;
+                    uint64_t F;
+                    uint32_t fl;
+                    float vm;
+                    fn.summary(tot, F, fl, vm);
+                    const uint32_t bad = (fl >> 1) & 1u;
+                    uint32_t oflow = fl & 1u;
+                    int n = tot;
+                    if (!bad && !oflow && tot <= A.cap_p) {
+                        fn.write_keys(pk);   // every warp's keys at its offset
+                    } else if (!bad && !oflow) {
+                        // too many: the certified bound over every candidate, repeated
+                        // until it stops rising (then it is the exact k-th value)
+                        uint32_t o2, b2;
+                        float vm2;
+                        n = fn.finish(F, o2, b2, vm2);
+                        uint64_t* list = sh.tk.cand;
+                        for (int it = 0; it < 8 && n > A.cap_p; ++it) {
+                            bool cert;
+                            const uint32_t F2 = hist_bound_list(list, n, A.top_k, hkey(F), sh.hist, sh.scratch, cert);
+                            if (!(cert && F2 > hkey(F))) break;
+                            n = compact_list(list, n, F2, sh.ired);
+                            F = static_cast<uint64_t>(F2) << 32;
+                        }
+                        if (n > A.cap_p) oflow = 1;   // ties at the k-th value: the fallback decides
+                        else for (int i = threadIdx.x; i < n; i += kThreads) __stcg(pk + i, list[i]);
                     }
-                    if (n > A.cap_p) {
-                        uint64_t* dst = reinterpret_cast<uint64_t*>(sh.scr);
-                        int* rank = reinterpret_cast<int*>(sh.scr + kScrKeys * 8);
-                        uint64_t kth;
-                        bool of2;
-                        const int keep = select_to(list, n, A.top_k, true, rank, dst, min(A.cap_p, kScrKeys), kth,
-                                                   of2, sh.sh64, sh.ired);
-                        if (of2) oflow = 1;
-                        else F = static_cast<uint64_t>(hkey(kth)) << 32;
-                        n = keep;
-                        list = dst;
+                    if (oflow || bad) n = 0;   // the combine does not read the keys then
+                    if (threadIdx.x == 0) {
+                        ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u) | (hint ? kPfHinted : 0u);
+                        ph->cnt = n;
+                        ph->kth = F;
+                        ph->vmax = vm;
+                        if (fn.dw.owns()) { ph->ly = wsl[0]; ph->qy = fn.dw.qy; }
                     }
-                }
-                if (oflow || bad) n = 0;   // the combine does not read the keys then
-                csync();
-                for (int i = threadIdx.x; i < n; i += kThreads) __stcg(pk + i, list[i]);
-                if (threadIdx.x == 0) {
-                    ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u) | (hint ? kPfHinted : 0u);
-                    ph->cnt = n;
-                    ph->kth = F;
-                    ph->vmax = vm;
-                    if (fn.dw.owns()) { ph->ly = wsl[0]; ph->qy = fn.dw.qy; }
                 }
             } else {
                 SumExpFn<E> fn;
                 fn.c = A.c2;
                 fn.dw = dw;
-                if (!consume_row<E>(P, seq, plan, tma, x0, fn)) break;
-                // fold per-thread (m_t, s_t) into the slice max and sum
-                const uint64_t mk = block_max_u64(static_cast<uint64_t>(fkey(fn.m)), reinterpret_cast<uint64_t*>(sh.red));
-                const float ms = fkey_inv(static_cast<uint32_t>(mk));
-                float sc = 0.f;
-                if (fn.s > 0.f) sc = fn.s * ex2((fn.m - ms) * A.c2);
-                const double tot = block_sum_d(static_cast<double>(sc), sh.red);
-                const uint32_t bad = block_or(fn.bad_flag(), reinterpret_cast<uint32_t*>(sh.red));
-                if (fn.dw.seen) wsl[0] = fn.dw.ly;
-                csync();
-                if (threadIdx.x == 0) {
-                    ph->flags = bad ? kPfBad : 0u;
-                    ph->cnt = 0;
-                    ph->vmax = ms;
-                    ph->sum = tot;
-                    if (fn.dw.owns()) { ph->ly = wsl[0]; ph->qy = fn.dw.qy; }
+                ok = consume_row<E>(P, seq, plan, tma, x0, fn);
+                if (ok) {
+                    // per warp: fold (m_t, s_t) into the warp's max and sum; then thread 0
+                    // folds the warps
+                    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+                    float wm = fn.m;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+                    const float sc = (fn.s > 0.f) ? fn.s * ex2((fn.m - wm) * A.c2) : 0.f;
+                    const double ws = warp_sum_d(static_cast<double>(sc));
+                    const uint32_t wb = __reduce_or_sync(0xffffffffu, fn.bad_flag());
+                    if (lane == 0) { sh.wm[w] = wm; sh.ws[w] = ws; sh.wb[w] = wb; }
+                    if (fn.dw.seen) wsl[0] = fn.dw.ly;
+                    csync();
+                    if (threadIdx.x == 0) {
+                        float ms = -kInf;
+                        uint32_t bad = 0;
+                        for (int j = 0; j < kWarps; ++j) { ms = fmaxf(ms, sh.wm[j]); bad |= sh.wb[j]; }
+                        double tot = 0.0;
+                        for (int j = 0; j < kWarps; ++j)
+                            if (sh.ws[j] > 0.0) tot += sh.ws[j] * static_cast<double>(ex2((sh.wm[j] - ms) * A.c2));
+                        ph->flags = bad ? kPfBad : 0u;
+                        ph->cnt = 0;
+                        ph->vmax = ms;
+                        ph->sum = tot;
+                        if (fn.dw.owns()) { ph->ly = wsl[0]; ph->qy = fn.dw.qy; }
+                    }
                 }
             }
         } else if (kind == kResid) {
@@ -664,31 +773,40 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
             fn.m = static_cast<float>(__ldcg(&rs->m));
             fn.c = A.c2;
             fn.invZ = static_cast<float>(1.0 / __ldcg(&rs->Z));
-            if (!consume_row2<E>(P, seq, plan, tma, x0, fn)) break;
-            const double rsum = block_sum_d(static_cast<double>(fn.r), sh.red);
-            const double psum = block_sum_d(static_cast<double>(fn.pw), sh.red);
-            if (threadIdx.x == 0) {
-                ph->flags = 0;
-                ph->sum = rsum;
-                ph->sum2 = psum;
+            ok = consume_row2<E>(P, seq, plan, tma, x0, fn);
+            if (ok) {
+                const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+                const double wr = warp_sum_d(static_cast<double>(fn.r));
+                const double wp = warp_sum_d(static_cast<double>(fn.pw));
+                if (lane == 0) { sh.ws[w] = wr; sh.ws2[w] = wp; }
+                csync();
+                if (threadIdx.x == 0) {
+                    double rsum = 0.0, psum = 0.0;
+                    for (int j = 0; j < kWarps; ++j) { rsum += sh.ws[j]; psum += sh.ws2[j]; }
+                    ph->flags = 0;
+                    ph->sum = rsum;
+                    ph->sum2 = psum;
+                }
             }
         }
+        if (!ok) break;
         SPEC_TRACE_EV(1, b, row, s, kind);
-        if (arrive(A.W, b, A.S, &sh.last)) {
-            SPEC_TRACE_EV(2, b, row, s, kind);
-            const int st = initial ? 0 : __ldcg(&A.W.req[b].status);
-            if (kind == kInvalid) {
-                chain_finish(A, b, 0, -1, 16);
-            } else if constexpr (kTopk) {
-                combine_topk<E>(A, sh, b, row, kind, st);
-            } else {
-                combine_full<E>(A, sh, b, row, kind, st);
-            }
-            csync();
-            SPEC_TRACE_EV(3, b, row, s, kind);
-        }
+        csync();   // every consumer's partial writes are ordered before the hand-over
+        Job j;
+        j.task = t; j.slice = s; j.kind = kind; j.stop = 0; j.flags = 0;
+        post_job(P, jseq, cseq, j, serve);
     }
+    // stop the combiner once it has taken every job (serving its last combines)
+    Job j;
+    j.task.b = 0; j.task.row = 0; j.task.kind = 0; j.task.aux = 0;
+    j.slice = 0; j.kind = 0; j.stop = 1; j.flags = 0;
+    post_job(P, jseq, cseq, j, serve);
+    // combines still in the combiner's queue are served until it stops
+    consumer_wait(P, cseq, [&]() { return mbar_test(&P.jempty[(jseq - 1) % kJobs], ((jseq - 1) / kJobs) & 1u); }, serve);
 }
+
+// two CTAs per SM (228 KiB of shared memory, 1 KiB reserved per CTA)
+static_assert(kStages * kChunkBytes + sizeof(ChainSmem<true>) <= 113 * 1024, "chain CTA too large for 2 per SM");
 
 template <class E, bool kTopk>
 static size_t chain_smem_bytes() {

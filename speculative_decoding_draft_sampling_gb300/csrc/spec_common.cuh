@@ -11,7 +11,9 @@ namespace spec {
 
 constexpr int kThreads = 256;                 // consumer threads of every engine CTA
 constexpr int kWarps = kThreads / 32;         // consumer warps
-constexpr int kBlockThreads = kThreads + 32;  // + one producer warp (warp kWarps)
+constexpr int kProducer = kThreads;           // the producer lane (warp kWarps, lane 0)
+constexpr int kCombiner0 = kThreads + 32;     // first thread of the combiner warp (warp kWarps + 1)
+constexpr int kBlockThreads = kThreads + 64;  // consumers + producer warp + combiner warp
 
 // Barrier among the consumer threads only (named barrier 1; the producer
 // warp never takes part), with the memory ordering of __syncthreads().
@@ -114,6 +116,16 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+// one non-blocking test of the phase with the given parity
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
 }
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
     unsigned long long t;
@@ -239,6 +251,32 @@ __device__ __forceinline__ uint32_t block_or(uint32_t v, uint32_t* red) {
     for (int i = 0; i < kWarps; ++i) r |= red[i];
     return r;
 }
+// warp-wide helpers (all 32 lanes)
+__device__ __forceinline__ double warp_exscan_d(double v, double& total) {
+    const int l = threadIdx.x & 31;
+    double inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (l >= o) inc += t;
+    }
+    total = __shfl_sync(0xffffffffu, inc, 31);
+    return inc - v;
+}
+__device__ __forceinline__ int warp_exscan_i(int v, int& total) {
+    const int l = threadIdx.x & 31;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (l >= o) inc += t;
+    }
+    total = __shfl_sync(0xffffffffu, inc, 31);
+    return inc - v;
+}
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) { return __reduce_max_sync(0xffffffffu, v); }
+__device__ __forceinline__ uint32_t warp_min_u32(uint32_t v) { return __reduce_min_sync(0xffffffffu, v); }
+
 // exclusive prefix sum (fp64) of one value per thread, in thread order; also
 // returns the block total.
 __device__ __forceinline__ double block_exscan_d(double v, double* red, double& total) {

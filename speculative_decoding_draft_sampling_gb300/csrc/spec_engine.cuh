@@ -68,6 +68,8 @@ __device__ __forceinline__ void trace_ev(int ev, int b, int row, int slice, int 
 }
 #define SPEC_TRACE_EV(ev, b, row, slice, aux) \
     do { if (threadIdx.x == 0) ::spec::trace_ev((ev), (b), (row), (slice), (aux)); } while (0)
+#define SPEC_TRACE_EVW(ev, b, row, slice, aux) \
+    do { if ((threadIdx.x & 31) == 0) ::spec::trace_ev((ev), (b), (row), (slice), (aux)); } while (0)
 #define SPEC_TRACE_EXPORT(name)                                                              \
     extern "C" int spec_trace_setup_##name(void* buf, unsigned cap) {                        \
         unsigned z = 0;                                                                      \
@@ -82,6 +84,7 @@ __device__ __forceinline__ void trace_ev(int ev, int b, int row, int slice, int 
     }
 #else
 #define SPEC_TRACE_EV(ev, b, row, slice, aux)
+#define SPEC_TRACE_EVW(ev, b, row, slice, aux)
 #define SPEC_TRACE_EXPORT(name)
 #endif
 
@@ -165,6 +168,7 @@ __device__ __forceinline__ uint64_t* part_keys(const Workspace& W, int b, int s,
     return reinterpret_cast<uint64_t*>(part_hdr(W, b, s, S) + 1);
 }
 
+
 // ---------------------------------------------------------------------------
 // queue
 // ---------------------------------------------------------------------------
@@ -212,28 +216,28 @@ __device__ inline Claimed claim_unit(const Workspace& W, int B, int S) {
     }
 }
 
-// Consumers: after the unit's partial is written.  Returns true (in every
-// consumer thread) in the CTA that completed the task's last slice; that CTA
-// owns the combine.
-__device__ __forceinline__ bool arrive(const Workspace& W, int b, int S, int* sh) {
-    csync();
-    if (threadIdx.x == 0) {
-        fence_acq_rel_gpu();   // release this CTA's partial
+// Combiner warp: count the arrival of a finished unit (its partial was
+// written by the consumers, ordered before the job hand-over).  Returns
+// true in every lane when the unit completed the task's last slice; this
+// CTA's combiner then owns the combine.
+__device__ __forceinline__ bool comb_arrive(const Workspace& W, int b, int S) {
+    int last = 0;
+    if ((threadIdx.x & 31) == 0) {
+        fence_acq_rel_gpu();   // release the partial (cumulative over the hand-over)
         const uint32_t prev = atomicAdd(&W.counter[b], 1u);
-        int last = (prev == static_cast<uint32_t>(S - 1));
+        last = (prev == static_cast<uint32_t>(S - 1));
         if (last) {
             fence_acq_rel_gpu();   // acquire the other slices' partials
-            W.counter[b] = 0;   // ready for the request's next task
+            W.counter[b] = 0;      // ready for the request's next task
         }
-        *sh = last;
     }
-    csync();
-    return *sh != 0;
+    return __shfl_sync(0xffffffffu, last, 0) != 0;
 }
 
-// Consumer thread 0 of the combining CTA: enqueue the request's next task.
+// Combiner lane 0: enqueue the request's next task.  The release store of
+// the ready flag orders every earlier write of this lane (the request state,
+// the task) before it.
 __device__ __forceinline__ void push_task(const Workspace& W, Task t) {
-    fence_acq_rel_gpu();
     const uint32_t ti = atomicAdd(&W.ctrl->tail, 1u);
     if (ti >= W.maxt) { atomicOr(&W.ctrl->error, kErrQueue); return; }
     __stcg(&W.tasks[ti].b, t.b);
@@ -243,16 +247,26 @@ __device__ __forceinline__ void push_task(const Workspace& W, Task t) {
     st_release(&W.ready[ti], 1u);
 }
 
-// Consumer thread 0 of the combining CTA, after the request's outputs are
-// written by all consumers (call after a csync()).
+// Combiner lane 0, after the request's outputs are written by the warp.
+// The count only tells claimers when to stop; the outputs are read after
+// the kernel.
 __device__ __forceinline__ void finish_request(const Workspace& W) {
-    fence_acq_rel_gpu();
     atomicAdd(&W.ctrl->done, 1u);
 }
 
 // ---------------------------------------------------------------------------
 // the producer / consumer pipeline of one CTA
 // ---------------------------------------------------------------------------
+// A finished unit handed from the consumers to the combiner warp.
+struct Job {
+    Task task;       // as claimed (kind -1: an initial task)
+    int slice;
+    int kind;        // the unit's resolved kind
+    int stop;        // no more jobs: the combiner leaves
+    uint32_t flags;  // kernel-specific
+};
+constexpr int kJobs = 4;
+
 // Warp kWarps (the producer) claims units, publishes each unit's descriptor
 // through a two-slot queue, and streams the unit's chunks HBM -> shared
 // memory with 1-D TMA bulk copies into a kStages ring.  The kWarps consumer
@@ -269,6 +283,12 @@ struct Pipe {
     uint64_t* ufull;       // [2] count 1: descriptor published
     uint64_t* uempty;      // [2] count kWarps: descriptor read
     Claimed* desc;         // [2]
+    uint64_t* jfull;       // [kJobs] count 1: job posted by consumer thread 0
+    uint64_t* jempty;      // [kJobs] count 1: job taken by the combiner
+    Job* jobs;             // [kJobs]
+    uint64_t* cready;
+    uint64_t* cdone;
+    volatile int* cflag;
     volatile int* abort;   // a wait timed out in this CTA
     __device__ __forceinline__ unsigned char* slot(int s) const { return buf + s * kChunkBytes; }
 };
@@ -279,9 +299,15 @@ struct PipeSmem {
     uint64_t empty[kStages];
     uint64_t ufull[2];
     uint64_t uempty[2];
+    uint64_t jfull[kJobs];
+    uint64_t jempty[kJobs];
+    uint64_t cready;       // count 1: the combiner prepared a combine for the consumers
+    uint64_t cdone;        // count 1: the consumers finished it
     Claimed desc[2];
+    Job jobs[kJobs];
     int abort;
-    int pad[3];
+    int cflag;             // consumer thread 0's poll result, broadcast
+    int pad[2];
 };
 
 // all kBlockThreads threads, once at kernel start
@@ -295,6 +321,12 @@ __device__ inline Pipe pipe_init(unsigned char* ring, PipeSmem& ps) {
             mbar_init(&ps.ufull[j], 1);
             mbar_init(&ps.uempty[j], kWarps);
         }
+        for (int j = 0; j < kJobs; ++j) {
+            mbar_init(&ps.jfull[j], 1);
+            mbar_init(&ps.jempty[j], 1);
+        }
+        mbar_init(&ps.cready, 1);
+        mbar_init(&ps.cdone, 1);
         ps.abort = 0;
         fence_mbar_init();
     }
@@ -303,6 +335,8 @@ __device__ inline Pipe pipe_init(unsigned char* ring, PipeSmem& ps) {
     P.buf = ring;
     P.full = ps.full; P.empty = ps.empty; P.ufull = ps.ufull; P.uempty = ps.uempty;
     P.desc = ps.desc;
+    P.jfull = ps.jfull; P.jempty = ps.jempty; P.jobs = ps.jobs;
+    P.cready = &ps.cready; P.cdone = &ps.cdone; P.cflag = &ps.cflag;
     P.abort = &ps.abort;
     return P;
 }
@@ -403,17 +437,99 @@ __device__ void producer_loop(const Workspace& W, int B, int S, const Pipe& P, b
     }
 }
 
+// Consumers (all threads): wait until thread 0's poll() reports done,
+// serving the combines the combiner warp prepares meanwhile (serve() runs
+// on every consumer thread; thread 0 then signals cdone).  `cseq` counts
+// the combines served.  Every wait is bounded; false on a timeout or abort.
+template <class Poll, class Serve>
+__device__ bool consumer_wait(const Pipe& P, uint32_t& cseq, Poll poll, Serve serve) {
+    unsigned long long t0 = 0;
+    uint32_t ns = 0;
+    for (uint32_t it = 0;; ++it) {
+        if (threadIdx.x == 0) {
+            int f = poll() ? 1 : 0;
+            if (mbar_test(P.cready, cseq & 1u)) f |= 2;
+            if (*P.abort) f |= 4;
+            if ((it & 63u) == 63u) {
+                const unsigned long long now = globaltimer_ns();
+                if (t0 == 0) t0 = now;
+                else if (now - t0 > kMbarLimitNs) f |= 4;
+            }
+            *P.cflag = f;
+        }
+        csync();
+        const int f = *P.cflag;
+        csync();   // every thread read the flag before thread 0 writes it again
+        if (f & 2) {
+            serve();
+            csync();
+            if (threadIdx.x == 0) mbar_arrive(P.cdone);
+            ++cseq;
+            ns = 0;
+        }
+        if (f & 1) return true;
+        if (f & 4) { if (threadIdx.x == 0) *P.abort = 1; return false; }
+        if (!(f & 2)) {
+            if (ns) nanosleep_ns(ns);
+            ns = ns ? (ns < 256 ? ns * 2 : ns) : 32;
+        }
+    }
+}
+
+// Combiner warp: hand the prepared combine number `cpub` to the consumers
+// and wait (bounded) until they finished it.
+__device__ inline bool publish_combine(const Pipe& P, uint32_t& cpub) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(P.cready);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(P.cdone, cpub & 1u));
+    ++cpub;
+    if (!ok) *P.abort = 1;
+    return ok;
+}
+
 // Consumers: the next unit's descriptor.  ok = 0 ends the consumer loop
 // (every request finished, the queue closed, or an abort).
-__device__ __forceinline__ Claimed next_unit(const Pipe& P, uint32_t u) {
+template <class Serve>
+__device__ __forceinline__ Claimed next_unit(const Pipe& P, uint32_t u, uint32_t& cseq, Serve serve) {
     const int j = u & 1;
-    const bool got = mbar_wait(&P.ufull[j], (u >> 1) & 1u);
+    const bool got = consumer_wait(P, cseq, [&]() { return mbar_test(&P.ufull[j], (u >> 1) & 1u); }, serve);
     Claimed c = P.desc[j];
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(&P.uempty[j]);
-    if (!got) *P.abort = 1;
-    if (csync_or(!got || *P.abort)) c.ok = 0;
+    if (!got || *P.abort) c.ok = 0;
     return c;
+}
+
+// Consumers (all threads): hand a finished unit (or the stop job) to the
+// combiner warp, after a csync() that ordered every consumer's partial
+// writes before it.  `jseq` counts the jobs posted so far.
+template <class Serve>
+__device__ inline void post_job(const Pipe& P, uint32_t& jseq, uint32_t& cseq, const Job& j, Serve serve) {
+    const int s = static_cast<int>(jseq % kJobs);
+    const uint32_t par = ((jseq / kJobs) - 1) & 1u;
+    const bool ok = consumer_wait(P, cseq, [&]() {
+        if (jseq >= static_cast<uint32_t>(kJobs) && !mbar_test(&P.jempty[s], par)) return false;
+        P.jobs[s] = j;
+        mbar_arrive(&P.jfull[s]);
+        return true;
+    }, serve);
+    if (ok) ++jseq;
+}
+
+// The combiner warp's loop: take jobs in order until the stop job (or a
+// timed-out wait).  on_job(job) runs on all 32 lanes.
+template <class F>
+__device__ void combiner_loop(const Pipe& P, F on_job) {
+    for (uint32_t j = 0;; ++j) {
+        const int s = static_cast<int>(j % kJobs);
+        const bool got = __all_sync(0xffffffffu, mbar_wait(&P.jfull[s], (j / kJobs) & 1u));
+        const Job job = P.jobs[s];
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&P.jempty[s]);
+        if (!got) { *P.abort = 1; return; }
+        if (job.stop) return;
+        on_job(job);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -665,7 +781,7 @@ __device__ int cta_icdf(int x0, int x1, double t, W& w, double* red, int* ired) 
     return last_pos >= 0 ? last_pos : x0;
 }
 
-// Every slice header of a task, in shared memory (loaded in parallel).
+// Every slice header of a task, in shared memory.
 struct SliceHdrs {
     int cnt[kMaxSlices];
     int off[kMaxSlices + 1];     // exclusive prefix of cnt
@@ -678,64 +794,226 @@ struct SliceHdrs {
     float qy[kMaxSlices];
 };
 
-__device__ inline void load_hdrs(const Workspace& W, int b, int S, SliceHdrs& H) {
-    for (int s = threadIdx.x; s < S; s += kThreads) {
-        const PartHdr* h = part_hdr(W, b, s, S);
-        H.cnt[s] = __ldcg(&h->cnt);
-        H.flags[s] = __ldcg(&h->flags);
-        H.vmax[s] = __ldcg(&h->vmax);
-        H.kth[s] = __ldcg(&h->kth);
-        H.sum[s] = __ldcg(&h->sum);
-        H.sum2[s] = __ldcg(&h->sum2);
-        H.ly[s] = __ldcg(&h->ly);
-        H.qy[s] = __ldcg(&h->qy);
+// Combiner warp: lane s loads slice s's header (one round trip), offsets by
+// a warp scan.
+__device__ inline void load_hdrs_w(const Workspace& W, int b, int S, SliceHdrs& H) {
+    const int l = threadIdx.x & 31;
+    int c = 0;
+    if (l < S) {
+        const PartHdr* h = part_hdr(W, b, l, S);
+        c = __ldcg(&h->cnt);
+        H.cnt[l] = c;
+        H.flags[l] = __ldcg(&h->flags);
+        H.vmax[l] = __ldcg(&h->vmax);
+        H.kth[l] = __ldcg(&h->kth);
+        H.sum[l] = __ldcg(&h->sum);
+        H.sum2[l] = __ldcg(&h->sum2);
+        H.ly[l] = __ldcg(&h->ly);
+        H.qy[l] = __ldcg(&h->qy);
     }
-    csync();
-    if (threadIdx.x == 0) {
-        int a = 0;
-        for (int s = 0; s < S; ++s) { H.off[s] = a; a += H.cnt[s]; }
-        H.off[S] = a;
-    }
-    csync();
+    int tot;
+    const int off = warp_exscan_i(c, tot);
+    if (l < S) H.off[l] = off;
+    if (l == 0) H.off[S] = tot;
+    __syncwarp();
 }
 
-// Gather every slice key that `keep(key)` accepts into list[0..*lcnt)
-// (order arbitrary); keys beyond `cap` set *oflow.  All loads independent.
+// Combiner warp: every slice key that keep(key) accepts into list[0..return)
+// (order arbitrary); `oflow` when more than cap were accepted.  Each lane
+// loads 8 keys per pass, all independent.
 template <class F>
-__device__ inline void gather_keys(const Workspace& W, int b, int S, const SliceHdrs& H, F keep,
-                                   uint64_t* list, int cap, int* lcnt, int* oflow) {
-    if (threadIdx.x == 0) { *lcnt = 0; *oflow = 0; }
-    csync();
+__device__ inline int gather_keys_w(const Workspace& W, int b, int S, const SliceHdrs& H, F keep,
+                                    uint64_t* list, int cap, bool& oflow) {
+    constexpr int U = 8;
+    const int l = threadIdx.x & 31;
+    const uint32_t lt = (1u << l) - 1u;
     const int total = H.off[S];
-    const int lane = threadIdx.x & 31;
-    for (int f0 = 0; f0 < total; f0 += kThreads * 4) {
-        uint64_t key[4];
+    int out = 0;
+    int s = 0;   // slice of this lane's current key (its keys come in increasing order)
+    for (int f0 = 0; f0 < total; f0 += 32 * U) {
+        uint64_t key[U];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int f = f0 + j * kThreads + threadIdx.x;
+        for (int j = 0; j < U; ++j) {
+            const int f = f0 + j * 32 + l;
             key[j] = 0;
             if (f < total) {
-                int s = 0;
                 while (s + 1 < S && H.off[s + 1] <= f) ++s;
                 key[j] = __ldcg(part_keys(W, b, s, S) + (f - H.off[s]));
             }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int f = f0 + j * kThreads + threadIdx.x;
+        for (int j = 0; j < U; ++j) {
+            const int f = f0 + j * 32 + l;
             const bool p = f < total && keep(key[j]);
             const uint32_t bal = __ballot_sync(0xffffffffu, p);
-            int base = 0;
-            if (lane == 0 && bal) base = atomicAdd(lcnt, __popc(bal));
-            base = __shfl_sync(0xffffffffu, base, 0);
             if (p) {
-                const int pos = base + __popc(bal & ((1u << lane) - 1u));
+                const int pos = out + __popc(bal & lt);
                 if (pos < cap) list[pos] = key[j];
-                else *oflow = 1;
+            }
+            out += __popc(bal);
+        }
+    }
+    oflow = out > cap;
+    __syncwarp();
+    return out < cap ? out : cap;
+}
+
+// Combiner warp: every key of every slice into list[H.off[s] ..] (lane s
+// copies slice s; its loads are independent, 8 in flight).  Returns the
+// count (at most cap; `oflow` when more).
+__device__ inline int gather_all_w(const Workspace& W, int b, int S, const SliceHdrs& H, uint64_t* list,
+                                   int cap, bool& oflow) {
+    const int l = threadIdx.x & 31;
+    const int total = H.off[S];
+    oflow = total > cap;
+    if (l < S) {
+        const int c = H.cnt[l], o = H.off[l];
+        const uint64_t* src = part_keys(W, b, l, S);
+        for (int j0 = 0; j0 < c; j0 += 8) {
+            uint64_t key[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) key[j] = (j0 + j < c) ? __ldcg(src + j0 + j) : 0ull;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j0 + j < c && o + j0 + j < cap) list[o + j0 + j] = key[j];
+        }
+    }
+    __syncwarp();
+    return total < cap ? total : cap;
+}
+
+// Combiner warp: keep list[i] with value key >= t, in place, order kept.
+__device__ inline int compact_w(uint64_t* list, int n, uint32_t t) {
+    const int l = threadIdx.x & 31;
+    const uint32_t lt = (1u << l) - 1u;
+    int out = 0;
+    for (int i0 = 0; i0 < n; i0 += 32) {
+        const int i = i0 + l;
+        uint64_t key = 0;
+        bool p = false;
+        if (i < n) { key = list[i]; p = static_cast<uint32_t>(key >> 32) >= t; }
+        const uint32_t bal = __ballot_sync(0xffffffffu, p);
+        if (p) list[out + __popc(bal & lt)] = key;
+        out += __popc(bal);
+    }
+    __syncwarp();
+    return out;
+}
+
+// Combiner warp: the value key of the k-th largest key of list[0..n)
+// (n >= k), by bisection over value keys (one warp reduction a step).
+__device__ inline uint32_t kth_value_w(const uint64_t* list, int n, int k) {
+    const int l = threadIdx.x & 31;
+    uint32_t mx = 0;
+    for (int i = l; i < n; i += 32) mx = max(mx, static_cast<uint32_t>(list[i] >> 32));
+    uint32_t lo = 0, hi = warp_max_u32(mx);
+    while (lo < hi) {
+        const uint32_t mid = lo + static_cast<uint32_t>((static_cast<uint64_t>(hi) - lo + 1) >> 1);
+        int c = 0;
+        for (int i = l; i < n; i += 32) c += static_cast<uint32_t>(list[i] >> 32) >= mid;
+        c = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(c)));
+        if (c >= k) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Combiner warp: the largest composite key t with at least k keys of
+// list[0..n) >= t (the exact k-th largest key; n >= k).
+__device__ inline uint64_t kth_key_w(const uint64_t* list, int n, int k) {
+    const int l = threadIdx.x & 31;
+    const uint32_t v = kth_value_w(list, n, k);
+    uint64_t lo = static_cast<uint64_t>(v) << 32, hi = lo | 0xffffffffull;
+    while (lo < hi) {
+        const uint64_t d = hi - lo;
+        const uint64_t mid = lo + (d >> 1) + (d & 1ull);
+        int c = 0;
+        for (int i = l; i < n; i += 32) c += list[i] >= mid;
+        c = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(c)));
+        if (c >= k) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Combiner warp: sum of w(x) over [x0, x1) (fp32 in blocks of 8, fp64 across).
+template <class Wt>
+__device__ double warp_range_sum(int x0, int x1, Wt& w) {
+    const int l = threadIdx.x & 31;
+    double acc = 0.0;
+    for (int b0 = x0 + l * 8; b0 < x1; b0 += 32 * 8) {
+        float part = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (b0 + j < x1) part += w(b0 + j);
+        acc += static_cast<double>(part);
+    }
+    return warp_sum_d(acc);
+}
+
+// Combiner warp: inverse CDF over non-negative weights w(x), x ascending in
+// [x0, x1): the smallest x with C(x) > t.  Two levels: every lane sums one
+// contiguous span, a warp scan finds the span where C crosses t, and the
+// warp splits that span again.  If rounding leaves no crossing, returns the
+// last x with w(x) > 0 (or x0).
+template <class Wt>
+__device__ int warp_icdf(int x0, int x1, double t, Wt& w) {
+    const int l = threadIdx.x & 31;
+    const int n = x1 - x0;
+    if (n <= 0) return x0;
+    int lo = x0, len = n;
+    double base = 0.0;
+    int last_pos = -1;
+    for (int level = 0; level < 2; ++level) {
+        const int span = (len + 31) / 32;
+        const int a = lo + l * span, e = min(lo + len, a + span);
+        double part = 0.0;
+        float blk = 0.f;
+        int lp = -1;
+        for (int x = a; x < e; ++x) {
+            const float wx = w(x);
+            if (wx > 0.f) lp = x;
+            blk += wx;
+            if (((x - a) & 7) == 7) { part += static_cast<double>(blk); blk = 0.f; }
+        }
+        part += static_cast<double>(blk);
+        double tot;
+        const double ex = warp_exscan_d(part, tot);
+        last_pos = max(last_pos, static_cast<int>(warp_max_u32(static_cast<uint32_t>(lp + 1))) - 1);
+        const bool cross = part > 0.0 && base + ex + part > t;
+        const uint32_t bal = __ballot_sync(0xffffffffu, cross);
+        if (!bal) return last_pos >= 0 ? last_pos : x0;
+        const int src = __ffs(bal) - 1;
+        base += __shfl_sync(0xffffffffu, ex, src);
+        lo = lo + src * span;
+        len = min(span, x0 + n - lo);
+        if (level == 1 || len <= 32) {
+            // one element per lane (len <= span <= 32 after the split)
+            if (len > 32) break;
+            const int x = lo + l;
+            const float wx = (l < len) ? w(x) : 0.f;
+            double tot2;
+            const double ex2v = warp_exscan_d(static_cast<double>(wx), tot2);
+            const bool c2 = wx > 0.f && base + ex2v + static_cast<double>(wx) > t;
+            const uint32_t b2 = __ballot_sync(0xffffffffu, c2);
+            if (b2) return lo + __ffs(b2) - 1;
+            const uint32_t bp = __ballot_sync(0xffffffffu, wx > 0.f);
+            return bp ? lo + 31 - __clz(bp) : (last_pos >= 0 ? last_pos : x0);
+        }
+    }
+    // a span longer than 32 after two levels (len > 32 * 32 * 32): scan it serially
+    double c = base;
+    int res = -1;
+    if (l == 0) {
+        for (int x = lo; x < lo + len; ++x) {
+            const float wx = w(x);
+            if (wx > 0.f) {
+                c += static_cast<double>(wx);
+                res = x;
+                if (c > t) break;
             }
         }
     }
-    csync();
+    res = __shfl_sync(0xffffffffu, res, 0);
+    return res >= 0 ? res : (last_pos >= 0 ? last_pos : x0);
 }
 
 }  // namespace spec

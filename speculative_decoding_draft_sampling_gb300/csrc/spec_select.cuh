@@ -330,6 +330,8 @@ struct TopkSmem {
     uint64_t slot[kSlots][kThreads];
     uint64_t pool[kThreads];
     uint64_t wthr[kWarps];
+    float wmax[kWarps];
+    int wn[kWarps];
     int hist[64];
     uint32_t scratch[kWarps + 2];
     uint64_t sh64[2];
@@ -574,24 +576,72 @@ struct TopkHistFn : FnHooks {
         nw = out;
         __syncwarp();
     }
+    // One-barrier finish, step 1 (per warp): the warp's candidate count,
+    // filter, flags (1: a region lost keys, 2: NaN / +inf seen) and max into
+    // shared memory.  The caller then csync()s and reads summary().
+    __device__ void publish() {
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+        lost |= nw > kRegion;
+        const uint32_t fl = (lost ? 1u : 0u) | (bad_max(vmx) ? 2u : 0u);
+        const uint32_t flw = __reduce_or_sync(0xffffffffu, fl);
+        float wm = vmx;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wm = max_nan(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+        if (lane == 0) {
+            S->wn[w] = nw < kRegion ? nw : kRegion;
+            S->wthr[w] = theta;
+            S->scratch[w] = flw;
+            S->wmax[w] = wm;
+        }
+    }
+    // step 2 (every consumer, after the csync): totals over the warps
+    __device__ void summary(int& tot, uint64_t& F, uint32_t& flags, float& vm) const {
+        tot = 0; F = 0; flags = 0; vm = -kInf;
+#pragma unroll
+        for (int j = 0; j < kWarps; ++j) {
+            tot += S->wn[j];
+            F = S->wthr[j] > F ? S->wthr[j] : F;
+            flags |= S->scratch[j];
+            vm = max_nan(vm, S->wmax[j]);
+        }
+    }
+    // step 3 (per warp): the warp's keys to dst at the warp's offset (the
+    // prefix of the warps' counts).  Keys below the slice filter F are kept
+    // too: a combine never counts them (it works at or above the largest
+    // filter of all slices).
+    __device__ void write_keys(uint64_t* dst) const {
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+        const uint64_t* reg = S->cand + w * kRegion;
+        int base = 0;
+        for (int j = 0; j < w; ++j) base += S->wn[j];
+        const int n = S->wn[w];
+        for (int j = lane; j < n; j += 32) __stcg(dst + base + j, reg[j]);
+    }
+
     // After the stream (all consumers): the candidates with key >= F (the
     // largest warp filter), compacted to S->cand[0..return).  `oflow` when a
-    // region lost keys, `bad` when the slice holds a NaN or +inf.
-    __device__ int finish(uint64_t& F, uint32_t& oflow, uint32_t& bad) {
+    // region lost keys, `bad` when the slice holds a NaN or +inf, `vm` the
+    // slice maximum (NaN-propagating).
+    __device__ int finish(uint64_t& F, uint32_t& oflow, uint32_t& bad, float& vm) {
         constexpr int kPer = kRegion / 32;
         const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
         const uint32_t lt = (1u << lane) - 1u;
         lost |= nw > kRegion;
         const uint32_t fl = (lost ? 1u : 0u) | (bad_max(vmx) ? 2u : 0u);
         const uint32_t flw = __reduce_or_sync(0xffffffffu, fl);
-        if (lane == 0) { S->wthr[w] = theta; S->scratch[w] = flw; }
+        float wm = vmx;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wm = max_nan(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+        if (lane == 0) { S->wthr[w] = theta; S->scratch[w] = flw; S->wmax[w] = wm; }
         csync();
         F = S->wthr[0];
         uint32_t fa = S->scratch[0];
+        vm = S->wmax[0];
 #pragma unroll
         for (int j = 1; j < kWarps; ++j) {
             F = S->wthr[j] > F ? S->wthr[j] : F;
             fa |= S->scratch[j];
+            vm = max_nan(vm, S->wmax[j]);
         }
         oflow = fa & 1u;
         bad = (fa >> 1) & 1u;

@@ -23,7 +23,6 @@
 
 namespace spec {
 
-constexpr int kBuildCap = kWarps * TopkSmem::kRegion;   // selected-list buffer (keys)
 
 struct Ent {                 // a frontier entry or an emitted node
     double Q;
@@ -39,18 +38,15 @@ struct EnumHdr {
 };
 
 struct __align__(16) BuildSmem {
-    TopkSmem tk;             // slice candidates; later the merged list and mask scratch
+    TopkSmem tk;             // slice candidates (consumers)
     PipeSmem pipe;
-    int last;
-    int lcnt;
-    int oflow;
     uint64_t sh64[4];
     double red[kWarps];
     int ired[kWarps + 4];
     int hist[64];
     uint32_t scratch[kWarps + 2];
-    EnumHdr eh;
-    SliceHdrs hdrs;
+    EnumHdr eh;              // combiner
+    SliceHdrs hdrs;          // combiner
 };
 
 // per-request extra scratch: [EnumHdr][lists L*M (tok,int) + (prob,float)][nodes N][pending 2N+2]
@@ -64,14 +60,17 @@ __host__ __device__ inline size_t build_pend_off(int N, int L) {
 size_t build_extra_bytes(int N, int L) {
     return (build_pend_off(N, L) + static_cast<size_t>(2 * N + 2) * sizeof(Ent) + 127) & ~static_cast<size_t>(127);
 }
-// dynamic shared memory beyond the ring and BuildSmem: scratch (depth lists,
-// gathered keys and their ranks) + nodes + pending
+// dynamic shared memory beyond the ring and BuildSmem, all the combiner's:
+// depth lists, gathered keys, ancestor-mask scratch, then nodes + pending
 constexpr int kBuildList = 2048;         // gathered keys in a combine
 __host__ __device__ inline size_t build_lists_bytes(int N, int L) {
     return (static_cast<size_t>(L) * (N - 1) * 8 + 15) & ~static_cast<size_t>(15);
 }
+__host__ __device__ inline size_t build_mask_off(int N, int L) {
+    return build_lists_bytes(N, L) + static_cast<size_t>(kBuildList) * 8;
+}
 __host__ __device__ inline size_t build_scr_bytes(int N, int L) {
-    return build_lists_bytes(N, L) + static_cast<size_t>(kBuildList) * 12;
+    return build_mask_off(N, L) + static_cast<size_t>(N) * ((N + 63) / 64) * 8;
 }
 static size_t build_enum_smem(int N, int L) {
     return build_scr_bytes(N, L) + static_cast<size_t>(3 * N + 2) * sizeof(Ent);
@@ -94,11 +93,12 @@ __device__ __forceinline__ void path_set(Ent& e, int d, int r) {
     }
 }
 
-// Exact top-M (value desc, index asc) of one q row, single CTA, by
-// bisection over composite keys; for rows whose slice candidate buffers
-// overflowed (adversarial value order).  Writes the keys (unordered) to
-// list[0..return).
-__device__ int build_fallback(const float* qrow, int V, int M, uint64_t* list, int* ired, int* lcnt) {
+// Exact top-M (value desc, index asc) of one q row by bisection over
+// composite keys, on the combiner warp; for rows whose slice candidate
+// buffers overflowed (adversarial value order).  Writes the keys
+// (unordered) to list[0..return).
+__device__ int build_fallback(const float* qrow, int V, int M, uint64_t* list) {
+    const int l = threadIdx.x & 31;
     uint64_t lo = 0, hi = ~0ull;
     if (V > M) {
         // invariant: count(key >= lo) >= M; the range halves every step
@@ -106,36 +106,40 @@ __device__ int build_fallback(const float* qrow, int V, int M, uint64_t* list, i
             const uint64_t d = hi - lo;
             const uint64_t mid = lo + (d >> 1) + (d & 1ull);
             int c = 0;
-            for (int x = threadIdx.x; x < V; x += kThreads) c += ckey(qrow[x], x) >= mid;
-            c = block_sum_i(c, ired);
+            for (int x = l; x < V; x += 32) c += ckey(qrow[x], x) >= mid;
+            c = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(c)));
             if (c >= M) lo = mid; else hi = mid - 1;
         }
     }
-    if (threadIdx.x == 0) *lcnt = 0;
-    csync();
-    for (int x = threadIdx.x; x < V; x += kThreads) {
-        const uint64_t key = ckey(qrow[x], x);
-        if (key >= lo) {
-            const int pos = atomicAdd(lcnt, 1);
+    const uint32_t lt = (1u << l) - 1u;
+    int out = 0;
+    for (int x0 = 0; x0 < V; x0 += 32) {
+        const int x = x0 + l;
+        uint64_t key = 0;
+        bool p = false;
+        if (x < V) { key = ckey(qrow[x], x); p = key >= lo; }
+        const uint32_t bal = __ballot_sync(0xffffffffu, p);
+        if (p) {
+            const int pos = out + __popc(bal & lt);
             if (pos < M) list[pos] = key;
         }
+        out += __popc(bal);
     }
-    csync();
-    const int n = *lcnt;
-    csync();
-    return n < M ? n : M;
+    __syncwarp();
+    return out < M ? out : M;
 }
 
-// Write the final tree of request b from shared memory (all threads).
-__device__ void build_finalize(const BuildArgs& A, BuildSmem& sh, const Ent* nodes, const int* ltok,
+// Write the final tree of request b from shared memory (combiner warp).
+__device__ void build_finalize(const BuildArgs& A, unsigned long long* msk, const Ent* nodes, const int* ltok,
                                int b, int count, int st) {
+    const int l = threadIdx.x & 31;
     const int N = A.N, M = A.M;
     const int W = (N + 63) / 64;
     int* tk = A.token + static_cast<long long>(b) * N;
     int* pr = A.parent + static_cast<long long>(b) * N;
     int* dp = A.depth + static_cast<long long>(b) * N;
     double* sc = A.score + static_cast<long long>(b) * N;
-    for (int n = threadIdx.x; n < N; n += kThreads) {
+    for (int n = l; n < N; n += 32) {
         if (n < count) {
             const Ent& e = nodes[n];
             tk[n] = n == 0 ? -1 : ltok[(e.depth - 1) * M + e.rank];
@@ -148,25 +152,182 @@ __device__ void build_finalize(const BuildArgs& A, BuildSmem& sh, const Ent* nod
     }
     // ancestor masks: mask[n] = mask[parent[n]] | bit n, parents first
     unsigned long long* mk = A.anc_mask + static_cast<long long>(b) * N * W;
-    unsigned long long* sm = reinterpret_cast<unsigned long long*>(sh.tk.cand);   // N*W <= 1024 words
-    if (threadIdx.x == 0) {
+    if (l == 0) {
         for (int n = 0; n < N; ++n) {
             for (int w = 0; w < W; ++w) {
                 unsigned long long v = 0;
-                if (n < count && nodes[n].parent >= 0) v = sm[nodes[n].parent * W + w];
+                if (n < count && nodes[n].parent >= 0) v = msk[nodes[n].parent * W + w];
                 if (n < count && w == n / 64) v |= 1ull << (n % 64);
-                sm[n * W + w] = v;
+                msk[n * W + w] = v;
             }
         }
     }
-    csync();
-    for (int i = threadIdx.x; i < N * W; i += kThreads) mk[i] = sm[i];
-    if (threadIdx.x == 0) {
+    __syncwarp();
+    for (int i = l; i < N * W; i += 32) mk[i] = msk[i];
+    if (l == 0) {
         A.num_nodes[b] = count;
         A.status[b] = st;
     }
-    csync();
-    if (threadIdx.x == 0) finish_request(A.W);
+    __syncwarp();
+    if (l == 0) finish_request(A.W);
+}
+
+// The combine of one depth row (combiner warp): merge the slice lists into
+// the depth's sorted top-M, then resume the best-first enumeration.
+__device__ void build_combine(const BuildArgs& A, BuildSmem& sh, unsigned char* scr, Ent* nodes, Ent* pend,
+                              const Job& job) {
+    const int l = threadIdx.x & 31;
+    const int N = A.N, M = A.M, L = A.L;
+    const int b = job.task.b;
+    const bool initial = job.task.kind < 0;
+    const int d = job.task.row + 1;
+    const bool trivial = job.kind != 0;
+    unsigned char* ex = A.W.extra + static_cast<size_t>(b) * A.W.extra_stride;
+    EnumHdr* gh = reinterpret_cast<EnumHdr*>(ex);
+    int* gl = reinterpret_cast<int*>(ex + build_lists_off());        // [L][M] (tok, prob bits)
+    Ent* gnodes = reinterpret_cast<Ent*>(ex + build_nodes_off(N, L));
+    Ent* gpend = reinterpret_cast<Ent*>(ex + build_pend_off(N, L));
+    const int LM = L * M;
+    int* ltok = reinterpret_cast<int*>(scr);
+    float* lprob = reinterpret_cast<float*>(scr + static_cast<size_t>(LM) * 4);
+    uint64_t* list = reinterpret_cast<uint64_t*>(scr + build_lists_bytes(N, L));
+    unsigned long long* msk = reinterpret_cast<unsigned long long*>(scr + build_mask_off(N, L));
+    EnumHdr& eh = sh.eh;
+    if (initial) {
+        if (l == 0) {
+            EnumHdr h{};
+            h.count = 1; h.npend = 0; h.want = 0; h.avail = 0; h.status = 0;
+            eh = h;
+            Ent root{};
+            root.Q = 1.0; root.depth = 0; root.parent = -1; root.rank = -1;
+            nodes[0] = root;
+        }
+    } else {
+        for (int i = l; i < static_cast<int>(sizeof(EnumHdr) / 4); i += 32)
+            reinterpret_cast<int*>(&eh)[i] = __ldcg(reinterpret_cast<const int*>(gh) + i);
+        __syncwarp();
+        const int nc = eh.count, np = eh.npend;
+        for (int i = l; i < nc * 5; i += 32)
+            reinterpret_cast<unsigned long long*>(nodes)[i] = __ldcg(reinterpret_cast<const unsigned long long*>(gnodes) + i);
+        for (int i = l; i < np * 5; i += 32)
+            reinterpret_cast<unsigned long long*>(pend)[i] = __ldcg(reinterpret_cast<const unsigned long long*>(gpend) + i);
+        for (int i = l; i < eh.avail * M; i += 32) {
+            ltok[i] = __ldcg(gl + 2 * i);
+            lprob[i] = __int_as_float(__ldcg(gl + 2 * i + 1));
+        }
+    }
+    __syncwarp();
+    if (!trivial) {
+        load_hdrs_w(A.W, b, A.S, sh.hdrs);
+        uint32_t flags = l < A.S ? sh.hdrs.flags[l] : 0u;
+        uint64_t theta = l < A.S ? sh.hdrs.kth[l] : 0ull;
+        flags = __reduce_or_sync(0xffffffffu, flags);
+        theta = warp_max_u64(theta);
+        int n = 0;
+        if (flags & kPfBad) {
+            n = 0;
+        } else if (flags & kPfOverflow) {
+            const float* qrow = A.q + static_cast<long long>(b) * A.q_bs + static_cast<long long>(d - 1) * A.q_rs;
+            n = build_fallback(qrow, A.V, M, list);
+        } else {
+            // every slice key at or above the largest slice filter, then the top M
+            bool of;
+            n = gather_keys_w(A.W, b, A.S, sh.hdrs, [&](uint64_t key) { return key >= theta; }, list, kBuildList, of);
+            if (n > M) {
+                const uint64_t kth = kth_key_w(list, n, M);
+                // keep the keys >= kth (exactly M: composite keys are unique)
+                const uint32_t lt = (1u << l) - 1u;
+                int out = 0;
+                for (int i0 = 0; i0 < n; i0 += 32) {
+                    const int i = i0 + l;
+                    uint64_t key = 0;
+                    bool p = false;
+                    if (i < n) { key = list[i]; p = key >= kth; }
+                    const uint32_t bal = __ballot_sync(0xffffffffu, p);
+                    if (p) list[out + __popc(bal & lt)] = key;
+                    out += __popc(bal);
+                }
+                __syncwarp();
+                n = out;
+            }
+        }
+        // the depth list in rank order (value desc, index asc)
+        for (int i = l; i < n; i += 32) {
+            const uint64_t key = list[i];
+            int r = 0;
+            for (int j = 0; j < n; ++j) r += list[j] > key;
+            const int o = (d - 1) * M + r;
+            ltok[o] = ckey_idx(key);
+            lprob[o] = ckey_val(key);
+            __stcg(gl + 2 * o, ckey_idx(key));
+            __stcg(gl + 2 * o + 1, __float_as_int(ckey_val(key)));
+        }
+        if (l == 0) {
+            eh.len[d] = n;
+            eh.avail = d;
+            if (flags & kPfBad) eh.status |= 1;
+        }
+        __syncwarp();
+    }
+    // ---- best-first enumeration (lane 0), resumable ----
+    int need = 0;
+    if (l == 0) {
+        int count = eh.count, np = eh.npend, want = eh.want;
+        while (count < N) {
+            if (want >= 0) {
+                const int dd = nodes[want].depth + 1;
+                if (dd <= L) {
+                    if (dd > eh.avail) { need = dd; break; }
+                    if (eh.len[dd] > 0) {
+                        Ent c = nodes[want];
+                        c.depth = dd; c.parent = want; c.rank = 0;
+                        path_set(c, dd, 0);
+                        c.Q = nodes[want].Q * static_cast<double>(lprob[(dd - 1) * M + 0]);
+                        pend[np++] = c;
+                    }
+                }
+                want = -1;
+            }
+            if (np == 0) break;
+            int best = 0;
+            for (int j = 1; j < np; ++j)
+                if (ent_before(pend[j], pend[best])) best = j;
+            const Ent c = pend[best];
+            pend[best] = pend[--np];
+            const int nid = count++;
+            nodes[nid] = c;
+            if (c.rank + 1 < eh.len[c.depth]) {
+                Ent s2 = c;
+                s2.rank = c.rank + 1;
+                path_set(s2, c.depth, c.rank + 1);
+                s2.Q = nodes[c.parent].Q * static_cast<double>(lprob[(c.depth - 1) * M + c.rank + 1]);
+                pend[np++] = s2;
+            }
+            want = nid;
+        }
+        eh.count = count; eh.npend = np; eh.want = want;
+    }
+    need = __shfl_sync(0xffffffffu, need, 0);
+    __syncwarp();
+    if (need == 0) {
+        build_finalize(A, msk, nodes, ltok, b, eh.count, eh.status);
+    } else {
+        // save the state and ask for depth `need`
+        const int nc = eh.count, np = eh.npend;
+        for (int i = l; i < nc * 5; i += 32)
+            __stcg(reinterpret_cast<unsigned long long*>(gnodes) + i, reinterpret_cast<const unsigned long long*>(nodes)[i]);
+        for (int i = l; i < np * 5; i += 32)
+            __stcg(reinterpret_cast<unsigned long long*>(gpend) + i, reinterpret_cast<const unsigned long long*>(pend)[i]);
+        for (int i = l; i < static_cast<int>(sizeof(EnumHdr) / 4); i += 32)
+            __stcg(reinterpret_cast<int*>(gh) + i, reinterpret_cast<const int*>(&eh)[i]);
+        __syncwarp();
+        if (l == 0) {
+            Task nt;
+            nt.b = b; nt.row = need - 1; nt.kind = 0; nt.aux = 0;
+            push_task(A.W, nt);
+        }
+    }
+    __syncwarp();
 }
 
 __global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs A) {
@@ -185,21 +346,27 @@ __global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs
         const float* qrow = A.q + static_cast<long long>(t.b) * A.q_bs + static_cast<long long>(t.row) * A.q_rs;
         return plan_single(qrow, 4, x0, x1);
     };
+    if (threadIdx.x >= kCombiner0) {
+        combiner_loop(P, [&](const Job& job) {
+            if (comb_arrive(A.W, job.task.b, A.S)) build_combine(A, sh, scr, nodes, pend, job);
+            __syncwarp();
+        });
+        return;
+    }
     if (threadIdx.x >= kThreads) {
-        if (threadIdx.x == kThreads)
+        if (threadIdx.x == kProducer)
             producer_loop(A.W, A.B, A.S, P, tma, [](Claimed&) {},
                           [&](const Claimed& c) { return plan(c.task, c.slice); });
         return;
     }
-    uint32_t seq = 0;
+    uint32_t seq = 0, jseq = 0, cseq = 0;
+    auto serve = []() {};   // every combine runs on the combiner warp
     for (uint32_t u = 0;; ++u) {
-        const Claimed cl = next_unit(P, u);
+        const Claimed cl = next_unit(P, u, cseq, serve);
         if (!cl.ok) break;
         const Task t = cl.task;
         const int s = cl.slice;
         const int b = t.b;
-        const bool initial = t.kind < 0;
-        const int d = t.row + 1;                 // depth of this row
         const bool trivial = trivial_of(t);
         PartHdr* ph = part_hdr(A.W, b, s, A.S);
         uint64_t* pk = part_keys(A.W, b, s, A.S);
@@ -210,19 +377,51 @@ __global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs
             if (!consume_row<F32>(P, seq, plan(t, s), tma, x0, fn)) break;
             uint64_t F;
             uint32_t oflow, bad;
-            int n = fn.finish(F, oflow, bad);
+            float vm;
+            int n = fn.finish(F, oflow, bad, vm);
             uint64_t* list = sh.tk.cand;
-            if (n > A.cap_p && !bad) {
-                // the slice's exact top-M (value desc, index asc); its M-th key is the filter
-                uint64_t* dst = reinterpret_cast<uint64_t*>(scr);
-                int* rank = reinterpret_cast<int*>(scr + static_cast<size_t>(A.cap_p) * 8);
-                uint64_t kth;
-                bool of2;
-                n = select_to(list, n, M, false, rank, dst, A.cap_p, kth, of2, sh.sh64, sh.ired);
-                F = kth;
-                list = dst;
+            if (n > A.cap_p && !bad && !oflow) {
+                // the slice's exact M-th key: a certified value bound, then the
+                // index bits within that value
+                // (repeated until it stops rising: then it is the exact M-th value)
+                for (int it = 0; it < 8 && n > A.cap_p; ++it) {
+                    bool cert;
+                    const uint32_t F2 = hist_bound_list(list, n, M, hkey(F), sh.hist, sh.scratch, cert);
+                    if (!(cert && F2 > hkey(F))) break;
+                    n = compact_list(list, n, F2, sh.ired);
+                    F = static_cast<uint64_t>(F2) << 32;
+                }
+                if (n > A.cap_p) {
+                    const uint64_t kth = composite_bound(
+                        [&](auto f) { for (int i = threadIdx.x; i < n; i += kThreads) f(list[i]); },
+                        M, F, sh.ired);
+                    // keep the keys >= kth (order kept)
+                    int out = 0;
+                    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+                    for (int i0 = 0; i0 < n; i0 += kThreads) {
+                        const int i = i0 + threadIdx.x;
+                        uint64_t key = 0;
+                        bool p = false;
+                        if (i < n) { key = list[i]; p = key >= kth; }
+                        const uint32_t bal = __ballot_sync(0xffffffffu, p);
+                        if (lane == 0) sh.ired[w] = __popc(bal);
+                        csync();
+                        int base = out, tot = 0;
+                        for (int j = 0; j < kWarps; ++j) {
+                            if (j < w) base += sh.ired[j];
+                            tot += sh.ired[j];
+                        }
+                        csync();
+                        if (p) list[base + __popc(bal & ((1u << lane) - 1u))] = key;
+                        out += tot;
+                        csync();
+                    }
+                    n = out;
+                    F = kth;
+                    if (n > A.cap_p) oflow = 1;
+                }
             }
-            if (bad) n = 0;
+            if (bad || oflow) n = 0;
             csync();
             for (int i = threadIdx.x; i < n; i += kThreads) __stcg(pk + i, list[i]);
             if (threadIdx.x == 0) {
@@ -231,159 +430,24 @@ __global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs
                 ph->kth = F;
             }
         }
-        if (!arrive(A.W, b, A.S, &sh.last)) continue;
-
-        // ---- combine: merge the slice lists into depth d's sorted top-M ----
-        unsigned char* ex = A.W.extra + static_cast<size_t>(b) * A.W.extra_stride;
-        EnumHdr* gh = reinterpret_cast<EnumHdr*>(ex);
-        int* gl = reinterpret_cast<int*>(ex + build_lists_off());        // [L][M] (tok, prob bits)
-        Ent* gnodes = reinterpret_cast<Ent*>(ex + build_nodes_off(N, L));
-        Ent* gpend = reinterpret_cast<Ent*>(ex + build_pend_off(N, L));
-        // depth lists at the front of the ring: tokens [L*M] then probabilities [L*M]
-        const int LM = L * M;
-        int* ltok = reinterpret_cast<int*>(scr);
-        float* lprob = reinterpret_cast<float*>(scr + static_cast<size_t>(LM) * 4);
-        if (initial) {
-            if (threadIdx.x == 0) {
-                EnumHdr h{};
-                h.count = 1; h.npend = 0; h.want = 0; h.avail = 0; h.status = 0;
-                sh.eh = h;
-            }
-        } else {
-            for (int i = threadIdx.x; i < static_cast<int>(sizeof(EnumHdr) / 4); i += kThreads)
-                reinterpret_cast<int*>(&sh.eh)[i] = __ldcg(reinterpret_cast<const int*>(gh) + i);
-        }
         csync();
-        EnumHdr& eh = sh.eh;
-        if (initial) {
-            if (threadIdx.x == 0) {
-                Ent root{};
-                root.Q = 1.0; root.depth = 0; root.parent = -1; root.rank = -1;
-                nodes[0] = root;
-            }
-        } else {
-            const int nc = eh.count, np = eh.npend;
-            for (int i = threadIdx.x; i < nc * 5; i += kThreads)
-                reinterpret_cast<unsigned long long*>(nodes)[i] = __ldcg(reinterpret_cast<const unsigned long long*>(gnodes) + i);
-            for (int i = threadIdx.x; i < np * 5; i += kThreads)
-                reinterpret_cast<unsigned long long*>(pend)[i] = __ldcg(reinterpret_cast<const unsigned long long*>(gpend) + i);
-            for (int i = threadIdx.x; i < eh.avail * M; i += kThreads) {
-                ltok[i] = __ldcg(gl + 2 * i);
-                lprob[i] = __int_as_float(__ldcg(gl + 2 * i + 1));
-            }
-        }
-        csync();
-        if (!trivial) {
-            load_hdrs(A.W, b, A.S, sh.hdrs);
-            uint32_t flags = 0;
-            uint64_t theta = 0;
-            for (int j = 0; j < A.S; ++j) {
-                flags |= sh.hdrs.flags[j];
-                theta = sh.hdrs.kth[j] > theta ? sh.hdrs.kth[j] : theta;
-            }
-            // gathered keys and their ranks in the rest of the ring
-            uint64_t* list = reinterpret_cast<uint64_t*>(scr + build_lists_bytes(N, L));
-            const int kList = kBuildList;
-            int* rank = reinterpret_cast<int*>(list + kList);
-            int n = 0;
-            if (flags & kPfBad) {
-                n = 0;
-            } else if (flags & kPfOverflow) {
-                const float* qrow = A.q + static_cast<long long>(b) * A.q_bs + static_cast<long long>(d - 1) * A.q_rs;
-                n = build_fallback(qrow, A.V, M, list, sh.ired, &sh.lcnt);
-            } else {
-                // every slice key at or above the largest slice filter, then the top M
-                gather_keys(A.W, b, A.S, sh.hdrs, [&](uint64_t key) { return key >= theta; }, list, kList,
-                            &sh.lcnt, &sh.oflow);
-                n = min(sh.lcnt, kList);
-            }
-            uint64_t kth;
-            bool of;
-            const int keep = (flags & kPfBad) ? 0
-                             : select_to(list, n, M, false, rank, sh.tk.cand, kBuildCap, kth, of, sh.sh64, sh.ired);
-            csync();
-            for (int i = threadIdx.x; i < keep; i += kThreads) {
-                const uint64_t key = sh.tk.cand[i];
-                ltok[(d - 1) * M + i] = ckey_idx(key);
-                lprob[(d - 1) * M + i] = ckey_val(key);
-                __stcg(gl + 2 * ((d - 1) * M + i), ckey_idx(key));
-                __stcg(gl + 2 * ((d - 1) * M + i) + 1, __float_as_int(ckey_val(key)));
-            }
-            if (threadIdx.x == 0) {
-                eh.len[d] = keep;
-                eh.avail = d;
-                if (flags & kPfBad) eh.status |= 1;
-            }
-            csync();
-        }
-        // ---- best-first enumeration (thread 0), resumable ----
-        if (threadIdx.x == 0) {
-            int count = eh.count, np = eh.npend, want = eh.want;
-            int need = 0;
-            while (count < N) {
-                if (want >= 0) {
-                    const int dd = nodes[want].depth + 1;
-                    if (dd <= L) {
-                        if (dd > eh.avail) { need = dd; break; }
-                        if (eh.len[dd] > 0) {
-                            Ent c = nodes[want];
-                            c.depth = dd; c.parent = want; c.rank = 0;
-                            path_set(c, dd, 0);
-                            c.Q = nodes[want].Q * static_cast<double>(lprob[(dd - 1) * M + 0]);
-                            pend[np++] = c;
-                        }
-                    }
-                    want = -1;
-                }
-                if (np == 0) break;
-                int best = 0;
-                for (int j = 1; j < np; ++j)
-                    if (ent_before(pend[j], pend[best])) best = j;
-                const Ent c = pend[best];
-                pend[best] = pend[--np];
-                const int nid = count++;
-                nodes[nid] = c;
-                if (c.rank + 1 < eh.len[c.depth]) {
-                    Ent s2 = c;
-                    s2.rank = c.rank + 1;
-                    path_set(s2, c.depth, c.rank + 1);
-                    s2.Q = nodes[c.parent].Q * static_cast<double>(lprob[(c.depth - 1) * M + c.rank + 1]);
-                    pend[np++] = s2;
-                }
-                want = nid;
-            }
-            eh.count = count; eh.npend = np; eh.want = want;
-            sh.ired[0] = need;
-        }
-        csync();
-        const int need = sh.ired[0];
-        if (need == 0) {
-            build_finalize(A, sh, nodes, ltok, b, eh.count, eh.status);
-        } else {
-            // save the state and ask for depth `need`
-            const int nc = eh.count, np = eh.npend;
-            for (int i = threadIdx.x; i < nc * 5; i += kThreads)
-                __stcg(reinterpret_cast<unsigned long long*>(gnodes) + i, reinterpret_cast<const unsigned long long*>(nodes)[i]);
-            for (int i = threadIdx.x; i < np * 5; i += kThreads)
-                __stcg(reinterpret_cast<unsigned long long*>(gpend) + i, reinterpret_cast<const unsigned long long*>(pend)[i]);
-            for (int i = threadIdx.x; i < static_cast<int>(sizeof(EnumHdr) / 4); i += kThreads)
-                __stcg(reinterpret_cast<int*>(gh) + i, reinterpret_cast<const int*>(&eh)[i]);
-            csync();
-            if (threadIdx.x == 0) {
-                Task nt;
-                nt.b = b; nt.row = need - 1; nt.kind = 0; nt.aux = 0;
-                push_task(A.W, nt);
-            }
-        }
-        csync();
+        Job j;
+        j.task = t; j.slice = s; j.kind = trivial ? 1 : 0; j.stop = 0; j.flags = 0;
+        post_job(P, jseq, cseq, j, serve);
     }
+    Job j;
+    j.task.b = 0; j.task.row = 0; j.task.kind = 0; j.task.aux = 0;
+    j.slice = 0; j.kind = 0; j.stop = 1; j.flags = 0;
+    post_job(P, jseq, cseq, j, serve);
 }
 
 // largest slice count whose candidate lists fit the combine's gather buffer
 int build_max_slices(int N, int L) {
     (void)L;
     const int M = N - 1;
-    const int s = M > 0 ? kBuildList / M : kMaxSlices;
+    // the combiner warp merges every slice's list: keep that under ~8 lists
+    int s = M > 0 ? kBuildList / M : kMaxSlices;
+    if (s > 8) s = 8;
     return s < 1 ? 1 : (s > kMaxSlices ? kMaxSlices : s);
 }
 

@@ -19,9 +19,8 @@ namespace spec {
 
 struct __align__(16) WalkSmem {
     PipeSmem pipe;
-    int last;
     uint64_t red[kWarps];
-    int ish[4];
+    uint32_t wb[kWarps];
 };
 
 template <class E>
@@ -32,39 +31,43 @@ __device__ __forceinline__ const void* walk_row(const WalkArgs& A, int b, int i,
     return static_cast<const unsigned char*>(A.logits) + r * E::kBytes;
 }
 
+// combiner warp
 __device__ void greedy_finish(const WalkArgs& A, int b, int n, int last, int st) {
     const int W = A.K + 1;
+    const int l = threadIdx.x & 31;
     int* out = A.out_tokens + static_cast<long long>(b) * W;
-    for (int i = threadIdx.x; i < W; i += kThreads) {
+    for (int i = l; i < W; i += 32) {
         int v = -1;
         if (i < n) v = A.draft[static_cast<long long>(b) * A.K + i];
         else if (i == n) v = last;
         out[i] = v;
     }
-    if (threadIdx.x == 0) {
+    if (l == 0) {
         A.num_accepted[b] = n;
         A.status[b] = st;
     }
-    csync();
-    if (threadIdx.x == 0) finish_request(A.W);
+    __syncwarp();
+    if (l == 0) finish_request(A.W);
 }
 
-// path_nodes[b][0..acc] and out_tokens[b][0..acc-1] were written on the way
+// combiner warp; path_nodes[b][0..acc] and out_tokens[b][0..acc-1] were
+// written on the way
 __device__ void tree_finish(const WalkArgs& A, int b, int acc, int last, int st) {
     const int W = A.L + 1;
+    const int l = threadIdx.x & 31;
     int* pn = A.path_nodes + static_cast<long long>(b) * W;
     int* ot = A.out_tokens + static_cast<long long>(b) * W;
-    for (int i = threadIdx.x; i < W; i += kThreads) {
+    for (int i = l; i < W; i += 32) {
         if (i > acc) { pn[i] = -1; ot[i] = -1; }
         if (i == acc) ot[i] = last;
     }
-    if (threadIdx.x == 0) {
+    if (l == 0) {
         pn[0] = 0;
         A.num_accepted[b] = acc;
         A.status[b] = st;
     }
-    csync();
-    if (threadIdx.x == 0) finish_request(A.W);
+    __syncwarp();
+    if (l == 0) finish_request(A.W);
 }
 
 template <class E, bool kTree>
@@ -72,6 +75,69 @@ __device__ __forceinline__ bool walk_invalid(const WalkArgs& A, const Task& t) {
     if (kTree || t.kind >= 0) return false;
     const int kb = A.k_per_req ? A.k_per_req[t.b] : A.K;
     return kb < 0 || kb > A.K;
+}
+
+// The combine of one row (combiner warp): argmax over the slice partials,
+// then the greedy decision or the tree step.
+template <class E, bool kTree>
+__device__ void walk_combine(const WalkArgs& A, const Job& job) {
+    const int l = threadIdx.x & 31;
+    const int b = job.task.b;
+    const int row = job.task.row;
+    const bool initial = job.task.kind < 0;
+    const int acc = initial ? 0 : job.task.aux;
+    int st = initial ? 0 : __ldcg(&A.W.req[b].status);
+    if (job.kind != 0) {   // invalid k
+        greedy_finish(A, b, 0, -1, 16);
+        return;
+    }
+    uint32_t flags = 0;
+    uint64_t best = 0;
+    for (int j = l; j < A.S; j += 32) {
+        const PartHdr* h = part_hdr(A.W, b, j, A.S);
+        flags |= __ldcg(&h->flags);
+        const uint64_t k = __ldcg(&h->kth);
+        best = k > best ? k : best;
+    }
+    flags = __reduce_or_sync(0xffffffffu, flags);
+    best = warp_max_u64(best);
+    const bool bad_row = (flags & kPfBad) || !(ckey_val(best) > -kInf);
+    const int am = ckey_idx(best);
+    if constexpr (!kTree) {
+        const int kb = A.k_per_req ? A.k_per_req[b] : A.K;
+        if (bad_row) { greedy_finish(A, b, row, -1, st | 1); return; }
+        if (row == kb) { greedy_finish(A, b, row, am, st); return; }
+        const int y = A.draft[static_cast<long long>(b) * A.K + row];
+        if (y < 0 || y >= A.V) st |= 8;
+        if (y != am) { greedy_finish(A, b, row, am, st); return; }
+        if (l == 0) {
+            __stcg(&A.W.req[b].status, st);
+            Task nt;
+            nt.b = b; nt.row = row + 1; nt.kind = 0; nt.aux = 0;
+            push_task(A.W, nt);
+        }
+    } else {
+        if (bad_row) { tree_finish(A, b, acc, -1, st | 1); return; }
+        // lowest child of `row` carrying the argmax token
+        int child = 0x7fffffff;
+        int nn = A.num_nodes[b];
+        nn = nn < A.N ? nn : A.N;
+        const int* par = A.parent + static_cast<long long>(b) * A.N;
+        const int* tok = A.token + static_cast<long long>(b) * A.N;
+        for (int c = l; c < nn; c += 32)
+            if (par[c] == row && tok[c] == am) child = min(child, c);
+        child = static_cast<int>(warp_min_u32(static_cast<uint32_t>(child)));
+        if (child == 0x7fffffff || acc >= A.L) { tree_finish(A, b, acc, am, st); return; }
+        if (l == 0) {
+            const int W = A.L + 1;
+            A.out_tokens[static_cast<long long>(b) * W + acc] = am;
+            A.path_nodes[static_cast<long long>(b) * W + acc + 1] = child;
+            __stcg(&A.W.req[b].status, st);
+            Task nt;
+            nt.b = b; nt.row = child; nt.kind = 0; nt.aux = acc + 1;
+            push_task(A.W, nt);
+        }
+    }
 }
 
 template <class E, bool kTree>
@@ -85,91 +151,55 @@ __global__ void __launch_bounds__(kBlockThreads, 2) walk_kernel(const WalkArgs A
         const int x0 = slice * A.SL, x1 = min(A.V, x0 + A.SL);
         return plan_single(walk_row<E>(A, t.b, t.row, kTree), E::kBytes, x0, x1);
     };
+    if (threadIdx.x >= kCombiner0) {
+        combiner_loop(P, [&](const Job& job) {
+            if (comb_arrive(A.W, job.task.b, A.S)) walk_combine<E, kTree>(A, job);
+            __syncwarp();
+        });
+        return;
+    }
     if (threadIdx.x >= kThreads) {
-        if (threadIdx.x == kThreads)
+        if (threadIdx.x == kProducer)
             producer_loop(A.W, A.B, A.S, P, tma, [](Claimed&) {},
                           [&](const Claimed& c) { return plan(c.task, c.slice); });
         return;
     }
-    uint32_t seq = 0;
+    uint32_t seq = 0, jseq = 0, cseq = 0;
+    auto serve = []() {};   // every combine runs on the combiner warp
     for (uint32_t u = 0;; ++u) {
-        const Claimed cl = next_unit(P, u);
+        const Claimed cl = next_unit(P, u, cseq, serve);
         if (!cl.ok) break;
         const Task t = cl.task;
         const int s = cl.slice;
         const int b = t.b;
-        const bool initial = t.kind < 0;
-        const int row = t.row;              // greedy: position; tree: node id
-        const int acc = initial ? 0 : t.aux;
         const bool invalid = walk_invalid<E, kTree>(A, t);
         PartHdr* ph = part_hdr(A.W, b, s, A.S);
         if (!invalid) {
             const int x0 = s * A.SL;
             ArgmaxFn<E> fn;
             if (!consume_row<E>(P, seq, plan(t, s), tma, x0, fn)) break;
-            const uint64_t best = block_max_u64(fn.key(), sh.red);
-            const uint32_t bad = block_or(fn.bad_flag(), reinterpret_cast<uint32_t*>(sh.red));
+            // per warp, then thread 0 over the warps (one barrier)
+            const uint64_t wbest = warp_max_u64(fn.key());
+            const uint32_t wbad = __reduce_or_sync(0xffffffffu, fn.bad_flag());
+            if ((threadIdx.x & 31) == 0) { sh.red[threadIdx.x >> 5] = wbest; sh.wb[threadIdx.x >> 5] = wbad; }
+            csync();
             if (threadIdx.x == 0) {
+                uint64_t best = 0;
+                uint32_t bad = 0;
+                for (int j = 0; j < kWarps; ++j) { best = sh.red[j] > best ? sh.red[j] : best; bad |= sh.wb[j]; }
                 ph->flags = bad ? kPfBad : 0u;
                 ph->kth = best;
             }
         }
-        if (!arrive(A.W, b, A.S, &sh.last)) continue;
-        int st = initial ? 0 : __ldcg(&A.W.req[b].status);
-        if (invalid) {
-            greedy_finish(A, b, 0, -1, 16);
-            continue;
-        }
-        uint32_t flags = 0;
-        uint64_t best = 0;
-        for (int j = threadIdx.x; j < A.S; j += kThreads) {
-            const PartHdr* h = part_hdr(A.W, b, j, A.S);
-            flags |= __ldcg(&h->flags);
-            const uint64_t k = __ldcg(&h->kth);
-            best = k > best ? k : best;
-        }
-        flags = block_or(flags, reinterpret_cast<uint32_t*>(sh.red));
-        best = block_max_u64(best, sh.red);
-        const bool bad_row = (flags & kPfBad) || !(ckey_val(best) > -kInf);
-        const int am = ckey_idx(best);
-        if constexpr (!kTree) {
-            const int kb = A.k_per_req ? A.k_per_req[b] : A.K;
-            if (bad_row) { greedy_finish(A, b, row, -1, st | 1); continue; }
-            if (row == kb) { greedy_finish(A, b, row, am, st); continue; }
-            const int y = A.draft[static_cast<long long>(b) * A.K + row];
-            if (y < 0 || y >= A.V) st |= 8;
-            if (y != am) { greedy_finish(A, b, row, am, st); continue; }
-            if (threadIdx.x == 0) {
-                __stcg(&A.W.req[b].status, st);
-                Task nt;
-                nt.b = b; nt.row = row + 1; nt.kind = 0; nt.aux = 0;
-                push_task(A.W, nt);
-            }
-        } else {
-            if (bad_row) { tree_finish(A, b, acc, -1, st | 1); continue; }
-            // lowest child of `row` carrying the argmax token
-            int child = 0x7fffffff;
-            int nn = A.num_nodes[b];
-            nn = nn < A.N ? nn : A.N;
-            const int* par = A.parent + static_cast<long long>(b) * A.N;
-            const int* tok = A.token + static_cast<long long>(b) * A.N;
-            for (int c = threadIdx.x; c < nn; c += kThreads)
-                if (par[c] == row && tok[c] == am) child = min(child, c);
-            child = static_cast<int>(block_max_u64(~static_cast<uint64_t>(static_cast<uint32_t>(child)) & 0xffffffffull,
-                                                   sh.red) ^ 0xffffffffull);
-            if (child == 0x7fffffff || acc >= A.L) { tree_finish(A, b, acc, am, st); continue; }
-            if (threadIdx.x == 0) {
-                const int W = A.L + 1;
-                A.out_tokens[static_cast<long long>(b) * W + acc] = am;
-                A.path_nodes[static_cast<long long>(b) * W + acc + 1] = child;
-                __stcg(&A.W.req[b].status, st);
-                Task nt;
-                nt.b = b; nt.row = child; nt.kind = 0; nt.aux = acc + 1;
-                push_task(A.W, nt);
-            }
-        }
         csync();
+        Job j;
+        j.task = t; j.slice = s; j.kind = invalid ? 1 : 0; j.stop = 0; j.flags = 0;
+        post_job(P, jseq, cseq, j, serve);
     }
+    Job j;
+    j.task.b = 0; j.task.row = 0; j.task.kind = 0; j.task.aux = 0;
+    j.slice = 0; j.kind = 0; j.stop = 1; j.flags = 0;
+    post_job(P, jseq, cseq, j, serve);
 }
 
 static size_t walk_smem() { return kStages * kChunkBytes + sizeof(WalkSmem); }
