@@ -43,6 +43,40 @@ UNIT = "positions/s"
 FALLBACK_HBM_GBS = 6800.0
 
 
+def kernel_source_hash():
+    """Hash of the library's kernel and header sources (ties a profile to the code it measured)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    pkg = os.path.join(ROOT, "speculative_decoding_draft_sampling_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(pkg, "*.cu")) + glob.glob(os.path.join(pkg, "*.cuh"))
+                   + glob.glob(os.path.join(ROOT, "include", "*.h")))
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, algorithmic_bytes):
+    """DRAM bytes per launch from the committed ncu summary of the same kernel
+    sources (scaled from its captured case by the bytes read), else None."""
+    path = os.path.join(ROOT, "profiles", f"chain_kernel_{workload}_b64_full.md")
+    if not os.path.exists(path):
+        return None
+    sha = ratio = None
+    with open(path) as f:
+        for line in f:
+            t = line.strip()
+            if t.startswith("source_sha256:"):
+                sha = t.split(":", 1)[1].strip()
+            elif t.startswith("traffic_ratio:"):
+                ratio = float(t.split(":", 1)[1])
+    if sha != kernel_source_hash() or ratio is None:
+        return None
+    return ratio * algorithmic_bytes
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -424,7 +458,7 @@ def main():
                     ms_per_step=ms_per_step, higher_is_better=True, scaling="weak", vs_baseline=None,
                     dtype=case["dtype"], data="synthetic (seeded)", config=cfg,
                     roofline=dict(bound="hbm", achieved=achieved, peak=peak, unit="GB/s", frac=achieved / peak,
-                                  traffic=None, peak_kind=peak_kind),
+                                  traffic=profiled_traffic(args.workload, bytes_step), peak_kind=peak_kind),
                     cpu_baseline=cpu, e2e=e2e, gpu_launches=args.steps * (2 if args.workload in ("ddtree", "dspark") else 1),
                     clocks=clocks, wall_s=wall)
         print(json.dumps(line), flush=True)
