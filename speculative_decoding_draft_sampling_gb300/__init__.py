@@ -205,6 +205,8 @@ def verify_chain(logits, q, draft, uniforms, temperature: float, top_k: int = 0,
                           torch.full((B, K + 1, 4), float("nan"), dtype=torch.float32, device=dev) if diag else None,
                           None)
     need = L.spec_verify_chain_workspace_size(B, K, V, int(top_k))
+    if ws is None and out.ws is not None and out.ws.numel() >= need and out.ws.device == dev:
+        ws = out.ws   # a reused result keeps its workspace (and the filter hint kept in it)
     if ws is None:
         ws = workspace(need, dev)
     out.ws = ws

@@ -47,7 +47,7 @@ int sm_count() {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-    size_t off_ready, off_counter, zero_bytes, off_tasks, off_req, off_part, off_extra, total;
+    size_t off_ready, off_counter, zero_bytes, off_tasks, off_req, off_part, off_extra, off_persist, total;
     uint32_t maxt, part_stride;
     uint64_t extra_stride;
     int smax;
@@ -72,7 +72,8 @@ Layout make_layout(int B, long long maxt, int cap_p, size_t extra_per_req, int s
     L.part_stride = static_cast<uint32_t>(align_up(sizeof(spec::PartHdr) + 8ull * cap_p, 128));
     L.off_extra = align_up(L.off_part + static_cast<size_t>(B) * smax * L.part_stride, 256);
     L.extra_stride = align_up(extra_per_req, 256);
-    L.total = L.off_extra + static_cast<size_t>(B) * L.extra_stride;
+    L.off_persist = align_up(L.off_extra + static_cast<size_t>(B) * L.extra_stride, 128);
+    L.total = L.off_persist + 128;
     return L;
 }
 
@@ -86,6 +87,7 @@ spec::Workspace make_ws(void* ws, const Layout& L) {
     W.req = reinterpret_cast<spec::ReqState*>(p + L.off_req);
     W.part = p + L.off_part;
     W.extra = p + L.off_extra;
+    W.persist = reinterpret_cast<uint32_t*>(p + L.off_persist);
     W.part_stride = L.part_stride;
     W.maxt = L.maxt;
     W.extra_stride = L.extra_stride;
@@ -108,6 +110,20 @@ void choose_slices(int B, int V, int esize, int grid, int max_s, int& S, int& SL
         const int by_size = static_cast<int>((row_bytes + 32767) / 32768);
         if (s > by_size) s = by_size;
     }
+    if (s > max_s) s = max_s;
+    if (s > spec::kMaxSlices) s = spec::kMaxSlices;
+    if (s < 1) s = 1;
+    SL = static_cast<int>(align_up(static_cast<size_t>((V + s - 1) / s), 64));
+    S = (V + SL - 1) / SL;
+    if (S < 1) S = 1;
+}
+
+// Slices of a pushed row (one that follows an accepted row).  The same as
+// a first row's: finer slices shorten a row's stream but add per-unit costs
+// that measured as a net loss on the chain workloads.
+void choose_slices_pushed(int V, int esize, int S0, int max_s, int& S, int& SL) {
+    (void)esize;
+    int s = g_tune_slices > 0 ? g_tune_slices : S0;
     if (s > max_s) s = max_s;
     if (s > spec::kMaxSlices) s = spec::kMaxSlices;
     if (s < 1) s = 1;
@@ -226,9 +242,11 @@ spec_status spec_verify_chain(
     const int occ = spec::chain_occupancy((int)ldt, topk);
     if (occ < 1) return fail(SPEC_CUDA_ERROR, "spec_verify_chain: kernel does not fit on this device");
     int S, SL;
-    const int max_s = topk ? (4096 / (A.cap_p > 0 ? A.cap_p : 1)) : spec::kMaxSlices;
+    // the combine gathers every slice's keys into 2048 slots
+    const int max_s = topk ? (2048 / (A.cap_p > 0 ? A.cap_p : 1)) : spec::kMaxSlices;
     choose_slices(B, V, es, grid_for(occ, 1 << 30), max_s, S, SL);
     A.S = S; A.SL = SL;
+    choose_slices_pushed(V, es, S, max_s, A.S1, A.SL1);
     const int grid = grid_for(occ, B * S);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(ws, 0, Lw.zero_bytes, st);
@@ -284,6 +302,7 @@ spec_status spec_verify_greedy(
     int S, SL;
     choose_slices(B, V, es, grid_for(occ, 1 << 30), spec::kMaxSlices, S, SL);
     A.S = S; A.SL = SL;
+    choose_slices_pushed(V, es, S, spec::kMaxSlices, A.S1, A.SL1);
     const int grid = grid_for(occ, B * S);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(ws, 0, Lw.zero_bytes, st);
@@ -338,6 +357,7 @@ spec_status spec_tree_build(
     int S, SL;
     choose_slices(B, V, 4, grid_for(occ, 1 << 30), spec::build_max_slices(budget, L), S, SL);
     A.S = S; A.SL = SL;
+    choose_slices_pushed(V, 4, S, spec::build_max_slices(budget, L), A.S1, A.SL1);
     const int grid = grid_for(occ, B * S);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(ws, 0, Lw.zero_bytes, st);
@@ -390,6 +410,7 @@ spec_status spec_verify_tree(
     int S, SL;
     choose_slices(B, V, es, grid_for(occ, 1 << 30), spec::kMaxSlices, S, SL);
     A.S = S; A.SL = SL;
+    choose_slices_pushed(V, es, S, spec::kMaxSlices, A.S1, A.SL1);
     const int grid = grid_for(occ, B * S);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(ws, 0, Lw.zero_bytes, st);

@@ -38,6 +38,7 @@ struct CombPrep {
     int y;            // drafted token (VERIFY)
     int fallback;     // 1: a slice overflowed; take the exact path
     int hinted;       // a slice streamed behind a hint
+    int sl;           // slice length of the row
     float vmax;
     float pad;
     uint64_t theta;   // largest slice filter
@@ -212,9 +213,9 @@ __device__ __forceinline__ uint32_t next_hint(float tau, float m) {
 // slice key -- into shared memory for the consumers.  Returns false when the
 // combine ended here (a bad row).
 template <class E>
-__device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st) {
+__device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st, bool initial) {
     const int l = threadIdx.x & 31;
-    const int S = A.S;
+    const int S = task_slices(A, initial);
     const int kb = chain_k(A, b);
     const double uk = static_cast<double>(chain_u(A, b, kb));
     const double ur = kind == kVerify ? static_cast<double>(chain_u(A, b, row)) : 0.0;
@@ -247,6 +248,7 @@ __device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, i
     if (l == 0) {
         CombPrep& p = cs.prep;
         p.b = b; p.row = row; p.kind = kind; p.st = st; p.n = n; p.y = y; p.fallback = fb;
+        p.sl = task_slen(A, initial);
         p.hinted = (flags & kPfHinted) ? 1 : 0;
         p.vmax = vmax; p.theta = theta; p.uk = uk; p.ur = ur;
     }
@@ -310,7 +312,16 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
     const double Z = block_sum_d(zpart, sh.red);
     const double invZ = 1.0 / Z;
     const uint32_t hint = next_hint(tau, m);
-    if (threadIdx.x == 0) __stcg(&A.W.ctrl->hint0, hint);
+    if (threadIdx.x == 0) {
+        __stcg(&A.W.ctrl->hint0, hint);
+        // for the next call's first rows: a wider margin (another call's rows
+        // may sit lower)
+        const float hw = tau - 0.5f * (m - tau);
+        __stcg(&A.W.persist[1], (hw == hw && hw > -kInf) ? fkey(hw) : 0u);
+        __stcg(&A.W.persist[2], static_cast<uint32_t>(A.V));
+        __stcg(&A.W.persist[3], static_cast<uint32_t>(A.top_k));
+        __stcg(&A.W.persist[0], kPersistTag);
+    }
 
     // weights of S sorted by token id (ascending)
     auto sort_by_token = [&](bool residual, const float* qrow, double& total) {
@@ -337,7 +348,7 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
         const int y = p.y;
         double py = 0.0, qy = 0.0;
         if (y >= 0 && y < A.V) {
-            const int sy = y / A.SL;
+            const int sy = y / p.sl;
             const float ly = cs.hdrs.ly[sy];
             qy = static_cast<double>(cs.hdrs.qy[sy]);
             if (fkey(ly) >= tau_key) py = static_cast<double>(ex2((ly - m) * c2)) * invZ;
@@ -472,9 +483,10 @@ __device__ __forceinline__ int find_slice_w(int S, double v, double t, double& b
 // Combiner warp: the combine of an untruncated row.  Returns true when a draw
 // needs a slice rescan, prepared in cs.prep for the consumers.
 template <class E>
-__device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st) {
+__device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st, bool initial) {
     const int l = threadIdx.x & 31;
-    const int S = A.S;
+    const int S = task_slices(A, initial);
+    const int SL = task_slen(A, initial);
     const int kb = chain_k(A, b);
     const double cd = static_cast<double>(A.c2);
     const double uk = static_cast<double>(chain_u(A, b, kb));
@@ -506,7 +518,7 @@ __device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, i
         if (l == 0) {
             CombPrep& p = cs.prep;
             p.b = b; p.row = row; p.kind = kind; p.st = st;
-            p.x0 = s * A.SL; p.x1 = min(A.V, p.x0 + A.SL); p.wmode = wmode;
+            p.x0 = s * SL; p.x1 = min(A.V, p.x0 + SL); p.wmode = wmode;
             p.m = m; p.invZf = static_cast<float>(1.0 / Z);
             p.t = t - before; p.Z = Z; p.R = R_mass;
         }
@@ -529,7 +541,7 @@ __device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, i
     if (kind == kVerify) {
         double py = 0.0, qy = 0.0;
         if (y >= 0 && y < A.V) {
-            const int sy = y / A.SL;
+            const int sy = y / SL;
             py = exp((static_cast<double>(H.ly[sy]) - m) / A.Td) / Z;
             qy = static_cast<double>(H.qy[sy]);
         }
@@ -557,7 +569,7 @@ __device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, i
     if (l == 0) {
         CombPrep& p = cs.prep;
         p.b = b; p.row = row; p.kind = kind; p.st = st;
-        p.x0 = s * A.SL; p.x1 = min(A.V, p.x0 + A.SL); p.wmode = 0;
+        p.x0 = s * SL; p.x1 = min(A.V, p.x0 + SL); p.wmode = 0;
         p.m = vmax; p.invZf = static_cast<float>(1.0 / Z);
         p.t = t - before; p.Z = Z; p.R = 0.0;
     }
@@ -609,7 +621,8 @@ __device__ __forceinline__ int chain_unit_kind(const ChainArgs& A, const Task& t
 }
 template <class E>
 __device__ __forceinline__ StreamPlan chain_plan(const ChainArgs& A, const Task& t, int kind, int slice) {
-    const int x0 = slice * A.SL, x1 = min(A.V, x0 + A.SL);
+    const int SL = task_slen(A, t.kind < 0);
+    const int x0 = slice * SL, x1 = min(A.V, x0 + SL);
     if (kind == kVerify || kind == kBonus) return plan_single(chain_lrow<E>(A, t.b, t.row), E::kBytes, x0, x1);
     if (kind == kResid) return plan_dual(chain_lrow<E>(A, t.b, t.row), E::kBytes, chain_qrow(A, t.b, t.row), x0, x1);
     return plan_none();
@@ -629,15 +642,16 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
         uint32_t cpub = 0;
         combiner_loop(P, [&](const Job& job) {
             const int b = job.task.b;
-            if (!comb_arrive(A.W, b, A.S)) return;
+            const bool initial = job.task.kind < 0;
+            if (!comb_arrive(A.W, b, task_slices(A, initial))) return;
             SPEC_TRACE_EVW(2, b, job.task.row, job.slice, job.kind);
             const int st = job.task.kind < 0 ? 0 : __ldcg(&A.W.req[b].status);
             if (job.kind == kInvalid) {
                 chain_finish(A, b, 0, -1, 16);
             } else if constexpr (kTopk) {
-                if (prepare_topk<E>(A, sh.comb, b, job.task.row, job.kind, st)) publish_combine(P, cpub);
+                if (prepare_topk<E>(A, sh.comb, b, job.task.row, job.kind, st, initial)) publish_combine(P, cpub);
             } else {
-                if (combine_full<E>(A, sh.comb, b, job.task.row, job.kind, st)) publish_combine(P, cpub);
+                if (combine_full<E>(A, sh.comb, b, job.task.row, job.kind, st, initial)) publish_combine(P, cpub);
             }
             __syncwarp();
             SPEC_TRACE_EVW(3, b, job.task.row, job.slice, job.kind);
@@ -646,9 +660,17 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
     }
     if (threadIdx.x >= kThreads) {
         if (threadIdx.x == kProducer) {
-            producer_loop(A.W, A.B, A.S, P, tma,
+            producer_loop(A.W, A.B, A.S, A.S1, P, tma,
                           [&](Claimed& c) {
-                              if (kTopk && c.task.kind < 0) c.hint = __ldcg(&A.W.ctrl->hint0);
+                              if (kTopk && c.task.kind < 0) {
+                                  // the latest finished row of this call, else of the previous call
+                                  // on this workspace
+                                  c.hint = __ldcg(&A.W.ctrl->hint0);
+                                  if (c.hint == 0 && __ldcg(&A.W.persist[0]) == kPersistTag &&
+                                      __ldcg(&A.W.persist[2]) == static_cast<uint32_t>(A.V) &&
+                                      __ldcg(&A.W.persist[3]) == static_cast<uint32_t>(A.top_k))
+                                      c.hint = __ldcg(&A.W.persist[1]);
+                              }
                           },
                           [&](const Claimed& c) {
                               return chain_plan<E>(A, c.task, chain_unit_kind<E>(A, c.task), c.slice);
@@ -674,7 +696,8 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
         const bool nohint = !initial && (t.kind & kNoHint);
         PartHdr* ph = part_hdr(A.W, b, s, A.S);
         uint64_t* pk = part_keys(A.W, b, s, A.S);
-        const int x0 = s * A.SL, x1 = min(A.V, x0 + A.SL);
+        const int SLt = task_slen(A, initial);
+        const int x0 = s * SLt, x1 = min(A.V, x0 + SLt);
         const StreamPlan plan = chain_plan<E>(A, t, kind, s);
         bool ok = true;
         if (kind == kVerify || kind == kBonus) {

@@ -25,7 +25,8 @@ struct ChainArgs {
     int* status;
     float* diag;
     Workspace W;
-    int S, SL, cap_p;
+    int S, SL, cap_p;              // slices of a first row and their length
+    int S1, SL1;                   // the same for a pushed row
     int tma_l, tma_q;
 };
 
@@ -45,7 +46,8 @@ struct WalkArgs {                  // greedy verify and tree walk
     int* num_accepted;
     int* status;
     Workspace W;
-    int S, SL;
+    int S, SL;                     // slices of a first row and their length
+    int S1, SL1;                   // the same for a pushed row
     int tma_l;
 };
 
@@ -61,9 +63,16 @@ struct BuildArgs {
     int* num_nodes;
     int* status;
     Workspace W;
-    int S, SL, cap_p;
+    int S, SL, cap_p;              // slices of a first row and their length
+    int S1, SL1;                   // the same for a pushed row
     int tma_q;
 };
+
+// slices of a task and their length: first rows (initial tasks) and pushed rows differ
+template <class Args>
+__device__ __forceinline__ int task_slices(const Args& A, bool initial) { return initial ? A.S : A.S1; }
+template <class Args>
+__device__ __forceinline__ int task_slen(const Args& A, bool initial) { return initial ? A.SL : A.SL1; }
 
 // chain
 cudaError_t chain_run(const ChainArgs& A, int grid, cudaStream_t st);

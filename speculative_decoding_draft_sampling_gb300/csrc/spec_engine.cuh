@@ -101,12 +101,15 @@ static_assert(kChunkBytes % 4096 == 0 && kStages >= 2, "ring geometry");
 constexpr int kMaxSlices = 32;
 
 enum : uint32_t { kErrWait = 1u, kErrQueue = 2u };
+constexpr uint32_t kPersistTag = 0x5e1ec7edu;
 
 // Queue control words, one 128-byte line per group so that the atomics on
 // `head` and `tail` do not serialise with the polling of `done` / `error`.
 struct Ctrl {
-    uint32_t head;     // next unit index to claim
+    uint32_t head;     // next initial unit to claim (the B*S0 units of the first rows)
     uint32_t pad0[31];
+    uint32_t head1;    // next pushed unit to claim (pushed task t owns units [t*S1, (t+1)*S1))
+    uint32_t pad4[31];
     uint32_t tail;     // pushed tasks
     uint32_t pad1[31];
     uint32_t done;     // finished requests
@@ -115,7 +118,7 @@ struct Ctrl {
     uint32_t hint0;    // top-k filter hint (value key) for first rows, from the latest finished row
     uint32_t pad3[31];
 };
-static_assert(sizeof(Ctrl) == 512, "Ctrl is four 128-byte lines");
+static_assert(sizeof(Ctrl) == 640, "Ctrl is five 128-byte lines");
 
 struct Task {
     int32_t b, row, kind, aux;
@@ -155,6 +158,9 @@ struct Workspace {
     ReqState* req;        // [B]
     unsigned char* part;  // [B][S] partials, part_stride bytes each
     unsigned char* extra; // [B] per-request op scratch, extra_stride bytes each
+    uint32_t* persist;    // 128 bytes kept across calls on the same workspace (not zeroed):
+                          // [0] = kPersistTag when [1] holds a top-k filter hint for rows
+                          // of vocabulary [2] and top-k [3]
     uint32_t part_stride;
     uint32_t maxt;
     uint64_t extra_stride;
@@ -180,23 +186,31 @@ struct Claimed {
     int pad;
 };
 
-// The producer's claim of the next unit (one thread).  Units [0, B*S) are
-// the initial tasks (kind = -1, row 0, one per request); unit u >= B*S
-// belongs to pushed task (u/S - B), whose ready flag it waits for, bounded.
-__device__ inline Claimed claim_unit(const Workspace& W, int B, int S) {
+// The producer's claim of the next unit (one thread).  First rows first
+// (the initial units: row 0 of every request, S0 slices each): every
+// request's chain starts as early as it can.  Then pushed tasks (rows that
+// follow an accepted row, residual passes, retries) in push order, S1
+// slices each; a claimer that finds none pushed yet takes the next pushed
+// unit and waits (bounded) for its task, or for every request to finish.
+// `cold` caches whether initial units may be left.
+__device__ inline Claimed claim_unit(const Workspace& W, int B, int S0, int S1, bool& cold) {
     Claimed c;
     c.ok = 1;
     c.hint = 0;
     c.pad = 0;
-    const uint32_t u = atomicAdd(&W.ctrl->head, 1u);
-    const uint32_t slot = u / static_cast<uint32_t>(S);
-    c.slice = static_cast<int>(u % static_cast<uint32_t>(S));
     c.task.b = 0; c.task.row = 0; c.task.kind = -1; c.task.aux = 0;
-    if (slot < static_cast<uint32_t>(B)) {
-        c.task.b = static_cast<int>(slot);
-        return c;
+    if (cold) {
+        const uint32_t u0 = atomicAdd(&W.ctrl->head, 1u);
+        if (u0 < static_cast<uint32_t>(B) * static_cast<uint32_t>(S0)) {
+            c.slice = static_cast<int>(u0 % static_cast<uint32_t>(S0));
+            c.task.b = static_cast<int>(u0 / static_cast<uint32_t>(S0));
+            return c;
+        }
+        cold = false;
     }
-    const uint32_t ti = slot - static_cast<uint32_t>(B);
+    const uint32_t u = atomicAdd(&W.ctrl->head1, 1u);
+    const uint32_t ti = u / static_cast<uint32_t>(S1);
+    c.slice = static_cast<int>(u % static_cast<uint32_t>(S1));
     if (ti >= W.maxt) { c.ok = 0; return c; }
     uint32_t ns = 32;
     SPEC_TRACE_EV(10, -1, -1, -1, static_cast<int>(ti));
@@ -396,9 +410,11 @@ __device__ __forceinline__ void issue_chunk(const Pipe& P, const StreamPlan& p, 
 // `plan(c)` returns the unit's StreamPlan (tma: issue the chunks; otherwise
 // the consumers copy them themselves).
 template <class Fetch, class PlanF>
-__device__ void producer_loop(const Workspace& W, int B, int S, const Pipe& P, bool tma, Fetch fetch, PlanF plan) {
+__device__ void producer_loop(const Workspace& W, int B, int S0, int S1, const Pipe& P, bool tma, Fetch fetch,
+                              PlanF plan) {
     uint32_t seq = 0;          // chunks issued so far (ring sequence number)
     bool dead = false;
+    bool cold = true;          // initial units may be left
     for (uint32_t u = 0;; ++u) {
         const int j = u & 1;
         if (u >= 2 && !mbar_wait(&P.uempty[j], ((u >> 1) - 1) & 1u)) dead = true;
@@ -407,7 +423,7 @@ __device__ void producer_loop(const Workspace& W, int B, int S, const Pipe& P, b
             c.ok = 0; c.slice = 0; c.hint = 0; c.pad = 0;
             c.task.b = 0; c.task.row = 0; c.task.kind = 0; c.task.aux = 0;
         } else {
-            c = claim_unit(W, B, S);
+            c = claim_unit(W, B, S0, S1, cold);
             if (c.ok) fetch(c);
         }
         P.desc[j] = c;

@@ -218,9 +218,10 @@ __device__ void build_combine(const BuildArgs& A, BuildSmem& sh, unsigned char* 
     }
     __syncwarp();
     if (!trivial) {
-        load_hdrs_w(A.W, b, A.S, sh.hdrs);
-        uint32_t flags = l < A.S ? sh.hdrs.flags[l] : 0u;
-        uint64_t theta = l < A.S ? sh.hdrs.kth[l] : 0ull;
+        const int S = task_slices(A, initial);
+        load_hdrs_w(A.W, b, S, sh.hdrs);
+        uint32_t flags = l < S ? sh.hdrs.flags[l] : 0u;
+        uint64_t theta = l < S ? sh.hdrs.kth[l] : 0ull;
         flags = __reduce_or_sync(0xffffffffu, flags);
         theta = warp_max_u64(theta);
         int n = 0;
@@ -232,7 +233,7 @@ __device__ void build_combine(const BuildArgs& A, BuildSmem& sh, unsigned char* 
         } else {
             // every slice key at or above the largest slice filter, then the top M
             bool of;
-            n = gather_keys_w(A.W, b, A.S, sh.hdrs, [&](uint64_t key) { return key >= theta; }, list, kBuildList, of);
+            n = gather_keys_w(A.W, b, S, sh.hdrs, [&](uint64_t key) { return key >= theta; }, list, kBuildList, of);
             if (n > M) {
                 const uint64_t kth = kth_key_w(list, n, M);
                 // keep the keys >= kth (exactly M: composite keys are unique)
@@ -342,20 +343,21 @@ __global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs
     auto trivial_of = [&](const Task& t) { return t.kind < 0 && (N <= 1 || L <= 0); };
     auto plan = [&](const Task& t, int slice) {
         if (trivial_of(t)) return plan_none();
-        const int x0 = slice * A.SL, x1 = min(A.V, x0 + A.SL);
+        const int SL = task_slen(A, t.kind < 0);
+        const int x0 = slice * SL, x1 = min(A.V, x0 + SL);
         const float* qrow = A.q + static_cast<long long>(t.b) * A.q_bs + static_cast<long long>(t.row) * A.q_rs;
         return plan_single(qrow, 4, x0, x1);
     };
     if (threadIdx.x >= kCombiner0) {
         combiner_loop(P, [&](const Job& job) {
-            if (comb_arrive(A.W, job.task.b, A.S)) build_combine(A, sh, scr, nodes, pend, job);
+            if (comb_arrive(A.W, job.task.b, task_slices(A, job.task.kind < 0))) build_combine(A, sh, scr, nodes, pend, job);
             __syncwarp();
         });
         return;
     }
     if (threadIdx.x >= kThreads) {
         if (threadIdx.x == kProducer)
-            producer_loop(A.W, A.B, A.S, P, tma, [](Claimed&) {},
+            producer_loop(A.W, A.B, A.S, A.S1, P, tma, [](Claimed&) {},
                           [&](const Claimed& c) { return plan(c.task, c.slice); });
         return;
     }
@@ -371,7 +373,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs
         PartHdr* ph = part_hdr(A.W, b, s, A.S);
         uint64_t* pk = part_keys(A.W, b, s, A.S);
         if (!trivial) {
-            const int x0 = s * A.SL;
+            const int x0 = s * task_slen(A, t.kind < 0);
             TopkHistFn<F32, false> fn;
             fn.init(&sh.tk, M, 0u);
             if (!consume_row<F32>(P, seq, plan(t, s), tma, x0, fn)) break;

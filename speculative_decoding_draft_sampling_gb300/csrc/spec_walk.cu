@@ -93,8 +93,9 @@ __device__ void walk_combine(const WalkArgs& A, const Job& job) {
     }
     uint32_t flags = 0;
     uint64_t best = 0;
-    for (int j = l; j < A.S; j += 32) {
-        const PartHdr* h = part_hdr(A.W, b, j, A.S);
+    const int S = task_slices(A, initial);
+    for (int j = l; j < S; j += 32) {
+        const PartHdr* h = part_hdr(A.W, b, j, S);
         flags |= __ldcg(&h->flags);
         const uint64_t k = __ldcg(&h->kth);
         best = k > best ? k : best;
@@ -148,19 +149,20 @@ __global__ void __launch_bounds__(kBlockThreads, 2) walk_kernel(const WalkArgs A
     const bool tma = A.tma_l != 0;
     auto plan = [&](const Task& t, int slice) {
         if (walk_invalid<E, kTree>(A, t)) return plan_none();
-        const int x0 = slice * A.SL, x1 = min(A.V, x0 + A.SL);
+        const int SL = task_slen(A, t.kind < 0);
+        const int x0 = slice * SL, x1 = min(A.V, x0 + SL);
         return plan_single(walk_row<E>(A, t.b, t.row, kTree), E::kBytes, x0, x1);
     };
     if (threadIdx.x >= kCombiner0) {
         combiner_loop(P, [&](const Job& job) {
-            if (comb_arrive(A.W, job.task.b, A.S)) walk_combine<E, kTree>(A, job);
+            if (comb_arrive(A.W, job.task.b, task_slices(A, job.task.kind < 0))) walk_combine<E, kTree>(A, job);
             __syncwarp();
         });
         return;
     }
     if (threadIdx.x >= kThreads) {
         if (threadIdx.x == kProducer)
-            producer_loop(A.W, A.B, A.S, P, tma, [](Claimed&) {},
+            producer_loop(A.W, A.B, A.S, A.S1, P, tma, [](Claimed&) {},
                           [&](const Claimed& c) { return plan(c.task, c.slice); });
         return;
     }
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) walk_kernel(const WalkArgs A
         const bool invalid = walk_invalid<E, kTree>(A, t);
         PartHdr* ph = part_hdr(A.W, b, s, A.S);
         if (!invalid) {
-            const int x0 = s * A.SL;
+            const int x0 = s * task_slen(A, t.kind < 0);
             ArgmaxFn<E> fn;
             if (!consume_row<E>(P, seq, plan(t, s), tma, x0, fn)) break;
             // per warp, then thread 0 over the warps (one barrier)
