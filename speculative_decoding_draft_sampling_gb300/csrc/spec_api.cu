@@ -48,7 +48,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
     size_t off_ready, off_counter, zero_bytes, off_tasks, off_req, off_part, off_extra, off_persist, total;
-    uint32_t maxt, part_stride;
+    uint32_t maxt, maxu, part_stride;
     uint64_t extra_stride;
     int smax;
 };
@@ -63,8 +63,9 @@ Layout make_layout(int B, long long maxt, int cap_p, size_t extra_per_req, int s
     Layout L{};
     L.maxt = static_cast<uint32_t>(maxt);
     L.smax = smax;
+    L.maxu = static_cast<uint32_t>(maxt * smax);   // a pushed task has at most smax slices
     L.off_ready = sizeof(spec::Ctrl);
-    L.off_counter = align_up(L.off_ready + 4ull * maxt, 16);
+    L.off_counter = align_up(L.off_ready + 4ull * L.maxu, 16);
     L.zero_bytes = align_up(L.off_counter + 4ull * B, 256);
     L.off_tasks = L.zero_bytes;
     L.off_req = align_up(L.off_tasks + sizeof(spec::Task) * maxt, 256);
@@ -81,7 +82,7 @@ spec::Workspace make_ws(void* ws, const Layout& L) {
     unsigned char* p = static_cast<unsigned char*>(ws);
     spec::Workspace W;
     W.ctrl = reinterpret_cast<spec::Ctrl*>(p);
-    W.ready = reinterpret_cast<uint32_t*>(p + L.off_ready);
+    W.urec = reinterpret_cast<uint32_t*>(p + L.off_ready);
     W.counter = reinterpret_cast<uint32_t*>(p + L.off_counter);
     W.tasks = reinterpret_cast<spec::Task*>(p + L.off_tasks);
     W.req = reinterpret_cast<spec::ReqState*>(p + L.off_req);
@@ -90,6 +91,7 @@ spec::Workspace make_ws(void* ws, const Layout& L) {
     W.persist = reinterpret_cast<uint32_t*>(p + L.off_persist);
     W.part_stride = L.part_stride;
     W.maxt = L.maxt;
+    W.maxu = L.maxu;
     W.extra_stride = L.extra_stride;
     W.smax = L.smax;
     return W;
@@ -110,20 +112,6 @@ void choose_slices(int B, int V, int esize, int grid, int max_s, int& S, int& SL
         const int by_size = static_cast<int>((row_bytes + 32767) / 32768);
         if (s > by_size) s = by_size;
     }
-    if (s > max_s) s = max_s;
-    if (s > spec::kMaxSlices) s = spec::kMaxSlices;
-    if (s < 1) s = 1;
-    SL = static_cast<int>(align_up(static_cast<size_t>((V + s - 1) / s), 64));
-    S = (V + SL - 1) / SL;
-    if (S < 1) S = 1;
-}
-
-// Slices of a pushed row (one that follows an accepted row).  The same as
-// a first row's: finer slices shorten a row's stream but add per-unit costs
-// that measured as a net loss on the chain workloads.
-void choose_slices_pushed(int V, int esize, int S0, int max_s, int& S, int& SL) {
-    (void)esize;
-    int s = g_tune_slices > 0 ? g_tune_slices : S0;
     if (s > max_s) s = max_s;
     if (s > spec::kMaxSlices) s = spec::kMaxSlices;
     if (s < 1) s = 1;
@@ -246,7 +234,7 @@ spec_status spec_verify_chain(
     const int max_s = topk ? (2048 / (A.cap_p > 0 ? A.cap_p : 1)) : spec::kMaxSlices;
     choose_slices(B, V, es, grid_for(occ, 1 << 30), max_s, S, SL);
     A.S = S; A.SL = SL;
-    choose_slices_pushed(V, es, S, max_s, A.S1, A.SL1);
+    A.S1 = max_s < max_slices_for(V) ? max_s : max_slices_for(V);
     const int grid = grid_for(occ, B * S);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(ws, 0, Lw.zero_bytes, st);
@@ -302,7 +290,7 @@ spec_status spec_verify_greedy(
     int S, SL;
     choose_slices(B, V, es, grid_for(occ, 1 << 30), spec::kMaxSlices, S, SL);
     A.S = S; A.SL = SL;
-    choose_slices_pushed(V, es, S, spec::kMaxSlices, A.S1, A.SL1);
+    A.S1 = max_slices_for(V);
     const int grid = grid_for(occ, B * S);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(ws, 0, Lw.zero_bytes, st);
@@ -357,7 +345,7 @@ spec_status spec_tree_build(
     int S, SL;
     choose_slices(B, V, 4, grid_for(occ, 1 << 30), spec::build_max_slices(budget, L), S, SL);
     A.S = S; A.SL = SL;
-    choose_slices_pushed(V, 4, S, spec::build_max_slices(budget, L), A.S1, A.SL1);
+    A.S1 = spec::build_max_slices(budget, L) < max_slices_for(V) ? spec::build_max_slices(budget, L) : max_slices_for(V);
     const int grid = grid_for(occ, B * S);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(ws, 0, Lw.zero_bytes, st);
@@ -410,7 +398,7 @@ spec_status spec_verify_tree(
     int S, SL;
     choose_slices(B, V, es, grid_for(occ, 1 << 30), spec::kMaxSlices, S, SL);
     A.S = S; A.SL = SL;
-    choose_slices_pushed(V, es, S, spec::kMaxSlices, A.S1, A.SL1);
+    A.S1 = max_slices_for(V);
     const int grid = grid_for(occ, B * S);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(ws, 0, Lw.zero_bytes, st);

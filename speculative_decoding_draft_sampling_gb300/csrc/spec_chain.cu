@@ -39,6 +39,7 @@ struct CombPrep {
     int fallback;     // 1: a slice overflowed; take the exact path
     int hinted;       // a slice streamed behind a hint
     int sl;           // slice length of the row
+    uint32_t done;    // finished requests when the row arrived (an estimate, for the next row's slicing)
     float vmax;
     float pad;
     uint64_t theta;   // largest slice filter
@@ -142,7 +143,7 @@ __device__ __forceinline__ void chain_diag(const ChainArgs& A, int b, int i, flo
 }
 
 // lane 0: push the request's next task after an accepted position
-__device__ void chain_advance(const ChainArgs& A, int b, int row, int kb, int st, uint32_t hint) {
+__device__ void chain_advance(const ChainArgs& A, int b, int row, int kb, int st, uint32_t hint, uint32_t done) {
     ReqState* rs = &A.W.req[b];
     __stcg(&rs->status, st);
     Task t;
@@ -150,7 +151,9 @@ __device__ void chain_advance(const ChainArgs& A, int b, int row, int kb, int st
     t.row = row + 1;
     t.kind = (row + 1 < kb) ? kVerify : kBonus;
     t.aux = static_cast<int>(hint);
-    push_task(A.W, t);
+    int S, SL;
+    pick_slices(A.B, A.V, A.S, A.S1, done, S, SL);
+    push_task(A.W, t, S, SL);
 }
 
 // acceptance of drafted y given p(y) and q(y): u < p/q (fp64)
@@ -213,9 +216,9 @@ __device__ __forceinline__ uint32_t next_hint(float tau, float m) {
 // slice key -- into shared memory for the consumers.  Returns false when the
 // combine ended here (a bad row).
 template <class E>
-__device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st, bool initial) {
+__device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st, int S, int SL,
+                             uint32_t done) {
     const int l = threadIdx.x & 31;
-    const int S = task_slices(A, initial);
     const int kb = chain_k(A, b);
     const double uk = static_cast<double>(chain_u(A, b, kb));
     const double ur = kind == kVerify ? static_cast<double>(chain_u(A, b, row)) : 0.0;
@@ -248,7 +251,8 @@ __device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, i
     if (l == 0) {
         CombPrep& p = cs.prep;
         p.b = b; p.row = row; p.kind = kind; p.st = st; p.n = n; p.y = y; p.fallback = fb;
-        p.sl = task_slen(A, initial);
+        p.sl = SL;
+        p.done = done;
         p.hinted = (flags & kPfHinted) ? 1 : 0;
         p.vmax = vmax; p.theta = theta; p.uk = uk; p.ur = ur;
     }
@@ -285,7 +289,9 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
                 __stcg(&A.W.req[b].status, st);
                 Task t;
                 t.b = b; t.row = row; t.kind = kind | kNoHint; t.aux = 0;
-                push_task(A.W, t);
+                int S, SL;
+                pick_slices(A.B, A.V, A.S, A.S1, p.done, S, SL);
+                push_task(A.W, t, S, SL);
             }
             return;
         }
@@ -357,7 +363,7 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
         if (acc) {
             if (threadIdx.x == 0) {
                 chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
-                chain_advance(A, b, row, kb, st, hint);
+                chain_advance(A, b, row, kb, st, hint, p.done);
             }
             return;
         }
@@ -430,7 +436,7 @@ __device__ void chain_fallback_cta(const ChainArgs& A, ChainSmem<true>& sh, int 
         if (chain_accept(A, y, py, qy, static_cast<double>(chain_u(A, b, row)), st)) {
             if (threadIdx.x == 0) {
                 chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
-                chain_advance(A, b, row, kb, st, 0u);
+                chain_advance(A, b, row, kb, st, 0u, sh.comb.prep.done);
             }
             return;
         }
@@ -483,10 +489,9 @@ __device__ __forceinline__ int find_slice_w(int S, double v, double t, double& b
 // Combiner warp: the combine of an untruncated row.  Returns true when a draw
 // needs a slice rescan, prepared in cs.prep for the consumers.
 template <class E>
-__device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st, bool initial) {
+__device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st, int S, int SL,
+                             uint32_t done) {
     const int l = threadIdx.x & 31;
-    const int S = task_slices(A, initial);
-    const int SL = task_slen(A, initial);
     const int kb = chain_k(A, b);
     const double cd = static_cast<double>(A.c2);
     const double uk = static_cast<double>(chain_u(A, b, kb));
@@ -548,7 +553,7 @@ __device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, i
         const bool acc = chain_accept(A, y, py, qy, ur, st);
         if (l == 0) chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
         if (acc) {
-            if (l == 0) chain_advance(A, b, row, kb, st, 0u);
+            if (l == 0) chain_advance(A, b, row, kb, st, 0u, done);
             return false;
         }
         if (l == 0) {
@@ -558,7 +563,9 @@ __device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, i
             __stcg(&rs->status, st);
             Task t;
             t.b = b; t.row = row; t.kind = kResid; t.aux = 0;
-            push_task(A.W, t);
+            int S1, SL1;
+            pick_slices(A.B, A.V, A.S, A.S1, done, S1, SL1);
+            push_task(A.W, t, S1, SL1);
         }
         return false;
     }
@@ -621,7 +628,7 @@ __device__ __forceinline__ int chain_unit_kind(const ChainArgs& A, const Task& t
 }
 template <class E>
 __device__ __forceinline__ StreamPlan chain_plan(const ChainArgs& A, const Task& t, int kind, int slice) {
-    const int SL = task_slen(A, t.kind < 0);
+    const int SL = task_SL(A, t);
     const int x0 = slice * SL, x1 = min(A.V, x0 + SL);
     if (kind == kVerify || kind == kBonus) return plan_single(chain_lrow<E>(A, t.b, t.row), E::kBytes, x0, x1);
     if (kind == kResid) return plan_dual(chain_lrow<E>(A, t.b, t.row), E::kBytes, chain_qrow(A, t.b, t.row), x0, x1);
@@ -642,16 +649,20 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
         uint32_t cpub = 0;
         combiner_loop(P, [&](const Job& job) {
             const int b = job.task.b;
-            const bool initial = job.task.kind < 0;
-            if (!comb_arrive(A.W, b, task_slices(A, initial))) return;
+            uint32_t done;
+            if (!comb_arrive(A.W, b, task_S(A, job.task), &done)) return;
             SPEC_TRACE_EVW(2, b, job.task.row, job.slice, job.kind);
             const int st = job.task.kind < 0 ? 0 : __ldcg(&A.W.req[b].status);
             if (job.kind == kInvalid) {
                 chain_finish(A, b, 0, -1, 16);
             } else if constexpr (kTopk) {
-                if (prepare_topk<E>(A, sh.comb, b, job.task.row, job.kind, st, initial)) publish_combine(P, cpub);
+                if (prepare_topk<E>(A, sh.comb, b, job.task.row, job.kind, st, task_S(A, job.task),
+                                    task_SL(A, job.task), done))
+                    publish_combine(P, cpub);
             } else {
-                if (combine_full<E>(A, sh.comb, b, job.task.row, job.kind, st, initial)) publish_combine(P, cpub);
+                if (combine_full<E>(A, sh.comb, b, job.task.row, job.kind, st, task_S(A, job.task),
+                                    task_SL(A, job.task), done))
+                    publish_combine(P, cpub);
             }
             __syncwarp();
             SPEC_TRACE_EVW(3, b, job.task.row, job.slice, job.kind);
@@ -660,7 +671,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
     }
     if (threadIdx.x >= kThreads) {
         if (threadIdx.x == kProducer) {
-            producer_loop(A.W, A.B, A.S, A.S1, P, tma,
+            producer_loop(A.W, A.B, A.S, P, tma,
                           [&](Claimed& c) {
                               if (kTopk && c.task.kind < 0) {
                                   // the latest finished row of this call, else of the previous call
@@ -696,7 +707,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
         const bool nohint = !initial && (t.kind & kNoHint);
         PartHdr* ph = part_hdr(A.W, b, s, A.S);
         uint64_t* pk = part_keys(A.W, b, s, A.S);
-        const int SLt = task_slen(A, initial);
+        const int SLt = task_SL(A, t);
         const int x0 = s * SLt, x1 = min(A.V, x0 + SLt);
         const StreamPlan plan = chain_plan<E>(A, t, kind, s);
         bool ok = true;

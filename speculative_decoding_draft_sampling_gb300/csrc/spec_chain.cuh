@@ -26,7 +26,7 @@ struct ChainArgs {
     float* diag;
     Workspace W;
     int S, SL, cap_p;              // slices of a first row and their length
-    int S1, SL1;                   // the same for a pushed row
+    int S1;                        // most slices of a pushed row
     int tma_l, tma_q;
 };
 
@@ -47,7 +47,7 @@ struct WalkArgs {                  // greedy verify and tree walk
     int* status;
     Workspace W;
     int S, SL;                     // slices of a first row and their length
-    int S1, SL1;                   // the same for a pushed row
+    int S1;                        // most slices of a pushed row
     int tma_l;
 };
 
@@ -64,15 +64,16 @@ struct BuildArgs {
     int* status;
     Workspace W;
     int S, SL, cap_p;              // slices of a first row and their length
-    int S1, SL1;                   // the same for a pushed row
+    int S1;                        // most slices of a pushed row
     int tma_q;
 };
 
-// slices of a task and their length: first rows (initial tasks) and pushed rows differ
+// slices of a task and their length: first rows take the call's, pushed
+// rows carry their own in the kind word
 template <class Args>
-__device__ __forceinline__ int task_slices(const Args& A, bool initial) { return initial ? A.S : A.S1; }
+__device__ __forceinline__ int task_S(const Args& A, const Task& t) { return t.kind < 0 ? A.S : task_kind_S(t.kind); }
 template <class Args>
-__device__ __forceinline__ int task_slen(const Args& A, bool initial) { return initial ? A.SL : A.SL1; }
+__device__ __forceinline__ int task_SL(const Args& A, const Task& t) { return t.kind < 0 ? A.SL : task_kind_SL(t.kind); }
 
 // chain
 cudaError_t chain_run(const ChainArgs& A, int grid, cudaStream_t st);

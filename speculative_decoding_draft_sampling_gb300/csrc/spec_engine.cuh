@@ -108,10 +108,10 @@ constexpr uint32_t kPersistTag = 0x5e1ec7edu;
 struct Ctrl {
     uint32_t head;     // next initial unit to claim (the B*S0 units of the first rows)
     uint32_t pad0[31];
-    uint32_t head1;    // next pushed unit to claim (pushed task t owns units [t*S1, (t+1)*S1))
+    uint32_t head1;    // next pushed unit to claim
     uint32_t pad4[31];
-    uint32_t tail;     // pushed tasks
-    uint32_t pad1[31];
+    unsigned long long tailc;   // (pushed tasks << 32) | pushed units
+    uint32_t pad1[30];
     uint32_t done;     // finished requests
     uint32_t error;    // kErr* bits
     uint32_t pad2[30];
@@ -123,6 +123,15 @@ static_assert(sizeof(Ctrl) == 640, "Ctrl is five 128-byte lines");
 struct Task {
     int32_t b, row, kind, aux;
 };
+// A pushed task's kind word: bits 0-7 the kernel's kind, 8-13 its slice
+// count, 14-31 its slice length / 64 (initial tasks have kind -1 and take
+// the call's first-row slicing).
+__host__ __device__ __forceinline__ int task_kind_base(int kind) { return kind & 0xff; }
+__host__ __device__ __forceinline__ int task_kind_pack(int base, int S, int SL) {
+    return (base & 0xff) | ((S & 63) << 8) | ((SL >> 6) << 14);
+}
+__host__ __device__ __forceinline__ int task_kind_S(int kind) { return (kind >> 8) & 63; }
+__host__ __device__ __forceinline__ int task_kind_SL(int kind) { return ((kind >> 14) & 0x3ffff) << 6; }
 
 struct ReqState {
     double m;          // row maximum (logit), carried to a residual pass
@@ -152,7 +161,7 @@ enum : uint32_t { kPfBad = 1u, kPfOverflow = 2u, kPfHinted = 4u };
 // Device view of the caller's workspace; offsets computed on the host.
 struct Workspace {
     Ctrl* ctrl;
-    uint32_t* ready;      // [maxt] ready flags of pushed tasks (zeroed per call)
+    uint32_t* urec;       // [maxu] pushed units: ((task + 1) << 6) | slice once pushed, else 0 (zeroed per call)
     uint32_t* counter;    // [B] arrival counters (zeroed per call)
     Task* tasks;          // [maxt]
     ReqState* req;        // [B]
@@ -163,6 +172,7 @@ struct Workspace {
                           // of vocabulary [2] and top-k [3]
     uint32_t part_stride;
     uint32_t maxt;
+    uint32_t maxu;
     uint64_t extra_stride;
     int smax;             // partial slots per request
 };
@@ -193,7 +203,7 @@ struct Claimed {
 // slices each; a claimer that finds none pushed yet takes the next pushed
 // unit and waits (bounded) for its task, or for every request to finish.
 // `cold` caches whether initial units may be left.
-__device__ inline Claimed claim_unit(const Workspace& W, int B, int S0, int S1, bool& cold) {
+__device__ inline Claimed claim_unit(const Workspace& W, int B, int S0, bool& cold) {
     Claimed c;
     c.ok = 1;
     c.hint = 0;
@@ -209,13 +219,14 @@ __device__ inline Claimed claim_unit(const Workspace& W, int B, int S0, int S1, 
         cold = false;
     }
     const uint32_t u = atomicAdd(&W.ctrl->head1, 1u);
-    const uint32_t ti = u / static_cast<uint32_t>(S1);
-    c.slice = static_cast<int>(u % static_cast<uint32_t>(S1));
-    if (ti >= W.maxt) { c.ok = 0; return c; }
+    if (u >= W.maxu) { c.ok = 0; return c; }
     uint32_t ns = 32;
-    SPEC_TRACE_EV(10, -1, -1, -1, static_cast<int>(ti));
+    SPEC_TRACE_EV(10, -1, -1, -1, static_cast<int>(u));
     for (uint32_t it = 0;; ++it) {
-        if (ld_acquire(&W.ready[ti])) {
+        const uint32_t rec = ld_acquire(&W.urec[u]);
+        if (rec) {
+            const uint32_t ti = (rec >> 6) - 1u;
+            c.slice = static_cast<int>(rec & 63u);
             c.task.b = __ldcg(&W.tasks[ti].b);
             c.task.row = __ldcg(&W.tasks[ti].row);
             c.task.kind = __ldcg(&W.tasks[ti].kind);
@@ -234,31 +245,50 @@ __device__ inline Claimed claim_unit(const Workspace& W, int B, int S0, int S1, 
 // written by the consumers, ordered before the job hand-over).  Returns
 // true in every lane when the unit completed the task's last slice; this
 // CTA's combiner then owns the combine.
-__device__ __forceinline__ bool comb_arrive(const Workspace& W, int b, int S) {
+__device__ __forceinline__ bool comb_arrive(const Workspace& W, int b, int S, uint32_t* done_est = nullptr) {
     int last = 0;
+    uint32_t dn = 0;
     if ((threadIdx.x & 31) == 0) {
         fence_acq_rel_gpu();   // release the partial (cumulative over the hand-over)
         const uint32_t prev = atomicAdd(&W.counter[b], 1u);
+        dn = ld_relaxed(&W.ctrl->done);   // (for the next row's slicing; not ordered)
         last = (prev == static_cast<uint32_t>(S - 1));
         if (last) {
             fence_acq_rel_gpu();   // acquire the other slices' partials
             W.counter[b] = 0;      // ready for the request's next task
         }
     }
+    if (done_est) *done_est = __shfl_sync(0xffffffffu, dn, 0);
     return __shfl_sync(0xffffffffu, last, 0) != 0;
 }
 
-// Combiner lane 0: enqueue the request's next task.  The release store of
-// the ready flag orders every earlier write of this lane (the request state,
-// the task) before it.
-__device__ __forceinline__ void push_task(const Workspace& W, Task t) {
-    const uint32_t ti = atomicAdd(&W.ctrl->tail, 1u);
-    if (ti >= W.maxt) { atomicOr(&W.ctrl->error, kErrQueue); return; }
+// One lane: enqueue the request's next task, cut into S slices of SL
+// elements.  One 64-bit atomic reserves the task slot and its S unit
+// records; the records are written after a fence that orders the task and
+// every earlier write of this lane (the request state) before them.
+__device__ __forceinline__ void push_task(const Workspace& W, Task t, int S, int SL) {
+    t.kind = task_kind_pack(t.kind, S, SL);
+    const unsigned long long r = atomicAdd(&W.ctrl->tailc, (1ull << 32) | static_cast<unsigned long long>(S));
+    const uint32_t ti = static_cast<uint32_t>(r >> 32), u0 = static_cast<uint32_t>(r);
+    if (ti >= W.maxt || u0 + static_cast<uint32_t>(S) > W.maxu) { atomicOr(&W.ctrl->error, kErrQueue); return; }
     __stcg(&W.tasks[ti].b, t.b);
     __stcg(&W.tasks[ti].row, t.row);
     __stcg(&W.tasks[ti].kind, t.kind);
     __stcg(&W.tasks[ti].aux, t.aux);
-    st_release(&W.ready[ti], 1u);
+    fence_acq_rel_gpu();
+    for (int s = 0; s < S; ++s) st_relaxed(&W.urec[u0 + s], ((ti + 1u) << 6) | static_cast<uint32_t>(s));
+}
+
+// Slices of a pushed row: a first row's while most requests are active;
+// finer as requests finish, so that the remaining chains keep the grid busy
+// (at most smax).  done = finished requests (an estimate).
+__device__ __forceinline__ void pick_slices(int B, int V, int S0, int smax, uint32_t done, int& S, int& SL) {
+    const int active = B - static_cast<int>(done) > 1 ? B - static_cast<int>(done) : 1;
+    int s = (2 * static_cast<int>(gridDim.x) + active - 1) / active;
+    if (s < S0) s = S0;
+    if (s > smax) s = smax;
+    SL = (((V + s - 1) / s) + 63) & ~63;
+    S = (V + SL - 1) / SL;
 }
 
 // Combiner lane 0, after the request's outputs are written by the warp.
@@ -410,7 +440,7 @@ __device__ __forceinline__ void issue_chunk(const Pipe& P, const StreamPlan& p, 
 // `plan(c)` returns the unit's StreamPlan (tma: issue the chunks; otherwise
 // the consumers copy them themselves).
 template <class Fetch, class PlanF>
-__device__ void producer_loop(const Workspace& W, int B, int S0, int S1, const Pipe& P, bool tma, Fetch fetch,
+__device__ void producer_loop(const Workspace& W, int B, int S0, const Pipe& P, bool tma, Fetch fetch,
                               PlanF plan) {
     uint32_t seq = 0;          // chunks issued so far (ring sequence number)
     bool dead = false;
@@ -423,7 +453,7 @@ __device__ void producer_loop(const Workspace& W, int B, int S0, int S1, const P
             c.ok = 0; c.slice = 0; c.hint = 0; c.pad = 0;
             c.task.b = 0; c.task.row = 0; c.task.kind = 0; c.task.aux = 0;
         } else {
-            c = claim_unit(W, B, S0, S1, cold);
+            c = claim_unit(W, B, S0, cold);
             if (c.ok) fetch(c);
         }
         P.desc[j] = c;

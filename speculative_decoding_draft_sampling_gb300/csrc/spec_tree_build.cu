@@ -175,7 +175,7 @@ __device__ void build_finalize(const BuildArgs& A, unsigned long long* msk, cons
 // The combine of one depth row (combiner warp): merge the slice lists into
 // the depth's sorted top-M, then resume the best-first enumeration.
 __device__ void build_combine(const BuildArgs& A, BuildSmem& sh, unsigned char* scr, Ent* nodes, Ent* pend,
-                              const Job& job) {
+                              const Job& job, uint32_t done) {
     const int l = threadIdx.x & 31;
     const int N = A.N, M = A.M, L = A.L;
     const int b = job.task.b;
@@ -218,7 +218,7 @@ __device__ void build_combine(const BuildArgs& A, BuildSmem& sh, unsigned char* 
     }
     __syncwarp();
     if (!trivial) {
-        const int S = task_slices(A, initial);
+        const int S = task_S(A, job.task);
         load_hdrs_w(A.W, b, S, sh.hdrs);
         uint32_t flags = l < S ? sh.hdrs.flags[l] : 0u;
         uint64_t theta = l < S ? sh.hdrs.kth[l] : 0ull;
@@ -325,7 +325,9 @@ __device__ void build_combine(const BuildArgs& A, BuildSmem& sh, unsigned char* 
         if (l == 0) {
             Task nt;
             nt.b = b; nt.row = need - 1; nt.kind = 0; nt.aux = 0;
-            push_task(A.W, nt);
+            int S1, SL1;
+            pick_slices(A.B, A.V, A.S, A.S1, done, S1, SL1);
+            push_task(A.W, nt, S1, SL1);
         }
     }
     __syncwarp();
@@ -343,21 +345,22 @@ __global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs
     auto trivial_of = [&](const Task& t) { return t.kind < 0 && (N <= 1 || L <= 0); };
     auto plan = [&](const Task& t, int slice) {
         if (trivial_of(t)) return plan_none();
-        const int SL = task_slen(A, t.kind < 0);
+        const int SL = task_SL(A, t);
         const int x0 = slice * SL, x1 = min(A.V, x0 + SL);
         const float* qrow = A.q + static_cast<long long>(t.b) * A.q_bs + static_cast<long long>(t.row) * A.q_rs;
         return plan_single(qrow, 4, x0, x1);
     };
     if (threadIdx.x >= kCombiner0) {
         combiner_loop(P, [&](const Job& job) {
-            if (comb_arrive(A.W, job.task.b, task_slices(A, job.task.kind < 0))) build_combine(A, sh, scr, nodes, pend, job);
+            uint32_t done;
+            if (comb_arrive(A.W, job.task.b, task_S(A, job.task), &done)) build_combine(A, sh, scr, nodes, pend, job, done);
             __syncwarp();
         });
         return;
     }
     if (threadIdx.x >= kThreads) {
         if (threadIdx.x == kProducer)
-            producer_loop(A.W, A.B, A.S, A.S1, P, tma, [](Claimed&) {},
+            producer_loop(A.W, A.B, A.S, P, tma, [](Claimed&) {},
                           [&](const Claimed& c) { return plan(c.task, c.slice); });
         return;
     }
@@ -373,7 +376,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs
         PartHdr* ph = part_hdr(A.W, b, s, A.S);
         uint64_t* pk = part_keys(A.W, b, s, A.S);
         if (!trivial) {
-            const int x0 = s * task_slen(A, t.kind < 0);
+            const int x0 = s * task_SL(A, t);
             TopkHistFn<F32, false> fn;
             fn.init(&sh.tk, M, 0u);
             if (!consume_row<F32>(P, seq, plan(t, s), tma, x0, fn)) break;

@@ -80,7 +80,7 @@ __device__ __forceinline__ bool walk_invalid(const WalkArgs& A, const Task& t) {
 // The combine of one row (combiner warp): argmax over the slice partials,
 // then the greedy decision or the tree step.
 template <class E, bool kTree>
-__device__ void walk_combine(const WalkArgs& A, const Job& job) {
+__device__ void walk_combine(const WalkArgs& A, const Job& job, uint32_t done) {
     const int l = threadIdx.x & 31;
     const int b = job.task.b;
     const int row = job.task.row;
@@ -93,7 +93,7 @@ __device__ void walk_combine(const WalkArgs& A, const Job& job) {
     }
     uint32_t flags = 0;
     uint64_t best = 0;
-    const int S = task_slices(A, initial);
+    const int S = task_S(A, job.task);
     for (int j = l; j < S; j += 32) {
         const PartHdr* h = part_hdr(A.W, b, j, S);
         flags |= __ldcg(&h->flags);
@@ -115,7 +115,9 @@ __device__ void walk_combine(const WalkArgs& A, const Job& job) {
             __stcg(&A.W.req[b].status, st);
             Task nt;
             nt.b = b; nt.row = row + 1; nt.kind = 0; nt.aux = 0;
-            push_task(A.W, nt);
+            int S1, SL1;
+            pick_slices(A.B, A.V, A.S, A.S1, done, S1, SL1);
+            push_task(A.W, nt, S1, SL1);
         }
     } else {
         if (bad_row) { tree_finish(A, b, acc, -1, st | 1); return; }
@@ -136,7 +138,9 @@ __device__ void walk_combine(const WalkArgs& A, const Job& job) {
             __stcg(&A.W.req[b].status, st);
             Task nt;
             nt.b = b; nt.row = child; nt.kind = 0; nt.aux = acc + 1;
-            push_task(A.W, nt);
+            int S1, SL1;
+            pick_slices(A.B, A.V, A.S, A.S1, done, S1, SL1);
+            push_task(A.W, nt, S1, SL1);
         }
     }
 }
@@ -149,20 +153,21 @@ __global__ void __launch_bounds__(kBlockThreads, 2) walk_kernel(const WalkArgs A
     const bool tma = A.tma_l != 0;
     auto plan = [&](const Task& t, int slice) {
         if (walk_invalid<E, kTree>(A, t)) return plan_none();
-        const int SL = task_slen(A, t.kind < 0);
+        const int SL = task_SL(A, t);
         const int x0 = slice * SL, x1 = min(A.V, x0 + SL);
         return plan_single(walk_row<E>(A, t.b, t.row, kTree), E::kBytes, x0, x1);
     };
     if (threadIdx.x >= kCombiner0) {
         combiner_loop(P, [&](const Job& job) {
-            if (comb_arrive(A.W, job.task.b, task_slices(A, job.task.kind < 0))) walk_combine<E, kTree>(A, job);
+            uint32_t done;
+            if (comb_arrive(A.W, job.task.b, task_S(A, job.task), &done)) walk_combine<E, kTree>(A, job, done);
             __syncwarp();
         });
         return;
     }
     if (threadIdx.x >= kThreads) {
         if (threadIdx.x == kProducer)
-            producer_loop(A.W, A.B, A.S, A.S1, P, tma, [](Claimed&) {},
+            producer_loop(A.W, A.B, A.S, P, tma, [](Claimed&) {},
                           [&](const Claimed& c) { return plan(c.task, c.slice); });
         return;
     }
@@ -177,7 +182,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) walk_kernel(const WalkArgs A
         const bool invalid = walk_invalid<E, kTree>(A, t);
         PartHdr* ph = part_hdr(A.W, b, s, A.S);
         if (!invalid) {
-            const int x0 = s * task_slen(A, t.kind < 0);
+            const int x0 = s * task_SL(A, t);
             ArgmaxFn<E> fn;
             if (!consume_row<E>(P, seq, plan(t, s), tma, x0, fn)) break;
             // per warp, then thread 0 over the warps (one barrier)
