@@ -224,7 +224,7 @@ __device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, i
     const double ur = kind == kVerify ? static_cast<double>(chain_u(A, b, row)) : 0.0;
     const int y = kind == kVerify ? A.draft[static_cast<long long>(b) * A.K + row] : -1;
     SliceHdrs& H = cs.hdrs;
-    load_hdrs_w(A.W, b, S, H);
+    load_hdrs_w(A.W, b, S, H, cs.list, kCombKeys);   // headers and each slice's first 8 keys
     SPEC_TRACE_EVW(5, b, row, S, kind);
     uint32_t flags = 0;
     float vmax = -kInf;
@@ -244,7 +244,7 @@ __device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, i
     int n = 0, fb = (flags & kPfOverflow) ? 1 : 0;
     if (!fb) {
         bool oflow;
-        n = gather_all_w(A.W, b, S, H, cs.list, kCombKeys, oflow);
+        n = gather_all_w(A.W, b, S, H, cs.list, kCombKeys, oflow, 8);
         if (oflow) fb = 1;
     }
     SPEC_TRACE_EVW(6, b, row, n, kind);
@@ -318,6 +318,7 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
     const double Z = block_sum_d(zpart, sh.red);
     const double invZ = 1.0 / Z;
     const uint32_t hint = next_hint(tau, m);
+    SPEC_TRACE_EV(8, b, row, keep, kind);
     if (threadIdx.x == 0) {
         __stcg(&A.W.ctrl->hint0, hint);
         // for the next call's first rows: a wider margin (another call's rows
@@ -365,6 +366,7 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
                 chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
                 chain_advance(A, b, row, kb, st, hint, p.done);
             }
+            SPEC_TRACE_EV(9, b, row, 1, kind);
             return;
         }
         // residual [p - q]_+ lives on S (p = 0 outside it)
@@ -381,7 +383,9 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
             chain_diag(A, b, row, (float)py, (float)qy, (float)Z, (st & 4) ? 0.f : (float)R_mass);
         }
         csync();
+        SPEC_TRACE_EV(11, b, row, 0, kind);
         chain_finish_cta(A, b, row, sh.ish[0], st);
+        SPEC_TRACE_EV(9, b, row, 0, kind);
         return;
     }
     // bonus row: draw from p

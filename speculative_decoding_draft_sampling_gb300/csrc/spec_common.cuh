@@ -308,6 +308,100 @@ __device__ __forceinline__ double block_exscan_d(double v, double* red, double& 
     return base + inc - v;
 }
 
+// ---------------------------------------------------------------------------
+// float-float ("double-single") sums: fp64 arithmetic is slow on this part,
+// so sums that need more than fp32 keep a pair (hi, lo) with hi = fl(hi+lo),
+// combined with the error-free two-sum (Knuth) -- about 48 significand bits
+// with fp32 operations only.  Explicit _rn intrinsics keep the compiler from
+// fusing or reordering the steps.
+// ---------------------------------------------------------------------------
+struct dfloat {
+    float hi, lo;
+};
+__device__ __forceinline__ dfloat df_make(float x) { return {x, 0.f}; }
+__device__ __forceinline__ dfloat df_add(dfloat a, dfloat b) {
+    const float s = __fadd_rn(a.hi, b.hi);
+    const float bb = __fsub_rn(s, a.hi);
+    const float e = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
+    const float t = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+    const float hi = __fadd_rn(s, t);
+    return {hi, __fsub_rn(t, __fsub_rn(hi, s))};
+}
+__device__ __forceinline__ dfloat df_add(dfloat a, float b) { return df_add(a, df_make(b)); }
+// x * y for fp32 x and a float-float y (error-free product of the hi parts)
+__device__ __forceinline__ dfloat df_mul(float x, dfloat y) {
+    const float p = __fmul_rn(x, y.hi);
+    const float e = __fmaf_rn(x, y.hi, -p);
+    const float t = __fmaf_rn(x, y.lo, e);
+    const float hi = __fadd_rn(p, t);
+    return {hi, __fsub_rn(t, __fsub_rn(hi, p))};
+}
+__device__ __forceinline__ bool df_gt(dfloat a, dfloat b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+__device__ __forceinline__ double df_to_d(dfloat a) { return static_cast<double>(a.hi) + static_cast<double>(a.lo); }
+__device__ __forceinline__ dfloat df_from_d(double d) {
+    const float hi = static_cast<float>(d);
+    return {hi, static_cast<float>(d - static_cast<double>(hi))};
+}
+__device__ __forceinline__ dfloat warp_sum_df(dfloat v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        dfloat w;
+        w.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
+        w.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
+        v = df_add(v, w);
+    }
+    return v;
+}
+// exclusive prefix (in lane order) and total
+__device__ __forceinline__ dfloat warp_exscan_df(dfloat v, dfloat& total) {
+    const int l = threadIdx.x & 31;
+    dfloat inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        dfloat t;
+        t.hi = __shfl_up_sync(0xffffffffu, inc.hi, o);
+        t.lo = __shfl_up_sync(0xffffffffu, inc.lo, o);
+        if (l >= o) inc = df_add(inc, t);
+    }
+    total.hi = __shfl_sync(0xffffffffu, inc.hi, 31);
+    total.lo = __shfl_sync(0xffffffffu, inc.lo, 31);
+    dfloat ex;
+    ex.hi = __shfl_up_sync(0xffffffffu, inc.hi, 1);
+    ex.lo = __shfl_up_sync(0xffffffffu, inc.lo, 1);
+    if (l == 0) ex = df_make(0.f);
+    return ex;
+}
+// consumers: sum over every consumer thread (red: kWarps float2 of shared scratch)
+__device__ __forceinline__ dfloat block_sum_df(dfloat v, float2* red) {
+    v = warp_sum_df(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    csync();
+    if (l == 0) red[w] = make_float2(v.hi, v.lo);
+    csync();
+    dfloat r = df_make(0.f);
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) r = df_add(r, dfloat{red[i].x, red[i].y});
+    return r;
+}
+// consumers: exclusive prefix in thread order, and the total
+__device__ __forceinline__ dfloat block_exscan_df(dfloat v, float2* red, dfloat& total) {
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    dfloat wt;
+    const dfloat ex = warp_exscan_df(v, wt);
+    csync();
+    if (l == 0) red[w] = make_float2(wt.hi, wt.lo);
+    csync();
+    dfloat base = df_make(0.f), tot = df_make(0.f);
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) {
+        const dfloat x{red[i].x, red[i].y};
+        if (i < w) base = df_add(base, x);
+        tot = df_add(tot, x);
+    }
+    total = tot;
+    return df_add(base, ex);
+}
+
 // max with NaN propagation (PTX max.NaN.f32): a NaN anywhere survives
 __device__ __forceinline__ float max_nan(float a, float b) {
     float r;

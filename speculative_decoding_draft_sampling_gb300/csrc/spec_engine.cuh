@@ -841,10 +841,19 @@ struct SliceHdrs {
 };
 
 // Combiner warp: lane s loads slice s's header (one round trip), offsets by
-// a warp scan.
-__device__ inline void load_hdrs_w(const Workspace& W, int b, int S, SliceHdrs& H) {
+// a warp scan.  With `list`, the same round trip also fetches each slice's
+// first 8 keys into list[off_s ..] (speculatively: the slot always holds
+// room for them), so that gather_all_w only fetches what lies beyond.
+__device__ inline void load_hdrs_w(const Workspace& W, int b, int S, SliceHdrs& H, uint64_t* list = nullptr,
+                                   int cap = 0) {
     const int l = threadIdx.x & 31;
     int c = 0;
+    uint64_t k8[8];
+    if (list && l < S) {
+        const uint64_t* src = part_keys(W, b, l, S);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) k8[j] = __ldcg(src + j);
+    }
     if (l < S) {
         const PartHdr* h = part_hdr(W, b, l, S);
         c = __ldcg(&h->cnt);
@@ -861,6 +870,11 @@ __device__ inline void load_hdrs_w(const Workspace& W, int b, int S, SliceHdrs& 
     const int off = warp_exscan_i(c, tot);
     if (l < S) H.off[l] = off;
     if (l == 0) H.off[S] = tot;
+    if (list && l < S) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (j < c && off + j < cap) list[off + j] = k8[j];
+    }
     __syncwarp();
 }
 
@@ -908,14 +922,14 @@ __device__ inline int gather_keys_w(const Workspace& W, int b, int S, const Slic
 // copies slice s; its loads are independent, 8 in flight).  Returns the
 // count (at most cap; `oflow` when more).
 __device__ inline int gather_all_w(const Workspace& W, int b, int S, const SliceHdrs& H, uint64_t* list,
-                                   int cap, bool& oflow) {
+                                   int cap, bool& oflow, int first = 0) {
     const int l = threadIdx.x & 31;
     const int total = H.off[S];
     oflow = total > cap;
     if (l < S) {
         const int c = H.cnt[l], o = H.off[l];
         const uint64_t* src = part_keys(W, b, l, S);
-        for (int j0 = 0; j0 < c; j0 += 8) {
+        for (int j0 = first; j0 < c; j0 += 8) {
             uint64_t key[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) key[j] = (j0 + j < c) ? __ldcg(src + j0 + j) : 0ull;
