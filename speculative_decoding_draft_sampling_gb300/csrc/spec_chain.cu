@@ -43,11 +43,12 @@ struct CombPrep {
     float vmax;
     float pad;
     uint64_t theta;   // largest slice filter
-    double uk, ur;    // uniforms: sample, accept
+    float uk, ur;     // uniforms: sample, accept
     // an untruncated draw: rescan slice [x0, x1) for the CDF crossing t
     int x0, x1, wmode;  // wmode 0: p weights 2^((l-m)c); 1: [p - q]_+
     float m, invZf;
-    double t, Z, R;
+    dfloat t;
+    double Z, R;        // diagnostics
 };
 struct CombSmem {
     SliceHdrs hdrs;
@@ -55,7 +56,7 @@ struct CombSmem {
     alignas(16) uint64_t list[kCombKeys];
     int rank[kCombKeys];
     int tok[kCombSet];
-    double wgt[kCombSet];
+    float2 wgt[kCombSet];    // float-float weights (hi, lo)
 };
 
 template <bool kTopk> struct ChainTopkPart {};
@@ -67,14 +68,14 @@ struct __align__(16) ChainSmem : ChainTopkPart<kTopk> {
     CombSmem comb;
     uint64_t sh64[4];
     int ish[4];
-    double red[kWarps];
+    float2 red2[kWarps];
     int ired[kWarps + 4];
     int hist[64];
     uint32_t scratch[kWarps + 2];
     float fsh[8];
     float wm[kWarps];        // per-warp partials of the one-barrier finishes
-    double ws[kWarps];
-    double ws2[kWarps];
+    float2 ws[kWarps];       // float-float
+    float2 ws2[kWarps];
     uint32_t wb[kWarps];
 };
 
@@ -156,39 +157,38 @@ __device__ void chain_advance(const ChainArgs& A, int b, int row, int kb, int st
     push_task(A.W, t, S, SL);
 }
 
-// acceptance of drafted y given p(y) and q(y): u < p/q (fp64)
-__device__ __forceinline__ bool chain_accept(const ChainArgs& A, int y, double py, double qy, double u, int& st) {
-    double ratio;
+// Acceptance of drafted y: u < p(y)/q(y).  With weights scaled by the
+// normaliser, p(y) = e_y / Z, the test is e_y > u q Z (float-float; no
+// division on this path).  A ratio within rounding of u is a near tie.
+__device__ __forceinline__ bool chain_accept_z(const ChainArgs& A, int y, float ey, float qy, dfloat Z, float u,
+                                               int& st) {
     if (y < 0 || y >= A.V) {
         st |= 8;
-        ratio = 0.0;
-    } else if (qy == 0.0) {
-        st |= 2;
-        ratio = py > 0.0 ? __longlong_as_double(0x7ff0000000000000LL) : 0.0;
-    } else {
-        // u < p/q as u*q < p: the two differ only within rounding of p/q,
-        // inside the near-tie band
-        return u * qy < py;
+        return false;
     }
-    return u < ratio;
+    if (qy == 0.f) {
+        st |= 2;
+        return ey > 0.f;   // p/q = inf when p > 0, else 0
+    }
+    return df_gt(df_make(ey), df_mul(u, df_mul(qy, Z)));
 }
 
-// Inverse CDF over n (token, weight) pairs sorted by token; the smallest
-// token with prefix > t.  Result in every lane.
-__device__ int warp_icdf_pairs(const int* tok, const double* w, int n, double t) {
+// Inverse CDF over n (token, weight) pairs sorted by token, float-float
+// weights; the smallest token with prefix > t.  Result in every lane.
+__device__ int warp_icdf_pairs(const int* tok, const float2* w, int n, dfloat t) {
     const int lane = threadIdx.x & 31;
     const int per = (n + 31) / 32;
     const int i0 = lane * per, i1 = min(n, i0 + per);
-    double loc = 0.0;
-    for (int i = i0; i < i1; ++i) loc += w[i];
-    double tot;
-    double c = warp_exscan_d(loc, tot);
+    dfloat loc = df_make(0.f);
+    for (int i = i0; i < i1; ++i) loc = df_add(loc, dfloat{w[i].x, w[i].y});
+    dfloat tot;
+    dfloat c = warp_exscan_df(loc, tot);
     int found = 0x7fffffff, lastpos = -1;
     for (int i = i0; i < i1; ++i) {
-        if (w[i] > 0.0) {
+        if (w[i].x > 0.f) {
             lastpos = i;
-            c += w[i];
-            if (c > t && found == 0x7fffffff) found = i;
+            c = df_add(c, dfloat{w[i].x, w[i].y});
+            if (df_gt(c, t) && found == 0x7fffffff) found = i;
         }
     }
 #pragma unroll
@@ -220,8 +220,8 @@ __device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, i
                              uint32_t done) {
     const int l = threadIdx.x & 31;
     const int kb = chain_k(A, b);
-    const double uk = static_cast<double>(chain_u(A, b, kb));
-    const double ur = kind == kVerify ? static_cast<double>(chain_u(A, b, row)) : 0.0;
+    const float uk = chain_u(A, b, kb);
+    const float ur = kind == kVerify ? chain_u(A, b, row) : 0.f;
     const int y = kind == kVerify ? A.draft[static_cast<long long>(b) * A.K + row] : -1;
     SliceHdrs& H = cs.hdrs;
     load_hdrs_w(A.W, b, S, H, cs.list, kCombKeys);   // headers and each slice's first 8 keys
@@ -311,12 +311,14 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
     // S = cand[0 .. keep): values >= tau, sorted by value descending
     const uint32_t tau_key = hkey(cand[keep - 1]);
     const float tau = ckey_val(cand[keep - 1]);
+    // weights e_x = 2^((l_x - m) c) and Z = sum over S in float-float; p(x) =
+    // e_x / Z is never formed on this path (tests compare Z-scaled masses)
     const float m = p.vmax, c2 = A.c2;
-    double zpart = 0.0;
-    for (int i = threadIdx.x; i < keep; i += kThreads)
-        zpart += static_cast<double>(ex2((ckey_val(cand[i]) - m) * c2));
-    const double Z = block_sum_d(zpart, sh.red);
-    const double invZ = 1.0 / Z;
+    dfloat zpart = df_make(0.f);
+    for (int i = threadIdx.x; i < keep; i += kThreads) zpart = df_add(zpart, ex2((ckey_val(cand[i]) - m) * c2));
+    const dfloat Z = block_sum_df(zpart, sh.red2);
+    const float Zf = Z.hi;
+    auto prob = [&](float e) { return static_cast<float>(static_cast<double>(e) / df_to_d(Z)); };   // diagnostics
     const uint32_t hint = next_hint(tau, m);
     SPEC_TRACE_EV(8, b, row, keep, kind);
     if (threadIdx.x == 0) {
@@ -330,57 +332,58 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
         __stcg(&A.W.persist[0], kPersistTag);
     }
 
-    // weights of S sorted by token id (ascending)
-    auto sort_by_token = [&](bool residual, const float* qrow, double& total) {
-        double part = 0.0;
+    // Z-scaled weights of S sorted by token id (ascending): e_x, or for the
+    // residual Z [p - q]_+ = [e_x - q_x Z]_+
+    auto sort_by_token = [&](bool residual, const float* qrow, dfloat& total) {
+        dfloat part = df_make(0.f);
         for (int i = threadIdx.x; i < keep; i += kThreads) {
             const int x = ckey_idx(cand[i]);
             int r = 0;
             for (int j = 0; j < keep; ++j) r += ckey_idx(cand[j]) < x;
-            const double pw = static_cast<double>(ex2((ckey_val(cand[i]) - m) * c2)) * invZ;
-            double w = pw;
+            dfloat w = df_make(ex2((ckey_val(cand[i]) - m) * c2));
             if (residual) {
                 const float qx = (x >= 0 && x < A.V) ? qrow[x] : 0.f;   // keys always hold in-range ids
-                const double d = pw - static_cast<double>(qx);
-                w = d > 0.0 ? d : 0.0;
+                const dfloat d = df_add(w, df_neg(df_mul(qx, Z)));
+                w = d.hi > 0.f ? d : df_make(0.f);
             }
             cs.tok[r] = x;
-            cs.wgt[r] = w;
-            part += w;
+            cs.wgt[r] = make_float2(w.hi, w.lo);
+            part = df_add(part, w);
         }
-        total = block_sum_d(part, sh.red);
+        total = block_sum_df(part, sh.red2);
     };
 
     if (kind == kVerify) {
         const int y = p.y;
-        double py = 0.0, qy = 0.0;
+        float ey = 0.f, qy = 0.f;
         if (y >= 0 && y < A.V) {
             const int sy = y / p.sl;
             const float ly = cs.hdrs.ly[sy];
-            qy = static_cast<double>(cs.hdrs.qy[sy]);
-            if (fkey(ly) >= tau_key) py = static_cast<double>(ex2((ly - m) * c2)) * invZ;
+            qy = cs.hdrs.qy[sy];
+            if (fkey(ly) >= tau_key) ey = ex2((ly - m) * c2);
         }
-        const bool acc = chain_accept(A, y, py, qy, p.ur, st);
+        const bool acc = chain_accept_z(A, y, ey, qy, Z, p.ur, st);
         if (acc) {
             if (threadIdx.x == 0) {
-                chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
+                if (A.diag) chain_diag(A, b, row, prob(ey), qy, Zf, 0.f);
                 chain_advance(A, b, row, kb, st, hint, p.done);
             }
             SPEC_TRACE_EV(9, b, row, 1, kind);
             return;
         }
         // residual [p - q]_+ lives on S (p = 0 outside it)
-        double R_mass;
+        dfloat R_mass;
         sort_by_token(true, chain_qrow(A, b, row), R_mass);
-        if (!(R_mass > 0.0)) {
+        if (!(R_mass.hi > 0.f)) {
             st |= 4;
             sort_by_token(false, nullptr, R_mass);
         }
         int x = -1;
-        if (threadIdx.x < 32) x = warp_icdf_pairs(cs.tok, cs.wgt, keep, p.uk * R_mass);
+        if (threadIdx.x < 32)
+            x = warp_icdf_pairs(cs.tok, cs.wgt, keep, df_mul(p.uk, R_mass));
         if (threadIdx.x == 0) {
             sh.ish[0] = x;
-            chain_diag(A, b, row, (float)py, (float)qy, (float)Z, (st & 4) ? 0.f : (float)R_mass);
+            if (A.diag) chain_diag(A, b, row, prob(ey), qy, Zf, (st & 4) ? 0.f : static_cast<float>(df_to_d(R_mass) / df_to_d(Z)));
         }
         csync();
         SPEC_TRACE_EV(11, b, row, 0, kind);
@@ -389,16 +392,15 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
         return;
     }
     // bonus row: draw from p
-    double tot;
+    dfloat tot;
     sort_by_token(false, nullptr, tot);
     int x = -1;
-    if (threadIdx.x < 32) x = warp_icdf_pairs(cs.tok, cs.wgt, keep, p.uk * tot);
+    if (threadIdx.x < 32) x = warp_icdf_pairs(cs.tok, cs.wgt, keep, df_mul(p.uk, tot));
     if (threadIdx.x == 0) sh.ish[0] = x;
     csync();
     x = sh.ish[0];
-    if (threadIdx.x == 0 && x >= 0 && x < A.V)
-        chain_diag(A, b, row, (float)(static_cast<double>(ex2((E::load(chain_lrow<E>(A, b, row), x) - m) * c2)) * invZ),
-                   0.f, (float)Z, 0.f);
+    if (threadIdx.x == 0 && A.diag && x >= 0 && x < A.V)
+        chain_diag(A, b, row, prob(ex2((E::load(chain_lrow<E>(A, b, row), x) - m) * c2)), 0.f, Zf, 0.f);
     chain_finish_cta(A, b, row, x, st);
 }
 
@@ -427,44 +429,47 @@ __device__ void chain_fallback_cta(const ChainArgs& A, ChainSmem<true>& sh, int 
         const float v = E::load(lrow, x);
         return fkey(v) >= tau ? ex2((v - m) * c2) : 0.f;
     };
-    const double Z = cta_sum(0, V, wp, sh.red);
+    // Z-scaled weights, as in the candidate-set combine
+    const dfloat Z = cta_sum(0, V, wp, sh.red2);
+    const double Zd = df_to_d(Z);
     const int kb = chain_k(A, b);
-    const double uk = static_cast<double>(chain_u(A, b, kb));
+    const float uk = chain_u(A, b, kb);
     if (kind == kVerify) {
         const int y = A.draft[static_cast<long long>(b) * A.K + row];
-        double py = 0.0, qy = 0.0;
+        float ey = 0.f, qy = 0.f;
         if (y >= 0 && y < V) {
-            py = static_cast<double>(wp(y)) / Z;
-            qy = static_cast<double>(chain_qrow(A, b, row)[y]);
+            ey = wp(y);
+            qy = chain_qrow(A, b, row)[y];
         }
-        if (chain_accept(A, y, py, qy, static_cast<double>(chain_u(A, b, row)), st)) {
+        auto py = [&]() { return static_cast<float>(static_cast<double>(ey) / Zd); };   // diagnostics
+        if (chain_accept_z(A, y, ey, qy, Z, chain_u(A, b, row), st)) {
             if (threadIdx.x == 0) {
-                chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
+                if (A.diag) chain_diag(A, b, row, py(), qy, Z.hi, 0.f);
                 chain_advance(A, b, row, kb, st, 0u, sh.comb.prep.done);
             }
             return;
         }
         const float* qrow = chain_qrow(A, b, row);
-        const float invZ = static_cast<float>(1.0 / Z);
-        auto wr = [&](int x) -> float {
-            const float d = wp(x) * invZ - qrow[x];
-            return d > 0.f ? d : 0.f;
+        auto wr = [&](int x) -> float {   // Z [p - q]_+
+            const dfloat d = df_add(df_make(wp(x)), df_neg(df_mul(qrow[x], Z)));
+            return d.hi > 0.f ? d.hi : 0.f;
         };
-        const double R_mass = cta_sum(0, V, wr, sh.red);
+        const dfloat R_mass = cta_sum(0, V, wr, sh.red2);
         int x;
-        if (R_mass > 0.0) {
-            x = cta_icdf(0, V, uk * R_mass, wr, sh.red, sh.ired);
+        if (R_mass.hi > 0.f) {
+            x = cta_icdf(0, V, df_mul(uk, R_mass), wr, sh.red2, sh.ired);
         } else {
             st |= 4;
-            x = cta_icdf(0, V, uk * Z, wp, sh.red, sh.ired);
+            x = cta_icdf(0, V, df_mul(uk, Z), wp, sh.red2, sh.ired);
         }
-        if (threadIdx.x == 0) chain_diag(A, b, row, (float)py, (float)qy, (float)Z, (float)R_mass);
+        if (threadIdx.x == 0 && A.diag)
+            chain_diag(A, b, row, py(), qy, Z.hi, (st & 4) ? 0.f : static_cast<float>(df_to_d(R_mass) / Zd));
         chain_finish_cta(A, b, row, x, st);
         return;
     }
-    const int x = cta_icdf(0, V, uk * Z, wp, sh.red, sh.ired);
-    if (threadIdx.x == 0)
-        chain_diag(A, b, row, (float)(static_cast<double>(wp(x)) / Z), 0.f, (float)Z, 0.f);
+    const int x = cta_icdf(0, V, df_mul(uk, Z), wp, sh.red2, sh.ired);
+    if (threadIdx.x == 0 && A.diag && x >= 0 && x < V)
+        chain_diag(A, b, row, static_cast<float>(static_cast<double>(wp(x)) / Zd), 0.f, Z.hi, 0.f);
     chain_finish_cta(A, b, row, x, st);
 }
 
@@ -472,55 +477,57 @@ __device__ void chain_fallback_cta(const ChainArgs& A, ChainSmem<true>& sh, int 
 // combine without truncation: per-slice (max, sum of 2^((l-m_s)c))
 // ---------------------------------------------------------------------------
 // the slice whose running prefix of v (lane s holds slice s's value) crosses
-// t, and the prefix before it
-__device__ __forceinline__ int find_slice_w(int S, double v, double t, double& before) {
+// t, and the prefix before it (float-float)
+__device__ __forceinline__ int find_slice_w(int S, dfloat v, dfloat t, dfloat& before) {
     const int l = threadIdx.x & 31;
-    if (l >= S) v = 0.0;
-    double tot;
-    const double ex = warp_exscan_d(v, tot);
-    const uint32_t bal = __ballot_sync(0xffffffffu, v > 0.0 && ex + v > t);
+    if (l >= S) v = df_make(0.f);
+    dfloat tot;
+    const dfloat ex = warp_exscan_df(v, tot);
+    const uint32_t bal = __ballot_sync(0xffffffffu, v.hi > 0.f && df_gt(df_add(ex, v), t));
     int pick;
     if (bal) {
         pick = __ffs(bal) - 1;
     } else {
-        const uint32_t pos = __ballot_sync(0xffffffffu, v > 0.0);
+        const uint32_t pos = __ballot_sync(0xffffffffu, v.hi > 0.f);
         pick = pos ? 31 - __clz(pos) : 0;
     }
-    before = __shfl_sync(0xffffffffu, ex, pick);
+    before.hi = __shfl_sync(0xffffffffu, ex.hi, pick);
+    before.lo = __shfl_sync(0xffffffffu, ex.lo, pick);
     return pick;
 }
 
+__device__ __forceinline__ dfloat df_of(float2 v) { return dfloat{v.x, v.y}; }
+
 // Combiner warp: the combine of an untruncated row.  Returns true when a draw
-// needs a slice rescan, prepared in cs.prep for the consumers.
+// needs a slice rescan, prepared in cs.prep for the consumers.  Slice sums
+// are Z-scaled (weights e_x = 2^((l_x - m) c)), float-float across slices.
 template <class E>
 __device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st, int S, int SL,
                              uint32_t done) {
     const int l = threadIdx.x & 31;
     const int kb = chain_k(A, b);
-    const double cd = static_cast<double>(A.c2);
-    const double uk = static_cast<double>(chain_u(A, b, kb));
-    const double ur = kind == kVerify ? static_cast<double>(chain_u(A, b, row)) : 0.0;
+    const float c2 = A.c2;
+    const float uk = chain_u(A, b, kb);
+    const float ur = kind == kVerify ? chain_u(A, b, row) : 0.f;
     const int y = kind == kVerify ? A.draft[static_cast<long long>(b) * A.K + row] : -1;
-    const void* lrow = chain_lrow<E>(A, b, row);
     SliceHdrs& H = cs.hdrs;
     load_hdrs_w(A.W, b, S, H);
     SPEC_TRACE_EVW(5, b, row, S, kind);
     if (kind == kResid) {
         const ReqState* rs = &A.W.req[b];
-        const float m = static_cast<float>(__ldcg(&rs->m));
-        const double Z = __ldcg(&rs->Z);
-        const double rv = l < S ? H.sum[l] : 0.0, pv = l < S ? H.sum2[l] : 0.0;
-        const double R_mass = warp_sum_d(rv);
-        const double P_mass = warp_sum_d(pv);
-        double before, t;
+        const dfloat rv = l < S ? df_of(H.sum[l]) : df_make(0.f);
+        const dfloat pv = l < S ? df_of(H.sum2[l]) : df_make(0.f);
+        const dfloat R_mass = warp_sum_df(rv);
+        const dfloat P_mass = warp_sum_df(pv);
+        dfloat before, t;
         int s, wmode;
-        if (R_mass > 0.0) {
-            t = uk * R_mass;
+        if (R_mass.hi > 0.f) {
+            t = df_mul(uk, R_mass);
             s = find_slice_w(S, rv, t, before);
             wmode = 1;
         } else {
             st |= 4;
-            t = uk * P_mass;
+            t = df_mul(uk, P_mass);
             s = find_slice_w(S, pv, t, before);
             wmode = 0;
         }
@@ -528,8 +535,10 @@ __device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, i
             CombPrep& p = cs.prep;
             p.b = b; p.row = row; p.kind = kind; p.st = st;
             p.x0 = s * SL; p.x1 = min(A.V, p.x0 + SL); p.wmode = wmode;
-            p.m = m; p.invZf = static_cast<float>(1.0 / Z);
-            p.t = t - before; p.Z = Z; p.R = R_mass;
+            p.m = __ldcg(&rs->m); p.invZf = __ldcg(&rs->invZ);
+            p.t = df_add(t, df_neg(before));
+            p.Z = 0.0;
+            p.R = df_to_d(R_mass);
         }
         return true;   // the consumers rescan the slice
     }
@@ -543,19 +552,19 @@ __device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, i
         chain_finish(A, b, row, -1, st | 1);
         return false;
     }
-    const double m = static_cast<double>(vmax);
-    double zv = 0.0;
-    if (l < S && H.sum[l] > 0.0) zv = H.sum[l] * exp2((static_cast<double>(H.vmax[l]) - m) * cd);
-    const double Z = warp_sum_d(zv);
+    const float m = vmax;
+    dfloat zv = df_make(0.f);
+    if (l < S && H.sum[l].x > 0.f) zv = df_mul(ex2((H.vmax[l] - m) * c2), df_of(H.sum[l]));
+    const dfloat Z = warp_sum_df(zv);
     if (kind == kVerify) {
-        double py = 0.0, qy = 0.0;
+        float ey = 0.f, qy = 0.f;
         if (y >= 0 && y < A.V) {
             const int sy = y / SL;
-            py = exp((static_cast<double>(H.ly[sy]) - m) / A.Td) / Z;
-            qy = static_cast<double>(H.qy[sy]);
+            ey = ex2((H.ly[sy] - m) * c2);
+            qy = H.qy[sy];
         }
-        const bool acc = chain_accept(A, y, py, qy, ur, st);
-        if (l == 0) chain_diag(A, b, row, (float)py, (float)qy, (float)Z, 0.f);
+        const bool acc = chain_accept_z(A, y, ey, qy, Z, ur, st);
+        if (l == 0 && A.diag) chain_diag(A, b, row, static_cast<float>(static_cast<double>(ey) / df_to_d(Z)), qy, Z.hi, 0.f);
         if (acc) {
             if (l == 0) chain_advance(A, b, row, kb, st, 0u, done);
             return false;
@@ -563,7 +572,7 @@ __device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, i
         if (l == 0) {
             ReqState* rs = &A.W.req[b];
             __stcg(&rs->m, m);
-            __stcg(&rs->Z, Z);
+            __stcg(&rs->invZ, __frcp_rn(Z.hi));
             __stcg(&rs->status, st);
             Task t;
             t.b = b; t.row = row; t.kind = kResid; t.aux = 0;
@@ -574,15 +583,16 @@ __device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, i
         return false;
     }
     // BONUS: inverse CDF of p; find the slice, the consumers rescan it
-    const double t = uk * Z;
-    double before;
+    const dfloat t = df_mul(uk, Z);
+    dfloat before;
     const int s = find_slice_w(S, zv, t, before);
     if (l == 0) {
         CombPrep& p = cs.prep;
         p.b = b; p.row = row; p.kind = kind; p.st = st;
         p.x0 = s * SL; p.x1 = min(A.V, p.x0 + SL); p.wmode = 0;
-        p.m = vmax; p.invZf = static_cast<float>(1.0 / Z);
-        p.t = t - before; p.Z = Z; p.R = 0.0;
+        p.m = vmax; p.invZf = 0.f;
+        p.t = df_add(t, df_neg(before));
+        p.Z = df_to_d(Z); p.R = 0.0;
     }
     return true;
 }
@@ -602,18 +612,17 @@ __device__ void rescan_cta(const ChainArgs& A, ChainSmem<false>& sh) {
             const float d = ex2((E::load(lrow, xx) - m) * c2) * invZ - qrow[xx];
             return d > 0.f ? d : 0.f;
         };
-        x = cta_icdf(p.x0, p.x1, p.t, wr, sh.red, sh.ired);
+        x = cta_icdf(p.x0, p.x1, p.t, wr, sh.red2, sh.ired);
     } else {
         auto wp = [&](int xx) -> float { return ex2((E::load(lrow, xx) - m) * c2); };
-        x = cta_icdf(p.x0, p.x1, p.t, wp, sh.red, sh.ired);
+        x = cta_icdf(p.x0, p.x1, p.t, wp, sh.red2, sh.ired);
     }
     if (threadIdx.x == 0) {
         if (p.kind == kResid) {
             if (A.diag) A.diag[(static_cast<long long>(b) * (A.K + 1) + row) * 4 + 3] = (p.st & 4) ? 0.f : (float)p.R;
-        } else if (x >= 0 && x < A.V) {
-            chain_diag(A, b, row,
-                       (float)(exp((static_cast<double>(E::load(lrow, x)) - static_cast<double>(m)) / A.Td) / p.Z), 0.f,
-                       (float)p.Z, 0.f);
+        } else if (A.diag && x >= 0 && x < A.V) {
+            chain_diag(A, b, row, static_cast<float>(static_cast<double>(ex2((E::load(lrow, x) - m) * c2)) / p.Z), 0.f,
+                       static_cast<float>(p.Z), 0.f);
         }
     }
     chain_finish_cta(A, b, row, x, p.st);
@@ -785,22 +794,22 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
                     const float sc = (fn.s > 0.f) ? fn.s * ex2((fn.m - wm) * A.c2) : 0.f;
-                    const double ws = warp_sum_d(static_cast<double>(sc));
+                    const dfloat ws = warp_sum_df(df_make(sc));
                     const uint32_t wb = __reduce_or_sync(0xffffffffu, fn.bad_flag());
-                    if (lane == 0) { sh.wm[w] = wm; sh.ws[w] = ws; sh.wb[w] = wb; }
+                    if (lane == 0) { sh.wm[w] = wm; sh.ws[w] = make_float2(ws.hi, ws.lo); sh.wb[w] = wb; }
                     if (fn.dw.seen) wsl[0] = fn.dw.ly;
                     csync();
                     if (threadIdx.x == 0) {
                         float ms = -kInf;
                         uint32_t bad = 0;
                         for (int j = 0; j < kWarps; ++j) { ms = fmaxf(ms, sh.wm[j]); bad |= sh.wb[j]; }
-                        double tot = 0.0;
+                        dfloat tot = df_make(0.f);
                         for (int j = 0; j < kWarps; ++j)
-                            if (sh.ws[j] > 0.0) tot += sh.ws[j] * static_cast<double>(ex2((sh.wm[j] - ms) * A.c2));
+                            if (sh.ws[j].x > 0.f) tot = df_add(tot, df_mul(ex2((sh.wm[j] - ms) * A.c2), df_of(sh.ws[j])));
                         ph->flags = bad ? kPfBad : 0u;
                         ph->cnt = 0;
                         ph->vmax = ms;
-                        ph->sum = tot;
+                        ph->sum = make_float2(tot.hi, tot.lo);
                         if (fn.dw.owns()) { ph->ly = wsl[0]; ph->qy = fn.dw.qy; }
                     }
                 }
@@ -808,22 +817,22 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
         } else if (kind == kResid) {
             const ReqState* rs = &A.W.req[b];
             ResidFn<E> fn;
-            fn.m = static_cast<float>(__ldcg(&rs->m));
+            fn.m = __ldcg(&rs->m);
             fn.c = A.c2;
-            fn.invZ = static_cast<float>(1.0 / __ldcg(&rs->Z));
+            fn.invZ = __ldcg(&rs->invZ);
             ok = consume_row2<E>(P, seq, plan, tma, x0, fn);
             if (ok) {
                 const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-                const double wr = warp_sum_d(static_cast<double>(fn.r));
-                const double wp = warp_sum_d(static_cast<double>(fn.pw));
-                if (lane == 0) { sh.ws[w] = wr; sh.ws2[w] = wp; }
+                const dfloat wr = warp_sum_df(df_make(fn.r));
+                const dfloat wp = warp_sum_df(df_make(fn.pw));
+                if (lane == 0) { sh.ws[w] = make_float2(wr.hi, wr.lo); sh.ws2[w] = make_float2(wp.hi, wp.lo); }
                 csync();
                 if (threadIdx.x == 0) {
-                    double rsum = 0.0, psum = 0.0;
-                    for (int j = 0; j < kWarps; ++j) { rsum += sh.ws[j]; psum += sh.ws2[j]; }
+                    dfloat rsum = df_make(0.f), psum = df_make(0.f);
+                    for (int j = 0; j < kWarps; ++j) { rsum = df_add(rsum, df_of(sh.ws[j])); psum = df_add(psum, df_of(sh.ws2[j])); }
                     ph->flags = 0;
-                    ph->sum = rsum;
-                    ph->sum2 = psum;
+                    ph->sum = make_float2(rsum.hi, rsum.lo);
+                    ph->sum2 = make_float2(psum.hi, psum.lo);
                 }
             }
         }

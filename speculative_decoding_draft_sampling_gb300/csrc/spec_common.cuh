@@ -328,6 +328,7 @@ __device__ __forceinline__ dfloat df_add(dfloat a, dfloat b) {
     return {hi, __fsub_rn(t, __fsub_rn(hi, s))};
 }
 __device__ __forceinline__ dfloat df_add(dfloat a, float b) { return df_add(a, df_make(b)); }
+__device__ __forceinline__ dfloat df_neg(dfloat a) { return {-a.hi, -a.lo}; }
 // x * y for fp32 x and a float-float y (error-free product of the hi parts)
 __device__ __forceinline__ dfloat df_mul(float x, dfloat y) {
     const float p = __fmul_rn(x, y.hi);

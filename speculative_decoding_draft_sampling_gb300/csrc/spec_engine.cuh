@@ -134,11 +134,11 @@ __host__ __device__ __forceinline__ int task_kind_S(int kind) { return (kind >> 
 __host__ __device__ __forceinline__ int task_kind_SL(int kind) { return ((kind >> 14) & 0x3ffff) << 6; }
 
 struct ReqState {
-    double m;          // row maximum (logit), carried to a residual pass
-    double Z;          // normaliser, carried to a residual pass
+    float m;           // row maximum (logit), carried to a residual pass
+    float invZ;        // 1 / Z rounded to fp32: the residual pass and its rescan share it
     int32_t status;    // accumulated SPEC_ST_* bits
     int32_t pad0;
-    double pad[5];
+    double pad[6];
 };
 static_assert(sizeof(ReqState) == 64, "ReqState is 64 bytes");
 
@@ -149,8 +149,8 @@ struct PartHdr {
     uint32_t flags;    // kPf* bits
     int32_t pad0;
     uint64_t kth;      // top-k: the slice's filter as a composite key / argmax: best key
-    double sum;        // slice sum (meaning depends on the op)
-    double sum2;
+    float2 sum;        // slice sum, float-float (meaning depends on the op)
+    float2 sum2;
     float ly;          // chain: logit of the drafted token (slice holding it)
     float qy;          // chain: q of the drafted token (slice holding it)
     uint64_t pad1[2];
@@ -768,48 +768,48 @@ __device__ bool consume_row2(const Pipe& P, uint32_t& seq, const StreamPlan& p, 
 // single-CTA passes over a global range (rescans and rare exact paths)
 // ---------------------------------------------------------------------------
 
-// Sum of w(x) over [x0, x1): fp32 per thread, fp64 across threads.
+// Sum of w(x) over [x0, x1), float-float.
 template <class W>
-__device__ double cta_sum(int x0, int x1, W& w, double* red) {
-    float acc = 0.f;
-    for (int x = x0 + threadIdx.x; x < x1; x += kThreads) acc += w(x);
-    return block_sum_d(static_cast<double>(acc), red);
+__device__ dfloat cta_sum(int x0, int x1, W& w, float2* red) {
+    dfloat acc = df_make(0.f);
+    for (int x = x0 + threadIdx.x; x < x1; x += kThreads) acc = df_add(acc, w(x));
+    return block_sum_df(acc, red);
 }
 
 // Inverse CDF over non-negative weights w(x), x ascending in [x0, x1): the
 // smallest x with C(x) > t.  Blocks of kThreads*16 consecutive elements; each
-// thread owns 16 consecutive elements (fp32 prefix inside, fp64 across), so
-// every thread has 16 independent loads in flight per block.  If rounding
-// leaves no crossing, returns the last x with w(x) > 0 (or x0).
+// thread owns 16 consecutive elements, so every thread has 16 independent
+// loads in flight per block; prefixes in float-float.  If rounding leaves no
+// crossing, returns the last x with w(x) > 0 (or x0).
 template <class W>
-__device__ int cta_icdf(int x0, int x1, double t, W& w, double* red, int* ired) {
+__device__ int cta_icdf(int x0, int x1, dfloat t, W& w, float2* red, int* ired) {
     constexpr int PER = 16;
-    double base = 0.0;
+    dfloat base = df_make(0.f);
     int last_pos = -1;
     for (int b0 = x0; b0 < x1; b0 += kThreads * PER) {
         const int xs = b0 + threadIdx.x * PER;
         float wv[PER];
-        float loc = 0.f;
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
             const int x = xs + j;
             wv[j] = (x < x1) ? w(x) : 0.f;
         }
+        dfloat loc = df_make(0.f);
         int lp = -1;
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
-            loc += wv[j];
+            loc = df_add(loc, wv[j]);
             if (wv[j] > 0.f) lp = xs + j;
         }
-        double tot;
-        const double ex = block_exscan_d(static_cast<double>(loc), red, tot);
+        dfloat tot;
+        const dfloat c0 = df_add(base, block_exscan_df(loc, red, tot));
         int found = 0x7fffffff;
-        if (loc > 0.f && base + ex + static_cast<double>(loc) > t) {
-            double c = base + ex;
+        if (loc.hi > 0.f && df_gt(df_add(c0, loc), t)) {
+            dfloat c = c0;
 #pragma unroll
             for (int j = 0; j < PER; ++j) {
-                c += static_cast<double>(wv[j]);
-                if (found == 0x7fffffff && wv[j] > 0.f && c > t) found = xs + j;
+                c = df_add(c, wv[j]);
+                if (found == 0x7fffffff && wv[j] > 0.f && df_gt(c, t)) found = xs + j;
             }
         }
         csync();
@@ -822,7 +822,7 @@ __device__ int cta_icdf(int x0, int x1, double t, W& w, double* red, int* ired) 
         if (ired[1] > last_pos) last_pos = ired[1];
         csync();
         if (fb != 0x7fffffff) return fb;
-        base += tot;
+        base = df_add(base, tot);
     }
     return last_pos >= 0 ? last_pos : x0;
 }
@@ -834,8 +834,8 @@ struct SliceHdrs {
     uint32_t flags[kMaxSlices];
     float vmax[kMaxSlices];
     uint64_t kth[kMaxSlices];
-    double sum[kMaxSlices];
-    double sum2[kMaxSlices];
+    float2 sum[kMaxSlices];
+    float2 sum2[kMaxSlices];
     float ly[kMaxSlices];
     float qy[kMaxSlices];
 };
@@ -992,88 +992,6 @@ __device__ inline uint64_t kth_key_w(const uint64_t* list, int n, int k) {
         if (c >= k) lo = mid; else hi = mid - 1;
     }
     return lo;
-}
-
-// Combiner warp: sum of w(x) over [x0, x1) (fp32 in blocks of 8, fp64 across).
-template <class Wt>
-__device__ double warp_range_sum(int x0, int x1, Wt& w) {
-    const int l = threadIdx.x & 31;
-    double acc = 0.0;
-    for (int b0 = x0 + l * 8; b0 < x1; b0 += 32 * 8) {
-        float part = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (b0 + j < x1) part += w(b0 + j);
-        acc += static_cast<double>(part);
-    }
-    return warp_sum_d(acc);
-}
-
-// Combiner warp: inverse CDF over non-negative weights w(x), x ascending in
-// [x0, x1): the smallest x with C(x) > t.  Two levels: every lane sums one
-// contiguous span, a warp scan finds the span where C crosses t, and the
-// warp splits that span again.  If rounding leaves no crossing, returns the
-// last x with w(x) > 0 (or x0).
-template <class Wt>
-__device__ int warp_icdf(int x0, int x1, double t, Wt& w) {
-    const int l = threadIdx.x & 31;
-    const int n = x1 - x0;
-    if (n <= 0) return x0;
-    int lo = x0, len = n;
-    double base = 0.0;
-    int last_pos = -1;
-    for (int level = 0; level < 2; ++level) {
-        const int span = (len + 31) / 32;
-        const int a = lo + l * span, e = min(lo + len, a + span);
-        double part = 0.0;
-        float blk = 0.f;
-        int lp = -1;
-        for (int x = a; x < e; ++x) {
-            const float wx = w(x);
-            if (wx > 0.f) lp = x;
-            blk += wx;
-            if (((x - a) & 7) == 7) { part += static_cast<double>(blk); blk = 0.f; }
-        }
-        part += static_cast<double>(blk);
-        double tot;
-        const double ex = warp_exscan_d(part, tot);
-        last_pos = max(last_pos, static_cast<int>(warp_max_u32(static_cast<uint32_t>(lp + 1))) - 1);
-        const bool cross = part > 0.0 && base + ex + part > t;
-        const uint32_t bal = __ballot_sync(0xffffffffu, cross);
-        if (!bal) return last_pos >= 0 ? last_pos : x0;
-        const int src = __ffs(bal) - 1;
-        base += __shfl_sync(0xffffffffu, ex, src);
-        lo = lo + src * span;
-        len = min(span, x0 + n - lo);
-        if (level == 1 || len <= 32) {
-            // one element per lane (len <= span <= 32 after the split)
-            if (len > 32) break;
-            const int x = lo + l;
-            const float wx = (l < len) ? w(x) : 0.f;
-            double tot2;
-            const double ex2v = warp_exscan_d(static_cast<double>(wx), tot2);
-            const bool c2 = wx > 0.f && base + ex2v + static_cast<double>(wx) > t;
-            const uint32_t b2 = __ballot_sync(0xffffffffu, c2);
-            if (b2) return lo + __ffs(b2) - 1;
-            const uint32_t bp = __ballot_sync(0xffffffffu, wx > 0.f);
-            return bp ? lo + 31 - __clz(bp) : (last_pos >= 0 ? last_pos : x0);
-        }
-    }
-    // a span longer than 32 after two levels (len > 32 * 32 * 32): scan it serially
-    double c = base;
-    int res = -1;
-    if (l == 0) {
-        for (int x = lo; x < lo + len; ++x) {
-            const float wx = w(x);
-            if (wx > 0.f) {
-                c += static_cast<double>(wx);
-                res = x;
-                if (c > t) break;
-            }
-        }
-    }
-    res = __shfl_sync(0xffffffffu, res, 0);
-    return res >= 0 ? res : (last_pos >= 0 ? last_pos : x0);
 }
 
 }  // namespace spec
