@@ -26,6 +26,9 @@
  *     aligned are streamed by the Tensor Memory Accelerator; other layouts
  *     are accepted and read with plain loads (slower).
  *   - Token ids are int32 in [0, V).  Output token rows are padded with -1.
+ *   - Shape limits (SPEC_UNSUPPORTED beyond them): B <= 4194302 requests per
+ *     call; K <= 4096 draft positions; N <= 8192 tree nodes; tree build
+ *     L <= 16, budget <= 256.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H

@@ -47,7 +47,7 @@ int sm_count() {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-    size_t off_ready, off_counter, zero_bytes, off_tasks, off_req, off_part, off_extra, off_persist, total;
+    size_t off_ready, off_counter, zero_bytes, off_req, off_part, off_extra, off_persist, total;
     uint32_t maxt, maxu, part_stride;
     uint64_t extra_stride;
     int smax;
@@ -65,12 +65,13 @@ Layout make_layout(int B, long long maxt, int cap_p, size_t extra_per_req, int s
     L.smax = smax;
     L.maxu = static_cast<uint32_t>(maxt * smax);   // a pushed task has at most smax slices
     L.off_ready = sizeof(spec::Ctrl);
-    L.off_counter = align_up(L.off_ready + 4ull * L.maxu, 16);
+    L.off_counter = align_up(L.off_ready + 16ull * L.maxu, 16);   // 16-byte unit records
     L.zero_bytes = align_up(L.off_counter + 4ull * B, 256);
-    L.off_tasks = L.zero_bytes;
-    L.off_req = align_up(L.off_tasks + sizeof(spec::Task) * maxt, 256);
+    L.off_req = L.zero_bytes;
     L.off_part = align_up(L.off_req + sizeof(spec::ReqState) * B, 256);
-    L.part_stride = static_cast<uint32_t>(align_up(sizeof(spec::PartHdr) + 8ull * cap_p, 128));
+    // room for at least the kPreKeys keys a combine fetches with the header
+    const int keys = cap_p > spec::kPreKeys ? cap_p : spec::kPreKeys;
+    L.part_stride = static_cast<uint32_t>(align_up(sizeof(spec::PartHdr) + 8ull * keys, 128));
     L.off_extra = align_up(L.off_part + static_cast<size_t>(B) * smax * L.part_stride, 256);
     L.extra_stride = align_up(extra_per_req, 256);
     L.off_persist = align_up(L.off_extra + static_cast<size_t>(B) * L.extra_stride, 128);
@@ -82,9 +83,8 @@ spec::Workspace make_ws(void* ws, const Layout& L) {
     unsigned char* p = static_cast<unsigned char*>(ws);
     spec::Workspace W;
     W.ctrl = reinterpret_cast<spec::Ctrl*>(p);
-    W.urec = reinterpret_cast<uint32_t*>(p + L.off_ready);
+    W.urec = reinterpret_cast<unsigned long long*>(p + L.off_ready);
     W.counter = reinterpret_cast<uint32_t*>(p + L.off_counter);
-    W.tasks = reinterpret_cast<spec::Task*>(p + L.off_tasks);
     W.req = reinterpret_cast<spec::ReqState*>(p + L.off_req);
     W.part = p + L.off_part;
     W.extra = p + L.off_extra;
@@ -99,6 +99,9 @@ spec::Workspace make_ws(void* ws, const Layout& L) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+#ifndef SPEC_FIRST_FACTOR
+#define SPEC_FIRST_FACTOR 4   // first-row units per CTA
+#endif
 // Slices per row: enough units to give every CTA several at the start, each
 // slice at least 32 KiB of row (a unit's fixed costs stay small next to its
 // stream), at most `max_s`.
@@ -107,7 +110,7 @@ void choose_slices(int B, int V, int esize, int grid, int max_s, int& S, int& SL
     if (g_tune_slices > 0) {
         s = g_tune_slices;
     } else {
-        s = static_cast<int>((4ll * grid + B - 1) / (B > 0 ? B : 1));
+        s = static_cast<int>((static_cast<long long>(SPEC_FIRST_FACTOR) * grid + B - 1) / (B > 0 ? B : 1));
         const long long row_bytes = static_cast<long long>(V) * esize;
         const int by_size = static_cast<int>((row_bytes + 32767) / 32768);
         if (s > by_size) s = by_size;
@@ -196,6 +199,7 @@ spec_status spec_verify_chain(
     void* ws, size_t ws_bytes, void* stream) {
     if (B < 0 || K < 0 || V < 1) return fail(SPEC_INVALID_ARG, "spec_verify_chain: need B >= 0, K >= 0, V >= 1");
     if (K > 4096) return fail(SPEC_UNSUPPORTED, "spec_verify_chain: K > 4096");
+    if (B > spec::kMaxRecB) return fail(SPEC_UNSUPPORTED, "spec_verify_chain: B > %d", spec::kMaxRecB);
     if (!valid_dtype(ldt)) return fail(SPEC_INVALID_ARG, "spec_verify_chain: unknown logits dtype %d", (int)ldt);
     if (!(temperature > 0.0f) || !(temperature < 3.0e38f))
         return fail(SPEC_INVALID_ARG, "spec_verify_chain: temperature must be finite and > 0");
@@ -264,6 +268,7 @@ spec_status spec_verify_greedy(
     void* ws, size_t ws_bytes, void* stream) {
     if (B < 0 || K < 0 || V < 1) return fail(SPEC_INVALID_ARG, "spec_verify_greedy: need B >= 0, K >= 0, V >= 1");
     if (K > 4096) return fail(SPEC_UNSUPPORTED, "spec_verify_greedy: K > 4096");
+    if (B > spec::kMaxRecB) return fail(SPEC_UNSUPPORTED, "spec_verify_greedy: B > %d", spec::kMaxRecB);
     if (!valid_dtype(ldt)) return fail(SPEC_INVALID_ARG, "spec_verify_greedy: unknown logits dtype");
     const bool ragged = k_per_req != nullptr;
     if (ragged != (l_row_off != nullptr))
@@ -322,6 +327,7 @@ spec_status spec_tree_build(
     if (B < 0 || L < 0 || V < 1 || budget < 1)
         return fail(SPEC_INVALID_ARG, "spec_tree_build: need B >= 0, L >= 0, V >= 1, budget >= 1");
     if (L > 16 || budget > 256) return fail(SPEC_UNSUPPORTED, "spec_tree_build: L <= 16 and budget <= 256");
+    if (B > spec::kMaxRecB) return fail(SPEC_UNSUPPORTED, "spec_tree_build: B > %d", spec::kMaxRecB);
     if (B == 0) return SPEC_OK;
     if (!token || !parent || !depth || !score || !anc_mask || !num_nodes || !status || !ws || (L > 0 && !q))
         return fail(SPEC_INVALID_ARG, "spec_tree_build: null pointer argument");
@@ -376,6 +382,8 @@ spec_status spec_verify_tree(
     if (B < 0 || N < 1 || V < 1 || max_depth < 0)
         return fail(SPEC_INVALID_ARG, "spec_verify_tree: need B >= 0, N >= 1, V >= 1, max_depth >= 0");
     if (!valid_dtype(ldt)) return fail(SPEC_INVALID_ARG, "spec_verify_tree: unknown logits dtype");
+    if (B > spec::kMaxRecB || N > spec::kMaxRecRow + 1)
+        return fail(SPEC_UNSUPPORTED, "spec_verify_tree: B > %d or N > %d", spec::kMaxRecB, spec::kMaxRecRow + 1);
     if (B == 0) return SPEC_OK;
     if (!logits || !token || !parent || !num_nodes || !path_nodes || !out_tokens || !num_accepted || !status || !ws)
         return fail(SPEC_INVALID_ARG, "spec_verify_tree: null pointer argument");

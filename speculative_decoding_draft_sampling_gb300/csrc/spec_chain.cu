@@ -40,6 +40,7 @@ struct CombPrep {
     int hinted;       // a slice streamed behind a hint
     int sl;           // slice length of the row
     uint32_t done;    // finished requests when the row arrived (an estimate, for the next row's slicing)
+    uint32_t base;    // arrival base of the request's next task
     float vmax;
     float pad;
     uint64_t theta;   // largest slice filter
@@ -143,18 +144,20 @@ __device__ __forceinline__ void chain_diag(const ChainArgs& A, int b, int i, flo
     d[0] = py; d[1] = qy; d[2] = Z; d[3] = R;
 }
 
-// lane 0: push the request's next task after an accepted position
-__device__ void chain_advance(const ChainArgs& A, int b, int row, int kb, int st, uint32_t hint, uint32_t done) {
-    ReqState* rs = &A.W.req[b];
-    __stcg(&rs->status, st);
+// lane 0: push the request's next task after an accepted position (the
+// record carries all the task needs: no release)
+__device__ void chain_advance(const ChainArgs& A, int b, int row, int kb, int st, uint32_t hint, uint32_t done,
+                              uint32_t base) {
     Task t;
     t.b = b;
     t.row = row + 1;
     t.kind = (row + 1 < kb) ? kVerify : kBonus;
     t.aux = static_cast<int>(hint);
+    t.st = st;
+    t.base = base;
     int S, SL;
     pick_slices(A.B, A.V, A.S, A.S1, done, S, SL);
-    push_task(A.W, t, S, SL);
+    push_task(A.W, t, S, SL, false);
 }
 
 // Acceptance of drafted y: u < p(y)/q(y).  With weights scaled by the
@@ -217,7 +220,7 @@ __device__ __forceinline__ uint32_t next_hint(float tau, float m) {
 // combine ended here (a bad row).
 template <class E>
 __device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st, int S, int SL,
-                             uint32_t done) {
+                             uint32_t done, uint32_t base) {
     const int l = threadIdx.x & 31;
     const int kb = chain_k(A, b);
     const float uk = chain_u(A, b, kb);
@@ -244,7 +247,7 @@ __device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, i
     int n = 0, fb = (flags & kPfOverflow) ? 1 : 0;
     if (!fb) {
         bool oflow;
-        n = gather_all_w(A.W, b, S, H, cs.list, kCombKeys, oflow, 8);
+        n = gather_all_w(A.W, b, S, H, cs.list, kCombKeys, oflow, kPreKeys);
         if (oflow) fb = 1;
     }
     SPEC_TRACE_EVW(6, b, row, n, kind);
@@ -253,6 +256,7 @@ __device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, i
         p.b = b; p.row = row; p.kind = kind; p.st = st; p.n = n; p.y = y; p.fallback = fb;
         p.sl = SL;
         p.done = done;
+        p.base = base;
         p.hinted = (flags & kPfHinted) ? 1 : 0;
         p.vmax = vmax; p.theta = theta; p.uk = uk; p.ur = ur;
     }
@@ -286,12 +290,11 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
         if (p.hinted) {
             // the hint was above the row's k-th value: stream the row again without it
             if (threadIdx.x == 0) {
-                __stcg(&A.W.req[b].status, st);
                 Task t;
-                t.b = b; t.row = row; t.kind = kind | kNoHint; t.aux = 0;
+                t.b = b; t.row = row; t.kind = kind | kNoHint; t.aux = 0; t.st = st; t.base = p.base;
                 int S, SL;
                 pick_slices(A.B, A.V, A.S, A.S1, p.done, S, SL);
-                push_task(A.W, t, S, SL);
+                push_task(A.W, t, S, SL, false);
             }
             return;
         }
@@ -313,9 +316,25 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
     const float tau = ckey_val(cand[keep - 1]);
     // weights e_x = 2^((l_x - m) c) and Z = sum over S in float-float; p(x) =
     // e_x / Z is never formed on this path (tests compare Z-scaled masses)
+    // Each thread holds up to kPer members of S: token, weight, and (VERIFY)
+    // q at the token, loaded now so that a rejection finds it in registers.
+    constexpr int kPer = kCombSet / kThreads;
     const float m = p.vmax, c2 = A.c2;
+    const float* qrow = kind == kVerify ? chain_qrow(A, b, row) : nullptr;
+    int xs[kPer];
+    float ev[kPer], qv[kPer];
     dfloat zpart = df_make(0.f);
-    for (int i = threadIdx.x; i < keep; i += kThreads) zpart = df_add(zpart, ex2((ckey_val(cand[i]) - m) * c2));
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int i = threadIdx.x + j * kThreads;
+        xs[j] = -1; ev[j] = 0.f; qv[j] = 0.f;
+        if (i < keep) {
+            xs[j] = ckey_idx(cand[i]);
+            ev[j] = ex2((ckey_val(cand[i]) - m) * c2);
+            zpart = df_add(zpart, ev[j]);
+            if (qrow && xs[j] >= 0 && xs[j] < A.V) qv[j] = __ldcg(qrow + xs[j]);   // keys hold in-range ids
+        }
+    }
     const dfloat Z = block_sum_df(zpart, sh.red2);
     const float Zf = Z.hi;
     auto prob = [&](float e) { return static_cast<float>(static_cast<double>(e) / df_to_d(Z)); };   // diagnostics
@@ -334,20 +353,29 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
 
     // Z-scaled weights of S sorted by token id (ascending): e_x, or for the
     // residual Z [p - q]_+ = [e_x - q_x Z]_+
-    auto sort_by_token = [&](bool residual, const float* qrow, dfloat& total) {
+    int rk[kPer];
+    bool ranked = false;
+    auto sort_by_token = [&](bool residual, dfloat& total) {
+        if (!ranked) {
+#pragma unroll
+            for (int j = 0; j < kPer; ++j) {
+                rk[j] = 0;
+                if (threadIdx.x + j * kThreads < keep)
+                    for (int t = 0; t < keep; ++t) rk[j] += ckey_idx(cand[t]) < xs[j];   // ids in S are distinct
+            }
+            ranked = true;
+        }
         dfloat part = df_make(0.f);
-        for (int i = threadIdx.x; i < keep; i += kThreads) {
-            const int x = ckey_idx(cand[i]);
-            int r = 0;
-            for (int j = 0; j < keep; ++j) r += ckey_idx(cand[j]) < x;
-            dfloat w = df_make(ex2((ckey_val(cand[i]) - m) * c2));
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            if (threadIdx.x + j * kThreads >= keep) continue;
+            dfloat w = df_make(ev[j]);
             if (residual) {
-                const float qx = (x >= 0 && x < A.V) ? qrow[x] : 0.f;   // keys always hold in-range ids
-                const dfloat d = df_add(w, df_neg(df_mul(qx, Z)));
+                const dfloat d = df_add(w, df_neg(df_mul(qv[j], Z)));
                 w = d.hi > 0.f ? d : df_make(0.f);
             }
-            cs.tok[r] = x;
-            cs.wgt[r] = make_float2(w.hi, w.lo);
+            cs.tok[rk[j]] = xs[j];
+            cs.wgt[rk[j]] = make_float2(w.hi, w.lo);
             part = df_add(part, w);
         }
         total = block_sum_df(part, sh.red2);
@@ -366,17 +394,17 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
         if (acc) {
             if (threadIdx.x == 0) {
                 if (A.diag) chain_diag(A, b, row, prob(ey), qy, Zf, 0.f);
-                chain_advance(A, b, row, kb, st, hint, p.done);
+                chain_advance(A, b, row, kb, st, hint, p.done, p.base);
             }
             SPEC_TRACE_EV(9, b, row, 1, kind);
             return;
         }
         // residual [p - q]_+ lives on S (p = 0 outside it)
         dfloat R_mass;
-        sort_by_token(true, chain_qrow(A, b, row), R_mass);
+        sort_by_token(true, R_mass);
         if (!(R_mass.hi > 0.f)) {
             st |= 4;
-            sort_by_token(false, nullptr, R_mass);
+            sort_by_token(false, R_mass);
         }
         int x = -1;
         if (threadIdx.x < 32)
@@ -393,7 +421,7 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
     }
     // bonus row: draw from p
     dfloat tot;
-    sort_by_token(false, nullptr, tot);
+    sort_by_token(false, tot);
     int x = -1;
     if (threadIdx.x < 32) x = warp_icdf_pairs(cs.tok, cs.wgt, keep, df_mul(p.uk, tot));
     if (threadIdx.x == 0) sh.ish[0] = x;
@@ -445,7 +473,7 @@ __device__ void chain_fallback_cta(const ChainArgs& A, ChainSmem<true>& sh, int 
         if (chain_accept_z(A, y, ey, qy, Z, chain_u(A, b, row), st)) {
             if (threadIdx.x == 0) {
                 if (A.diag) chain_diag(A, b, row, py(), qy, Z.hi, 0.f);
-                chain_advance(A, b, row, kb, st, 0u, sh.comb.prep.done);
+                chain_advance(A, b, row, kb, st, 0u, sh.comb.prep.done, sh.comb.prep.base);
             }
             return;
         }
@@ -503,7 +531,7 @@ __device__ __forceinline__ dfloat df_of(float2 v) { return dfloat{v.x, v.y}; }
 // are Z-scaled (weights e_x = 2^((l_x - m) c)), float-float across slices.
 template <class E>
 __device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st, int S, int SL,
-                             uint32_t done) {
+                             uint32_t done, uint32_t base) {
     const int l = threadIdx.x & 31;
     const int kb = chain_k(A, b);
     const float c2 = A.c2;
@@ -566,19 +594,18 @@ __device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, i
         const bool acc = chain_accept_z(A, y, ey, qy, Z, ur, st);
         if (l == 0 && A.diag) chain_diag(A, b, row, static_cast<float>(static_cast<double>(ey) / df_to_d(Z)), qy, Z.hi, 0.f);
         if (acc) {
-            if (l == 0) chain_advance(A, b, row, kb, st, 0u, done);
+            if (l == 0) chain_advance(A, b, row, kb, st, 0u, done, base);
             return false;
         }
         if (l == 0) {
             ReqState* rs = &A.W.req[b];
             __stcg(&rs->m, m);
             __stcg(&rs->invZ, __frcp_rn(Z.hi));
-            __stcg(&rs->status, st);
             Task t;
-            t.b = b; t.row = row; t.kind = kResid; t.aux = 0;
+            t.b = b; t.row = row; t.kind = kResid; t.aux = 0; t.st = st; t.base = base;
             int S1, SL1;
             pick_slices(A.B, A.V, A.S, A.S1, done, S1, SL1);
-            push_task(A.W, t, S1, SL1);
+            push_task(A.W, t, S1, SL1, true);   // the residual units read m and 1/Z
         }
         return false;
     }
@@ -662,19 +689,19 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
         uint32_t cpub = 0;
         combiner_loop(P, [&](const Job& job) {
             const int b = job.task.b;
-            uint32_t done;
-            if (!comb_arrive(A.W, b, task_S(A, job.task), &done)) return;
+            uint32_t done, base;
+            if (!comb_arrive(A.W, job.task, task_S(A, job.task), &done, &base)) return;
             SPEC_TRACE_EVW(2, b, job.task.row, job.slice, job.kind);
-            const int st = job.task.kind < 0 ? 0 : __ldcg(&A.W.req[b].status);
+            const int st = job.task.st;
             if (job.kind == kInvalid) {
                 chain_finish(A, b, 0, -1, 16);
             } else if constexpr (kTopk) {
                 if (prepare_topk<E>(A, sh.comb, b, job.task.row, job.kind, st, task_S(A, job.task),
-                                    task_SL(A, job.task), done))
+                                    task_SL(A, job.task), done, base))
                     publish_combine(P, cpub);
             } else {
                 if (combine_full<E>(A, sh.comb, b, job.task.row, job.kind, st, task_S(A, job.task),
-                                    task_SL(A, job.task), done))
+                                    task_SL(A, job.task), done, base))
                     publish_combine(P, cpub);
             }
             __syncwarp();
@@ -845,7 +872,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
     }
     // stop the combiner once it has taken every job (serving its last combines)
     Job j;
-    j.task.b = 0; j.task.row = 0; j.task.kind = 0; j.task.aux = 0;
+    j.task.b = 0; j.task.row = 0; j.task.kind = 0; j.task.aux = 0; j.task.st = 0; j.task.base = 0;
     j.slice = 0; j.kind = 0; j.stop = 1; j.flags = 0;
     post_job(P, jseq, cseq, j, serve);
     // combines still in the combiner's queue are served until it stops

@@ -122,6 +122,8 @@ static_assert(sizeof(Ctrl) == 640, "Ctrl is five 128-byte lines");
 
 struct Task {
     int32_t b, row, kind, aux;
+    int32_t st;       // the request's SPEC_ST_* bits so far
+    uint32_t base;    // the request's arrival count before this task (mod 2^kBaseBits)
 };
 // A pushed task's kind word: bits 0-7 the kernel's kind, 8-13 its slice
 // count, 14-31 its slice length / 64 (initial tasks have kind -1 and take
@@ -136,9 +138,7 @@ __host__ __device__ __forceinline__ int task_kind_SL(int kind) { return ((kind >
 struct ReqState {
     float m;           // row maximum (logit), carried to a residual pass
     float invZ;        // 1 / Z rounded to fp32: the residual pass and its rescan share it
-    int32_t status;    // accumulated SPEC_ST_* bits
-    int32_t pad0;
-    double pad[6];
+    double pad[7];
 };
 static_assert(sizeof(ReqState) == 64, "ReqState is 64 bytes");
 
@@ -161,9 +161,8 @@ enum : uint32_t { kPfBad = 1u, kPfOverflow = 2u, kPfHinted = 4u };
 // Device view of the caller's workspace; offsets computed on the host.
 struct Workspace {
     Ctrl* ctrl;
-    uint32_t* urec;       // [maxu] pushed units: ((task + 1) << 6) | slice once pushed, else 0 (zeroed per call)
-    uint32_t* counter;    // [B] arrival counters (zeroed per call)
-    Task* tasks;          // [maxt]
+    unsigned long long* urec;   // [maxu][2] pushed unit records, zero until pushed (zeroed per call)
+    uint32_t* counter;    // [B] arrivals per request, never reset within a call (zeroed per call)
     ReqState* req;        // [B]
     unsigned char* part;  // [B][S] partials, part_stride bytes each
     unsigned char* extra; // [B] per-request op scratch, extra_stride bytes each
@@ -188,6 +187,34 @@ __device__ __forceinline__ uint64_t* part_keys(const Workspace& W, int b, int s,
 // ---------------------------------------------------------------------------
 // queue
 // ---------------------------------------------------------------------------
+// A pushed unit's record carries its whole task, so that a claimer needs no
+// further read and a push needs no fence when the task depends on nothing
+// else the pusher wrote.  w0: b + 1 (bits 0-21), row (22-34), slice (35-40),
+// st (41-45), base (46-63); w1: the packed kind (low word), aux (high word).
+// Both words are nonzero once written (b + 1 >= 1; the kind word holds S >= 1).
+constexpr int kBaseBits = 18;
+constexpr uint32_t kBaseMask = (1u << kBaseBits) - 1u;
+constexpr int kMaxRecB = (1 << 22) - 2;     // requests per call
+constexpr int kMaxRecRow = (1 << 13) - 1;   // row (or node) index
+__device__ __forceinline__ void rec_encode(const Task& t, int slice, unsigned long long& w0, unsigned long long& w1) {
+    w0 = static_cast<unsigned long long>(static_cast<uint32_t>(t.b + 1) & 0x3fffffu) |
+         (static_cast<unsigned long long>(static_cast<uint32_t>(t.row) & 0x1fffu) << 22) |
+         (static_cast<unsigned long long>(static_cast<uint32_t>(slice) & 63u) << 35) |
+         (static_cast<unsigned long long>(static_cast<uint32_t>(t.st) & 31u) << 41) |
+         (static_cast<unsigned long long>(t.base & kBaseMask) << 46);
+    w1 = static_cast<unsigned long long>(static_cast<uint32_t>(t.kind)) |
+         (static_cast<unsigned long long>(static_cast<uint32_t>(t.aux)) << 32);
+}
+__device__ __forceinline__ void rec_decode(unsigned long long w0, unsigned long long w1, Task& t, int& slice) {
+    t.b = static_cast<int>(w0 & 0x3fffffu) - 1;
+    t.row = static_cast<int>((w0 >> 22) & 0x1fffu);
+    slice = static_cast<int>((w0 >> 35) & 63u);
+    t.st = static_cast<int>((w0 >> 41) & 31u);
+    t.base = static_cast<uint32_t>(w0 >> 46) & kBaseMask;
+    t.kind = static_cast<int>(static_cast<uint32_t>(w1));
+    t.aux = static_cast<int>(static_cast<uint32_t>(w1 >> 32));
+}
+
 struct Claimed {
     Task task;
     int slice;
@@ -208,7 +235,7 @@ __device__ inline Claimed claim_unit(const Workspace& W, int B, int S0, bool& co
     c.ok = 1;
     c.hint = 0;
     c.pad = 0;
-    c.task.b = 0; c.task.row = 0; c.task.kind = -1; c.task.aux = 0;
+    c.task.b = 0; c.task.row = 0; c.task.kind = -1; c.task.aux = 0; c.task.st = 0; c.task.base = 0;
     if (cold) {
         const uint32_t u0 = atomicAdd(&W.ctrl->head, 1u);
         if (u0 < static_cast<uint32_t>(B) * static_cast<uint32_t>(S0)) {
@@ -223,14 +250,10 @@ __device__ inline Claimed claim_unit(const Workspace& W, int B, int S0, bool& co
     uint32_t ns = 32;
     SPEC_TRACE_EV(10, -1, -1, -1, static_cast<int>(u));
     for (uint32_t it = 0;; ++it) {
-        const uint32_t rec = ld_acquire(&W.urec[u]);
-        if (rec) {
-            const uint32_t ti = (rec >> 6) - 1u;
-            c.slice = static_cast<int>(rec & 63u);
-            c.task.b = __ldcg(&W.tasks[ti].b);
-            c.task.row = __ldcg(&W.tasks[ti].row);
-            c.task.kind = __ldcg(&W.tasks[ti].kind);
-            c.task.aux = __ldcg(&W.tasks[ti].aux);
+        unsigned long long w0, w1;
+        ld_acquire_v2(W.urec + 2ull * u, w0, w1);
+        if (w0 != 0ull && w1 != 0ull) {
+            rec_decode(w0, w1, c.task, c.slice);
             return c;
         }
         if (ld_acquire(&W.ctrl->done) >= static_cast<uint32_t>(B)) { c.ok = 0; return c; }
@@ -244,47 +267,53 @@ __device__ inline Claimed claim_unit(const Workspace& W, int B, int S0, bool& co
 // Combiner warp: count the arrival of a finished unit (its partial was
 // written by the consumers, ordered before the job hand-over).  Returns
 // true in every lane when the unit completed the task's last slice; this
-// CTA's combiner then owns the combine.
-__device__ __forceinline__ bool comb_arrive(const Workspace& W, int b, int S, uint32_t* done_est = nullptr) {
+// CTA's combiner then owns the combine.  A request has one task in flight,
+// and its counter only grows: the task's arrivals are those past its base,
+// and the last one's count is the base of the request's next task.
+__device__ __forceinline__ bool comb_arrive(const Workspace& W, const Task& t, int S, uint32_t* done_est,
+                                            uint32_t* next_base) {
     int last = 0;
-    uint32_t dn = 0;
+    uint32_t dn = 0, nb = 0;
     if ((threadIdx.x & 31) == 0) {
         fence_acq_rel_gpu();   // release the partial (cumulative over the hand-over)
-        const uint32_t prev = atomicAdd(&W.counter[b], 1u);
+        const uint32_t prev = atomicAdd(&W.counter[t.b], 1u);
         dn = ld_relaxed(&W.ctrl->done);   // (for the next row's slicing; not ordered)
-        last = (prev == static_cast<uint32_t>(S - 1));
-        if (last) {
-            fence_acq_rel_gpu();   // acquire the other slices' partials
-            W.counter[b] = 0;      // ready for the request's next task
-        }
+        nb = (prev + 1u) & kBaseMask;
+        last = (((prev + 1u - t.base) & kBaseMask) == static_cast<uint32_t>(S));
+        if (last) fence_acq_rel_gpu();   // acquire the other slices' partials
     }
     if (done_est) *done_est = __shfl_sync(0xffffffffu, dn, 0);
+    if (next_base) *next_base = __shfl_sync(0xffffffffu, nb, 0);
     return __shfl_sync(0xffffffffu, last, 0) != 0;
 }
 
 // One lane: enqueue the request's next task, cut into S slices of SL
-// elements.  One 64-bit atomic reserves the task slot and its S unit
-// records; the records are written after a fence that orders the task and
-// every earlier write of this lane (the request state) before them.
-__device__ __forceinline__ void push_task(const Workspace& W, Task t, int S, int SL) {
+// elements.  One 64-bit atomic reserves a task count (bounded by the
+// workspace) and S unit records; each record carries the whole task.
+__device__ __forceinline__ void push_task(const Workspace& W, Task t, int S, int SL, bool release) {
     t.kind = task_kind_pack(t.kind, S, SL);
     const unsigned long long r = atomicAdd(&W.ctrl->tailc, (1ull << 32) | static_cast<unsigned long long>(S));
     const uint32_t ti = static_cast<uint32_t>(r >> 32), u0 = static_cast<uint32_t>(r);
     if (ti >= W.maxt || u0 + static_cast<uint32_t>(S) > W.maxu) { atomicOr(&W.ctrl->error, kErrQueue); return; }
-    __stcg(&W.tasks[ti].b, t.b);
-    __stcg(&W.tasks[ti].row, t.row);
-    __stcg(&W.tasks[ti].kind, t.kind);
-    __stcg(&W.tasks[ti].aux, t.aux);
-    fence_acq_rel_gpu();
-    for (int s = 0; s < S; ++s) st_relaxed(&W.urec[u0 + s], ((ti + 1u) << 6) | static_cast<uint32_t>(s));
+    // release: the task's units or combine read what the pusher wrote
+    // before (request state beyond the record)
+    if (release) fence_acq_rel_gpu();
+    for (int s = 0; s < S; ++s) {
+        unsigned long long w0, w1;
+        rec_encode(t, s, w0, w1);
+        st_relaxed_v2(W.urec + 2ull * (u0 + s), w0, w1);
+    }
 }
 
 // Slices of a pushed row: a first row's while most requests are active;
 // finer as requests finish, so that the remaining chains keep the grid busy
 // (at most smax).  done = finished requests (an estimate).
+#ifndef SPEC_SLICE_FACTOR
+#define SPEC_SLICE_FACTOR 2   // pushed units per CTA when every active request has one row queued
+#endif
 __device__ __forceinline__ void pick_slices(int B, int V, int S0, int smax, uint32_t done, int& S, int& SL) {
     const int active = B - static_cast<int>(done) > 1 ? B - static_cast<int>(done) : 1;
-    int s = (2 * static_cast<int>(gridDim.x) + active - 1) / active;
+    int s = (SPEC_SLICE_FACTOR * static_cast<int>(gridDim.x) + active - 1) / active;
     if (s < S0) s = S0;
     if (s > smax) s = smax;
     SL = (((V + s - 1) / s) + 63) & ~63;
@@ -451,7 +480,7 @@ __device__ void producer_loop(const Workspace& W, int B, int S0, const Pipe& P, 
         Claimed c;
         if (dead || *P.abort) {
             c.ok = 0; c.slice = 0; c.hint = 0; c.pad = 0;
-            c.task.b = 0; c.task.row = 0; c.task.kind = 0; c.task.aux = 0;
+            c.task.b = 0; c.task.row = 0; c.task.kind = 0; c.task.aux = 0; c.task.st = 0; c.task.base = 0;
         } else {
             c = claim_unit(W, B, S0, cold);
             if (c.ok) fetch(c);
@@ -842,17 +871,18 @@ struct SliceHdrs {
 
 // Combiner warp: lane s loads slice s's header (one round trip), offsets by
 // a warp scan.  With `list`, the same round trip also fetches each slice's
-// first 8 keys into list[off_s ..] (speculatively: the slot always holds
-// room for them), so that gather_all_w only fetches what lies beyond.
+// first kPreKeys keys into list[off_s ..] (speculatively: the slot always
+// holds room for them), so that gather_all_w only fetches what lies beyond.
+constexpr int kPreKeys = 16;
 __device__ inline void load_hdrs_w(const Workspace& W, int b, int S, SliceHdrs& H, uint64_t* list = nullptr,
                                    int cap = 0) {
     const int l = threadIdx.x & 31;
     int c = 0;
-    uint64_t k8[8];
+    ulonglong2 kp[kPreKeys / 2];
     if (list && l < S) {
-        const uint64_t* src = part_keys(W, b, l, S);
+        const ulonglong2* src = reinterpret_cast<const ulonglong2*>(part_keys(W, b, l, S));   // 16-byte aligned
 #pragma unroll
-        for (int j = 0; j < 8; ++j) k8[j] = __ldcg(src + j);
+        for (int j = 0; j < kPreKeys / 2; ++j) kp[j] = __ldcg(src + j);
     }
     if (l < S) {
         const PartHdr* h = part_hdr(W, b, l, S);
@@ -872,8 +902,10 @@ __device__ inline void load_hdrs_w(const Workspace& W, int b, int S, SliceHdrs& 
     if (l == 0) H.off[S] = tot;
     if (list && l < S) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j < c && off + j < cap) list[off + j] = k8[j];
+        for (int j = 0; j < kPreKeys / 2; ++j) {
+            if (2 * j < c && off + 2 * j < cap) list[off + 2 * j] = kp[j].x;
+            if (2 * j + 1 < c && off + 2 * j + 1 < cap) list[off + 2 * j + 1] = kp[j].y;
+        }
     }
     __syncwarp();
 }

@@ -175,7 +175,7 @@ __device__ void build_finalize(const BuildArgs& A, unsigned long long* msk, cons
 // The combine of one depth row (combiner warp): merge the slice lists into
 // the depth's sorted top-M, then resume the best-first enumeration.
 __device__ void build_combine(const BuildArgs& A, BuildSmem& sh, unsigned char* scr, Ent* nodes, Ent* pend,
-                              const Job& job, uint32_t done) {
+                              const Job& job, uint32_t done, uint32_t base) {
     const int l = threadIdx.x & 31;
     const int N = A.N, M = A.M, L = A.L;
     const int b = job.task.b;
@@ -324,10 +324,10 @@ __device__ void build_combine(const BuildArgs& A, BuildSmem& sh, unsigned char* 
         __syncwarp();
         if (l == 0) {
             Task nt;
-            nt.b = b; nt.row = need - 1; nt.kind = 0; nt.aux = 0;
+            nt.b = b; nt.row = need - 1; nt.kind = 0; nt.aux = 0; nt.st = 0; nt.base = base;
             int S1, SL1;
             pick_slices(A.B, A.V, A.S, A.S1, done, S1, SL1);
-            push_task(A.W, nt, S1, SL1);
+            push_task(A.W, nt, S1, SL1, true);   // the next combine reads the saved state
         }
     }
     __syncwarp();
@@ -353,7 +353,9 @@ __global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs
     if (threadIdx.x >= kCombiner0) {
         combiner_loop(P, [&](const Job& job) {
             uint32_t done;
-            if (comb_arrive(A.W, job.task.b, task_S(A, job.task), &done)) build_combine(A, sh, scr, nodes, pend, job, done);
+            uint32_t base;
+            if (comb_arrive(A.W, job.task, task_S(A, job.task), &done, &base))
+                build_combine(A, sh, scr, nodes, pend, job, done, base);
             __syncwarp();
         });
         return;
@@ -441,7 +443,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs
         post_job(P, jseq, cseq, j, serve);
     }
     Job j;
-    j.task.b = 0; j.task.row = 0; j.task.kind = 0; j.task.aux = 0;
+    j.task.b = 0; j.task.row = 0; j.task.kind = 0; j.task.aux = 0; j.task.st = 0; j.task.base = 0;
     j.slice = 0; j.kind = 0; j.stop = 1; j.flags = 0;
     post_job(P, jseq, cseq, j, serve);
 }

@@ -80,13 +80,13 @@ __device__ __forceinline__ bool walk_invalid(const WalkArgs& A, const Task& t) {
 // The combine of one row (combiner warp): argmax over the slice partials,
 // then the greedy decision or the tree step.
 template <class E, bool kTree>
-__device__ void walk_combine(const WalkArgs& A, const Job& job, uint32_t done) {
+__device__ void walk_combine(const WalkArgs& A, const Job& job, uint32_t done, uint32_t base) {
     const int l = threadIdx.x & 31;
     const int b = job.task.b;
     const int row = job.task.row;
     const bool initial = job.task.kind < 0;
     const int acc = initial ? 0 : job.task.aux;
-    int st = initial ? 0 : __ldcg(&A.W.req[b].status);
+    int st = job.task.st;
     if (job.kind != 0) {   // invalid k
         greedy_finish(A, b, 0, -1, 16);
         return;
@@ -112,12 +112,11 @@ __device__ void walk_combine(const WalkArgs& A, const Job& job, uint32_t done) {
         if (y < 0 || y >= A.V) st |= 8;
         if (y != am) { greedy_finish(A, b, row, am, st); return; }
         if (l == 0) {
-            __stcg(&A.W.req[b].status, st);
             Task nt;
-            nt.b = b; nt.row = row + 1; nt.kind = 0; nt.aux = 0;
+            nt.b = b; nt.row = row + 1; nt.kind = 0; nt.aux = 0; nt.st = st; nt.base = base;
             int S1, SL1;
             pick_slices(A.B, A.V, A.S, A.S1, done, S1, SL1);
-            push_task(A.W, nt, S1, SL1);
+            push_task(A.W, nt, S1, SL1, false);
         }
     } else {
         if (bad_row) { tree_finish(A, b, acc, -1, st | 1); return; }
@@ -135,12 +134,11 @@ __device__ void walk_combine(const WalkArgs& A, const Job& job, uint32_t done) {
             const int W = A.L + 1;
             A.out_tokens[static_cast<long long>(b) * W + acc] = am;
             A.path_nodes[static_cast<long long>(b) * W + acc + 1] = child;
-            __stcg(&A.W.req[b].status, st);
             Task nt;
-            nt.b = b; nt.row = child; nt.kind = 0; nt.aux = acc + 1;
+            nt.b = b; nt.row = child; nt.kind = 0; nt.aux = acc + 1; nt.st = st; nt.base = base;
             int S1, SL1;
             pick_slices(A.B, A.V, A.S, A.S1, done, S1, SL1);
-            push_task(A.W, nt, S1, SL1);
+            push_task(A.W, nt, S1, SL1, false);   // outputs only: nothing for later tasks to read
         }
     }
 }
@@ -160,7 +158,8 @@ __global__ void __launch_bounds__(kBlockThreads, 2) walk_kernel(const WalkArgs A
     if (threadIdx.x >= kCombiner0) {
         combiner_loop(P, [&](const Job& job) {
             uint32_t done;
-            if (comb_arrive(A.W, job.task.b, task_S(A, job.task), &done)) walk_combine<E, kTree>(A, job, done);
+            uint32_t base;
+            if (comb_arrive(A.W, job.task, task_S(A, job.task), &done, &base)) walk_combine<E, kTree>(A, job, done, base);
             __syncwarp();
         });
         return;
@@ -204,7 +203,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) walk_kernel(const WalkArgs A
         post_job(P, jseq, cseq, j, serve);
     }
     Job j;
-    j.task.b = 0; j.task.row = 0; j.task.kind = 0; j.task.aux = 0;
+    j.task.b = 0; j.task.row = 0; j.task.kind = 0; j.task.aux = 0; j.task.st = 0; j.task.base = 0;
     j.slice = 0; j.kind = 0; j.stop = 1; j.flags = 0;
     post_job(P, jseq, cseq, j, serve);
 }
