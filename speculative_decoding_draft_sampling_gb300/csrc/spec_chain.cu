@@ -51,14 +51,20 @@ struct CombPrep {
     dfloat t;
     double Z, R;        // diagnostics
 };
+// Written by the combiner warp while the consumers stream; the consumers'
+// own scratch for a combine lives in TopkSmem (free at unit boundaries,
+// where they serve combines): select ranks in `slot`, the selected keys in
+// the first kCombOut entries of `cand`, tokens and weights after them.
 struct CombSmem {
     SliceHdrs hdrs;
     CombPrep prep;
     alignas(16) uint64_t list[kCombKeys];
-    int rank[kCombKeys];
-    int tok[kCombSet];
-    float2 wgt[kCombSet];    // float-float weights (hi, lo)
 };
+constexpr int kCombOut = 1024;   // select output (> kCombSet: a larger set takes the exact path)
+static_assert(sizeof(uint64_t) * TopkSmem::kSlots * kThreads >= sizeof(int) * kCombKeys, "ranks fit in slot");
+static_assert(sizeof(uint64_t) * (kCombOut) + (sizeof(int) + sizeof(float2)) * kCombSet <=
+                  sizeof(uint64_t) * kWarps * TopkSmem::kRegion,
+              "selected keys, tokens and weights fit in cand");
 
 template <bool kTopk> struct ChainTopkPart {};
 template <> struct ChainTopkPart<true> { TopkSmem tk; };
@@ -277,6 +283,7 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
     const CombPrep p = cs.prep;
     const int b = p.b, row = p.row, kind = p.kind, k = A.top_k;
     int st = p.st;
+    SPEC_TRACE_EV(20, b, row, 0, kind);
     const int kb = chain_k(A, b);
     if (p.fallback) {
         chain_fallback_cta<E>(A, sh, b, row, kind, st, p.vmax);
@@ -304,8 +311,10 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
     uint64_t kth;
     bool of = false;
     uint64_t* cand = sh.tk.cand;
-    constexpr int kCandCap = kWarps * TopkSmem::kRegion;
-    const int keep = select_to(list, n, k, true, cs.rank, cand, kCandCap, kth, of, sh.sh64, sh.ired);
+    int* ctok = reinterpret_cast<int*>(cand + kCombOut);
+    float2* cwgt = reinterpret_cast<float2*>(ctok + kCombSet);
+    const int keep = select_to(list, n, k, true, reinterpret_cast<int*>(&sh.tk.slot[0][0]), cand, kCombOut, kth, of,
+                               sh.sh64, sh.ired);
     SPEC_TRACE_EV(7, b, row, n, kind);
     if (of || keep > kCombSet) {
         chain_fallback_cta<E>(A, sh, b, row, kind, st, p.vmax);
@@ -374,8 +383,8 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
                 const dfloat d = df_add(w, df_neg(df_mul(qv[j], Z)));
                 w = d.hi > 0.f ? d : df_make(0.f);
             }
-            cs.tok[rk[j]] = xs[j];
-            cs.wgt[rk[j]] = make_float2(w.hi, w.lo);
+            ctok[rk[j]] = xs[j];
+            cwgt[rk[j]] = make_float2(w.hi, w.lo);
             part = df_add(part, w);
         }
         total = block_sum_df(part, sh.red2);
@@ -408,7 +417,7 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
         }
         int x = -1;
         if (threadIdx.x < 32)
-            x = warp_icdf_pairs(cs.tok, cs.wgt, keep, df_mul(p.uk, R_mass));
+            x = warp_icdf_pairs(ctok, cwgt, keep, df_mul(p.uk, R_mass));
         if (threadIdx.x == 0) {
             sh.ish[0] = x;
             if (A.diag) chain_diag(A, b, row, prob(ey), qy, Zf, (st & 4) ? 0.f : static_cast<float>(df_to_d(R_mass) / df_to_d(Z)));
@@ -423,7 +432,7 @@ __device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
     dfloat tot;
     sort_by_token(false, tot);
     int x = -1;
-    if (threadIdx.x < 32) x = warp_icdf_pairs(cs.tok, cs.wgt, keep, df_mul(p.uk, tot));
+    if (threadIdx.x < 32) x = warp_icdf_pairs(ctok, cwgt, keep, df_mul(p.uk, tot));
     if (threadIdx.x == 0) sh.ish[0] = x;
     csync();
     x = sh.ish[0];
@@ -679,6 +688,9 @@ template <class E, bool kTopk>
 __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     auto& sh = *reinterpret_cast<ChainSmem<kTopk>*>(smem + kStages * kChunkBytes);
+    if constexpr (kTopk) {
+        if (threadIdx.x == 0) topk_smem_init(sh.tk);   // made visible by pipe_init's barrier
+    }
     const Pipe P = pipe_init(smem, sh.pipe);
     // the residual pass streams q beside the logits; without q rows (K = 0)
     // there is no residual pass
@@ -695,6 +707,8 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
             const int st = job.task.st;
             if (job.kind == kInvalid) {
                 chain_finish(A, b, 0, -1, 16);
+            } else if (!combine_reuse(P, cpub)) {
+                return;   // the consumers stopped answering: the kernel is aborting
             } else if constexpr (kTopk) {
                 if (prepare_topk<E>(A, sh.comb, b, job.task.row, job.kind, st, task_S(A, job.task),
                                     task_SL(A, job.task), done, base))
@@ -706,7 +720,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
             }
             __syncwarp();
             SPEC_TRACE_EVW(3, b, job.task.row, job.slice, job.kind);
-        });
+        }, [&]() { combine_reuse(P, cpub); });
         return;
     }
     if (threadIdx.x >= kThreads) {
@@ -715,12 +729,13 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
                           [&](Claimed& c) {
                               if (kTopk && c.task.kind < 0) {
                                   // the latest finished row of this call, else of the previous call
-                                  // on this workspace
-                                  c.hint = __ldcg(&A.W.ctrl->hint0);
-                                  if (c.hint == 0 && __ldcg(&A.W.persist[0]) == kPersistTag &&
-                                      __ldcg(&A.W.persist[2]) == static_cast<uint32_t>(A.V) &&
-                                      __ldcg(&A.W.persist[3]) == static_cast<uint32_t>(A.top_k))
-                                      c.hint = __ldcg(&A.W.persist[1]);
+                                  // on this workspace (all five words in one round trip)
+                                  const uint32_t h0 = __ldcg(&A.W.ctrl->hint0);
+                                  const uint4 ps = __ldcg(reinterpret_cast<const uint4*>(A.W.persist));
+                                  c.hint = h0;
+                                  if (h0 == 0 && ps.x == kPersistTag && ps.z == static_cast<uint32_t>(A.V) &&
+                                      ps.w == static_cast<uint32_t>(A.top_k))
+                                      c.hint = ps.y;
                               }
                           },
                           [&](const Claimed& c) {
@@ -764,7 +779,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
             if constexpr (kTopk) {
                 const uint32_t hint = nohint ? 0u : (initial ? cl.hint : static_cast<uint32_t>(t.aux));
                 TopkHistFn<E, true> fn;
-                fn.init(&sh.tk, A.top_k, hint);
+                fn.init(&sh.tk, A.top_k, hint, u + 1u);
                 fn.dw = dw;
                 ok = consume_row<E>(P, seq, plan, tma, x0, fn);
                 if (ok) {
@@ -782,6 +797,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
                     int n = tot;
                     if (!bad && !oflow && tot <= A.cap_p) {
                         fn.write_keys(pk);   // every warp's keys at its offset
+                        SPEC_TRACE_EV(17, b, row, s, tot);
                     } else if (!bad && !oflow) {
                         // too many: the certified bound over every candidate, repeated
                         // until it stops rising (then it is the exact k-th value)
@@ -798,6 +814,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
                         }
                         if (n > A.cap_p) oflow = 1;   // ties at the k-th value: the fallback decides
                         else for (int i = threadIdx.x; i < n; i += kThreads) __stcg(pk + i, list[i]);
+                        SPEC_TRACE_EV(17, b, row, s, tot | (1 << 20));
                     }
                     if (oflow || bad) n = 0;   // the combine does not read the keys then
                     if (threadIdx.x == 0) {
@@ -869,6 +886,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
         Job j;
         j.task = t; j.slice = s; j.kind = kind; j.stop = 0; j.flags = 0;
         post_job(P, jseq, cseq, j, serve);
+        SPEC_TRACE_EV(18, b, row, s, 0);
     }
     // stop the combiner once it has taken every job (serving its last combines)
     Job j;

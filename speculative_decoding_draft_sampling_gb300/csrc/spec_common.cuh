@@ -80,9 +80,9 @@ __device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
 }
 // 128-bit record halves: each 64-bit half is single-copy atomic (a reader
 // that needs both waits until neither reads zero)
-__device__ __forceinline__ void ld_acquire_v2(const unsigned long long* p, unsigned long long& a,
+__device__ __forceinline__ void ld_relaxed_v2(const unsigned long long* p, unsigned long long& a,
                                               unsigned long long& b) {
-    asm volatile("ld.acquire.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 __device__ __forceinline__ void st_relaxed_v2(unsigned long long* p, unsigned long long a, unsigned long long b) {
     asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");

@@ -70,6 +70,7 @@ __device__ __forceinline__ void trace_ev(int ev, int b, int row, int slice, int 
     do { if (threadIdx.x == 0) ::spec::trace_ev((ev), (b), (row), (slice), (aux)); } while (0)
 #define SPEC_TRACE_EVW(ev, b, row, slice, aux) \
     do { if ((threadIdx.x & 31) == 0) ::spec::trace_ev((ev), (b), (row), (slice), (aux)); } while (0)
+#define SPEC_TRACE_EV1(ev, b, row, slice, aux) ::spec::trace_ev((ev), (b), (row), (slice), (aux))
 #define SPEC_TRACE_EXPORT(name)                                                              \
     extern "C" int spec_trace_setup_##name(void* buf, unsigned cap) {                        \
         unsigned z = 0;                                                                      \
@@ -85,6 +86,7 @@ __device__ __forceinline__ void trace_ev(int ev, int b, int row, int slice, int 
 #else
 #define SPEC_TRACE_EV(ev, b, row, slice, aux)
 #define SPEC_TRACE_EVW(ev, b, row, slice, aux)
+#define SPEC_TRACE_EV1(ev, b, row, slice, aux)
 #define SPEC_TRACE_EXPORT(name)
 #endif
 
@@ -190,18 +192,22 @@ __device__ __forceinline__ uint64_t* part_keys(const Workspace& W, int b, int s,
 // A pushed unit's record carries its whole task, so that a claimer needs no
 // further read and a push needs no fence when the task depends on nothing
 // else the pusher wrote.  w0: b + 1 (bits 0-21), row (22-34), slice (35-40),
-// st (41-45), base (46-63); w1: the packed kind (low word), aux (high word).
-// Both words are nonzero once written (b + 1 >= 1; the kind word holds S >= 1).
-constexpr int kBaseBits = 18;
+// st (41-45), base (46-62), and bit 63 when the push released earlier writes
+// (the claimer then acquires); w1: the packed kind (low word), aux (high
+// word).  Both words are nonzero once written (b + 1 >= 1; the kind word
+// holds S >= 1).
+constexpr int kBaseBits = 17;
+constexpr unsigned long long kRecAcquire = 1ull << 63;
 constexpr uint32_t kBaseMask = (1u << kBaseBits) - 1u;
 constexpr int kMaxRecB = (1 << 22) - 2;     // requests per call
 constexpr int kMaxRecRow = (1 << 13) - 1;   // row (or node) index
-__device__ __forceinline__ void rec_encode(const Task& t, int slice, unsigned long long& w0, unsigned long long& w1) {
+__device__ __forceinline__ void rec_encode(const Task& t, int slice, bool release, unsigned long long& w0,
+                                           unsigned long long& w1) {
     w0 = static_cast<unsigned long long>(static_cast<uint32_t>(t.b + 1) & 0x3fffffu) |
          (static_cast<unsigned long long>(static_cast<uint32_t>(t.row) & 0x1fffu) << 22) |
          (static_cast<unsigned long long>(static_cast<uint32_t>(slice) & 63u) << 35) |
          (static_cast<unsigned long long>(static_cast<uint32_t>(t.st) & 31u) << 41) |
-         (static_cast<unsigned long long>(t.base & kBaseMask) << 46);
+         (static_cast<unsigned long long>(t.base & kBaseMask) << 46) | (release ? kRecAcquire : 0ull);
     w1 = static_cast<unsigned long long>(static_cast<uint32_t>(t.kind)) |
          (static_cast<unsigned long long>(static_cast<uint32_t>(t.aux)) << 32);
 }
@@ -230,14 +236,16 @@ struct Claimed {
 // slices each; a claimer that finds none pushed yet takes the next pushed
 // unit and waits (bounded) for its task, or for every request to finish.
 // `cold` caches whether initial units may be left.
-__device__ inline Claimed claim_unit(const Workspace& W, int B, int S0, bool& cold) {
+constexpr uint32_t kNoPre = 0xffffffffu;
+__device__ inline Claimed claim_unit(const Workspace& W, int B, int S0, bool& cold, uint32_t& pre) {
     Claimed c;
     c.ok = 1;
     c.hint = 0;
     c.pad = 0;
     c.task.b = 0; c.task.row = 0; c.task.kind = -1; c.task.aux = 0; c.task.st = 0; c.task.base = 0;
     if (cold) {
-        const uint32_t u0 = atomicAdd(&W.ctrl->head, 1u);
+        const uint32_t u0 = pre != kNoPre ? pre : atomicAdd(&W.ctrl->head, 1u);
+        pre = kNoPre;
         if (u0 < static_cast<uint32_t>(B) * static_cast<uint32_t>(S0)) {
             c.slice = static_cast<int>(u0 % static_cast<uint32_t>(S0));
             c.task.b = static_cast<int>(u0 / static_cast<uint32_t>(S0));
@@ -250,14 +258,18 @@ __device__ inline Claimed claim_unit(const Workspace& W, int B, int S0, bool& co
     uint32_t ns = 32;
     SPEC_TRACE_EV(10, -1, -1, -1, static_cast<int>(u));
     for (uint32_t it = 0;; ++it) {
+        // one round trip a poll: the record and the stop conditions together
         unsigned long long w0, w1;
-        ld_acquire_v2(W.urec + 2ull * u, w0, w1);
+        ld_relaxed_v2(W.urec + 2ull * u, w0, w1);
+        const uint32_t fin = ld_relaxed(&W.ctrl->done);
+        const uint32_t err = ld_relaxed(&W.ctrl->error);
         if (w0 != 0ull && w1 != 0ull) {
+            if (w0 & kRecAcquire) fence_acq_rel_gpu();   // pairs with the pusher's release
             rec_decode(w0, w1, c.task, c.slice);
             return c;
         }
-        if (ld_acquire(&W.ctrl->done) >= static_cast<uint32_t>(B)) { c.ok = 0; return c; }
-        if (ld_acquire(&W.ctrl->error) != 0) { c.ok = 0; return c; }   // another CTA gave up
+        if (fin >= static_cast<uint32_t>(B)) { c.ok = 0; return c; }
+        if (err != 0) { c.ok = 0; return c; }   // another CTA gave up
         if (it >= kWaitLimit) { atomicOr(&W.ctrl->error, kErrWait); c.ok = 0; return c; }
         nanosleep_ns(ns);
         if (ns < 256) ns <<= 1;
@@ -300,7 +312,7 @@ __device__ __forceinline__ void push_task(const Workspace& W, Task t, int S, int
     if (release) fence_acq_rel_gpu();
     for (int s = 0; s < S; ++s) {
         unsigned long long w0, w1;
-        rec_encode(t, s, w0, w1);
+        rec_encode(t, s, release, w0, w1);
         st_relaxed_v2(W.urec + 2ull * (u0 + s), w0, w1);
     }
 }
@@ -474,6 +486,7 @@ __device__ void producer_loop(const Workspace& W, int B, int S0, const Pipe& P, 
     uint32_t seq = 0;          // chunks issued so far (ring sequence number)
     bool dead = false;
     bool cold = true;          // initial units may be left
+    uint32_t pre = kNoPre;     // the next initial unit, taken while the current one streams
     for (uint32_t u = 0;; ++u) {
         const int j = u & 1;
         if (u >= 2 && !mbar_wait(&P.uempty[j], ((u >> 1) - 1) & 1u)) dead = true;
@@ -482,8 +495,10 @@ __device__ void producer_loop(const Workspace& W, int B, int S0, const Pipe& P, 
             c.ok = 0; c.slice = 0; c.hint = 0; c.pad = 0;
             c.task.b = 0; c.task.row = 0; c.task.kind = 0; c.task.aux = 0; c.task.st = 0; c.task.base = 0;
         } else {
-            c = claim_unit(W, B, S0, cold);
+            SPEC_TRACE_EV1(14, -1, -1, -1, static_cast<int>(u));
+            c = claim_unit(W, B, S0, cold, pre);
             if (c.ok) fetch(c);
+            SPEC_TRACE_EV1(13, c.task.b, c.task.row, c.slice, c.ok);
         }
         P.desc[j] = c;
         mbar_arrive(&P.ufull[j]);
@@ -498,6 +513,9 @@ __device__ void producer_loop(const Workspace& W, int B, int S0, const Pipe& P, 
             }
             if (*P.abort) { dead = true; break; }
             issue_chunk(P, p, ci, s);
+            // initial units are independent of every push: take the next one now,
+            // its round trip overlaps this unit
+            if (ci == 0 && cold && pre == kNoPre) pre = atomicAdd(&W.ctrl->head, 1u);
         }
         if (dead) {
             // unblock consumers waiting for a descriptor, then stop
@@ -552,12 +570,20 @@ __device__ bool consumer_wait(const Pipe& P, uint32_t& cseq, Poll poll, Serve se
 }
 
 // Combiner warp: hand the prepared combine number `cpub` to the consumers
-// and wait (bounded) until they finished it.
-__device__ inline bool publish_combine(const Pipe& P, uint32_t& cpub) {
+// and go back to arrivals; the combine's shared memory stays theirs until
+// combine_reuse().
+__device__ inline void publish_combine(const Pipe& P, uint32_t& cpub) {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(P.cready);
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(P.cdone, cpub & 1u));
     ++cpub;
+}
+
+// Combiner warp: before writing the combine's shared memory again, wait
+// (bounded) until the consumers finished the last published combine.
+__device__ inline bool combine_reuse(const Pipe& P, uint32_t cpub) {
+    if (cpub == 0) return true;
+    if (*P.abort) return false;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(P.cdone, (cpub - 1) & 1u));
     if (!ok) *P.abort = 1;
     return ok;
 }
@@ -592,19 +618,26 @@ __device__ inline void post_job(const Pipe& P, uint32_t& jseq, uint32_t& cseq, c
 }
 
 // The combiner warp's loop: take jobs in order until the stop job (or a
-// timed-out wait).  on_job(job) runs on all 32 lanes.
-template <class F>
-__device__ void combiner_loop(const Pipe& P, F on_job) {
+// timed-out wait).  on_job(job) runs on all 32 lanes; on_stop() runs before
+// the stop job is marked taken (the consumers leave once it is), so that
+// whatever the combiner handed them is finished first.
+template <class F, class G>
+__device__ void combiner_loop(const Pipe& P, F on_job, G on_stop) {
     for (uint32_t j = 0;; ++j) {
         const int s = static_cast<int>(j % kJobs);
         const bool got = __all_sync(0xffffffffu, mbar_wait(&P.jfull[s], (j / kJobs) & 1u));
         const Job job = P.jobs[s];
+        if (got && job.stop) on_stop();
         __syncwarp();
         if ((threadIdx.x & 31) == 0) mbar_arrive(&P.jempty[s]);
         if (!got) { *P.abort = 1; return; }
         if (job.stop) return;
         on_job(job);
     }
+}
+template <class F>
+__device__ void combiner_loop(const Pipe& P, F on_job) {
+    combiner_loop(P, on_job, []() {});
 }
 
 // ---------------------------------------------------------------------------
@@ -687,6 +720,7 @@ __device__ bool consume_row(const Pipe& P, uint32_t& seq, const StreamPlan& p, b
     bool dead = false;
     for (int c = 0; c < p.nch; ++c, ++seq) {
         const bool have = take_chunk(P, seq, tma, dead, p, c);
+        if (c == 0) SPEC_TRACE_EV(15, -1, -1, -1, p.nch);
         const unsigned char* sm = P.slot(static_cast<int>(seq % kStages));
         const int ne = min(p.ce, p.n - c * p.ce);
         const int cx0 = x0 + c * p.ce;

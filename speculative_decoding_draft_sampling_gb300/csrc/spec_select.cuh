@@ -336,7 +336,11 @@ struct TopkSmem {
     uint32_t scratch[kWarps + 2];
     uint64_t sh64[2];
     int ired[kWarps + 4];
+    // the best certified value filter any warp found for the current unit:
+    // (unit tag << 32) | value key; a stale tag is ignored.  Zero at kernel start.
+    unsigned long long shared_thr;
 };
+__device__ __forceinline__ void topk_smem_init(TopkSmem& s) { s.shared_thr = 0ull; }
 
 // Every element of a slice that can belong to the row's top-k: composite
 // key >= the filter `theta`.  The filter is only ever raised to a certified
@@ -378,11 +382,13 @@ struct TopkHistFn : FnHooks {
     uint32_t cmask;     // rounds of the current chunk deferred to chunk_end()
     int rr;             // rounds seen in the current chunk
     int tcnt;           // keys in this thread's slots
+    uint32_t tag;       // the unit's tag for the shared filter (nonzero, CTA-uniform)
     DraftWatch dw;
 
     __device__ __forceinline__ void set_theta(uint64_t t) { theta = t; thr_f = key_to_thr(hkey(t)); }
-    __device__ __forceinline__ void init(TopkSmem* s, int kk, uint32_t hint) {
-        S = s; k = kk;
+    // `unit_tag`: nonzero, distinct for every unit a CTA streams
+    __device__ __forceinline__ void init(TopkSmem* s, int kk, uint32_t hint, uint32_t unit_tag) {
+        S = s; k = kk; tag = unit_tag;
         set_theta(static_cast<uint64_t>(hint) << 32);
         vmx = -kInf; nw = 0; lost = 0; tmax = 0; cmask = 0; rr = 0; tcnt = 0;
     }
@@ -522,18 +528,28 @@ struct TopkHistFn : FnHooks {
         cmask = 0;
         rr = 0;
     }
-    // per warp: past half a region, refine this warp's filter
+    // per warp, after every chunk: adopt a better filter another warp found;
+    // past half a region, refine this warp's own
     __device__ __forceinline__ void after_release(int) {
+        const unsigned long long v = *reinterpret_cast<volatile unsigned long long*>(&S->shared_thr);
+        if (static_cast<uint32_t>(v >> 32) == tag) {
+            const uint64_t t = (v & 0xffffffffull) << 32;
+            if (t > theta) set_theta(t);
+        }
         if (nw > kRefineAt) refine_warp();
     }
-    // The exact k-th largest key of this warp's candidates by bisection
-    // (value key; then the index bits without kTies), and compaction.
+    // A higher filter from this warp's candidates: the value key where at
+    // least k of them remain (certified: they are elements of the slice),
+    // found by bisection that stops once at most k + k/2 remain; with a
+    // bisection that runs to the end and !kTies, the exact k-th composite
+    // key.  Then the region is compacted to the keys at or above the filter
+    // (keys below a filter another warp raised are dropped too) and the
+    // filter is shared with the other warps.
     __device__ void refine_warp() {
         const int lane = threadIdx.x & 31;
         uint64_t* reg = S->cand + (threadIdx.x >> 5) * kRegion;
         const int n = nw < kRegion ? nw : kRegion;
         lost |= nw > kRegion;
-        if (n < k) return;                  // not certifiable from this warp alone
         auto count_ge = [&](uint64_t t, bool value_only) {
             int c = 0;
             for (int j0 = 0; j0 < n; j0 += 32) {
@@ -544,24 +560,37 @@ struct TopkHistFn : FnHooks {
             }
             return c;
         };
-        // every stored key reaches theta, so count(value >= hkey(theta)) = n >= k
-        uint32_t lo = hkey(theta), hi = 0xffffffffu;
-        while (lo < hi) {
-            const uint32_t mid = lo + static_cast<uint32_t>((static_cast<uint64_t>(hi) - lo + 1) >> 1);
-            if (count_ge(mid, true) >= k) lo = mid; else hi = mid - 1;
-        }
-        uint64_t nt = static_cast<uint64_t>(lo) << 32;
-        if (!kTies) {
-            uint64_t clo = nt > theta ? nt : theta, chi = nt | 0xffffffffull;
-            while (clo < chi) {
-                const uint64_t d = chi - clo;
-                const uint64_t mid = clo + (d >> 1) + (d & 1ull);
-                if (count_ge(mid, false) >= k) clo = mid; else chi = mid - 1;
+        uint64_t nt = theta;
+        int clo = count_ge(hkey(theta), true);
+        if (clo >= k) {
+            uint32_t mx = 0;
+            for (int j = lane; j < n; j += 32) mx = max(mx, hkey(reg[j]));
+            uint32_t lo = hkey(theta), hi = warp_max_u32(mx);
+            const int enough = k + (k >> 1);
+            while (lo < hi && clo > enough) {
+                const uint32_t mid = lo + static_cast<uint32_t>((static_cast<uint64_t>(hi) - lo + 1) >> 1);
+                const int c = count_ge(mid, true);
+                if (c >= k) { lo = mid; clo = c; } else { hi = mid - 1; }
             }
-            nt = clo;
+            nt = static_cast<uint64_t>(lo) << 32;
+            if (!kTies && clo > enough) {
+                // every remaining key shares the value lo: split on the index bits
+                uint64_t cl = nt > theta ? nt : theta, ch = nt | 0xffffffffull;
+                while (cl < ch) {
+                    const uint64_t d = ch - cl;
+                    const uint64_t mid = cl + (d >> 1) + (d & 1ull);
+                    if (count_ge(mid, false) >= k) cl = mid; else ch = mid - 1;
+                }
+                nt = cl;
+            }
+            if (nt > theta) {
+                set_theta(nt);
+                if (lane == 0)
+                    atomicMax(&S->shared_thr, (static_cast<unsigned long long>(tag) << 32) | hkey(nt));
+            } else {
+                nt = theta;
+            }
         }
-        if (nt <= theta) return;
-        set_theta(nt);
         const uint32_t lt = (1u << lane) - 1u;
         int out = 0;
         for (int j0 = 0; j0 < n; j0 += 32) {

@@ -339,6 +339,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs
     unsigned char* scr = smem + kStages * kChunkBytes + sizeof(BuildSmem);
     Ent* nodes = reinterpret_cast<Ent*>(scr + build_scr_bytes(A.N, A.L));
     Ent* pend = nodes + A.N;
+    if (threadIdx.x == 0) topk_smem_init(sh.tk);   // made visible by pipe_init's barrier
     const Pipe P = pipe_init(smem, sh.pipe);
     const int N = A.N, M = A.M, L = A.L;
     const bool tma = A.tma_q != 0;
@@ -380,7 +381,7 @@ __global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs
         if (!trivial) {
             const int x0 = s * task_SL(A, t);
             TopkHistFn<F32, false> fn;
-            fn.init(&sh.tk, M, 0u);
+            fn.init(&sh.tk, M, 0u, u + 1u);
             if (!consume_row<F32>(P, seq, plan(t, s), tma, x0, fn)) break;
             uint64_t F;
             uint32_t oflow, bad;
