@@ -490,9 +490,9 @@ struct TopkHistFn : FnHooks {
             append(any ? 1u : 0u, vv, x);
         }
     }
-    __device__ __forceinline__ void chunk_end(int, const unsigned char* sm, int cx0, int nv) {
+    // per warp: the lanes' slots into the warp's region, one ballot per slot
+    __device__ __forceinline__ void flush_slots() {
         if (__any_sync(0xffffffffu, tcnt != 0)) {
-            // the warp's slots into its region, one ballot per slot
             const uint32_t lt = (1u << (threadIdx.x & 31)) - 1u;
             uint64_t* reg = S->cand + (threadIdx.x >> 5) * kRegion;
             int base = nw;
@@ -509,6 +509,10 @@ struct TopkHistFn : FnHooks {
             nw = base;
             tcnt = 0;
         }
+    }
+    // Before the chunk is released: only the rounds deferred for want of
+    // slot room need its data (the slots are flushed after the release).
+    __device__ __forceinline__ void chunk_end(int, const unsigned char* sm, int cx0, int nv) {
         if (__any_sync(0xffffffffu, cmask != 0)) {
             for (int r = 0; r < rr; ++r) {
                 const bool mine = (cmask >> r) & 1u;
@@ -536,6 +540,8 @@ struct TopkHistFn : FnHooks {
             const uint64_t t = (v & 0xffffffffull) << 32;
             if (t > theta) set_theta(t);
         }
+        // slots are flushed only once a lane's are nearly full (and at the end)
+        if (__any_sync(0xffffffffu, tcnt >= TopkSmem::kSlots - 1)) flush_slots();
         if (nw > kRefineAt) refine_warp();
     }
     // A higher filter from this warp's candidates: the value key where at
@@ -610,6 +616,7 @@ struct TopkHistFn : FnHooks {
     // shared memory.  The caller then csync()s and reads summary().
     __device__ void publish() {
         const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+        flush_slots();
         lost |= nw > kRegion;
         const uint32_t fl = (lost ? 1u : 0u) | (bad_max(vmx) ? 2u : 0u);
         const uint32_t flw = __reduce_or_sync(0xffffffffu, fl);
@@ -655,6 +662,7 @@ struct TopkHistFn : FnHooks {
         constexpr int kPer = kRegion / 32;
         const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
         const uint32_t lt = (1u << lane) - 1u;
+        flush_slots();
         lost |= nw > kRegion;
         const uint32_t fl = (lost ? 1u : 0u) | (bad_max(vmx) ? 2u : 0u);
         const uint32_t flw = __reduce_or_sync(0xffffffffu, fl);
