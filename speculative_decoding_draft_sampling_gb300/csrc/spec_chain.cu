@@ -685,7 +685,7 @@ __device__ __forceinline__ StreamPlan chain_plan(const ChainArgs& A, const Task&
 }
 
 template <class E, bool kTopk>
-__global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs A) {
+__global__ void __launch_bounds__(kBlockThreads, kCtasPerSm) chain_kernel(const ChainArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     auto& sh = *reinterpret_cast<ChainSmem<kTopk>*>(smem + kStages * kChunkBytes);
     if constexpr (kTopk) {
@@ -897,8 +897,9 @@ __global__ void __launch_bounds__(kBlockThreads, 2) chain_kernel(const ChainArgs
     consumer_wait(P, cseq, [&]() { return mbar_test(&P.jempty[(jseq - 1) % kJobs], ((jseq - 1) / kJobs) & 1u); }, serve);
 }
 
-// two CTAs per SM (228 KiB of shared memory, 1 KiB reserved per CTA)
-static_assert(kStages * kChunkBytes + sizeof(ChainSmem<true>) <= 113 * 1024, "chain CTA too large for 2 per SM");
+// kCtasPerSm CTAs per SM (228 KiB of shared memory, 1 KiB reserved per CTA)
+static_assert(kStages * kChunkBytes + sizeof(ChainSmem<true>) <= (228 * 1024) / kCtasPerSm - 1024,
+              "chain CTA too large for kCtasPerSm per SM");
 
 template <class E, bool kTopk>
 static size_t chain_smem_bytes() {

@@ -9,7 +9,14 @@
 
 namespace spec {
 
-constexpr int kThreads = 256;                 // consumer threads of every engine CTA
+#ifndef SPEC_THREADS
+#define SPEC_THREADS 256
+#endif
+#ifndef SPEC_CTAS_PER_SM
+#define SPEC_CTAS_PER_SM 2
+#endif
+constexpr int kThreads = SPEC_THREADS;        // consumer threads of every engine CTA
+constexpr int kCtasPerSm = SPEC_CTAS_PER_SM;  // engine CTAs resident per SM (register and smem budget)
 constexpr int kWarps = kThreads / 32;         // consumer warps
 constexpr int kProducer = kThreads;           // the producer lane (warp kWarps, lane 0)
 constexpr int kCombiner0 = kThreads + 32;     // first thread of the combiner warp (warp kWarps + 1)

@@ -15,11 +15,12 @@
 // different requests and depths interleave freely: there is no grid-wide
 // barrier, and a request's next row starts as soon as its decision is known.
 //
-// Waits.  A CTA that claimed a unit of a task not yet pushed waits for that
-// task's ready flag, or for every request to be finished; the wait is
-// bounded and gives up with SPEC_WS_ERR_WAIT.  Progress never depends on a
-// waiting CTA: units are claimed in order and processed without waiting, so
-// the kernel terminates even if only part of the grid is resident.
+// Waits.  A CTA that claimed a pushed unit not yet written waits for that
+// unit's record (which carries the whole task), or for every request to be
+// finished; the wait is bounded and gives up with SPEC_WS_ERR_WAIT.
+// Progress never depends on a waiting CTA: units are claimed in order and
+// processed without waiting, so the kernel terminates even if only part of
+// the grid is resident.
 #pragma once
 
 #include "spec_common.cuh"

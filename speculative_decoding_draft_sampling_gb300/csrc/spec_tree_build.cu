@@ -333,7 +333,7 @@ __device__ void build_combine(const BuildArgs& A, BuildSmem& sh, unsigned char* 
     __syncwarp();
 }
 
-__global__ void __launch_bounds__(kBlockThreads, 2) build_kernel(const BuildArgs A) {
+__global__ void __launch_bounds__(kBlockThreads, kCtasPerSm) build_kernel(const BuildArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     auto& sh = *reinterpret_cast<BuildSmem*>(smem + kStages * kChunkBytes);
     unsigned char* scr = smem + kStages * kChunkBytes + sizeof(BuildSmem);

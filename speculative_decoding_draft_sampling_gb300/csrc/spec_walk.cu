@@ -144,7 +144,7 @@ __device__ void walk_combine(const WalkArgs& A, const Job& job, uint32_t done, u
 }
 
 template <class E, bool kTree>
-__global__ void __launch_bounds__(kBlockThreads, 2) walk_kernel(const WalkArgs A) {
+__global__ void __launch_bounds__(kBlockThreads, kCtasPerSm) walk_kernel(const WalkArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     auto& sh = *reinterpret_cast<WalkSmem*>(smem + kStages * kChunkBytes);
     const Pipe P = pipe_init(smem, sh.pipe);
