@@ -69,8 +69,8 @@ Layout make_layout(int B, long long maxt, int cap_p, size_t extra_per_req, int s
     L.zero_bytes = align_up(L.off_counter + 4ull * B, 256);
     L.off_req = L.zero_bytes;
     L.off_part = align_up(L.off_req + sizeof(spec::ReqState) * B, 256);
-    // room for at least the kPreKeys keys a combine fetches with the header
-    const int keys = cap_p > spec::kPreKeys ? cap_p : spec::kPreKeys;
+    // room for the (up to 2 * kPreKeys) keys a combine fetches with the header
+    const int keys = cap_p > 2 * spec::kPreKeys ? cap_p : 2 * spec::kPreKeys;
     L.part_stride = static_cast<uint32_t>(align_up(sizeof(spec::PartHdr) + 8ull * keys, 128));
     L.off_extra = align_up(L.off_part + static_cast<size_t>(B) * smax * L.part_stride, 256);
     L.extra_stride = align_up(extra_per_req, 256);

@@ -212,8 +212,11 @@ __device__ int warp_icdf_pairs(const int* tok, const float2* w, int n, dfloat t)
 // Filter hint for the next row from this row's top-k threshold tau and max
 // m: 0.15 of the gap below tau (rows of one target differ little in tau; a
 // hint above the next row's tau only costs a re-read of that row).
+#ifndef SPEC_HINT_MARGIN
+#define SPEC_HINT_MARGIN 0.15f
+#endif
 __device__ __forceinline__ uint32_t next_hint(float tau, float m) {
-    const float h = tau - 0.15f * (m - tau);
+    const float h = tau - SPEC_HINT_MARGIN * (m - tau);
     return (h == h && h > -kInf) ? fkey(h) : 0u;
 }
 
@@ -233,7 +236,7 @@ __device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, i
     const float ur = kind == kVerify ? chain_u(A, b, row) : 0.f;
     const int y = kind == kVerify ? A.draft[static_cast<long long>(b) * A.K + row] : -1;
     SliceHdrs& H = cs.hdrs;
-    load_hdrs_w(A.W, b, S, H, cs.list, kCombKeys);   // headers and each slice's first 8 keys
+    const int pre = load_hdrs_w(A.W, b, S, H, cs.list, kCombKeys);   // headers and each slice's first keys
     SPEC_TRACE_EVW(5, b, row, S, kind);
     uint32_t flags = 0;
     float vmax = -kInf;
@@ -253,7 +256,7 @@ __device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, i
     int n = 0, fb = (flags & kPfOverflow) ? 1 : 0;
     if (!fb) {
         bool oflow;
-        n = gather_all_w(A.W, b, S, H, cs.list, kCombKeys, oflow, kPreKeys);
+        n = gather_all_w(A.W, b, S, H, cs.list, kCombKeys, oflow, pre);
         if (oflow) fb = 1;
     }
     SPEC_TRACE_EVW(6, b, row, n, kind);

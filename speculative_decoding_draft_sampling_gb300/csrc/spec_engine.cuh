@@ -906,16 +906,22 @@ struct SliceHdrs {
 
 // Combiner warp: lane s loads slice s's header (one round trip), offsets by
 // a warp scan.  With `list`, the same round trip also fetches each slice's
-// first kPreKeys keys into list[off_s ..] (speculatively: the slot always
-// holds room for them), so that gather_all_w only fetches what lies beyond.
+// first keys into list[off_s ..] (speculatively: the slot always holds room
+// for 2 * kPreKeys of them): kPreKeys per slice, or twice that when S <= 16
+// (lane 16 + s fetches slice s's second kPreKeys).  Returns the keys per
+// slice already in list (0 without list); gather_all_w fetches the rest.
 constexpr int kPreKeys = 16;
-__device__ inline void load_hdrs_w(const Workspace& W, int b, int S, SliceHdrs& H, uint64_t* list = nullptr,
-                                   int cap = 0) {
+__device__ inline int load_hdrs_w(const Workspace& W, int b, int S, SliceHdrs& H, uint64_t* list = nullptr,
+                                  int cap = 0) {
     const int l = threadIdx.x & 31;
+    const bool two = list && S <= 16;
+    const int ps = two ? (l & 15) : l;              // the slice whose keys this lane fetches
+    const int k0 = (two && l >= 16) ? kPreKeys : 0; // its first key
+    const bool fetch = list && ps < S;
     int c = 0;
     ulonglong2 kp[kPreKeys / 2];
-    if (list && l < S) {
-        const ulonglong2* src = reinterpret_cast<const ulonglong2*>(part_keys(W, b, l, S));   // 16-byte aligned
+    if (fetch) {
+        const ulonglong2* src = reinterpret_cast<const ulonglong2*>(part_keys(W, b, ps, S) + k0);   // 16-byte aligned
 #pragma unroll
         for (int j = 0; j < kPreKeys / 2; ++j) kp[j] = __ldcg(src + j);
     }
@@ -935,14 +941,18 @@ __device__ inline void load_hdrs_w(const Workspace& W, int b, int S, SliceHdrs& 
     const int off = warp_exscan_i(c, tot);
     if (l < S) H.off[l] = off;
     if (l == 0) H.off[S] = tot;
-    if (list && l < S) {
+    const int cs = __shfl_sync(0xffffffffu, c, ps & 31);     // the fetched slice's count and offset
+    const int os = __shfl_sync(0xffffffffu, off, ps & 31);
+    if (fetch) {
 #pragma unroll
         for (int j = 0; j < kPreKeys / 2; ++j) {
-            if (2 * j < c && off + 2 * j < cap) list[off + 2 * j] = kp[j].x;
-            if (2 * j + 1 < c && off + 2 * j + 1 < cap) list[off + 2 * j + 1] = kp[j].y;
+            const int a = k0 + 2 * j;
+            if (a < cs && os + a < cap) list[os + a] = kp[j].x;
+            if (a + 1 < cs && os + a + 1 < cap) list[os + a + 1] = kp[j].y;
         }
     }
     __syncwarp();
+    return list ? (two ? 2 * kPreKeys : kPreKeys) : 0;
 }
 
 // Combiner warp: every slice key that keep(key) accepts into list[0..return)
