@@ -88,3 +88,17 @@ def test_package_import_is_lazy_and_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(sv, "_lib", None)
     with pytest.raises(sv.SpecError):
         sv.lib()
+
+
+def test_shape_limits_rejected_on_host(lib):
+    # a pushed unit's record holds the request in 22 bits and the row (or tree
+    # node) in 13: larger shapes are refused before any device work
+    too_many = 4194303
+    assert _chain(lib, B=too_many) == 2
+    assert b"B >" in lib.spec_last_error()
+    assert _chain(lib, B=too_many - 1, wsb=16) == 1        # at the limit: only the tiny workspace is wrong
+    assert lib.spec_verify_greedy(1, 0, 0, 10, 1, too_many, 1, 10, None, None, 1, 1, 1, 16, 1 << 30, None) == 2
+    assert lib.spec_verify_tree(1, 0, 0, 10, 1, 1, 1, 2, 8193, 10, 4, 1, 1, 1, 1, 16, 1 << 30, None) == 2
+    assert b"N >" in lib.spec_last_error()
+    assert lib.spec_verify_tree(1, 0, 0, 10, 1, 1, 1, too_many, 8, 10, 4, 1, 1, 1, 1, 16, 1 << 30, None) == 2
+    assert lib.spec_tree_build(1, 10, 10, too_many, 4, 10, 8, 1, 1, 1, 1, 1, 1, 1, 16, 1 << 30, None) == 2
