@@ -16,7 +16,7 @@ A step is one pass of the verification hot path over one batch:
 Inputs are seeded synthetic tensors (see workloads/), resident in HBM before
 the timed region.  Successive steps rotate over 3 independently seeded input
 copies, so no step re-reads rows the previous one left in L2 (each copy's
-rows read per step exceed the 126 MB L2 for dflash/dspark; see DESIGN.md).
+rows read per step exceed the 126 MB L2 for dflash/dspark).
 
 Multi-GPU (torchrun): every rank verifies its own batch (weak scaling, no
 collective on the data path); the time is the max over ranks.
@@ -29,6 +29,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -97,7 +98,7 @@ class ClockSampler:
     def __init__(self, gpu_index=0):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"spec_bench_clocks_{os.getpid()}.csv")
 
     def start(self):
         try:
