@@ -476,6 +476,19 @@ static int cmp_cand(const void* a, const void* b)
     return 0;
 }
 
+/* Rank of token x in row q_d: how many tokens come before it in the order
+ * "probability descending, then id ascending".  Counted pairwise, so that the
+ * brute force shares no ordering code with the heap's candidate lists. */
+static int rank_by_count(const float* row, int V, int x)
+{
+    int r = 0;
+    for (int z = 0; z < V; ++z) {
+        if (z == x) continue;
+        if (row[z] > row[x] || (row[z] == row[x] && z < x)) r++;
+    }
+    return r;
+}
+
 int oracle_tree_build_bruteforce(
     const float* q, int64_t q_bstride, int64_t q_rstride,
     int B, int L, int V, int budget, int64_t max_prefixes,
@@ -483,45 +496,57 @@ int oracle_tree_build_bruteforce(
     uint64_t* anc_mask, int32_t* num_nodes)
 {
     const int N = budget;
-    const int M = N - 1;
     const int W = (N + 63) / 64;
-    if (L > ORC_MAX_L) return -1;
-    vid_t* all = (vid_t*)malloc((size_t)V * sizeof(vid_t));
-    vid_t* lists = (vid_t*)malloc((size_t)(L + 1) * (M > 0 ? M : 1) * sizeof(vid_t));
-    int* len = (int*)malloc((size_t)(L + 1) * sizeof(int));
+    if (L > ORC_MAX_L || V > 255) return -1;
+    int* rank = (int*)malloc((size_t)(L + 1) * V * sizeof(int));
     int rc = 0;
 
     for (int b = 0; b < B && rc == 0; ++b) {
-        int64_t total = 1;   /* root */
-        int64_t level = 1;
+        /* every token of every depth: V + V^2 + ... + V^L prefixes */
+        int64_t total = 1, level = 1;
         for (int d = 1; d <= L; ++d) {
             const float* row = q + (int64_t)b * q_bstride + (int64_t)(d - 1) * q_rstride;
-            len[d] = depth_list(row, V, M, all, lists + (int64_t)d * M);
-            if (len[d] < 0) { rc = -1; break; }
-            level *= len[d];
+            for (int x = 0; x < V; ++x) {
+                if (isnan(row[x]) || row[x] == INFINITY) { rc = -1; break; }
+                rank[(int64_t)d * V + x] = rank_by_count(row, V, x);
+            }
+            if (rc) break;
+            level *= V;
             total += level;
             if (total > max_prefixes) { rc = -1; break; }
         }
         if (rc) break;
         orc_cand* pre = (orc_cand*)calloc((size_t)total, sizeof(orc_cand));
+        int32_t* tok_of = (int32_t*)calloc((size_t)total, sizeof(int32_t));
         int64_t cnt = 0;
-        pre[cnt].Q = 1.0; pre[cnt].depth = 0; cnt++;
-        /* every rank path of length d, built from those of length d - 1 */
+        pre[cnt].Q = 1.0; pre[cnt].depth = 0; tok_of[cnt] = -1; cnt++;
+        /* each prefix of length d extends one of length d - 1 by any token x;
+         * Q multiplies q_d(x), and the tie order uses x's rank in row d */
         int64_t lo = 0, hi = 1;
         for (int d = 1; d <= L; ++d) {
+            const float* row = q + (int64_t)b * q_bstride + (int64_t)(d - 1) * q_rstride;
             for (int64_t j = lo; j < hi; ++j) {
-                for (int r = 0; r < len[d]; ++r) {
+                for (int x = 0; x < V; ++x) {
                     orc_cand c = pre[j];
                     c.depth = d;
-                    c.rank = r;
-                    c.path[d - 1] = (uint8_t)r;
-                    c.Q = pre[j].Q * lists[(int64_t)d * M + r].v;
+                    c.rank = rank[(int64_t)d * V + x];
+                    c.path[d - 1] = (uint8_t)c.rank;
+                    c.Q = pre[j].Q * (double)row[x];
+                    tok_of[cnt] = x;
                     pre[cnt++] = c;
                 }
             }
             lo = hi; hi = cnt;
         }
-        qsort(pre, (size_t)cnt, sizeof(orc_cand), cmp_cand);
+        /* sort indices (not the records) so that each keeps its token */
+        int64_t* ord = (int64_t*)malloc((size_t)cnt * sizeof(int64_t));
+        for (int64_t i = 0; i < cnt; ++i) ord[i] = i;
+        /* insertion sort by the pop order: tiny inputs only */
+        for (int64_t i = 1; i < cnt; ++i) {
+            int64_t v = ord[i], j = i - 1;
+            while (j >= 0 && cand_before(&pre[v], &pre[ord[j]])) { ord[j + 1] = ord[j]; --j; }
+            ord[j + 1] = v;
+        }
         int take = (int)(cnt < N ? cnt : N);
         int32_t* tk = token + (int64_t)b * N;
         int32_t* pr = parent + (int64_t)b * N;
@@ -529,24 +554,26 @@ int oracle_tree_build_bruteforce(
         double* sc = score + (int64_t)b * N;
         for (int n = 0; n < N; ++n) { tk[n] = -1; pr[n] = -1; dp[n] = -1; sc[n] = 0.0; }
         for (int n = 0; n < take; ++n) {
-            dp[n] = pre[n].depth;
-            sc[n] = pre[n].Q;
-            tk[n] = n == 0 ? -1 : lists[(int64_t)pre[n].depth * M + pre[n].rank].id;
+            const orc_cand* c = &pre[ord[n]];
+            dp[n] = c->depth;
+            sc[n] = c->Q;
+            tk[n] = tok_of[ord[n]];
             pr[n] = -1;
             if (n > 0) {
-                /* parent: the kept prefix one rank shorter (must precede n) */
+                /* parent: the kept prefix one token shorter (must precede n) */
                 for (int m = 0; m < n; ++m) {
-                    if (pre[m].depth != pre[n].depth - 1) continue;
-                    if (memcmp(pre[m].path, pre[n].path, (size_t)pre[m].depth) == 0) { pr[n] = m; break; }
+                    const orc_cand* a = &pre[ord[m]];
+                    if (a->depth != c->depth - 1) continue;
+                    if (memcmp(a->path, c->path, (size_t)a->depth) == 0) { pr[n] = m; break; }
                 }
                 if (pr[n] < 0) rc = -2;   /* the kept set is not prefix-closed */
             }
         }
         num_nodes[b] = take;
         write_masks(pr, take, N, anc_mask + (int64_t)b * N * W);
-        free(pre);
+        free(pre); free(tok_of); free(ord);
     }
-    free(all); free(lists); free(len);
+    free(rank);
     return rc;
 }
 

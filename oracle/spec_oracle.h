@@ -69,10 +69,11 @@ void oracle_tree_build(
     uint64_t* anc_mask, int32_t* num_nodes, int32_t* status,
     int32_t* rows_needed);
 
-/* Brute force for tiny V and L: every prefix of length <= L over the
- * per-depth candidate lists, sorted by (Q desc, depth asc, rank path asc),
- * first N kept.  Same outputs as oracle_tree_build.  Returns -1 when the
- * prefix count exceeds max_prefixes. */
+/* Brute force for tiny V (<= 255) and L: every prefix of length <= L over
+ * ALL V tokens of every depth (no candidate list, no sort of the rows: each
+ * token's rank is counted pairwise), sorted by (Q desc, depth asc, rank path
+ * asc), first N kept.  Same outputs as oracle_tree_build.  Returns -1 when
+ * the prefix count exceeds max_prefixes. */
 int oracle_tree_build_bruteforce(
     const float* q, int64_t q_bstride, int64_t q_rstride,
     int B, int L, int V, int budget, int64_t max_prefixes,

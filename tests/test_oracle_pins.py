@@ -304,6 +304,48 @@ def test_residual_mass_closed_form():
     assert out["tokens"][0].tolist() == [1, -1]
 
 
+def test_near_tie_flags_at_the_accept_boundary():
+    """p = (1/2, 1/2) and q = (5/8, 3/8): drafting token 0 gives p/q = 4/5
+    exactly.  |u - 4/5| = 5e-7 sets the position's near-tie bit; 5e-6 does not
+    (the window is 1e-6); the decision itself follows u < p/q."""
+    logits = np.zeros((1, 2, 2), np.float32)
+    q = np.array([[[0.625, 0.375]]], np.float32)
+    d = np.array([[0]], np.int32)
+    for du, flagged in ((-5e-7, True), (5e-7, True), (-5e-6, False), (5e-6, False)):
+        u0 = np.float32(0.8 + du)
+        out = oracle.verify_chain(logits, q, d, np.array([[u0, 0.3]], np.float32), 1.0, 0)
+        assert bool(out["near_tie"][0] & 1) == flagged, du
+        assert out["num_accepted"][0] == (1 if du < 0 else 0), du
+        assert not (out["near_tie"][0] >> 31), du     # the sample is far from its CDF edges
+
+
+def test_near_tie_flags_at_a_cdf_boundary():
+    """Position 0 always accepts (p = q); the bonus row has p = (1/4, 3/4),
+    so its CDF boundary is 1/4.  u within 5e-7 of it sets bit 31, 5e-6 away
+    does not; the token is 0 below the boundary and 1 above it."""
+    logits = np.zeros((1, 2, 2), np.float32)
+    logits[0, 1] = [0.0, np.log(3.0)]
+    q = np.full((1, 1, 2), 0.5, np.float32)
+    d = np.array([[1]], np.int32)
+    for du, flagged in ((-5e-7, True), (5e-7, True), (-5e-6, False), (5e-6, False)):
+        us = np.float32(0.25 + du)
+        out = oracle.verify_chain(logits, q, d, np.array([[0.3, us]], np.float32), 1.0, 0)
+        assert out["num_accepted"][0] == 1
+        assert bool(out["near_tie"][0] >> 31) == flagged, du
+        assert out["tokens"][0, 1] == (0 if du < 0 else 1), du
+        assert not (out["near_tie"][0] & 1)
+    # the residual's boundaries: a rejection whose residual is one token
+    # (p = (1/2, 1/2), q = (5/8, 3/8): [p - q]_+ = (0, 1/8)) has its CDF edges
+    # at 0 and R, i.e. at u = 0 and u = 1
+    logits = np.zeros((1, 2, 2), np.float32)
+    q = np.array([[[0.625, 0.375]]], np.float32)
+    d = np.array([[0]], np.int32)
+    for us, flagged in ((5e-7, True), (5e-6, False), (0.5, False)):
+        out = oracle.verify_chain(logits, q, d, np.array([[0.9, us]], np.float32), 1.0, 0)
+        assert out["num_accepted"][0] == 0 and out["tokens"][0, 0] == 1
+        assert bool(out["near_tie"][0] >> 31) == flagged, us
+
+
 def test_uniform_indexing_accept_vs_sample():
     """u[b, i] decides position i; u[b, k] drives the single sample."""
     p = [0.5, 0.5, 0.0, 0.0]
@@ -413,10 +455,13 @@ def _rand_q(rng, B, L, V, ties=False):
     return (q / q.sum(-1, keepdims=True)).astype(np.float32)
 
 
-@pytest.mark.parametrize("V,L", [(2, 4), (3, 3), (4, 4), (3, 1)])
-@pytest.mark.parametrize("budget", [1, 2, 5, 17, 64])
+@pytest.mark.parametrize("V,L", [(2, 4), (3, 3), (4, 4), (3, 1), (6, 3), (5, 4)])
+@pytest.mark.parametrize("budget", [1, 2, 3, 4, 5, 17, 64])
 @pytest.mark.parametrize("ties", [False, True])
 def test_tree_heap_equals_bruteforce(V, L, budget, ties):
+    """The brute force enumerates every prefix over all V tokens of every
+    depth (ranks counted pairwise), so cases with budget - 1 < V also pin
+    the heap's per-depth cut to the budget - 1 most probable tokens."""
     rng = np.random.default_rng(100 + V * 10 + L + budget + (7 if ties else 0))
     q = _rand_q(rng, 6, L, V, ties)
     if ties:
