@@ -7,6 +7,7 @@ A step is one pass of the verification hot path over one batch:
   dflash   (default) block-draft chain verify, B=256 K=8 V=151936 fp32,
            T=1, top-k 50 -- the chain-verification workload large enough
            to be bound by HBM bandwidth
+  dflash_vs  the same shape, every row with its own logit scale and offset
   eagle3   chain verify B=64 K=3 V=128256 bf16, T=0.8
   eagle3_greedy  greedy verify on the same shape
   chain_small    chain verify B=4 K=4 V=1000
@@ -17,6 +18,13 @@ Inputs are seeded synthetic tensors (see workloads/), resident in HBM before
 the timed region.  Successive steps rotate over 3 independently seeded input
 copies, so no step re-reads rows the previous one left in L2 (each copy's
 rows read per step exceed the 126 MB L2 for dflash/dspark).
+
+The line also carries: `parity` -- every request of input copy 0 re-run on
+the float64 oracle (threads over requests on the host cores) and compared
+with the GPU's outputs; `cpu_baseline` -- that oracle timed on one thread and
+on every host core; `e2e` -- the same step through the public API with the
+inputs copied from pinned host buffers and the results copied back inside
+the timed region.
 
 Multi-GPU (torchrun): every rank verifies its own batch (weak scaling, no
 collective on the data path); the time is the max over ranks.
@@ -42,6 +50,7 @@ import torch
 METRIC = "draft positions verified/sec; achieved HBM GB/s vs GB300 peak (1 GPU)"
 UNIT = "positions/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
 
 
 def kernel_source_hash():
@@ -147,21 +156,25 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workloads: (setup) -> step callable, positions, algorithmic bytes
 # ---------------------------------------------------------------------------
-def chain_bytes(w, res):
+def chain_bytes(K, V, es, top_k, n, st, k=None):
     """Bytes a chain verify must move: logits rows 0..n_b of every request,
     a 32-byte sector per q(y) point read, the q values of the top-k set (or
-    the whole q row without top-k) at a rejection, and the small arrays."""
-    n = res.num_accepted.cpu().numpy().astype(np.int64)
-    st = res.status.cpu().numpy()
-    K, V, B = w.K, w.V, w.B
-    es = w.logits.element_size()
-    rows = n + 1
-    rej = (n < K) & ((st & 1) == 0)
-    q_pts = np.minimum(n + rej, K)
-    topk = 0 < w.top_k < V
-    per_rej = (w.top_k * 32) if topk else V * 4
-    small = B * (K * 4 + (K + 1) * 4 + (K + 1) * 4 + 8)
-    return int(rows.sum() * V * es + q_pts.sum() * 32 + rej.sum() * per_rej + small)
+    the whole q row without top-k) at a rejection, and the small per-request
+    arrays (drafts, uniforms, outputs)."""
+    n = np.asarray(n, np.int64)
+    st = np.asarray(st)
+    kk = np.full_like(n, K) if k is None else np.asarray(k, np.int64)
+    B = n.shape[0]
+    rej = (n < kk) & ((st & 1) == 0)
+    q_pts = np.minimum(n + rej, kk)
+    topk = 0 < top_k < V
+    per_rej = (top_k * 32) if topk else V * 4
+    small = B * (K * 4 + (K + 1) * 4 + (K + 1) * 4 + 8) + (B * 12 if k is not None else 0)
+    return int((n + 1).sum() * V * es + q_pts.sum() * 32 + rej.sum() * per_rej + small)
+
+
+def pinned(t):
+    return t.cpu().pin_memory()
 
 
 def make_chain_case(name, dev, copies, greedy=False, over=None):
@@ -176,13 +189,13 @@ def make_chain_case(name, dev, copies, greedy=False, over=None):
         else:
             outs.append(sv.verify_chain(w.logits, w.q, w.draft, w.uniforms, w.temperature, w.top_k))
     torch.cuda.synchronize()
-    if greedy:
-        nbytes = []
-        for w, r in zip(ws, outs):
-            n = r.num_accepted.cpu().numpy().astype(np.int64)
+    nbytes = []
+    for w, r in zip(ws, outs):
+        n = r.num_accepted.cpu().numpy().astype(np.int64)
+        if greedy:
             nbytes.append(int((n + 1).sum() * w.V * w.logits.element_size() + w.B * (w.K * 4 + (w.K + 1) * 4 + 8)))
-    else:
-        nbytes = [chain_bytes(w, r) for w, r in zip(ws, outs)]
+        else:
+            nbytes.append(chain_bytes(w.K, w.V, w.logits.element_size(), w.top_k, n, r.status.cpu().numpy()))
 
     def step(i):
         w, r = ws[i % copies], outs[i % copies]
@@ -191,12 +204,42 @@ def make_chain_case(name, dev, copies, greedy=False, over=None):
         else:
             sv.verify_chain(w.logits, w.q, w.draft, w.uniforms, w.temperature, w.top_k, out=r)
 
+    def e2e():
+        w = ws[0]
+        d_in = [w.logits, w.draft_greedy if greedy else w.draft]
+        if not greedy:
+            d_in += [w.uniforms, w.q]
+        d_in = [torch.empty_like(t) for t in d_in]
+        h_in = [pinned(t) for t in ([w.logits, w.draft_greedy] if greedy else [w.logits, w.draft, w.uniforms, w.q])]
+
+        def call():
+            if greedy:
+                r = sv.verify_greedy(d_in[0], d_in[1])
+            else:
+                r = sv.verify_chain(d_in[0], d_in[3], d_in[1], d_in[2], w.temperature, w.top_k)
+            return [r.tokens, r.num_accepted, r.status]
+        return h_in, d_in, call
+
     w0 = ws[0]
     cfg = dict(workload=name + ("_greedy" if greedy else ""), B=w0.B, K=w0.K, V=w0.V,
                logits_dtype=str(w0.logits.dtype).replace("torch.", ""), temperature=w0.temperature,
                top_k=w0.top_k, mode="greedy" if greedy else "stochastic")
     return dict(step=step, positions=w0.B * w0.K, bytes=nbytes, cfg=cfg, inputs=ws, outs=outs,
-                dtype="f32" if w0.logits.dtype == torch.float32 else "bf16")
+                launches_per_step=1, e2e=e2e, dtype="f32" if w0.logits.dtype == torch.float32 else "bf16")
+
+
+def tree_bytes(q_shape, budget, depth, walk_n, target_es):
+    """DDTree step bytes: the q rows the best-first order consults (per
+    request, up to the deepest kept depth, plus the next one unless the budget
+    filled at that depth's first node or the depth limit), and the target rows
+    on the walked path."""
+    B, L, V = q_shape
+    rows = 0
+    for b in range(B):
+        dmax = depth[b].max()
+        first = int(np.argmax(depth[b] == dmax))
+        rows += dmax if (first == budget - 1 or dmax == L) else dmax + 1
+    return int(rows * V * 4 + (np.asarray(walk_n) + 1).sum() * V * target_es)
 
 
 def make_tree_case(dev, copies):
@@ -207,28 +250,30 @@ def make_tree_case(dev, copies):
     tls = [workloads.tree_target_logits(t, tr.depth) for t, tr in zip(ts, trees)]
     walks = [sv.verify_tree(tl, tr.token, tr.parent, tr.num_nodes, t.q.shape[1]) for t, tl, tr in zip(ts, tls, trees)]
     torch.cuda.synchronize()
-    nbytes = []
-    for t, tr, wk, tl in zip(ts, trees, walks, tls):
-        B, L, V = t.q.shape
-        dep = tr.depth.cpu().numpy()
-        rows = 0
-        for b in range(B):
-            dmax = dep[b].max()
-            first = int(np.argmax(dep[b] == dmax))
-            need = dmax if (first == t.budget - 1 or dmax == L) else dmax + 1
-            rows += need
-        walk_rows = int((wk.num_accepted.cpu().numpy() + 1).sum())
-        nbytes.append(int(rows * V * 4 + walk_rows * V * tl.element_size()))
+    nbytes = [tree_bytes(t.q.shape, t.budget, tr.depth.cpu().numpy(), wk.num_accepted.cpu().numpy(),
+                         tl.element_size()) for t, tr, wk, tl in zip(ts, trees, walks, tls)]
+    L = ts[0].q.shape[1]
 
     def step(i):
         t, tr, tl, wk = ts[i % copies], trees[i % copies], tls[i % copies], walks[i % copies]
         sv.tree_build(t.q, t.budget, out=tr)
-        sv.verify_tree(tl, tr.token, tr.parent, tr.num_nodes, t.q.shape[1], out=wk)
+        sv.verify_tree(tl, tr.token, tr.parent, tr.num_nodes, L, out=wk)
+
+    def e2e():
+        t, tl = ts[0], tls[0]
+        h_in = [pinned(t.q), pinned(tl)]
+        d_in = [torch.empty_like(t.q), torch.empty_like(tl)]
+
+        def call():
+            tr = sv.tree_build(d_in[0], t.budget)
+            wk = sv.verify_tree(d_in[1], tr.token, tr.parent, tr.num_nodes, L)
+            return [wk.tokens, wk.num_accepted, wk.path_nodes, wk.status]
+        return h_in, d_in, call
 
     B, L, V = ts[0].q.shape
     cfg = dict(workload="ddtree", B=B, L=L, V=V, budget=ts[0].budget, q_dtype="float32", target_dtype="bfloat16")
     return dict(step=step, positions=B * (ts[0].budget - 1), bytes=nbytes, cfg=cfg, inputs=ts, outs=walks,
-                dtype="f32+bf16")
+                trees=trees, target=tls, launches_per_step=2, e2e=e2e, dtype="f32+bf16")
 
 
 def make_dspark_case(dev, copies):
@@ -244,11 +289,8 @@ def make_dspark_case(dev, copies):
     nbytes, pos = [], []
     for w, a, r in zip(ws, lens, outs):
         k = a.k.cpu().numpy().astype(np.int64)
-        n = r.num_accepted.cpu().numpy().astype(np.int64)
-        rej = n < k
-        es = w.logits.element_size()
-        nbytes.append(int((n + 1).sum() * w.V * es + (np.minimum(n + rej, k)).sum() * 32 + rej.sum() * w.top_k * 32
-                          + w.B * (w.K * 4 * 2 + 8 * 3 + w.K * 8)))
+        nbytes.append(chain_bytes(w.K, w.V, w.logits.element_size(), w.top_k, r.num_accepted.cpu().numpy(),
+                                  r.status.cpu().numpy(), k=k) + w.B * w.K * (4 + 8))
         pos.append(int(k.sum()))
 
     def step(i):
@@ -257,10 +299,29 @@ def make_dspark_case(dev, copies):
         sv.verify_chain(pl, pq, w.draft, w.uniforms, w.temperature, w.top_k, k_per_req=a.k,
                         l_row_off=a.l_row_off, q_row_off=a.q_row_off, out=r)
 
+    def e2e():
+        # the target's rows arrive packed for the verify lengths the
+        # confidences give (the same on the host and the device)
+        w, (pl, pq) = ws[0], packs[0]
+        src = [w.conf, pl, pq, w.draft, w.uniforms]
+        h_in = [pinned(t) for t in src]
+        d_in = [torch.empty_like(t) for t in src]
+
+        def call():
+            a = sv.adaptive_len(d_in[0], 1.0, 0.15)
+            r = sv.verify_chain(d_in[1], d_in[2], d_in[3], d_in[4], w.temperature, w.top_k, k_per_req=a.k,
+                                l_row_off=a.l_row_off, q_row_off=a.q_row_off)
+            return [r.tokens, r.num_accepted, r.status, a.k]
+        return h_in, d_in, call
+
     w0 = ws[0]
     cfg = dict(workload="dspark", B=w0.B, Kmax=w0.K, V=w0.V, logits_dtype="bfloat16", temperature=1.0,
                top_k=w0.top_k, a=1.0, b=0.15, mode="adaptive ragged (compact)")
-    return dict(step=step, positions=pos, bytes=nbytes, cfg=cfg, inputs=ws, outs=outs, dtype="bf16")
+    return dict(step=step, positions=pos, bytes=nbytes, cfg=cfg, inputs=ws, outs=outs, lens=lens, packs=packs,
+                launches_per_step=2, e2e=e2e, dtype="bf16")
+
+
+WORKLOAD_CHOICES = ["dflash", "dflash_vs", "eagle3", "eagle3_greedy", "chain_small", "ddtree", "dspark"]
 
 
 def make_case(name, dev, copies, over=None):
@@ -276,7 +337,7 @@ def make_case(name, dev, copies, over=None):
 
 
 # ---------------------------------------------------------------------------
-# CPU baseline: the float64 oracle on a bounded sample of the same workload
+# the float64 oracle: whole requests of input copy 0, on the host cores
 # ---------------------------------------------------------------------------
 def host_view(t: torch.Tensor) -> np.ndarray:
     """Host copy in the oracle's input format (bf16 as raw uint16 bits)."""
@@ -285,39 +346,141 @@ def host_view(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().cpu().numpy()
 
 
-def oracle_sample(case, budget_s=12.0):
-    import oracle
-    name = case["cfg"]["workload"]
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+class OracleJob:
+    """Host copies of one input copy and the oracle for requests [lo, hi).
+
+    `target` (DDTree) is the tree's target logits; `tree_depth` the depth
+    array they were generated from.  Nothing here calls the CUDA library."""
+
+    def __init__(self, name, w, target=None):
+        self.name = name
+        self.w = w
+        if name == "ddtree":
+            self.q = host_view(w.q)
+            self.tl = host_view(target)
+            self.B, self.L, self.V = w.q.shape
+            self.per_req = w.budget - 1
+        else:
+            self.lg, self.qq = host_view(w.logits), host_view(w.q)
+            self.d = host_view(w.draft_greedy if name == "eagle3_greedy" else w.draft)
+            self.u = host_view(w.uniforms)
+            self.conf = host_view(w.conf) if w.conf is not None else None
+            self.B, self.K, self.V = w.B, w.K, w.V
+            self.per_req = None if name == "dspark" else w.K
+
+    def run(self, lo, hi):
+        import oracle
+        w = self.w
+        if self.name == "ddtree":
+            tr = oracle.tree_build(self.q[lo:hi], w.budget)
+            wk = oracle.verify_tree(self.tl[lo:hi], tr["token"], tr["parent"], tr["num_nodes"], self.L)
+            out = {f"tree_{k}": v for k, v in tr.items()}
+            out.update(wk)
+            out["positions"] = np.full(hi - lo, self.per_req, np.int64)
+            return out
+        if self.name == "eagle3_greedy":
+            out = oracle.verify_greedy(self.lg[lo:hi], self.d[lo:hi])
+            out["positions"] = np.full(hi - lo, self.K, np.int64)
+            return out
+        if self.name == "dspark":
+            a = oracle.adaptive_len(self.conf[lo:hi], 1.0, 0.15)
+            k = a["k"]
+            lo_off = np.concatenate([[0], np.cumsum(k + 1)]).astype(np.int32)
+            qo_off = np.concatenate([[0], np.cumsum(k)]).astype(np.int32)
+            pl = np.concatenate([self.lg[j, :k[j - lo] + 1] for j in range(lo, hi)])
+            pq = np.concatenate([self.qq[j, :k[j - lo]] for j in range(lo, hi)] + [np.zeros((1, self.V), np.float32)])
+            out = oracle.verify_chain(pl, pq, self.d[lo:hi], self.u[lo:hi], w.temperature, w.top_k, K=self.K,
+                                      V=self.V, k_per_req=k, l_row_off=lo_off, q_row_off=qo_off)
+            out["k"] = k
+            out["positions"] = k.astype(np.int64)
+            return out
+        out = oracle.verify_chain(self.lg[lo:hi], self.qq[lo:hi], self.d[lo:hi], self.u[lo:hi], w.temperature,
+                                  w.top_k)
+        out["positions"] = np.full(hi - lo, self.K, np.int64)
+        return out
+
+
+def run_threads(job, reqs, threads):
+    """The oracle over the listed requests, one request per task on
+    `threads` host threads (the oracle's C calls release the GIL).
+    Returns (results in request order, positions, seconds)."""
+    from concurrent.futures import ThreadPoolExecutor
     t0 = time.perf_counter()
-    done_pos = 0
-    n_req = 0
-    if name == "ddtree":
-        t = case["inputs"][0]
-        B = t.q.shape[0]
-        b = 0
-        while time.perf_counter() - t0 < budget_s and b < B:
-            tr = oracle.tree_build(host_view(t.q[b:b + 1]), t.budget)
-            tl = __import__("workloads").tree_target_logits(t, torch.from_numpy(tr["depth"]).to(t.q.device))
-            oracle.verify_tree(host_view(tl[b:b + 1]), tr["token"], tr["parent"], tr["num_nodes"], t.q.shape[1])
-            done_pos += t.budget - 1
-            b += 1
-            n_req += 1
-    else:
-        w = case["inputs"][0]
-        B = w.B
-        b = 0
-        while time.perf_counter() - t0 < budget_s and b < B:
-            sl = slice(b, b + 1)
-            if name == "eagle3_greedy":
-                oracle.verify_greedy(host_view(w.logits[sl]), host_view(w.draft_greedy[sl]))
-            else:
-                oracle.verify_chain(host_view(w.logits[sl]), host_view(w.q[sl]), host_view(w.draft[sl]),
-                                    host_view(w.uniforms[sl]), w.temperature, w.top_k)
-            done_pos += w.K
-            b += 1
-            n_req += 1
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(lambda b: job.run(b, b + 1), reqs))
     el = time.perf_counter() - t0
-    return done_pos / el, n_req, el
+    res = {k: np.concatenate([p[k] for p in parts]) for k in parts[0]} if parts else {}
+    return res, int(res["positions"].sum()) if parts else 0, el
+
+
+def cpu_baseline(job, budget_s=12.0):
+    """The oracle as it stands on one thread (requests one by one for about
+    budget_s/2 seconds) and on every host core (a pool over the next
+    requests, about as long)."""
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    b, pos1 = 0, 0
+    while b < job.B and time.perf_counter() - t0 < budget_s / 2:
+        pos1 += int(job.run(b, b + 1)["positions"].sum())
+        b += 1
+    el1 = time.perf_counter() - t0
+    n1 = b
+    # all cores: as many requests as one thread did in its half, times the
+    # cores (cycling over the batch)
+    reqs = [(n1 + i) % job.B for i in range(max(cores, min(job.B * 4, n1 * cores)))]
+    _, posn, eln = run_threads(job, reqs, cores)
+    return dict(value=posn / eln, unit=UNIT, cores=cores, kind="oracle", cpu_model=cpu_model(),
+                sample=f"{len(reqs)} whole requests of input copy 0 on {cores} host threads ({eln:.1f} s); "
+                       f"float64 C oracle, one request per task",
+                single_thread=dict(value=pos1 / el1, cores=1,
+                                   sample=f"{n1} whole requests one by one ({el1:.1f} s)"))
+
+
+def parity_report(case, job):
+    """Every request of input copy 0 on the oracle (all host cores), compared
+    with the GPU's outputs for the same inputs: decisions and tokens must be
+    equal except at the near-ties the oracle flags."""
+    name = case["cfg"]["workload"]
+    ref, _, el = run_threads(job, list(range(job.B)), os.cpu_count() or 1)
+    out = case["outs"][0]
+    mism, near, flagged = 0, 0, 0
+    if name == "ddtree":
+        tr = case["trees"][0]
+        for k in ("token", "parent", "depth", "score", "num_nodes", "status"):
+            g = getattr(tr, k).cpu().numpy()
+            mism += int((g != ref["tree_" + k]).reshape(g.shape[0], -1).any(1).sum())
+        for k in ("tokens", "num_accepted", "path_nodes", "status"):
+            g = getattr(out, k).cpu().numpy()
+            mism += int((g != ref[k]).reshape(g.shape[0], -1).any(1).sum())
+    else:
+        tok = out.tokens.cpu().numpy()
+        n = out.num_accepted.cpu().numpy()
+        st = out.status.cpu().numpy()
+        nt = ref.get("near_tie", np.zeros(job.B, np.uint32))
+        flagged = int((nt != 0).sum())
+        for b in range(job.B):
+            same = n[b] == ref["num_accepted"][b] and (tok[b] == ref["tokens"][b]).all() and st[b] == ref["status"][b]
+            if not same:
+                if nt[b] != 0:
+                    near += 1
+                else:
+                    mism += 1
+        if name == "dspark":
+            mism += int((case["lens"][0].k.cpu().numpy() != ref["k"]).sum())
+    return dict(requests=job.B, mismatches=mism, near_tie_mismatches=near, near_tie_flagged=flagged,
+                oracle_s=round(el, 2))
 
 
 # ---------------------------------------------------------------------------
@@ -348,34 +511,97 @@ def barrier(world):
         dist.barrier()
 
 
+def reference_job(name):
+    """Inputs for the reference arm, built by the seeded generator and, where
+    the method's own earlier step decides the layout (the DDTree target rows
+    depend on the tree), by the oracle: the CUDA library is not used."""
+    import workloads
+    import oracle
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    if name == "ddtree":
+        t = workloads.make_tree("ddtree", device=dev)
+        depth = oracle.tree_build(host_view(t.q), t.budget)["depth"]
+        tl = workloads.tree_target_logits(t, torch.from_numpy(depth).to(dev))
+        cfg = dict(workload="ddtree", B=t.q.shape[0], L=t.q.shape[1], V=t.q.shape[2], budget=t.budget,
+                   q_dtype="float32", target_dtype="bfloat16")
+        return OracleJob(name, t, tl), cfg
+    base = "eagle3" if name == "eagle3_greedy" else name
+    w = workloads.make_chain(base, device=dev)
+    if name == "dspark":
+        cfg = dict(workload="dspark", B=w.B, Kmax=w.K, V=w.V, logits_dtype="bfloat16", temperature=1.0,
+                   top_k=w.top_k, a=1.0, b=0.15, mode="adaptive ragged (compact)")
+    else:
+        cfg = dict(workload=name, B=w.B, K=w.K, V=w.V, logits_dtype=str(w.logits.dtype).replace("torch.", ""),
+                   temperature=w.temperature, top_k=w.top_k,
+                   mode="greedy" if name == "eagle3_greedy" else "stochastic")
+    return OracleJob(name, w), cfg
+
+
 def run_reference(args, rank, world):
-    """--impl reference: the float64 oracle on the host cores, bounded sample per step."""
+    """--impl reference: the float64 oracle on every host core, a bounded
+    sample of whole requests of the same workload per step."""
     if rank != 0:
         return 0
-    dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
-    case = make_case_cpu_or_gpu(args.workload, dev)
-    vals = []
+    job, cfg = reference_job(args.workload)
+    cores = os.cpu_count() or 1
+    budget = max(1.0, min(6.0, 60.0 / max(1, args.steps)))
+    # requests per step: about `budget` seconds on every core (from a probe)
+    t0 = time.perf_counter()
+    job.run(0, 1)
+    per_req = max(1e-3, time.perf_counter() - t0)
+    n = max(cores, int(budget / per_req * cores))
+    vals, nreq = [], 0
+    start = 1
     for i in range(args.warmup + args.steps):
-        v, n_req, el = oracle_sample(case, budget_s=max(1.0, min(6.0, 60.0 / max(1, args.steps))))
+        reqs = [(start + j) % job.B for j in range(n)]
+        start = (start + n) % job.B
+        _, pos, el = run_threads(job, reqs, cores)
         if i >= args.warmup:
-            vals.append(v)
+            vals.append(pos / el)
+            nreq = n
     val = statistics.mean(vals)
     line = dict(impl="reference", metric=METRIC, value=val, unit=UNIT, n_gpus=args.gpus, steps=args.steps,
                 warmup=args.warmup, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
-                data="synthetic", config=case["cfg"],
-                cpu_baseline=dict(value=val, unit=UNIT, cores=1, kind="oracle",
-                                  sample=f"whole requests of the same workload, ~{n_req} per step, single-threaded C"),
+                data="synthetic (seeded)", config=cfg,
+                cpu_baseline=dict(value=val, unit=UNIT, cores=cores, kind="oracle", cpu_model=cpu_model(),
+                                  sample=f"{nreq} whole requests of the same workload per step, one per task "
+                                         f"on {cores} host threads, float64 C oracle"),
                 e2e=dict(value=val, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line), flush=True)
     return 0
 
 
-def make_case_cpu_or_gpu(name, dev):
-    if dev.type == "cuda":
-        import speculative_decoding_draft_sampling_gb300 as sv
-        sv.build()
-        return make_case(name, dev, 1)
-    raise SystemExit("the reference arm generates its inputs on the GPU; no GPU found")
+def run_e2e(case, steps):
+    """The same step through the public API from pinned host buffers: every
+    step copies its inputs host -> device and its results device -> host
+    inside the timed region."""
+    h_in, d_in, call = case["e2e"]()
+    outs = call()
+    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    stream = torch.cuda.current_stream()
+
+    def one():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        res = call()
+        for h, o in zip(h_out, res):
+            h.copy_(o, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    pos = case["positions"]
+    pos0 = pos[0] if isinstance(pos, list) else pos
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    return dict(value=pos0 / (ms / 1e3), unit=UNIT, h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
+                ms_per_step=ms)
 
 
 def main():
@@ -383,12 +609,12 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="dflash",
-                    choices=["dflash", "eagle3", "eagle3_greedy", "chain_small", "ddtree", "dspark"])
+    ap.add_argument("--workload", default="dflash", choices=WORKLOAD_CHOICES)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--copies", type=int, default=3)
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--B", type=int, default=0, help="override the batch size of a chain workload (sweeps)")
     ap.add_argument("--slices", type=int, default=0, help="slices per row (0 = automatic)")
     ap.add_argument("--ctas-per-sm", type=int, default=0, help="resident CTAs per SM (0 = occupancy limit)")
@@ -439,17 +665,16 @@ def main():
     peak, peak_kind = peaks()
     achieved = bytes_step / (statistics.mean(step_ms) / 1e3) / 1e9
 
-    # end to end through the public API from pinned host buffers
-    e2e = None
-    if args.e2e_steps > 0 and args.workload not in ("ddtree", "dspark"):
-        e2e = run_e2e(case, args.e2e_steps, args.workload == "eagle3_greedy")
+    e2e = run_e2e(case, args.e2e_steps) if args.e2e_steps > 0 else None
 
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        v, n_req, el = oracle_sample(case, budget_s=15.0)
-        cpu = dict(value=v, unit=UNIT, cores=1, kind="oracle",
-                   sample=f"{n_req} whole requests of copy 0 run one by one by the single-threaded float64 C oracle "
-                          f"({el:.1f} s)")
+    cpu = parity = None
+    if rank == 0 and not (args.no_cpu_baseline and args.no_parity):
+        job = OracleJob(args.workload, case["inputs"][0],
+                        case["target"][0] if args.workload == "ddtree" else None)
+        if not args.no_parity:
+            parity = parity_report(case, job)
+        if not args.no_cpu_baseline:
+            cpu = cpu_baseline(job)
 
     if rank == 0:
         cfg = dict(case["cfg"])
@@ -459,56 +684,16 @@ def main():
                     ms_per_step=ms_per_step, higher_is_better=True, scaling="weak", vs_baseline=None,
                     dtype=case["dtype"], data="synthetic (seeded)", config=cfg,
                     roofline=dict(bound="hbm", achieved=achieved, peak=peak, unit="GB/s", frac=achieved / peak,
-                                  traffic=profiled_traffic(args.workload, bytes_step), peak_kind=peak_kind),
-                    cpu_baseline=cpu, e2e=e2e, gpu_launches=args.steps * (2 if args.workload in ("ddtree", "dspark") else 1),
+                                  traffic=profiled_traffic(args.workload, bytes_step), peak_kind=peak_kind,
+                                  nominal_peak=NOMINAL_HBM_GBS, frac_of_nominal=achieved / NOMINAL_HBM_GBS),
+                    parity=parity, cpu_baseline=cpu, e2e=e2e,
+                    gpu_launches=args.steps * case["launches_per_step"],
                     clocks=clocks, wall_s=wall)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
-
-
-def run_e2e(case, steps, greedy):
-    import speculative_decoding_draft_sampling_gb300 as sv
-    w = case["inputs"][0]
-    pin = lambda t: t.cpu().pin_memory()
-    h_logits, h_draft, h_u = pin(w.logits), pin(w.draft_greedy if greedy else w.draft), pin(w.uniforms)
-    h_q = None if greedy else pin(w.q)
-    d_logits, d_draft, d_u = torch.empty_like(w.logits), torch.empty_like(w.draft), torch.empty_like(w.uniforms)
-    d_q = None if greedy else torch.empty_like(w.q)
-    B, K = w.B, w.K
-    o_tok = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
-    o_n = torch.empty(B, dtype=torch.int32).pin_memory()
-    o_st = torch.empty(B, dtype=torch.int32).pin_memory()
-    stream = torch.cuda.current_stream()
-
-    def one():
-        d_logits.copy_(h_logits, non_blocking=True)
-        d_draft.copy_(h_draft, non_blocking=True)
-        d_u.copy_(h_u, non_blocking=True)
-        if greedy:
-            r = sv.verify_greedy(d_logits, d_draft)
-        else:
-            d_q.copy_(h_q, non_blocking=True)
-            r = sv.verify_chain(d_logits, d_q, d_draft, d_u, w.temperature, w.top_k)
-        o_tok.copy_(r.tokens, non_blocking=True)
-        o_n.copy_(r.num_accepted, non_blocking=True)
-        o_st.copy_(r.status, non_blocking=True)
-
-    one()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        one()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
-    h2d = sum(t.numel() * t.element_size() for t in (h_logits, h_draft, h_u) + (() if h_q is None else (h_q,)))
-    d2h = sum(t.numel() * t.element_size() for t in (o_tok, o_n, o_st))
-    return dict(value=B * K / (ms / 1e3), unit=UNIT, h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
-                ms_per_step=ms)
 
 
 if __name__ == "__main__":

@@ -12,6 +12,8 @@
  *     library never allocates device memory; scratch space comes from the
  *     caller's `ws` buffer, sized by the matching *_workspace_size() query.
  *     The workspace must not be shared by two calls in flight at once.
+ *     One exception: spec_verify_greedy_static takes no `ws` and uses a
+ *     fixed array the library reserves in device memory (described there).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls enqueue work and return without synchronising; they are
  *     free of host-device synchronisation and of allocation.
@@ -157,7 +159,10 @@ spec_status spec_verify_greedy(
  * rejected with SPEC_INVALID_ARG.  Nothing is allocated.
  * The first call on a device, with that device current, looks up the array's
  * device address (cudaGetSymbolAddress); make that first call before any
- * stream capture.  Every call on a device shares the array: calls whose GPU
+ * stream capture.  The address is kept per device together with the context
+ * it belongs to; a call that finds another context current (after a device
+ * reset) looks it up again, so make the first call after a reset outside
+ * capture too.  Every call on a device shares the array: calls whose GPU
  * work overlaps (different streams or host threads) race and must be
  * serialised by the caller.
  * ---------------------------------------------------------------------- */

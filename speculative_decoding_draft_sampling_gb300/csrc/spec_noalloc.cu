@@ -29,6 +29,26 @@ static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspa
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_ws_addr[kMaxDevices] = {};
+void* g_ws_ctx[kMaxDevices] = {};   // the context the address belongs to
+
+// The current CUDA context, through the driver entry point the runtime
+// resolves (no link-time dependency on the driver library); null if none.
+typedef int (*CtxGetCurrentFn)(void**);
+void* current_context() {
+    static CtxGetCurrentFn fn = nullptr;
+    static bool looked = false;
+    if (!looked) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+        looked = true;
+    }
+    void* ctx = nullptr;
+    if (!fn || fn(&ctx) != 0) return nullptr;
+    return ctx;
+}
 
 }  // namespace
 
@@ -55,15 +75,23 @@ extern "C" spec_status spec_verify_greedy_static(
     }
     void* ws = nullptr;
     {
-        // first call on this device (made current): look up the array's device address once
+        // First call on this device (made current): look up the array's
+        // device address.  The address belongs to the context the library's
+        // module was loaded into; after a device reset the device has a new
+        // context, so a changed context handle repeats the look-up.
         std::lock_guard<std::mutex> lk(g_mu);
-        if (!g_ws_addr[dev]) {
-            e = cudaGetSymbolAddress(&g_ws_addr[dev], g_static_workspace);
+        void* ctx = current_context();
+        if (!g_ws_addr[dev] || ctx == nullptr || ctx != g_ws_ctx[dev]) {
+            void* addr = nullptr;
+            e = cudaGetSymbolAddress(&addr, g_static_workspace);
             if (e != cudaSuccess) {
                 g_ws_addr[dev] = nullptr;
+                g_ws_ctx[dev] = nullptr;
                 spec::set_last_error("spec_verify_greedy_static: cudaGetSymbolAddress failed");
                 return SPEC_CUDA_ERROR;
             }
+            g_ws_addr[dev] = addr;
+            g_ws_ctx[dev] = current_context();
         }
         ws = g_ws_addr[dev];
     }

@@ -14,7 +14,7 @@ import torch
 import oracle
 import speculative_decoding_draft_sampling_gb300 as sv
 import workloads
-from gpu_util import compare_chain, compare_exact, host
+from gpu_util import assert_chain_parity, compare_exact, host, run_chunks
 
 pytestmark = pytest.mark.gpu
 
@@ -80,12 +80,16 @@ def test_tree_build_never_reads_past_needed_rows():
     _assert_tree_equal(_tree_np(g), ref)
 
 
-def test_tree_build_full_size_sampled():
+def _oracle_tree_all(qh, budget):
+    out = run_chunks(lambda a, b: {k: v for k, v in oracle.tree_build(qh[a:b], budget).items()}, qh.shape[0], chunk=1)
+    return out
+
+
+def test_tree_build_full_size_every_request():
     t = workloads.make_tree("ddtree", device=DEV)
     g = _tree_np(sv.tree_build(t.q, t.budget))
-    rows = [0, 13, 31]
-    ref = oracle.tree_build(host(t.q[rows]), t.budget)
-    _assert_tree_equal(g, ref, rows)
+    ref = _oracle_tree_all(host(t.q), t.budget)
+    _assert_tree_equal(g, ref)
     assert (g["num_nodes"] == t.budget).all()
 
 
@@ -106,16 +110,17 @@ def test_tree_walk_parity(B, L, V, N, dtype):
     assert sv.workspace_error(w.ws) == 0
 
 
-def test_tree_walk_full_size():
+def test_tree_walk_full_size_every_request():
     t = workloads.make_tree("ddtree", device=DEV)
     g = sv.tree_build(t.q, t.budget)
     tl = workloads.tree_target_logits(t, g.depth)
     w = sv.verify_tree(tl, g.token, g.parent, g.num_nodes, 16)
-    rows = [0, 7, 19, 31]
-    ref_t = oracle.tree_build(host(t.q[rows]), t.budget)
-    ref = oracle.verify_tree(host(tl[rows]), ref_t["token"], ref_t["parent"], ref_t["num_nodes"], 16)
-    for k in ("path_nodes", "tokens", "num_accepted"):
-        assert np.array_equal(getattr(w, k).cpu().numpy()[rows], ref[k]), k
+    ref_t = _oracle_tree_all(host(t.q), t.budget)
+    tlh = host(tl)
+    ref = run_chunks(lambda a, b: oracle.verify_tree(tlh[a:b], ref_t["token"][a:b], ref_t["parent"][a:b],
+                                                     ref_t["num_nodes"][a:b], 16), t.q.shape[0])
+    for k in ("path_nodes", "tokens", "num_accepted", "status"):
+        assert np.array_equal(getattr(w, k).cpu().numpy(), ref[k]), k
     assert (w.num_accepted.cpu().numpy() >= 1).mean() > 0.5     # the walk gets somewhere
 
 
@@ -162,35 +167,36 @@ def _ragged(w, a):
     return pl, pq
 
 
-@pytest.mark.parametrize("over", [dict(B=48, V=30011), dict(B=512, V=128256)])
+@pytest.mark.parametrize("over", [dict(B=48, V=30011), dict()])
 def test_ragged_verify_parity(over):
+    """The DSpark workload (over={} is the full B=512, Kmax=8, V=128256
+    configuration the benchmark times): verify lengths from the library, then
+    the ragged chain verify; every request compared with the oracle, which
+    packs its own rows from its own verify lengths."""
     w = workloads.make_chain("dspark", device=DEV, **over)
     a = sv.adaptive_len(w.conf, 1.0, 0.15)
     pl, pq = _ragged(w, a)
     r = sv.verify_chain(pl, pq, w.draft, w.uniforms, w.temperature, w.top_k,
                         k_per_req=a.k, l_row_off=a.l_row_off, q_row_off=a.q_row_off, diag=True)
     torch.cuda.synchronize()
-    full = over["B"] <= 64
-    idx = list(range(w.B)) if full else list(range(0, w.B, 64))
+    assert sv.workspace_error(r.ws) == 0
     aref = oracle.adaptive_len(host(w.conf), 1.0, 0.15)
     k = aref["k"]
-    # the oracle packs its own rows with its own offsets
-    sel_k = k[idx]
-    lo = np.concatenate([[0], np.cumsum(sel_k + 1)]).astype(np.int32)
-    qo = np.concatenate([[0], np.cumsum(sel_k)]).astype(np.int32)
-    lh = host(w.logits[idx])
-    qh = host(w.q[idx])
-    pl_h = np.concatenate([lh[j, :sel_k[j] + 1] for j in range(len(idx))])
-    pq_h = np.concatenate([qh[j, :sel_k[j]] for j in range(len(idx))] + [np.zeros((1, w.V), np.float32)])
-    ref = oracle.verify_chain(pl_h, pq_h, host(w.draft[idx]), host(w.uniforms[idx]), w.temperature, w.top_k,
-                              K=w.K, V=w.V, k_per_req=sel_k, l_row_off=lo, q_row_off=qo)
+    assert np.array_equal(a.k.cpu().numpy(), k)
+    lh, qh, dh, uh = host(w.logits), host(w.q), host(w.draft), host(w.uniforms)
 
-    class Sub:
-        pass
-    sub = Sub()
-    sub.tokens, sub.num_accepted, sub.status, sub.diag = r.tokens[idx], r.num_accepted[idx], r.status[idx], r.diag[idx]
-    bad, near = compare_chain(sub, ref, w.K)
-    assert not bad, bad[:5]
+    def part(lo_b, hi_b):
+        sel_k = k[lo_b:hi_b]
+        lo = np.concatenate([[0], np.cumsum(sel_k + 1)]).astype(np.int32)
+        qo = np.concatenate([[0], np.cumsum(sel_k)]).astype(np.int32)
+        pl_h = np.concatenate([lh[j, :sel_k[j - lo_b] + 1] for j in range(lo_b, hi_b)])
+        pq_h = np.concatenate([qh[j, :sel_k[j - lo_b]] for j in range(lo_b, hi_b)] + [np.zeros((1, w.V), np.float32)])
+        return oracle.verify_chain(pl_h, pq_h, dh[lo_b:hi_b], uh[lo_b:hi_b], w.temperature, w.top_k,
+                                   K=w.K, V=w.V, k_per_req=sel_k, l_row_off=lo, q_row_off=qo)
+
+    ref = run_chunks(part, w.B)
+    near = assert_chain_parity(r, ref, w.K, draft=w.draft)
+    print(f"dspark {over}: {w.B} requests compared, {near} near-tie(s) excused")
 
 
 def test_ragged_greedy_and_bad_lengths():
@@ -209,8 +215,7 @@ def test_ragged_greedy_and_bad_lengths():
                         q_row_off=qog)
     ref = oracle.verify_chain(host(pl), host(pq), host(w.draft), host(w.uniforms), w.temperature, w.top_k,
                               K=w.K, V=w.V, k_per_req=k.numpy(), l_row_off=lo.numpy(), q_row_off=qo.numpy())
-    bad, _ = compare_chain(r, ref, w.K, check_diag=False)
-    assert not bad, bad
+    assert_chain_parity(r, ref, w.K, check_diag=False)
     assert r.status[3].item() == 16 and r.status[4].item() == 16
     g = sv.verify_greedy(pl, w.draft, k_per_req=kg, l_row_off=log)
     gref = oracle.verify_greedy(host(pl), host(w.draft), K=w.K, V=w.V, k_per_req=k.numpy(), l_row_off=lo.numpy())

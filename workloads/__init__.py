@@ -34,6 +34,8 @@ WORKLOADS = {
     "dflash": (2, "block-draft chain verify B=256 K=8 V=151936, fp32 logits N(0,3^2), T=1, top-k 50"),
     "ddtree": (3, "DDTree B=32 L=16 budget 64 V=151936, q fp32, target bf16"),
     "dspark": (4, "DSpark adaptive ragged verify B=512 Kmax=8 V=128256, bf16, T=1, top-k 50"),
+    "dflash_vs": (5, "block-draft chain verify, DFlash shape, every row with its own logit scale "
+                     "U[0.5, 6] and offset U[-20, 20], T=1, top-k 50"),
 }
 
 DEFAULTS = {
@@ -43,6 +45,7 @@ DEFAULTS = {
     "ddtree": dict(B=32, L=16, N=64, V=151936),
     "dspark": dict(B=512, K=8, V=128256, dtype="bf16", sigma=3.0, T=1.0, top_k=50,
                    a=1.0, b=0.15),
+    "dflash_vs": dict(B=256, K=8, V=151936, dtype="f32", sigma=3.0, T=1.0, top_k=50),
 }
 
 
@@ -117,6 +120,13 @@ def make_chain(name: str, device="cpu", seed: Optional[int] = None, **over) -> C
     g = _gen(device, seed)
     sigma = cfg["sigma"]
     logits32 = torch.randn((B, K + 1, V), generator=g, device=device) * sigma
+    row_scale = None
+    if name == "dflash_vs":
+        # every row its own scale and offset: the top-k threshold of one row
+        # says little about the next row's (or the next call's)
+        row_scale = torch.rand((B, K + 1, 1), generator=g, device=device) * 5.5 + 0.5
+        offset = torch.rand((B, K + 1, 1), generator=g, device=device) * 40.0 - 20.0
+        logits32 = logits32 / sigma * row_scale + offset
     if cfg["dtype"] == "bf16":
         logits = logits32.to(torch.bfloat16)
         base = logits.float()
@@ -130,10 +140,15 @@ def make_chain(name: str, device="cpu", seed: Optional[int] = None, **over) -> C
     elif name == "eagle3":
         z = base * 0.9 + torch.randn((B, K, V), generator=g, device=device)
         draft_greedy = torch.argmax(z, dim=-1).to(torch.int32)
-    elif name == "dflash":
-        # noise std grows linearly from 0.5 to 2.0 across the block
+    elif name in ("dflash", "dflash_vs"):
+        # noise std grows linearly from 0.5 to 2.0 across the block (relative
+        # to the row's own scale for the varying-scale variant)
         stds = torch.linspace(0.5, 2.0, K, device=device) if K > 1 else torch.full((1,), 0.5, device=device)
-        z = base + torch.randn((B, K, V), generator=g, device=device) * stds.view(1, K, 1)
+        noise = torch.randn((B, K, V), generator=g, device=device) * stds.view(1, K, 1)
+        if row_scale is not None:
+            noise = noise * (row_scale[:, :K] / sigma)
+        z = base + noise
+        del noise
         z = _truncate_top(z, cfg["top_k"])       # "top-k applied to both p and q"
     elif name == "dspark":
         z = base + torch.randn((B, K, V), generator=g, device=device) * 1.0
