@@ -79,6 +79,9 @@ def _load():
             lib.oracle_verify_tree.argtypes = [P, i32, i64, i64, P, P, P, i32, i32, i32, i32,
                                                P, P, P, P]
             lib.oracle_verify_tree.restype = None
+            lib.oracle_verify_tree_sample.argtypes = [P, i32, i64, i64, P, P, P, P, i32, i32, i32, i32,
+                                                      f32, i32, P, P, P, P, P]
+            lib.oracle_verify_tree_sample.restype = None
             lib.oracle_adaptive_len.argtypes = [P, i32, i32, f32, f32, P, P, P, P, P, P]
             lib.oracle_adaptive_len.restype = None
             _lib = lib
@@ -229,6 +232,33 @@ def verify_tree(logits, token, parent, num_nodes, max_depth, *, l_strides=None):
     lib.oracle_verify_tree(_ptr(la), ldt, l_strides[0], l_strides[1], _ptr(tk), _ptr(pr),
                            _ptr(nn), B, N, V, max_depth, _ptr(pn), _ptr(ot), _ptr(na), _ptr(st))
     return dict(path_nodes=pn, tokens=ot, num_accepted=na, status=st)
+
+
+def verify_tree_sample(logits, token, parent, num_nodes, uniforms, max_depth, temperature, top_k=0, *,
+                       l_strides=None):
+    """Stochastic tree walk over target logits [B, N, V]: at depth d the
+    current node's token is drawn from its p with uniforms[b, d] (page §1,
+    §5 DDTree)."""
+    lib = _load()
+    la, ldt = _logits_arg(logits)
+    tk = np.ascontiguousarray(token, dtype=np.int32)
+    pr = np.ascontiguousarray(parent, dtype=np.int32)
+    nn = np.ascontiguousarray(num_nodes, dtype=np.int32)
+    u = np.ascontiguousarray(uniforms, dtype=np.float32)
+    B, N = tk.shape
+    V = la.shape[-1]
+    if l_strides is None:
+        l_strides = (N * V, V)
+    assert u.shape == (B, max_depth + 1)
+    pn = np.empty((B, max_depth + 1), np.int32)
+    ot = np.empty((B, max_depth + 1), np.int32)
+    na = np.empty(B, np.int32)
+    st = np.empty(B, np.int32)
+    nt = np.empty(B, np.int32)
+    lib.oracle_verify_tree_sample(_ptr(la), ldt, l_strides[0], l_strides[1], _ptr(tk), _ptr(pr), _ptr(nn), _ptr(u),
+                                  B, N, V, max_depth, float(temperature), int(top_k),
+                                  _ptr(pn), _ptr(ot), _ptr(na), _ptr(st), _ptr(nt))
+    return dict(path_nodes=pn, tokens=ot, num_accepted=na, status=st, near_tie=nt.view(np.uint32))
 
 
 def adaptive_len(conf, a, b):

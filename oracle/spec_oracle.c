@@ -617,6 +617,59 @@ void oracle_verify_tree(
 }
 
 /* ------------------------------------------------------------------ */
+/* [SD-survey] §1 (the chain rule is not a tree sampler: a tree needs a   */
+/* sampling rule of its own) and §5 "DDTree" (follow the target-selected  */
+/* token): at every walked node the target token is drawn from that      */
+/* node's p (temperature and top-k folded in) with the depth's uniform;   */
+/* a child carrying it is accepted and the walk continues there,          */
+/* otherwise the drawn token is the bonus.  Every committed token is a    */
+/* draw from the target, so the committed sequence follows the target.   */
+/* ------------------------------------------------------------------ */
+
+void oracle_verify_tree_sample(
+    const void* logits, int ldt, int64_t l_bstride, int64_t l_rstride,
+    const int32_t* token, const int32_t* parent, const int32_t* num_nodes,
+    const float* uniforms, int B, int N, int V, int max_depth,
+    float temperature, int top_k,
+    int32_t* path_nodes, int32_t* out_tokens, int32_t* num_accepted,
+    int32_t* status, int32_t* near_tie)
+{
+    double* l = (double*)malloc((size_t)V * sizeof(double));
+    double* p = (double*)malloc((size_t)V * sizeof(double));
+    double* scratch = (double*)malloc((size_t)V * sizeof(double));
+    const double T = (double)temperature;
+    for (int b = 0; b < B; ++b) {
+        int32_t* pn = path_nodes + (int64_t)b * (max_depth + 1);
+        int32_t* ot = out_tokens + (int64_t)b * (max_depth + 1);
+        const float* u = uniforms + (int64_t)b * (max_depth + 1);
+        for (int i = 0; i <= max_depth; ++i) { pn[i] = -1; ot[i] = -1; }
+        int st = 0, acc = 0, cur = 0, nt = 0;
+        int nn = num_nodes[b];
+        pn[0] = 0;
+        for (;;) {
+            load_row(logits, ldt, (int64_t)b * l_bstride + (int64_t)cur * l_rstride, V, l);
+            if (!row_valid(l, V)) { st |= ORC_ST_BAD_ROW; break; }
+            form_p(l, V, T, top_k, p, scratch);
+            int near = 0;
+            int t = sample_icdf(p, V, (double)u[acc], &near, NULL);
+            if (near && acc < 31) nt |= 1 << acc;
+            int child = -1;
+            for (int c = 0; c < nn && c < N; ++c)
+                if (parent[(int64_t)b * N + c] == cur && token[(int64_t)b * N + c] == t) { child = c; break; }
+            ot[acc] = t;
+            if (child < 0 || acc >= max_depth) break;
+            acc++;
+            pn[acc] = child;
+            cur = child;
+        }
+        num_accepted[b] = acc;
+        status[b] = st;
+        if (near_tie) near_tie[b] = nt;
+    }
+    free(l); free(p); free(scratch);
+}
+
+/* ------------------------------------------------------------------ */
 /* [SD-survey] §5 "DSpark": s_j = prod_{i<=j} c_i, expected advance      */
 /* 1 + sum_{j<=k} s_j; the verify length maximises advance per cost      */
 /* a + b*k (ties to the smaller k)                                        */

@@ -88,6 +88,21 @@ void oracle_verify_tree(
     int32_t* path_nodes, int32_t* out_tokens, int32_t* num_accepted,
     int32_t* status);
 
+/* Stochastic tree-walk verification ([SD-survey] §1, a tree needs its own
+ * sampling rule; §5 "DDTree", follow the target-selected token).  At depth d
+ * the current node's target token is the inverse-CDF draw from its p
+ * (temperature, top-k, ties kept) with uniforms[b, d]; a child carrying it is
+ * accepted, otherwise it is the bonus token.  uniforms [B, max_depth+1].
+ * near_tie[b] bit d: the draw at depth d lay within 1e-6 (normalised) of a
+ * CDF boundary. */
+void oracle_verify_tree_sample(
+    const void* logits, int ldt, int64_t l_bstride, int64_t l_rstride,
+    const int32_t* token, const int32_t* parent, const int32_t* num_nodes,
+    const float* uniforms, int B, int N, int V, int max_depth,
+    float temperature, int top_k,
+    int32_t* path_nodes, int32_t* out_tokens, int32_t* num_accepted,
+    int32_t* status, int32_t* near_tie);
+
 /* DSpark prefix survival and adaptive verify length ([SD-survey] §5
  * "DSpark", s_j equation and expected advance).  near_tie[b] = 1 when the
  * best and second-best E(k)/(a+b*k) differ by <= 1e-6 relative. */

@@ -570,6 +570,84 @@ def test_tree_walk_follows_constructed_target():
 
 
 # ---------------------------------------------------------------------------
+# §1 + §5 stochastic tree walk: every committed token is a target draw
+# ---------------------------------------------------------------------------
+
+
+def _walk_case(seed, B=40, L=5, V=60, N=24):
+    rng = np.random.default_rng(seed)
+    t = oracle.tree_build(_rand_q(rng, B, L, V), N)
+    # distinct logits (no tied maximum), with the tree's tokens pushed up so
+    # that walks go deep
+    logits = (rng.permutation(B * N * V).reshape(B, N, V) * 1e-3).astype(np.float32)
+    for b in range(B):
+        for c in range(1, N):
+            par = t["parent"][b, c]
+            if par >= 0 and rng.random() < 0.6:
+                logits[b, par, t["token"][b, c]] += 500.0 + rng.random()
+    return rng, t, logits, L
+
+
+def test_tree_sample_top1_equals_greedy_walk():
+    rng, t, logits, L = _walk_case(71)
+    u = rng.random((logits.shape[0], L + 1), dtype=np.float32)
+    s = oracle.verify_tree_sample(logits, t["token"], t["parent"], t["num_nodes"], u, L, 1.0, 1)
+    g = oracle.verify_tree(logits, t["token"], t["parent"], t["num_nodes"], L)
+    for k in ("path_nodes", "tokens", "num_accepted", "status"):
+        np.testing.assert_array_equal(s[k], g[k], err_msg=k)
+    assert (g["num_accepted"] >= 1).mean() > 0.3
+
+
+def test_tree_sample_tiny_temperature_equals_greedy_walk():
+    rng, t, logits, L = _walk_case(72)
+    u = np.clip(rng.random((logits.shape[0], L + 1), dtype=np.float32), 1e-3, 1 - 1e-3)
+    s = oracle.verify_tree_sample(logits, t["token"], t["parent"], t["num_nodes"], u, L, 1e-4, 0)
+    g = oracle.verify_tree(logits, t["token"], t["parent"], t["num_nodes"], L)
+    for k in ("path_nodes", "tokens", "num_accepted"):
+        np.testing.assert_array_equal(s[k], g[k], err_msg=k)
+
+
+def test_tree_sample_tokens_follow_target():
+    """A hand tree over V = 6: root -> tokens 0 (node 1) and 2 (node 2);
+    node 1 -> tokens 1 (node 3) and 3 (node 4); node 2 -> token 5 (node 5).
+    Over 10^6 walks the first committed token follows p_root, and the second
+    follows the p of the node the first one reached (the joint law of the
+    first two tokens is p_root(a) p_node(a)(b) whenever a has a node)."""
+    rng = np.random.default_rng(73)
+    V, L, n = 6, 2, 1_000_000
+    P = np.array([[0.30, 0.10, 0.25, 0.05, 0.20, 0.10],    # root
+                  [0.05, 0.40, 0.10, 0.25, 0.10, 0.10],    # node 1 (after token 0)
+                  [0.20, 0.10, 0.10, 0.10, 0.10, 0.40],    # node 2 (after token 2)
+                  [0.50, 0.10, 0.10, 0.10, 0.10, 0.10],
+                  [0.10, 0.50, 0.10, 0.10, 0.10, 0.10],
+                  [0.10, 0.10, 0.50, 0.10, 0.10, 0.10]])
+    token = np.array([-1, 0, 2, 1, 3, 5], np.int32)
+    parent = np.array([-1, 0, 0, 1, 1, 2], np.int32)
+    N = 6
+    logits = np.log(P).astype(np.float32)[None]                      # [1, N, V], broadcast
+    u = rng.random((n, L + 1), dtype=np.float32)
+    out = oracle.verify_tree_sample(logits, np.broadcast_to(token, (n, N)), np.broadcast_to(parent, (n, N)),
+                                    np.full(n, N, np.int32), u, L, 1.0, 0, l_strides=(0, V))
+    tok = out["tokens"]
+    assert chi2_pvalue(np.bincount(tok[:, 0], minlength=V), P[0]) > 1e-3
+    node_of = {0: 1, 2: 2}
+    for a, node in node_of.items():
+        sel = tok[:, 0] == a
+        assert (out["num_accepted"][sel] >= 1).all()
+        assert chi2_pvalue(np.bincount(tok[sel, 1], minlength=V), P[node]) > 1e-3
+    # tokens without a node end the walk: nothing after them
+    ends = ~np.isin(tok[:, 0], [0, 2])
+    assert (out["num_accepted"][ends] == 0).all() and (tok[ends, 1] == -1).all()
+    # the joint of the first two tokens over the walks that reached depth 1
+    pairs = tok[:, 0] * V + np.where(tok[:, 1] >= 0, tok[:, 1], 0)
+    deep = np.isin(tok[:, 0], [0, 2])
+    joint = np.zeros(V * V)
+    for a, node in node_of.items():
+        joint[a * V:(a + 1) * V] = P[0, a] * P[node]
+    assert chi2_pvalue(np.bincount(pairs[deep], minlength=V * V), joint) > 1e-3
+
+
+# ---------------------------------------------------------------------------
 # §5 DSpark: s_j = prod c_i, advance 1 + sum s_j, k maximising advance/cost
 # ---------------------------------------------------------------------------
 
