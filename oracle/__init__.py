@@ -82,7 +82,7 @@ def _load():
             lib.oracle_verify_tree_sample.argtypes = [P, i32, i64, i64, P, P, P, P, i32, i32, i32, i32,
                                                       f32, i32, P, P, P, P, P]
             lib.oracle_verify_tree_sample.restype = None
-            lib.oracle_adaptive_len.argtypes = [P, i32, i32, f32, f32, P, P, P, P, P, P]
+            lib.oracle_adaptive_len.argtypes = [P, i32, i32, f32, f32, P, P, P, P, P, P, P]
             lib.oracle_adaptive_len.restype = None
             _lib = lib
     return _lib
@@ -108,7 +108,9 @@ def verify_chain(logits, q, draft, uniforms, temperature, top_k=0, *,
     """Chain speculative sampling, per request (page §1).
 
     Dense: logits [B, K+1, V], q [B, K, V].  Ragged: logits packed rows
-    [sum(k_b+1), V], q packed rows [sum(k_b), V] with exclusive offsets.
+    [sum(k_b+1), V], q packed rows [sum(k_b), V] with exclusive offsets;
+    k_per_req without offsets keeps the dense rows and caps each request at
+    its k_b (page §9 "cap-accept").
     ``l_strides`` / ``q_strides`` = (batch, row) element strides override the
     contiguous defaults (batch stride 0 broadcasts one set of rows).
     Returns a dict of numpy arrays: tokens [B, K+1], num_accepted, status,
@@ -129,10 +131,11 @@ def verify_chain(logits, q, draft, uniforms, temperature, top_k=0, *,
     kp = lo = qo = None
     if k_per_req is not None:
         kp = np.ascontiguousarray(k_per_req, dtype=np.int32)
-        lo = np.ascontiguousarray(l_row_off, dtype=np.int32)
-        qo = np.ascontiguousarray(q_row_off, dtype=np.int32)
-        l_strides = (0, V) if l_strides is None else (0, l_strides[1])
-        q_strides = (0, V) if q_strides is None else (0, q_strides[1])
+        if l_row_off is not None:        # packed rows ("compact")
+            lo = np.ascontiguousarray(l_row_off, dtype=np.int32)
+            qo = np.ascontiguousarray(q_row_off, dtype=np.int32)
+            l_strides = (0, V) if l_strides is None else (0, l_strides[1])
+            q_strides = (0, V) if q_strides is None else (0, q_strides[1])
     tok = np.empty((B, K + 1), np.int32)
     n = np.empty(B, np.int32)
     st = np.empty(B, np.int32)
@@ -162,8 +165,9 @@ def verify_greedy(logits, draft, *, K=None, V=None, k_per_req=None, l_row_off=No
     kp = lo = None
     if k_per_req is not None:
         kp = np.ascontiguousarray(k_per_req, dtype=np.int32)
-        lo = np.ascontiguousarray(l_row_off, dtype=np.int32)
-        l_strides = (0, l_strides[1])
+        if l_row_off is not None:
+            lo = np.ascontiguousarray(l_row_off, dtype=np.int32)
+            l_strides = (0, l_strides[1])
     tok = np.empty((B, K + 1), np.int32)
     n = np.empty(B, np.int32)
     st = np.empty(B, np.int32)
@@ -261,17 +265,22 @@ def verify_tree_sample(logits, token, parent, num_nodes, uniforms, max_depth, te
     return dict(path_nodes=pn, tokens=ot, num_accepted=na, status=st, near_tie=nt.view(np.uint32))
 
 
-def adaptive_len(conf, a, b):
-    """DSpark survival, expected advance and verify length (page §5)."""
+def adaptive_len(conf, a, b, cost=None):
+    """DSpark survival, expected advance and verify length (page §5); the
+    cost of k positions is a + b*k, or cost[k] with a table (page §9)."""
     lib = _load()
     c = np.ascontiguousarray(conf, dtype=np.float32)
     B, Kmax = c.shape
+    ct = None
+    if cost is not None:
+        ct = np.ascontiguousarray(cost, dtype=np.float64)
+        assert ct.shape == (Kmax + 1,)
     k = np.empty(B, np.int32)
     surv = np.empty((B, Kmax), np.float64)
     adv = np.empty(B, np.float64)
     lo = np.empty(B + 1, np.int32)
     qo = np.empty(B + 1, np.int32)
     nt = np.empty(B, np.int32)
-    lib.oracle_adaptive_len(_ptr(c), B, Kmax, float(a), float(b), _ptr(k), _ptr(surv),
+    lib.oracle_adaptive_len(_ptr(c), B, Kmax, float(a), float(b), _ptr(ct), _ptr(k), _ptr(surv),
                             _ptr(adv), _ptr(lo), _ptr(qo), _ptr(nt))
     return dict(k=k, surv=surv, exp_adv=adv, l_row_off=lo, q_row_off=qo, near_tie=nt)

@@ -170,9 +170,9 @@ void oracle_verify_chain(
 
         int finished = 0;
         for (int i = 0; i < k && !finished; ++i) {
-            int64_t lrow = k_per_req ? ((int64_t)l_row_off[b] + i) * l_rstride
+            int64_t lrow = l_row_off ? ((int64_t)l_row_off[b] + i) * l_rstride
                                      : (int64_t)b * l_bstride + (int64_t)i * l_rstride;
-            int64_t qrow = k_per_req ? ((int64_t)q_row_off[b] + i) * q_rstride
+            int64_t qrow = q_row_off ? ((int64_t)q_row_off[b] + i) * q_rstride
                                      : (int64_t)b * q_bstride + (int64_t)i * q_rstride;
             load_row(logits, ldt, lrow, V, l);
             nread++;
@@ -230,7 +230,7 @@ void oracle_verify_chain(
         if (!finished) {
             /* [SD-survey] §1: every draft passed, sample one more token from
              * the target distribution of the next position */
-            int64_t lrow = k_per_req ? ((int64_t)l_row_off[b] + k) * l_rstride
+            int64_t lrow = l_row_off ? ((int64_t)l_row_off[b] + k) * l_rstride
                                      : (int64_t)b * l_bstride + (int64_t)k * l_rstride;
             load_row(logits, ldt, lrow, V, l);
             nread++;
@@ -293,7 +293,7 @@ void oracle_verify_greedy(
             }
         }
         for (int i = 0; i <= k; ++i) {
-            int64_t lrow = k_per_req ? ((int64_t)l_row_off[b] + i) * l_rstride
+            int64_t lrow = l_row_off ? ((int64_t)l_row_off[b] + i) * l_rstride
                                      : (int64_t)b * l_bstride + (int64_t)i * l_rstride;
             load_row(logits, ldt, lrow, V, l);
             nread++;
@@ -676,7 +676,7 @@ void oracle_verify_tree_sample(
 /* ------------------------------------------------------------------ */
 
 void oracle_adaptive_len(
-    const float* conf, int B, int Kmax, float a, float b,
+    const float* conf, int B, int Kmax, float a, float b, const double* cost,
     int32_t* k_out, double* surv, double* exp_adv,
     int32_t* l_row_off, int32_t* q_row_off, int32_t* near_tie)
 {
@@ -684,7 +684,7 @@ void oracle_adaptive_len(
     int32_t lo = 0, qo = 0;
     for (int r = 0; r < B; ++r) {
         double s = 1.0, E = 1.0;
-        double best = 1.0 / (A + Bc * 0.0);
+        double best = 1.0 / (cost ? cost[0] : A + Bc * 0.0);
         double second = -INFINITY;
         double best_E = 1.0;
         int best_k = 0;
@@ -692,7 +692,9 @@ void oracle_adaptive_len(
             s = s * (double)conf[(int64_t)r * Kmax + (j - 1)];
             if (surv) surv[(int64_t)r * Kmax + (j - 1)] = s;
             E = E + s;
-            double ratio = E / (A + Bc * (double)j);
+            /* [SD-survey] §9: with a profiled cost table the cost of verifying
+             * j positions is its entry j, otherwise a + b*j */
+            double ratio = E / (cost ? cost[j] : A + Bc * (double)j);
             if (ratio > best) { second = best; best = ratio; best_k = j; best_E = E; }
             else if (ratio > second) { second = ratio; }
         }

@@ -35,7 +35,10 @@ extern "C" {
 /* near-tie window (absolute on the ratio, relative to the mass on the CDF) */
 #define ORC_NEAR_TIE 1e-6
 
-/* Chain speculative sampling ([SD-survey] §1).  near_tie[b]: bit i set when
+/* Chain speculative sampling ([SD-survey] §1).  With k_per_req and no row
+ * offsets the rows keep the dense layout and request b verifies only its
+ * first k_b positions ([SD-survey] §9 "cap-accept": the full window is
+ * computed, the commit is capped).  near_tie[b]: bit i set when
  * |u_i - p_i(y_i)/q_i(y_i)| <= 1e-6 at an examined position i (i < 31);
  * bit 31 set when the final sample's target lies within 1e-6 (normalised) of
  * either boundary of the chosen token's CDF interval.  rows_read[b] = number
@@ -104,10 +107,12 @@ void oracle_verify_tree_sample(
     int32_t* status, int32_t* near_tie);
 
 /* DSpark prefix survival and adaptive verify length ([SD-survey] §5
- * "DSpark", s_j equation and expected advance).  near_tie[b] = 1 when the
- * best and second-best E(k)/(a+b*k) differ by <= 1e-6 relative. */
+ * "DSpark", s_j equation and expected advance).  The cost of verifying k
+ * positions is a + b*k, or cost[k] when a table (Kmax+1 entries, [SD-survey]
+ * §9's profiled per-deployment table) is given.  near_tie[b] = 1 when the
+ * best and second-best E(k)/cost(k) differ by <= 1e-6 relative. */
 void oracle_adaptive_len(
-    const float* conf, int B, int Kmax, float a, float b,
+    const float* conf, int B, int Kmax, float a, float b, const double* cost,
     int32_t* k_out, double* surv, double* exp_adv,
     int32_t* l_row_off, int32_t* q_row_off, int32_t* near_tie);
 

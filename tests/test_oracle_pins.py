@@ -409,6 +409,43 @@ def test_ragged_equals_dense_per_request():
         assert rg["num_accepted"][b] == d1["num_accepted"][0]
 
 
+def test_cap_accept_equals_compact_and_dense_prefix():
+    """Page §9's ragged modes: "cap-accept" keeps the full dense window and
+    caps the commit at k_b; "compact" packs only the k_b + 1 rows; both equal
+    a dense verify of the first k_b + 1 rows of each request."""
+    rng = np.random.default_rng(19)
+    B, K, V = 30, 6, 40
+    logits = (rng.standard_normal((B, K + 1, V)) * 2).astype(np.float32)
+    q = rng.dirichlet(np.ones(V) * 0.5, size=(B, K)).astype(np.float32)
+    draft = np.stack([[draw(rng, q[b, i], 1)[0] for i in range(K)] for b in range(B)]).astype(np.int32)
+    u = rng.random((B, K + 1), dtype=np.float32)
+    k = rng.integers(0, K + 1, B).astype(np.int32)
+    for top_k in (0, 5):
+        cap = oracle.verify_chain(logits, q, draft, u, 0.8, top_k, k_per_req=k)
+        lo = np.concatenate([[0], np.cumsum(k + 1)]).astype(np.int32)
+        qo = np.concatenate([[0], np.cumsum(k)]).astype(np.int32)
+        pl = np.concatenate([logits[b, :k[b] + 1] for b in range(B)])
+        pq = np.concatenate([q[b, :k[b]] for b in range(B)] + [np.zeros((1, V), np.float32)])
+        comp = oracle.verify_chain(pl, pq, draft, u, 0.8, top_k, K=K, V=V, k_per_req=k, l_row_off=lo, q_row_off=qo)
+        for key in ("tokens", "num_accepted", "status", "rows_read"):
+            np.testing.assert_array_equal(cap[key], comp[key], err_msg=key)
+        for b in range(B):
+            kb = int(k[b])
+            uu = np.concatenate([u[b, :kb], [u[b, kb]]])[None].astype(np.float32)
+            d1 = oracle.verify_chain(logits[b:b + 1, :kb + 1],
+                                     q[b:b + 1, :kb] if kb else np.zeros((1, 1, V), np.float32),
+                                     draft[b:b + 1, :kb] if kb else np.zeros((1, 0), np.int32), uu, 0.8, top_k,
+                                     K=kb, V=V)
+            assert cap["tokens"][b, :kb + 1].tolist() == d1["tokens"][0].tolist()
+            assert (cap["tokens"][b, kb + 1:] == -1).all()
+            assert cap["num_accepted"][b] == d1["num_accepted"][0] <= kb
+    # every k_b = K: the cap never binds, the result is the static (dense) one
+    full = oracle.verify_chain(logits, q, draft, u, 0.8, 5, k_per_req=np.full(B, K, np.int32))
+    dense = oracle.verify_chain(logits, q, draft, u, 0.8, 5)
+    np.testing.assert_array_equal(full["tokens"], dense["tokens"])
+    np.testing.assert_array_equal(full["num_accepted"], dense["num_accepted"])
+
+
 # ---------------------------------------------------------------------------
 # greedy: argmax with the lowest index on ties
 # ---------------------------------------------------------------------------
@@ -697,3 +734,45 @@ def test_adaptive_exact_rational_bruteforce():
         np.testing.assert_allclose(o["surv"][r], np.cumprod(c[r].astype(np.float64)), rtol=1e-14)
     np.testing.assert_array_equal(o["l_row_off"], lo)
     np.testing.assert_array_equal(np.diff(o["q_row_off"]), o["k"])
+
+
+def test_adaptive_cost_table_of_a_linear_cost_is_the_linear_rule():
+    rng = np.random.default_rng(62)
+    B, Kmax = 3000, 8
+    c = rng.beta(8, 2, size=(B, Kmax)).astype(np.float32)
+    a, b = 1.0, 0.15
+    table = np.float64(np.float32(a)) + np.float64(np.float32(b)) * np.arange(Kmax + 1, dtype=np.float64)
+    lin = oracle.adaptive_len(c, a, b)
+    tab = oracle.adaptive_len(c, 7.0, 3.0, cost=table)        # a, b ignored with a table
+    for key in ("k", "surv", "exp_adv", "l_row_off", "q_row_off"):
+        np.testing.assert_array_equal(lin[key], tab[key], err_msg=key)
+
+
+def test_adaptive_cost_table_hand_example():
+    # E = 1, 1.9, 2.62, 2.98, 3.16 (as in the linear hand example, where k = 3);
+    # a table where two positions cost as much as none and the third doubles
+    # the price: E/cost = 1, 1.9, 2.62, 1.192, 1.264 -> k = 2
+    c = np.array([[0.9, 0.8, 0.5, 0.5]], np.float32)
+    o = oracle.adaptive_len(c, 1.0, 0.15, cost=np.array([1.0, 1.0, 1.0, 2.5, 2.5]))
+    assert o["k"][0] == 2
+    np.testing.assert_allclose(o["exp_adv"][0], 2.62, rtol=1e-6)
+    np.testing.assert_array_equal(o["l_row_off"], [0, 3])
+
+
+def test_adaptive_cost_table_exact_rational_bruteforce():
+    rng = np.random.default_rng(63)
+    B, Kmax = 1500, 8
+    c = rng.beta(8, 2, size=(B, Kmax)).astype(np.float32)
+    table = np.cumsum(rng.random(Kmax + 1) * 0.4 + 0.05) + 0.5
+    o = oracle.adaptive_len(c, 1.0, 0.15, cost=table)
+    Ct = [Fraction(float(x)) for x in table]
+    for r in range(B):
+        s, E = Fraction(1), Fraction(1)
+        ratios = [E / Ct[0]]
+        for j in range(Kmax):
+            s *= Fraction(float(c[r, j]))
+            E += s
+            ratios.append(E / Ct[j + 1])
+        best = max(range(Kmax + 1), key=lambda k: (ratios[k], -k))
+        if not o["near_tie"][r]:
+            assert o["k"][r] == best, r
