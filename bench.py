@@ -616,8 +616,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--B", type=int, default=0, help="override the batch size of a chain workload (sweeps)")
-    ap.add_argument("--slices", type=int, default=0, help="slices per row (0 = automatic)")
-    ap.add_argument("--ctas-per-sm", type=int, default=0, help="resident CTAs per SM (0 = occupancy limit)")
+    ap.add_argument("--slices", type=int, default=0, help="CTAs per cluster, one row slice each (0 = automatic)")
+    ap.add_argument("--slots-per-cta", type=int, default=0, help="requests in flight per CTA (0 = automatic)")
     args = ap.parse_args()
     rank, world, local = dist_setup()
     if torch.cuda.is_available():
@@ -631,7 +631,7 @@ def main():
     barrier(world)
     sv.build()
     dev = torch.device("cuda", local)
-    sv.set_tuning(args.slices, args.ctas_per_sm)
+    sv.set_tuning(args.slices, args.slots_per_cta)
     case = make_case(args.workload, dev, args.copies, over={"B": args.B} if args.B > 0 else None)
     step = case["step"]
     stream = torch.cuda.current_stream()

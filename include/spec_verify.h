@@ -28,9 +28,8 @@
  *     aligned are streamed by the Tensor Memory Accelerator; other layouts
  *     are accepted and read with plain loads (slower).
  *   - Token ids are int32 in [0, V).  Output token rows are padded with -1.
- *   - Shape limits (SPEC_UNSUPPORTED beyond them): B <= 4194302 requests per
- *     call; K <= 4096 draft positions; N <= 8192 tree nodes; tree build
- *     L <= 16, budget <= 256.
+ *   - Shape limits (SPEC_UNSUPPORTED beyond them): K <= 4096 draft
+ *     positions; N <= 8192 tree nodes; tree build L <= 16, budget <= 256.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -72,12 +71,14 @@ const char* spec_last_error(void);
 int spec_version(void);
 
 /*
- * Optional tuning, for benchmarking sweeps.  slices_per_row: how many CTAs
- * share one vocabulary row (0 = automatic).  ctas_per_sm: resident CTAs per
- * SM of the persistent grid (0 = automatic, i.e. as many as fit).  Affects
- * later calls of this process and later workspace-size queries.
+ * Optional tuning, for benchmarking sweeps.  The kernels run on thread-block
+ * clusters: every CTA of a cluster takes one slice of every vocabulary row
+ * the cluster reads.  slices_per_row: CTAs per cluster, 1..16 (0 =
+ * automatic: a power of two up to 8, each slice at least 2048 elements).
+ * slots_per_cta: requests each CTA's cluster keeps in flight per CTA, 1..4
+ * (0 = automatic, 2).  Affects later calls of this process.
  */
-spec_status spec_set_tuning(int slices_per_row, int ctas_per_sm);
+spec_status spec_set_tuning(int slices_per_row, int slots_per_cta);
 
 /*
  * Reads the device error word of a workspace after the stream is drained
@@ -93,9 +94,9 @@ spec_status spec_workspace_error(const void* ws, void* stream, uint32_t* err_out
  * if every draft passes, a bonus token is drawn from p_{K+1}.  Temperature
  * and top-k truncation are folded into p (same section).
  *
- *   logits   target logits, dtype `ldt`.  Dense mode (k_per_req == NULL):
+ *   logits   target logits, dtype `ldt`.  Dense layout (no row offsets):
  *            row (b, i), i = 0..K, starts at b*l_batch_stride + i*l_row_stride.
- *            Ragged mode: row (b, i), i = 0..k_b, starts at
+ *            Packed layout: row (b, i), i = 0..k_b, starts at
  *            (l_row_off[b] + i) * l_row_stride; l_batch_stride is ignored.
  *   q        draft proposal probabilities, fp32, used as given (not
  *            truncated or renormalised).  Row (b, i), i = 0..k-1, addressed
@@ -106,8 +107,12 @@ spec_status spec_workspace_error(const void* ws, void* stream, uint32_t* err_out
  *            token id, smallest x with C(x) > u * total).
  *   temperature > 0.  top_k <= 0 or >= V disables truncation; otherwise
  *            S = {x : l_x >= tau}, tau = top_k-th largest raw logit, ties kept.
- *   k_per_req, l_row_off, q_row_off  NULL for dense mode; else [B], [B+1],
- *            [B+1] (from spec_adaptive_len or the caller).
+ *   k_per_req, l_row_off, q_row_off  Ragged verify ([SD-survey] §9): NULL,
+ *            NULL, NULL = "static" (every request verifies all K rows);
+ *            k_per_req [B] with row offsets [B+1], [B+1] = "compact" (packed
+ *            rows, request b verifies k_b positions); k_per_req alone =
+ *            "cap-accept" (the dense rows of the full window, request b
+ *            verifies and commits only its first k_b positions).
  * Outputs:
  *   out_tokens   [B, K+1]: accepted drafts, then the correction or bonus token, then -1.
  *   num_accepted [B]: accepted draft tokens (excludes the correction/bonus token).
@@ -153,10 +158,12 @@ spec_status spec_verify_greedy(
  * host callbacks or allocator-free runtimes, plugins handed raw buffers by an
  * engine that owns every allocation, loops that forbid allocation after
  * start-up).  Same arguments and results as spec_verify_greedy, minus `ws`
- * and `ws_bytes`: the scratch space is an 8 MiB array in device memory that
+ * and `ws_bytes`: the scratch space is a 64 KiB array in device memory that
  * the library reserves on every GPU it is loaded on, until the process exits.
- * Batches whose spec_verify_greedy_workspace_size() exceeds 8 MiB are
- * rejected with SPEC_INVALID_ARG.  Nothing is allocated.
+ * Batches whose spec_verify_greedy_workspace_size() exceeds 64 KiB are
+ * rejected with SPEC_INVALID_ARG (greedy verification needs a fixed 256 bytes
+ * whatever the batch, so every shape within the other limits fits).  Nothing
+ * is allocated.
  * The first call on a device, with that device current, looks up the array's
  * device address (cudaGetSymbolAddress); make that first call before any
  * stream capture.  The address is kept per device together with the context
@@ -224,6 +231,32 @@ spec_status spec_verify_tree(
     void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * spec_verify_tree_sample -- stochastic tree-walk verification
+ * [SD-survey] §1: the chain acceptance rule is not a sampler for a tree of
+ * drafts, a tree needs its own rule; §5 "DDTree": verification follows the
+ * target-selected token, and a token no child carries becomes the bonus.
+ * At depth d the current node's target token is drawn from its p
+ * (temperature and top-k folded in exactly as in spec_verify_chain: ascending
+ * token id, the smallest x with C(x) > u[b, d] * total); a child carrying it
+ * is accepted and the walk continues there, otherwise the drawn token is the
+ * bonus.  Every committed token is a draw from the target, so the committed
+ * sequence follows the target distribution.
+ *
+ *   logits   [B, N, V] target rows of the tree's nodes (as spec_verify_tree).
+ *   token, parent, num_nodes   the tree (as produced by spec_tree_build).
+ *   uniforms [B, max_depth+1] fp32 in [0, 1): u[b, d] draws at depth d.
+ * Outputs as spec_verify_tree: path_nodes [B, L+1], out_tokens [B, L+1],
+ *   num_accepted [B], status [B].  Only rows on the walked path are read.
+ * ---------------------------------------------------------------------- */
+size_t spec_verify_tree_sample_workspace_size(int B, int N, int V);
+spec_status spec_verify_tree_sample(
+    const void* logits, spec_dtype ldt, int64_t l_batch_stride, int64_t l_row_stride,
+    const int32_t* token, const int32_t* parent, const int32_t* num_nodes, const float* uniforms,
+    int B, int N, int V, int max_depth, float temperature, int top_k,
+    int32_t* path_nodes, int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
+    void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * spec_adaptive_len -- DSpark verify length
  * [SD-survey] §5 "DSpark": prefix survival s_j = prod_{i<=j} c_i, expected
  * advance 1 + sum_{j<=k} s_j; each request verifies the k in [0, Kmax] that
@@ -238,6 +271,20 @@ spec_status spec_verify_tree(
  * ---------------------------------------------------------------------- */
 spec_status spec_adaptive_len(
     const float* conf, int B, int Kmax, float a, float b,
+    int32_t* k_out, double* surv, double* exp_adv,
+    int32_t* l_row_off, int32_t* q_row_off, void* stream);
+
+/* ------------------------------------------------------------------------
+ * spec_adaptive_len_table -- DSpark verify length with a profiled cost table
+ * [SD-survey] §9 (DSpark in SGLang): the cost of verifying k positions comes
+ * from a table profiled for the deployment rather than a formula.  As
+ * spec_adaptive_len with the cost a + b*k replaced by cost[k]:
+ *   cost   DEVICE pointer, [Kmax+1] fp64, every entry finite and > 0 (the
+ *          caller's responsibility: the kernel divides by it).
+ * Outputs as spec_adaptive_len.
+ * ---------------------------------------------------------------------- */
+spec_status spec_adaptive_len_table(
+    const float* conf, int B, int Kmax, const double* cost,
     int32_t* k_out, double* surv, double* exp_adv,
     int32_t* l_row_off, int32_t* q_row_off, void* stream);
 

@@ -13,6 +13,7 @@ Functions (same names as the C entry points, without the ``spec_`` prefix):
   verify_greedy  greedy argmax-match verification
   tree_build     DDTree best-first tree under a node budget
   verify_tree    greedy tree-walk verification
+  verify_tree_sample  stochastic tree-walk verification (target draws along the tree)
   adaptive_len   DSpark survival, expected advance and verify length
 """
 from __future__ import annotations
@@ -74,8 +75,14 @@ def _load():
         lib.spec_verify_tree_workspace_size.restype = sz
         lib.spec_verify_tree.argtypes = [P, i32, i64, i64, P, P, P, i32, i32, i32, i32, P, P, P, P, P, sz, P]
         lib.spec_adaptive_len.argtypes = [P, i32, i32, f32, f32, P, P, P, P, P, P]
+        lib.spec_adaptive_len_table.argtypes = [P, i32, i32, P, P, P, P, P, P, P]
+        lib.spec_adaptive_len_table.restype = ctypes.c_int
+        lib.spec_verify_tree_sample_workspace_size.argtypes = [i32, i32, i32]
+        lib.spec_verify_tree_sample_workspace_size.restype = sz
+        lib.spec_verify_tree_sample.argtypes = [P, i32, i64, i64, P, P, P, P, i32, i32, i32, i32, f32, i32,
+                                                P, P, P, P, P, sz, P]
         for name in ("spec_set_tuning", "spec_workspace_error", "spec_verify_chain", "spec_verify_greedy",
-                     "spec_tree_build", "spec_verify_tree", "spec_adaptive_len"):
+                     "spec_tree_build", "spec_verify_tree", "spec_adaptive_len", "spec_verify_tree_sample"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -131,8 +138,10 @@ def workspace(nbytes: int, device) -> torch.Tensor:
     return buf
 
 
-def set_tuning(slices_per_row: int = 0, ctas_per_sm: int = 0):
-    _check(_load().spec_set_tuning(int(slices_per_row), int(ctas_per_sm)), "spec_set_tuning")
+def set_tuning(slices_per_row: int = 0, slots_per_cta: int = 0):
+    """CTAs per cluster (one row slice each) and requests in flight per CTA;
+    0 = automatic.  For benchmarking sweeps."""
+    _check(_load().spec_set_tuning(int(slices_per_row), int(slots_per_cta)), "spec_set_tuning")
 
 
 def workspace_error(ws: torch.Tensor, stream=None) -> int:
@@ -164,9 +173,11 @@ def verify_chain(logits, q, draft, uniforms, temperature: float, top_k: int = 0,
     """Chain speculative sampling.
 
     Dense: logits [B, K+1, V], q [B, K, V] (any batch/row strides, unit
-    element stride).  Ragged (k_per_req given): logits [rows, V] packed by
-    l_row_off, q [rows, V] packed by q_row_off.  draft [B, K] int32,
-    uniforms [B, K+1] fp32.
+    element stride); with k_per_req alone each request verifies only its
+    first k_b positions ("cap-accept").  Packed ("compact", k_per_req with
+    l_row_off and q_row_off): logits [rows, V] packed by l_row_off, q
+    [rows, V] packed by q_row_off.  draft [B, K] int32, uniforms [B, K+1]
+    fp32.
     """
     L = _load()
     _cuda(logits, "logits")
@@ -182,15 +193,21 @@ def verify_chain(logits, q, draft, uniforms, temperature: float, top_k: int = 0,
         raise SpecError("uniforms must be [B, K+1]")
     if logits.stride(-1) != 1 or q.stride(-1) != 1:
         raise SpecError("logits and q need unit element stride")
-    ragged = k_per_req is not None
-    if ragged:
-        for t, n in ((k_per_req, "k_per_req"), (l_row_off, "l_row_off"), (q_row_off, "q_row_off")):
+    packed = l_row_off is not None
+    if k_per_req is not None:
+        _cuda(k_per_req, "k_per_req", torch.int32)
+    if packed:
+        if k_per_req is None or q_row_off is None:
+            raise SpecError("packed rows need k_per_req, l_row_off and q_row_off")
+        for t, n in ((l_row_off, "l_row_off"), (q_row_off, "q_row_off")):
             _cuda(t, n, torch.int32)
         if logits.dim() != 2 or q.dim() != 2:
-            raise SpecError("ragged mode takes packed 2-D logits and q")
+            raise SpecError("packed ('compact') mode takes packed 2-D logits and q")
         lbs, lrs = 0, logits.stride(0)
         qbs, qrs = 0, q.stride(0)
     else:
+        # dense rows: every request verifies K positions, or with k_per_req
+        # only its first k_b ("cap-accept")
         if logits.dim() != 3 or logits.shape[:2] != (B, K + 1):
             raise SpecError("dense logits must be [B, K+1, V]")
         if q.dim() != 3 or q.shape[0] != B or q.shape[1] < K or q.shape[2] != V:
@@ -245,6 +262,9 @@ def verify_greedy(logits, draft, *, k_per_req=None, l_row_off=None, out: Optiona
         raise SpecError("logits need unit element stride")
     if k_per_req is not None:
         _cuda(k_per_req, "k_per_req", torch.int32)
+    if l_row_off is not None:
+        if k_per_req is None:
+            raise SpecError("l_row_off needs k_per_req")
         _cuda(l_row_off, "l_row_off", torch.int32)
         lbs, lrs = 0, logits.stride(0)
     else:
@@ -355,6 +375,45 @@ def verify_tree(logits, token, parent, num_nodes, max_depth: int, *, out: Option
     return out
 
 
+def verify_tree_sample(logits, token, parent, num_nodes, uniforms, max_depth: int, temperature: float,
+                       top_k: int = 0, *, out: Optional[TreeWalk] = None, ws: Optional[torch.Tensor] = None,
+                       stream=None) -> TreeWalk:
+    """Stochastic tree walk over target logits [B, N, V] (fp32 or bf16):
+    at depth d the current node's token is drawn from its p (temperature,
+    top-k) with uniforms[b, d]; uniforms [B, max_depth+1] fp32."""
+    Lb = _load()
+    _cuda(logits, "logits")
+    ldt = _ldt(logits)
+    for t, n in ((token, "token"), (parent, "parent"), (num_nodes, "num_nodes")):
+        _cuda(t, n, torch.int32)
+        if not t.is_contiguous():
+            raise SpecError(f"{n} must be contiguous")
+    _cuda(uniforms, "uniforms", torch.float32)
+    if logits.dim() != 3 or logits.stride(-1) != 1:
+        raise SpecError("logits must be [B, N, V] with unit element stride")
+    B, N = token.shape
+    V = logits.shape[-1]
+    Ld = int(max_depth)
+    if uniforms.shape != (B, Ld + 1) or not uniforms.is_contiguous():
+        raise SpecError("uniforms must be a contiguous [B, max_depth+1] tensor")
+    dev = logits.device
+    if out is None:
+        out = TreeWalk(torch.empty((B, Ld + 1), dtype=torch.int32, device=dev),
+                       torch.empty((B, Ld + 1), dtype=torch.int32, device=dev),
+                       torch.empty(B, dtype=torch.int32, device=dev),
+                       torch.empty(B, dtype=torch.int32, device=dev), None)
+    need = Lb.spec_verify_tree_sample_workspace_size(B, N, V)
+    if ws is None:
+        ws = workspace(need, dev)
+    out.ws = ws
+    rc = Lb.spec_verify_tree_sample(_p(logits), ldt, logits.stride(0), logits.stride(1), _p(token), _p(parent),
+                                    _p(num_nodes), _p(uniforms), B, N, V, Ld, float(temperature), int(top_k),
+                                    _p(out.path_nodes), _p(out.tokens), _p(out.num_accepted), _p(out.status),
+                                    _p(ws), ws.numel(), _stream(stream))
+    _check(rc, "spec_verify_tree_sample")
+    return out
+
+
 # ---------------------------------------------------------------------------
 # DSpark
 # ---------------------------------------------------------------------------
@@ -367,8 +426,11 @@ class AdaptiveLen:
     q_row_off: torch.Tensor  # [B+1] int32
 
 
-def adaptive_len(conf, a: float, b: float, *, out: Optional[AdaptiveLen] = None, stream=None) -> AdaptiveLen:
-    """DSpark verify length from conditional confidences conf [B, Kmax] fp32."""
+def adaptive_len(conf, a: float, b: float, *, cost=None, out: Optional[AdaptiveLen] = None,
+                 stream=None) -> AdaptiveLen:
+    """DSpark verify length from conditional confidences conf [B, Kmax] fp32;
+    the cost of k positions is a + b*k, or cost[k] with a profiled table
+    (a CUDA float64 tensor of Kmax+1 positive entries)."""
     Lb = _load()
     _cuda(conf, "conf", torch.float32)
     if conf.dim() != 2 or not conf.is_contiguous():
@@ -381,7 +443,15 @@ def adaptive_len(conf, a: float, b: float, *, out: Optional[AdaptiveLen] = None,
                           torch.empty(B, dtype=torch.float64, device=dev),
                           torch.empty(B + 1, dtype=torch.int32, device=dev),
                           torch.empty(B + 1, dtype=torch.int32, device=dev))
-    rc = Lb.spec_adaptive_len(_p(conf), B, Kmax, float(a), float(b), _p(out.k), _p(out.surv), _p(out.exp_adv),
-                              _p(out.l_row_off), _p(out.q_row_off), _stream(stream))
-    _check(rc, "spec_adaptive_len")
+    if cost is None:
+        rc = Lb.spec_adaptive_len(_p(conf), B, Kmax, float(a), float(b), _p(out.k), _p(out.surv), _p(out.exp_adv),
+                                  _p(out.l_row_off), _p(out.q_row_off), _stream(stream))
+        _check(rc, "spec_adaptive_len")
+    else:
+        _cuda(cost, "cost", torch.float64)
+        if cost.shape != (Kmax + 1,) or not cost.is_contiguous():
+            raise SpecError("cost must be a contiguous [Kmax+1] float64 tensor")
+        rc = Lb.spec_adaptive_len_table(_p(conf), B, Kmax, _p(cost), _p(out.k), _p(out.surv), _p(out.exp_adv),
+                                        _p(out.l_row_off), _p(out.q_row_off), _stream(stream))
+        _check(rc, "spec_adaptive_len_table")
     return out

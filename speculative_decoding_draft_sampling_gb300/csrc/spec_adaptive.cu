@@ -13,7 +13,9 @@
 //
 // Arithmetic is fp64 with explicit round-to-nearest intrinsics, so no
 // multiply-add is fused and the sequence of roundings is the plain one:
-// s = s*c_j; E = E + s; ratio = E / (a + b*j).
+// s = s*c_j; E = E + s; ratio = E / (a + b*j).  With a cost table (§9: the
+// per-deployment profile of what verifying k positions costs) the ratio is
+// E / cost[j] instead.
 #include "spec_chain.cuh"
 
 namespace spec {
@@ -21,7 +23,9 @@ namespace spec {
 constexpr int kAdaptThreads = 256;
 
 __global__ void __launch_bounds__(kAdaptThreads) adaptive_kernel(const float* __restrict__ conf, int B, int Kmax,
-                                                                  double a, double bc, int* __restrict__ k_out,
+                                                                  double a, double bc,
+                                                                  const double* __restrict__ cost,
+                                                                  int* __restrict__ k_out,
                                                                   double* __restrict__ surv,
                                                                   double* __restrict__ exp_adv,
                                                                   int* __restrict__ l_off, int* __restrict__ q_off) {
@@ -35,13 +39,14 @@ __global__ void __launch_bounds__(kAdaptThreads) adaptive_kernel(const float* __
         int kbest = 0;
         if (r < B) {
             double s = 1.0, E = 1.0;
-            double best = __ddiv_rn(1.0, __dadd_rn(a, __dmul_rn(bc, 0.0)));
+            double best = __ddiv_rn(1.0, cost ? cost[0] : __dadd_rn(a, __dmul_rn(bc, 0.0)));
             double bestE = 1.0;
             for (int j = 1; j <= Kmax; ++j) {
                 s = __dmul_rn(s, static_cast<double>(conf[static_cast<long long>(r) * Kmax + (j - 1)]));
                 if (surv) surv[static_cast<long long>(r) * Kmax + (j - 1)] = s;
                 E = __dadd_rn(E, s);
-                const double ratio = __ddiv_rn(E, __dadd_rn(a, __dmul_rn(bc, static_cast<double>(j))));
+                const double ratio =
+                    __ddiv_rn(E, cost ? cost[j] : __dadd_rn(a, __dmul_rn(bc, static_cast<double>(j))));
                 if (ratio > best) { best = ratio; kbest = j; bestE = E; }
             }
             k_out[r] = kbest;
@@ -78,9 +83,9 @@ __global__ void __launch_bounds__(kAdaptThreads) adaptive_kernel(const float* __
     }
 }
 
-cudaError_t adaptive_run(const float* conf, int B, int Kmax, float a, float b, int* k_out, double* surv,
-                         double* exp_adv, int* l_off, int* q_off, cudaStream_t st) {
-    adaptive_kernel<<<1, kAdaptThreads, 0, st>>>(conf, B, Kmax, static_cast<double>(a), static_cast<double>(b),
+cudaError_t adaptive_run(const float* conf, int B, int Kmax, float a, float b, const double* cost, int* k_out,
+                         double* surv, double* exp_adv, int* l_off, int* q_off, cudaStream_t st) {
+    adaptive_kernel<<<1, kAdaptThreads, 0, st>>>(conf, B, Kmax, static_cast<double>(a), static_cast<double>(b), cost,
                                                  k_out, surv, exp_adv, l_off, q_off);
     return cudaGetLastError();
 }

@@ -1,4 +1,4 @@
-// spec_chain.cu -- batched chain speculative sampling on the row-task engine.
+// spec_chain.cu -- batched chain speculative sampling on the cluster engine.
 //
 // [SD-survey] = "大模型投机解码：Medusa、MTP、EAGLE、DFlash、DDTree 与 DSpark"
 // (Speculative decoding for LLMs: Medusa, MTP, EAGLE, DFlash, DDTree and
@@ -8,108 +8,91 @@
 // the normalised residual [p_i - q_i]_+; if every draft passes, a bonus token
 // is drawn from p_{K+1}; temperature and top-k truncation are part of p.
 //
-// Tasks of one request, in order:
-//   VERIFY row i   stream logits row i; combine: p_i(y_i), accept test;
-//                  accept -> VERIFY i+1 (or BONUS at i = k); reject -> with
-//                  top-k the correction is drawn in the same combine (the
-//                  residual lives on the top-k set); without top-k -> RESID i
-//   RESID row i    (untruncated p only) stream logits row i and q row i
-//                  together, sum [p - q]_+ per slice, then draw the token
-//   BONUS row k    stream logits row k, draw from p
+// Jobs of one request (every CTA of the cluster streams its vocabulary slice
+// of the row unless a job names one target CTA):
+//   TK row i      top-k rows: every slice's candidates for the row's top-k
+//                 set (behind a certified or hinted value filter); the combine
+//                 selects the set S, forms Z on it and takes the accept test;
+//                 a rejection draws the correction from [p - q]_+ on S (q is
+//                 gathered at S), a bonus row draws from p on S
+//   SE row i      untruncated rows (or a top-k row whose threshold is known
+//                 and whose tied set is too large to list): per slice the max
+//                 and the sum of the weights; the combine takes the accept test
+//   RESID row i   after an SE rejection: per slice the residual mass
+//   RESCAN        one CTA draws inside its slice (the combine found the slice
+//                 whose cumulative mass crosses the target)
+//   RADIX round   an exact radix select of the k-th largest value (4 rounds),
+//                 for top-k rows whose candidates overflowed (massive ties)
 // Rows past the first rejection are never touched.
 #include "spec_chain.cuh"
 #include "spec_select.cuh"
 
 namespace spec {
 
-enum ChainKind : int { kVerify = 0, kBonus = 1, kResid = 2, kInvalid = 3 };
-constexpr int kKindMask = 7;
-constexpr int kNoHint = 8;        // kind bit: stream the row without a filter hint (a retry)
+enum ChainKind : int { kTk = 0, kSe = 1, kResid = 2, kRescan = 3, kRadix = 4 };
+// Job fields per kind:
+//   row            the row (draft position; K or k_b is the bonus row)
+//   aux            TK/SE/RADIX: 1 when the row is the bonus row
+//   hint           TK: filter hint (value key, 0 = none); SE/RESID/RESCAN: mask
+//                  value key (0 = none); RADIX: the prefix found so far
+//   aux2           RADIX: round (low byte) and the rank still sought (>> 8);
+//                  RESCAN: weight mode (0: p weights, 1: [p - q]_+)
+//   f[0..3]        RESID: m, 1/Z; RESCAN: m, 1/Z, target t (float-float)
 
-// Combiner scratch: the gathered candidate keys, then the top-k set sorted by
-// token (ids and fp64 weights; a larger tied set takes the exact fallback).
+// Combiner scratch: the gathered candidate keys, then the top-k set sorted
+// by token (ids and float-float weights).
 constexpr int kCombKeys = 2048;
 constexpr int kCombSet = 512;
-// A top-k combine as the combiner warp prepared it for the consumers: the
-// gathered keys are in CombSmem::list.
-struct CombPrep {
-    int b, row, kind, st;
-    int n;            // gathered keys
-    int y;            // drafted token (VERIFY)
-    int fallback;     // 1: a slice overflowed; take the exact path
-    int hinted;       // a slice streamed behind a hint
-    int sl;           // slice length of the row
-    uint32_t done;    // finished requests when the row arrived (an estimate, for the next row's slicing)
-    uint32_t base;    // arrival base of the request's next task
-    float vmax;
-    float pad;
-    uint64_t theta;   // largest slice filter
-    float uk, ur;     // uniforms: sample, accept
-    // an untruncated draw: rescan slice [x0, x1) for the CDF crossing t
-    int x0, x1, wmode;  // wmode 0: p weights 2^((l-m)c); 1: [p - q]_+
-    float m, invZf;
-    dfloat t;
-    double Z, R;        // diagnostics
-};
-// Written by the combiner warp while the consumers stream; the consumers'
-// own scratch for a combine lives in TopkSmem (free at unit boundaries,
-// where they serve combines): select ranks in `slot`, the selected keys in
-// the first kCombOut entries of `cand`, tokens and weights after them.
-struct CombSmem {
-    SliceHdrs hdrs;
-    CombPrep prep;
-    alignas(16) uint64_t list[kCombKeys];
-};
-constexpr int kCombOut = 1024;   // select output (> kCombSet: a larger set takes the exact path)
-static_assert(sizeof(uint64_t) * TopkSmem::kSlots * kThreads >= sizeof(int) * kCombKeys, "ranks fit in slot");
-static_assert(sizeof(uint64_t) * (kCombOut) + (sizeof(int) + sizeof(float2)) * kCombSet <=
-                  sizeof(uint64_t) * kWarps * TopkSmem::kRegion,
-              "selected keys, tokens and weights fit in cand");
 
-template <bool kTopk> struct ChainTopkPart {};
-template <> struct ChainTopkPart<true> { TopkSmem tk; };
-
-template <bool kTopk>
-struct __align__(16) ChainSmem : ChainTopkPart<kTopk> {
-    PipeSmem pipe;
-    CombSmem comb;
-    uint64_t sh64[4];
-    int ish[4];
+struct ChainSmem {
+    TopkSmem tk;                      // consumers: slice candidates (top-k rows)
+    alignas(16) uint64_t list[kCombKeys];   // combiner: gathered keys
+    int stok[kCombSet];               // combiner: S by token
+    float sval[kCombSet];             // combiner: S's logits by token
+    float2 swt[kCombSet];             // combiner: weights by token
+    int bins[256];                    // consumers: radix histogram
     float2 red2[kWarps];
     int ired[kWarps + 4];
     int hist[64];
     uint32_t scratch[kWarps + 2];
-    float fsh[8];
-    float wm[kWarps];        // per-warp partials of the one-barrier finishes
-    float2 ws[kWarps];       // float-float
+    uint64_t sh64[4];
+    float wm[kWarps];
+    float2 ws[kWarps];
     float2 ws2[kWarps];
     uint32_t wb[kWarps];
+    float fsh[4];
+    uint32_t last_hint;               // combiner: filter hint from this CTA's latest top-k row
+    uint32_t tag;                     // consumers: unit tag for the shared filter
 };
 
 __device__ __forceinline__ int chain_k(const ChainArgs& A, int b) {
     return A.k_per_req ? A.k_per_req[b] : A.K;
 }
+// the uniform that drives a row's draw: u[b, k_b] (chain), u[b, depth] (tree)
+__device__ __forceinline__ int draw_uidx(const ChainArgs& A, const Job& j) {
+    return A.tree ? j.depth : chain_k(A, j.b);
+}
 template <class E>
 __device__ __forceinline__ const void* chain_lrow(const ChainArgs& A, int b, int i) {
-    const long long r = A.k_per_req ? static_cast<long long>(A.l_row_off[b] + i) * A.l_rs
-                                    : static_cast<long long>(b) * A.l_bs + static_cast<long long>(i) * A.l_rs;
+    const long long r = A.k_per_req && A.l_row_off ? static_cast<long long>(A.l_row_off[b] + i) * A.l_rs
+                                                   : static_cast<long long>(b) * A.l_bs + static_cast<long long>(i) * A.l_rs;
     return static_cast<const unsigned char*>(A.logits) + r * E::kBytes;
 }
 __device__ __forceinline__ const float* chain_qrow(const ChainArgs& A, int b, int i) {
-    const long long r = A.k_per_req ? static_cast<long long>(A.q_row_off[b] + i) * A.q_rs
-                                    : static_cast<long long>(b) * A.q_bs + static_cast<long long>(i) * A.q_rs;
+    const long long r = A.k_per_req && A.q_row_off ? static_cast<long long>(A.q_row_off[b] + i) * A.q_rs
+                                                   : static_cast<long long>(b) * A.q_bs + static_cast<long long>(i) * A.q_rs;
     return A.q + r;
 }
 __device__ __forceinline__ float chain_u(const ChainArgs& A, int b, int i) {
-    return A.uniforms[static_cast<long long>(b) * (A.K + 1) + i];
+    return A.uniforms[static_cast<long long>(b) * ((A.tree ? A.L : A.K) + 1) + i];
 }
 
 // ---------------------------------------------------------------------------
-// combiner-warp steps (all 32 lanes unless stated)
+// combiner-warp steps (all 32 lanes)
 // ---------------------------------------------------------------------------
 // Commit the request: accepted drafts, then `last` (correction/bonus, or -1),
-// then -1 padding; lane 0 publishes completion.
-__device__ void chain_finish(const ChainArgs& A, int b, int n, int last, int st) {
+// then -1 padding.
+__device__ Job chain_finish(const ChainArgs& A, int b, int n, int last, int st) {
     const int W = A.K + 1;
     int* out = A.out_tokens + static_cast<long long>(b) * W;
     for (int i = threadIdx.x & 31; i < W; i += 32) {
@@ -123,52 +106,72 @@ __device__ void chain_finish(const ChainArgs& A, int b, int n, int last, int st)
         A.status[b] = st;
     }
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) finish_request(A.W);
+    return job_done();
 }
 
-// The same on every consumer thread (a combine the consumers run).
-__device__ void chain_finish_cta(const ChainArgs& A, int b, int n, int last, int st) {
-    const int W = A.K + 1;
-    int* out = A.out_tokens + static_cast<long long>(b) * W;
-    for (int i = threadIdx.x; i < W; i += kThreads) {
-        int v = -1;
-        if (i < n) v = A.draft[static_cast<long long>(b) * A.K + i];
-        else if (i == n) v = last;
-        out[i] = v;
+// The stochastic tree walk's outputs: path_nodes[b][1..depth] and
+// out_tokens[b][0..depth-1] were written on the way.
+__device__ Job tree_done(const ChainArgs& A, int b, int depth, int last, int st) {
+    const int W = A.L + 1;
+    const int l = threadIdx.x & 31;
+    int* pn = A.path_nodes + static_cast<long long>(b) * W;
+    int* ot = A.out_tokens + static_cast<long long>(b) * W;
+    for (int i = l; i < W; i += 32) {
+        if (i > depth) { pn[i] = -1; ot[i] = -1; }
+        if (i == depth) ot[i] = last;
     }
-    if (threadIdx.x == 0) {
-        A.num_accepted[b] = n;
+    if (l == 0) {
+        pn[0] = 0;
+        A.num_accepted[b] = depth;
         A.status[b] = st;
     }
-    csync();
-    if (threadIdx.x == 0) finish_request(A.W);
+    __syncwarp();
+    return job_done();
+}
+
+// The request ends at the job's row with `last` committed (or -1).
+__device__ __forceinline__ Job finish_at(const ChainArgs& A, const Job& j, int last, int st) {
+    return A.tree ? tree_done(A, j.b, j.depth, last, st) : chain_finish(A, j.b, j.row, last, st);
 }
 
 __device__ __forceinline__ void chain_diag(const ChainArgs& A, int b, int i, float py, float qy, float Z, float R) {
-    if (!A.diag) return;
+    if (!A.diag || (threadIdx.x & 31) != 0) return;
     float* d = A.diag + (static_cast<long long>(b) * (A.K + 1) + i) * 4;
     d[0] = py; d[1] = qy; d[2] = Z; d[3] = R;
 }
+__device__ __forceinline__ void chain_diag_R(const ChainArgs& A, int b, int i, float R) {
+    if (!A.diag || (threadIdx.x & 31) != 0) return;
+    A.diag[(static_cast<long long>(b) * (A.K + 1) + i) * 4 + 3] = R;
+}
 
-// lane 0: push the request's next task after an accepted position (the
-// record carries all the task needs: no release)
-__device__ void chain_advance(const ChainArgs& A, int b, int row, int kb, int st, uint32_t hint, uint32_t done,
-                              uint32_t base) {
-    Task t;
-    t.b = b;
-    t.row = row + 1;
-    t.kind = (row + 1 < kb) ? kVerify : kBonus;
-    t.aux = static_cast<int>(hint);
-    t.st = st;
-    t.base = base;
-    int S, SL;
-    pick_slices(A.B, A.V, A.S, A.S1, done, S, SL);
-    push_task(A.W, t, S, SL, false);
+// The job that reads row `row` of request b (a bonus row when row == k_b;
+// in a tree walk every row is drawn from).
+__device__ __forceinline__ Job row_job(const ChainArgs& A, int b, int row, int st, uint32_t hint, int depth = 0) {
+    Job j = make_job(b, row, A.top_k > 0 ? kTk : kSe, st);
+    j.aux = (A.tree || row >= chain_k(A, b)) ? 1 : 0;
+    j.hint = A.top_k > 0 ? hint : 0u;
+    j.depth = depth;
+    return j;
+}
+
+// A row's draw x is known: the chain commits it; the tree walk looks it up
+// among the node's children and goes on there, or commits it as the bonus.
+__device__ Job draw_done(const ChainArgs& A, const Job& j, int x, int st, uint32_t hint) {
+    if (!A.tree) return chain_finish(A, j.b, j.row, x, st);
+    const int child = x >= 0 ? find_child_w(A.t_token, A.t_parent, A.t_nn, A.N, j.b, j.row, x) : -1;
+    if (child < 0 || j.depth >= A.L) return tree_done(A, j.b, j.depth, x, st);
+    if ((threadIdx.x & 31) == 0) {
+        const int W = A.L + 1;
+        A.out_tokens[static_cast<long long>(j.b) * W + j.depth] = x;
+        A.path_nodes[static_cast<long long>(j.b) * W + j.depth + 1] = child;
+    }
+    __syncwarp();
+    return row_job(A, j.b, child, st, hint, j.depth + 1);
 }
 
 // Acceptance of drafted y: u < p(y)/q(y).  With weights scaled by the
 // normaliser, p(y) = e_y / Z, the test is e_y > u q Z (float-float; no
-// division on this path).  A ratio within rounding of u is a near tie.
+// division on this path).
 __device__ __forceinline__ bool chain_accept_z(const ChainArgs& A, int y, float ey, float qy, dfloat Z, float u,
                                                int& st) {
     if (y < 0 || y >= A.V) {
@@ -210,312 +213,17 @@ __device__ int warp_icdf_pairs(const int* tok, const float2* w, int n, dfloat t)
 }
 
 // Filter hint for the next row from this row's top-k threshold tau and max
-// m: 0.15 of the gap below tau (rows of one target differ little in tau; a
-// hint above the next row's tau only costs a re-read of that row).
+// m: `margin` of the gap below tau (rows of one target differ little in tau;
+// a hint above the next row's tau costs a re-read of that row, one far below
+// it extra candidates).
 #ifndef SPEC_HINT_MARGIN
 #define SPEC_HINT_MARGIN 0.15f
 #endif
-__device__ __forceinline__ uint32_t next_hint(float tau, float m) {
-    const float h = tau - SPEC_HINT_MARGIN * (m - tau);
+__device__ __forceinline__ uint32_t hint_from(float tau, float m, float margin) {
+    const float h = tau - margin * (m - tau);
     return (h == h && h > -kInf) ? fkey(h) : 0u;
 }
 
-// ---------------------------------------------------------------------------
-// combine with top-k: the candidate lists of all slices hold S exactly
-// ---------------------------------------------------------------------------
-// Combiner warp, last arrival of a top-k row: everything that waits on
-// global memory -- the slice headers, the drafted token, the uniforms, every
-// slice key -- into shared memory for the consumers.  Returns false when the
-// combine ended here (a bad row).
-template <class E>
-__device__ bool prepare_topk(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st, int S, int SL,
-                             uint32_t done, uint32_t base) {
-    const int l = threadIdx.x & 31;
-    const int kb = chain_k(A, b);
-    const float uk = chain_u(A, b, kb);
-    const float ur = kind == kVerify ? chain_u(A, b, row) : 0.f;
-    const int y = kind == kVerify ? A.draft[static_cast<long long>(b) * A.K + row] : -1;
-    SliceHdrs& H = cs.hdrs;
-    const int pre = load_hdrs_w(A.W, b, S, H, cs.list, kCombKeys);   // headers and each slice's first keys
-    SPEC_TRACE_EVW(5, b, row, S, kind);
-    uint32_t flags = 0;
-    float vmax = -kInf;
-    uint64_t theta = 0;
-    if (l < S) { flags = H.flags[l]; vmax = H.vmax[l]; theta = H.kth[l]; }
-    flags = __reduce_or_sync(0xffffffffu, flags);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        vmax = max_nan(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
-        const uint64_t t2 = __shfl_xor_sync(0xffffffffu, theta, o);
-        theta = t2 > theta ? t2 : theta;
-    }
-    if ((flags & kPfBad) || !(vmax > -kInf)) {
-        chain_finish(A, b, row, -1, st | 1);
-        return false;
-    }
-    int n = 0, fb = (flags & kPfOverflow) ? 1 : 0;
-    if (!fb) {
-        bool oflow;
-        n = gather_all_w(A.W, b, S, H, cs.list, kCombKeys, oflow, pre);
-        if (oflow) fb = 1;
-    }
-    SPEC_TRACE_EVW(6, b, row, n, kind);
-    if (l == 0) {
-        CombPrep& p = cs.prep;
-        p.b = b; p.row = row; p.kind = kind; p.st = st; p.n = n; p.y = y; p.fallback = fb;
-        p.sl = SL;
-        p.done = done;
-        p.base = base;
-        p.hinted = (flags & kPfHinted) ? 1 : 0;
-        p.vmax = vmax; p.theta = theta; p.uk = uk; p.ur = ur;
-    }
-    return true;
-}
-
-template <class E>
-__device__ void chain_fallback_cta(const ChainArgs& A, ChainSmem<true>& sh, int b, int row, int kind,
-                                   int st, float vmax);
-
-// Consumers: the compute of a prepared top-k combine.  The set S of the
-// row's k largest values (ties kept) from the gathered keys, its normaliser
-// Z, then the accept test at the drafted token, or a draw from the residual
-// [p - q]_+ on S (rejection) or from p (bonus row).
-template <class E>
-__device__ void combine_topk_cta(const ChainArgs& A, ChainSmem<true>& sh) {
-    CombSmem& cs = sh.comb;
-    const CombPrep p = cs.prep;
-    const int b = p.b, row = p.row, kind = p.kind, k = A.top_k;
-    int st = p.st;
-    SPEC_TRACE_EV(20, b, row, 0, kind);
-    const int kb = chain_k(A, b);
-    if (p.fallback) {
-        chain_fallback_cta<E>(A, sh, b, row, kind, st, p.vmax);
-        return;
-    }
-    uint64_t* list = cs.list;
-    const uint32_t th = hkey(p.theta);
-    // keys at or above the largest slice filter: enough for the k-th?
-    int n = compact_list(list, p.n, th, sh.ired);
-    if (n < k) {
-        if (p.hinted) {
-            // the hint was above the row's k-th value: stream the row again without it
-            if (threadIdx.x == 0) {
-                Task t;
-                t.b = b; t.row = row; t.kind = kind | kNoHint; t.aux = 0; t.st = st; t.base = p.base;
-                int S, SL;
-                pick_slices(A.B, A.V, A.S, A.S1, p.done, S, SL);
-                push_task(A.W, t, S, SL, false);
-            }
-            return;
-        }
-        chain_fallback_cta<E>(A, sh, b, row, kind, st, p.vmax);
-        return;
-    }
-    uint64_t kth;
-    bool of = false;
-    uint64_t* cand = sh.tk.cand;
-    int* ctok = reinterpret_cast<int*>(cand + kCombOut);
-    float2* cwgt = reinterpret_cast<float2*>(ctok + kCombSet);
-    const int keep = select_to(list, n, k, true, reinterpret_cast<int*>(&sh.tk.slot[0][0]), cand, kCombOut, kth, of,
-                               sh.sh64, sh.ired);
-    SPEC_TRACE_EV(7, b, row, n, kind);
-    if (of || keep > kCombSet) {
-        chain_fallback_cta<E>(A, sh, b, row, kind, st, p.vmax);
-        return;
-    }
-    // S = cand[0 .. keep): values >= tau, sorted by value descending
-    const uint32_t tau_key = hkey(cand[keep - 1]);
-    const float tau = ckey_val(cand[keep - 1]);
-    // weights e_x = 2^((l_x - m) c) and Z = sum over S in float-float; p(x) =
-    // e_x / Z is never formed on this path (tests compare Z-scaled masses)
-    // Each thread holds up to kPer members of S: token, weight, and (VERIFY)
-    // q at the token, loaded now so that a rejection finds it in registers.
-    constexpr int kPer = kCombSet / kThreads;
-    const float m = p.vmax, c2 = A.c2;
-    const float* qrow = kind == kVerify ? chain_qrow(A, b, row) : nullptr;
-    int xs[kPer];
-    float ev[kPer], qv[kPer];
-    dfloat zpart = df_make(0.f);
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int i = threadIdx.x + j * kThreads;
-        xs[j] = -1; ev[j] = 0.f; qv[j] = 0.f;
-        if (i < keep) {
-            xs[j] = ckey_idx(cand[i]);
-            ev[j] = ex2((ckey_val(cand[i]) - m) * c2);
-            zpart = df_add(zpart, ev[j]);
-            if (qrow && xs[j] >= 0 && xs[j] < A.V) qv[j] = __ldcg(qrow + xs[j]);   // keys hold in-range ids
-        }
-    }
-    const dfloat Z = block_sum_df(zpart, sh.red2);
-    const float Zf = Z.hi;
-    auto prob = [&](float e) { return static_cast<float>(static_cast<double>(e) / df_to_d(Z)); };   // diagnostics
-    const uint32_t hint = next_hint(tau, m);
-    SPEC_TRACE_EV(8, b, row, keep, kind);
-    if (threadIdx.x == 0) {
-        __stcg(&A.W.ctrl->hint0, hint);
-        // for the next call's first rows: a wider margin (another call's rows
-        // may sit lower)
-        const float hw = tau - 0.5f * (m - tau);
-        __stcg(&A.W.persist[1], (hw == hw && hw > -kInf) ? fkey(hw) : 0u);
-        __stcg(&A.W.persist[2], static_cast<uint32_t>(A.V));
-        __stcg(&A.W.persist[3], static_cast<uint32_t>(A.top_k));
-        __stcg(&A.W.persist[0], kPersistTag);
-    }
-
-    // Z-scaled weights of S sorted by token id (ascending): e_x, or for the
-    // residual Z [p - q]_+ = [e_x - q_x Z]_+
-    int rk[kPer];
-    bool ranked = false;
-    auto sort_by_token = [&](bool residual, dfloat& total) {
-        if (!ranked) {
-#pragma unroll
-            for (int j = 0; j < kPer; ++j) {
-                rk[j] = 0;
-                if (threadIdx.x + j * kThreads < keep)
-                    for (int t = 0; t < keep; ++t) rk[j] += ckey_idx(cand[t]) < xs[j];   // ids in S are distinct
-            }
-            ranked = true;
-        }
-        dfloat part = df_make(0.f);
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            if (threadIdx.x + j * kThreads >= keep) continue;
-            dfloat w = df_make(ev[j]);
-            if (residual) {
-                const dfloat d = df_add(w, df_neg(df_mul(qv[j], Z)));
-                w = d.hi > 0.f ? d : df_make(0.f);
-            }
-            ctok[rk[j]] = xs[j];
-            cwgt[rk[j]] = make_float2(w.hi, w.lo);
-            part = df_add(part, w);
-        }
-        total = block_sum_df(part, sh.red2);
-    };
-
-    if (kind == kVerify) {
-        const int y = p.y;
-        float ey = 0.f, qy = 0.f;
-        if (y >= 0 && y < A.V) {
-            const int sy = y / p.sl;
-            const float ly = cs.hdrs.ly[sy];
-            qy = cs.hdrs.qy[sy];
-            if (fkey(ly) >= tau_key) ey = ex2((ly - m) * c2);
-        }
-        const bool acc = chain_accept_z(A, y, ey, qy, Z, p.ur, st);
-        if (acc) {
-            if (threadIdx.x == 0) {
-                if (A.diag) chain_diag(A, b, row, prob(ey), qy, Zf, 0.f);
-                chain_advance(A, b, row, kb, st, hint, p.done, p.base);
-            }
-            SPEC_TRACE_EV(9, b, row, 1, kind);
-            return;
-        }
-        // residual [p - q]_+ lives on S (p = 0 outside it)
-        dfloat R_mass;
-        sort_by_token(true, R_mass);
-        if (!(R_mass.hi > 0.f)) {
-            st |= 4;
-            sort_by_token(false, R_mass);
-        }
-        int x = -1;
-        if (threadIdx.x < 32)
-            x = warp_icdf_pairs(ctok, cwgt, keep, df_mul(p.uk, R_mass));
-        if (threadIdx.x == 0) {
-            sh.ish[0] = x;
-            if (A.diag) chain_diag(A, b, row, prob(ey), qy, Zf, (st & 4) ? 0.f : static_cast<float>(df_to_d(R_mass) / df_to_d(Z)));
-        }
-        csync();
-        SPEC_TRACE_EV(11, b, row, 0, kind);
-        chain_finish_cta(A, b, row, sh.ish[0], st);
-        SPEC_TRACE_EV(9, b, row, 0, kind);
-        return;
-    }
-    // bonus row: draw from p
-    dfloat tot;
-    sort_by_token(false, tot);
-    int x = -1;
-    if (threadIdx.x < 32) x = warp_icdf_pairs(ctok, cwgt, keep, df_mul(p.uk, tot));
-    if (threadIdx.x == 0) sh.ish[0] = x;
-    csync();
-    x = sh.ish[0];
-    if (threadIdx.x == 0 && A.diag && x >= 0 && x < A.V)
-        chain_diag(A, b, row, prob(ex2((E::load(chain_lrow<E>(A, b, row), x) - m) * c2)), 0.f, Zf, 0.f);
-    chain_finish_cta(A, b, row, x, st);
-}
-
-// Exact path for rows whose top-k set did not fit the candidate buffers
-// (massive ties, adversarial order), on the consumers: tau by bisection over
-// order-preserving keys, then full-row passes.  Slow; correctness only.
-template <class E>
-__device__ void chain_fallback_cta(const ChainArgs& A, ChainSmem<true>& sh, int b, int row, int kind,
-                                   int st, float vmax) {
-    const void* lrow = chain_lrow<E>(A, b, row);
-    const int V = A.V, k = A.top_k;
-    // largest key t with #{x : key(l_x) >= t} >= k
-    // invariant: count(lo) >= k (count(0) = V > k); the range halves every
-    // step (64-bit midpoint: hi - lo + 1 can be 2^32), so 32 steps suffice
-    uint32_t lo = 0, hi = 0xffffffffu;
-    for (int it = 0; it < 33 && lo < hi; ++it) {
-        const uint32_t mid = lo + static_cast<uint32_t>((static_cast<uint64_t>(hi) - lo + 1) >> 1);
-        int c = 0;
-        for (int x = threadIdx.x; x < V; x += kThreads) c += fkey(E::load(lrow, x)) >= mid;
-        c = block_sum_i(c, sh.ired);
-        if (c >= k) lo = mid; else hi = mid - 1;
-    }
-    const uint32_t tau = lo;
-    const float m = vmax, c2 = A.c2;
-    auto wp = [&](int x) -> float {
-        const float v = E::load(lrow, x);
-        return fkey(v) >= tau ? ex2((v - m) * c2) : 0.f;
-    };
-    // Z-scaled weights, as in the candidate-set combine
-    const dfloat Z = cta_sum(0, V, wp, sh.red2);
-    const double Zd = df_to_d(Z);
-    const int kb = chain_k(A, b);
-    const float uk = chain_u(A, b, kb);
-    if (kind == kVerify) {
-        const int y = A.draft[static_cast<long long>(b) * A.K + row];
-        float ey = 0.f, qy = 0.f;
-        if (y >= 0 && y < V) {
-            ey = wp(y);
-            qy = chain_qrow(A, b, row)[y];
-        }
-        auto py = [&]() { return static_cast<float>(static_cast<double>(ey) / Zd); };   // diagnostics
-        if (chain_accept_z(A, y, ey, qy, Z, chain_u(A, b, row), st)) {
-            if (threadIdx.x == 0) {
-                if (A.diag) chain_diag(A, b, row, py(), qy, Z.hi, 0.f);
-                chain_advance(A, b, row, kb, st, 0u, sh.comb.prep.done, sh.comb.prep.base);
-            }
-            return;
-        }
-        const float* qrow = chain_qrow(A, b, row);
-        auto wr = [&](int x) -> float {   // Z [p - q]_+
-            const dfloat d = df_add(df_make(wp(x)), df_neg(df_mul(qrow[x], Z)));
-            return d.hi > 0.f ? d.hi : 0.f;
-        };
-        const dfloat R_mass = cta_sum(0, V, wr, sh.red2);
-        int x;
-        if (R_mass.hi > 0.f) {
-            x = cta_icdf(0, V, df_mul(uk, R_mass), wr, sh.red2, sh.ired);
-        } else {
-            st |= 4;
-            x = cta_icdf(0, V, df_mul(uk, Z), wp, sh.red2, sh.ired);
-        }
-        if (threadIdx.x == 0 && A.diag)
-            chain_diag(A, b, row, py(), qy, Z.hi, (st & 4) ? 0.f : static_cast<float>(df_to_d(R_mass) / Zd));
-        chain_finish_cta(A, b, row, x, st);
-        return;
-    }
-    const int x = cta_icdf(0, V, df_mul(uk, Z), wp, sh.red2, sh.ired);
-    if (threadIdx.x == 0 && A.diag && x >= 0 && x < V)
-        chain_diag(A, b, row, static_cast<float>(static_cast<double>(wp(x)) / Zd), 0.f, Z.hi, 0.f);
-    chain_finish_cta(A, b, row, x, st);
-}
-
-// ---------------------------------------------------------------------------
-// combine without truncation: per-slice (max, sum of 2^((l-m_s)c))
-// ---------------------------------------------------------------------------
 // the slice whose running prefix of v (lane s holds slice s's value) crosses
 // t, and the prefix before it (float-float)
 __device__ __forceinline__ int find_slice_w(int S, dfloat v, dfloat t, dfloat& before) {
@@ -535,418 +243,613 @@ __device__ __forceinline__ int find_slice_w(int S, dfloat v, dfloat t, dfloat& b
     before.lo = __shfl_sync(0xffffffffu, ex.lo, pick);
     return pick;
 }
-
 __device__ __forceinline__ dfloat df_of(float2 v) { return dfloat{v.x, v.y}; }
 
-// Combiner warp: the combine of an untruncated row.  Returns true when a draw
-// needs a slice rescan, prepared in cs.prep for the consumers.  Slice sums
-// are Z-scaled (weights e_x = 2^((l_x - m) c)), float-float across slices.
-template <class E>
-__device__ bool combine_full(const ChainArgs& A, CombSmem& cs, int b, int row, int kind, int st, int S, int SL,
-                             uint32_t done, uint32_t base) {
+// the drafted token's logit and q, from the slice that holds it
+__device__ __forceinline__ void slice_y(const unsigned char* parts, int pb, int C, float& ly, float& qy) {
     const int l = threadIdx.x & 31;
-    const int kb = chain_k(A, b);
-    const float c2 = A.c2;
-    const float uk = chain_u(A, b, kb);
-    const float ur = kind == kVerify ? chain_u(A, b, row) : 0.f;
-    const int y = kind == kVerify ? A.draft[static_cast<long long>(b) * A.K + row] : -1;
-    SliceHdrs& H = cs.hdrs;
-    load_hdrs_w(A.W, b, S, H);
-    SPEC_TRACE_EVW(5, b, row, S, kind);
-    if (kind == kResid) {
-        const ReqState* rs = &A.W.req[b];
-        const dfloat rv = l < S ? df_of(H.sum[l]) : df_make(0.f);
-        const dfloat pv = l < S ? df_of(H.sum2[l]) : df_make(0.f);
-        const dfloat R_mass = warp_sum_df(rv);
-        const dfloat P_mass = warp_sum_df(pv);
-        dfloat before, t;
-        int s, wmode;
-        if (R_mass.hi > 0.f) {
-            t = df_mul(uk, R_mass);
-            s = find_slice_w(S, rv, t, before);
-            wmode = 1;
-        } else {
-            st |= 4;
-            t = df_mul(uk, P_mass);
-            s = find_slice_w(S, pv, t, before);
-            wmode = 0;
-        }
-        if (l == 0) {
-            CombPrep& p = cs.prep;
-            p.b = b; p.row = row; p.kind = kind; p.st = st;
-            p.x0 = s * SL; p.x1 = min(A.V, p.x0 + SL); p.wmode = wmode;
-            p.m = __ldcg(&rs->m); p.invZf = __ldcg(&rs->invZ);
-            p.t = df_add(t, df_neg(before));
-            p.Z = 0.0;
-            p.R = df_to_d(R_mass);
-        }
-        return true;   // the consumers rescan the slice
+    uint32_t has = 0;
+    float a = 0.f, q = 0.f;
+    if (l < C) {
+        const PartHdr* h = part_at(parts, pb, l);
+        has = h->hasy;
+        a = h->ly;
+        q = h->qy;
     }
-    // VERIFY or BONUS: max and normaliser from the slice partials
-    uint32_t flags = l < S ? H.flags[l] : 0u;
-    float vmax = l < S ? H.vmax[l] : -kInf;
+    const uint32_t bal = __ballot_sync(0xffffffffu, has != 0);
+    const int src = bal ? __ffs(bal) - 1 : 0;
+    ly = __shfl_sync(0xffffffffu, a, src);
+    qy = __shfl_sync(0xffffffffu, q, src);
+    if (!bal) { ly = -kInf; qy = 0.f; }
+}
+
+// ---------------------------------------------------------------------------
+// combine of a top-k row: the candidate lists of all slices hold S exactly
+// ---------------------------------------------------------------------------
+template <class E>
+__device__ Job combine_topk(const ChainArgs& A, const Geo& G, const Job& job, const unsigned char* parts,
+                            ChainSmem& sm) {
+    const int l = threadIdx.x & 31;
+    const int C = G.C, pb = G.part_bytes;
+    const int b = job.b, row = job.row, k = A.top_k;
+    const bool bonus = job.aux != 0;
+    int st = job.st;
+    const int kb = chain_k(A, b);
+    uint32_t flags = 0;
+    float vmax = -kInf;
+    uint64_t theta = 0;
+    int cnt = 0;
+    if (l < C) {
+        const PartHdr* h = part_at(parts, pb, l);
+        flags = h->flags; vmax = h->vmax; theta = h->kth; cnt = h->cnt;
+    }
     flags = __reduce_or_sync(0xffffffffu, flags);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) vmax = max_nan(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
-    if ((flags & kPfBad) || !(vmax > -kInf)) {
-        chain_finish(A, b, row, -1, st | 1);
-        return false;
+    for (int o = 16; o > 0; o >>= 1) {
+        vmax = max_nan(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+        const uint64_t t2 = __shfl_xor_sync(0xffffffffu, theta, o);
+        theta = t2 > theta ? t2 : theta;
     }
-    const float m = vmax;
-    dfloat zv = df_make(0.f);
-    if (l < S && H.sum[l].x > 0.f) zv = df_mul(ex2((H.vmax[l] - m) * c2), df_of(H.sum[l]));
-    const dfloat Z = warp_sum_df(zv);
-    if (kind == kVerify) {
-        float ey = 0.f, qy = 0.f;
-        if (y >= 0 && y < A.V) {
-            const int sy = y / SL;
-            ey = ex2((H.ly[sy] - m) * c2);
-            qy = H.qy[sy];
+    if ((flags & kPfBad) || !(vmax > -kInf)) return finish_at(A, job, -1, st | 1);
+    if (flags & kPfOverflow) {
+        // massive ties: the exact k-th value by radix select
+        Job j = make_job(b, row, kRadix, st);
+        j.aux = bonus ? 1 : 0;
+        j.aux2 = (k << 8);
+        j.depth = job.depth;
+        return j;
+    }
+    // every key at or above the largest slice filter (the others can not be in S)
+    const uint32_t th = hkey(theta);
+    int n = 0;
+    const uint32_t lt = (1u << l) - 1u;
+    for (int r = 0; r < C; ++r) {
+        const int cr = __shfl_sync(0xffffffffu, cnt, r);
+        const uint64_t* keys = reinterpret_cast<const uint64_t*>(part_at(parts, pb, r) + 1);
+        for (int i0 = 0; i0 < cr; i0 += 32) {
+            const int i = i0 + l;
+            uint64_t key = 0;
+            bool p = false;
+            if (i < cr) { key = keys[i]; p = hkey(key) >= th; }
+            const uint32_t bal = __ballot_sync(0xffffffffu, p);
+            if (p) {
+                const int pos = n + __popc(bal & lt);
+                if (pos < kCombKeys) sm.list[pos] = key;
+            }
+            n += __popc(bal);
         }
-        const bool acc = chain_accept_z(A, y, ey, qy, Z, ur, st);
-        if (l == 0 && A.diag) chain_diag(A, b, row, static_cast<float>(static_cast<double>(ey) / df_to_d(Z)), qy, Z.hi, 0.f);
+    }
+    __syncwarp();
+    if (n < k) {
+        // a hinted slice filter sat above the row's k-th value: stream the row
+        // again without a hint (certified filters always leave k keys; without
+        // a hint this is unreachable, and the radix path decides)
+        if (job.hint != 0u) return row_job(A, b, row, st, 0u, job.depth);
+        Job j = make_job(b, row, kRadix, st);
+        j.aux = bonus ? 1 : 0;
+        j.aux2 = (k << 8);
+        j.depth = job.depth;
+        return j;
+    }
+    if (n > kCombKeys) {
+        Job j = make_job(b, row, kRadix, st);
+        j.aux = bonus ? 1 : 0;
+        j.aux2 = (k << 8);
+        j.depth = job.depth;
+        return j;
+    }
+    const uint32_t tau_key = kth_value_w(sm.list, n, k);
+    const int keep = compact_w(sm.list, n, tau_key);
+    const float m = vmax, c2 = A.c2;
+    const float tau = fkey_inv(tau_key);
+    if (keep > kCombSet) {
+        // a large tied set: the masked full-row passes, with the threshold known
+        Job j = make_job(b, row, kSe, st);
+        j.aux = bonus ? 1 : 0;
+        j.hint = tau_key;
+        j.depth = job.depth;
+        return j;
+    }
+    // S sorted by token id (ids in S are distinct): rank by counting
+    for (int i = l; i < keep; i += 32) {
+        const uint64_t key = sm.list[i];
+        const int x = ckey_idx(key);
+        int r = 0;
+        for (int t = 0; t < keep; ++t) r += ckey_idx(sm.list[t]) < x;
+        sm.stok[r] = x;
+        sm.sval[r] = ckey_val(key);
+    }
+    __syncwarp();
+    // weights e_x = 2^((l_x - m) c) and Z = sum over S (float-float)
+    dfloat zp = df_make(0.f);
+    for (int i = l; i < keep; i += 32) {
+        const float e = ex2((sm.sval[i] - m) * c2);
+        sm.swt[i] = make_float2(e, 0.f);
+        zp = df_add(zp, e);
+    }
+    const dfloat Z = warp_sum_df(zp);
+    __syncwarp();
+    // the next rows' filter hint (and, persisted, the next call's)
+    const uint32_t hint = hint_from(tau, m, SPEC_HINT_MARGIN);
+    if (l == 0) {
+        sm.last_hint = hint;
+        const uint32_t hw = hint_from(tau, m, 0.5f);
+        volatile uint32_t* ps = A.E.W.ctrl->persist;
+        ps[1] = hw; ps[2] = static_cast<uint32_t>(A.V); ps[3] = static_cast<uint32_t>(A.top_k); ps[0] = kPersistTag;
+    }
+    const float uk = chain_u(A, b, draw_uidx(A, job));
+    auto prob = [&](float e) { return static_cast<float>(static_cast<double>(e) / df_to_d(Z)); };   // diagnostics
+    if (!bonus) {
+        const int y = A.draft[static_cast<long long>(b) * A.K + row];
+        float ly, qy;
+        slice_y(parts, pb, C, ly, qy);
+        const float ey = (y >= 0 && y < A.V && fkey(ly) >= tau_key) ? ex2((ly - m) * c2) : 0.f;
+        if (y < 0 || y >= A.V) qy = 0.f;
+        const bool acc = chain_accept_z(A, y, ey, qy, Z, chain_u(A, b, row), st);
         if (acc) {
-            if (l == 0) chain_advance(A, b, row, kb, st, 0u, done, base);
-            return false;
+            chain_diag(A, b, row, prob(ey), qy, Z.hi, 0.f);
+            return row_job(A, b, row + 1, st, hint);
         }
-        if (l == 0) {
-            ReqState* rs = &A.W.req[b];
-            __stcg(&rs->m, m);
-            __stcg(&rs->invZ, __frcp_rn(Z.hi));
-            Task t;
-            t.b = b; t.row = row; t.kind = kResid; t.aux = 0; t.st = st; t.base = base;
-            int S1, SL1;
-            pick_slices(A.B, A.V, A.S, A.S1, done, S1, SL1);
-            push_task(A.W, t, S1, SL1, true);   // the residual units read m and 1/Z
+        // residual [p - q]_+ lives on S (p = 0 outside it): gather q at S
+        const float* qrow = chain_qrow(A, b, row);
+        dfloat rp = df_make(0.f);
+        for (int i = l; i < keep; i += 32) {
+            const float qx = __ldcg(qrow + sm.stok[i]);
+            const dfloat d = df_add(df_make(sm.swt[i].x), df_neg(df_mul(qx, Z)));
+            const dfloat w = d.hi > 0.f ? d : df_make(0.f);
+            sm.swt[i] = make_float2(w.hi, w.lo);
+            rp = df_add(rp, w);
         }
-        return false;
+        dfloat R = warp_sum_df(rp);
+        __syncwarp();
+        if (!(R.hi > 0.f)) {
+            st |= 4;
+            for (int i = l; i < keep; i += 32) sm.swt[i] = make_float2(ex2((sm.sval[i] - m) * c2), 0.f);
+            __syncwarp();
+            R = Z;
+        }
+        const int x = warp_icdf_pairs(sm.stok, sm.swt, keep, df_mul(uk, R));
+        chain_diag(A, b, row, prob(ey), qy, Z.hi, (st & 4) ? 0.f : static_cast<float>(df_to_d(R) / df_to_d(Z)));
+        return chain_finish(A, b, row, x, st);
     }
-    // BONUS: inverse CDF of p; find the slice, the consumers rescan it
+    // bonus row: draw from p on S
+    const int x = warp_icdf_pairs(sm.stok, sm.swt, keep, df_mul(uk, Z));
+    float px = 0.f;
+    for (int i = l; i < keep; i += 32)
+        if (sm.stok[i] == x) px = prob(sm.swt[i].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) px = fmaxf(px, __shfl_xor_sync(0xffffffffu, px, o));
+    if (!A.tree) chain_diag(A, b, row, px, 0.f, Z.hi, 0.f);
+    return draw_done(A, job, x, st, hint);
+}
+
+// ---------------------------------------------------------------------------
+// combine of a sum-exp row (untruncated, or masked at a known threshold)
+// ---------------------------------------------------------------------------
+__device__ Job combine_se(const ChainArgs& A, const Geo& G, const Job& job, const unsigned char* parts,
+                          ChainSmem& sm) {
+    const int l = threadIdx.x & 31;
+    const int C = G.C, pb = G.part_bytes;
+    const int b = job.b, row = job.row;
+    const bool bonus = job.aux != 0;
+    const uint32_t mask = job.hint;
+    int st = job.st;
+    const float c2 = A.c2;
+    uint32_t flags = 0;
+    float vm = -kInf;
+    dfloat sv = df_make(0.f);
+    if (l < C) {
+        const PartHdr* h = part_at(parts, pb, l);
+        flags = h->flags; vm = h->vmax; sv = df_of(h->sum);
+    }
+    flags = __reduce_or_sync(0xffffffffu, flags);
+    float m = vm;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((flags & kPfBad) || !(m > -kInf)) return finish_at(A, job, -1, st | 1);
+    dfloat zv = df_make(0.f);
+    if (l < C && sv.hi > 0.f) zv = df_mul(ex2((vm - m) * c2), sv);
+    const dfloat Z = warp_sum_df(zv);
+    const float uk = chain_u(A, b, draw_uidx(A, job));
+    if (!bonus) {
+        const int y = A.draft[static_cast<long long>(b) * A.K + row];
+        float ly, qy;
+        slice_y(parts, pb, C, ly, qy);
+        const float ey = (y >= 0 && y < A.V && fkey(ly) >= mask) ? ex2((ly - m) * c2) : 0.f;
+        if (y < 0 || y >= A.V) qy = 0.f;
+        const bool acc = chain_accept_z(A, y, ey, qy, Z, chain_u(A, b, row), st);
+        chain_diag(A, b, row, static_cast<float>(static_cast<double>(ey) / df_to_d(Z)), qy, Z.hi, 0.f);
+        if (acc) return row_job(A, b, row + 1, st, sm.last_hint);
+        // the residual pass: every slice's [p - q]_+ mass with this row's m and Z
+        Job j = make_job(b, row, kResid, st);
+        j.hint = mask;
+        j.f[0] = m;
+        j.f[1] = __frcp_rn(Z.hi);
+        return j;
+    }
+    // bonus: the slice where the cumulative p mass crosses u Z, then a rescan there
     const dfloat t = df_mul(uk, Z);
     dfloat before;
-    const int s = find_slice_w(S, zv, t, before);
-    if (l == 0) {
-        CombPrep& p = cs.prep;
-        p.b = b; p.row = row; p.kind = kind; p.st = st;
-        p.x0 = s * SL; p.x1 = min(A.V, p.x0 + SL); p.wmode = 0;
-        p.m = vmax; p.invZf = 0.f;
-        p.t = df_add(t, df_neg(before));
-        p.Z = df_to_d(Z); p.R = 0.0;
-    }
-    return true;
+    const int s = find_slice_w(C, zv, t, before);
+    const dfloat tr = df_add(t, df_neg(before));
+    Job j = make_job(b, row, kRescan, st);
+    j.target = s;
+    j.hint = mask;
+    j.aux = 1;                       // bonus row
+    j.aux2 = 0;                      // p weights
+    j.f[0] = m; j.f[1] = 0.f; j.f[2] = tr.hi; j.f[3] = tr.lo;
+    j.depth = job.depth;
+    if (!A.tree) chain_diag(A, b, row, 0.f, 0.f, Z.hi, 0.f);
+    return j;
 }
 
-// Consumers: the rescan of an untruncated draw prepared by combine_full --
-// the inverse CDF over one slice -- then the commit.
-template <class E>
-__device__ void rescan_cta(const ChainArgs& A, ChainSmem<false>& sh) {
-    const CombPrep p = sh.comb.prep;
-    const int b = p.b, row = p.row;
-    const void* lrow = chain_lrow<E>(A, b, row);
-    const float m = p.m, c2 = A.c2, invZ = p.invZf;
-    int x;
-    if (p.wmode == 1) {
-        const float* qrow = chain_qrow(A, b, row);
-        auto wr = [&](int xx) -> float {
-            const float d = ex2((E::load(lrow, xx) - m) * c2) * invZ - qrow[xx];
-            return d > 0.f ? d : 0.f;
-        };
-        x = cta_icdf(p.x0, p.x1, p.t, wr, sh.red2, sh.ired);
+__device__ Job combine_resid(const ChainArgs& A, const Geo& G, const Job& job, const unsigned char* parts) {
+    const int l = threadIdx.x & 31;
+    const int C = G.C, pb = G.part_bytes;
+    const int b = job.b, row = job.row;
+    int st = job.st;
+    const int kb = chain_k(A, b);
+    dfloat rv = df_make(0.f), pv = df_make(0.f);
+    if (l < C) {
+        const PartHdr* h = part_at(parts, pb, l);
+        rv = df_of(h->sum);
+        pv = df_of(h->sum2);
+    }
+    const dfloat R = warp_sum_df(rv), Pm = warp_sum_df(pv);
+    const float uk = chain_u(A, b, kb);
+    dfloat t, before;
+    int s, wmode;
+    if (R.hi > 0.f) {
+        t = df_mul(uk, R);
+        s = find_slice_w(C, rv, t, before);
+        wmode = 1;
     } else {
-        auto wp = [&](int xx) -> float { return ex2((E::load(lrow, xx) - m) * c2); };
-        x = cta_icdf(p.x0, p.x1, p.t, wp, sh.red2, sh.ired);
+        st |= 4;
+        t = df_mul(uk, Pm);
+        s = find_slice_w(C, pv, t, before);
+        wmode = 0;
     }
-    if (threadIdx.x == 0) {
-        if (p.kind == kResid) {
-            if (A.diag) A.diag[(static_cast<long long>(b) * (A.K + 1) + row) * 4 + 3] = (p.st & 4) ? 0.f : (float)p.R;
-        } else if (A.diag && x >= 0 && x < A.V) {
-            chain_diag(A, b, row, static_cast<float>(static_cast<double>(ex2((E::load(lrow, x) - m) * c2)) / p.Z), 0.f,
-                       static_cast<float>(p.Z), 0.f);
+    chain_diag_R(A, b, row, (st & 4) ? 0.f : static_cast<float>(df_to_d(R)));
+    const dfloat tr = df_add(t, df_neg(before));
+    Job j = make_job(b, row, kRescan, st);
+    j.target = s;
+    j.hint = job.hint;
+    j.aux = 0;
+    j.aux2 = wmode;
+    j.f[0] = job.f[0]; j.f[1] = job.f[1]; j.f[2] = tr.hi; j.f[3] = tr.lo;
+    return j;
+}
+
+template <class E>
+__device__ Job combine_rescan(const ChainArgs& A, const Job& job, const unsigned char* parts, int pb,
+                              uint32_t hint) {
+    const PartHdr* h = part_at(parts, pb, job.target);
+    const int x = h->tok;
+    const int b = job.b, row = job.row;
+    if (job.aux != 0) {
+        if (A.diag && !A.tree && (threadIdx.x & 31) == 0 && x >= 0 && x < A.V) {
+        // bonus row: p(x) = e_x / Z, with Z as the SE combine recorded it
+            float* d = A.diag + (static_cast<long long>(b) * (A.K + 1) + row) * 4;
+            const float e = ex2((E::load(chain_lrow<E>(A, b, row), x) - job.f[0]) * A.c2);
+            d[0] = static_cast<float>(static_cast<double>(e) / static_cast<double>(d[2]));
+        }
+        __syncwarp();
+        return draw_done(A, job, x, job.st, hint);
+    }
+    return chain_finish(A, b, row, x, job.st);
+}
+
+__device__ Job combine_radix(const ChainArgs& A, const Geo& G, const Job& job, const unsigned char* parts) {
+    const int l = threadIdx.x & 31;
+    const int C = G.C, pb = G.part_bytes;
+    const int round = job.aux2 & 0xff;
+    int want = job.aux2 >> 8;                 // rank sought among keys with this prefix
+    uint32_t flags = 0;
+    if (l < C) flags = part_at(parts, pb, l)->flags;
+    flags = __reduce_or_sync(0xffffffffu, flags);
+    if (flags & kPfBad) return finish_at(A, job, -1, job.st | 1);
+    // bins summed over the slices; lane l holds digits 8l .. 8l+7
+    int cnt[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        int c = 0;
+        for (int r = 0; r < C; ++r) c += reinterpret_cast<const int*>(part_at(parts, pb, r) + 1)[8 * l + j];
+        cnt[j] = c;
+    }
+    // digits from the top: the one where the running count reaches `want`
+    int lane_tot = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) lane_tot += cnt[j];
+    int above = 0;   // keys in higher lanes (larger digits)
+    {
+        int suf = lane_tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_down_sync(0xffffffffu, suf, o);
+            if (l + o < 32) suf += t;
+        }
+        above = suf - lane_tot;
+    }
+    int digit = -1, rem = 0;
+    {
+        int run = above;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {
+            if (digit < 0 && run + cnt[j] >= want) { digit = 8 * l + j; rem = want - run; }
+            run += cnt[j];
         }
     }
-    chain_finish_cta(A, b, row, x, p.st);
+    const uint32_t bal = __ballot_sync(0xffffffffu, digit >= 0);
+    const int src = bal ? 31 - __clz(bal) : 0;   // the highest lane that reached it holds the digit
+    digit = __shfl_sync(0xffffffffu, digit, src);
+    rem = __shfl_sync(0xffffffffu, rem, src);
+    if (digit < 0) { digit = 0; rem = 1; }        // unreachable: fewer than k keys in the row
+    const uint32_t prefix = (job.hint << 8) | static_cast<uint32_t>(digit);
+    if (round < 3) {
+        Job j = make_job(job.b, job.row, kRadix, job.st);
+        j.aux = job.aux;
+        j.hint = prefix;
+        j.aux2 = (rem << 8) | (round + 1);
+        j.depth = job.depth;
+        return j;
+    }
+    // the exact threshold: the masked sum-exp passes take it from here
+    Job j = make_job(job.b, job.row, kSe, job.st);
+    j.aux = job.aux;
+    j.hint = prefix;
+    j.depth = job.depth;
+    return j;
 }
 
 // ---------------------------------------------------------------------------
-// the kernel
+// the op
 // ---------------------------------------------------------------------------
-// what a unit streams: logits row range (VERIFY/BONUS), logits and q
-// (RESID), nothing (invalid k)
-template <class E>
-__device__ __forceinline__ int chain_unit_kind(const ChainArgs& A, const Task& t) {
-    if (t.kind >= 0) return t.kind & kKindMask;
-    const int kb = chain_k(A, t.b);
-    return (kb < 0 || kb > A.K) ? kInvalid : (kb == 0 ? kBonus : kVerify);
-}
-template <class E>
-__device__ __forceinline__ StreamPlan chain_plan(const ChainArgs& A, const Task& t, int kind, int slice) {
-    const int SL = task_SL(A, t);
-    const int x0 = slice * SL, x1 = min(A.V, x0 + SL);
-    if (kind == kVerify || kind == kBonus) return plan_single(chain_lrow<E>(A, t.b, t.row), E::kBytes, x0, x1);
-    if (kind == kResid) return plan_dual(chain_lrow<E>(A, t.b, t.row), E::kBytes, chain_qrow(A, t.b, t.row), x0, x1);
-    return plan_none();
-}
-
 template <class E, bool kTopk>
-__global__ void __launch_bounds__(kBlockThreads, kCtasPerSm) chain_kernel(const ChainArgs A) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    auto& sh = *reinterpret_cast<ChainSmem<kTopk>*>(smem + kStages * kChunkBytes);
-    if constexpr (kTopk) {
-        if (threadIdx.x == 0) topk_smem_init(sh.tk);   // made visible by pipe_init's barrier
-    }
-    const Pipe P = pipe_init(smem, sh.pipe);
-    // the residual pass streams q beside the logits; without q rows (K = 0)
-    // there is no residual pass
-    const bool tma = A.tma_l && (kTopk || A.K == 0 || A.tma_q);
-    if (threadIdx.x >= kCombiner0) {
-        // combiner warp: arrivals, combines (top-k: prepared here, computed by
-        // the consumers at their next wait)
-        uint32_t cpub = 0;
-        combiner_loop(P, [&](const Job& job) {
-            const int b = job.task.b;
-            uint32_t done, base;
-            if (!comb_arrive(A.W, job.task, task_S(A, job.task), &done, &base)) return;
-            SPEC_TRACE_EVW(2, b, job.task.row, job.slice, job.kind);
-            const int st = job.task.st;
-            if (job.kind == kInvalid) {
-                chain_finish(A, b, 0, -1, 16);
-            } else if (!combine_reuse(P, cpub)) {
-                return;   // the consumers stopped answering: the kernel is aborting
-            } else if constexpr (kTopk) {
-                if (prepare_topk<E>(A, sh.comb, b, job.task.row, job.kind, st, task_S(A, job.task),
-                                    task_SL(A, job.task), done, base))
-                    publish_combine(P, cpub);
-            } else {
-                if (combine_full<E>(A, sh.comb, b, job.task.row, job.kind, st, task_S(A, job.task),
-                                    task_SL(A, job.task), done, base))
-                    publish_combine(P, cpub);
-            }
-            __syncwarp();
-            SPEC_TRACE_EVW(3, b, job.task.row, job.slice, job.kind);
-        }, [&]() { combine_reuse(P, cpub); });
-        return;
-    }
-    if (threadIdx.x >= kThreads) {
-        if (threadIdx.x == kProducer) {
-            producer_loop(A.W, A.B, A.S, P, tma,
-                          [&](Claimed& c) {
-                              if (kTopk && c.task.kind < 0) {
-                                  // the latest finished row of this call, else of the previous call
-                                  // on this workspace (all five words in one round trip)
-                                  const uint32_t h0 = __ldcg(&A.W.ctrl->hint0);
-                                  const uint4 ps = __ldcg(reinterpret_cast<const uint4*>(A.W.persist));
-                                  c.hint = h0;
-                                  if (h0 == 0 && ps.x == kPersistTag && ps.z == static_cast<uint32_t>(A.V) &&
-                                      ps.w == static_cast<uint32_t>(A.top_k))
-                                      c.hint = ps.y;
-                              }
-                          },
-                          [&](const Claimed& c) {
-                              return chain_plan<E>(A, c.task, chain_unit_kind<E>(A, c.task), c.slice);
-                          });
+struct ChainOp {
+    using Args = ChainArgs;
+    using Smem = ChainSmem;
+
+    __device__ static int batch(const Args& A) { return A.B; }
+    __device__ static bool tma(const Args& A) { return A.tma_l && (kTopk || A.K == 0 || A.tma_q); }
+    __device__ static void init_smem(const Args&, const Geo&, Smem& sm) {
+        if (threadIdx.x == 0) {
+            topk_smem_init(sm.tk);
+            sm.tag = 0;
+            sm.last_hint = 0;
         }
-        return;
     }
-    uint32_t seq = 0, jseq = 0, cseq = 0;
-    auto serve = [&]() {
-        if constexpr (kTopk) combine_topk_cta<E>(A, sh);
-        else rescan_cta<E>(A, sh);
-    };
-    for (uint32_t u = 0;; ++u) {
-        const Claimed cl = next_unit(P, u, cseq, serve);
-        if (!cl.ok) break;
-        const Task t = cl.task;
-        const int s = cl.slice;
-        SPEC_TRACE_EV(0, t.b, t.row, s, t.kind);
-        const int b = t.b;
-        const int row = t.row;
-        const bool initial = t.kind < 0;
-        const int kind = chain_unit_kind<E>(A, t);
-        const bool nohint = !initial && (t.kind & kNoHint);
-        PartHdr* ph = part_hdr(A.W, b, s, A.S);
-        uint64_t* pk = part_keys(A.W, b, s, A.S);
-        const int SLt = task_SL(A, t);
-        const int x0 = s * SLt, x1 = min(A.V, x0 + SLt);
-        const StreamPlan plan = chain_plan<E>(A, t, kind, s);
-        bool ok = true;
-        if (kind == kVerify || kind == kBonus) {
-            // the drafted token: its logit is recorded as the slice streams,
-            // its q fetched early by the slice that holds it
+    __device__ static Job first(const Args& A, const Geo&, int b, Smem& sm) {
+        const int kb = A.tree ? 0 : chain_k(A, b);
+        if (kb < 0 || kb > A.K) return chain_finish(A, b, 0, -1, 16);
+        uint32_t hint = sm.last_hint;
+        if (kTopk && hint == 0) {
+            // the previous call on this workspace, for the same vocabulary and top-k
+            const volatile uint32_t* ps = A.E.W.ctrl->persist;
+            if (ps[0] == kPersistTag && ps[2] == static_cast<uint32_t>(A.V) && ps[3] == static_cast<uint32_t>(A.top_k))
+                hint = ps[1];
+        }
+        return row_job(A, b, 0, 0, hint);
+    }
+    __device__ static StreamPlan plan(const Args& A, const Geo& G, const Job& j) {
+        const int x0 = slice_x0(G, G.rank), x1 = slice_x1(G, G.rank, A.V);
+        switch (j.kind) {
+            case kTk: case kSe: case kRadix:
+                return plan_single(chain_lrow<E>(A, j.b, j.row), E::kBytes, x0, x1);
+            case kResid:
+                return plan_dual(chain_lrow<E>(A, j.b, j.row), E::kBytes, chain_qrow(A, j.b, j.row), x0, x1);
+            default:
+                return plan_none();
+        }
+    }
+
+    // consumers: this CTA's slice of the job -> the partial in `out`
+    __device__ static int consume(const Args& A, const Geo& G, const Pipe& P, uint32_t& seq, bool tma, const Job& j,
+                                  Smem& sm, unsigned char* out) {
+        PartHdr* ph = reinterpret_cast<PartHdr*>(out);
+        uint64_t* pk = reinterpret_cast<uint64_t*>(ph + 1);
+        const int x0 = slice_x0(G, G.rank), x1 = slice_x1(G, G.rank, A.V);
+        const int b = j.b, row = j.row;
+        const StreamPlan plan = ChainOp::plan(A, G, j);
+        if (threadIdx.x == 0) {
+            ph->flags = 0; ph->cnt = 0; ph->tok = -1; ph->kth = 0; ph->vmax = -kInf; ph->hasy = 0;
+            ph->sum = make_float2(0.f, 0.f); ph->sum2 = make_float2(0.f, 0.f); ph->ly = -kInf; ph->qy = 0.f;
+        }
+        int nkeys = 0;
+        if (j.kind == kTk || j.kind == kSe) {
             DraftWatch dw;
             dw.x0 = x0; dw.x1 = x1;
-            if (kind == kVerify) {
+            if (j.aux == 0) {
                 dw.y = A.draft[static_cast<long long>(b) * A.K + row];
                 dw.qrow = chain_qrow(A, b, row);
             }
-            float* wsl = sh.fsh;
-            if constexpr (kTopk) {
-                const uint32_t hint = nohint ? 0u : (initial ? cl.hint : static_cast<uint32_t>(t.aux));
+            float* wsl = sm.fsh;
+            if (kTopk && j.kind == kTk) {
+                if (threadIdx.x == 0) sm.tag = sm.tag + 1;
+                csync();
                 TopkHistFn<E, true> fn;
-                fn.init(&sh.tk, A.top_k, hint, u + 1u);
+                fn.init(&sm.tk, A.top_k, j.hint, sm.tag);
                 fn.dw = dw;
-                ok = consume_row<E>(P, seq, plan, tma, x0, fn);
-                if (ok) {
-                    SPEC_TRACE_EV(4, b, row, s, kind);
-                    fn.publish();
-                    if (fn.dw.seen) wsl[0] = fn.dw.ly;
-                    csync();
-                    int tot;
-                    uint64_t F;
-                    uint32_t fl;
-                    float vm;
-                    fn.summary(tot, F, fl, vm);
-                    const uint32_t bad = (fl >> 1) & 1u;
-                    uint32_t oflow = fl & 1u;
-                    int n = tot;
-                    if (!bad && !oflow && tot <= A.cap_p) {
-                        fn.write_keys(pk);   // every warp's keys at its offset
-                        SPEC_TRACE_EV(17, b, row, s, tot);
-                    } else if (!bad && !oflow) {
-                        // too many: the certified bound over every candidate, repeated
-                        // until it stops rising (then it is the exact k-th value)
-                        uint32_t o2, b2;
-                        float vm2;
-                        n = fn.finish(F, o2, b2, vm2);
-                        uint64_t* list = sh.tk.cand;
-                        for (int it = 0; it < 8 && n > A.cap_p; ++it) {
-                            bool cert;
-                            const uint32_t F2 = hist_bound_list(list, n, A.top_k, hkey(F), sh.hist, sh.scratch, cert);
-                            if (!(cert && F2 > hkey(F))) break;
-                            n = compact_list(list, n, F2, sh.ired);
-                            F = static_cast<uint64_t>(F2) << 32;
-                        }
-                        if (n > A.cap_p) oflow = 1;   // ties at the k-th value: the fallback decides
-                        else for (int i = threadIdx.x; i < n; i += kThreads) __stcg(pk + i, list[i]);
-                        SPEC_TRACE_EV(17, b, row, s, tot | (1 << 20));
+                if (!consume_row<E>(P, seq, plan, tma, x0, fn)) return -1;
+                fn.publish();
+                if (fn.dw.seen) wsl[0] = fn.dw.ly;
+                csync();
+                int tot;
+                uint64_t F;
+                uint32_t fl;
+                float vm;
+                fn.summary(tot, F, fl, vm);
+                const uint32_t bad = (fl >> 1) & 1u;
+                uint32_t oflow = fl & 1u;
+                int n = tot;
+                if (!bad && !oflow && tot <= A.cap_p) {
+                    fn.write_keys(pk);   // every warp's keys at its offset
+                } else if (!bad && !oflow) {
+                    // too many: the certified bound over every candidate, repeated
+                    // until it stops rising (then it is the exact k-th value)
+                    uint32_t o2, b2;
+                    float vm2;
+                    n = fn.finish(F, o2, b2, vm2);
+                    uint64_t* list = sm.tk.cand;
+                    for (int it = 0; it < 8 && n > A.cap_p; ++it) {
+                        bool cert;
+                        const uint32_t F2 = hist_bound_list(list, n, A.top_k, hkey(F), sm.hist, sm.scratch, cert);
+                        if (!(cert && F2 > hkey(F))) break;
+                        n = compact_list(list, n, F2, sm.ired);
+                        F = static_cast<uint64_t>(F2) << 32;
                     }
-                    if (oflow || bad) n = 0;   // the combine does not read the keys then
-                    if (threadIdx.x == 0) {
-                        ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u) | (hint ? kPfHinted : 0u);
-                        ph->cnt = n;
-                        ph->kth = F;
-                        ph->vmax = vm;
-                        if (fn.dw.owns()) { ph->ly = wsl[0]; ph->qy = fn.dw.qy; }
-                    }
+                    if (n > A.cap_p) oflow = 1;   // ties at the k-th value: the combine takes the radix path
+                    else for (int i = threadIdx.x; i < n; i += kThreads) pk[i] = list[i];
+                }
+                if (oflow || bad) n = 0;
+                nkeys = n;
+                if (threadIdx.x == 0) {
+                    ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u) | (j.hint ? kPfHinted : 0u);
+                    ph->cnt = n;
+                    ph->kth = F;
+                    ph->vmax = vm;
+                    if (fn.dw.owns()) { ph->ly = wsl[0]; ph->qy = fn.dw.qy; ph->hasy = 1; }
                 }
             } else {
-                SumExpFn<E> fn;
-                fn.c = A.c2;
-                fn.dw = dw;
-                ok = consume_row<E>(P, seq, plan, tma, x0, fn);
-                if (ok) {
-                    // per warp: fold (m_t, s_t) into the warp's max and sum; then thread 0
-                    // folds the warps
+                // sum-exp (masked at the job's threshold when it carries one)
+                const uint32_t mask = j.hint;
+                auto run = [&](auto& fn) -> bool {
+                    fn.c = A.c2;
+                    fn.dw = dw;
+                    if (!consume_row<E>(P, seq, plan, tma, x0, fn)) return false;
                     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
                     float wm = fn.m;
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
                     const float sc = (fn.s > 0.f) ? fn.s * ex2((fn.m - wm) * A.c2) : 0.f;
-                    const dfloat ws = warp_sum_df(df_make(sc));
+                    const dfloat wsd = warp_sum_df(df_make(sc));
+                    float wv = fn.vmx;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) wv = max_nan(wv, __shfl_xor_sync(0xffffffffu, wv, o));
                     const uint32_t wb = __reduce_or_sync(0xffffffffu, fn.bad_flag());
-                    if (lane == 0) { sh.wm[w] = wm; sh.ws[w] = make_float2(ws.hi, ws.lo); sh.wb[w] = wb; }
+                    if (lane == 0) { sm.wm[w] = wm; sm.ws[w] = make_float2(wsd.hi, wsd.lo); sm.wb[w] = wb; sm.ws2[w].x = wv; }
                     if (fn.dw.seen) wsl[0] = fn.dw.ly;
                     csync();
                     if (threadIdx.x == 0) {
-                        float ms = -kInf;
+                        float ms = -kInf, vx = -kInf;
                         uint32_t bad = 0;
-                        for (int j = 0; j < kWarps; ++j) { ms = fmaxf(ms, sh.wm[j]); bad |= sh.wb[j]; }
+                        for (int q = 0; q < kWarps; ++q) { ms = fmaxf(ms, sm.wm[q]); bad |= sm.wb[q]; vx = max_nan(vx, sm.ws2[q].x); }
                         dfloat tot = df_make(0.f);
-                        for (int j = 0; j < kWarps; ++j)
-                            if (sh.ws[j].x > 0.f) tot = df_add(tot, df_mul(ex2((sh.wm[j] - ms) * A.c2), df_of(sh.ws[j])));
+                        for (int q = 0; q < kWarps; ++q)
+                            if (sm.ws[q].x > 0.f) tot = df_add(tot, df_mul(ex2((sm.wm[q] - ms) * A.c2), df_of(sm.ws[q])));
                         ph->flags = bad ? kPfBad : 0u;
-                        ph->cnt = 0;
-                        ph->vmax = ms;
+                        ph->vmax = bad ? vx : ms;
                         ph->sum = make_float2(tot.hi, tot.lo);
-                        if (fn.dw.owns()) { ph->ly = wsl[0]; ph->qy = fn.dw.qy; }
+                        if (fn.dw.owns()) { ph->ly = wsl[0]; ph->qy = fn.dw.qy; ph->hasy = 1; }
                     }
+                    return true;
+                };
+                bool ok;
+                if (mask == 0u) {
+                    SumExpFn<E, false> fn;
+                    ok = run(fn);
+                } else {
+                    SumExpFn<E, true> fn;
+                    fn.thr = key_to_thr(mask);
+                    ok = run(fn);
                 }
+                if (!ok) return -1;
             }
-        } else if (kind == kResid) {
-            const ReqState* rs = &A.W.req[b];
+        } else if (j.kind == kResid) {
             ResidFn<E> fn;
-            fn.m = __ldcg(&rs->m);
+            fn.m = j.f[0];
             fn.c = A.c2;
-            fn.invZ = __ldcg(&rs->invZ);
-            ok = consume_row2<E>(P, seq, plan, tma, x0, fn);
-            if (ok) {
-                const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-                const dfloat wr = warp_sum_df(df_make(fn.r));
-                const dfloat wp = warp_sum_df(df_make(fn.pw));
-                if (lane == 0) { sh.ws[w] = make_float2(wr.hi, wr.lo); sh.ws2[w] = make_float2(wp.hi, wp.lo); }
-                csync();
-                if (threadIdx.x == 0) {
-                    dfloat rsum = df_make(0.f), psum = df_make(0.f);
-                    for (int j = 0; j < kWarps; ++j) { rsum = df_add(rsum, df_of(sh.ws[j])); psum = df_add(psum, df_of(sh.ws2[j])); }
-                    ph->flags = 0;
-                    ph->sum = make_float2(rsum.hi, rsum.lo);
-                    ph->sum2 = make_float2(psum.hi, psum.lo);
-                }
+            fn.invZ = j.f[1];
+            fn.thr = j.hint ? key_to_thr(j.hint) : -kInf;
+            if (!consume_row2<E>(P, seq, plan, tma, x0, fn)) return -1;
+            const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+            const dfloat wr = warp_sum_df(df_make(fn.r));
+            const dfloat wp = warp_sum_df(df_make(fn.pw));
+            if (lane == 0) { sm.ws[w] = make_float2(wr.hi, wr.lo); sm.ws2[w] = make_float2(wp.hi, wp.lo); }
+            csync();
+            if (threadIdx.x == 0) {
+                dfloat rsum = df_make(0.f), psum = df_make(0.f);
+                for (int q = 0; q < kWarps; ++q) { rsum = df_add(rsum, df_of(sm.ws[q])); psum = df_add(psum, df_of(sm.ws2[q])); }
+                ph->sum = make_float2(rsum.hi, rsum.lo);
+                ph->sum2 = make_float2(psum.hi, psum.lo);
             }
+        } else if (j.kind == kRescan) {
+            // the inverse CDF inside this slice, reading the row from global memory
+            const void* lrow = chain_lrow<E>(A, b, row);
+            const float m = j.f[0], c2 = A.c2, invZ = j.f[1];
+            const float thr = j.hint ? key_to_thr(j.hint) : -kInf;
+            const dfloat t{j.f[2], j.f[3]};
+            int x;
+            if (j.aux2 == 1) {
+                const float* qrow = chain_qrow(A, b, row);
+                auto wr = [&](int xx) -> float {
+                    const float lv = E::load(lrow, xx);
+                    const float w = lv >= thr ? ex2((lv - m) * c2) : 0.f;
+                    const float d = w * invZ - qrow[xx];
+                    return d > 0.f ? d : 0.f;
+                };
+                x = cta_icdf(x0, x1, t, wr, sm.red2, sm.ired);
+            } else {
+                auto wp = [&](int xx) -> float {
+                    const float lv = E::load(lrow, xx);
+                    return lv >= thr ? ex2((lv - m) * c2) : 0.f;
+                };
+                x = cta_icdf(x0, x1, t, wp, sm.red2, sm.ired);
+            }
+            if (threadIdx.x == 0) ph->tok = x;
+        } else if (j.kind == kRadix) {
+            for (int i = threadIdx.x; i < 256; i += kThreads) sm.bins[i] = 0;
+            csync();
+            RadixFn<E> fn;
+            fn.bins = sm.bins;
+            fn.round = j.aux2 & 0xff;
+            fn.prefix = j.hint;
+            if (!consume_row<E>(P, seq, plan, tma, x0, fn)) return -1;
+            const float wv = block_max_nan(fn.vmx, sm.wm);
+            csync();
+            int* ob = reinterpret_cast<int*>(pk);
+            for (int i = threadIdx.x; i < 256; i += kThreads) ob[i] = sm.bins[i];
+            if (threadIdx.x == 0) {
+                ph->flags = bad_max(wv) ? kPfBad : 0u;
+                ph->vmax = wv;
+            }
+            nkeys = 128;   // 256 int bins = 1024 bytes
         }
-        if (!ok) break;
-        SPEC_TRACE_EV(1, b, row, s, kind);
-        csync();   // every consumer's partial writes are ordered before the hand-over
-        Job j;
-        j.task = t; j.slice = s; j.kind = kind; j.stop = 0; j.flags = 0;
-        post_job(P, jseq, cseq, j, serve);
-        SPEC_TRACE_EV(18, b, row, s, 0);
+        return static_cast<int>(sizeof(PartHdr)) + ((nkeys * 8 + 15) & ~15);
     }
-    // stop the combiner once it has taken every job (serving its last combines)
-    Job j;
-    j.task.b = 0; j.task.row = 0; j.task.kind = 0; j.task.aux = 0; j.task.st = 0; j.task.base = 0;
-    j.slice = 0; j.kind = 0; j.stop = 1; j.flags = 0;
-    post_job(P, jseq, cseq, j, serve);
-    // combines still in the combiner's queue are served until it stops
-    consumer_wait(P, cseq, [&]() { return mbar_test(&P.jempty[(jseq - 1) % kJobs], ((jseq - 1) / kJobs) & 1u); }, serve);
-}
 
-// kCtasPerSm CTAs per SM (228 KiB of shared memory, 1 KiB reserved per CTA)
-static_assert(kStages * kChunkBytes + sizeof(ChainSmem<true>) <= (228 * 1024) / kCtasPerSm - 1024,
-              "chain CTA too large for kCtasPerSm per SM");
+    __device__ static Job combine(const Args& A, const Geo& G, const Job& j, const unsigned char* parts, Smem& sm) {
+        switch (j.kind) {
+            case kTk: return combine_topk<E>(A, G, j, parts, sm);
+            case kSe: return combine_se(A, G, j, parts, sm);
+            case kResid: return combine_resid(A, G, j, parts);
+            case kRescan: return combine_rescan<E>(A, j, parts, G.part_bytes, sm.last_hint);
+            default: return combine_radix(A, G, j, parts);
+        }
+    }
+};
 
 template <class E, bool kTopk>
-static size_t chain_smem_bytes() {
-    return kStages * kChunkBytes + sizeof(ChainSmem<kTopk>);
+__global__ void __launch_bounds__(kBlockThreads, 1) chain_kernel(const ChainArgs A) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    Engine<ChainOp<E, kTopk>>::run(A, A.E.W, make_geo(A.E), smem);
 }
 
 template <class E, bool kTopk>
-static cudaError_t chain_launch(const ChainArgs& A, int grid, cudaStream_t st) {
-    const size_t smem = chain_smem_bytes<E, kTopk>();
-    cudaError_t e = cudaFuncSetAttribute(chain_kernel<E, kTopk>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    chain_kernel<E, kTopk><<<grid, kBlockThreads, smem, st>>>(A);
-    return cudaGetLastError();
+static const void* chain_fn() { return reinterpret_cast<const void*>(&chain_kernel<E, kTopk>); }
+
+const void* chain_kernel_ptr(int ldt, bool topk) {
+    if (ldt == 0) return topk ? chain_fn<F32, true>() : chain_fn<F32, false>();
+    return topk ? chain_fn<BF16, true>() : chain_fn<BF16, false>();
 }
 
-size_t chain_smem(int ldt, bool topk) {
-    if (ldt == 0) return topk ? chain_smem_bytes<F32, true>() : chain_smem_bytes<F32, false>();
-    return topk ? chain_smem_bytes<BF16, true>() : chain_smem_bytes<BF16, false>();
+size_t chain_smem(int C, int own, int part_bytes, int stages) {
+    // the same layout for every instantiation
+    return Engine<ChainOp<F32, true>>::smem_bytes(C, own, part_bytes, stages);
 }
 
-int chain_occupancy(int ldt, bool topk) {
-    int n = 0;
-    const int smem = static_cast<int>(chain_smem(ldt, topk));
-    if (ldt == 0) {
-        if (topk) { cudaFuncSetAttribute(chain_kernel<F32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, chain_kernel<F32, true>, kBlockThreads, smem); }
-        else { cudaFuncSetAttribute(chain_kernel<F32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-               cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, chain_kernel<F32, false>, kBlockThreads, smem); }
-    } else {
-        if (topk) { cudaFuncSetAttribute(chain_kernel<BF16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-                    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, chain_kernel<BF16, true>, kBlockThreads, smem); }
-        else { cudaFuncSetAttribute(chain_kernel<BF16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-               cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, chain_kernel<BF16, false>, kBlockThreads, smem); }
-    }
-    return n;
-}
-
-cudaError_t chain_run(const ChainArgs& A, int grid, cudaStream_t st) {
-    const bool topk = A.top_k > 0 && A.top_k < A.V;
-    if (A.ldt == 0) return topk ? chain_launch<F32, true>(A, grid, st) : chain_launch<F32, false>(A, grid, st);
-    return topk ? chain_launch<BF16, true>(A, grid, st) : chain_launch<BF16, false>(A, grid, st);
+int chain_part_bytes(int top_k, int cap_p) {
+    const int keys = top_k > 0 ? (cap_p > 128 ? cap_p : 128) : 128;   // radix bins need 1 KiB
+    return static_cast<int>(sizeof(PartHdr)) + keys * 8;
 }
 
 }  // namespace spec
-
-SPEC_TRACE_EXPORT(chain)

@@ -1,441 +1,218 @@
-// spec_engine.cuh -- the persistent row-task engine shared by every
-// verification kernel.
+// spec_engine.cuh -- the cluster engine shared by every verification kernel.
 //
-// Work model.  Every verification in this library walks, per request, a
-// chain of vocabulary rows where row i+1 is read only if row i's decision
-// says so (early exit).  A *task* is "process row r of request b"; it is cut
-// into S contiguous *slices* of the vocabulary, and each (task, slice) pair
-// is a *unit*.  A persistent grid of CTAs claims units from one global FIFO
-// counter.  Inside a CTA a producer warp claims units and streams each
-// unit's slice HBM -> shared memory with 1-D TMA bulk copies through a
-// kStages mbarrier ring, while eight consumer warps process the chunks and
-// write a small partial result per unit.  The CTA that completes the last slice of a task (atomic arrival
-// counter, last-arriver pattern) combines the partials, takes the decision,
-// and pushes the request's next task, if any, onto the queue.  Tasks of
-// different requests and depths interleave freely: there is no grid-wide
-// barrier, and a request's next row starts as soon as its decision is known.
+// Work model.  Per request, a verification walks a chain of vocabulary rows
+// in which row i+1 is read only when row i's decision says so (early exit).
+// A thread-block cluster of C CTAs (one CTA per SM) owns up to R requests at
+// a time, one per *slot*.  Every row is split across the cluster: CTA r
+// streams elements [r*SL, min(V, (r+1)*SL)) of the row HBM -> shared memory
+// with 1-D TMA bulk copies through a ring of mbarrier-tracked stages and
+// reduces them to a small *partial*, which it stores into the shared memory
+// of the slot's *leader* CTA (distributed shared memory) and counts on the
+// leader's arrival mbarrier.  The leader's combiner warp takes the decision
+// and posts the slot's next *job* (the request's next row, a residual pass,
+// or the first row of a newly claimed request) to the mailbox of every CTA
+// of the cluster.  Every CTA streams the jobs of all slots interleaved, so
+// one slot's combine overlaps the other slots' streaming; slot s is led by
+// CTA s mod C, so combines spread over the cluster.  Requests are claimed
+// from one global counter whenever a slot frees up; there is no grid-wide
+// barrier and no global queue.
 //
-// Waits.  A CTA that claimed a pushed unit not yet written waits for that
-// unit's record (which carries the whole task), or for every request to be
-// finished; the wait is bounded and gives up with SPEC_WS_ERR_WAIT.
-// Progress never depends on a waiting CTA: units are claimed in order and
-// processed without waiting, so the kernel terminates even if only part of
-// the grid is resident.
+// Roles inside a CTA (kBlockThreads threads):
+//   warps 0..kWarps-1   consumers: take each job from the producer, process
+//                       the streamed chunks, write the partial to the leader
+//   warp kWarps         producer (lane 0): picks the next posted job of any
+//                       slot (round robin), hands it to the consumers and
+//                       issues its chunks
+//   warp kWarps + 1     combiner: leads this CTA's slots (claims requests,
+//                       combines their partials, posts their jobs)
+//
+// Waits.  Every wait is bounded (kMbarLimitNs of wall time); a wait that
+// gives up sets the workspace error word and the CTA's abort flag, and every
+// loop leaves.  No CTA leaves the kernel before the final cluster barrier,
+// so no distributed-shared-memory store can target an exited CTA.
 #pragma once
 
 #include "spec_common.cuh"
 
 namespace spec {
 
-// Optional phase timers for development builds (-DSPEC_PROFILE): thread 0
-// adds clock64() deltas per phase to g_prof[2*i] and counts to g_prof[2*i+1].
-#ifdef SPEC_PROFILE
-static __device__ unsigned long long g_prof[64];
-#define SPEC_PROF_T(v) const long long v = clock64()
-#define SPEC_PROF_ADD(i, v)                                                                   \
-    do {                                                                                      \
-        if (threadIdx.x == 0) {                                                               \
-            atomicAdd(&g_prof[2 * (i)], static_cast<unsigned long long>(clock64() - (v)));    \
-            atomicAdd(&g_prof[2 * (i) + 1], 1ull);                                            \
-        }                                                                                     \
-    } while (0)
-#else
-#define SPEC_PROF_T(v)
-#define SPEC_PROF_ADD(i, v)
-#endif
-
-// Optional event trace for development builds (-DSPEC_TRACE): thread 0
-// appends (globaltimer, SM, event, request, row, slice, aux) records to a
-// buffer installed by the translation unit's spec_trace_setup_<name>().
-#ifdef SPEC_TRACE
-struct TraceRec {
-    unsigned long long t;
-    int sm, ev, b, row, slice, aux;
-};
-static __device__ TraceRec* g_trace;
-static __device__ unsigned g_trace_cap;
-static __device__ unsigned g_trace_n;
-__device__ __forceinline__ void trace_ev(int ev, int b, int row, int slice, int aux) {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    int sm;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
-    const unsigned i = atomicAdd(&g_trace_n, 1u);
-    if (g_trace && i < g_trace_cap) {
-        TraceRec r;
-        r.t = t; r.sm = sm | (blockIdx.x << 8); r.ev = ev; r.b = b; r.row = row; r.slice = slice; r.aux = aux;
-        g_trace[i] = r;
-    }
-}
-#define SPEC_TRACE_EV(ev, b, row, slice, aux) \
-    do { if (threadIdx.x == 0) ::spec::trace_ev((ev), (b), (row), (slice), (aux)); } while (0)
-#define SPEC_TRACE_EVW(ev, b, row, slice, aux) \
-    do { if ((threadIdx.x & 31) == 0) ::spec::trace_ev((ev), (b), (row), (slice), (aux)); } while (0)
-#define SPEC_TRACE_EV1(ev, b, row, slice, aux) ::spec::trace_ev((ev), (b), (row), (slice), (aux))
-#define SPEC_TRACE_EXPORT(name)                                                              \
-    extern "C" int spec_trace_setup_##name(void* buf, unsigned cap) {                        \
-        unsigned z = 0;                                                                      \
-        if (cudaMemcpyToSymbol(::spec::g_trace, &buf, sizeof(buf)) != cudaSuccess) return 1; \
-        if (cudaMemcpyToSymbol(::spec::g_trace_cap, &cap, sizeof(cap)) != cudaSuccess) return 1; \
-        return cudaMemcpyToSymbol(::spec::g_trace_n, &z, sizeof(z)) != cudaSuccess;          \
-    }                                                                                        \
-    extern "C" unsigned spec_trace_count_##name(void) {                                      \
-        unsigned n = 0;                                                                      \
-        cudaMemcpyFromSymbol(&n, ::spec::g_trace_n, sizeof(n));                               \
-        return n;                                                                            \
-    }
-#else
-#define SPEC_TRACE_EV(ev, b, row, slice, aux)
-#define SPEC_TRACE_EVW(ev, b, row, slice, aux)
-#define SPEC_TRACE_EV1(ev, b, row, slice, aux)
-#define SPEC_TRACE_EXPORT(name)
-#endif
-
 // Ring geometry (development builds may override it).
 #ifndef SPEC_CHUNK_BYTES
-#define SPEC_CHUNK_BYTES 12288
+#define SPEC_CHUNK_BYTES 16384
 #endif
 #ifndef SPEC_STAGES
-#define SPEC_STAGES 4
+#define SPEC_STAGES 8
 #endif
 constexpr int kChunkBytes = SPEC_CHUNK_BYTES;   // one ring stage
-constexpr int kStages = SPEC_STAGES;            // ring depth: 48 KiB in flight per CTA by default
+constexpr int kStages = SPEC_STAGES;            // most ring stages (the launch picks how many fit)
 static_assert(kChunkBytes % 4096 == 0 && kStages >= 2, "ring geometry");
-constexpr int kMaxSlices = 32;
+
+constexpr int kMaxC = 16;          // CTAs per cluster, at most
+constexpr int kMaxSlots = 32;      // slots per cluster, at most
+constexpr int kMaxOwn = 4;         // slots one CTA leads, at most
+constexpr int kQ = 4;              // producer -> consumer job queue entries
 
 enum : uint32_t { kErrWait = 1u, kErrQueue = 2u };
 constexpr uint32_t kPersistTag = 0x5e1ec7edu;
 
-// Queue control words, one 128-byte line per group so that the atomics on
-// `head` and `tail` do not serialise with the polling of `done` / `error`.
+// Workspace control block (caller memory; the first 128 bytes are zeroed
+// by the call, the persist line is kept across calls).
 struct Ctrl {
-    uint32_t head;     // next initial unit to claim (the B*S0 units of the first rows)
-    uint32_t pad0[31];
-    uint32_t head1;    // next pushed unit to claim
-    uint32_t pad4[31];
-    unsigned long long tailc;   // (pushed tasks << 32) | pushed units
-    uint32_t pad1[30];
-    uint32_t done;     // finished requests
+    uint32_t next;     // next request to claim
     uint32_t error;    // kErr* bits
-    uint32_t pad2[30];
-    uint32_t hint0;    // top-k filter hint (value key) for first rows, from the latest finished row
-    uint32_t pad3[31];
+    uint32_t pad0[30];
+    uint32_t persist[32];   // [0] = kPersistTag when [1] holds a top-k filter hint for
+                            // rows of vocabulary [2] and top-k [3]
 };
-static_assert(sizeof(Ctrl) == 640, "Ctrl is five 128-byte lines");
+static_assert(sizeof(Ctrl) == 256, "Ctrl is two 128-byte lines");
 
-struct Task {
-    int32_t b, row, kind, aux;
-    int32_t st;       // the request's SPEC_ST_* bits so far
-    uint32_t base;    // the request's arrival count before this task (mod 2^kBaseBits)
+// A job: what the cluster does next for one slot.  Posted by the slot's
+// leader into every CTA's mailbox; 64 bytes.
+struct Job {
+    int b;             // request; kJobStop: the slot retires
+    int row;           // row index (meaning per kernel)
+    int kind;          // per kernel
+    int target;        // -1: every CTA streams its slice; else the one rank that works
+    int st;            // the request's SPEC_ST_* bits so far
+    uint32_t hint;     // per kernel (top-k filter hint, mask key)
+    int aux, aux2;     // per kernel
+    float f[4];        // per kernel
+    int depth;         // tree walks: the depth of the node the job reads
+    int pad[3];
 };
-// A pushed task's kind word: bits 0-7 the kernel's kind, 8-13 its slice
-// count, 14-31 its slice length / 64 (initial tasks have kind -1 and take
-// the call's first-row slicing).
-__host__ __device__ __forceinline__ int task_kind_base(int kind) { return kind & 0xff; }
-__host__ __device__ __forceinline__ int task_kind_pack(int base, int S, int SL) {
-    return (base & 0xff) | ((S & 63) << 8) | ((SL >> 6) << 14);
+static_assert(sizeof(Job) == 64, "Job is 64 bytes");
+constexpr int kJobStop = -1;
+constexpr int kJobDone = -2;       // returned by a combine: the request finished
+
+__device__ __forceinline__ Job make_job(int b, int row, int kind, int st) {
+    Job j;
+    j.b = b; j.row = row; j.kind = kind; j.target = -1; j.st = st; j.hint = 0; j.aux = 0; j.aux2 = 0;
+    j.f[0] = j.f[1] = j.f[2] = j.f[3] = 0.f;
+    j.depth = 0; j.pad[0] = j.pad[1] = j.pad[2] = 0;
+    return j;
 }
-__host__ __device__ __forceinline__ int task_kind_S(int kind) { return (kind >> 8) & 63; }
-__host__ __device__ __forceinline__ int task_kind_SL(int kind) { return ((kind >> 14) & 0x3ffff) << 6; }
+__device__ __forceinline__ Job job_done() { return make_job(kJobDone, 0, 0, 0); }
 
-struct ReqState {
-    float m;           // row maximum (logit), carried to a residual pass
-    float invZ;        // 1 / Z rounded to fp32: the residual pass and its rescan share it
-    double pad[7];
-};
-static_assert(sizeof(ReqState) == 64, "ReqState is 64 bytes");
-
-// Slice partial written to global scratch; `keys` follow the header.
+// Slice partial header (64 bytes); kernels append keys or bins after it.
 struct PartHdr {
     float vmax;        // slice maximum (over every element, NaN-propagating)
-    int32_t cnt;       // number of keys written
+    int32_t cnt;       // number of keys that follow
     uint32_t flags;    // kPf* bits
-    int32_t pad0;
+    int32_t tok;       // a token the slice found (argmax, a draw)
     uint64_t kth;      // top-k: the slice's filter as a composite key / argmax: best key
-    float2 sum;        // slice sum, float-float (meaning depends on the op)
+    float2 sum;        // slice sum, float-float (meaning per kernel)
     float2 sum2;
     float ly;          // chain: logit of the drafted token (slice holding it)
     float qy;          // chain: q of the drafted token (slice holding it)
-    uint64_t pad1[2];
+    uint32_t hasy;     // 1: this slice holds the drafted token
+    uint32_t pad1[3];
 };
 static_assert(sizeof(PartHdr) == 64, "PartHdr is 64 bytes");
 enum : uint32_t { kPfBad = 1u, kPfOverflow = 2u, kPfHinted = 4u };
 
-// Device view of the caller's workspace; offsets computed on the host.
+__device__ __forceinline__ const PartHdr* part_at(const unsigned char* parts, int pb, int r) {
+    return reinterpret_cast<const PartHdr*>(parts + static_cast<size_t>(r) * pb);
+}
+
+// Device view of the caller's workspace.
 struct Workspace {
     Ctrl* ctrl;
-    unsigned long long* urec;   // [maxu][2] pushed unit records, zero until pushed (zeroed per call)
-    uint32_t* counter;    // [B] arrivals per request, never reset within a call (zeroed per call)
-    ReqState* req;        // [B]
-    unsigned char* part;  // [B][S] partials, part_stride bytes each
-    unsigned char* extra; // [B] per-request op scratch, extra_stride bytes each
-    uint32_t* persist;    // 128 bytes kept across calls on the same workspace (not zeroed):
-                          // [0] = kPersistTag when [1] holds a top-k filter hint for rows
-                          // of vocabulary [2] and top-k [3]
-    uint32_t part_stride;
-    uint32_t maxt;
-    uint32_t maxu;
+    unsigned char* extra;   // [B] per-request op scratch, extra_stride bytes each
     uint64_t extra_stride;
-    int smax;             // partial slots per request
 };
 
-__device__ __forceinline__ PartHdr* part_hdr(const Workspace& W, int b, int s, int /*S*/) {
-    return reinterpret_cast<PartHdr*>(W.part + (static_cast<size_t>(b) * W.smax + s) * W.part_stride);
-}
-__device__ __forceinline__ uint64_t* part_keys(const Workspace& W, int b, int s, int S) {
-    return reinterpret_cast<uint64_t*>(part_hdr(W, b, s, S) + 1);
-}
-
-
-// ---------------------------------------------------------------------------
-// queue
-// ---------------------------------------------------------------------------
-// A pushed unit's record carries its whole task, so that a claimer needs no
-// further read and a push needs no fence when the task depends on nothing
-// else the pusher wrote.  w0: b + 1 (bits 0-21), row (22-34), slice (35-40),
-// st (41-45), base (46-62), and bit 63 when the push released earlier writes
-// (the claimer then acquires); w1: the packed kind (low word), aux (high
-// word).  Both words are nonzero once written (b + 1 >= 1; the kind word
-// holds S >= 1).
-constexpr int kBaseBits = 17;
-constexpr unsigned long long kRecAcquire = 1ull << 63;
-constexpr uint32_t kBaseMask = (1u << kBaseBits) - 1u;
-constexpr int kMaxRecB = (1 << 22) - 2;     // requests per call
-constexpr int kMaxRecRow = (1 << 13) - 1;   // row (or node) index
-__device__ __forceinline__ void rec_encode(const Task& t, int slice, bool release, unsigned long long& w0,
-                                           unsigned long long& w1) {
-    w0 = static_cast<unsigned long long>(static_cast<uint32_t>(t.b + 1) & 0x3fffffu) |
-         (static_cast<unsigned long long>(static_cast<uint32_t>(t.row) & 0x1fffu) << 22) |
-         (static_cast<unsigned long long>(static_cast<uint32_t>(slice) & 63u) << 35) |
-         (static_cast<unsigned long long>(static_cast<uint32_t>(t.st) & 31u) << 41) |
-         (static_cast<unsigned long long>(t.base & kBaseMask) << 46) | (release ? kRecAcquire : 0ull);
-    w1 = static_cast<unsigned long long>(static_cast<uint32_t>(t.kind)) |
-         (static_cast<unsigned long long>(static_cast<uint32_t>(t.aux)) << 32);
-}
-__device__ __forceinline__ void rec_decode(unsigned long long w0, unsigned long long w1, Task& t, int& slice) {
-    t.b = static_cast<int>(w0 & 0x3fffffu) - 1;
-    t.row = static_cast<int>((w0 >> 22) & 0x1fffu);
-    slice = static_cast<int>((w0 >> 35) & 63u);
-    t.st = static_cast<int>((w0 >> 41) & 31u);
-    t.base = static_cast<uint32_t>(w0 >> 46) & kBaseMask;
-    t.kind = static_cast<int>(static_cast<uint32_t>(w1));
-    t.aux = static_cast<int>(static_cast<uint32_t>(w1 >> 32));
-}
-
-struct Claimed {
-    Task task;
-    int slice;
-    int ok;
-    uint32_t hint;     // a kernel-specific word the producer fetched with the claim
-    int pad;
+// Launch geometry every kernel's argument block carries (host-computed).
+struct EngArgs {
+    Workspace W;
+    int stages;        // ring stages, 2..kStages
+    int C;             // CTAs per cluster (the launch's cluster size)
+    int R;             // slots per cluster
+    int SL;            // slice length in elements (a multiple of 64)
+    int part_bytes;    // bytes of one partial (header + payload), multiple of 16
+    int own;           // slots one CTA leads at most: ceil(R / C)
 };
 
-// The producer's claim of the next unit (one thread).  First rows first
-// (the initial units: row 0 of every request, S0 slices each): every
-// request's chain starts as early as it can.  Then pushed tasks (rows that
-// follow an accepted row, residual passes, retries) in push order, S1
-// slices each; a claimer that finds none pushed yet takes the next pushed
-// unit and waits (bounded) for its task, or for every request to finish.
-// `cold` caches whether initial units may be left.
-constexpr uint32_t kNoPre = 0xffffffffu;
-__device__ inline Claimed claim_unit(const Workspace& W, int B, int S0, bool& cold, uint32_t& pre) {
-    Claimed c;
-    c.ok = 1;
-    c.hint = 0;
-    c.pad = 0;
-    c.task.b = 0; c.task.row = 0; c.task.kind = -1; c.task.aux = 0; c.task.st = 0; c.task.base = 0;
-    if (cold) {
-        const uint32_t u0 = pre != kNoPre ? pre : atomicAdd(&W.ctrl->head, 1u);
-        pre = kNoPre;
-        if (u0 < static_cast<uint32_t>(B) * static_cast<uint32_t>(S0)) {
-            c.slice = static_cast<int>(u0 % static_cast<uint32_t>(S0));
-            c.task.b = static_cast<int>(u0 / static_cast<uint32_t>(S0));
-            return c;
-        }
-        cold = false;
-    }
-    const uint32_t u = atomicAdd(&W.ctrl->head1, 1u);
-    if (u >= W.maxu) { c.ok = 0; return c; }
+// cluster geometry of a launch, the same in every CTA but for the rank
+struct Geo {
+    int stages;        // ring stages
+    int C;             // CTAs per cluster
+    int R;             // slots per cluster
+    int rank;          // this CTA's rank
+    int SL;            // slice length in elements (a multiple of 64)
+    int part_bytes;    // bytes of one partial slot (header + keys), multiple of 16
+    int own;           // ceil(R / C)
+};
+__device__ __forceinline__ Geo make_geo(const EngArgs& E) {
+    Geo g;
+    g.C = static_cast<int>(cluster_size());
+    g.rank = static_cast<int>(cluster_rank());
+    g.R = E.R; g.SL = E.SL; g.part_bytes = E.part_bytes; g.own = E.own; g.stages = E.stages;
+    return g;
+}
+__device__ __forceinline__ int slice_x0(const Geo& g, int r) { return r * g.SL; }
+__device__ __forceinline__ int slice_x1(const Geo& g, int r, int V) { return min(V, (r + 1) * g.SL); }
+
+// ---------------------------------------------------------------------------
+// shared memory of the engine (every kernel's smem starts with the ring,
+// then this block)
+// ---------------------------------------------------------------------------
+struct QEnt {
+    Job job;
+    int slot;
+    int pad[3];
+};
+static_assert(sizeof(QEnt) == 80, "QEnt is 80 bytes");
+struct EngSmem {
+    uint64_t full[kStages];      // count 1: producer's expect_tx + the copies' bytes
+    uint64_t empty[kStages];     // count kWarps: one arrive per consumer warp
+    uint64_t qfull[kQ];          // count 1: producer posted a queue entry
+    uint64_t qempty[kQ];         // count kWarps: every consumer warp read it
+    uint64_t jfull[kMaxSlots];   // count 1: the slot's leader posted a job (remote arrive)
+    uint64_t parr[kMaxOwn];      // count C: the partials of an own slot arrived (remote arrives)
+    Job jd[kMaxSlots];           // mailboxes, written by the leaders
+    QEnt q[kQ];
+    int abort;                   // a wait in this CTA gave up
+    int pad[3];
+};
+
+// ---------------------------------------------------------------------------
+// bounded waits
+// ---------------------------------------------------------------------------
+// Spin on test(), with backoff, up to kMbarLimitNs; also gives up when the
+// CTA aborted or another CTA raised the workspace error.  false: gave up.
+template <class T>
+__device__ __forceinline__ bool bounded_wait(T test, volatile int* abort, const Ctrl* ctrl) {
+    if (test()) return true;
+    unsigned long long t0 = globaltimer_ns();
     uint32_t ns = 32;
-    SPEC_TRACE_EV(10, -1, -1, -1, static_cast<int>(u));
     for (uint32_t it = 0;; ++it) {
-        // one round trip a poll: the record and the stop conditions together
-        unsigned long long w0, w1;
-        ld_relaxed_v2(W.urec + 2ull * u, w0, w1);
-        const uint32_t fin = ld_relaxed(&W.ctrl->done);
-        const uint32_t err = ld_relaxed(&W.ctrl->error);
-        if (w0 != 0ull && w1 != 0ull) {
-            if (w0 & kRecAcquire) fence_acq_rel_gpu();   // pairs with the pusher's release
-            rec_decode(w0, w1, c.task, c.slice);
-            return c;
+        if (test()) return true;
+        if (*abort) return false;
+        if ((it & 15u) == 15u) {
+            if (ld_relaxed(&ctrl->error) != 0u) return false;
+            if (globaltimer_ns() - t0 > kMbarLimitNs) return false;
         }
-        if (fin >= static_cast<uint32_t>(B)) { c.ok = 0; return c; }
-        if (err != 0) { c.ok = 0; return c; }   // another CTA gave up
-        if (it >= kWaitLimit) { atomicOr(&W.ctrl->error, kErrWait); c.ok = 0; return c; }
         nanosleep_ns(ns);
         if (ns < 256) ns <<= 1;
     }
 }
-
-// Combiner warp: count the arrival of a finished unit (its partial was
-// written by the consumers, ordered before the job hand-over).  Returns
-// true in every lane when the unit completed the task's last slice; this
-// CTA's combiner then owns the combine.  A request has one task in flight,
-// and its counter only grows: the task's arrivals are those past its base,
-// and the last one's count is the base of the request's next task.
-__device__ __forceinline__ bool comb_arrive(const Workspace& W, const Task& t, int S, uint32_t* done_est,
-                                            uint32_t* next_base) {
-    int last = 0;
-    uint32_t dn = 0, nb = 0;
-    if ((threadIdx.x & 31) == 0) {
-        fence_acq_rel_gpu();   // release the partial (cumulative over the hand-over)
-        const uint32_t prev = atomicAdd(&W.counter[t.b], 1u);
-        dn = ld_relaxed(&W.ctrl->done);   // (for the next row's slicing; not ordered)
-        nb = (prev + 1u) & kBaseMask;
-        last = (((prev + 1u - t.base) & kBaseMask) == static_cast<uint32_t>(S));
-        if (last) fence_acq_rel_gpu();   // acquire the other slices' partials
-    }
-    if (done_est) *done_est = __shfl_sync(0xffffffffu, dn, 0);
-    if (next_base) *next_base = __shfl_sync(0xffffffffu, nb, 0);
-    return __shfl_sync(0xffffffffu, last, 0) != 0;
-}
-
-// One lane: enqueue the request's next task, cut into S slices of SL
-// elements.  One 64-bit atomic reserves a task count (bounded by the
-// workspace) and S unit records; each record carries the whole task.
-__device__ __forceinline__ void push_task(const Workspace& W, Task t, int S, int SL, bool release) {
-    t.kind = task_kind_pack(t.kind, S, SL);
-    const unsigned long long r = atomicAdd(&W.ctrl->tailc, (1ull << 32) | static_cast<unsigned long long>(S));
-    const uint32_t ti = static_cast<uint32_t>(r >> 32), u0 = static_cast<uint32_t>(r);
-    if (ti >= W.maxt || u0 + static_cast<uint32_t>(S) > W.maxu) { atomicOr(&W.ctrl->error, kErrQueue); return; }
-    // release: the task's units or combine read what the pusher wrote
-    // before (request state beyond the record)
-    if (release) fence_acq_rel_gpu();
-    for (int s = 0; s < S; ++s) {
-        unsigned long long w0, w1;
-        rec_encode(t, s, release, w0, w1);
-        st_relaxed_v2(W.urec + 2ull * (u0 + s), w0, w1);
-    }
-}
-
-// Slices of a pushed row: a first row's while most requests are active;
-// finer as requests finish, so that the remaining chains keep the grid busy
-// (at most smax).  done = finished requests (an estimate).
-#ifndef SPEC_SLICE_FACTOR
-#define SPEC_SLICE_FACTOR 2   // pushed units per CTA when every active request has one row queued
-#endif
-__device__ __forceinline__ void pick_slices(int B, int V, int S0, int smax, uint32_t done, int& S, int& SL) {
-    const int active = B - static_cast<int>(done) > 1 ? B - static_cast<int>(done) : 1;
-    int s = (SPEC_SLICE_FACTOR * static_cast<int>(gridDim.x) + active - 1) / active;
-    if (s < S0) s = S0;
-    if (s > smax) s = smax;
-    SL = (((V + s - 1) / s) + 63) & ~63;
-    S = (V + SL - 1) / SL;
-}
-
-// Combiner lane 0, after the request's outputs are written by the warp.
-// The count only tells claimers when to stop; the outputs are read after
-// the kernel.
-__device__ __forceinline__ void finish_request(const Workspace& W) {
-    atomicAdd(&W.ctrl->done, 1u);
+__device__ __forceinline__ void raise_abort(volatile int* abort, Ctrl* ctrl) {
+    *abort = 1;
+    atomicOr(&ctrl->error, kErrWait);
 }
 
 // ---------------------------------------------------------------------------
-// the producer / consumer pipeline of one CTA
+// what a CTA streams for a job
 // ---------------------------------------------------------------------------
-// A finished unit handed from the consumers to the combiner warp.
-struct Job {
-    Task task;       // as claimed (kind -1: an initial task)
-    int slice;
-    int kind;        // the unit's resolved kind
-    int stop;        // no more jobs: the combiner leaves
-    uint32_t flags;  // kernel-specific
-};
-constexpr int kJobs = 4;
-
-// Warp kWarps (the producer) claims units, publishes each unit's descriptor
-// through a two-slot queue, and streams the unit's chunks HBM -> shared
-// memory with 1-D TMA bulk copies into a kStages ring.  The kWarps consumer
-// warps take descriptors in order, wait for each chunk's `full` barrier,
-// process it, and release the stage with one arrive per warp on its `empty`
-// barrier; no consumer ever waits for another consumer while streaming.  The
-// producer runs ahead by up to one unit, so a unit's claim and first bytes
-// overlap the previous unit's tail, finish and combine.  Every wait is
-// bounded; a timeout raises the CTA's abort flag and the workspace error.
-struct Pipe {
-    unsigned char* buf;    // kStages * kChunkBytes, 128-byte aligned
-    uint64_t* full;        // [kStages] count 1: producer's expect_tx + the copies' bytes
-    uint64_t* empty;       // [kStages] count kWarps: one arrive per consumer warp
-    uint64_t* ufull;       // [2] count 1: descriptor published
-    uint64_t* uempty;      // [2] count kWarps: descriptor read
-    Claimed* desc;         // [2]
-    uint64_t* jfull;       // [kJobs] count 1: job posted by consumer thread 0
-    uint64_t* jempty;      // [kJobs] count 1: job taken by the combiner
-    Job* jobs;             // [kJobs]
-    uint64_t* cready;
-    uint64_t* cdone;
-    volatile int* cflag;
-    volatile int* abort;   // a wait timed out in this CTA
-    __device__ __forceinline__ unsigned char* slot(int s) const { return buf + s * kChunkBytes; }
-};
-
-// shared-memory control block of the pipe (part of every kernel's smem)
-struct PipeSmem {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t ufull[2];
-    uint64_t uempty[2];
-    uint64_t jfull[kJobs];
-    uint64_t jempty[kJobs];
-    uint64_t cready;       // count 1: the combiner prepared a combine for the consumers
-    uint64_t cdone;        // count 1: the consumers finished it
-    Claimed desc[2];
-    Job jobs[kJobs];
-    int abort;
-    int cflag;             // consumer thread 0's poll result, broadcast
-    int pad[2];
-};
-
-// all kBlockThreads threads, once at kernel start
-__device__ inline Pipe pipe_init(unsigned char* ring, PipeSmem& ps) {
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&ps.full[s], 1);
-            mbar_init(&ps.empty[s], kWarps);
-        }
-        for (int j = 0; j < 2; ++j) {
-            mbar_init(&ps.ufull[j], 1);
-            mbar_init(&ps.uempty[j], kWarps);
-        }
-        for (int j = 0; j < kJobs; ++j) {
-            mbar_init(&ps.jfull[j], 1);
-            mbar_init(&ps.jempty[j], 1);
-        }
-        mbar_init(&ps.cready, 1);
-        mbar_init(&ps.cdone, 1);
-        ps.abort = 0;
-        fence_mbar_init();
-    }
-    __syncthreads();
-    Pipe P;
-    P.buf = ring;
-    P.full = ps.full; P.empty = ps.empty; P.ufull = ps.ufull; P.uempty = ps.uempty;
-    P.desc = ps.desc;
-    P.jfull = ps.jfull; P.jempty = ps.jempty; P.jobs = ps.jobs;
-    P.cready = &ps.cready; P.cdone = &ps.cdone; P.cflag = &ps.cflag;
-    P.abort = &ps.abort;
-    return P;
-}
-
-// What one unit streams: one row range (logits or q), or a logits range and
-// the fp32 q range beside it in the same stages (the residual pass).
+// One row range (logits or q), or a logits range and the fp32 q range
+// beside it in the same stages (the residual pass).
 struct StreamPlan {
     const unsigned char* src0;   // element x0 of stream 0
     const unsigned char* src1;   // element x0 of stream 1 (fp32), or null
     int es0;                     // element bytes of stream 0
     int n;                       // elements
     int ce;                      // elements per chunk
-    int nch;                     // chunks (0: the unit streams nothing)
+    int nch;                     // chunks (0: the job streams nothing here)
 };
 __device__ __forceinline__ StreamPlan plan_none() {
     StreamPlan p;
@@ -465,6 +242,17 @@ __device__ __forceinline__ StreamPlan plan_dual(const void* lrow, int es, const 
     return p;
 }
 
+// The ring as the consumers and the producer see it.
+struct Pipe {
+    unsigned char* buf;    // stages * kChunkBytes, 128-byte aligned
+    uint64_t* full;
+    uint64_t* empty;
+    volatile int* abort;
+    Ctrl* ctrl;
+    uint32_t stages;
+    __device__ __forceinline__ unsigned char* slot(int s) const { return buf + s * kChunkBytes; }
+};
+
 // Producer lane: issue chunk c of plan p into stage s.  Bytes past the
 // largest 16-byte multiple of each range are not copied (the consumers read
 // them from global memory).
@@ -476,169 +264,6 @@ __device__ __forceinline__ void issue_chunk(const Pipe& P, const StreamPlan& p, 
     unsigned char* dst = P.slot(s);
     if (b0) tma_load_1d(dst, p.src0 + static_cast<long long>(c) * p.ce * p.es0, b0, &P.full[s]);
     if (b1) tma_load_1d(dst + p.ce * p.es0, p.src1 + static_cast<long long>(c) * p.ce * 4, b1, &P.full[s]);
-}
-
-// The producer warp's loop (lane 0 only).  `fetch(c)` may fill c.hint;
-// `plan(c)` returns the unit's StreamPlan (tma: issue the chunks; otherwise
-// the consumers copy them themselves).
-template <class Fetch, class PlanF>
-__device__ void producer_loop(const Workspace& W, int B, int S0, const Pipe& P, bool tma, Fetch fetch,
-                              PlanF plan) {
-    uint32_t seq = 0;          // chunks issued so far (ring sequence number)
-    bool dead = false;
-    bool cold = true;          // initial units may be left
-    uint32_t pre = kNoPre;     // the next initial unit, taken while the current one streams
-    for (uint32_t u = 0;; ++u) {
-        const int j = u & 1;
-        if (u >= 2 && !mbar_wait(&P.uempty[j], ((u >> 1) - 1) & 1u)) dead = true;
-        Claimed c;
-        if (dead || *P.abort) {
-            c.ok = 0; c.slice = 0; c.hint = 0; c.pad = 0;
-            c.task.b = 0; c.task.row = 0; c.task.kind = 0; c.task.aux = 0; c.task.st = 0; c.task.base = 0;
-        } else {
-            SPEC_TRACE_EV1(14, -1, -1, -1, static_cast<int>(u));
-            c = claim_unit(W, B, S0, cold, pre);
-            if (c.ok) fetch(c);
-            SPEC_TRACE_EV1(13, c.task.b, c.task.row, c.slice, c.ok);
-        }
-        P.desc[j] = c;
-        mbar_arrive(&P.ufull[j]);
-        if (!c.ok) break;
-        if (!tma) continue;
-        const StreamPlan p = plan(c);
-        for (int ci = 0; ci < p.nch; ++ci, ++seq) {
-            const int s = static_cast<int>(seq % kStages);
-            if (seq >= static_cast<uint32_t>(kStages) && !mbar_wait(&P.empty[s], ((seq / kStages) - 1) & 1u)) {
-                dead = true;
-                break;
-            }
-            if (*P.abort) { dead = true; break; }
-            issue_chunk(P, p, ci, s);
-            // initial units are independent of every push: take the next one now,
-            // its round trip overlaps this unit
-            if (ci == 0 && cold && pre == kNoPre) pre = atomicAdd(&W.ctrl->head, 1u);
-        }
-        if (dead) {
-            // unblock consumers waiting for a descriptor, then stop
-            *P.abort = 1;
-            atomicOr(&W.ctrl->error, kErrWait);
-        }
-    }
-    if (dead || *P.abort) {
-        // wait (bounded) for the copies still in flight before the CTA can end
-        const uint32_t first = seq > static_cast<uint32_t>(kStages) ? seq - kStages : 0u;
-        for (uint32_t q = first; q < seq; ++q) mbar_wait(&P.full[q % kStages], (q / kStages) & 1u);
-    }
-}
-
-// Consumers (all threads): wait until thread 0's poll() reports done,
-// serving the combines the combiner warp prepares meanwhile (serve() runs
-// on every consumer thread; thread 0 then signals cdone).  `cseq` counts
-// the combines served.  Every wait is bounded; false on a timeout or abort.
-template <class Poll, class Serve>
-__device__ bool consumer_wait(const Pipe& P, uint32_t& cseq, Poll poll, Serve serve) {
-    unsigned long long t0 = 0;
-    uint32_t ns = 0;
-    for (uint32_t it = 0;; ++it) {
-        if (threadIdx.x == 0) {
-            int f = poll() ? 1 : 0;
-            if (mbar_test(P.cready, cseq & 1u)) f |= 2;
-            if (*P.abort) f |= 4;
-            if ((it & 63u) == 63u) {
-                const unsigned long long now = globaltimer_ns();
-                if (t0 == 0) t0 = now;
-                else if (now - t0 > kMbarLimitNs) f |= 4;
-            }
-            *P.cflag = f;
-        }
-        csync();
-        const int f = *P.cflag;
-        csync();   // every thread read the flag before thread 0 writes it again
-        if (f & 2) {
-            serve();
-            csync();
-            if (threadIdx.x == 0) mbar_arrive(P.cdone);
-            ++cseq;
-            ns = 0;
-        }
-        if (f & 1) return true;
-        if (f & 4) { if (threadIdx.x == 0) *P.abort = 1; return false; }
-        if (!(f & 2)) {
-            if (ns) nanosleep_ns(ns);
-            ns = ns ? (ns < 256 ? ns * 2 : ns) : 32;
-        }
-    }
-}
-
-// Combiner warp: hand the prepared combine number `cpub` to the consumers
-// and go back to arrivals; the combine's shared memory stays theirs until
-// combine_reuse().
-__device__ inline void publish_combine(const Pipe& P, uint32_t& cpub) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(P.cready);
-    ++cpub;
-}
-
-// Combiner warp: before writing the combine's shared memory again, wait
-// (bounded) until the consumers finished the last published combine.
-__device__ inline bool combine_reuse(const Pipe& P, uint32_t cpub) {
-    if (cpub == 0) return true;
-    if (*P.abort) return false;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(P.cdone, (cpub - 1) & 1u));
-    if (!ok) *P.abort = 1;
-    return ok;
-}
-
-// Consumers: the next unit's descriptor.  ok = 0 ends the consumer loop
-// (every request finished, the queue closed, or an abort).
-template <class Serve>
-__device__ __forceinline__ Claimed next_unit(const Pipe& P, uint32_t u, uint32_t& cseq, Serve serve) {
-    const int j = u & 1;
-    const bool got = consumer_wait(P, cseq, [&]() { return mbar_test(&P.ufull[j], (u >> 1) & 1u); }, serve);
-    Claimed c = P.desc[j];
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&P.uempty[j]);
-    if (!got || *P.abort) c.ok = 0;
-    return c;
-}
-
-// Consumers (all threads): hand a finished unit (or the stop job) to the
-// combiner warp, after a csync() that ordered every consumer's partial
-// writes before it.  `jseq` counts the jobs posted so far.
-template <class Serve>
-__device__ inline void post_job(const Pipe& P, uint32_t& jseq, uint32_t& cseq, const Job& j, Serve serve) {
-    const int s = static_cast<int>(jseq % kJobs);
-    const uint32_t par = ((jseq / kJobs) - 1) & 1u;
-    const bool ok = consumer_wait(P, cseq, [&]() {
-        if (jseq >= static_cast<uint32_t>(kJobs) && !mbar_test(&P.jempty[s], par)) return false;
-        P.jobs[s] = j;
-        mbar_arrive(&P.jfull[s]);
-        return true;
-    }, serve);
-    if (ok) ++jseq;
-}
-
-// The combiner warp's loop: take jobs in order until the stop job (or a
-// timed-out wait).  on_job(job) runs on all 32 lanes; on_stop() runs before
-// the stop job is marked taken (the consumers leave once it is), so that
-// whatever the combiner handed them is finished first.
-template <class F, class G>
-__device__ void combiner_loop(const Pipe& P, F on_job, G on_stop) {
-    for (uint32_t j = 0;; ++j) {
-        const int s = static_cast<int>(j % kJobs);
-        const bool got = __all_sync(0xffffffffu, mbar_wait(&P.jfull[s], (j / kJobs) & 1u));
-        const Job job = P.jobs[s];
-        if (got && job.stop) on_stop();
-        __syncwarp();
-        if ((threadIdx.x & 31) == 0) mbar_arrive(&P.jempty[s]);
-        if (!got) { *P.abort = 1; return; }
-        if (job.stop) return;
-        on_job(job);
-    }
-}
-template <class F>
-__device__ void combiner_loop(const Pipe& P, F on_job) {
-    combiner_loop(P, on_job, []() {});
 }
 
 // ---------------------------------------------------------------------------
@@ -678,9 +303,10 @@ static_assert(kChunkVecs % kThreads == 0, "a full chunk is a whole number of rou
 // nothing in that mode).
 __device__ __forceinline__ bool take_chunk(const Pipe& P, uint32_t seq, bool tma, bool& dead,
                                            const StreamPlan& p, int c) {
-    const int s = static_cast<int>(seq % kStages);
+    const int s = static_cast<int>(seq % P.stages);
     if (tma) {
-        const bool ok = !dead && mbar_wait(&P.full[s], (seq / kStages) & 1u);
+        const uint32_t par = (seq / P.stages) & 1u;
+        const bool ok = !dead && bounded_wait([&]() { return mbar_test(&P.full[s], par); }, P.abort, P.ctrl);
         dead = !__all_sync(0xffffffffu, ok);   // warp-uniform from here on
         if (dead) *P.abort = 1;
         return !dead;
@@ -709,20 +335,19 @@ __device__ __forceinline__ bool take_chunk(const Pipe& P, uint32_t seq, bool tma
 __device__ __forceinline__ void release_chunk(const Pipe& P, uint32_t seq, bool tma, bool dead) {
     if (!tma || dead) return;
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&P.empty[seq % kStages]);
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&P.empty[seq % P.stages]);
 }
 
 // Stream one row range (plan from plan_single) through fn.  Returns false
-// (in every consumer thread) when a chunk wait timed out; the caller then
-// leaves the kernel.  `seq` is the consumer's ring sequence number.
+// (in every consumer thread) when a chunk wait gave up.  `seq` is the
+// consumer's ring sequence number.
 template <class E, class Fn>
 __device__ bool consume_row(const Pipe& P, uint32_t& seq, const StreamPlan& p, bool tma, int x0, Fn& fn) {
     constexpr int VEC = E::kVec;
     bool dead = false;
     for (int c = 0; c < p.nch; ++c, ++seq) {
         const bool have = take_chunk(P, seq, tma, dead, p, c);
-        if (c == 0) SPEC_TRACE_EV(15, -1, -1, -1, p.nch);
-        const unsigned char* sm = P.slot(static_cast<int>(seq % kStages));
+        const unsigned char* sm = P.slot(static_cast<int>(seq % P.stages));
         const int ne = min(p.ce, p.n - c * p.ce);
         const int cx0 = x0 + c * p.ce;
         const int nv = (ne * E::kBytes) >> 4;
@@ -785,7 +410,7 @@ __device__ bool consume_row2(const Pipe& P, uint32_t& seq, const StreamPlan& p, 
     bool dead = false;
     for (int c = 0; c < p.nch; ++c, ++seq) {
         const bool have = take_chunk(P, seq, tma, dead, p, c);
-        const unsigned char* sm = P.slot(static_cast<int>(seq % kStages));
+        const unsigned char* sm = P.slot(static_cast<int>(seq % P.stages));
         const int ne = min(p.ce, p.n - c * p.ce);
         const int cx0 = x0 + c * p.ce;
         const int qoff = p.ce * E::kBytes;
@@ -891,135 +516,10 @@ __device__ int cta_icdf(int x0, int x1, dfloat t, W& w, float2* red, int* ired) 
     return last_pos >= 0 ? last_pos : x0;
 }
 
-// Every slice header of a task, in shared memory.
-struct SliceHdrs {
-    int cnt[kMaxSlices];
-    int off[kMaxSlices + 1];     // exclusive prefix of cnt
-    uint32_t flags[kMaxSlices];
-    float vmax[kMaxSlices];
-    uint64_t kth[kMaxSlices];
-    float2 sum[kMaxSlices];
-    float2 sum2[kMaxSlices];
-    float ly[kMaxSlices];
-    float qy[kMaxSlices];
-};
-
-// Combiner warp: lane s loads slice s's header (one round trip), offsets by
-// a warp scan.  With `list`, the same round trip also fetches each slice's
-// first keys into list[off_s ..] (speculatively: the slot always holds room
-// for 2 * kPreKeys of them): kPreKeys per slice, or twice that when S <= 16
-// (lane 16 + s fetches slice s's second kPreKeys).  Returns the keys per
-// slice already in list (0 without list); gather_all_w fetches the rest.
-constexpr int kPreKeys = 16;
-__device__ inline int load_hdrs_w(const Workspace& W, int b, int S, SliceHdrs& H, uint64_t* list = nullptr,
-                                  int cap = 0) {
-    const int l = threadIdx.x & 31;
-    const bool two = list && S <= 16;
-    const int ps = two ? (l & 15) : l;              // the slice whose keys this lane fetches
-    const int k0 = (two && l >= 16) ? kPreKeys : 0; // its first key
-    const bool fetch = list && ps < S;
-    int c = 0;
-    ulonglong2 kp[kPreKeys / 2];
-    if (fetch) {
-        const ulonglong2* src = reinterpret_cast<const ulonglong2*>(part_keys(W, b, ps, S) + k0);   // 16-byte aligned
-#pragma unroll
-        for (int j = 0; j < kPreKeys / 2; ++j) kp[j] = __ldcg(src + j);
-    }
-    if (l < S) {
-        const PartHdr* h = part_hdr(W, b, l, S);
-        c = __ldcg(&h->cnt);
-        H.cnt[l] = c;
-        H.flags[l] = __ldcg(&h->flags);
-        H.vmax[l] = __ldcg(&h->vmax);
-        H.kth[l] = __ldcg(&h->kth);
-        H.sum[l] = __ldcg(&h->sum);
-        H.sum2[l] = __ldcg(&h->sum2);
-        H.ly[l] = __ldcg(&h->ly);
-        H.qy[l] = __ldcg(&h->qy);
-    }
-    int tot;
-    const int off = warp_exscan_i(c, tot);
-    if (l < S) H.off[l] = off;
-    if (l == 0) H.off[S] = tot;
-    const int cs = __shfl_sync(0xffffffffu, c, ps & 31);     // the fetched slice's count and offset
-    const int os = __shfl_sync(0xffffffffu, off, ps & 31);
-    if (fetch) {
-#pragma unroll
-        for (int j = 0; j < kPreKeys / 2; ++j) {
-            const int a = k0 + 2 * j;
-            if (a < cs && os + a < cap) list[os + a] = kp[j].x;
-            if (a + 1 < cs && os + a + 1 < cap) list[os + a + 1] = kp[j].y;
-        }
-    }
-    __syncwarp();
-    return list ? (two ? 2 * kPreKeys : kPreKeys) : 0;
-}
-
-// Combiner warp: every slice key that keep(key) accepts into list[0..return)
-// (order arbitrary); `oflow` when more than cap were accepted.  Each lane
-// loads 8 keys per pass, all independent.
-template <class F>
-__device__ inline int gather_keys_w(const Workspace& W, int b, int S, const SliceHdrs& H, F keep,
-                                    uint64_t* list, int cap, bool& oflow) {
-    constexpr int U = 8;
-    const int l = threadIdx.x & 31;
-    const uint32_t lt = (1u << l) - 1u;
-    const int total = H.off[S];
-    int out = 0;
-    int s = 0;   // slice of this lane's current key (its keys come in increasing order)
-    for (int f0 = 0; f0 < total; f0 += 32 * U) {
-        uint64_t key[U];
-#pragma unroll
-        for (int j = 0; j < U; ++j) {
-            const int f = f0 + j * 32 + l;
-            key[j] = 0;
-            if (f < total) {
-                while (s + 1 < S && H.off[s + 1] <= f) ++s;
-                key[j] = __ldcg(part_keys(W, b, s, S) + (f - H.off[s]));
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < U; ++j) {
-            const int f = f0 + j * 32 + l;
-            const bool p = f < total && keep(key[j]);
-            const uint32_t bal = __ballot_sync(0xffffffffu, p);
-            if (p) {
-                const int pos = out + __popc(bal & lt);
-                if (pos < cap) list[pos] = key[j];
-            }
-            out += __popc(bal);
-        }
-    }
-    oflow = out > cap;
-    __syncwarp();
-    return out < cap ? out : cap;
-}
-
-// Combiner warp: every key of every slice into list[H.off[s] ..] (lane s
-// copies slice s; its loads are independent, 8 in flight).  Returns the
-// count (at most cap; `oflow` when more).
-__device__ inline int gather_all_w(const Workspace& W, int b, int S, const SliceHdrs& H, uint64_t* list,
-                                   int cap, bool& oflow, int first = 0) {
-    const int l = threadIdx.x & 31;
-    const int total = H.off[S];
-    oflow = total > cap;
-    if (l < S) {
-        const int c = H.cnt[l], o = H.off[l];
-        const uint64_t* src = part_keys(W, b, l, S);
-        for (int j0 = first; j0 < c; j0 += 8) {
-            uint64_t key[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) key[j] = (j0 + j < c) ? __ldcg(src + j0 + j) : 0ull;
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (j0 + j < c && o + j0 + j < cap) list[o + j0 + j] = key[j];
-        }
-    }
-    __syncwarp();
-    return total < cap ? total : cap;
-}
-
-// Combiner warp: keep list[i] with value key >= t, in place, order kept.
+// ---------------------------------------------------------------------------
+// warp-level key selection over a shared-memory list (combiner warp)
+// ---------------------------------------------------------------------------
+// Keep list[i] with value key >= t, in place, order kept.
 __device__ inline int compact_w(uint64_t* list, int n, uint32_t t) {
     const int l = threadIdx.x & 31;
     const uint32_t lt = (1u << l) - 1u;
@@ -1036,14 +536,35 @@ __device__ inline int compact_w(uint64_t* list, int n, uint32_t t) {
     __syncwarp();
     return out;
 }
+// the same on the full 64-bit key
+__device__ inline int compact_key_w(uint64_t* list, int n, uint64_t t) {
+    const int l = threadIdx.x & 31;
+    const uint32_t lt = (1u << l) - 1u;
+    int out = 0;
+    for (int i0 = 0; i0 < n; i0 += 32) {
+        const int i = i0 + l;
+        uint64_t key = 0;
+        bool p = false;
+        if (i < n) { key = list[i]; p = key >= t; }
+        const uint32_t bal = __ballot_sync(0xffffffffu, p);
+        if (p) list[out + __popc(bal & lt)] = key;
+        out += __popc(bal);
+    }
+    __syncwarp();
+    return out;
+}
 
-// Combiner warp: the value key of the k-th largest key of list[0..n)
-// (n >= k), by bisection over value keys (one warp reduction a step).
+// The value key of the k-th largest key of list[0..n) (n >= k), by
+// bisection over value keys (one warp reduction a step).
 __device__ inline uint32_t kth_value_w(const uint64_t* list, int n, int k) {
     const int l = threadIdx.x & 31;
-    uint32_t mx = 0;
-    for (int i = l; i < n; i += 32) mx = max(mx, static_cast<uint32_t>(list[i] >> 32));
-    uint32_t lo = 0, hi = warp_max_u32(mx);
+    uint32_t mx = 0, mn = 0xffffffffu;
+    for (int i = l; i < n; i += 32) {
+        const uint32_t h = static_cast<uint32_t>(list[i] >> 32);
+        mx = max(mx, h);
+        mn = min(mn, h);
+    }
+    uint32_t lo = warp_min_u32(mn), hi = warp_max_u32(mx);
     while (lo < hi) {
         const uint32_t mid = lo + static_cast<uint32_t>((static_cast<uint64_t>(hi) - lo + 1) >> 1);
         int c = 0;
@@ -1054,8 +575,8 @@ __device__ inline uint32_t kth_value_w(const uint64_t* list, int n, int k) {
     return lo;
 }
 
-// Combiner warp: the largest composite key t with at least k keys of
-// list[0..n) >= t (the exact k-th largest key; n >= k).
+// The largest composite key t with at least k keys of list[0..n) >= t (the
+// exact k-th largest key; n >= k).
 __device__ inline uint64_t kth_key_w(const uint64_t* list, int n, int k) {
     const int l = threadIdx.x & 31;
     const uint32_t v = kth_value_w(list, n, k);
@@ -1070,5 +591,261 @@ __device__ inline uint64_t kth_key_w(const uint64_t* list, int n, int k) {
     }
     return lo;
 }
+
+// ---------------------------------------------------------------------------
+// the engine
+// ---------------------------------------------------------------------------
+// An Op provides (all device functions, every argument by const reference
+// where it can):
+//   using Args;  struct Smem (its own shared memory, after EngSmem)
+//   int  R(A), ...                          (host side: see the kernel files)
+//   Job  first(A, G, b, sm)                 combiner warp: the first job of
+//                                           request b, or kJobDone when it
+//                                           finishes without reading a row
+//   StreamPlan plan(A, G, job)              producer: what this CTA streams
+//   bool tma(A)                             TMA or plain loads
+//   int  consume(A, G, P, seq, job, sm, out)   consumers: process this CTA's
+//                                           part of the job, write the partial
+//                                           (header + payload) to `out`; returns
+//                                           its byte count (multiple of 16), or
+//                                           -1 when a wait gave up
+//   Job  combine(A, G, job, parts, sm)      combiner warp of the slot's leader:
+//                                           parts = the C partials of the job;
+//                                           returns the slot's next job, or
+//                                           kJobDone when the request finished
+template <class Op>
+struct Engine {
+    using Args = typename Op::Args;
+    using OSmem = typename Op::Smem;
+
+    // dynamic shared memory: EngSmem | Op::Smem | partials (own slots x C) |
+    // staging (one partial) | ring (stages x kChunkBytes) | kernel extras
+    __host__ __device__ static size_t op_off() { return (sizeof(EngSmem) + 127) & ~size_t(127); }
+    __host__ __device__ static size_t part_off() { return (op_off() + sizeof(OSmem) + 127) & ~size_t(127); }
+    __host__ __device__ static size_t stage_off(int C, int own, int part_bytes) {
+        return part_off() + static_cast<size_t>(own) * C * part_bytes;
+    }
+    __host__ __device__ static size_t ring_off(int C, int own, int part_bytes) {
+        return (stage_off(C, own, part_bytes) + part_bytes + 1023) & ~size_t(1023);
+    }
+    __host__ __device__ static size_t smem_bytes(int C, int own, int part_bytes, int stages) {
+        return ring_off(C, own, part_bytes) + static_cast<size_t>(stages) * kChunkBytes;
+    }
+
+    __device__ static void run(const Args& A, const Workspace& W, Geo G, unsigned char* smem) {
+        EngSmem& es = *reinterpret_cast<EngSmem*>(smem);
+        OSmem& os = *reinterpret_cast<OSmem*>(smem + op_off());
+        unsigned char* parts = smem + part_off();
+        unsigned char* stage = smem + stage_off(G.C, G.own, G.part_bytes);
+        unsigned char* ring = smem + ring_off(G.C, G.own, G.part_bytes);
+        const int C = G.C;
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < G.stages; ++s) {
+                mbar_init(&es.full[s], 1);
+                mbar_init(&es.empty[s], kWarps);
+            }
+            for (int j = 0; j < kQ; ++j) {
+                mbar_init(&es.qfull[j], 1);
+                mbar_init(&es.qempty[j], kWarps);
+            }
+            for (int s = 0; s < kMaxSlots; ++s) mbar_init(&es.jfull[s], 1);
+            for (int j = 0; j < kMaxOwn; ++j) mbar_init(&es.parr[j], C);
+            es.abort = 0;
+            fence_mbar_init();
+        }
+        Op::init_smem(A, G, os);
+        __syncthreads();
+        // every CTA's barriers exist before any CTA posts to them
+        cluster_sync();
+        Pipe P;
+        P.buf = ring; P.full = es.full; P.empty = es.empty; P.abort = &es.abort; P.ctrl = W.ctrl;
+        P.stages = static_cast<uint32_t>(G.stages);
+        const bool tma = Op::tma(A);
+        if (threadIdx.x >= kCombiner0) {
+            combiner(A, W, G, es, os, parts);
+        } else if (threadIdx.x >= kThreads) {
+            if (threadIdx.x == kProducer) producer(A, W, G, es, P, tma);
+        } else {
+            consumers(A, W, G, es, os, P, tma, parts, stage);
+        }
+        __syncthreads();
+        // no CTA leaves while another may still store to its shared memory
+        cluster_sync();
+    }
+
+    // slots s with s % C == rank, s < R
+    __device__ static int own_count(const Geo& G) { return G.rank < G.R ? (G.R - 1 - G.rank) / G.C + 1 : 0; }
+
+    // ---- combiner warp: lead this CTA's slots -----------------------------
+    __device__ static void post(const Geo& G, EngSmem& es, int s, const Job& j) {
+        // lane r < C writes slot s's mailbox of CTA r and arrives on its jfull[s]
+        const int l = threadIdx.x & 31;
+        __syncwarp();
+        if (l < G.C) {
+            const uint32_t a = mapa(smem_u32(&es.jd[s]), static_cast<uint32_t>(l));
+            const uint4* v = reinterpret_cast<const uint4*>(&j);
+            st_cluster_v4(a, v[0]);
+            st_cluster_v4(a + 16, v[1]);
+            st_cluster_v4(a + 32, v[2]);
+            st_cluster_v4(a + 48, v[3]);
+            mbar_arrive_cluster(mapa(smem_u32(&es.jfull[s]), static_cast<uint32_t>(l)), 1u);
+        }
+        __syncwarp();
+    }
+    // claim requests until one needs a row (or none are left: the stop job)
+    __device__ static Job claim(const Args& A, const Workspace& W, const Geo& G, OSmem& os) {
+        for (;;) {
+            int b = 0;
+            if ((threadIdx.x & 31) == 0) b = static_cast<int>(atomicAdd(&W.ctrl->next, 1u));
+            b = __shfl_sync(0xffffffffu, b, 0);
+            Job j;
+            if (b >= Op::batch(A)) return make_job(kJobStop, 0, 0, 0);
+            j = Op::first(A, G, b, os);
+            if (j.b != kJobDone) return j;
+        }
+    }
+    __device__ static void combiner(const Args& A, const Workspace& W, const Geo& G, EngSmem& es, OSmem& os,
+                                    unsigned char* parts) {
+        const int nown = own_count(G);
+        Job cur[kMaxOwn];
+        uint32_t phase = 0;     // bit i: parity of own slot i's next arrival phase
+        int active = 0;
+        for (int i = 0; i < nown; ++i) {
+            const int s = G.rank + i * G.C;
+            cur[i] = claim(A, W, G, os);
+            post(G, es, s, cur[i]);
+            if (cur[i].b >= 0) active |= 1 << i;
+        }
+        while (active) {
+            int ready = -1;
+            const bool ok = bounded_wait([&]() {
+                for (int i = 0; i < nown; ++i)
+                    if (((active >> i) & 1) && mbar_test_cluster(&es.parr[i], (phase >> i) & 1u)) {
+                        ready = i;
+                        return true;
+                    }
+                return false;
+            }, &es.abort, W.ctrl);
+            if (!__all_sync(0xffffffffu, ok)) { raise_abort(&es.abort, W.ctrl); break; }
+            ready = __shfl_sync(0xffffffffu, ready, 0);
+            const int i = ready;
+            const int s = G.rank + i * G.C;
+            phase ^= 1u << i;
+            const unsigned char* pp = parts + static_cast<size_t>(i) * G.C * G.part_bytes;
+            Job nx = Op::combine(A, G, cur[i], pp, os);
+            if (nx.b == kJobDone) nx = claim(A, W, G, os);
+            cur[i] = nx;
+            post(G, es, s, nx);
+            if (nx.b < 0) active &= ~(1 << i);
+        }
+    }
+
+    // ---- producer lane ----------------------------------------------------
+    __device__ static void producer(const Args& A, const Workspace& W, const Geo& G, EngSmem& es, const Pipe& P,
+                                    bool tma) {
+        uint32_t jph = 0;       // bit s: parity of slot s's next mailbox phase
+        uint32_t seq = 0;       // chunks issued (ring sequence number)
+        uint32_t qn = 0;        // queue entries posted
+        int retired = 0, s0 = 0;
+        bool dead = false;
+        while (retired < G.R) {
+            int s = -1;
+            dead = !bounded_wait([&]() {
+                for (int k = 0; k < G.R; ++k) {
+                    const int t = (s0 + k) % G.R;
+                    if (mbar_test_cluster(&es.jfull[t], (jph >> t) & 1u)) { s = t; return true; }
+                }
+                return false;
+            }, P.abort, W.ctrl);
+            if (dead) break;
+            s0 = s + 1 == G.R ? 0 : s + 1;
+            jph ^= 1u << s;
+            Job job;
+            {
+                const volatile Job* vj = &es.jd[s];
+                job.b = vj->b; job.row = vj->row; job.kind = vj->kind; job.target = vj->target;
+                job.st = vj->st; job.hint = vj->hint; job.aux = vj->aux; job.aux2 = vj->aux2;
+                job.f[0] = vj->f[0]; job.f[1] = vj->f[1]; job.f[2] = vj->f[2]; job.f[3] = vj->f[3];
+                job.depth = vj->depth; job.pad[0] = job.pad[1] = job.pad[2] = 0;
+            }
+            if (job.b < 0) ++retired;
+            // hand the job to the consumers
+            const int qi = static_cast<int>(qn % kQ);
+            if (qn >= static_cast<uint32_t>(kQ) &&
+                !bounded_wait([&]() { return mbar_test(&es.qempty[qi], ((qn / kQ) - 1) & 1u); }, P.abort, W.ctrl)) {
+                dead = true;
+                break;
+            }
+            es.q[qi].job = job;
+            es.q[qi].slot = s;
+            mbar_arrive(&es.qfull[qi]);
+            ++qn;
+            if (job.b < 0 || !tma || (job.target >= 0 && job.target != G.rank)) continue;
+            const StreamPlan p = Op::plan(A, G, job);
+            for (int ci = 0; ci < p.nch; ++ci, ++seq) {
+                const int st = static_cast<int>(seq % P.stages);
+                if (seq >= P.stages &&
+                    !bounded_wait([&]() { return mbar_test(&P.empty[st], ((seq / P.stages) - 1) & 1u); }, P.abort,
+                                  W.ctrl)) {
+                    dead = true;
+                    break;
+                }
+                issue_chunk(P, p, ci, st);
+            }
+            if (dead) break;
+        }
+        if (dead) {
+            raise_abort(P.abort, W.ctrl);
+            // wait (bounded) for the copies still in flight before the CTA can end
+            const uint32_t first = seq > P.stages ? seq - P.stages : 0u;
+            for (uint32_t q = first; q < seq; ++q) {
+                const int st = static_cast<int>(q % P.stages);
+                const uint32_t par = (q / P.stages) & 1u;
+                const unsigned long long t0 = globaltimer_ns();
+                while (!mbar_test(&P.full[st], par) && globaltimer_ns() - t0 < kMbarLimitNs) nanosleep_ns(128);
+            }
+        }
+    }
+
+    // ---- consumer warps ---------------------------------------------------
+    __device__ static void consumers(const Args& A, const Workspace& W, const Geo& G, EngSmem& es, OSmem& os,
+                                     const Pipe& P, bool tma, unsigned char* parts, unsigned char* stage) {
+        uint32_t seq = 0, qn = 0;
+        int retired = 0;
+        while (retired < G.R) {
+            const int qi = static_cast<int>(qn % kQ);
+            const bool ok = bounded_wait([&]() { return mbar_test(&es.qfull[qi], (qn / kQ) & 1u); }, P.abort, W.ctrl);
+            if (csync_or(!ok)) { raise_abort(P.abort, W.ctrl); break; }
+            const Job job = es.q[qi].job;
+            const int s = es.q[qi].slot;
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) mbar_arrive(&es.qempty[qi]);
+            ++qn;
+            if (job.b < 0) { ++retired; continue; }
+            const int leader = s % G.C;
+            const int oi = s / G.C;
+            const uint32_t arr = mapa(smem_u32(&es.parr[oi]), static_cast<uint32_t>(leader));
+            if (job.target >= 0 && job.target != G.rank) {
+                // not this CTA's job: acknowledge it (the leader posts the
+                // slot's next job only after every CTA has taken this one)
+                if (threadIdx.x == 0) mbar_arrive_cluster(arr, 1u);
+                continue;
+            }
+            const int nb = Op::consume(A, G, P, seq, tma, job, os, stage);
+            if (nb < 0) { raise_abort(P.abort, W.ctrl); break; }
+            // the partial into the leader's slot area, then one counted arrival
+            const uint32_t dst = mapa(smem_u32(parts + (static_cast<size_t>(oi) * G.C + G.rank) * G.part_bytes),
+                                      static_cast<uint32_t>(leader));
+            csync();   // the staging partial is complete
+            for (int i = threadIdx.x; i < nb / 16; i += kThreads)
+                st_cluster_v4(dst + 16u * i, reinterpret_cast<const uint4*>(stage)[i]);
+            csync();   // every store of the partial is ordered before the arrive
+            if (threadIdx.x == 0) {
+                fence_acq_rel_cluster();
+                mbar_arrive_cluster(arr, 1u);
+            }
+        }
+    }
+};
 
 }  // namespace spec

@@ -20,7 +20,7 @@
 
 namespace {
 
-constexpr size_t kStaticWorkspaceBytes = size_t(8) << 20;   // 8 MiB, held by every GPU that loads the library
+constexpr size_t kStaticWorkspaceBytes = size_t(64) << 10;   // 64 KiB, held by every GPU that loads the library
 
 // Device memory; in host code this name is only a stand-in, never a usable
 // device address: the address comes from cudaGetSymbolAddress below.
@@ -64,7 +64,7 @@ extern "C" spec_status spec_verify_greedy_static(
     const size_t need = spec_verify_greedy_workspace_size(B, K, V);
     if (need > kStaticWorkspaceBytes) {
         spec::set_last_error("spec_verify_greedy_static: this batch needs a larger workspace than the "
-                             "8 MiB static one; use spec_verify_greedy with a caller-provided workspace");
+                             "64 KiB static one; use spec_verify_greedy with a caller-provided workspace");
         return SPEC_INVALID_ARG;
     }
     int dev = 0;

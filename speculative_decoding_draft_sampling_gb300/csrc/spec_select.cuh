@@ -284,10 +284,14 @@ struct ArgmaxFn : FnHooks {
     __device__ __forceinline__ uint32_t bad_flag() const { return bad_max(vmx); }
 };
 
-// max and sum of 2^((l - m_t) c) with a per-thread running max m_t
-template <class E>
+// max and sum of 2^((l - m_t) c) with a per-thread running max m_t; with
+// kMask only elements whose value key reaches `mask` are summed (the row's
+// top-k set when its threshold is known; the running max is over every
+// element, and the row maximum always belongs to the set)
+template <class E, bool kMask = false>
 struct SumExpFn : FnHooks {
     float c;
+    float thr = -kInf;   // kMask: v >= thr  <=>  value key >= mask
     float m = -kInf;
     float s = 0.f;
     float vmx = -kInf;
@@ -304,7 +308,10 @@ struct SumExpFn : FnHooks {
         }
         if (m == -kInf) return;   // every value so far is -inf
 #pragma unroll
-        for (int j = 0; j < E::kVec; ++j) s += ex2((v[j] - m) * c);
+        for (int j = 0; j < E::kVec; ++j) {
+            if (kMask && !(v[j] >= thr)) continue;
+            s += ex2((v[j] - m) * c);
+        }
     }
     __device__ __forceinline__ void scalar(bool act, float v, int x) {
         if (!act) return;
@@ -315,16 +322,42 @@ struct SumExpFn : FnHooks {
             m = v;
         }
         if (m == -kInf) return;
+        if (kMask && !(v >= thr)) return;
         s += ex2((v - m) * c);
     }
     __device__ __forceinline__ uint32_t bad_flag() const { return bad_max(vmx); }
+};
+
+// Histogram of one 8-bit digit of the value keys (round r: bits 31-8r down
+// to 24-8r) over the elements whose higher digits equal `prefix`: one round
+// of an exact radix select of the row's k-th largest value.
+template <class E>
+struct RadixFn : FnHooks {
+    int* bins;          // 256 shared counters, zeroed by the caller
+    int round;
+    uint32_t prefix;
+    float vmx = -kInf;
+    __device__ __forceinline__ void one(float v) {
+        vmx = max_nan(vmx, v);
+        const uint32_t k = fkey(v);
+        const int sh = 24 - 8 * round;
+        if (round == 0 || (k >> (sh + 8)) == prefix) atomicAdd(&bins[(k >> sh) & 255u], 1);
+    }
+    __device__ __forceinline__ void vec(bool act, const float (&v)[E::kVec], int) {
+        if (!act) return;
+#pragma unroll
+        for (int j = 0; j < E::kVec; ++j) one(v[j]);
+    }
+    __device__ __forceinline__ void scalar(bool act, float v, int) {
+        if (act) one(v);
+    }
 };
 
 // Shared state of TopkHistFn: one candidate region per warp, so a warp
 // appends with ballots and a register counter and never waits for the other
 // warps.
 struct TopkSmem {
-    static constexpr int kRegion = 256;                 // keys per warp
+    static constexpr int kRegion = 512;                 // keys per warp
     static constexpr int kSlots = 4;                    // per-thread keys within a chunk
     alignas(16) uint64_t cand[kWarps * kRegion];
     uint64_t slot[kSlots][kThreads];
@@ -527,6 +560,9 @@ struct TopkHistFn : FnHooks {
                         if (passes(vals[j], cx0 + vi * VEC + j)) m |= 1u << j;
                 }
                 append(m, vals, cx0 + vi * VEC);
+                // a filter far below the row's k-th value (a stale hint) passes
+                // whole rounds: refine before the region can overflow
+                if (nw > kRefineAt) refine_warp();
             }
         }
         cmask = 0;
@@ -651,7 +687,7 @@ struct TopkHistFn : FnHooks {
         int base = 0;
         for (int j = 0; j < w; ++j) base += S->wn[j];
         const int n = S->wn[w];
-        for (int j = lane; j < n; j += 32) __stcg(dst + base + j, reg[j]);
+        for (int j = lane; j < n; j += 32) dst[base + j] = reg[j];
     }
 
     // After the stream (all consumers): the candidates with key >= F (the
@@ -717,15 +753,18 @@ struct TopkHistFn : FnHooks {
 };
 
 // [p - q]_+ and p weights over one row with known max m and normaliser Z
+// (elements below the mask threshold have p = 0: only the -q part, which
+// the positive part drops)
 template <class E>
 struct ResidFn {
     float m, c, invZ;
+    float thr = -kInf;
     float r = 0.f, pw = 0.f;
     __device__ __forceinline__ void vec2(bool act, const float (&lv)[E::kVec], const float (&qv)[E::kVec], int) {
         if (!act) return;
 #pragma unroll
         for (int j = 0; j < E::kVec; ++j) {
-            const float w = ex2((lv[j] - m) * c);
+            const float w = lv[j] >= thr ? ex2((lv[j] - m) * c) : 0.f;
             const float d = w * invZ - qv[j];
             r += d > 0.f ? d : 0.f;
             pw += w;
@@ -733,7 +772,7 @@ struct ResidFn {
     }
     __device__ __forceinline__ void scalar2(bool act, float l, float q, int) {
         if (!act) return;
-        const float w = ex2((l - m) * c);
+        const float w = l >= thr ? ex2((l - m) * c) : 0.f;
         const float d = w * invZ - q;
         r += d > 0.f ? d : 0.f;
         pw += w;

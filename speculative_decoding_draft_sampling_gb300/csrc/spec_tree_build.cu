@@ -1,4 +1,4 @@
-// spec_tree_build.cu -- DDTree best-first draft tree on the row-task engine.
+// spec_tree_build.cu -- DDTree best-first draft tree on the cluster engine.
 //
 // [SD-survey] = "大模型投机解码：Medusa、MTP、EAGLE、DFlash、DDTree 与 DSpark"
 // (Speculative decoding for LLMs: Medusa, MTP, EAGLE, DFlash, DDTree and
@@ -9,20 +9,21 @@
 //
 // Depth d contributes at most M = budget-1 nodes, all among the M most
 // probable tokens of q_d, so each depth row is reduced to its sorted top-M
-// list (one task per depth: slices find their local top-M, the combine
-// merges them).  The best-first enumeration then runs in the combining CTA:
-// pop the best frontier entry, emit it, push its next sibling (same parent,
-// next rank) and its first child (rank 0 of the next depth).  Every emitted
-// entry's successors score no higher than it (q <= 1), so pops come out in
-// non-increasing Q and the first `budget` pops are the best prefixes.  When a
-// first child needs a depth whose list is not built yet, the enumeration
-// saves its state to the workspace and pushes that depth's row task; depth
-// rows past the last one the enumeration consults are never read.
+// list: one job per depth, in which every CTA of the cluster finds its
+// slice's top-M composite keys and the slot's leader merges them.  The
+// best-first enumeration then runs on the leader's combiner warp: each pop is
+// a warp-wide arg-max over the frontier; the popped entry is emitted and its
+// next sibling (same parent, next rank) and first child (rank 0 of the next
+// depth) join the frontier.  Every emitted entry's successors score no
+// higher than it (q <= 1), so pops come out in non-increasing Q and the first
+// `budget` pops are the best prefixes.  When a first child needs a depth
+// whose list is not built yet, the enumeration saves its state to the
+// workspace and posts that depth's row job; depth rows past the last one the
+// enumeration consults are never read.
 #include "spec_chain.cuh"
 #include "spec_select.cuh"
 
 namespace spec {
-
 
 struct Ent {                 // a frontier entry or an emitted node
     double Q;
@@ -37,19 +38,20 @@ struct EnumHdr {
     int len[24];             // list length per depth (index 1..L)
 };
 
-struct __align__(16) BuildSmem {
-    TopkSmem tk;             // slice candidates (consumers)
-    PipeSmem pipe;
+constexpr int kBuildList = 2048;         // gathered keys in a combine (at most C * M)
+
+struct BuildSmem {
+    TopkSmem tk;             // consumers: slice candidates
     uint64_t sh64[4];
-    double red[kWarps];
     int ired[kWarps + 4];
     int hist[64];
     uint32_t scratch[kWarps + 2];
+    uint32_t tag;            // consumers: unit tag for the shared filter
     EnumHdr eh;              // combiner
-    SliceHdrs hdrs;          // combiner
+    alignas(16) uint64_t list[kBuildList];   // combiner: gathered keys
 };
 
-// per-request extra scratch: [EnumHdr][lists L*M (tok,int) + (prob,float)][nodes N][pending 2N+2]
+// per-request workspace: [EnumHdr][lists L*M (tok, prob bits)][nodes N][pending 2N+2]
 __host__ __device__ inline size_t build_lists_off() { return 128; }
 __host__ __device__ inline size_t build_nodes_off(int N, int L) {
     return (build_lists_off() + static_cast<size_t>(L) * (N - 1) * 8 + 127) & ~static_cast<size_t>(127);
@@ -60,20 +62,10 @@ __host__ __device__ inline size_t build_pend_off(int N, int L) {
 size_t build_extra_bytes(int N, int L) {
     return (build_pend_off(N, L) + static_cast<size_t>(2 * N + 2) * sizeof(Ent) + 127) & ~static_cast<size_t>(127);
 }
-// dynamic shared memory beyond the ring and BuildSmem, all the combiner's:
-// depth lists, gathered keys, ancestor-mask scratch, then nodes + pending
-constexpr int kBuildList = 2048;         // gathered keys in a combine
-__host__ __device__ inline size_t build_lists_bytes(int N, int L) {
-    return (static_cast<size_t>(L) * (N - 1) * 8 + 15) & ~static_cast<size_t>(15);
-}
-__host__ __device__ inline size_t build_mask_off(int N, int L) {
-    return build_lists_bytes(N, L) + static_cast<size_t>(kBuildList) * 8;
-}
-__host__ __device__ inline size_t build_scr_bytes(int N, int L) {
-    return build_mask_off(N, L) + static_cast<size_t>(N) * ((N + 63) / 64) * 8;
-}
-static size_t build_enum_smem(int N, int L) {
-    return build_scr_bytes(N, L) + static_cast<size_t>(3 * N + 2) * sizeof(Ent);
+// combiner shared memory after the partial areas: depth lists, nodes and pending
+__host__ __device__ inline size_t enum_smem_bytes(int N, int L) {
+    return ((static_cast<size_t>(L) * (N - 1) * 8 + 15) & ~static_cast<size_t>(15)) +
+           static_cast<size_t>(3 * N + 2) * sizeof(Ent);
 }
 
 __device__ __forceinline__ bool ent_before(const Ent& a, const Ent& b) {
@@ -93,45 +85,26 @@ __device__ __forceinline__ void path_set(Ent& e, int d, int r) {
     }
 }
 
-// Exact top-M (value desc, index asc) of one q row by bisection over
-// composite keys, on the combiner warp; for rows whose slice candidate
-// buffers overflowed (adversarial value order).  Writes the keys
-// (unordered) to list[0..return).
-__device__ int build_fallback(const float* qrow, int V, int M, uint64_t* list) {
-    const int l = threadIdx.x & 31;
-    uint64_t lo = 0, hi = ~0ull;
-    if (V > M) {
-        // invariant: count(key >= lo) >= M; the range halves every step
-        for (int it = 0; it < 66 && lo < hi; ++it) {
-            const uint64_t d = hi - lo;
-            const uint64_t mid = lo + (d >> 1) + (d & 1ull);
-            int c = 0;
-            for (int x = l; x < V; x += 32) c += ckey(qrow[x], x) >= mid;
-            c = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(c)));
-            if (c >= M) lo = mid; else hi = mid - 1;
-        }
-    }
-    const uint32_t lt = (1u << l) - 1u;
-    int out = 0;
-    for (int x0 = 0; x0 < V; x0 += 32) {
-        const int x = x0 + l;
-        uint64_t key = 0;
-        bool p = false;
-        if (x < V) { key = ckey(qrow[x], x); p = key >= lo; }
-        const uint32_t bal = __ballot_sync(0xffffffffu, p);
-        if (p) {
-            const int pos = out + __popc(bal & lt);
-            if (pos < M) list[pos] = key;
-        }
-        out += __popc(bal);
-    }
-    __syncwarp();
-    return out < M ? out : M;
+// the enumeration's shared-memory view (combiner warp): depth lists
+// (tokens, probabilities), emitted nodes, frontier
+struct EnumView {
+    int* ltok;
+    float* lprob;
+    Ent* nodes;
+    Ent* pend;
+};
+__device__ __forceinline__ EnumView enum_view(unsigned char* base, int N, int L) {
+    EnumView v;
+    const int LM = L * (N - 1);
+    v.ltok = reinterpret_cast<int*>(base);
+    v.lprob = reinterpret_cast<float*>(base + static_cast<size_t>(LM) * 4);
+    v.nodes = reinterpret_cast<Ent*>(base + ((static_cast<size_t>(LM) * 8 + 15) & ~static_cast<size_t>(15)));
+    v.pend = v.nodes + N;
+    return v;
 }
 
-// Write the final tree of request b from shared memory (combiner warp).
-__device__ void build_finalize(const BuildArgs& A, unsigned long long* msk, const Ent* nodes, const int* ltok,
-                               int b, int count, int st) {
+// Write the final tree of request b (combiner warp).
+__device__ void build_finalize(const BuildArgs& A, const EnumView& ev, int b, int count, int st) {
     const int l = threadIdx.x & 31;
     const int N = A.N, M = A.M;
     const int W = (N + 63) / 64;
@@ -139,129 +112,355 @@ __device__ void build_finalize(const BuildArgs& A, unsigned long long* msk, cons
     int* pr = A.parent + static_cast<long long>(b) * N;
     int* dp = A.depth + static_cast<long long>(b) * N;
     double* sc = A.score + static_cast<long long>(b) * N;
+    unsigned long long* mk = A.anc_mask + static_cast<long long>(b) * N * W;
     for (int n = l; n < N; n += 32) {
         if (n < count) {
-            const Ent& e = nodes[n];
-            tk[n] = n == 0 ? -1 : ltok[(e.depth - 1) * M + e.rank];
+            const Ent& e = ev.nodes[n];
+            tk[n] = n == 0 ? -1 : ev.ltok[(e.depth - 1) * M + e.rank];
             pr[n] = e.parent;
             dp[n] = e.depth;
             sc[n] = e.Q;
         } else {
             tk[n] = -1; pr[n] = -1; dp[n] = -1; sc[n] = 0.0;
         }
-    }
-    // ancestor masks: mask[n] = mask[parent[n]] | bit n, parents first
-    unsigned long long* mk = A.anc_mask + static_cast<long long>(b) * N * W;
-    if (l == 0) {
-        for (int n = 0; n < N; ++n) {
-            for (int w = 0; w < W; ++w) {
-                unsigned long long v = 0;
-                if (n < count && nodes[n].parent >= 0) v = msk[nodes[n].parent * W + w];
-                if (n < count && w == n / 64) v |= 1ull << (n % 64);
-                msk[n * W + w] = v;
+        // ancestor mask: the node itself and every ancestor (parents precede
+        // children, so the walk up ends at the root); W <= 4 words (N <= 256)
+        unsigned long long mw[4] = {0ull, 0ull, 0ull, 0ull};
+        if (n < count) {
+            int m = n;
+            for (int guard = 0; m >= 0 && guard <= N; ++guard) {
+                mw[m / 64] |= 1ull << (m % 64);
+                m = ev.nodes[m].parent;
             }
         }
+        for (int w = 0; w < W; ++w) mk[static_cast<long long>(n) * W + w] = mw[w];
     }
-    __syncwarp();
-    for (int i = l; i < N * W; i += 32) mk[i] = msk[i];
     if (l == 0) {
         A.num_nodes[b] = count;
         A.status[b] = st;
     }
     __syncwarp();
-    if (l == 0) finish_request(A.W);
 }
 
-// The combine of one depth row (combiner warp): merge the slice lists into
-// the depth's sorted top-M, then resume the best-first enumeration.
-__device__ void build_combine(const BuildArgs& A, BuildSmem& sh, unsigned char* scr, Ent* nodes, Ent* pend,
-                              const Job& job, uint32_t done, uint32_t base) {
+// warp-wide pop of the best frontier entry: its index in every lane
+__device__ __forceinline__ int best_pending_w(const Ent* pend, int np) {
+    const int l = threadIdx.x & 31;
+    int best = -1;
+    for (int j = l; j < np; j += 32)
+        if (best < 0 || ent_before(pend[j], pend[best])) best = j;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const int other = __shfl_xor_sync(0xffffffffu, best, o);
+        if (other >= 0 && (best < 0 || ent_before(pend[other], pend[best]) ||
+                           (!ent_before(pend[best], pend[other]) && other < best)))
+            best = other;
+    }
+    return best;
+}
+
+// The best-first enumeration from the saved state in `eh` / `ev` (combiner
+// warp).  Returns the depth whose list it needs next, or 0 when the tree is
+// complete.
+__device__ int enumerate_w(const BuildArgs& A, EnumHdr& eh, const EnumView& ev) {
     const int l = threadIdx.x & 31;
     const int N = A.N, M = A.M, L = A.L;
-    const int b = job.task.b;
-    const bool initial = job.task.kind < 0;
-    const int d = job.task.row + 1;
-    const bool trivial = job.kind != 0;
-    unsigned char* ex = A.W.extra + static_cast<size_t>(b) * A.W.extra_stride;
-    EnumHdr* gh = reinterpret_cast<EnumHdr*>(ex);
-    int* gl = reinterpret_cast<int*>(ex + build_lists_off());        // [L][M] (tok, prob bits)
-    Ent* gnodes = reinterpret_cast<Ent*>(ex + build_nodes_off(N, L));
-    Ent* gpend = reinterpret_cast<Ent*>(ex + build_pend_off(N, L));
-    const int LM = L * M;
-    int* ltok = reinterpret_cast<int*>(scr);
-    float* lprob = reinterpret_cast<float*>(scr + static_cast<size_t>(LM) * 4);
-    uint64_t* list = reinterpret_cast<uint64_t*>(scr + build_lists_bytes(N, L));
-    unsigned long long* msk = reinterpret_cast<unsigned long long*>(scr + build_mask_off(N, L));
-    EnumHdr& eh = sh.eh;
-    if (initial) {
+    int count = eh.count, np = eh.npend, want = eh.want;
+    int need = 0;
+    while (count < N) {
+        if (want >= 0) {
+            const int dd = ev.nodes[want].depth + 1;
+            if (dd <= L) {
+                if (dd > eh.avail) { need = dd; break; }
+                if (eh.len[dd] > 0) {
+                    if (l == 0) {
+                        Ent c = ev.nodes[want];
+                        c.depth = dd; c.parent = want; c.rank = 0;
+                        path_set(c, dd, 0);
+                        c.Q = ev.nodes[want].Q * static_cast<double>(ev.lprob[(dd - 1) * M + 0]);
+                        ev.pend[np] = c;
+                    }
+                    ++np;
+                    __syncwarp();
+                }
+            }
+            want = -1;
+        }
+        if (np == 0) break;
+        const int best = best_pending_w(ev.pend, np);
+        const Ent c = ev.pend[best];
+        __syncwarp();
+        if (l == 0) {
+            ev.pend[best] = ev.pend[np - 1];
+            ev.nodes[count] = c;
+        }
+        --np;
+        const int nid = count++;
+        if (c.rank + 1 < eh.len[c.depth]) {
+            if (l == 0) {
+                Ent s2 = c;
+                s2.rank = c.rank + 1;
+                path_set(s2, c.depth, c.rank + 1);
+                s2.Q = ev.nodes[c.parent].Q * static_cast<double>(ev.lprob[(c.depth - 1) * M + c.rank + 1]);
+                ev.pend[np] = s2;
+            }
+            ++np;
+        }
+        __syncwarp();
+        want = nid;
+    }
+    if (l == 0) { eh.count = count; eh.npend = np; eh.want = want; }
+    __syncwarp();
+    return need;
+}
+
+// save / load the enumeration state of request b (combiner warp; the
+// workspace lines bypass L1)
+__device__ void enum_save(const BuildArgs& A, int b, const EnumHdr& eh, const EnumView& ev, int first_list) {
+    const int l = threadIdx.x & 31;
+    const int N = A.N, M = A.M, L = A.L;
+    unsigned char* ex = A.E.W.extra + static_cast<size_t>(b) * A.E.W.extra_stride;
+    int* gl = reinterpret_cast<int*>(ex + build_lists_off());
+    const int nc = eh.count, np = eh.npend;
+    for (int i = l; i < nc * 5; i += 32)
+        __stcg(reinterpret_cast<unsigned long long*>(ex + build_nodes_off(N, L)) + i,
+               reinterpret_cast<const unsigned long long*>(ev.nodes)[i]);
+    for (int i = l; i < np * 5; i += 32)
+        __stcg(reinterpret_cast<unsigned long long*>(ex + build_pend_off(N, L)) + i,
+               reinterpret_cast<const unsigned long long*>(ev.pend)[i]);
+    for (int i = first_list * M + l; i < eh.avail * M; i += 32) {
+        __stcg(gl + 2 * i, ev.ltok[i]);
+        __stcg(gl + 2 * i + 1, __float_as_int(ev.lprob[i]));
+    }
+    for (int i = l; i < static_cast<int>(sizeof(EnumHdr) / 4); i += 32)
+        __stcg(reinterpret_cast<int*>(ex) + i, reinterpret_cast<const int*>(&eh)[i]);
+    __syncwarp();
+}
+__device__ void enum_load(const BuildArgs& A, int b, EnumHdr& eh, const EnumView& ev) {
+    const int l = threadIdx.x & 31;
+    const int N = A.N, M = A.M, L = A.L;
+    const unsigned char* ex = A.E.W.extra + static_cast<size_t>(b) * A.E.W.extra_stride;
+    const int* gl = reinterpret_cast<const int*>(ex + build_lists_off());
+    for (int i = l; i < static_cast<int>(sizeof(EnumHdr) / 4); i += 32)
+        reinterpret_cast<int*>(&eh)[i] = __ldcg(reinterpret_cast<const int*>(ex) + i);
+    __syncwarp();
+    const int nc = eh.count, np = eh.npend;
+    for (int i = l; i < nc * 5; i += 32)
+        reinterpret_cast<unsigned long long*>(ev.nodes)[i] =
+            __ldcg(reinterpret_cast<const unsigned long long*>(ex + build_nodes_off(N, L)) + i);
+    for (int i = l; i < np * 5; i += 32)
+        reinterpret_cast<unsigned long long*>(ev.pend)[i] =
+            __ldcg(reinterpret_cast<const unsigned long long*>(ex + build_pend_off(N, L)) + i);
+    for (int i = l; i < eh.avail * M; i += 32) {
+        ev.ltok[i] = __ldcg(gl + 2 * i);
+        ev.lprob[i] = __int_as_float(__ldcg(gl + 2 * i + 1));
+    }
+    __syncwarp();
+}
+
+struct BuildOp {
+    using Args = BuildArgs;
+    using Smem = BuildSmem;
+
+    __device__ static int batch(const Args& A) { return A.B; }
+    __device__ static bool tma(const Args& A) { return A.tma_q != 0; }
+    __device__ static void init_smem(const Args&, const Geo&, Smem& sm) {
+        if (threadIdx.x == 0) {
+            topk_smem_init(sm.tk);
+            sm.tag = 0;
+        }
+    }
+    // the combiner's enumeration scratch sits after the ring
+    __device__ static EnumView view(const Args& A, const Geo& G) {
+        extern __shared__ __align__(128) unsigned char smem[];
+        const size_t off = Engine<BuildOp>::smem_bytes(G.C, G.own, G.part_bytes, G.stages);
+        return enum_view(smem + ((off + 15) & ~static_cast<size_t>(15)), A.N, A.L);
+    }
+    __device__ static Job first(const Args& A, const Geo& G, int b, Smem& sm) {
+        const int l = threadIdx.x & 31;
+        const EnumView ev = view(A, G);
+        EnumHdr& eh = sm.eh;
         if (l == 0) {
             EnumHdr h{};
             h.count = 1; h.npend = 0; h.want = 0; h.avail = 0; h.status = 0;
             eh = h;
             Ent root{};
             root.Q = 1.0; root.depth = 0; root.parent = -1; root.rank = -1;
-            nodes[0] = root;
+            ev.nodes[0] = root;
         }
-    } else {
-        for (int i = l; i < static_cast<int>(sizeof(EnumHdr) / 4); i += 32)
-            reinterpret_cast<int*>(&eh)[i] = __ldcg(reinterpret_cast<const int*>(gh) + i);
         __syncwarp();
-        const int nc = eh.count, np = eh.npend;
-        for (int i = l; i < nc * 5; i += 32)
-            reinterpret_cast<unsigned long long*>(nodes)[i] = __ldcg(reinterpret_cast<const unsigned long long*>(gnodes) + i);
-        for (int i = l; i < np * 5; i += 32)
-            reinterpret_cast<unsigned long long*>(pend)[i] = __ldcg(reinterpret_cast<const unsigned long long*>(gpend) + i);
-        for (int i = l; i < eh.avail * M; i += 32) {
-            ltok[i] = __ldcg(gl + 2 * i);
-            lprob[i] = __int_as_float(__ldcg(gl + 2 * i + 1));
+        if (A.N <= 1 || A.L <= 0) {
+            build_finalize(A, ev, b, 1, 0);
+            return job_done();
         }
+        enum_save(A, b, eh, ev, 0);
+        return make_job(b, 0, 0, 0);   // depth 1's row
     }
-    __syncwarp();
-    if (!trivial) {
-        const int S = task_S(A, job.task);
-        load_hdrs_w(A.W, b, S, sh.hdrs);
-        uint32_t flags = l < S ? sh.hdrs.flags[l] : 0u;
-        uint64_t theta = l < S ? sh.hdrs.kth[l] : 0ull;
+    __device__ static StreamPlan plan(const Args& A, const Geo& G, const Job& j) {
+        const float* qrow = A.q + static_cast<long long>(j.b) * A.q_bs + static_cast<long long>(j.row) * A.q_rs;
+        return plan_single(qrow, 4, slice_x0(G, G.rank), slice_x1(G, G.rank, A.V));
+    }
+    // consumers: this slice's top-M composite keys (value desc, index asc)
+    __device__ static int consume(const Args& A, const Geo& G, const Pipe& P, uint32_t& seq, bool tma, const Job& j,
+                                  Smem& sm, unsigned char* out) {
+        PartHdr* ph = reinterpret_cast<PartHdr*>(out);
+        uint64_t* pk = reinterpret_cast<uint64_t*>(ph + 1);
+        const int M = A.M;
+        if (threadIdx.x == 0) sm.tag = sm.tag + 1u;
+        csync();
+        TopkHistFn<F32, false> fn;
+        fn.init(&sm.tk, M, 0u, sm.tag);
+        if (!consume_row<F32>(P, seq, plan(A, G, j), tma, slice_x0(G, G.rank), fn)) return -1;
+        uint64_t F;
+        uint32_t oflow, bad;
+        float vm;
+        int n = fn.finish(F, oflow, bad, vm);
+        uint64_t* list = sm.tk.cand;
+        if (n > A.cap_p && !bad && !oflow) {
+            // the slice's exact M-th key: a certified value bound (repeated
+            // until it stops rising), then the index bits within that value
+            for (int it = 0; it < 8 && n > A.cap_p; ++it) {
+                bool cert;
+                const uint32_t F2 = hist_bound_list(list, n, M, hkey(F), sm.hist, sm.scratch, cert);
+                if (!(cert && F2 > hkey(F))) break;
+                n = compact_list(list, n, F2, sm.ired);
+                F = static_cast<uint64_t>(F2) << 32;
+            }
+            if (n > A.cap_p) {
+                const uint64_t kth = composite_bound(
+                    [&](auto f) { for (int i = threadIdx.x; i < n; i += kThreads) f(list[i]); }, M, F, sm.ired);
+                // keep the keys >= kth (order kept)
+                int outn = 0;
+                const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+                for (int i0 = 0; i0 < n; i0 += kThreads) {
+                    const int i = i0 + threadIdx.x;
+                    uint64_t key = 0;
+                    bool p = false;
+                    if (i < n) { key = list[i]; p = key >= kth; }
+                    const uint32_t bal = __ballot_sync(0xffffffffu, p);
+                    if (lane == 0) sm.ired[w] = __popc(bal);
+                    csync();
+                    int base = outn, tot = 0;
+                    for (int q = 0; q < kWarps; ++q) {
+                        if (q < w) base += sm.ired[q];
+                        tot += sm.ired[q];
+                    }
+                    csync();
+                    if (p) list[base + __popc(bal & ((1u << lane) - 1u))] = key;
+                    outn += tot;
+                    csync();
+                }
+                n = outn;
+                F = kth;
+                if (n > A.cap_p) oflow = 1;
+            }
+        }
+        if (bad || oflow) n = 0;
+        csync();
+        for (int i = threadIdx.x; i < n; i += kThreads) pk[i] = list[i];
+        if (threadIdx.x == 0) {
+            ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u);
+            ph->cnt = n;
+            ph->kth = F;
+        }
+        return static_cast<int>(sizeof(PartHdr)) + ((n * 8 + 15) & ~15);
+    }
+
+    // Exact top-M (value desc, index asc) of one q row by bisection over
+    // composite keys, on the combiner warp; for rows whose slice candidate
+    // buffers overflowed (adversarial value order).  Keys (unordered) to
+    // list[0..return).
+    __device__ static int fallback(const float* qrow, int V, int M, uint64_t* list) {
+        const int l = threadIdx.x & 31;
+        uint64_t lo = 0, hi = ~0ull;
+        if (V > M) {
+            // invariant: count(key >= lo) >= M; the range halves every step
+            for (int it = 0; it < 66 && lo < hi; ++it) {
+                const uint64_t d = hi - lo;
+                const uint64_t mid = lo + (d >> 1) + (d & 1ull);
+                int c = 0;
+                for (int x = l; x < V; x += 32) c += ckey(qrow[x], x) >= mid;
+                c = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<uint32_t>(c)));
+                if (c >= M) lo = mid; else hi = mid - 1;
+            }
+        }
+        const uint32_t lt = (1u << l) - 1u;
+        int out = 0;
+        for (int x0 = 0; x0 < V; x0 += 32) {
+            const int x = x0 + l;
+            uint64_t key = 0;
+            bool p = false;
+            if (x < V) { key = ckey(qrow[x], x); p = key >= lo; }
+            const uint32_t bal = __ballot_sync(0xffffffffu, p);
+            if (p) {
+                const int pos = out + __popc(bal & lt);
+                if (pos < M) list[pos] = key;
+            }
+            out += __popc(bal);
+        }
+        __syncwarp();
+        return out < M ? out : M;
+    }
+
+    __device__ static Job combine(const Args& A, const Geo& G, const Job& j, const unsigned char* parts, Smem& sm) {
+        const int l = threadIdx.x & 31;
+        const int M = A.M, C = G.C, pb = G.part_bytes;
+        const int b = j.b;
+        const int d = j.row + 1;
+        const EnumView ev = view(A, G);
+        EnumHdr& eh = sm.eh;
+        enum_load(A, b, eh, ev);
+        uint32_t flags = 0;
+        uint64_t theta = 0;
+        int cnt = 0;
+        if (l < C) {
+            const PartHdr* h = part_at(parts, pb, l);
+            flags = h->flags; theta = h->kth; cnt = h->cnt;
+        }
         flags = __reduce_or_sync(0xffffffffu, flags);
         theta = warp_max_u64(theta);
+        uint64_t* list = sm.list;
         int n = 0;
         if (flags & kPfBad) {
             n = 0;
         } else if (flags & kPfOverflow) {
             const float* qrow = A.q + static_cast<long long>(b) * A.q_bs + static_cast<long long>(d - 1) * A.q_rs;
-            n = build_fallback(qrow, A.V, M, list);
+            n = fallback(qrow, A.V, M, list);
         } else {
             // every slice key at or above the largest slice filter, then the top M
-            bool of;
-            n = gather_keys_w(A.W, b, S, sh.hdrs, [&](uint64_t key) { return key >= theta; }, list, kBuildList, of);
-            if (n > M) {
-                const uint64_t kth = kth_key_w(list, n, M);
-                // keep the keys >= kth (exactly M: composite keys are unique)
-                const uint32_t lt = (1u << l) - 1u;
-                int out = 0;
-                for (int i0 = 0; i0 < n; i0 += 32) {
+            const uint32_t lt = (1u << l) - 1u;
+            for (int r = 0; r < C; ++r) {
+                const int cr = __shfl_sync(0xffffffffu, cnt, r);
+                const uint64_t* keys = reinterpret_cast<const uint64_t*>(part_at(parts, pb, r) + 1);
+                for (int i0 = 0; i0 < cr; i0 += 32) {
                     const int i = i0 + l;
                     uint64_t key = 0;
                     bool p = false;
-                    if (i < n) { key = list[i]; p = key >= kth; }
+                    if (i < cr) { key = keys[i]; p = key >= theta; }
                     const uint32_t bal = __ballot_sync(0xffffffffu, p);
-                    if (p) list[out + __popc(bal & lt)] = key;
-                    out += __popc(bal);
+                    if (p) {
+                        const int pos = n + __popc(bal & lt);
+                        if (pos < kBuildList) list[pos] = key;
+                    }
+                    n += __popc(bal);
                 }
-                __syncwarp();
-                n = out;
+            }
+            __syncwarp();
+            if (n > kBuildList) {
+                const float* qrow = A.q + static_cast<long long>(b) * A.q_bs + static_cast<long long>(d - 1) * A.q_rs;
+                n = fallback(qrow, A.V, M, list);
+            } else if (n > M) {
+                const uint64_t kth = kth_key_w(list, n, M);
+                n = compact_key_w(list, n, kth);   // exactly M: composite keys are unique
             }
         }
         // the depth list in rank order (value desc, index asc)
         for (int i = l; i < n; i += 32) {
             const uint64_t key = list[i];
             int r = 0;
-            for (int j = 0; j < n; ++j) r += list[j] > key;
+            for (int q = 0; q < n; ++q) r += list[q] > key;
             const int o = (d - 1) * M + r;
-            ltok[o] = ckey_idx(key);
-            lprob[o] = ckey_val(key);
-            __stcg(gl + 2 * o, ckey_idx(key));
-            __stcg(gl + 2 * o + 1, __float_as_int(ckey_val(key)));
+            ev.ltok[o] = ckey_idx(key);
+            ev.lprob[o] = ckey_val(key);
         }
         if (l == 0) {
             eh.len[d] = n;
@@ -269,213 +468,27 @@ __device__ void build_combine(const BuildArgs& A, BuildSmem& sh, unsigned char* 
             if (flags & kPfBad) eh.status |= 1;
         }
         __syncwarp();
-    }
-    // ---- best-first enumeration (lane 0), resumable ----
-    int need = 0;
-    if (l == 0) {
-        int count = eh.count, np = eh.npend, want = eh.want;
-        while (count < N) {
-            if (want >= 0) {
-                const int dd = nodes[want].depth + 1;
-                if (dd <= L) {
-                    if (dd > eh.avail) { need = dd; break; }
-                    if (eh.len[dd] > 0) {
-                        Ent c = nodes[want];
-                        c.depth = dd; c.parent = want; c.rank = 0;
-                        path_set(c, dd, 0);
-                        c.Q = nodes[want].Q * static_cast<double>(lprob[(dd - 1) * M + 0]);
-                        pend[np++] = c;
-                    }
-                }
-                want = -1;
-            }
-            if (np == 0) break;
-            int best = 0;
-            for (int j = 1; j < np; ++j)
-                if (ent_before(pend[j], pend[best])) best = j;
-            const Ent c = pend[best];
-            pend[best] = pend[--np];
-            const int nid = count++;
-            nodes[nid] = c;
-            if (c.rank + 1 < eh.len[c.depth]) {
-                Ent s2 = c;
-                s2.rank = c.rank + 1;
-                path_set(s2, c.depth, c.rank + 1);
-                s2.Q = nodes[c.parent].Q * static_cast<double>(lprob[(c.depth - 1) * M + c.rank + 1]);
-                pend[np++] = s2;
-            }
-            want = nid;
+        const int need = enumerate_w(A, eh, ev);
+        if (need == 0) {
+            build_finalize(A, ev, b, eh.count, eh.status);
+            return job_done();
         }
-        eh.count = count; eh.npend = np; eh.want = want;
+        enum_save(A, b, eh, ev, d - 1);
+        return make_job(b, need - 1, 0, 0);
     }
-    need = __shfl_sync(0xffffffffu, need, 0);
-    __syncwarp();
-    if (need == 0) {
-        build_finalize(A, msk, nodes, ltok, b, eh.count, eh.status);
-    } else {
-        // save the state and ask for depth `need`
-        const int nc = eh.count, np = eh.npend;
-        for (int i = l; i < nc * 5; i += 32)
-            __stcg(reinterpret_cast<unsigned long long*>(gnodes) + i, reinterpret_cast<const unsigned long long*>(nodes)[i]);
-        for (int i = l; i < np * 5; i += 32)
-            __stcg(reinterpret_cast<unsigned long long*>(gpend) + i, reinterpret_cast<const unsigned long long*>(pend)[i]);
-        for (int i = l; i < static_cast<int>(sizeof(EnumHdr) / 4); i += 32)
-            __stcg(reinterpret_cast<int*>(gh) + i, reinterpret_cast<const int*>(&eh)[i]);
-        __syncwarp();
-        if (l == 0) {
-            Task nt;
-            nt.b = b; nt.row = need - 1; nt.kind = 0; nt.aux = 0; nt.st = 0; nt.base = base;
-            int S1, SL1;
-            pick_slices(A.B, A.V, A.S, A.S1, done, S1, SL1);
-            push_task(A.W, nt, S1, SL1, true);   // the next combine reads the saved state
-        }
-    }
-    __syncwarp();
-}
+};
 
-__global__ void __launch_bounds__(kBlockThreads, kCtasPerSm) build_kernel(const BuildArgs A) {
+__global__ void __launch_bounds__(kBlockThreads, 1) build_kernel(const BuildArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
-    auto& sh = *reinterpret_cast<BuildSmem*>(smem + kStages * kChunkBytes);
-    unsigned char* scr = smem + kStages * kChunkBytes + sizeof(BuildSmem);
-    Ent* nodes = reinterpret_cast<Ent*>(scr + build_scr_bytes(A.N, A.L));
-    Ent* pend = nodes + A.N;
-    if (threadIdx.x == 0) topk_smem_init(sh.tk);   // made visible by pipe_init's barrier
-    const Pipe P = pipe_init(smem, sh.pipe);
-    const int N = A.N, M = A.M, L = A.L;
-    const bool tma = A.tma_q != 0;
-    auto trivial_of = [&](const Task& t) { return t.kind < 0 && (N <= 1 || L <= 0); };
-    auto plan = [&](const Task& t, int slice) {
-        if (trivial_of(t)) return plan_none();
-        const int SL = task_SL(A, t);
-        const int x0 = slice * SL, x1 = min(A.V, x0 + SL);
-        const float* qrow = A.q + static_cast<long long>(t.b) * A.q_bs + static_cast<long long>(t.row) * A.q_rs;
-        return plan_single(qrow, 4, x0, x1);
-    };
-    if (threadIdx.x >= kCombiner0) {
-        combiner_loop(P, [&](const Job& job) {
-            uint32_t done;
-            uint32_t base;
-            if (comb_arrive(A.W, job.task, task_S(A, job.task), &done, &base))
-                build_combine(A, sh, scr, nodes, pend, job, done, base);
-            __syncwarp();
-        });
-        return;
-    }
-    if (threadIdx.x >= kThreads) {
-        if (threadIdx.x == kProducer)
-            producer_loop(A.W, A.B, A.S, P, tma, [](Claimed&) {},
-                          [&](const Claimed& c) { return plan(c.task, c.slice); });
-        return;
-    }
-    uint32_t seq = 0, jseq = 0, cseq = 0;
-    auto serve = []() {};   // every combine runs on the combiner warp
-    for (uint32_t u = 0;; ++u) {
-        const Claimed cl = next_unit(P, u, cseq, serve);
-        if (!cl.ok) break;
-        const Task t = cl.task;
-        const int s = cl.slice;
-        const int b = t.b;
-        const bool trivial = trivial_of(t);
-        PartHdr* ph = part_hdr(A.W, b, s, A.S);
-        uint64_t* pk = part_keys(A.W, b, s, A.S);
-        if (!trivial) {
-            const int x0 = s * task_SL(A, t);
-            TopkHistFn<F32, false> fn;
-            fn.init(&sh.tk, M, 0u, u + 1u);
-            if (!consume_row<F32>(P, seq, plan(t, s), tma, x0, fn)) break;
-            uint64_t F;
-            uint32_t oflow, bad;
-            float vm;
-            int n = fn.finish(F, oflow, bad, vm);
-            uint64_t* list = sh.tk.cand;
-            if (n > A.cap_p && !bad && !oflow) {
-                // the slice's exact M-th key: a certified value bound, then the
-                // index bits within that value
-                // (repeated until it stops rising: then it is the exact M-th value)
-                for (int it = 0; it < 8 && n > A.cap_p; ++it) {
-                    bool cert;
-                    const uint32_t F2 = hist_bound_list(list, n, M, hkey(F), sh.hist, sh.scratch, cert);
-                    if (!(cert && F2 > hkey(F))) break;
-                    n = compact_list(list, n, F2, sh.ired);
-                    F = static_cast<uint64_t>(F2) << 32;
-                }
-                if (n > A.cap_p) {
-                    const uint64_t kth = composite_bound(
-                        [&](auto f) { for (int i = threadIdx.x; i < n; i += kThreads) f(list[i]); },
-                        M, F, sh.ired);
-                    // keep the keys >= kth (order kept)
-                    int out = 0;
-                    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-                    for (int i0 = 0; i0 < n; i0 += kThreads) {
-                        const int i = i0 + threadIdx.x;
-                        uint64_t key = 0;
-                        bool p = false;
-                        if (i < n) { key = list[i]; p = key >= kth; }
-                        const uint32_t bal = __ballot_sync(0xffffffffu, p);
-                        if (lane == 0) sh.ired[w] = __popc(bal);
-                        csync();
-                        int base = out, tot = 0;
-                        for (int j = 0; j < kWarps; ++j) {
-                            if (j < w) base += sh.ired[j];
-                            tot += sh.ired[j];
-                        }
-                        csync();
-                        if (p) list[base + __popc(bal & ((1u << lane) - 1u))] = key;
-                        out += tot;
-                        csync();
-                    }
-                    n = out;
-                    F = kth;
-                    if (n > A.cap_p) oflow = 1;
-                }
-            }
-            if (bad || oflow) n = 0;
-            csync();
-            for (int i = threadIdx.x; i < n; i += kThreads) __stcg(pk + i, list[i]);
-            if (threadIdx.x == 0) {
-                ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u);
-                ph->cnt = n;
-                ph->kth = F;
-            }
-        }
-        csync();
-        Job j;
-        j.task = t; j.slice = s; j.kind = trivial ? 1 : 0; j.stop = 0; j.flags = 0;
-        post_job(P, jseq, cseq, j, serve);
-    }
-    Job j;
-    j.task.b = 0; j.task.row = 0; j.task.kind = 0; j.task.aux = 0; j.task.st = 0; j.task.base = 0;
-    j.slice = 0; j.kind = 0; j.stop = 1; j.flags = 0;
-    post_job(P, jseq, cseq, j, serve);
+    Engine<BuildOp>::run(A, A.E.W, make_geo(A.E), smem);
 }
 
-// largest slice count whose candidate lists fit the combine's gather buffer
-int build_max_slices(int N, int L) {
-    (void)L;
-    const int M = N - 1;
-    // the combiner warp merges every slice's list: keep that under ~8 lists
-    int s = M > 0 ? kBuildList / M : kMaxSlices;
-    if (s > 8) s = 8;
-    return s < 1 ? 1 : (s > kMaxSlices ? kMaxSlices : s);
-}
+const void* build_kernel_ptr() { return reinterpret_cast<const void*>(&build_kernel); }
 
-static size_t build_smem(int N, int L) { return kStages * kChunkBytes + sizeof(BuildSmem) + build_enum_smem(N, L); }
-
-int build_occupancy(int N, int L) {
-    const int smem = static_cast<int>(build_smem(N, L));
-    int n = 0;
-    cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, build_kernel, kBlockThreads, smem);
-    return n;
+size_t build_smem(int C, int own, int part_bytes, int stages, int N, int L) {
+    return ((Engine<BuildOp>::smem_bytes(C, own, part_bytes, stages) + 15) & ~static_cast<size_t>(15)) +
+           enum_smem_bytes(N, L);
 }
-
-cudaError_t build_run(const BuildArgs& A, int grid, cudaStream_t st) {
-    const size_t smem = build_smem(A.N, A.L);
-    cudaError_t e = cudaFuncSetAttribute(build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    build_kernel<<<grid, kBlockThreads, smem, st>>>(A);
-    return cudaGetLastError();
-}
+int build_part_bytes(int M) { return static_cast<int>(sizeof(PartHdr)) + ((M > 0 ? M : 1) * 8 + 15) / 16 * 16; }
 
 }  // namespace spec

@@ -1,4 +1,4 @@
-// spec_walk.cu -- argmax walks on the row-task engine.
+// spec_walk.cu -- argmax walks on the cluster engine.
 //
 // [SD-survey] = "大模型投机解码：Medusa、MTP、EAGLE、DFlash、DDTree 与 DSpark"
 // (Speculative decoding for LLMs: Medusa, MTP, EAGLE, DFlash, DDTree and
@@ -12,27 +12,30 @@
 // row is looked up among the node's children; a matching child is accepted
 // and becomes the current node; otherwise the argmax is the bonus token.
 // Only rows on the walked path are read.
+//
+// One job per row: every CTA of the cluster reduces its vocabulary slice to
+// (max value, lowest index) as a composite key; the slot's leader takes the
+// maximum over the slices and decides.
 #include "spec_chain.cuh"
 #include "spec_select.cuh"
 
 namespace spec {
 
-struct __align__(16) WalkSmem {
-    PipeSmem pipe;
+struct WalkSmem {
     uint64_t red[kWarps];
     uint32_t wb[kWarps];
 };
 
-template <class E>
-__device__ __forceinline__ const void* walk_row(const WalkArgs& A, int b, int i, bool tree) {
+template <class E, bool kTree>
+__device__ __forceinline__ const void* walk_row(const WalkArgs& A, int b, int i) {
     long long r;
-    if (!tree && A.k_per_req) r = static_cast<long long>(A.l_row_off[b] + i) * A.l_rs;
+    if (!kTree && A.k_per_req && A.l_row_off) r = static_cast<long long>(A.l_row_off[b] + i) * A.l_rs;
     else r = static_cast<long long>(b) * A.l_bs + static_cast<long long>(i) * A.l_rs;
     return static_cast<const unsigned char*>(A.logits) + r * E::kBytes;
 }
 
-// combiner warp
-__device__ void greedy_finish(const WalkArgs& A, int b, int n, int last, int st) {
+// combiner warp: the greedy request's outputs
+__device__ Job greedy_finish(const WalkArgs& A, int b, int n, int last, int st) {
     const int W = A.K + 1;
     const int l = threadIdx.x & 31;
     int* out = A.out_tokens + static_cast<long long>(b) * W;
@@ -47,12 +50,12 @@ __device__ void greedy_finish(const WalkArgs& A, int b, int n, int last, int st)
         A.status[b] = st;
     }
     __syncwarp();
-    if (l == 0) finish_request(A.W);
+    return job_done();
 }
 
-// combiner warp; path_nodes[b][0..acc] and out_tokens[b][0..acc-1] were
-// written on the way
-__device__ void tree_finish(const WalkArgs& A, int b, int acc, int last, int st) {
+// combiner warp: the tree walk's outputs; path_nodes[b][1..acc] and
+// out_tokens[b][0..acc-1] were written on the way
+__device__ Job tree_finish(const WalkArgs& A, int b, int acc, int last, int st) {
     const int W = A.L + 1;
     const int l = threadIdx.x & 31;
     int* pn = A.path_nodes + static_cast<long long>(b) * W;
@@ -67,176 +70,109 @@ __device__ void tree_finish(const WalkArgs& A, int b, int acc, int last, int st)
         A.status[b] = st;
     }
     __syncwarp();
-    if (l == 0) finish_request(A.W);
+    return job_done();
 }
 
 template <class E, bool kTree>
-__device__ __forceinline__ bool walk_invalid(const WalkArgs& A, const Task& t) {
-    if (kTree || t.kind >= 0) return false;
-    const int kb = A.k_per_req ? A.k_per_req[t.b] : A.K;
-    return kb < 0 || kb > A.K;
-}
+struct WalkOp {
+    using Args = WalkArgs;
+    using Smem = WalkSmem;
 
-// The combine of one row (combiner warp): argmax over the slice partials,
-// then the greedy decision or the tree step.
-template <class E, bool kTree>
-__device__ void walk_combine(const WalkArgs& A, const Job& job, uint32_t done, uint32_t base) {
-    const int l = threadIdx.x & 31;
-    const int b = job.task.b;
-    const int row = job.task.row;
-    const bool initial = job.task.kind < 0;
-    const int acc = initial ? 0 : job.task.aux;
-    int st = job.task.st;
-    if (job.kind != 0) {   // invalid k
-        greedy_finish(A, b, 0, -1, 16);
-        return;
-    }
-    uint32_t flags = 0;
-    uint64_t best = 0;
-    const int S = task_S(A, job.task);
-    for (int j = l; j < S; j += 32) {
-        const PartHdr* h = part_hdr(A.W, b, j, S);
-        flags |= __ldcg(&h->flags);
-        const uint64_t k = __ldcg(&h->kth);
-        best = k > best ? k : best;
-    }
-    flags = __reduce_or_sync(0xffffffffu, flags);
-    best = warp_max_u64(best);
-    const bool bad_row = (flags & kPfBad) || !(ckey_val(best) > -kInf);
-    const int am = ckey_idx(best);
-    if constexpr (!kTree) {
-        const int kb = A.k_per_req ? A.k_per_req[b] : A.K;
-        if (bad_row) { greedy_finish(A, b, row, -1, st | 1); return; }
-        if (row == kb) { greedy_finish(A, b, row, am, st); return; }
-        const int y = A.draft[static_cast<long long>(b) * A.K + row];
-        if (y < 0 || y >= A.V) st |= 8;
-        if (y != am) { greedy_finish(A, b, row, am, st); return; }
-        if (l == 0) {
-            Task nt;
-            nt.b = b; nt.row = row + 1; nt.kind = 0; nt.aux = 0; nt.st = st; nt.base = base;
-            int S1, SL1;
-            pick_slices(A.B, A.V, A.S, A.S1, done, S1, SL1);
-            push_task(A.W, nt, S1, SL1, false);
+    __device__ static int batch(const Args& A) { return A.B; }
+    __device__ static bool tma(const Args& A) { return A.tma_l != 0; }
+    __device__ static void init_smem(const Args&, const Geo&, Smem&) {}
+    __device__ static Job first(const Args& A, const Geo&, int b, Smem&) {
+        if (!kTree) {
+            const int kb = A.k_per_req ? A.k_per_req[b] : A.K;
+            if (kb < 0 || kb > A.K) return greedy_finish(A, b, 0, -1, 16);
         }
-    } else {
-        if (bad_row) { tree_finish(A, b, acc, -1, st | 1); return; }
-        // lowest child of `row` carrying the argmax token
-        int child = 0x7fffffff;
-        int nn = A.num_nodes[b];
-        nn = nn < A.N ? nn : A.N;
-        const int* par = A.parent + static_cast<long long>(b) * A.N;
-        const int* tok = A.token + static_cast<long long>(b) * A.N;
-        for (int c = l; c < nn; c += 32)
-            if (par[c] == row && tok[c] == am) child = min(child, c);
-        child = static_cast<int>(warp_min_u32(static_cast<uint32_t>(child)));
-        if (child == 0x7fffffff || acc >= A.L) { tree_finish(A, b, acc, am, st); return; }
-        if (l == 0) {
-            const int W = A.L + 1;
-            A.out_tokens[static_cast<long long>(b) * W + acc] = am;
-            A.path_nodes[static_cast<long long>(b) * W + acc + 1] = child;
-            Task nt;
-            nt.b = b; nt.row = child; nt.kind = 0; nt.aux = acc + 1; nt.st = st; nt.base = base;
-            int S1, SL1;
-            pick_slices(A.B, A.V, A.S, A.S1, done, S1, SL1);
-            push_task(A.W, nt, S1, SL1, false);   // outputs only: nothing for later tasks to read
-        }
+        Job j = make_job(b, 0, 0, 0);
+        j.depth = 0;
+        return j;
     }
-}
-
-template <class E, bool kTree>
-__global__ void __launch_bounds__(kBlockThreads, kCtasPerSm) walk_kernel(const WalkArgs A) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    auto& sh = *reinterpret_cast<WalkSmem*>(smem + kStages * kChunkBytes);
-    const Pipe P = pipe_init(smem, sh.pipe);
-    const bool tma = A.tma_l != 0;
-    auto plan = [&](const Task& t, int slice) {
-        if (walk_invalid<E, kTree>(A, t)) return plan_none();
-        const int SL = task_SL(A, t);
-        const int x0 = slice * SL, x1 = min(A.V, x0 + SL);
-        return plan_single(walk_row<E>(A, t.b, t.row, kTree), E::kBytes, x0, x1);
-    };
-    if (threadIdx.x >= kCombiner0) {
-        combiner_loop(P, [&](const Job& job) {
-            uint32_t done;
-            uint32_t base;
-            if (comb_arrive(A.W, job.task, task_S(A, job.task), &done, &base)) walk_combine<E, kTree>(A, job, done, base);
-            __syncwarp();
-        });
-        return;
+    __device__ static StreamPlan plan(const Args& A, const Geo& G, const Job& j) {
+        return plan_single(walk_row<E, kTree>(A, j.b, j.row), E::kBytes, slice_x0(G, G.rank),
+                           slice_x1(G, G.rank, A.V));
     }
-    if (threadIdx.x >= kThreads) {
-        if (threadIdx.x == kProducer)
-            producer_loop(A.W, A.B, A.S, P, tma, [](Claimed&) {},
-                          [&](const Claimed& c) { return plan(c.task, c.slice); });
-        return;
-    }
-    uint32_t seq = 0, jseq = 0, cseq = 0;
-    auto serve = []() {};   // every combine runs on the combiner warp
-    for (uint32_t u = 0;; ++u) {
-        const Claimed cl = next_unit(P, u, cseq, serve);
-        if (!cl.ok) break;
-        const Task t = cl.task;
-        const int s = cl.slice;
-        const int b = t.b;
-        const bool invalid = walk_invalid<E, kTree>(A, t);
-        PartHdr* ph = part_hdr(A.W, b, s, A.S);
-        if (!invalid) {
-            const int x0 = s * task_SL(A, t);
-            ArgmaxFn<E> fn;
-            if (!consume_row<E>(P, seq, plan(t, s), tma, x0, fn)) break;
-            // per warp, then thread 0 over the warps (one barrier)
-            const uint64_t wbest = warp_max_u64(fn.key());
-            const uint32_t wbad = __reduce_or_sync(0xffffffffu, fn.bad_flag());
-            if ((threadIdx.x & 31) == 0) { sh.red[threadIdx.x >> 5] = wbest; sh.wb[threadIdx.x >> 5] = wbad; }
-            csync();
-            if (threadIdx.x == 0) {
-                uint64_t best = 0;
-                uint32_t bad = 0;
-                for (int j = 0; j < kWarps; ++j) { best = sh.red[j] > best ? sh.red[j] : best; bad |= sh.wb[j]; }
-                ph->flags = bad ? kPfBad : 0u;
-                ph->kth = best;
-            }
-        }
+    __device__ static int consume(const Args& A, const Geo& G, const Pipe& P, uint32_t& seq, bool tma, const Job& j,
+                                  Smem& sm, unsigned char* out) {
+        PartHdr* ph = reinterpret_cast<PartHdr*>(out);
+        ArgmaxFn<E> fn;
+        if (!consume_row<E>(P, seq, plan(A, G, j), tma, slice_x0(G, G.rank), fn)) return -1;
+        // per warp, then thread 0 over the warps (one barrier)
+        const uint64_t wbest = warp_max_u64(fn.key());
+        const uint32_t wbad = __reduce_or_sync(0xffffffffu, fn.bad_flag());
+        if ((threadIdx.x & 31) == 0) { sm.red[threadIdx.x >> 5] = wbest; sm.wb[threadIdx.x >> 5] = wbad; }
         csync();
-        Job j;
-        j.task = t; j.slice = s; j.kind = invalid ? 1 : 0; j.stop = 0; j.flags = 0;
-        post_job(P, jseq, cseq, j, serve);
+        if (threadIdx.x == 0) {
+            uint64_t best = 0;
+            uint32_t bad = 0;
+            for (int q = 0; q < kWarps; ++q) { best = sm.red[q] > best ? sm.red[q] : best; bad |= sm.wb[q]; }
+            ph->flags = bad ? kPfBad : 0u;
+            ph->kth = best;
+            ph->cnt = 0;
+        }
+        return static_cast<int>(sizeof(PartHdr));
     }
-    Job j;
-    j.task.b = 0; j.task.row = 0; j.task.kind = 0; j.task.aux = 0; j.task.st = 0; j.task.base = 0;
-    j.slice = 0; j.kind = 0; j.stop = 1; j.flags = 0;
-    post_job(P, jseq, cseq, j, serve);
-}
-
-static size_t walk_smem() { return kStages * kChunkBytes + sizeof(WalkSmem); }
+    __device__ static Job combine(const Args& A, const Geo& G, const Job& j, const unsigned char* parts, Smem&) {
+        const int l = threadIdx.x & 31;
+        const int b = j.b, row = j.row;
+        int st = j.st;
+        uint32_t flags = 0;
+        uint64_t best = 0;
+        if (l < G.C) {
+            const PartHdr* h = part_at(parts, G.part_bytes, l);
+            flags = h->flags;
+            best = h->kth;
+        }
+        flags = __reduce_or_sync(0xffffffffu, flags);
+        best = warp_max_u64(best);
+        const bool bad_row = (flags & kPfBad) || !(ckey_val(best) > -kInf);
+        const int am = ckey_idx(best);
+        if (!kTree) {
+            const int kb = A.k_per_req ? A.k_per_req[b] : A.K;
+            if (bad_row) return greedy_finish(A, b, row, -1, st | 1);
+            if (row == kb) return greedy_finish(A, b, row, am, st);
+            const int y = A.draft[static_cast<long long>(b) * A.K + row];
+            if (y < 0 || y >= A.V) st |= 8;
+            if (y != am) return greedy_finish(A, b, row, am, st);
+            Job nj = make_job(b, row + 1, 0, st);
+            return nj;
+        } else {
+            const int acc = j.depth;
+            if (bad_row) return tree_finish(A, b, acc, -1, st | 1);
+            const int child = find_child_w(A.token, A.parent, A.num_nodes, A.N, b, row, am);
+            if (child < 0 || acc >= A.L) return tree_finish(A, b, acc, am, st);
+            if (l == 0) {
+                const int W = A.L + 1;
+                A.out_tokens[static_cast<long long>(b) * W + acc] = am;
+                A.path_nodes[static_cast<long long>(b) * W + acc + 1] = child;
+            }
+            __syncwarp();
+            Job nj = make_job(b, child, 0, st);
+            nj.depth = acc + 1;
+            return nj;
+        }
+    }
+};
 
 template <class E, bool kTree>
-static cudaError_t walk_launch(const WalkArgs& A, int grid, cudaStream_t st) {
-    const size_t smem = walk_smem();
-    cudaError_t e = cudaFuncSetAttribute(walk_kernel<E, kTree>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    walk_kernel<E, kTree><<<grid, kBlockThreads, smem, st>>>(A);
-    return cudaGetLastError();
+__global__ void __launch_bounds__(kBlockThreads, 1) walk_kernel(const WalkArgs A) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    Engine<WalkOp<E, kTree>>::run(A, A.E.W, make_geo(A.E), smem);
 }
 
 template <class E, bool kTree>
-static int walk_occ() {
-    const int smem = static_cast<int>(walk_smem());
-    int n = 0;
-    cudaFuncSetAttribute(walk_kernel<E, kTree>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, walk_kernel<E, kTree>, kBlockThreads, smem);
-    return n;
+static const void* walk_fn() { return reinterpret_cast<const void*>(&walk_kernel<E, kTree>); }
+
+const void* walk_kernel_ptr(int ldt, int mode) {
+    if (ldt == 0) return mode ? walk_fn<F32, true>() : walk_fn<F32, false>();
+    return mode ? walk_fn<BF16, true>() : walk_fn<BF16, false>();
 }
 
-int walk_occupancy(int ldt, bool tree) {
-    if (ldt == 0) return tree ? walk_occ<F32, true>() : walk_occ<F32, false>();
-    return tree ? walk_occ<BF16, true>() : walk_occ<BF16, false>();
+size_t walk_smem(int C, int own, int part_bytes, int stages) {
+    return Engine<WalkOp<F32, false>>::smem_bytes(C, own, part_bytes, stages);
 }
-
-cudaError_t walk_run(const WalkArgs& A, bool tree, int grid, cudaStream_t st) {
-    if (A.ldt == 0) return tree ? walk_launch<F32, true>(A, grid, st) : walk_launch<F32, false>(A, grid, st);
-    return tree ? walk_launch<BF16, true>(A, grid, st) : walk_launch<BF16, false>(A, grid, st);
-}
+int walk_part_bytes() { return static_cast<int>(sizeof(PartHdr)); }
 
 }  // namespace spec

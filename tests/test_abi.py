@@ -44,11 +44,13 @@ def test_version_and_tuning(lib):
     sv.set_tuning(0, 0)
 
 
-def test_workspace_sizes_grow_with_shape(lib):
+def test_workspace_sizes(lib):
+    # chain / greedy / tree-walk scratch is one control block whatever the
+    # shape; the tree build keeps per-request enumeration state
     a = lib.spec_verify_chain_workspace_size(4, 4, 1000, 0)
     b = lib.spec_verify_chain_workspace_size(256, 8, 151936, 50)
-    assert 0 < a < b
-    assert lib.spec_tree_build_workspace_size(32, 16, 151936, 64) > 0
+    assert 0 < a <= b <= 4096
+    assert 0 < lib.spec_tree_build_workspace_size(4, 16, 151936, 64) < lib.spec_tree_build_workspace_size(32, 16, 151936, 64)
     assert lib.spec_tree_build_workspace_size(32, 17, 151936, 64) == 0      # L > 16 unsupported
     assert lib.spec_tree_build_workspace_size(32, 16, 151936, 257) == 0     # budget > 256
     assert lib.spec_verify_greedy_workspace_size(-1, 3, 10) == 0
@@ -70,7 +72,8 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert _chain(lib, T=0.0) == 1
     assert _chain(lib, T=float("nan")) == 1
     assert _chain(lib, ldt=7) == 1
-    assert _chain(lib, kp=16) == 1                         # ragged needs all three arrays
+    assert _chain(lib, lo=16) == 1                         # row offsets need k_per_req and q offsets
+    assert _chain(lib, kp=16, lo=16) == 1
     assert _chain(lib, logits=None) == 1
     assert _chain(lib, lrs=5) == 1                         # row stride < V
     assert _chain(lib, wsb=16) == 1                        # workspace too small
@@ -91,14 +94,10 @@ def test_package_import_is_lazy_and_fails_loudly(tmp_path, monkeypatch):
 
 
 def test_shape_limits_rejected_on_host(lib):
-    # a pushed unit's record holds the request in 22 bits and the row (or tree
-    # node) in 13: larger shapes are refused before any device work
-    too_many = 4194303
-    assert _chain(lib, B=too_many) == 2
-    assert b"B >" in lib.spec_last_error()
-    assert _chain(lib, B=too_many - 1, wsb=16) == 1        # at the limit: only the tiny workspace is wrong
-    assert lib.spec_verify_greedy(1, 0, 0, 10, 1, too_many, 1, 10, None, None, 1, 1, 1, 16, 1 << 30, None) == 2
+    # documented shape limits are refused before any device work
+    assert _chain(lib, K=4097) == 2
+    assert b"K > 4096" in lib.spec_last_error()
+    assert lib.spec_verify_greedy(1, 0, 0, 10, 1, 2, 4097, 10, None, None, 1, 1, 1, 16, 1 << 30, None) == 2
     assert lib.spec_verify_tree(1, 0, 0, 10, 1, 1, 1, 2, 8193, 10, 4, 1, 1, 1, 1, 16, 1 << 30, None) == 2
-    assert b"N >" in lib.spec_last_error()
-    assert lib.spec_verify_tree(1, 0, 0, 10, 1, 1, 1, too_many, 8, 10, 4, 1, 1, 1, 1, 16, 1 << 30, None) == 2
-    assert lib.spec_tree_build(1, 10, 10, too_many, 4, 10, 8, 1, 1, 1, 1, 1, 1, 1, 16, 1 << 30, None) == 2
+    assert b"N > 8192" in lib.spec_last_error()
+    assert lib.spec_tree_build(1, 10, 10, 2, 4, 10, 257, 1, 1, 1, 1, 1, 1, 1, 16, 1 << 30, None) == 2

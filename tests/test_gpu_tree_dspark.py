@@ -142,6 +142,54 @@ def test_tree_walk_rows_off_path_never_read():
 
 
 # ---------------------------------------------------------------------------
+# stochastic tree walk
+# ---------------------------------------------------------------------------
+def _compare_walk(w, ref, B):
+    """Every request equal to the oracle unless a draw sat within 1e-6 of a
+    CDF boundary (counted, bounded)."""
+    near = 0
+    got = {k: getattr(w, k).cpu().numpy() for k in ("path_nodes", "tokens", "num_accepted", "status")}
+    for b in range(B):
+        same = all(np.array_equal(got[k][b], ref[k][b]) for k in got)
+        if not same:
+            assert ref["near_tie"][b] != 0, (b, {k: (got[k][b], ref[k][b]) for k in got})
+            near += 1
+    assert near <= max(2, B // 100), near
+    return near
+
+
+@pytest.mark.parametrize("B,L,V,N,dtype,T,top_k", [(8, 6, 3000, 24, torch.bfloat16, 1.0, 50),
+                                                   (8, 6, 3000, 24, torch.float32, 0.9, 0),
+                                                   (12, 16, 20011, 64, torch.bfloat16, 0.7, 20),
+                                                   (32, 16, 151936, 64, torch.bfloat16, 1.0, 50)])
+def test_tree_sample_parity(B, L, V, N, dtype, T, top_k):
+    t = workloads.make_tree("ddtree", device=DEV, B=B, L=L, V=V, N=N)
+    g = sv.tree_build(t.q, t.budget)
+    tl = workloads.tree_target_logits(t, g.depth, dtype=dtype)
+    u = workloads.tree_uniforms(t, L)
+    w = sv.verify_tree_sample(tl, g.token, g.parent, g.num_nodes, u, L, T, top_k)
+    torch.cuda.synchronize()
+    assert sv.workspace_error(w.ws) == 0
+    ref_t = oracle.tree_build(host(t.q), t.budget)
+    tlh, uh = host(tl), host(u)
+    ref = run_chunks(lambda a, b: oracle.verify_tree_sample(tlh[a:b], ref_t["token"][a:b], ref_t["parent"][a:b],
+                                                            ref_t["num_nodes"][a:b], uh[a:b], L, T, top_k), B)
+    near = _compare_walk(w, ref, B)
+    print(f"tree sample B={B} V={V} top_k={top_k}: {near} near-tie(s) excused")
+
+
+def test_tree_sample_top1_equals_greedy_walk_on_gpu():
+    t = workloads.make_tree("ddtree", device=DEV, B=16, L=8, V=20011, N=48)
+    g = sv.tree_build(t.q, t.budget)
+    tl = workloads.tree_target_logits(t, g.depth, dtype=torch.float32)
+    u = workloads.tree_uniforms(t, 8)
+    s1 = sv.verify_tree_sample(tl, g.token, g.parent, g.num_nodes, u, 8, 1.0, 1)
+    gw = sv.verify_tree(tl, g.token, g.parent, g.num_nodes, 8)
+    for k in ("path_nodes", "tokens", "num_accepted", "status"):
+        assert torch.equal(getattr(s1, k), getattr(gw, k)), k
+
+
+# ---------------------------------------------------------------------------
 # DSpark verify length + ragged chain verify
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("B,Kmax", [(512, 8), (3, 1), (1000, 16), (7, 0)])
@@ -197,6 +245,38 @@ def test_ragged_verify_parity(over):
     ref = run_chunks(part, w.B)
     near = assert_chain_parity(r, ref, w.K, draft=w.draft)
     print(f"dspark {over}: {w.B} requests compared, {near} near-tie(s) excused")
+
+
+@pytest.mark.parametrize("over", [dict(B=64, V=30011), dict()])
+def test_cap_accept_parity(over):
+    """Page §9's "cap-accept" mode: the dense rows of the full window, each
+    request verifying and committing only its first k_b positions (k_b from
+    the verify-length step); every request against the oracle."""
+    w = workloads.make_chain("dspark", device=DEV, **over)
+    a = sv.adaptive_len(w.conf, 1.0, 0.15)
+    r = sv.verify_chain(w.logits, w.q, w.draft, w.uniforms, w.temperature, w.top_k, k_per_req=a.k, diag=True)
+    torch.cuda.synchronize()
+    assert sv.workspace_error(r.ws) == 0
+    k = a.k.cpu().numpy()
+    lh, qh, dh, uh = host(w.logits), host(w.q), host(w.draft), host(w.uniforms)
+    ref = run_chunks(lambda lo, hi: oracle.verify_chain(lh[lo:hi], qh[lo:hi], dh[lo:hi], uh[lo:hi], w.temperature,
+                                                        w.top_k, k_per_req=k[lo:hi]), w.B)
+    assert_chain_parity(r, ref, w.K, draft=w.draft)
+    g = sv.verify_greedy(w.logits, w.draft, k_per_req=a.k)
+    gref = run_chunks(lambda lo, hi: oracle.verify_greedy(lh[lo:hi], dh[lo:hi], k_per_req=k[lo:hi]), w.B)
+    compare_exact(g.tokens, g.num_accepted, gref)
+
+
+@pytest.mark.parametrize("B,Kmax", [(512, 8), (1000, 16), (5, 0)])
+def test_adaptive_len_table_bit_exact(B, Kmax):
+    g = torch.Generator(device="cpu")
+    g.manual_seed(7 * B + Kmax)
+    c = torch.distributions.Beta(8.0, 2.0).sample((B, Kmax)).float()
+    table = (torch.cumsum(torch.rand(Kmax + 1, generator=g, dtype=torch.float64) * 0.4 + 0.05, 0) + 0.5)
+    a = sv.adaptive_len(c.to(DEV), 1.0, 0.15, cost=table.to(DEV))
+    ref = oracle.adaptive_len(c.numpy(), 1.0, 0.15, cost=table.numpy())
+    for key in ("k", "surv", "exp_adv", "l_row_off", "q_row_off"):
+        assert np.array_equal(getattr(a, key).cpu().numpy(), ref[key]), key
 
 
 def test_ragged_greedy_and_bad_lengths():

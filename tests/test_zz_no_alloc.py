@@ -66,12 +66,16 @@ def test_static_workspace_matches_caller_workspace_twice():
         assert torch.equal(st, ref.status)
 
 
-def test_static_workspace_rejects_oversized_batches():
+def test_static_workspace_limits():
     lib, f = _static_fn()
-    B, K, V = 1 << 16, 8, 151936                    # needs far more than the 8 MiB array
-    assert lib.spec_verify_greedy_workspace_size(B, K, V) > (8 << 20)
+    # greedy scratch is a fixed control block: every batch within the
+    # library's shape limits fits the 64 KiB array
+    assert lib.spec_verify_greedy_workspace_size(1 << 20, 8, 151936) <= (64 << 10)
+    # shapes beyond those limits are refused before any device work
     lg = torch.zeros((1, 1, 64), device=DEV)
     d = torch.zeros((1, 1), dtype=torch.int32, device=DEV)
-    rc = f(_p(lg), 0, 0, V, _p(d), B, K, V, None, None, _p(d), _p(d), _p(d), None)
+    rc = f(_p(lg), 0, 0, 64, _p(d), 1, 4097, 64, None, None, _p(d), _p(d), _p(d), None)
+    assert rc == 2
+    assert b"K > 4096" in lib.spec_last_error()
+    rc = f(_p(lg), 0, 0, 64, _p(d), 1, 1, 0, None, None, _p(d), _p(d), _p(d), None)
     assert rc == 1
-    assert b"static" in lib.spec_last_error()

@@ -235,6 +235,15 @@ def tree_target_logits(tree: TreeInputs, depth: torch.Tensor, seed: Optional[int
     return out.to(dtype).contiguous()
 
 
+def tree_uniforms(tree: TreeInputs, max_depth: int, seed: Optional[int] = None) -> torch.Tensor:
+    """Uniforms [B, max_depth+1] in [0, 1) for a stochastic tree walk (one
+    per depth), seeded."""
+    B = tree.q_logits.shape[0]
+    dev = tree.q_logits.device
+    g = _gen(dev, (seed_of(tree.name) + 4093) if seed is None else seed)
+    return torch.rand((B, max_depth + 1), generator=g, device=dev).contiguous()
+
+
 def rotate_copies(fn, name: str, n: int, **kw):
     """n independently seeded copies of a workload (seeds s, s+100, ...),
     used to keep successive benchmark steps from re-reading rows that the
