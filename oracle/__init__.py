@@ -83,6 +83,9 @@ def _load():
                                                       f32, i32, P, P, P, P, P]
             lib.oracle_verify_tree_sample.restype = None
             lib.oracle_adaptive_len.argtypes = [P, i32, i32, f32, f32, P, P, P, P, P, P, P]
+            lib.oracle_kv_compact.argtypes = [P, i64, i64, i64, P, i64, i64, i64, i32, i32, i32, i64,
+                                              P, i32, P, P]
+            lib.oracle_kv_compact.restype = None
             lib.oracle_adaptive_len.restype = None
             _lib = lib
     return _lib
@@ -263,6 +266,26 @@ def verify_tree_sample(logits, token, parent, num_nodes, uniforms, max_depth, te
                                   B, N, V, max_depth, float(temperature), int(top_k),
                                   _ptr(pn), _ptr(ot), _ptr(na), _ptr(st), _ptr(nt))
     return dict(path_nodes=pn, tokens=ot, num_accepted=na, status=st, near_tie=nt.view(np.uint32))
+
+
+def kv_compact(src, dst, path_nodes, num_accepted, dst_pos=None):
+    """Accepted-path KV compaction (page §5, DDTree): src [P, B, N, R] and
+    dst [P, B, M, R] arrays of any dtype (rows of R elements); returns a copy
+    of dst where row dst_pos[b] + j of every plane holds src row
+    path_nodes[b, j], j = 0..num_accepted[b]."""
+    lib = _load()
+    s = np.ascontiguousarray(src)
+    d = np.array(dst, copy=True, order="C")
+    assert s.dtype == d.dtype and s.ndim == 4 and d.ndim == 4
+    P, B, N, R = s.shape
+    es = s.itemsize
+    pn = np.ascontiguousarray(path_nodes, dtype=np.int32)
+    na = np.ascontiguousarray(num_accepted, dtype=np.int32)
+    dp = None if dst_pos is None else np.ascontiguousarray(dst_pos, dtype=np.int32)
+    lib.oracle_kv_compact(s.ctypes.data_as(ctypes.c_void_p), s.strides[0], s.strides[1], s.strides[2],
+                          d.ctypes.data_as(ctypes.c_void_p), d.strides[0], d.strides[1], d.strides[2],
+                          P, B, N, R * es, _ptr(pn), pn.shape[1], _ptr(na), _ptr(dp))
+    return d
 
 
 def adaptive_len(conf, a, b, cost=None):

@@ -670,6 +670,34 @@ void oracle_verify_tree_sample(
 }
 
 /* ------------------------------------------------------------------ */
+/* [SD-survey] §5 "DDTree": the KV cache keeps the accepted path only.   */
+/* Request b's accepted path is path_nodes[b, 0..n_b] (the root, then    */
+/* the accepted nodes by depth); its rows move, in that order, to        */
+/* destination rows dst_pos[b] + 0 .. dst_pos[b] + n_b of every plane    */
+/* (a layer's keys or values).  Other destination rows are not written.  */
+/* ------------------------------------------------------------------ */
+
+void oracle_kv_compact(
+    const unsigned char* src, int64_t s_plane, int64_t s_batch, int64_t s_row,
+    unsigned char* dst, int64_t d_plane, int64_t d_batch, int64_t d_row,
+    int P, int B, int N, int64_t row_bytes,
+    const int32_t* path_nodes, int W, const int32_t* num_accepted, const int32_t* dst_pos)
+{
+    for (int p = 0; p < P; ++p)
+        for (int b = 0; b < B; ++b) {
+            const int n = num_accepted[b];
+            const int base = dst_pos ? dst_pos[b] : 0;
+            for (int j = 0; j <= n && j < W; ++j) {
+                const int node = path_nodes[(int64_t)b * W + j];
+                if (node < 0 || node >= N) continue;
+                const unsigned char* from = src + p * s_plane + b * s_batch + node * s_row;
+                unsigned char* to = dst + p * d_plane + b * d_batch + (int64_t)(base + j) * d_row;
+                for (int64_t x = 0; x < row_bytes; ++x) to[x] = from[x];
+            }
+        }
+}
+
+/* ------------------------------------------------------------------ */
 /* [SD-survey] §5 "DSpark": s_j = prod_{i<=j} c_i, expected advance      */
 /* 1 + sum_{j<=k} s_j; the verify length maximises advance per cost      */
 /* a + b*k (ties to the smaller k)                                        */

@@ -106,6 +106,17 @@ void oracle_verify_tree_sample(
     int32_t* path_nodes, int32_t* out_tokens, int32_t* num_accepted,
     int32_t* status, int32_t* near_tie);
 
+/* Accepted-path KV compaction ([SD-survey] §5 "DDTree": only the accepted
+ * path's KV is kept).  For every plane p and request b, destination row
+ * dst_pos[b] + j (dst_pos NULL: j) receives source row path_nodes[b, j],
+ * j = 0..num_accepted[b] (node ids outside [0, N) are skipped).  Strides in
+ * bytes; W = path width (max depth + 1). */
+void oracle_kv_compact(
+    const unsigned char* src, int64_t s_plane, int64_t s_batch, int64_t s_row,
+    unsigned char* dst, int64_t d_plane, int64_t d_batch, int64_t d_row,
+    int P, int B, int N, int64_t row_bytes,
+    const int32_t* path_nodes, int W, const int32_t* num_accepted, const int32_t* dst_pos);
+
 /* DSpark prefix survival and adaptive verify length ([SD-survey] §5
  * "DSpark", s_j equation and expected advance).  The cost of verifying k
  * positions is a + b*k, or cost[k] when a table (Kmax+1 entries, [SD-survey]

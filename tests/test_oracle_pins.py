@@ -685,6 +685,43 @@ def test_tree_sample_tokens_follow_target():
 
 
 # ---------------------------------------------------------------------------
+# §5 DDTree: the KV cache keeps only the accepted path
+# ---------------------------------------------------------------------------
+
+
+def test_kv_compact_keeps_the_walked_path_in_depth_order():
+    """Rows tagged with their own (plane, request, node) coordinates: after a
+    constructed walk the destination holds exactly the root and the accepted
+    nodes' rows, in depth order, at each request's cache position; every
+    other destination row keeps its contents."""
+    rng, t, logits, L = _walk_case(81, B=12, L=5, V=60, N=24)
+    walk = oracle.verify_tree(logits, t["token"], t["parent"], t["num_nodes"], L)
+    P, B, N, R = 3, 12, 24, 4
+    src = np.zeros((P, B, N, R), np.int32)
+    for p in range(P):
+        for b in range(B):
+            for n in range(N):
+                src[p, b, n] = [p, b, n, 7]
+    M = 40
+    pos = rng.integers(0, M - (L + 1), B).astype(np.int32)
+    dst = np.full((P, B, M, R), -9, np.int32)
+    out = oracle.kv_compact(src, dst, walk["path_nodes"], walk["num_accepted"], dst_pos=pos)
+    for p in range(P):
+        for b in range(B):
+            n = walk["num_accepted"][b]
+            path = walk["path_nodes"][b, :n + 1]
+            assert path[0] == 0                                        # the root first
+            for j, node in enumerate(path):
+                assert out[p, b, pos[b] + j].tolist() == [p, b, node, 7]
+            # depth order: each kept node's parent is the row before it
+            for j in range(1, n + 1):
+                assert t["parent"][b, path[j]] == path[j - 1]
+            mask = np.ones(M, bool)
+            mask[pos[b]:pos[b] + n + 1] = False
+            assert (out[p, b, mask] == -9).all()
+
+
+# ---------------------------------------------------------------------------
 # §5 DSpark: s_j = prod c_i, advance 1 + sum s_j, k maximising advance/cost
 # ---------------------------------------------------------------------------
 
