@@ -36,6 +36,7 @@ _lock = threading.Lock()
 _lib = None
 
 ST_BAD_ROW, ST_Q_ZERO, ST_R_ZERO, ST_BAD_TOKEN, ST_BAD_K = 1, 2, 4, 8, 16
+ST_TREE_FULL, ST_BAD_NODE = 32, 64
 NEAR_TIE_SAMPLE_BIT = 1 << 31
 MAX_BUDGET = 256   # ranks are stored in one byte per depth
 
@@ -87,6 +88,11 @@ def _load():
                                               P, i32, P, P]
             lib.oracle_kv_compact.restype = None
             lib.oracle_adaptive_len.restype = None
+            lib.oracle_eagle_expand.argtypes = [P, i64, i64, i32, i32, i32, i32, i32, i32,
+                                                P, P, P, P, P, P, P, P, P, P]
+            lib.oracle_eagle_expand.restype = None
+            lib.oracle_eagle_rerank.argtypes = [P, P, P, P, P, i32, i32, i32, P, P, P, P, P, P, P]
+            lib.oracle_eagle_rerank.restype = None
             _lib = lib
     return _lib
 
@@ -286,6 +292,54 @@ def kv_compact(src, dst, path_nodes, num_accepted, dst_pos=None):
                           d.ctypes.data_as(ctypes.c_void_p), d.strides[0], d.strides[1], d.strides[2],
                           P, B, N, R * es, _ptr(pn), pn.shape[1], _ptr(na), _ptr(dp))
     return d
+
+
+def eagle_init(B, G):
+    """EAGLE-2 node arrays of capacity G holding only the root (page §4)."""
+    st = dict(token=np.full((B, G), -1, np.int32), parent=np.full((B, G), -1, np.int32),
+              depth=np.full((B, G), -1, np.int32), score=np.zeros((B, G), np.float64),
+              num_gen=np.ones(B, np.int32))
+    st["depth"][:, 0] = 0
+    st["score"][:, 0] = 1.0
+    return st
+
+
+def eagle_expand(q, state, front, num_front, K2, Fn):
+    """One EAGLE-2 expansion step (page §4): q [B, F, V] holds the draft's
+    conditional rows of the frontier nodes front [B, F] (num_front valid).
+    Updates `state` in place; returns (front_out [B, Fn], num_front_out [B],
+    status [B])."""
+    lib = _load()
+    qa = np.ascontiguousarray(q, dtype=np.float32)
+    B, F, V = qa.shape
+    G = state["token"].shape[1]
+    fi = np.ascontiguousarray(front, dtype=np.int32)
+    nfi = np.ascontiguousarray(num_front, dtype=np.int32)
+    assert fi.shape == (B, F)
+    fo = np.empty((B, Fn), np.int32)
+    nfo = np.empty(B, np.int32)
+    st = np.empty(B, np.int32)
+    for key in ("token", "parent", "depth", "num_gen"):
+        assert state[key].dtype == np.int32 and state[key].flags.c_contiguous
+    lib.oracle_eagle_expand(_ptr(qa), F * V, V, B, F, V, K2, Fn, G,
+                            _ptr(state["token"]), _ptr(state["parent"]), _ptr(state["depth"]),
+                            _ptr(state["score"]), _ptr(state["num_gen"]), _ptr(fi), _ptr(nfi),
+                            _ptr(fo), _ptr(nfo), _ptr(st))
+    return fo, nfo, st
+
+
+def eagle_rerank(state, budget):
+    """EAGLE-2 rerank (page §4): the root and the budget-1 best generated
+    nodes as a verification tree (outputs as tree_build)."""
+    lib = _load()
+    B, G = state["token"].shape
+    o = _tree_out(B, budget)
+    o["status"] = np.empty(B, np.int32)
+    lib.oracle_eagle_rerank(_ptr(state["token"]), _ptr(state["parent"]), _ptr(state["depth"]),
+                            _ptr(state["score"]), _ptr(state["num_gen"]), B, G, budget,
+                            _ptr(o["token"]), _ptr(o["parent"]), _ptr(o["depth"]), _ptr(o["score"]),
+                            _ptr(o["anc_mask"]), _ptr(o["num_nodes"]), _ptr(o["status"]))
+    return o
 
 
 def adaptive_len(conf, a, b, cost=None):

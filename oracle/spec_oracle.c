@@ -467,14 +467,6 @@ void oracle_tree_build(
     free(all); free(lists); free(list_len); free(pend); free(node);
 }
 
-static int cmp_cand(const void* a, const void* b)
-{
-    const orc_cand* x = (const orc_cand*)a;
-    const orc_cand* y = (const orc_cand*)b;
-    if (cand_before(x, y)) return -1;
-    if (cand_before(y, x)) return 1;
-    return 0;
-}
 
 /* Rank of token x in row q_d: how many tokens come before it in the order
  * "probability descending, then id ascending".  Counted pairwise, so that the
@@ -736,4 +728,132 @@ void oracle_adaptive_len(
     }
     if (l_row_off) l_row_off[B] = lo;
     if (q_row_off) q_row_off[B] = qo;
+}
+
+/* ---------------------------------------------------------------------------
+ * EAGLE-2 dynamic draft tree ([SD-survey] §4 "EAGLE-2")
+ * ------------------------------------------------------------------------- */
+
+void oracle_eagle_expand(
+    const float* q, int64_t q_bstride, int64_t q_rstride,
+    int B, int F, int V, int K2, int Fn, int G,
+    int32_t* token, int32_t* parent, int32_t* depth, double* score, int32_t* num_gen,
+    const int32_t* front_in, const int32_t* num_front_in,
+    int32_t* front_out, int32_t* num_front_out, int32_t* status)
+{
+    vid_t* all = (vid_t*)malloc((size_t)(V > 0 ? V : 1) * sizeof(vid_t));
+    vid_t* kids = (vid_t*)malloc((size_t)(K2 > 0 ? K2 : 1) * sizeof(vid_t));
+    char* taken = (char*)malloc((size_t)(G > 0 ? G : 1));
+    for (int b = 0; b < B; ++b) {
+        int32_t* tk = token + (int64_t)b * G;
+        int32_t* pr = parent + (int64_t)b * G;
+        int32_t* dp = depth + (int64_t)b * G;
+        double* sc = score + (int64_t)b * G;
+        int st = 0;
+        int g0 = num_gen[b];
+        if (g0 < 1 || g0 > G) { st |= ORC_ST_BAD_NODE; g0 = g0 < 1 ? 0 : G; }
+        int g = g0;
+        int nf = num_front_in[b];
+        if (nf < 0) nf = 0;
+        if (nf > F) nf = F;
+        /* children of every frontier row, in slot order, ranks in order */
+        for (int f = 0; f < nf; ++f) {
+            const int u = front_in[(int64_t)b * F + f];
+            if (u < 0 || u >= g0) { st |= ORC_ST_BAD_NODE; continue; }
+            const float* row = q + (int64_t)b * q_bstride + (int64_t)f * q_rstride;
+            const int n = depth_list(row, V, K2, all, kids);
+            if (n < 0) { st |= ORC_ST_BAD_ROW; continue; }
+            for (int r = 0; r < n; ++r) {
+                if (g >= G) { st |= ORC_ST_TREE_FULL; break; }
+                tk[g] = kids[r].id;
+                pr[g] = u;
+                dp[g] = dp[u] + 1;
+                sc[g] = sc[u] * kids[r].v;
+                g++;
+            }
+        }
+        num_gen[b] = g;
+        /* the next frontier: repeatedly the best child not yet chosen */
+        const int nc = g - g0;
+        const int nn = Fn < nc ? Fn : nc;
+        memset(taken, 0, (size_t)(G > 0 ? G : 1));
+        for (int j = 0; j < Fn; ++j) front_out[(int64_t)b * Fn + j] = -1;
+        for (int j = 0; j < nn; ++j) {
+            int best = -1;
+            for (int c = g0; c < g; ++c) {
+                if (taken[c]) continue;
+                if (best < 0 || sc[c] > sc[best]) best = c;   /* strict: the earlier wins a tie */
+            }
+            taken[best] = 1;
+            front_out[(int64_t)b * Fn + j] = best;
+        }
+        num_front_out[b] = nn;
+        status[b] = st;
+    }
+    free(all); free(kids); free(taken);
+}
+
+typedef struct { double s; int32_t d; int32_t i; } rerank_t;
+
+/* rerank order: score descending, then depth ascending, then generated first */
+static int cmp_rerank(const void* a, const void* b)
+{
+    const rerank_t* x = (const rerank_t*)a;
+    const rerank_t* y = (const rerank_t*)b;
+    if (x->s > y->s) return -1;
+    if (x->s < y->s) return 1;
+    if (x->d != y->d) return x->d < y->d ? -1 : 1;
+    return (x->i > y->i) - (x->i < y->i);
+}
+
+void oracle_eagle_rerank(
+    const int32_t* token, const int32_t* parent, const int32_t* depth, const double* score,
+    const int32_t* num_gen, int B, int G, int budget,
+    int32_t* out_token, int32_t* out_parent, int32_t* out_depth, double* out_score,
+    uint64_t* anc_mask, int32_t* num_nodes, int32_t* status)
+{
+    const int N = budget;
+    const int W = (N + 63) / 64;
+    rerank_t* cand = (rerank_t*)malloc((size_t)(G > 0 ? G : 1) * sizeof(rerank_t));
+    int32_t* newid = (int32_t*)malloc((size_t)(G > 0 ? G : 1) * sizeof(int32_t));
+    for (int b = 0; b < B; ++b) {
+        const int32_t* tk = token + (int64_t)b * G;
+        const int32_t* pr = parent + (int64_t)b * G;
+        const int32_t* dp = depth + (int64_t)b * G;
+        const double* sc = score + (int64_t)b * G;
+        int32_t* ot = out_token + (int64_t)b * N;
+        int32_t* op = out_parent + (int64_t)b * N;
+        int32_t* od = out_depth + (int64_t)b * N;
+        double* os = out_score + (int64_t)b * N;
+        int st = 0;
+        int g = num_gen[b];
+        if (g < 1 || g > G) { st |= ORC_ST_BAD_NODE; g = g < 1 ? 1 : G; }
+        for (int n = 0; n < N; ++n) { ot[n] = -1; op[n] = -1; od[n] = -1; os[n] = 0.0; }
+        for (int i = 0; i < G; ++i) newid[i] = -1;
+        /* the root, then the generated nodes in rerank order */
+        ot[0] = -1; op[0] = -1; od[0] = 0; os[0] = 1.0;
+        newid[0] = 0;
+        int count = N > 0 ? 1 : 0;
+        int nc = 0;
+        for (int i = 1; i < g; ++i) {
+            cand[nc].s = sc[i]; cand[nc].d = dp[i]; cand[nc].i = i;
+            nc++;
+        }
+        qsort(cand, (size_t)nc, sizeof(rerank_t), cmp_rerank);
+        for (int c = 0; c < nc && count < N; ++c) {
+            const int i = cand[c].i;
+            const int p = pr[i];
+            if (p < 0 || p >= g || newid[p] < 0) { st |= ORC_ST_BAD_NODE; continue; }
+            newid[i] = count;
+            ot[count] = tk[i];
+            op[count] = newid[p];
+            od[count] = dp[i];
+            os[count] = sc[i];
+            count++;
+        }
+        num_nodes[b] = count;
+        status[b] = st;
+        write_masks(op, count, N, anc_mask + (int64_t)b * N * W);
+    }
+    free(cand); free(newid);
 }

@@ -32,6 +32,9 @@ extern "C" {
 #define ORC_ST_BAD_TOKEN    8   /* drafted token id outside [0, V)                */
 #define ORC_ST_BAD_K       16   /* per-request draft length outside [0, K]        */
 
+#define ORC_ST_TREE_FULL   32   /* EAGLE-2: the node arrays' capacity was reached */
+#define ORC_ST_BAD_NODE    64   /* EAGLE-2: a frontier or parent id out of range   */
+
 /* near-tie window (absolute on the ratio, relative to the mass on the CDF) */
 #define ORC_NEAR_TIE 1e-6
 
@@ -126,6 +129,37 @@ void oracle_adaptive_len(
     const float* conf, int B, int Kmax, float a, float b, const double* cost,
     int32_t* k_out, double* surv, double* exp_adv,
     int32_t* l_row_off, int32_t* q_row_off, int32_t* near_tie);
+
+/* EAGLE-2 dynamic draft tree, one expansion step ([SD-survey] §4
+ * "EAGLE-2": the branches of highest cumulative path confidence are
+ * expanded; depth and width follow the context).  Per request b the
+ * generated nodes so far are node arrays of capacity G (token, parent,
+ * depth, score = product of the draft probabilities along the path; node 0
+ * is the root: token -1, parent -1, depth 0, score 1), num_gen[b] of them.
+ * front_in[b, 0..num_front_in[b]) are node ids whose conditional draft rows
+ * q[b, f, 0..V) are given.  For each frontier slot f in order, the K2 most
+ * probable tokens of its row (probability descending, lower id first)
+ * become children, appended in (f, rank) order with score = score(parent) *
+ * q(token).  The next frontier is the Fn children of this step with the
+ * highest score (ties: appended earlier first), in that order, into
+ * front_out[b, 0..Fn), padded with -1; num_front_out[b] of them. */
+void oracle_eagle_expand(
+    const float* q, int64_t q_bstride, int64_t q_rstride,
+    int B, int F, int V, int K2, int Fn, int G,
+    int32_t* token, int32_t* parent, int32_t* depth, double* score, int32_t* num_gen,
+    const int32_t* front_in, const int32_t* num_front_in,
+    int32_t* front_out, int32_t* num_front_out, int32_t* status);
+
+/* EAGLE-2 rerank ([SD-survey] §4 "EAGLE-2": every candidate is reranked and
+ * the best form the verification tree).  The tree is the root and the
+ * budget - 1 generated nodes of highest score (ties: smaller depth, then
+ * generated earlier), emitted in that order -- a parent always precedes its
+ * children -- with parent ids renumbered.  Outputs as oracle_tree_build. */
+void oracle_eagle_rerank(
+    const int32_t* token, const int32_t* parent, const int32_t* depth, const double* score,
+    const int32_t* num_gen, int B, int G, int budget,
+    int32_t* out_token, int32_t* out_parent, int32_t* out_depth, double* out_score,
+    uint64_t* anc_mask, int32_t* num_nodes, int32_t* status);
 
 #ifdef __cplusplus
 }
