@@ -321,7 +321,94 @@ def make_dspark_case(dev, copies):
                 launches_per_step=2, e2e=e2e, dtype="bf16")
 
 
-WORKLOAD_CHOICES = ["dflash", "dflash_vs", "eagle3", "eagle3_greedy", "chain_small", "ddtree", "dspark"]
+def eagle_node_paths(token, parent, num_gen, b):
+    """token path of every generated node of request b (host arrays)"""
+    out = {0: ()}
+    for i in range(1, int(num_gen[b])):
+        out[i] = out[int(parent[b, i])] + (int(token[b, i]),)
+    return out
+
+
+class EagleInputs:
+    """The conditional draft rows of every expansion step of an EAGLE-2
+    tree: step s's rows q[s] [B, F_s, V] belong to the frontier that step
+    s - 1 selected (found once by a first run, the same every run)."""
+
+    def __init__(self, cfg, q, fronts):
+        self.cfg = cfg
+        self.q = q              # list of [B, F_s, V] tensors
+        self.fronts = fronts    # list of (front [B, F_s] int32, num_front [B] int32) tensors
+        self.B, self.V = cfg["B"], cfg["V"]
+        self.K2, self.Fn, self.steps, self.N = cfg["K2"], cfg["Fn"], cfg["steps"], cfg["N"]
+        self.G = 1 + self.K2 + (self.steps - 1) * self.Fn * self.K2
+
+
+def eagle_rows_for(state_host, front, nfront, V, seed, dev):
+    import workloads
+    tok, par, ng = state_host
+    paths = []
+    for b in range(front.shape[0]):
+        pb = eagle_node_paths(tok, par, ng, b)
+        paths.append([pb[int(front[b, f])] if f < nfront[b] else None for f in range(front.shape[1])])
+    return workloads.eagle2_rows(paths, V, seed, device=dev)
+
+
+def make_eagle_case(dev, copies):
+    import workloads
+    import speculative_decoding_draft_sampling_gb300 as sv
+    cfg = dict(workloads.DEFAULTS["eagle2"])
+    B, V, K2, Fn, steps, N = cfg["B"], cfg["V"], cfg["K2"], cfg["Fn"], cfg["steps"], cfg["N"]
+    G = 1 + K2 + (steps - 1) * Fn * K2
+    seed = workloads.seed_of("eagle2")
+    st = sv.eagle_state(B, G, dev)
+    front = torch.zeros((B, 1), dtype=torch.int32, device=dev)
+    nf = torch.ones(B, dtype=torch.int32, device=dev)
+    qs, fronts = [], []
+    for _ in range(steps):
+        q = eagle_rows_for((st.token.cpu().numpy(), st.parent.cpu().numpy(), st.num_gen.cpu().numpy()),
+                           front.cpu().numpy(), nf.cpu().numpy(), V, seed, dev)
+        qs.append(q)
+        fronts.append((front, nf))
+        front, nf, _ = sv.eagle_expand(q, st, front, nf, K2, Fn)
+    inp = EagleInputs(cfg, qs, fronts)
+    # preallocated outputs and workspaces: each step's calls are fixed
+    outs_f = [(torch.empty((B, Fn), dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.int32, device=dev),
+               torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(steps)]
+    ws = [sv.workspace(sv.lib().spec_eagle_expand_workspace_size(B, q.shape[1], K2), dev) for q in qs]
+    tree = sv.eagle_rerank(st, N)
+    torch.cuda.synchronize()
+    rows = sum(int(fr[1].cpu().numpy().clip(0, q.shape[1]).sum()) for q, fr in zip(qs, fronts))
+    nbytes = rows * V * 4 + B * G * (4 * 3 + 8) + B * N * (4 * 3 + 8 + 8)
+
+    def step(i):
+        st.num_gen.fill_(1)
+        fr, n = fronts[0]
+        for s in range(steps):
+            fo, no, so = outs_f[s]
+            sv.eagle_expand(qs[s], st, fr, n, K2, Fn, front_out=fo, num_front_out=no, status=so, ws=ws[s])
+            fr, n = fo, no
+        sv.eagle_rerank(st, N, out=tree)
+
+    def e2e():
+        h_in = [pinned(q) for q in qs]
+        d_in = [torch.empty_like(q) for q in qs]
+
+        def call():
+            s2 = sv.eagle_state(B, G, dev)
+            fr, n = fronts[0]
+            for s in range(steps):
+                fr, n, _ = sv.eagle_expand(d_in[s], s2, fr, n, K2, Fn)
+            t = sv.eagle_rerank(s2, N)
+            return [t.token, t.parent, t.depth, t.num_nodes]
+        return h_in, d_in, call
+
+    ccfg = dict(workload="eagle2", B=B, V=V, steps=steps, children_per_node=K2, frontier=Fn, budget=N,
+                q_dtype="float32", node_capacity=G)
+    return dict(step=step, positions=B * (N - 1), bytes=[nbytes] * copies, cfg=ccfg, inputs=[inp], outs=[tree],
+                state=st, launches_per_step=2 * steps + 1, e2e=e2e, dtype="f32")
+
+
+WORKLOAD_CHOICES = ["dflash", "dflash_vs", "eagle3", "eagle3_greedy", "chain_small", "ddtree", "dspark", "eagle2"]
 
 
 def make_case(name, dev, copies, over=None):
@@ -331,6 +418,8 @@ def make_case(name, dev, copies, over=None):
         return make_tree_case(dev, copies)
     if name == "dspark":
         return make_dspark_case(dev, copies)
+    if name == "eagle2":
+        return make_eagle_case(dev, copies)
     if name == "eagle3_greedy":
         return make_chain_case("eagle3", dev, copies, greedy=True, over=over)
     return make_chain_case(name, dev, copies, over=over)
@@ -367,6 +456,11 @@ class OracleJob:
     def __init__(self, name, w, target=None):
         self.name = name
         self.w = w
+        if name == "eagle2":
+            self.q = [host_view(q) for q in w.q]
+            self.B, self.V = w.B, w.V
+            self.per_req = w.N - 1
+            return
         if name == "ddtree":
             self.q = host_view(w.q)
             self.tl = host_view(target)
@@ -383,6 +477,15 @@ class OracleJob:
     def run(self, lo, hi):
         import oracle
         w = self.w
+        if self.name == "eagle2":
+            st = oracle.eagle_init(hi - lo, w.G)
+            fr = np.zeros((hi - lo, 1), np.int32)
+            nf = np.ones(hi - lo, np.int32)
+            for s in range(w.steps):
+                fr, nf, _ = oracle.eagle_expand(self.q[s][lo:hi], st, fr, nf, w.K2, w.Fn)
+            out = {f"tree_{k}": v for k, v in oracle.eagle_rerank(st, w.N).items()}
+            out["positions"] = np.full(hi - lo, self.per_req, np.int64)
+            return out
         if self.name == "ddtree":
             tr = oracle.tree_build(self.q[lo:hi], w.budget)
             wk = oracle.verify_tree(self.tl[lo:hi], tr["token"], tr["parent"], tr["num_nodes"], self.L)
@@ -456,7 +559,11 @@ def parity_report(case, job):
     ref, _, el = run_threads(job, list(range(job.B)), os.cpu_count() or 1)
     out = case["outs"][0]
     mism, near, flagged = 0, 0, 0
-    if name == "ddtree":
+    if name == "eagle2":
+        for k in ("token", "parent", "depth", "score", "num_nodes", "status"):
+            g = getattr(out, k).cpu().numpy()
+            mism += int((g != ref["tree_" + k]).reshape(g.shape[0], -1).any(1).sum())
+    elif name == "ddtree":
         tr = case["trees"][0]
         for k in ("token", "parent", "depth", "score", "num_nodes", "status"):
             g = getattr(tr, k).cpu().numpy()
@@ -518,6 +625,22 @@ def reference_job(name):
     import workloads
     import oracle
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    if name == "eagle2":
+        # the frontier of every step from the oracle itself
+        cfg = dict(workloads.DEFAULTS["eagle2"])
+        B, V, K2, Fn, steps, N = cfg["B"], cfg["V"], cfg["K2"], cfg["Fn"], cfg["steps"], cfg["N"]
+        G = 1 + K2 + (steps - 1) * Fn * K2
+        st = oracle.eagle_init(B, G)
+        fr, nf = np.zeros((B, 1), np.int32), np.ones(B, np.int32)
+        qs, fronts = [], []
+        for _ in range(steps):
+            q = eagle_rows_for((st["token"], st["parent"], st["num_gen"]), fr, nf, V, workloads.seed_of("eagle2"), dev)
+            qs.append(q)
+            fronts.append((fr, nf))
+            fr, nf, _ = oracle.eagle_expand(host_view(q), st, fr, nf, K2, Fn)
+        ccfg = dict(workload="eagle2", B=B, V=V, steps=steps, children_per_node=K2, frontier=Fn, budget=N,
+                    q_dtype="float32", node_capacity=G)
+        return OracleJob(name, EagleInputs(cfg, qs, fronts)), ccfg
     if name == "ddtree":
         t = workloads.make_tree("ddtree", device=dev)
         depth = oracle.tree_build(host_view(t.q), t.budget)["depth"]
@@ -615,6 +738,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="time eager calls instead of CUDA-graph replays")
     ap.add_argument("--B", type=int, default=0, help="override the batch size of a chain workload (sweeps)")
     ap.add_argument("--slices", type=int, default=0, help="CTAs per cluster, one row slice each (0 = automatic)")
     ap.add_argument("--slots-per-cta", type=int, default=0, help="requests in flight per CTA (0 = automatic)")
@@ -634,10 +758,28 @@ def main():
     sv.set_tuning(args.slices, args.slots_per_cta)
     case = make_case(args.workload, dev, args.copies, over={"B": args.B} if args.B > 0 else None)
     step = case["step"]
-    stream = torch.cuda.current_stream()
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
+    if not args.no_graph:
+        # the steps as a serving loop issues them: each input copy's calls
+        # captured once into a CUDA graph and replayed (the library's calls
+        # are one memset and one kernel launch each, on the caller's stream)
+        graphs = []
+        cap_stream = torch.cuda.Stream()
+        with torch.cuda.stream(cap_stream):
+            for c in range(args.copies):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap_stream, capture_error_mode="thread_local"):
+                    step(c)
+                graphs.append(g)
+        torch.cuda.synchronize()
+        eager = step
+        step = lambda i: graphs[i % args.copies].replay()
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
 
     # timed region: per-step events on the launching stream
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -679,7 +821,8 @@ def main():
     if rank == 0:
         cfg = dict(case["cfg"])
         cfg.update(parallelism=f"dp{world}", l2=f"steps rotate over {args.copies} seeded input copies",
-                   bytes_per_step=int(bytes_step))
+                   bytes_per_step=int(bytes_step),
+                   launch="eager calls" if args.no_graph else "CUDA-graph replay of the library calls")
         line = dict(metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps, warmup=args.warmup,
                     ms_per_step=ms_per_step, higher_is_better=True, scaling="weak", vs_baseline=None,
                     dtype=case["dtype"], data="synthetic (seeded)", config=cfg,

@@ -62,6 +62,8 @@ typedef enum {
                                  token was sampled from p instead */
 #define SPEC_ST_BAD_TOKEN 8   /* a drafted or tree token id outside [0, V) */
 #define SPEC_ST_BAD_K    16   /* per-request draft length outside [0, K] */
+#define SPEC_ST_TREE_FULL 32  /* EAGLE-2: the node arrays' capacity G was reached */
+#define SPEC_ST_BAD_NODE  64  /* EAGLE-2: a frontier or parent id (or num_gen) out of range */
 
 /* workspace error bits */
 #define SPEC_WS_ERR_WAIT     1u   /* a bounded device wait gave up; outputs invalid */
@@ -209,6 +211,61 @@ spec_status spec_tree_build(
     void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * spec_eagle_expand -- one expansion step of an EAGLE-2 dynamic draft tree
+ * [SD-survey] §4 "EAGLE-2": candidates grow along the branches of highest
+ * cumulative path confidence; the tree's depth and width follow the context.
+ *
+ * Node arrays of capacity G per request (caller-owned, in/out):
+ *   token, parent, depth [B, G] int32; score [B, G] fp64 = the product of
+ *   the draft probabilities along the node's path; num_gen [B] = nodes so
+ *   far.  Node 0 is the root (token -1, parent -1, depth 0, score 1,
+ *   num_gen 1) -- the caller initialises it.
+ *   q        [B, F, V] fp32: row (b, f) at b*q_batch_stride + f*q_row_stride
+ *            is the draft's conditional distribution after the path of node
+ *            front_in[b, f], f < num_front_in[b] (other rows are not read).
+ *   K2       children per expanded node: its row's K2 most probable tokens
+ *            (probability descending, lower id first), 1 <= K2 <= 255.
+ *   Fn       next frontier width, 0 <= Fn <= 64; F <= 64; F * K2 <= 2048;
+ *            G <= 8192.
+ * The children are appended in (slot, rank) order with depth = parent's + 1
+ * and score = parent's score * q; when G is reached the rest are dropped
+ * (SPEC_ST_TREE_FULL).  front_out [B, Fn] receives the Fn appended children
+ * of highest score (ties: appended first), padded with -1; num_front_out [B]
+ * their count.  A row holding NaN/+Inf adds no children (SPEC_ST_BAD_ROW);
+ * a frontier id outside [0, num_gen) is skipped (SPEC_ST_BAD_NODE).
+ * status [B] is written, not accumulated.  front_in and front_out must not
+ * overlap; ws as sized below, 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+size_t spec_eagle_expand_workspace_size(int B, int F, int K2);
+spec_status spec_eagle_expand(
+    const float* q, int64_t q_batch_stride, int64_t q_row_stride,
+    int B, int F, int V, int K2, int Fn, int G,
+    int32_t* token, int32_t* parent, int32_t* depth, double* score, int32_t* num_gen,
+    const int32_t* front_in, const int32_t* num_front_in,
+    int32_t* front_out, int32_t* num_front_out, int32_t* status,
+    void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * spec_eagle_rerank -- the EAGLE-2 verification tree
+ * [SD-survey] §4 "EAGLE-2": every generated candidate is reranked and the
+ * best form the tree the target verifies.
+ *
+ * The tree is the root and the budget-1 generated nodes of highest score
+ * (ties: smaller depth, then lower index), emitted in that order -- a
+ * parent always precedes its children -- with parents renumbered.  Outputs
+ * exactly as spec_tree_build (token, parent, depth, score, anc_mask
+ * [B, budget, ceil(budget/64)], num_nodes, status), so the tree feeds
+ * spec_verify_tree, spec_verify_tree_sample and spec_kv_compact.
+ * 1 <= budget <= 1024, G <= 8192.  A generated node whose parent is out of
+ * range or not emitted before it is skipped (SPEC_ST_BAD_NODE).
+ * ---------------------------------------------------------------------- */
+spec_status spec_eagle_rerank(
+    const int32_t* token, const int32_t* parent, const int32_t* depth, const double* score,
+    const int32_t* num_gen, int B, int G, int budget,
+    int32_t* out_token, int32_t* out_parent, int32_t* out_depth, double* out_score,
+    uint64_t* anc_mask, int32_t* num_nodes, int32_t* status, void* stream);
+
+/* ------------------------------------------------------------------------
  * spec_verify_tree -- greedy tree-walk verification
  * [SD-survey] §5 "DDTree": verification walks the target-selected token;
  * when no child of the current node carries it, that token becomes the
@@ -255,6 +312,35 @@ spec_status spec_verify_tree_sample(
     int B, int N, int V, int max_depth, float temperature, int top_k,
     int32_t* path_nodes, int32_t* out_tokens, int32_t* num_accepted, int32_t* status,
     void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * spec_kv_compact -- keep the accepted path's KV rows
+ * [SD-survey] §5 "DDTree": after the tree walk only the accepted path's KV
+ * is kept.  The tree's forward pass wrote one KV row per tree node; for
+ * every plane p (a layer's keys or values) and request b, the rows of the
+ * root and the accepted nodes, path_nodes[b, 0..num_accepted[b]], move in
+ * that order to destination rows dst_pos[b] + 0 .. dst_pos[b] +
+ * num_accepted[b] (dst_pos NULL: rows 0 ..).  No other destination row is
+ * written.  A gather bound by HBM bandwidth.
+ *
+ *   src      DEVICE, row (p, b, n) at src + p*src_plane_stride +
+ *            b*src_batch_stride + n*src_row_stride (strides in BYTES), n < N.
+ *   dst      DEVICE, row (p, b, m) at dst + p*dst_plane_stride +
+ *            b*dst_batch_stride + m*dst_row_stride (bytes).  The rows written
+ *            must not overlap the rows read (copy from the tree's own buffer
+ *            into the cache, not within one buffer).
+ *   row_bytes  bytes of one row (a 16-byte-aligned layout moves 16 bytes a
+ *            load; others 4 or 1).
+ *   path_nodes [B, path_width], num_accepted [B] (spec_verify_tree or
+ *            spec_verify_tree_sample outputs); node ids outside [0, N) are
+ *            skipped.  dst_pos NULL or [B] int32.
+ * ---------------------------------------------------------------------- */
+spec_status spec_kv_compact(
+    const void* src, int64_t src_plane_stride, int64_t src_batch_stride, int64_t src_row_stride,
+    void* dst, int64_t dst_plane_stride, int64_t dst_batch_stride, int64_t dst_row_stride,
+    int P, int B, int N, int64_t row_bytes,
+    const int32_t* path_nodes, int path_width, const int32_t* num_accepted, const int32_t* dst_pos,
+    void* stream);
 
 /* ------------------------------------------------------------------------
  * spec_adaptive_len -- DSpark verify length

@@ -14,6 +14,7 @@ Functions (same names as the C entry points, without the ``spec_`` prefix):
   tree_build     DDTree best-first tree under a node budget
   verify_tree    greedy tree-walk verification
   verify_tree_sample  stochastic tree-walk verification (target draws along the tree)
+  kv_compact     keep the accepted path's KV rows
   adaptive_len   DSpark survival, expected advance and verify length
 """
 from __future__ import annotations
@@ -71,11 +72,18 @@ def _load():
         lib.spec_tree_build_workspace_size.argtypes = [i32, i32, i32, i32]
         lib.spec_tree_build_workspace_size.restype = sz
         lib.spec_tree_build.argtypes = [P, i64, i64, i32, i32, i32, i32, P, P, P, P, P, P, P, P, sz, P]
+        lib.spec_eagle_expand_workspace_size.argtypes = [i32, i32, i32]
+        lib.spec_eagle_expand_workspace_size.restype = sz
+        lib.spec_eagle_expand.argtypes = [P, i64, i64, i32, i32, i32, i32, i32, i32,
+                                          P, P, P, P, P, P, P, P, P, P, P, sz, P]
+        lib.spec_eagle_rerank.argtypes = [P, P, P, P, P, i32, i32, i32, P, P, P, P, P, P, P, P]
         lib.spec_verify_tree_workspace_size.argtypes = [i32, i32, i32]
         lib.spec_verify_tree_workspace_size.restype = sz
         lib.spec_verify_tree.argtypes = [P, i32, i64, i64, P, P, P, i32, i32, i32, i32, P, P, P, P, P, sz, P]
         lib.spec_adaptive_len.argtypes = [P, i32, i32, f32, f32, P, P, P, P, P, P]
         lib.spec_adaptive_len_table.argtypes = [P, i32, i32, P, P, P, P, P, P, P]
+        lib.spec_kv_compact.argtypes = [P, i64, i64, i64, P, i64, i64, i64, i32, i32, i32, i64, P, i32, P, P, P]
+        lib.spec_kv_compact.restype = ctypes.c_int
         lib.spec_adaptive_len_table.restype = ctypes.c_int
         lib.spec_verify_tree_sample_workspace_size.argtypes = [i32, i32, i32]
         lib.spec_verify_tree_sample_workspace_size.restype = sz
@@ -335,6 +343,89 @@ def tree_build(q, budget: int, *, out: Optional[Tree] = None, ws: Optional[torch
 
 
 @dataclass
+class EagleState:
+    """EAGLE-2 node arrays of capacity G (page §4): the generated candidates."""
+    token: torch.Tensor        # [B, G] int32
+    parent: torch.Tensor       # [B, G] int32
+    depth: torch.Tensor        # [B, G] int32
+    score: torch.Tensor        # [B, G] fp64, product of draft probabilities along the path
+    num_gen: torch.Tensor      # [B] int32
+
+
+def eagle_state(B: int, G: int, device) -> EagleState:
+    """Node arrays holding only the root (node 0: token -1, depth 0, score 1)."""
+    st = EagleState(torch.full((B, G), -1, dtype=torch.int32, device=device),
+                    torch.full((B, G), -1, dtype=torch.int32, device=device),
+                    torch.full((B, G), -1, dtype=torch.int32, device=device),
+                    torch.zeros((B, G), dtype=torch.float64, device=device),
+                    torch.ones(B, dtype=torch.int32, device=device))
+    st.depth[:, 0] = 0
+    st.score[:, 0] = 1.0
+    return st
+
+
+def eagle_expand(q, state: EagleState, front, num_front, K2: int, Fn: int, *, front_out=None,
+                 num_front_out=None, status=None, ws: Optional[torch.Tensor] = None, stream=None):
+    """One EAGLE-2 expansion step (page §4): q [B, F, V] fp32 holds the draft's
+    conditional rows of the frontier nodes front [B, F] (num_front [B] valid).
+    Appends the children to `state`; returns (front_out [B, Fn], num_front_out
+    [B], status [B])."""
+    Lb = _load()
+    _cuda(q, "q", torch.float32)
+    if q.dim() != 3 or q.stride(-1) != 1:
+        raise SpecError("q must be [B, F, V] with unit element stride")
+    B, F, V = q.shape
+    G = state.token.shape[1]
+    _cuda(front, "front", torch.int32)
+    _cuda(num_front, "num_front", torch.int32)
+    for name in ("token", "parent", "depth", "num_gen"):
+        _cuda(getattr(state, name), name, torch.int32)
+    _cuda(state.score, "score", torch.float64)
+    if tuple(front.shape) != (B, F) or not front.is_contiguous():
+        raise SpecError("front must be a contiguous [B, F] tensor")
+    dev = q.device
+    if front_out is None:
+        front_out = torch.empty((B, Fn), dtype=torch.int32, device=dev)
+    if num_front_out is None:
+        num_front_out = torch.empty(B, dtype=torch.int32, device=dev)
+    if status is None:
+        status = torch.empty(B, dtype=torch.int32, device=dev)
+    need = Lb.spec_eagle_expand_workspace_size(B, F, K2)
+    if ws is None:
+        ws = workspace(need, dev)
+    rc = Lb.spec_eagle_expand(_p(q), q.stride(0), q.stride(1), B, F, V, int(K2), int(Fn), G,
+                              _p(state.token), _p(state.parent), _p(state.depth), _p(state.score),
+                              _p(state.num_gen), _p(front), _p(num_front), _p(front_out), _p(num_front_out),
+                              _p(status), _p(ws), ws.numel(), _stream(stream))
+    _check(rc, "spec_eagle_expand")
+    return front_out, num_front_out, status
+
+
+def eagle_rerank(state: EagleState, budget: int, *, out: Optional[Tree] = None, stream=None) -> Tree:
+    """The EAGLE-2 verification tree (page §4): the root and the budget-1
+    best generated nodes, in the layout tree_build returns."""
+    Lb = _load()
+    B, G = state.token.shape
+    N = int(budget)
+    W = (N + 63) // 64
+    dev = state.token.device
+    if out is None:
+        out = Tree(torch.empty((B, N), dtype=torch.int32, device=dev),
+                   torch.empty((B, N), dtype=torch.int32, device=dev),
+                   torch.empty((B, N), dtype=torch.int32, device=dev),
+                   torch.empty((B, N), dtype=torch.float64, device=dev),
+                   torch.empty((B, N, W), dtype=torch.int64, device=dev),
+                   torch.empty(B, dtype=torch.int32, device=dev),
+                   torch.empty(B, dtype=torch.int32, device=dev), None)
+    rc = Lb.spec_eagle_rerank(_p(state.token), _p(state.parent), _p(state.depth), _p(state.score),
+                              _p(state.num_gen), B, G, N,
+                              _p(out.token), _p(out.parent), _p(out.depth), _p(out.score), _p(out.anc_mask),
+                              _p(out.num_nodes), _p(out.status), _stream(stream))
+    _check(rc, "spec_eagle_rerank")
+    return out
+
+
+@dataclass
 class TreeWalk:
     path_nodes: torch.Tensor   # [B, L+1]
     tokens: torch.Tensor       # [B, L+1]
@@ -412,6 +503,37 @@ def verify_tree_sample(logits, token, parent, num_nodes, uniforms, max_depth: in
                                     _p(ws), ws.numel(), _stream(stream))
     _check(rc, "spec_verify_tree_sample")
     return out
+
+
+def kv_compact(src, dst, path_nodes, num_accepted, dst_pos=None, stream=None):
+    """Keep the accepted path's KV rows (page §5, DDTree): src [P, B, N, ...]
+    (one row per tree node), dst [P, B, M, ...] (the cache), same dtype and
+    row shape; row dst_pos[b] + j of dst receives src row path_nodes[b, j],
+    j = 0..num_accepted[b].  In place on dst."""
+    Lb = _load()
+    _cuda(src, "src")
+    _cuda(dst, "dst", src.dtype)
+    _cuda(path_nodes, "path_nodes", torch.int32)
+    _cuda(num_accepted, "num_accepted", torch.int32)
+    if src.dim() < 4 or dst.dim() != src.dim() or src.shape[3:] != dst.shape[3:]:
+        raise SpecError("src [P, B, N, ...] and dst [P, B, M, ...] with the same row shape")
+    if src.shape[:2] != dst.shape[:2]:
+        raise SpecError("src and dst need the same P and B")
+    row = src[0, 0, 0]
+    if not (src.stride(-1) == 1 and row.is_contiguous() and dst[0, 0, 0].is_contiguous()):
+        raise SpecError("rows must be contiguous")
+    es = src.element_size()
+    P, B, N = src.shape[:3]
+    if not path_nodes.is_contiguous() or path_nodes.dim() != 2 or path_nodes.shape[0] != B:
+        raise SpecError("path_nodes must be a contiguous [B, path_width] tensor")
+    if dst_pos is not None:
+        _cuda(dst_pos, "dst_pos", torch.int32)
+    rc = Lb.spec_kv_compact(_p(src), src.stride(0) * es, src.stride(1) * es, src.stride(2) * es,
+                            _p(dst), dst.stride(0) * es, dst.stride(1) * es, dst.stride(2) * es,
+                            P, B, N, row.numel() * es, _p(path_nodes), path_nodes.shape[1], _p(num_accepted),
+                            _p(dst_pos), _stream(stream))
+    _check(rc, "spec_kv_compact")
+    return dst
 
 
 # ---------------------------------------------------------------------------

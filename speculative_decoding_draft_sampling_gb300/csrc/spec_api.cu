@@ -76,7 +76,8 @@ int cluster_size_for(int V) {
 struct Plan {
     spec::EngArgs E;
     size_t smem;
-    int clusters;
+    int clusters;   // clusters launched
+    int resident;   // clusters the device holds at once
 };
 
 // Cached occupancy per (kernel, cluster size, shared memory) and device.
@@ -126,41 +127,87 @@ int max_clusters(const void* fn, int C, size_t smem, cudaError_t& err) {
 }
 
 // Geometry: cluster size, slots, slice length, ring depth (as many stages as
-// fit next to the rest of the shared memory, at most kStages).
+// fit next to the rest of the shared memory, at most kStages).  Requests
+// spread over every cluster that fits on the device: a cluster keeps
+// R = ceil(B / clusters) of them in flight (at most slots_per_cta per CTA),
+// so small batches still use every SM.
+template <class SmemFn>
+spec_status make_plan_c(const char* who, const void* fn, int C, int V, int part_bytes, int B, SmemFn smem_of,
+                        Plan& pl);
+
+// The automatic cluster size also weighs how many SMs its clusters cover:
+// clusters must fit inside a GPC, so the largest size can leave SMs idle.
 template <class SmemFn>
 spec_status make_plan(const char* who, const void* fn, int V, int part_bytes, int B, SmemFn smem_of, Plan& pl) {
     const int C = cluster_size_for(V);
-    int spc = g_tune_spc > 0 ? g_tune_spc : kDefaultSpc;
-    if (spc > spec::kMaxOwn) spc = spec::kMaxOwn;
-    if (C * spc > spec::kMaxSlots) spc = spec::kMaxSlots / C;
+    spec_status s = make_plan_c(who, fn, C, V, part_bytes, B, smem_of, pl);
+    if (s != SPEC_OK || g_tune_c > 0 || C < 4) return s;
+    Plan half;
+    if (make_plan_c(who, fn, C / 2, V, part_bytes, B, smem_of, half) != SPEC_OK) return s;
+    // compare the SMs each plan can keep busy (all resident clusters)
+    if (half.resident * (C / 2) > pl.resident * C * 21 / 20) pl = half;
+    return SPEC_OK;
+}
+
+template <class SmemFn>
+spec_status make_plan_c(const char* who, const void* fn, int C, int V, int part_bytes, int B, SmemFn smem_of,
+                        Plan& pl) {
+    int spc_max = g_tune_spc > 0 ? g_tune_spc : kDefaultSpc;
+    if (spc_max > spec::kMaxOwn) spc_max = spec::kMaxOwn;
+    if (C * spc_max > spec::kMaxSlots) spc_max = spec::kMaxSlots / C;
     const int optin = smem_optin();
+    // large stages when at least two fit (fewer waits and releases per
+    // byte), else small ones
+    int chunk = spec::kChunkLarge;
+    auto fit = [&](int own, int& stages, size_t& smem) {
+        const size_t base = smem_of(C, own, part_bytes, 0, spec::kChunkSmall);
+        stages = 0;
+        if (optin <= 0 || base > static_cast<size_t>(optin)) return false;
+        const size_t room = static_cast<size_t>(optin) - base;
+        if (room >= 2ull * spec::kChunkLarge) {
+            chunk = spec::kChunkLarge;
+        } else if (room >= 2ull * spec::kChunkSmall) {
+            chunk = spec::kChunkSmall;
+        } else {
+            return false;
+        }
+        stages = static_cast<int>(room / chunk);
+        if (stages > spec::kStages) stages = spec::kStages;
+        smem = smem_of(C, own, part_bytes, stages, chunk);
+        return true;
+    };
     int stages = 0;
     size_t smem = 0;
-    for (; spc >= 1; --spc) {
-        const size_t base = smem_of(C, spc, part_bytes, 0);
-        if (optin > 0 && base + 2ull * spec::kChunkBytes <= static_cast<size_t>(optin)) {
-            stages = static_cast<int>((static_cast<size_t>(optin) - base) / spec::kChunkBytes);
-            if (stages > spec::kStages) stages = spec::kStages;
-            smem = smem_of(C, spc, part_bytes, stages);
-            break;
-        }
-    }
-    if (stages < 2) return fail(SPEC_UNSUPPORTED, "%s: the kernel's shared memory does not fit this device", who);
+    while (spc_max > 1 && !fit(spc_max, stages, smem)) --spc_max;
+    if (!fit(spc_max, stages, smem))
+        return fail(SPEC_UNSUPPORTED, "%s: the kernel's shared memory does not fit this device", who);
     cudaError_t e;
-    const int n = max_clusters(fn, C, smem, e);
+    int n = max_clusters(fn, C, smem, e);
     if (e != cudaSuccess) return cuda_fail(e, who);
     if (n < 1) return fail(SPEC_CUDA_ERROR, "%s: no cluster of %d CTAs fits this device", who, C);
+    int R = (B + n - 1) / n;
+    if (R > C * spc_max) R = C * spc_max;
+    if (R < 1) R = 1;
+    const int own = (R + C - 1) / C;
+    if (own < spc_max) {
+        // fewer slots per CTA: less shared memory for partials, maybe more stages
+        fit(own, stages, smem);
+        const int n2 = max_clusters(fn, C, smem, e);
+        if (e != cudaSuccess) return cuda_fail(e, who);
+        if (n2 >= 1) n = n2;
+    }
     pl.E.stages = stages;
+    pl.E.chunk = chunk;
     pl.E.C = C;
-    pl.E.R = C * spc;
-    pl.E.own = spc;
+    pl.E.R = R;
+    pl.E.own = own;
     pl.E.SL = static_cast<int>(align_up(static_cast<size_t>((V + C - 1) / C), 64));
     pl.E.part_bytes = part_bytes;
     pl.smem = smem;
-    // no more clusters than can have a request each
-    const int need = (B + pl.E.R - 1) / pl.E.R;
+    const int need = (B + R - 1) / R;
     pl.clusters = n < need ? n : need;
     if (pl.clusters < 1) pl.clusters = 1;
+    pl.resident = n;
     return SPEC_OK;
 }
 
@@ -293,7 +340,7 @@ spec_status spec_verify_chain(
     const void* fn = spec::chain_kernel_ptr((int)ldt, topk);
     Plan pl;
     spec_status s = make_plan(who, fn, V, spec::chain_part_bytes(A.top_k, A.cap_p), B,
-                              [](int C, int own, int pb, int stages) { return spec::chain_smem(C, own, pb, stages); },
+                              [](int C, int own, int pb, int stages, int chunk) { return spec::chain_smem(C, own, pb, stages, chunk); },
                               pl);
     if (s != SPEC_OK) return s;
     A.E = pl.E;
@@ -340,7 +387,7 @@ spec_status spec_verify_greedy(
     const void* fn = spec::walk_kernel_ptr((int)ldt, 0);
     Plan pl;
     spec_status s = make_plan(who, fn, V, spec::walk_part_bytes(), B,
-                              [](int C, int own, int pb, int stages) { return spec::walk_smem(C, own, pb, stages); },
+                              [](int C, int own, int pb, int stages, int chunk) { return spec::walk_smem(C, own, pb, stages, chunk); },
                               pl);
     if (s != SPEC_OK) return s;
     A.E = pl.E;
@@ -384,14 +431,95 @@ spec_status spec_tree_build(
     const void* fn = spec::build_kernel_ptr();
     Plan pl;
     spec_status s = make_plan(who, fn, V, spec::build_part_bytes(A.M), B,
-                              [&](int C, int own, int pb, int stages) {
-                                  return spec::build_smem(C, own, pb, stages, budget, L);
+                              [&](int C, int own, int pb, int stages, int chunk) {
+                                  return spec::build_smem(C, own, pb, stages, chunk, budget, L);
                               },
                               pl);
     if (s != SPEC_OK) return s;
     A.E = pl.E;
     A.E.W = make_ws(ws, spec::build_extra_bytes(budget, L));
     return launch(who, fn, pl, A, ws, static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// EAGLE-2 dynamic tree
+// ---------------------------------------------------------------------------
+size_t spec_eagle_expand_workspace_size(int B, int F, int K2) {
+    if (B < 0 || F < 1 || K2 < 1) return 0;
+    return ws_bytes_for(B * F, spec::eagle_row_extra_bytes(K2));
+}
+
+spec_status spec_eagle_expand(
+    const float* q, int64_t q_batch_stride, int64_t q_row_stride,
+    int B, int F, int V, int K2, int Fn, int G,
+    int32_t* token, int32_t* parent, int32_t* depth, double* score, int32_t* num_gen,
+    const int32_t* front_in, const int32_t* num_front_in,
+    int32_t* front_out, int32_t* num_front_out, int32_t* status,
+    void* ws, size_t ws_bytes, void* stream) {
+    const char* who = "spec_eagle_expand";
+    if (B < 0 || F < 1 || V < 1 || K2 < 1 || Fn < 0 || G < 1)
+        return fail(SPEC_INVALID_ARG, "%s: need B >= 0, F >= 1, V >= 1, K2 >= 1, Fn >= 0, G >= 1", who);
+    if (F > 64 || K2 > 255 || Fn > 64 || F * K2 > 2048 || G > 8192)
+        return fail(SPEC_UNSUPPORTED, "%s: F <= 64, K2 <= 255, Fn <= 64, F * K2 <= 2048, G <= 8192", who);
+    if (B == 0) return SPEC_OK;
+    if (!q || !token || !parent || !depth || !score || !num_gen || !front_in || !num_front_in ||
+        (Fn > 0 && !front_out) || !num_front_out || !status || !ws)
+        return fail(SPEC_INVALID_ARG, "%s: null pointer argument", who);
+    if (q_row_stride < V || q_batch_stride < 0) return fail(SPEC_INVALID_ARG, "%s: row stride must be >= V", who);
+    const size_t need = ws_bytes_for(B * F, spec::eagle_row_extra_bytes(K2));
+    if (ws_bytes < need) return fail(SPEC_INVALID_ARG, "%s: workspace too small (%zu < %zu)", who, ws_bytes, need);
+    if (!aligned16(ws)) return fail(SPEC_INVALID_ARG, "%s: workspace must be 16-byte aligned", who);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    spec::EagleArgs A{};
+    A.base.q = q; A.base.q_bs = q_batch_stride; A.base.q_rs = q_row_stride;
+    A.base.B = B; A.base.L = 1; A.base.V = V; A.base.N = K2 + 1; A.base.M = K2;
+    A.base.cap_p = K2;
+    A.base.tma_q = aligned16(q) && (q_row_stride * 4) % 16 == 0 && (q_batch_stride * 4) % 16 == 0 && device_memory(q);
+    A.F = F; A.G = G; A.front_in = front_in; A.num_front_in = num_front_in; A.num_gen = num_gen;
+    const void* fn = spec::eagle_rows_kernel_ptr();
+    Plan pl;
+    spec_status s = make_plan(who, fn, V, spec::build_part_bytes(K2), B * F,
+                              [](int C, int own, int pb, int stages, int chunk) {
+                                  return spec::eagle_rows_smem(C, own, pb, stages, chunk);
+                              },
+                              pl);
+    if (s != SPEC_OK) return s;
+    A.base.E = pl.E;
+    A.base.E.W = make_ws(ws, spec::eagle_row_extra_bytes(K2));
+    s = launch(who, fn, pl, A, ws, st);
+    if (s != SPEC_OK) return s;
+    spec::EagleGrowArgs g{};
+    g.rows = static_cast<const unsigned char*>(ws) + kCtrlBytes;
+    g.row_stride = static_cast<long long>(align_up(spec::eagle_row_extra_bytes(K2), 256));
+    g.B = B; g.F = F; g.K2 = K2; g.Fn = Fn; g.G = G;
+    g.token = token; g.parent = parent; g.depth = depth; g.score = score; g.num_gen = num_gen;
+    g.front_in = front_in; g.num_front_in = num_front_in;
+    g.front_out = front_out; g.num_front_out = num_front_out; g.status = status;
+    const cudaError_t e = spec::eagle_grow_run(g, st);
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return SPEC_OK;
+}
+
+spec_status spec_eagle_rerank(
+    const int32_t* token, const int32_t* parent, const int32_t* depth, const double* score,
+    const int32_t* num_gen, int B, int G, int budget,
+    int32_t* out_token, int32_t* out_parent, int32_t* out_depth, double* out_score,
+    uint64_t* anc_mask, int32_t* num_nodes, int32_t* status, void* stream) {
+    const char* who = "spec_eagle_rerank";
+    if (B < 0 || G < 1 || budget < 1) return fail(SPEC_INVALID_ARG, "%s: need B >= 0, G >= 1, budget >= 1", who);
+    if (G > 8192 || budget > 1024) return fail(SPEC_UNSUPPORTED, "%s: G <= 8192 and budget <= 1024", who);
+    if (B == 0) return SPEC_OK;
+    if (!token || !parent || !depth || !score || !num_gen || !out_token || !out_parent || !out_depth || !out_score ||
+        !anc_mask || !num_nodes || !status)
+        return fail(SPEC_INVALID_ARG, "%s: null pointer argument", who);
+    spec::EagleRerankArgs A{};
+    A.token = token; A.parent = parent; A.depth = depth; A.score = score; A.num_gen = num_gen;
+    A.B = B; A.G = G; A.N = budget;
+    A.out_token = out_token; A.out_parent = out_parent; A.out_depth = out_depth; A.out_score = out_score;
+    A.anc_mask = reinterpret_cast<unsigned long long*>(anc_mask); A.num_nodes = num_nodes; A.status = status;
+    const cudaError_t e = spec::eagle_rerank_run(A, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return SPEC_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -431,7 +559,7 @@ spec_status spec_verify_tree(
     const void* fn = spec::walk_kernel_ptr((int)ldt, 1);
     Plan pl;
     spec_status s = make_plan(who, fn, V, spec::walk_part_bytes(), B,
-                              [](int C, int own, int pb, int stages) { return spec::walk_smem(C, own, pb, stages); },
+                              [](int C, int own, int pb, int stages, int chunk) { return spec::walk_smem(C, own, pb, stages, chunk); },
                               pl);
     if (s != SPEC_OK) return s;
     A.E = pl.E;
@@ -487,12 +615,51 @@ spec_status spec_verify_tree_sample(
     const void* fn = spec::chain_kernel_ptr((int)ldt, topk);
     Plan pl;
     spec_status s = make_plan(who, fn, V, spec::chain_part_bytes(A.top_k, A.cap_p), B,
-                              [](int C, int own, int pb, int stages) { return spec::chain_smem(C, own, pb, stages); },
+                              [](int C, int own, int pb, int stages, int chunk) { return spec::chain_smem(C, own, pb, stages, chunk); },
                               pl);
     if (s != SPEC_OK) return s;
     A.E = pl.E;
     A.E.W = make_ws(ws, 0);
     return launch(who, fn, pl, A, ws, static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// accepted-path KV compaction
+// ---------------------------------------------------------------------------
+spec_status spec_kv_compact(
+    const void* src, int64_t src_plane_stride, int64_t src_batch_stride, int64_t src_row_stride,
+    void* dst, int64_t dst_plane_stride, int64_t dst_batch_stride, int64_t dst_row_stride,
+    int P, int B, int N, int64_t row_bytes,
+    const int32_t* path_nodes, int path_width, const int32_t* num_accepted, const int32_t* dst_pos,
+    void* stream) {
+    const char* who = "spec_kv_compact";
+    if (P < 0 || B < 0 || N < 1 || path_width < 1 || row_bytes < 1)
+        return fail(SPEC_INVALID_ARG, "%s: need P >= 0, B >= 0, N >= 1, path_width >= 1, row_bytes >= 1", who);
+    if (P == 0 || B == 0) return SPEC_OK;
+    if (!src || !dst || !path_nodes || !num_accepted) return fail(SPEC_INVALID_ARG, "%s: null pointer argument", who);
+    if (src_row_stride < row_bytes || dst_row_stride < row_bytes || src_batch_stride < 0 || dst_batch_stride < 0 ||
+        src_plane_stride < 0 || dst_plane_stride < 0)
+        return fail(SPEC_INVALID_ARG, "%s: row strides must be >= row_bytes, other strides >= 0", who);
+    spec::KvArgs A{};
+    A.src = static_cast<const unsigned char*>(src);
+    A.s_plane = src_plane_stride; A.s_batch = src_batch_stride; A.s_row = src_row_stride;
+    A.dst = static_cast<unsigned char*>(dst);
+    A.d_plane = dst_plane_stride; A.d_batch = dst_batch_stride; A.d_row = dst_row_stride;
+    A.P = P; A.B = B; A.N = N; A.W = path_width; A.row_bytes = row_bytes;
+    A.path_nodes = path_nodes; A.num_accepted = num_accepted; A.dst_pos = dst_pos;
+    auto all_mult = [&](long long m) {
+        const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+        return s0 % m == 0 && d0 % m == 0 && row_bytes % m == 0 && src_row_stride % m == 0 &&
+               dst_row_stride % m == 0 && src_batch_stride % m == 0 && dst_batch_stride % m == 0 &&
+               src_plane_stride % m == 0 && dst_plane_stride % m == 0;
+    };
+    A.width = all_mult(16) ? 16 : (all_mult(4) ? 4 : 1);
+    int d = 0, sms = 0;
+    cudaGetDevice(&d);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
+    cudaError_t e = spec::kv_compact_run(A, sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, who);
+    return SPEC_OK;
 }
 
 // ---------------------------------------------------------------------------

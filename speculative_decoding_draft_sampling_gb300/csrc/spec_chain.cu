@@ -41,8 +41,9 @@ enum ChainKind : int { kTk = 0, kSe = 1, kResid = 2, kRescan = 3, kRadix = 4 };
 
 // Combiner scratch: the gathered candidate keys, then the top-k set sorted
 // by token (ids and float-float weights).
-constexpr int kCombKeys = 2048;
+constexpr int kCombKeys = 1024;
 constexpr int kCombSet = 512;
+constexpr int kRegKeys = 4;        // gathered keys a combiner lane holds in registers (128 per warp)
 
 struct ChainSmem {
     TopkSmem tk;                      // consumers: slice candidates (top-k rows)
@@ -60,9 +61,8 @@ struct ChainSmem {
     float2 ws[kWarps];
     float2 ws2[kWarps];
     uint32_t wb[kWarps];
-    float fsh[4];
     uint32_t last_hint;               // combiner: filter hint from this CTA's latest top-k row
-    uint32_t tag;                     // consumers: unit tag for the shared filter
+    int nsel;                         // consumers: keys a slice reports
 };
 
 __device__ __forceinline__ int chain_k(const ChainArgs& A, int b) {
@@ -217,7 +217,7 @@ __device__ int warp_icdf_pairs(const int* tok, const float2* w, int n, dfloat t)
 // a hint above the next row's tau costs a re-read of that row, one far below
 // it extra candidates).
 #ifndef SPEC_HINT_MARGIN
-#define SPEC_HINT_MARGIN 0.15f
+#define SPEC_HINT_MARGIN 0.08f
 #endif
 __device__ __forceinline__ uint32_t hint_from(float tau, float m, float margin) {
     const float h = tau - margin * (m - tau);
@@ -264,32 +264,67 @@ __device__ __forceinline__ void slice_y(const unsigned char* parts, int pb, int 
 }
 
 // ---------------------------------------------------------------------------
-// combine of a top-k row: the candidate lists of all slices hold S exactly
+// combine of a top-k row.  Every slice reports its keys at or above its own
+// k-th value, sorted descending (composite keys: value, then lower id
+// first).  S -- every element whose value reaches the row's k-th largest
+// value tau -- is a union of prefixes of those lists, and tau is the value of
+// the key whose merged rank is k - 1: each key's rank is the sum over the
+// lists of the keys greater than it, by binary search.
 // ---------------------------------------------------------------------------
+
+// entries of the descending list lst[0..m) greater than x, for a warp's
+// kRegKeys keys at once (s0: a power of two, at least m / 2)
+__device__ __forceinline__ void count_gt4(const uint64_t* lst, int m, int s0, const uint64_t (&x)[kRegKeys],
+                                          int (&pos)[kRegKeys]) {
+#pragma unroll
+    for (int j = 0; j < kRegKeys; ++j) pos[j] = 0;
+    for (int s = s0; s > 0; s >>= 1) {
+#pragma unroll
+        for (int j = 0; j < kRegKeys; ++j) {
+            const int np = pos[j] + s;
+            if (np <= m && lst[np - 1] > x[j]) pos[j] = np;
+        }
+    }
+}
+__device__ __forceinline__ const uint64_t* slice_keys(const unsigned char* parts, int pb, int r) {
+    return reinterpret_cast<const uint64_t*>(part_at(parts, pb, r) + 1);
+}
+// the list holding flattened entry f (offsets `off` in lanes 0..C-1)
+__device__ __forceinline__ int list_of(int off, int C, int f) {
+    int r = 0;
+    for (int q = 1; q < C; ++q) r += __shfl_sync(0xffffffffu, off, q) <= f ? 1 : 0;
+    return r;
+}
+
 template <class E>
-__device__ Job combine_topk(const ChainArgs& A, const Geo& G, const Job& job, const unsigned char* parts,
-                            ChainSmem& sm) {
+__device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const Job job, const unsigned char* parts,
+                                         ChainSmem& sm) {
+    SPEC_TRACE_T(tc0);
     const int l = threadIdx.x & 31;
     const int C = G.C, pb = G.part_bytes;
     const int b = job.b, row = job.row, k = A.top_k;
     const bool bonus = job.aux != 0;
     int st = job.st;
-    const int kb = chain_k(A, b);
-    uint32_t flags = 0;
-    float vmax = -kInf;
-    uint64_t theta = 0;
+    // the request's global inputs this combine needs, issued first so that
+    // their latency overlaps the selection below
+    const float uk = __uint_as_float(ldg_now_u32(&A.uniforms[static_cast<long long>(b) * ((A.tree ? A.L : A.K) + 1) +
+                                                              draw_uidx(A, job)]));
+    const float ur = bonus ? 0.f : __uint_as_float(ldg_now_u32(&A.uniforms[static_cast<long long>(b) *
+                                                                                ((A.tree ? A.L : A.K) + 1) + row]));
+    const int yd = bonus ? -1 : static_cast<int>(ldg_now_u32(&A.draft[static_cast<long long>(b) * A.K + row]));
+    // the slices' headers (value filters: the low key halves are zero)
+    const uint32_t hb = smem_u32(parts) + static_cast<uint32_t>(l * pb);
+    uint32_t flags = 0, vkey = 0, thk = 0;
     int cnt = 0;
     if (l < C) {
-        const PartHdr* h = part_at(parts, pb, l);
-        flags = h->flags; vmax = h->vmax; theta = h->kth; cnt = h->cnt;
+        flags = lds_u32(hb + offsetof(PartHdr, flags));
+        vkey = fkey(__uint_as_float(lds_u32(hb + offsetof(PartHdr, vmax))));
+        thk = hkey(lds_u64(hb + offsetof(PartHdr, kth)));
+        cnt = static_cast<int>(lds_u32(hb + offsetof(PartHdr, cnt)));
     }
     flags = __reduce_or_sync(0xffffffffu, flags);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        vmax = max_nan(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
-        const uint64_t t2 = __shfl_xor_sync(0xffffffffu, theta, o);
-        theta = t2 > theta ? t2 : theta;
-    }
+    const float vmax = fkey_inv(__reduce_max_sync(0xffffffffu, vkey));
+    const uint32_t th = __reduce_max_sync(0xffffffffu, thk);
     if ((flags & kPfBad) || !(vmax > -kInf)) return finish_at(A, job, -1, st | 1);
     if (flags & kPfOverflow) {
         // massive ties: the exact k-th value by radix select
@@ -299,27 +334,21 @@ __device__ Job combine_topk(const ChainArgs& A, const Geo& G, const Job& job, co
         j.depth = job.depth;
         return j;
     }
-    // every key at or above the largest slice filter (the others can not be in S)
-    const uint32_t th = hkey(theta);
-    int n = 0;
-    const uint32_t lt = (1u << l) - 1u;
-    for (int r = 0; r < C; ++r) {
-        const int cr = __shfl_sync(0xffffffffu, cnt, r);
-        const uint64_t* keys = reinterpret_cast<const uint64_t*>(part_at(parts, pb, r) + 1);
-        for (int i0 = 0; i0 < cr; i0 += 32) {
-            const int i = i0 + l;
-            uint64_t key = 0;
-            bool p = false;
-            if (i < cr) { key = keys[i]; p = hkey(key) >= th; }
-            const uint32_t bal = __ballot_sync(0xffffffffu, p);
-            if (p) {
-                const int pos = n + __popc(bal & lt);
-                if (pos < kCombKeys) sm.list[pos] = key;
-            }
-            n += __popc(bal);
+    // the prefix of each list at or above the largest slice filter holds
+    // every member of S in that slice
+    int mr = 0;
+    if (l < C && cnt > 0) {
+        const uint32_t lr = hb + static_cast<uint32_t>(sizeof(PartHdr));
+        int lo = 0, hi = cnt;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (hkey(lds_u64(lr + 8u * mid)) >= th) lo = mid + 1; else hi = mid;
         }
+        mr = lo;
     }
-    __syncwarp();
+    int n;
+    const int off = warp_exscan_i(mr, n);
+    const uint32_t lt = (1u << l) - 1u;
     if (n < k) {
         // a hinted slice filter sat above the row's k-th value: stream the row
         // again without a hint (certified filters always leave k keys; without
@@ -338,10 +367,102 @@ __device__ Job combine_topk(const ChainArgs& A, const Geo& G, const Job& job, co
         j.depth = job.depth;
         return j;
     }
-    const uint32_t tau_key = kth_value_w(sm.list, n, k);
-    const int keep = compact_w(sm.list, n, tau_key);
+    SPEC_TRACE_T(tc1);
+    // the key of merged rank k - 1; then S (every key whose value reaches
+    // it): its size, Z = sum of e_x = 2^((l_x - m) c) over it (float-float),
+    // and its keys into the list (for a draw)
+    const uint32_t mmax = warp_max_u32(static_cast<uint32_t>(mr));
+    const int s0 = 1 << (31 - __clz(mmax));
+    const uint32_t kbase = smem_u32(parts) + static_cast<uint32_t>(sizeof(PartHdr));   // + r * pb: slice r's keys
     const float m = vmax, c2 = A.c2;
+    uint64_t tauc = 0;
+    uint32_t tau_key;
+    int keep = 0;
+    dfloat zp = df_make(0.f);
+    if (C <= 4 && n <= 32 * kRegKeys) {
+        // every search of every key at once: lists q >= C are empty (offset n)
+        int o[4], mq[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            o[q] = __shfl_sync(0xffffffffu, off, q);
+            mq[q] = __shfl_sync(0xffffffffu, mr, q);
+        }
+        uint64_t key[kRegKeys];
+#pragma unroll
+        for (int j = 0; j < kRegKeys; ++j) {
+            const int f = l + 32 * j;
+            const int r = (f >= o[1] ? 1 : 0) + (f >= o[2] ? 1 : 0) + (f >= o[3] ? 1 : 0);
+            const int base = r == 0 ? 0 : (r == 1 ? o[1] : (r == 2 ? o[2] : o[3]));
+            key[j] = f < n ? lds_u64(kbase + static_cast<uint32_t>(r * pb + (f - base) * 8)) : 0ull;
+        }
+        int pos[4][kRegKeys];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int j = 0; j < kRegKeys; ++j) pos[q][j] = 0;
+        for (int s = s0; s > 0; s >>= 1) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int j = 0; j < kRegKeys; ++j) {
+                    const int np = pos[q][j] + s;
+                    if (np <= mq[q] && lds_u64(kbase + static_cast<uint32_t>(q * pb + (np - 1) * 8)) > key[j])
+                        pos[q][j] = np;
+                }
+        }
+#pragma unroll
+        for (int j = 0; j < kRegKeys; ++j)
+            if (l + 32 * j < n && pos[0][j] + pos[1][j] + pos[2][j] + pos[3][j] == k - 1) tauc = key[j];
+        tauc = warp_max_u64(tauc);   // the one key of rank k - 1
+        tau_key = hkey(tauc);
+#pragma unroll
+        for (int j = 0; j < kRegKeys; ++j) {
+            const bool p = l + 32 * j < n && hkey(key[j]) >= tau_key;
+            if (p) zp = df_add(zp, ex2((ckey_val(key[j]) - m) * c2));
+            const uint32_t bal = __ballot_sync(0xffffffffu, p);
+            if (p) sm.list[keep + __popc(bal & lt)] = key[j];
+            keep += __popc(bal);
+        }
+    } else {
+        for (int f0 = 0; f0 < n; f0 += 32 * kRegKeys) {
+            uint64_t key[kRegKeys];
+            int rank[kRegKeys], pos[kRegKeys];
+#pragma unroll
+            for (int j = 0; j < kRegKeys; ++j) {
+                const int f = f0 + l + 32 * j;
+                const int r = list_of(off, C, f);
+                const int base = __shfl_sync(0xffffffffu, off, r);
+                key[j] = f < n ? lds_u64(kbase + static_cast<uint32_t>(r * pb + (f - base) * 8)) : 0ull;
+                rank[j] = 0;
+            }
+            for (int q = 0; q < C; ++q) {
+                const int mqq = __shfl_sync(0xffffffffu, mr, q);
+                count_gt4(slice_keys(parts, pb, q), mqq, s0, key, pos);
+#pragma unroll
+                for (int j = 0; j < kRegKeys; ++j) rank[j] += pos[j];
+            }
+#pragma unroll
+            for (int j = 0; j < kRegKeys; ++j)
+                if (f0 + l + 32 * j < n && rank[j] == k - 1) tauc = key[j];
+        }
+        tauc = warp_max_u64(tauc);
+        tau_key = hkey(tauc);
+        for (int f0 = 0; f0 < n; f0 += 32) {
+            const int f = f0 + l;
+            const int r = list_of(off, C, f);
+            const int base = __shfl_sync(0xffffffffu, off, r);
+            const uint64_t key = f < n ? lds_u64(kbase + static_cast<uint32_t>(r * pb + (f - base) * 8)) : 0ull;
+            const bool p = f < n && hkey(key) >= tau_key;
+            if (p) zp = df_add(zp, ex2((ckey_val(key) - m) * c2));
+            const uint32_t bal = __ballot_sync(0xffffffffu, p);
+            if (p) sm.list[keep + __popc(bal & lt)] = key;
+            keep += __popc(bal);
+        }
+    }
     const float tau = fkey_inv(tau_key);
+    const dfloat Z = warp_sum_df(zp);
+    __syncwarp();
+    SPEC_TRACE_T(tc2);
     if (keep > kCombSet) {
         // a large tied set: the masked full-row passes, with the threshold known
         Job j = make_job(b, row, kSe, st);
@@ -350,52 +471,73 @@ __device__ Job combine_topk(const ChainArgs& A, const Geo& G, const Job& job, co
         j.depth = job.depth;
         return j;
     }
-    // S sorted by token id (ids in S are distinct): rank by counting
-    for (int i = l; i < keep; i += 32) {
-        const uint64_t key = sm.list[i];
-        const int x = ckey_idx(key);
-        int r = 0;
-        for (int t = 0; t < keep; ++t) r += ckey_idx(sm.list[t]) < x;
-        sm.stok[r] = x;
-        sm.sval[r] = ckey_val(key);
-    }
-    __syncwarp();
-    // weights e_x = 2^((l_x - m) c) and Z = sum over S (float-float)
-    dfloat zp = df_make(0.f);
-    for (int i = l; i < keep; i += 32) {
-        const float e = ex2((sm.sval[i] - m) * c2);
-        sm.swt[i] = make_float2(e, 0.f);
-        zp = df_add(zp, e);
-    }
-    const dfloat Z = warp_sum_df(zp);
-    __syncwarp();
     // the next rows' filter hint (and, persisted, the next call's)
     const uint32_t hint = hint_from(tau, m, SPEC_HINT_MARGIN);
     if (l == 0) {
         sm.last_hint = hint;
+        // for the next call's first rows, with a wider margin (another call's
+        // rows may sit lower); one 16-byte store
         const uint32_t hw = hint_from(tau, m, 0.5f);
-        volatile uint32_t* ps = A.E.W.ctrl->persist;
-        ps[1] = hw; ps[2] = static_cast<uint32_t>(A.V); ps[3] = static_cast<uint32_t>(A.top_k); ps[0] = kPersistTag;
+        __stcg(reinterpret_cast<uint4*>(A.E.W.ctrl->persist),
+               make_uint4(kPersistTag, hw, static_cast<uint32_t>(A.V), static_cast<uint32_t>(A.top_k)));
     }
-    const float uk = chain_u(A, b, draw_uidx(A, job));
     auto prob = [&](float e) { return static_cast<float>(static_cast<double>(e) / df_to_d(Z)); };   // diagnostics
+    float ey = 0.f, qy = 0.f;
     if (!bonus) {
-        const int y = A.draft[static_cast<long long>(b) * A.K + row];
-        float ly, qy;
+        const int y = yd;
+        float ly;
         slice_y(parts, pb, C, ly, qy);
-        const float ey = (y >= 0 && y < A.V && fkey(ly) >= tau_key) ? ex2((ly - m) * c2) : 0.f;
+        ey = (y >= 0 && y < A.V && fkey(ly) >= tau_key) ? ex2((ly - m) * c2) : 0.f;
         if (y < 0 || y >= A.V) qy = 0.f;
-        const bool acc = chain_accept_z(A, y, ey, qy, Z, chain_u(A, b, row), st);
+        const bool acc = chain_accept_z(A, y, ey, qy, Z, ur, st);
+#ifdef SPEC_TRACE
+        SPEC_TRACE_T(tc3);
+        if (l == 0) {
+            SPEC_TRACE_EV(11, n, keep, static_cast<int>(tc1 - tc0));
+            SPEC_TRACE_EV(12, static_cast<int>(tc2 - tc1), static_cast<int>(tc3 - tc2), 0);
+        }
+#endif
         if (acc) {
-            chain_diag(A, b, row, prob(ey), qy, Z.hi, 0.f);
+            if (A.diag) chain_diag(A, b, row, prob(ey), qy, Z.hi, 0.f);
             return row_job(A, b, row + 1, st, hint);
         }
-        // residual [p - q]_+ lives on S (p = 0 outside it): gather q at S
+    }
+    // a draw on S (the residual at a rejection, p at the bonus row): S sorted
+    // by token id (ids in S are distinct), each member's rank the number of
+    // smaller ids, counted over shuffles (or shared memory beyond 64)
+    if (keep <= 64) {
+        const uint64_t k0 = l < keep ? sm.list[l] : 0ull, k1 = l + 32 < keep ? sm.list[l + 32] : 0ull;
+        const int t0 = l < keep ? ckey_idx(k0) : 0x7fffffff;
+        const int t1 = l + 32 < keep ? ckey_idx(k1) : 0x7fffffff;
+        int r0 = 0, r1 = 0;
+#pragma unroll 8
+        for (int o = 0; o < 32; ++o) {
+            const int a = __shfl_sync(0xffffffffu, t0, o), c = __shfl_sync(0xffffffffu, t1, o);
+            r0 += (a < t0) + (c < t0);
+            r1 += (a < t1) + (c < t1);
+        }
+        __syncwarp();
+        if (l < keep) { sm.stok[r0] = t0; sm.sval[r0] = ckey_val(k0); }
+        if (l + 32 < keep) { sm.stok[r1] = t1; sm.sval[r1] = ckey_val(k1); }
+    } else {
+        for (int i = l; i < keep; i += 32) {
+            const uint64_t key = sm.list[i];
+            const int x = ckey_idx(key);
+            int r = 0;
+            for (int t = 0; t < keep; ++t) r += ckey_idx(sm.list[t]) < x;
+            sm.stok[r] = x;
+            sm.sval[r] = ckey_val(key);
+        }
+    }
+    __syncwarp();
+    if (!bonus) {
+        // residual [p - q]_+ lives on S (p = 0 outside it)
         const float* qrow = chain_qrow(A, b, row);
         dfloat rp = df_make(0.f);
         for (int i = l; i < keep; i += 32) {
             const float qx = __ldcg(qrow + sm.stok[i]);
-            const dfloat d = df_add(df_make(sm.swt[i].x), df_neg(df_mul(qx, Z)));
+            const float e = ex2((sm.sval[i] - m) * c2);
+            const dfloat d = df_add(df_make(e), df_neg(df_mul(qx, Z)));
             const dfloat w = d.hi > 0.f ? d : df_make(0.f);
             sm.swt[i] = make_float2(w.hi, w.lo);
             rp = df_add(rp, w);
@@ -413,6 +555,8 @@ __device__ Job combine_topk(const ChainArgs& A, const Geo& G, const Job& job, co
         return chain_finish(A, b, row, x, st);
     }
     // bonus row: draw from p on S
+    for (int i = l; i < keep; i += 32) sm.swt[i] = make_float2(ex2((sm.sval[i] - m) * c2), 0.f);
+    __syncwarp();
     const int x = warp_icdf_pairs(sm.stok, sm.swt, keep, df_mul(uk, Z));
     float px = 0.f;
     for (int i = l; i < keep; i += 32)
@@ -426,8 +570,8 @@ __device__ Job combine_topk(const ChainArgs& A, const Geo& G, const Job& job, co
 // ---------------------------------------------------------------------------
 // combine of a sum-exp row (untruncated, or masked at a known threshold)
 // ---------------------------------------------------------------------------
-__device__ Job combine_se(const ChainArgs& A, const Geo& G, const Job& job, const unsigned char* parts,
-                          ChainSmem& sm) {
+__device__ __noinline__ Job combine_se(const ChainArgs& A, const Geo& G, const Job job, const unsigned char* parts,
+                                       ChainSmem& sm) {
     const int l = threadIdx.x & 31;
     const int C = G.C, pb = G.part_bytes;
     const int b = job.b, row = job.row;
@@ -483,7 +627,7 @@ __device__ Job combine_se(const ChainArgs& A, const Geo& G, const Job& job, cons
     return j;
 }
 
-__device__ Job combine_resid(const ChainArgs& A, const Geo& G, const Job& job, const unsigned char* parts) {
+__device__ __noinline__ Job combine_resid(const ChainArgs& A, const Geo& G, const Job job, const unsigned char* parts) {
     const int l = threadIdx.x & 31;
     const int C = G.C, pb = G.part_bytes;
     const int b = job.b, row = job.row;
@@ -521,8 +665,8 @@ __device__ Job combine_resid(const ChainArgs& A, const Geo& G, const Job& job, c
 }
 
 template <class E>
-__device__ Job combine_rescan(const ChainArgs& A, const Job& job, const unsigned char* parts, int pb,
-                              uint32_t hint) {
+__device__ __noinline__ Job combine_rescan(const ChainArgs& A, const Job job, const unsigned char* parts, int pb,
+                                           uint32_t hint) {
     const PartHdr* h = part_at(parts, pb, job.target);
     const int x = h->tok;
     const int b = job.b, row = job.row;
@@ -539,7 +683,7 @@ __device__ Job combine_rescan(const ChainArgs& A, const Job& job, const unsigned
     return chain_finish(A, b, row, x, job.st);
 }
 
-__device__ Job combine_radix(const ChainArgs& A, const Geo& G, const Job& job, const unsigned char* parts) {
+__device__ __noinline__ Job combine_radix(const ChainArgs& A, const Geo& G, const Job job, const unsigned char* parts) {
     const int l = threadIdx.x & 31;
     const int C = G.C, pb = G.part_bytes;
     const int round = job.aux2 & 0xff;
@@ -601,6 +745,40 @@ __device__ Job combine_radix(const ChainArgs& A, const Geo& G, const Job& job, c
     return j;
 }
 
+// A slice's report of a top-k row (all consumers): the keys src[0..n) at or
+// above the slice filter F, sorted descending into dst by rank (the number of
+// greater keys; keys are distinct), then cut after the last key whose value
+// reaches the slice's k-th largest value -- no element below that value can
+// be among the row's top k.  F is raised to that value.  Returns the count.
+static_assert(TopkSmem::kSlots * kThreads >= 512, "the slots hold a slice's reported keys");
+__device__ int slice_sort_trim(const uint64_t* src, int n, uint64_t& F, int k, uint64_t* dst, int* nsel) {
+    if (threadIdx.x == 0) *nsel = 0;
+    csync();   // src complete, the count zeroed
+    int mine = 0;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        const uint64_t x = src[i];
+        if (x < F) continue;
+        int r = 0;
+#pragma unroll 8
+        for (int j = 0; j < n; ++j) r += src[j] > x ? 1 : 0;   // greater keys reach F as well
+        dst[r] = x;
+        ++mine;
+    }
+    if (mine) atomicAdd(nsel, mine);
+    csync();
+    const int nf = *nsel;
+    if (nf < k) return nf;   // a hint above the slice's k-th value: every key counts
+    const uint32_t vk = hkey(dst[k - 1]);
+    int lo = k, hi = nf;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (hkey(dst[mid]) >= vk) lo = mid + 1; else hi = mid;
+    }
+    const uint64_t fk = static_cast<uint64_t>(vk) << 32;
+    if (fk > F) F = fk;
+    return lo;
+}
+
 // ---------------------------------------------------------------------------
 // the op
 // ---------------------------------------------------------------------------
@@ -611,32 +789,34 @@ struct ChainOp {
 
     __device__ static int batch(const Args& A) { return A.B; }
     __device__ static bool tma(const Args& A) { return A.tma_l && (kTopk || A.K == 0 || A.tma_q); }
-    __device__ static void init_smem(const Args&, const Geo&, Smem& sm) {
+    __device__ static void init_smem(const Args& A, const Geo&, Smem& sm) {
         if (threadIdx.x == 0) {
             topk_smem_init(sm.tk);
-            sm.tag = 0;
-            sm.last_hint = 0;
+            // the previous call's hint on this workspace, for the same
+            // vocabulary and top-k: the first rows' filter until a row of
+            // this call gives a better one
+            uint32_t h = 0;
+            if (kTopk) {
+                const uint4 ps = __ldcg(reinterpret_cast<const uint4*>(A.E.W.ctrl->persist));
+                if (ps.x == kPersistTag && ps.z == static_cast<uint32_t>(A.V) &&
+                    ps.w == static_cast<uint32_t>(A.top_k))
+                    h = ps.y;
+            }
+            sm.last_hint = h;
         }
     }
     __device__ static Job first(const Args& A, const Geo&, int b, Smem& sm) {
         const int kb = A.tree ? 0 : chain_k(A, b);
         if (kb < 0 || kb > A.K) return chain_finish(A, b, 0, -1, 16);
-        uint32_t hint = sm.last_hint;
-        if (kTopk && hint == 0) {
-            // the previous call on this workspace, for the same vocabulary and top-k
-            const volatile uint32_t* ps = A.E.W.ctrl->persist;
-            if (ps[0] == kPersistTag && ps[2] == static_cast<uint32_t>(A.V) && ps[3] == static_cast<uint32_t>(A.top_k))
-                hint = ps[1];
-        }
-        return row_job(A, b, 0, 0, hint);
+        return row_job(A, b, 0, 0, sm.last_hint);
     }
     __device__ static StreamPlan plan(const Args& A, const Geo& G, const Job& j) {
         const int x0 = slice_x0(G, G.rank), x1 = slice_x1(G, G.rank, A.V);
         switch (j.kind) {
             case kTk: case kSe: case kRadix:
-                return plan_single(chain_lrow<E>(A, j.b, j.row), E::kBytes, x0, x1);
+                return plan_single(chain_lrow<E>(A, j.b, j.row), E::kBytes, x0, x1, G.chunk);
             case kResid:
-                return plan_dual(chain_lrow<E>(A, j.b, j.row), E::kBytes, chain_qrow(A, j.b, j.row), x0, x1);
+                return plan_dual(chain_lrow<E>(A, j.b, j.row), E::kBytes, chain_qrow(A, j.b, j.row), x0, x1, G.chunk);
             default:
                 return plan_none();
         }
@@ -656,22 +836,21 @@ struct ChainOp {
         }
         int nkeys = 0;
         if (j.kind == kTk || j.kind == kSe) {
-            DraftWatch dw;
-            dw.x0 = x0; dw.x1 = x1;
-            if (j.aux == 0) {
-                dw.y = A.draft[static_cast<long long>(b) * A.K + row];
-                dw.qrow = chain_qrow(A, b, row);
+            // the drafted token: the thread 0 of the slice that holds it loads
+            // its logit and q at once (the loads overlap the stream)
+            int y = -1;
+            if (j.aux == 0) y = A.draft[static_cast<long long>(b) * A.K + row];
+            const bool owns = y >= x0 && y < x1;
+            float ly = -kInf, qy = 0.f;
+            if (owns && threadIdx.x == 0) {
+                ly = E::load(chain_lrow<E>(A, b, row), y);
+                qy = __ldg(chain_qrow(A, b, row) + y);
             }
-            float* wsl = sm.fsh;
             if (kTopk && j.kind == kTk) {
-                if (threadIdx.x == 0) sm.tag = sm.tag + 1;
-                csync();
                 TopkHistFn<E, true> fn;
-                fn.init(&sm.tk, A.top_k, j.hint, sm.tag);
-                fn.dw = dw;
+                fn.init(&sm.tk, A.top_k, j.hint, seq + 1u);   // every consumer holds the same seq
                 if (!consume_row<E>(P, seq, plan, tma, x0, fn)) return -1;
                 fn.publish();
-                if (fn.dw.seen) wsl[0] = fn.dw.ly;
                 csync();
                 int tot;
                 uint64_t F;
@@ -681,8 +860,12 @@ struct ChainOp {
                 const uint32_t bad = (fl >> 1) & 1u;
                 uint32_t oflow = fl & 1u;
                 int n = tot;
+                const uint64_t* src = nullptr;
                 if (!bad && !oflow && tot <= A.cap_p) {
-                    fn.write_keys(pk);   // every warp's keys at its offset
+                    // every warp's keys at its offset, into the (flushed) slots
+                    uint64_t* tmp = &sm.tk.slot[0][0];
+                    fn.write_keys(tmp);
+                    src = tmp;
                 } else if (!bad && !oflow) {
                     // too many: the certified bound over every candidate, repeated
                     // until it stops rising (then it is the exact k-th value)
@@ -698,23 +881,23 @@ struct ChainOp {
                         F = static_cast<uint64_t>(F2) << 32;
                     }
                     if (n > A.cap_p) oflow = 1;   // ties at the k-th value: the combine takes the radix path
-                    else for (int i = threadIdx.x; i < n; i += kThreads) pk[i] = list[i];
+                    else src = list;
                 }
                 if (oflow || bad) n = 0;
+                else n = slice_sort_trim(src, n, F, A.top_k, pk, &sm.nsel);
                 nkeys = n;
                 if (threadIdx.x == 0) {
                     ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u) | (j.hint ? kPfHinted : 0u);
                     ph->cnt = n;
                     ph->kth = F;
                     ph->vmax = vm;
-                    if (fn.dw.owns()) { ph->ly = wsl[0]; ph->qy = fn.dw.qy; ph->hasy = 1; }
+                    if (owns) { ph->ly = ly; ph->qy = qy; ph->hasy = 1; }
                 }
             } else {
                 // sum-exp (masked at the job's threshold when it carries one)
                 const uint32_t mask = j.hint;
                 auto run = [&](auto& fn) -> bool {
                     fn.c = A.c2;
-                    fn.dw = dw;
                     if (!consume_row<E>(P, seq, plan, tma, x0, fn)) return false;
                     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
                     float wm = fn.m;
@@ -727,7 +910,6 @@ struct ChainOp {
                     for (int o = 16; o > 0; o >>= 1) wv = max_nan(wv, __shfl_xor_sync(0xffffffffu, wv, o));
                     const uint32_t wb = __reduce_or_sync(0xffffffffu, fn.bad_flag());
                     if (lane == 0) { sm.wm[w] = wm; sm.ws[w] = make_float2(wsd.hi, wsd.lo); sm.wb[w] = wb; sm.ws2[w].x = wv; }
-                    if (fn.dw.seen) wsl[0] = fn.dw.ly;
                     csync();
                     if (threadIdx.x == 0) {
                         float ms = -kInf, vx = -kInf;
@@ -739,7 +921,7 @@ struct ChainOp {
                         ph->flags = bad ? kPfBad : 0u;
                         ph->vmax = bad ? vx : ms;
                         ph->sum = make_float2(tot.hi, tot.lo);
-                        if (fn.dw.owns()) { ph->ly = wsl[0]; ph->qy = fn.dw.qy; ph->hasy = 1; }
+                        if (owns) { ph->ly = ly; ph->qy = qy; ph->hasy = 1; }
                     }
                     return true;
                 };
@@ -837,14 +1019,21 @@ __global__ void __launch_bounds__(kBlockThreads, 1) chain_kernel(const ChainArgs
 template <class E, bool kTopk>
 static const void* chain_fn() { return reinterpret_cast<const void*>(&chain_kernel<E, kTopk>); }
 
+#ifdef SPEC_TEST_HOOKS
+// test builds only: make the chain kernel's first posted job go missing
+extern "C" int spec_test_drop_first_post(int on) {
+    return static_cast<int>(cudaMemcpyToSymbol(g_test_drop_post, &on, sizeof(int)));
+}
+#endif
+
 const void* chain_kernel_ptr(int ldt, bool topk) {
     if (ldt == 0) return topk ? chain_fn<F32, true>() : chain_fn<F32, false>();
     return topk ? chain_fn<BF16, true>() : chain_fn<BF16, false>();
 }
 
-size_t chain_smem(int C, int own, int part_bytes, int stages) {
+size_t chain_smem(int C, int own, int part_bytes, int stages, int chunk) {
     // the same layout for every instantiation
-    return Engine<ChainOp<F32, true>>::smem_bytes(C, own, part_bytes, stages);
+    return Engine<ChainOp<F32, true>>::smem_bytes(C, own, part_bytes, stages, chunk);
 }
 
 int chain_part_bytes(int top_k, int cap_p) {
@@ -853,3 +1042,18 @@ int chain_part_bytes(int top_k, int cap_p) {
 }
 
 }  // namespace spec
+
+#ifdef SPEC_TRACE
+// development builds: install the chain kernels' event buffer and reset it
+extern "C" int spec_trace_setup_chain(void* buf, unsigned cap) {
+    unsigned z = 0;
+    if (cudaMemcpyToSymbol(spec::g_trace, &buf, sizeof(buf)) != cudaSuccess) return 1;
+    if (cudaMemcpyToSymbol(spec::g_trace_cap, &cap, sizeof(cap)) != cudaSuccess) return 1;
+    return cudaMemcpyToSymbol(spec::g_trace_n, &z, sizeof(z)) != cudaSuccess;
+}
+extern "C" unsigned spec_trace_count_chain(void) {
+    unsigned n = 0;
+    cudaMemcpyFromSymbol(&n, spec::g_trace_n, sizeof(n));
+    return n;
+}
+#endif

@@ -93,19 +93,69 @@ struct BuildArgs {
     int tma_q;
 };
 
+// EAGLE-2 expansion rows: unit u = b * F + f is frontier slot f of request
+// b; its q row is base.q + b * base.q_bs + f * base.q_rs.  Each unit's top-K2
+// (base.M) children go to the unit's workspace extra: EagleRowHdr, then K2
+// tokens, then K2 probabilities.
+struct EagleArgs {
+    BuildArgs base;                // q, strides, B, V, M = K2, cap_p, tma_q, E
+    int F, G;
+    const int* front_in;           // [B, F]
+    const int* num_front_in;       // [B]
+    const int* num_gen;            // [B]
+};
+struct EagleRowHdr {
+    int n;                         // children found; -1: no row (slot past the frontier); -2: bad node id
+    int bad;                       // the row held a NaN or +inf
+    int pad[2];
+};
+size_t eagle_row_extra_bytes(int K2);
+const void* eagle_rows_kernel_ptr();
+size_t eagle_rows_smem(int C, int own, int part_bytes, int stages, int chunk);
+// the grow step (one CTA per request) and the rerank
+struct EagleGrowArgs {
+    const unsigned char* rows;     // workspace extras of the row units
+    long long row_stride;          // bytes between units
+    int B, F, K2, Fn, G;
+    int* token; int* parent; int* depth; double* score; int* num_gen;
+    const int* front_in; const int* num_front_in;
+    int* front_out; int* num_front_out; int* status;
+};
+cudaError_t eagle_grow_run(const EagleGrowArgs& A, cudaStream_t st);
+struct EagleRerankArgs {
+    const int* token; const int* parent; const int* depth; const double* score; const int* num_gen;
+    int B, G, N;
+    int* out_token; int* out_parent; int* out_depth; double* out_score;
+    unsigned long long* anc_mask; int* num_nodes; int* status;
+};
+cudaError_t eagle_rerank_run(const EagleRerankArgs& A, cudaStream_t st);
 // chain
 const void* chain_kernel_ptr(int ldt, bool topk);
-size_t chain_smem(int C, int own, int part_bytes, int stages);
+size_t chain_smem(int C, int own, int part_bytes, int stages, int chunk);
 int chain_part_bytes(int top_k, int cap_p);
 // greedy / tree walk
 const void* walk_kernel_ptr(int ldt, int mode);   // mode 0 greedy, 1 tree, 2 stochastic tree
-size_t walk_smem(int C, int own, int part_bytes, int stages);
+size_t walk_smem(int C, int own, int part_bytes, int stages, int chunk);
 int walk_part_bytes();
 // tree build
 const void* build_kernel_ptr();
-size_t build_smem(int C, int own, int part_bytes, int stages, int N, int L);
+size_t build_smem(int C, int own, int part_bytes, int stages, int chunk, int N, int L);
 int build_part_bytes(int M);
 size_t build_extra_bytes(int N, int L);
+// accepted-path KV compaction
+struct KvArgs {
+    const unsigned char* src;
+    long long s_plane, s_batch, s_row;    // bytes
+    unsigned char* dst;
+    long long d_plane, d_batch, d_row;    // bytes
+    int P, B, N, W;
+    long long row_bytes;
+    const int* path_nodes;                // [B, W]
+    const int* num_accepted;              // [B]
+    const int* dst_pos;                   // [B] or null
+    int width;                            // 16, 4 or 1: the copy unit the layout allows
+};
+cudaError_t kv_compact_run(const KvArgs& A, int sms, cudaStream_t st);
 // error text for spec_last_error() from outside the API file
 void set_last_error(const char* msg);
 // adaptive length

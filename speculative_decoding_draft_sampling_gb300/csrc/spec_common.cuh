@@ -10,7 +10,7 @@
 namespace spec {
 
 #ifndef SPEC_THREADS
-#define SPEC_THREADS 256
+#define SPEC_THREADS 384
 #endif
 #ifndef SPEC_CTAS_PER_SM
 #define SPEC_CTAS_PER_SM 2
@@ -39,7 +39,11 @@ __device__ __forceinline__ int csync_or(int p) {
     return r;
 }
 constexpr uint32_t kWaitLimit = 1u << 22;     // queue-wait polls (with backoff): ~seconds, never forever
-constexpr unsigned long long kMbarLimitNs = 2000000000ull;   // an mbarrier wait gives up after 2 s
+// an mbarrier wait gives up after 2 s (test builds may shorten it)
+#ifndef SPEC_WAIT_LIMIT_NS
+#define SPEC_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr unsigned long long kMbarLimitNs = SPEC_WAIT_LIMIT_NS;
 constexpr uint32_t kMbarPollLimit = 1u << 26;                  // ... or after this many polls
 constexpr float kInf = __builtin_huge_valf();
 
@@ -201,6 +205,25 @@ __device__ __forceinline__ uint32_t mapa(uint32_t local_smem, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
     return r;
+}
+// A load through a 32-bit shared-window address (data that reaches a
+// function through a generic pointer would otherwise take the generic path).
+__device__ __forceinline__ uint64_t lds_u64(uint32_t a) {
+    uint64_t v;
+    asm("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+    uint32_t v;
+    asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+// A read-only global load issued where it stands (the compiler may not sink
+// it towards its first use), so that its latency overlaps the work between.
+__device__ __forceinline__ uint32_t ldg_now_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
 }
 __device__ __forceinline__ void st_cluster_v4(uint32_t a, const uint4& v) {
     asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};"

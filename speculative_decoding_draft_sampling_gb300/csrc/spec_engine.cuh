@@ -36,16 +36,50 @@
 
 namespace spec {
 
-// Ring geometry (development builds may override it).
-#ifndef SPEC_CHUNK_BYTES
-#define SPEC_CHUNK_BYTES 16384
+// Optional event trace for development builds (-DSPEC_TRACE): one lane
+// appends (globaltimer, CTA, event, a, b, c) records to a buffer installed by
+// the translation unit's spec_trace_setup_<name>() (every .cu file is its own
+// device module with its own copy of the buffer pointer).
+#ifdef SPEC_TRACE
+struct TraceRec {
+    unsigned long long t;
+    int cta, ev, a, b, c, d;
+};
+static __device__ TraceRec* g_trace;
+static __device__ unsigned g_trace_cap;
+static __device__ unsigned g_trace_n;
+__device__ __forceinline__ void trace_ev(int ev, int a, int b, int c) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    const unsigned i = atomicAdd(&g_trace_n, 1u);
+    if (g_trace && i < g_trace_cap) {
+        TraceRec r;
+        r.t = t; r.cta = blockIdx.x; r.ev = ev; r.a = a; r.b = b; r.c = c; r.d = 0;
+        g_trace[i] = r;
+    }
+}
+#define SPEC_TRACE_EV(ev, a, b, c) ::spec::trace_ev((ev), (a), (b), (c))
+#define SPEC_TRACE_T(v) const long long v = clock64()
+#else
+#define SPEC_TRACE_EV(ev, a, b, c)
+#define SPEC_TRACE_T(v)
 #endif
-#ifndef SPEC_STAGES
-#define SPEC_STAGES 8
+
+// Failure-path test builds (-DSPEC_TEST_HOOKS): when g_test_drop_post is
+// set, the combiner of cluster rank 0 never posts its first slot's first job,
+// so every wait that depends on it runs into its limit and the kernel must
+// leave with the workspace error set.
+#ifdef SPEC_TEST_HOOKS
+static __device__ int g_test_drop_post;
 #endif
-constexpr int kChunkBytes = SPEC_CHUNK_BYTES;   // one ring stage
-constexpr int kStages = SPEC_STAGES;            // most ring stages (the launch picks how many fit)
-static_assert(kChunkBytes % 4096 == 0 && kStages >= 2, "ring geometry");
+
+// Ring geometry: the launch picks the stage size (a multiple of kChunkUnit:
+// a full stage is whole groups of four rounds of 16-byte vectors) and how
+// many stages fit, at most kStages.
+constexpr int kStages = 8;
+constexpr int kChunkUnit = 4 * 16 * (SPEC_THREADS);
+constexpr int kChunkLarge = 2 * kChunkUnit;    // 48 KiB with 384 consumer threads
+constexpr int kChunkSmall = kChunkUnit;        // 24 KiB
 
 constexpr int kMaxC = 16;          // CTAs per cluster, at most
 constexpr int kMaxSlots = 32;      // slots per cluster, at most
@@ -125,6 +159,7 @@ struct Workspace {
 struct EngArgs {
     Workspace W;
     int stages;        // ring stages, 2..kStages
+    int chunk;         // bytes of one stage, a multiple of kChunkUnit
     int C;             // CTAs per cluster (the launch's cluster size)
     int R;             // slots per cluster
     int SL;            // slice length in elements (a multiple of 64)
@@ -135,6 +170,7 @@ struct EngArgs {
 // cluster geometry of a launch, the same in every CTA but for the rank
 struct Geo {
     int stages;        // ring stages
+    int chunk;         // bytes of one stage
     int C;             // CTAs per cluster
     int R;             // slots per cluster
     int rank;          // this CTA's rank
@@ -146,7 +182,7 @@ __device__ __forceinline__ Geo make_geo(const EngArgs& E) {
     Geo g;
     g.C = static_cast<int>(cluster_size());
     g.rank = static_cast<int>(cluster_rank());
-    g.R = E.R; g.SL = E.SL; g.part_bytes = E.part_bytes; g.own = E.own; g.stages = E.stages;
+    g.R = E.R; g.SL = E.SL; g.part_bytes = E.part_bytes; g.own = E.own; g.stages = E.stages; g.chunk = E.chunk;
     return g;
 }
 __device__ __forceinline__ int slice_x0(const Geo& g, int r) { return r * g.SL; }
@@ -170,6 +206,7 @@ struct EngSmem {
     uint64_t jfull[kMaxSlots];   // count 1: the slot's leader posted a job (remote arrive)
     uint64_t parr[kMaxOwn];      // count C: the partials of an own slot arrived (remote arrives)
     Job jd[kMaxSlots];           // mailboxes, written by the leaders
+    Job cur[kMaxOwn];            // combiner: the job in flight of each own slot
     QEnt q[kQ];
     int abort;                   // a wait in this CTA gave up
     int pad[3];
@@ -178,22 +215,63 @@ struct EngSmem {
 // ---------------------------------------------------------------------------
 // bounded waits
 // ---------------------------------------------------------------------------
-// Spin on test(), with backoff, up to kMbarLimitNs; also gives up when the
+// One try_wait on a phase parity: the hardware suspends the thread until the
+// phase completes or kSuspendNs pass (a suspended warp issues nothing, so
+// waiting warps leave the issue slots to the warps that work).
+constexpr uint32_t kSuspendNs = 200000;
+__device__ __forceinline__ bool mbar_try(const uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+// the same for a phase completed by arrivals from other CTAs (acquire at
+// cluster scope: their writes before the arrive are visible)
+__device__ __forceinline__ bool mbar_try_cluster(const uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(bar))), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for one mbarrier phase, up to kMbarLimitNs; gives up early when the
 // CTA aborted or another CTA raised the workspace error.  false: gave up.
+template <bool kCluster = false>
+__device__ __forceinline__ bool wait_phase(const uint64_t* bar, uint32_t parity, volatile int* abort,
+                                           const Ctrl* ctrl) {
+    if (kCluster ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        if (kCluster ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
+        if (*abort) return false;
+        if (ld_relaxed(&ctrl->error) != 0u) return false;
+        if (globaltimer_ns() - t0 > kMbarLimitNs) return false;
+    }
+}
+
+// Poll test() (several barriers at once) until it holds, up to kMbarLimitNs:
+// tight polling first, then a short sleep between polls.  false: gave up.
 template <class T>
-__device__ __forceinline__ bool bounded_wait(T test, volatile int* abort, const Ctrl* ctrl) {
-    if (test()) return true;
-    unsigned long long t0 = globaltimer_ns();
-    uint32_t ns = 32;
+__device__ __forceinline__ bool poll_until(T test, volatile int* abort, const Ctrl* ctrl) {
+    unsigned long long t0 = 0;
     for (uint32_t it = 0;; ++it) {
         if (test()) return true;
-        if (*abort) return false;
-        if ((it & 15u) == 15u) {
+        if ((it & 255u) == 255u) {
+            if (*abort) return false;
             if (ld_relaxed(&ctrl->error) != 0u) return false;
-            if (globaltimer_ns() - t0 > kMbarLimitNs) return false;
+            const unsigned long long now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kMbarLimitNs) return false;
         }
-        nanosleep_ns(ns);
-        if (ns < 256) ns <<= 1;
+        if (it >= 8u) nanosleep_ns(it >= 64u ? 256 : 64);
     }
 }
 __device__ __forceinline__ void raise_abort(volatile int* abort, Ctrl* ctrl) {
@@ -219,38 +297,46 @@ __device__ __forceinline__ StreamPlan plan_none() {
     p.src0 = nullptr; p.src1 = nullptr; p.es0 = 4; p.n = 0; p.ce = 1; p.nch = 0;
     return p;
 }
-__device__ __forceinline__ StreamPlan plan_single(const void* row, int es, int x0, int x1) {
+// `chunk`: the launch's stage size in bytes
+__device__ __forceinline__ StreamPlan plan_single(const void* row, int es, int x0, int x1, int chunk) {
     StreamPlan p;
     p.src0 = static_cast<const unsigned char*>(row) + static_cast<long long>(x0) * es;
     p.src1 = nullptr;
     p.es0 = es;
     p.n = x1 > x0 ? x1 - x0 : 0;
-    p.ce = kChunkBytes / es;
+    p.ce = chunk / es;
     p.nch = (p.n + p.ce - 1) / p.ce;
     return p;
 }
-template <int kEs>
-__device__ __forceinline__ constexpr int dual_chunk_elems() { return (kChunkBytes / (kEs + 4)) & ~63; }
-__device__ __forceinline__ StreamPlan plan_dual(const void* lrow, int es, const float* qrow, int x0, int x1) {
+__device__ __forceinline__ StreamPlan plan_dual(const void* lrow, int es, const float* qrow, int x0, int x1,
+                                                int chunk) {
     StreamPlan p;
     p.src0 = static_cast<const unsigned char*>(lrow) + static_cast<long long>(x0) * es;
     p.src1 = reinterpret_cast<const unsigned char*>(qrow + x0);
     p.es0 = es;
     p.n = x1 > x0 ? x1 - x0 : 0;
-    p.ce = es == 4 ? dual_chunk_elems<4>() : dual_chunk_elems<2>();
+    p.ce = (chunk / (es + 4)) & ~63;
     p.nch = (p.n + p.ce - 1) / p.ce;
     return p;
 }
 
 // The ring as the consumers and the producer see it.
 struct Pipe {
-    unsigned char* buf;    // stages * kChunkBytes, 128-byte aligned
+    unsigned char* buf;    // stages * chunk bytes, 1024-byte aligned
     uint64_t* full;
     uint64_t* empty;
     volatile int* abort;
     Ctrl* ctrl;
     uint32_t stages;
-    __device__ __forceinline__ unsigned char* slot(int s) const { return buf + s * kChunkBytes; }
+    uint32_t magic;        // ceil(2^32 / stages): seq / stages by one multiply-high
+    int chunk;             // bytes of one stage
+    __device__ __forceinline__ unsigned char* slot(int s) const { return buf + s * chunk; }
+    // ring position of sequence number seq: the stage, and how many times
+    // the ring wrapped before it (exact for seq < 2^32 / stages)
+    __device__ __forceinline__ int stage(uint32_t seq) const {
+        return static_cast<int>(seq - __umulhi(seq, magic) * stages);
+    }
+    __device__ __forceinline__ uint32_t wraps(uint32_t seq) const { return __umulhi(seq, magic); }
 };
 
 // Producer lane: issue chunk c of plan p into stage s.  Bytes past the
@@ -285,6 +371,7 @@ __device__ __forceinline__ void issue_chunk(const Pipe& P, const StreamPlan& p, 
 // derive from FnHooks for the hooks they do not use.
 struct FnHooks {
     static constexpr bool kPrepass = false;
+    static constexpr bool kVec4 = false;   // the functor has vec4() for four rounds at once
     __device__ __forceinline__ bool use_prepass() const { return false; }
     template <int N> __device__ __forceinline__ void pre_vec(bool, const float (&)[N], int) {}
     __device__ __forceinline__ void pre_scalar(bool, float, int) {}
@@ -294,19 +381,17 @@ struct FnHooks {
     __device__ __forceinline__ void after_release(int) {}
 };
 
-constexpr int kChunkVecs = kChunkBytes / 16;                  // vectors in a full chunk
-constexpr int kFullRounds = (kChunkVecs + kThreads - 1) / kThreads;
-static_assert(kChunkVecs % kThreads == 0, "a full chunk is a whole number of rounds");
+static_assert(kChunkUnit % (4 * 16 * kThreads) == 0, "a full stage is whole groups of four rounds");
 
 // Wait for chunk `seq` (every consumer thread).  With tma = false the
 // consumers copy it from global memory themselves (the producer issues
 // nothing in that mode).
 __device__ __forceinline__ bool take_chunk(const Pipe& P, uint32_t seq, bool tma, bool& dead,
                                            const StreamPlan& p, int c) {
-    const int s = static_cast<int>(seq % P.stages);
+    const int s = P.stage(seq);
     if (tma) {
-        const uint32_t par = (seq / P.stages) & 1u;
-        const bool ok = !dead && bounded_wait([&]() { return mbar_test(&P.full[s], par); }, P.abort, P.ctrl);
+        const uint32_t par = P.wraps(seq) & 1u;
+        const bool ok = !dead && wait_phase(&P.full[s], par, P.abort, P.ctrl);
         dead = !__all_sync(0xffffffffu, ok);   // warp-uniform from here on
         if (dead) *P.abort = 1;
         return !dead;
@@ -335,19 +420,54 @@ __device__ __forceinline__ bool take_chunk(const Pipe& P, uint32_t seq, bool tma
 __device__ __forceinline__ void release_chunk(const Pipe& P, uint32_t seq, bool tma, bool dead) {
     if (!tma || dead) return;
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(&P.empty[seq % P.stages]);
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&P.empty[P.stage(seq)]);
 }
 
 // Stream one row range (plan from plan_single) through fn.  Returns false
 // (in every consumer thread) when a chunk wait gave up.  `seq` is the
 // consumer's ring sequence number.
+// The kRounds rounds of a full stage, four rounds' vectors loaded at a time
+// (independent loads); functors with vec4() test the four together.
+template <class E, int kRounds, class Fn>
+__device__ __forceinline__ void full_stage(const uint4* sv, int cx0, Fn& fn) {
+    constexpr int VEC = E::kVec;
+    static_assert(kRounds % 4 == 0, "whole groups of four rounds");
+#pragma unroll
+    for (int g = 0; g < kRounds; g += 4) {
+        float vals[4][VEC];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) E::unpack(sv[(g + r) * kThreads + threadIdx.x], vals[r]);
+        if constexpr (Fn::kVec4) {
+            fn.vec4(vals, cx0 + (g * kThreads + threadIdx.x) * VEC);
+        } else {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) fn.vec(true, vals[r], cx0 + ((g + r) * kThreads + threadIdx.x) * VEC);
+        }
+    }
+}
+
 template <class E, class Fn>
 __device__ bool consume_row(const Pipe& P, uint32_t& seq, const StreamPlan& p, bool tma, int x0, Fn& fn) {
     constexpr int VEC = E::kVec;
     bool dead = false;
+#ifdef SPEC_TRACE
+    long long wait_cyc = 0, first_wait = 0, comp_cyc = 0, rel_cyc = 0;
+    const long long t_beg = clock64();
+#endif
     for (int c = 0; c < p.nch; ++c, ++seq) {
+#ifdef SPEC_TRACE
+        const long long tw = clock64();
+#endif
         const bool have = take_chunk(P, seq, tma, dead, p, c);
-        const unsigned char* sm = P.slot(static_cast<int>(seq % P.stages));
+#ifdef SPEC_TRACE
+        wait_cyc += clock64() - tw;
+        if (c == 0) first_wait = clock64() - tw;
+        if (threadIdx.x == 0) SPEC_TRACE_EV(21, static_cast<int>(seq), static_cast<int>(clock64() - tw), c);
+#endif
+#ifdef SPEC_TRACE
+        const long long tcb = clock64();
+#endif
+        const unsigned char* sm = P.slot(P.stage(seq));
         const int ne = min(p.ce, p.n - c * p.ce);
         const int cx0 = x0 + c * p.ce;
         const int nv = (ne * E::kBytes) >> 4;
@@ -368,13 +488,10 @@ __device__ bool consume_row(const Pipe& P, uint32_t& seq, const StreamPlan& p, b
             fn.pre_end();
         }
         if (have) {
-            if (nv == kChunkVecs) {
-                // full chunk: every round's vector loaded first (independent loads)
-                float vals[kFullRounds][VEC];
-#pragma unroll
-                for (int r = 0; r < kFullRounds; ++r) E::unpack(sv[r * kThreads + threadIdx.x], vals[r]);
-#pragma unroll
-                for (int r = 0; r < kFullRounds; ++r) fn.vec(true, vals[r], cx0 + (r * kThreads + threadIdx.x) * VEC);
+            if (nv * 16 == P.chunk) {
+                // full stage: whole groups of four rounds, unrolled
+                if (P.chunk == kChunkLarge) full_stage<E, kChunkLarge / (16 * kThreads)>(sv, cx0, fn);
+                else full_stage<E, kChunkSmall / (16 * kThreads)>(sv, cx0, fn);
             } else {
                 const int rounds = (nv + kThreads - 1) / kThreads;
                 for (int r = 0; r < rounds; ++r) {
@@ -395,9 +512,22 @@ __device__ bool consume_row(const Pipe& P, uint32_t& seq, const StreamPlan& p, b
             }
             fn.chunk_end(c, sm, cx0, nv);
         }
+#ifdef SPEC_TRACE
+        const long long tce = clock64();
+        comp_cyc += tce - tcb;
+#endif
         release_chunk(P, seq, tma, dead);
         if (have) fn.after_release(c);
+#ifdef SPEC_TRACE
+        rel_cyc += clock64() - tce;
+#endif
     }
+#ifdef SPEC_TRACE
+    if (threadIdx.x == 0) {
+        SPEC_TRACE_EV(10, static_cast<int>(first_wait), static_cast<int>(wait_cyc), static_cast<int>(clock64() - t_beg));
+        SPEC_TRACE_EV(13, static_cast<int>(comp_cyc), static_cast<int>(rel_cyc), p.nch);
+    }
+#endif
     return !csync_or(dead);
 }
 
@@ -410,7 +540,7 @@ __device__ bool consume_row2(const Pipe& P, uint32_t& seq, const StreamPlan& p, 
     bool dead = false;
     for (int c = 0; c < p.nch; ++c, ++seq) {
         const bool have = take_chunk(P, seq, tma, dead, p, c);
-        const unsigned char* sm = P.slot(static_cast<int>(seq % P.stages));
+        const unsigned char* sm = P.slot(P.stage(seq));
         const int ne = min(p.ce, p.n - c * p.ce);
         const int cx0 = x0 + c * p.ce;
         const int qoff = p.ce * E::kBytes;
@@ -619,7 +749,7 @@ struct Engine {
     using OSmem = typename Op::Smem;
 
     // dynamic shared memory: EngSmem | Op::Smem | partials (own slots x C) |
-    // staging (one partial) | ring (stages x kChunkBytes) | kernel extras
+    // staging (one partial) | ring (stages x chunk bytes) | kernel extras
     __host__ __device__ static size_t op_off() { return (sizeof(EngSmem) + 127) & ~size_t(127); }
     __host__ __device__ static size_t part_off() { return (op_off() + sizeof(OSmem) + 127) & ~size_t(127); }
     __host__ __device__ static size_t stage_off(int C, int own, int part_bytes) {
@@ -628,8 +758,8 @@ struct Engine {
     __host__ __device__ static size_t ring_off(int C, int own, int part_bytes) {
         return (stage_off(C, own, part_bytes) + part_bytes + 1023) & ~size_t(1023);
     }
-    __host__ __device__ static size_t smem_bytes(int C, int own, int part_bytes, int stages) {
-        return ring_off(C, own, part_bytes) + static_cast<size_t>(stages) * kChunkBytes;
+    __host__ __device__ static size_t smem_bytes(int C, int own, int part_bytes, int stages, int chunk) {
+        return ring_off(C, own, part_bytes) + static_cast<size_t>(stages) * chunk;
     }
 
     __device__ static void run(const Args& A, const Workspace& W, Geo G, unsigned char* smem) {
@@ -660,6 +790,8 @@ struct Engine {
         Pipe P;
         P.buf = ring; P.full = es.full; P.empty = es.empty; P.abort = &es.abort; P.ctrl = W.ctrl;
         P.stages = static_cast<uint32_t>(G.stages);
+        P.magic = static_cast<uint32_t>(0xffffffffu / P.stages + 1u);
+        P.chunk = G.chunk;
         const bool tma = Op::tma(A);
         if (threadIdx.x >= kCombiner0) {
             combiner(A, W, G, es, os, parts);
@@ -707,35 +839,57 @@ struct Engine {
     __device__ static void combiner(const Args& A, const Workspace& W, const Geo& G, EngSmem& es, OSmem& os,
                                     unsigned char* parts) {
         const int nown = own_count(G);
-        Job cur[kMaxOwn];
+        Job* cur = es.cur;      // shared memory: a register array indexed by slot would live in local memory
         uint32_t phase = 0;     // bit i: parity of own slot i's next arrival phase
         int active = 0;
         for (int i = 0; i < nown; ++i) {
             const int s = G.rank + i * G.C;
-            cur[i] = claim(A, W, G, os);
-            post(G, es, s, cur[i]);
-            if (cur[i].b >= 0) active |= 1 << i;
+            const Job j = claim(A, W, G, os);
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) cur[i] = j;
+#ifdef SPEC_TEST_HOOKS
+            if (!(g_test_drop_post && G.rank == 0 && i == 0 && blockIdx.x == 0))
+#endif
+            post(G, es, s, j);
+            if (j.b >= 0) active |= 1 << i;
         }
         while (active) {
             int ready = -1;
-            const bool ok = bounded_wait([&]() {
-                for (int i = 0; i < nown; ++i)
-                    if (((active >> i) & 1) && mbar_test_cluster(&es.parr[i], (phase >> i) & 1u)) {
-                        ready = i;
-                        return true;
-                    }
-                return false;
-            }, &es.abort, W.ctrl);
+            bool ok;
+            if (nown == 1) {
+                ok = wait_phase<true>(&es.parr[0], phase & 1u, &es.abort, W.ctrl);
+                ready = 0;
+            } else {
+                ok = poll_until([&]() {
+                    for (int i = 0; i < nown; ++i)
+                        if (((active >> i) & 1) && mbar_test_cluster(&es.parr[i], (phase >> i) & 1u)) {
+                            ready = i;
+                            return true;
+                        }
+                    return false;
+                }, &es.abort, W.ctrl);
+            }
             if (!__all_sync(0xffffffffu, ok)) { raise_abort(&es.abort, W.ctrl); break; }
             ready = __shfl_sync(0xffffffffu, ready, 0);
             const int i = ready;
             const int s = G.rank + i * G.C;
             phase ^= 1u << i;
             const unsigned char* pp = parts + static_cast<size_t>(i) * G.C * G.part_bytes;
-            Job nx = Op::combine(A, G, cur[i], pp, os);
+            const Job cj = cur[i];
+            if ((threadIdx.x & 31) == 0) SPEC_TRACE_EV(6, s, cj.b, cj.row);
+            SPEC_TRACE_T(tk0);
+            Job nx = Op::combine(A, G, cj, pp, os);
+            SPEC_TRACE_T(tk1);
             if (nx.b == kJobDone) nx = claim(A, W, G, os);
-            cur[i] = nx;
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) cur[i] = nx;
+            SPEC_TRACE_T(tk2);
             post(G, es, s, nx);
+            if ((threadIdx.x & 31) == 0) {
+                SPEC_TRACE_EV(7, s, nx.b, nx.row);
+                SPEC_TRACE_EV(14, static_cast<int>(tk1 - tk0), static_cast<int>(tk2 - tk1),
+                              static_cast<int>(clock64() - tk2));
+            }
             if (nx.b < 0) active &= ~(1 << i);
         }
     }
@@ -750,7 +904,7 @@ struct Engine {
         bool dead = false;
         while (retired < G.R) {
             int s = -1;
-            dead = !bounded_wait([&]() {
+            dead = !poll_until([&]() {
                 for (int k = 0; k < G.R; ++k) {
                     const int t = (s0 + k) % G.R;
                     if (mbar_test_cluster(&es.jfull[t], (jph >> t) & 1u)) { s = t; return true; }
@@ -771,8 +925,7 @@ struct Engine {
             if (job.b < 0) ++retired;
             // hand the job to the consumers
             const int qi = static_cast<int>(qn % kQ);
-            if (qn >= static_cast<uint32_t>(kQ) &&
-                !bounded_wait([&]() { return mbar_test(&es.qempty[qi], ((qn / kQ) - 1) & 1u); }, P.abort, W.ctrl)) {
+            if (qn >= static_cast<uint32_t>(kQ) && !wait_phase(&es.qempty[qi], ((qn / kQ) - 1) & 1u, P.abort, W.ctrl)) {
                 dead = true;
                 break;
             }
@@ -780,18 +933,19 @@ struct Engine {
             es.q[qi].slot = s;
             mbar_arrive(&es.qfull[qi]);
             ++qn;
+            SPEC_TRACE_EV(1, s, job.b, job.row);
             if (job.b < 0 || !tma || (job.target >= 0 && job.target != G.rank)) continue;
             const StreamPlan p = Op::plan(A, G, job);
             for (int ci = 0; ci < p.nch; ++ci, ++seq) {
-                const int st = static_cast<int>(seq % P.stages);
-                if (seq >= P.stages &&
-                    !bounded_wait([&]() { return mbar_test(&P.empty[st], ((seq / P.stages) - 1) & 1u); }, P.abort,
-                                  W.ctrl)) {
+                const int st = P.stage(seq);
+                if (seq >= P.stages && !wait_phase(&P.empty[st], (P.wraps(seq) - 1) & 1u, P.abort, W.ctrl)) {
                     dead = true;
                     break;
                 }
                 issue_chunk(P, p, ci, st);
+                SPEC_TRACE_EV(20, static_cast<int>(seq), st, ci);
             }
+            SPEC_TRACE_EV(2, s, job.b, job.row);
             if (dead) break;
         }
         if (dead) {
@@ -799,8 +953,8 @@ struct Engine {
             // wait (bounded) for the copies still in flight before the CTA can end
             const uint32_t first = seq > P.stages ? seq - P.stages : 0u;
             for (uint32_t q = first; q < seq; ++q) {
-                const int st = static_cast<int>(q % P.stages);
-                const uint32_t par = (q / P.stages) & 1u;
+                const int st = P.stage(q);
+                const uint32_t par = P.wraps(q) & 1u;
                 const unsigned long long t0 = globaltimer_ns();
                 while (!mbar_test(&P.full[st], par) && globaltimer_ns() - t0 < kMbarLimitNs) nanosleep_ns(128);
             }
@@ -814,7 +968,7 @@ struct Engine {
         int retired = 0;
         while (retired < G.R) {
             const int qi = static_cast<int>(qn % kQ);
-            const bool ok = bounded_wait([&]() { return mbar_test(&es.qfull[qi], (qn / kQ) & 1u); }, P.abort, W.ctrl);
+            const bool ok = wait_phase(&es.qfull[qi], (qn / kQ) & 1u, P.abort, W.ctrl);
             if (csync_or(!ok)) { raise_abort(P.abort, W.ctrl); break; }
             const Job job = es.q[qi].job;
             const int s = es.q[qi].slot;
@@ -831,18 +985,22 @@ struct Engine {
                 if (threadIdx.x == 0) mbar_arrive_cluster(arr, 1u);
                 continue;
             }
+            if (threadIdx.x == 0) SPEC_TRACE_EV(3, s, job.b, job.row);
             const int nb = Op::consume(A, G, P, seq, tma, job, os, stage);
             if (nb < 0) { raise_abort(P.abort, W.ctrl); break; }
+            if (threadIdx.x == 0) SPEC_TRACE_EV(4, s, job.b, job.row);
             // the partial into the leader's slot area, then one counted arrival
             const uint32_t dst = mapa(smem_u32(parts + (static_cast<size_t>(oi) * G.C + G.rank) * G.part_bytes),
                                       static_cast<uint32_t>(leader));
             csync();   // the staging partial is complete
             for (int i = threadIdx.x; i < nb / 16; i += kThreads)
                 st_cluster_v4(dst + 16u * i, reinterpret_cast<const uint4*>(stage)[i]);
-            csync();   // every store of the partial is ordered before the arrive
+            csync();   // every consumer's stores of the partial happen before the arrive
             if (threadIdx.x == 0) {
-                fence_acq_rel_cluster();
+                // release at cluster scope: with the barrier above it makes
+                // every consumer's stores visible to the leader's acquire
                 mbar_arrive_cluster(arr, 1u);
+                SPEC_TRACE_EV(5, s, job.b, job.row);
             }
         }
     }

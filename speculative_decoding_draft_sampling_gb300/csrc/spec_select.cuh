@@ -223,35 +223,6 @@ __device__ inline int compact_list(uint64_t* list, int n, uint32_t t, int* ired)
 // ---------------------------------------------------------------------------
 // functors
 // ---------------------------------------------------------------------------
-// Watches one element (the drafted token y) as the slice streams by: records
-// its logit from the chunk in shared memory, and thread 0 of the slice that
-// holds y fetches q(y) at the first chunk so that the load overlaps the
-// stream.  The slice reports both with its partial.
-struct DraftWatch {
-    int y = -1;                 // watched index (-1: none)
-    int x0 = 0, x1 = 0;         // the slice
-    const float* qrow = nullptr;
-    float ly = 0.f, qy = 0.f;
-    bool seen = false;
-    __device__ __forceinline__ bool owns() const { return y >= x0 && y < x1; }
-    __device__ __forceinline__ void begin(int c) {
-        if (c == 0 && threadIdx.x == 0 && qrow && owns()) qy = qrow[y];
-    }
-    template <int N>
-    __device__ __forceinline__ void see(const float (&v)[N], int x) {
-        const unsigned d = static_cast<unsigned>(y - x);
-        if (d < static_cast<unsigned>(N)) {
-#pragma unroll
-            for (int j = 0; j < N; ++j)
-                if (static_cast<unsigned>(j) == d) ly = v[j];
-            seen = true;
-        }
-    }
-    __device__ __forceinline__ void see1(float v, int x) {
-        if (x == y) { ly = v; seen = true; }
-    }
-};
-
 // a value that poisons a row: NaN or +inf (a running max_nan sees both)
 __device__ __forceinline__ uint32_t bad_max(float vmx) { return !(vmx < kInf); }
 
@@ -279,6 +250,23 @@ struct ArgmaxFn : FnHooks {
         vmx = max_nan(vmx, v);
         if (v > bv) { bv = v; bx = x; }
     }
+    // four rounds at once (vector r at x + r * kThreads * VEC): one test
+    // decides whether any element can beat the thread's best; the rounds are
+    // then examined in increasing index order, so the lowest index still wins
+    static constexpr bool kVec4 = true;
+    __device__ __forceinline__ void vec4(const float (&v)[4][E::kVec], int x) {
+        const float m0 = vmax_nan(v[0]), m1 = vmax_nan(v[1]), m2 = vmax_nan(v[2]), m3 = vmax_nan(v[3]);
+        const float mm = max_nan(max_nan(m0, m1), max_nan(m2, m3));
+        vmx = max_nan(vmx, mm);
+        if (!(mm <= bv)) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+#pragma unroll
+                for (int j = 0; j < E::kVec; ++j)
+                    if (v[r][j] > bv) { bv = v[r][j]; bx = x + r * kThreads * E::kVec + j; }
+            }
+        }
+    }
     // composite key of the thread's best (0 when it saw no value above -inf)
     __device__ __forceinline__ uint64_t key() const { return bx >= 0 ? ckey(bv, bx) : 0ull; }
     __device__ __forceinline__ uint32_t bad_flag() const { return bad_max(vmx); }
@@ -295,11 +283,8 @@ struct SumExpFn : FnHooks {
     float m = -kInf;
     float s = 0.f;
     float vmx = -kInf;
-    DraftWatch dw;
-    __device__ __forceinline__ void chunk_begin(int ci) { dw.begin(ci); }
-    __device__ __forceinline__ void vec(bool act, const float (&v)[E::kVec], int x) {
+    __device__ __forceinline__ void vec(bool act, const float (&v)[E::kVec], int) {
         if (!act) return;
-        dw.see(v, x);
         const float lm = vmax_nan(v);
         vmx = max_nan(vmx, lm);
         if (lm > m) {
@@ -313,9 +298,8 @@ struct SumExpFn : FnHooks {
             s += ex2((v[j] - m) * c);
         }
     }
-    __device__ __forceinline__ void scalar(bool act, float v, int x) {
+    __device__ __forceinline__ void scalar(bool act, float v, int) {
         if (!act) return;
-        dw.see1(v, x);
         vmx = max_nan(vmx, v);
         if (v > m) {
             s *= ex2((m - v) * c);
@@ -357,7 +341,7 @@ struct RadixFn : FnHooks {
 // appends with ballots and a register counter and never waits for the other
 // warps.
 struct TopkSmem {
-    static constexpr int kRegion = 512;                 // keys per warp
+    static constexpr int kRegion = 256;                 // keys per warp
     static constexpr int kSlots = 4;                    // per-thread keys within a chunk
     alignas(16) uint64_t cand[kWarps * kRegion];
     uint64_t slot[kSlots][kThreads];
@@ -416,7 +400,6 @@ struct TopkHistFn : FnHooks {
     int rr;             // rounds seen in the current chunk
     int tcnt;           // keys in this thread's slots
     uint32_t tag;       // the unit's tag for the shared filter (nonzero, CTA-uniform)
-    DraftWatch dw;
 
     __device__ __forceinline__ void set_theta(uint64_t t) { theta = t; thr_f = key_to_thr(hkey(t)); }
     // `unit_tag`: nonzero, distinct for every unit a CTA streams
@@ -425,7 +408,6 @@ struct TopkHistFn : FnHooks {
         set_theta(static_cast<uint64_t>(hint) << 32);
         vmx = -kInf; nw = 0; lost = 0; tmax = 0; cmask = 0; rr = 0; tcnt = 0;
     }
-    __device__ __forceinline__ void chunk_begin(int c) { dw.begin(c); }
     __device__ __forceinline__ bool use_prepass() const { return theta == 0; }
     __device__ __forceinline__ void pre_vec(bool act, const float (&v)[VEC], int) {
         if (!act) return;
@@ -486,7 +468,6 @@ struct TopkHistFn : FnHooks {
     // to the thread's slots, or the round is deferred to chunk_end().
     __device__ __forceinline__ void vec(bool act, const float (&v)[VEC], int x) {
         if (act) {
-            dw.see(v, x);
             const float m4 = vmax_nan(v);
             vmx = max_nan(vmx, m4);
             if (!(m4 < thr_f)) {
@@ -510,10 +491,43 @@ struct TopkHistFn : FnHooks {
         }
         ++rr;
     }
+    // four rounds at once (vector r at x + r * kThreads * VEC): one test
+    // whether any element reaches the filter; only then per round as vec()
+    static constexpr bool kVec4 = true;
+    __device__ __forceinline__ void vec4(const float (&v)[4][VEC], int x) {
+        const float m0 = vmax_nan(v[0]), m1 = vmax_nan(v[1]), m2 = vmax_nan(v[2]), m3 = vmax_nan(v[3]);
+        const float mm = max_nan(max_nan(m0, m1), max_nan(m2, m3));
+        vmx = max_nan(vmx, mm);
+        if (!(mm < thr_f)) {
+            const float ms[4] = {m0, m1, m2, m3};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                if (!(ms[r] < thr_f)) {
+                    const int xr = x + r * kThreads * VEC;
+                    uint32_t m = 0;
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j)
+                        if (passes(v[r][j], xr + j)) m |= 1u << j;
+                    const int c = __popc(m);
+                    if (tcnt + c <= TopkSmem::kSlots) {
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) {
+                            if ((m >> j) & 1u) {
+                                S->slot[tcnt][threadIdx.x] = ckey(v[r][j], xr + j);
+                                ++tcnt;
+                            }
+                        }
+                    } else {
+                        cmask |= 1u << (rr + r);
+                    }
+                }
+            }
+        }
+        rr += 4;
+    }
     __device__ __forceinline__ void scalar(bool act, float v, int x) {
         bool any = false;
         if (act) {
-            dw.see1(v, x);
             vmx = max_nan(vmx, v);
             any = passes(v, x);
         }

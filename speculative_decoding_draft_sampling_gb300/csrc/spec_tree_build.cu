@@ -46,7 +46,6 @@ struct BuildSmem {
     int ired[kWarps + 4];
     int hist[64];
     uint32_t scratch[kWarps + 2];
-    uint32_t tag;            // consumers: unit tag for the shared filter
     EnumHdr eh;              // combiner
     alignas(16) uint64_t list[kBuildList];   // combiner: gathered keys
 };
@@ -257,6 +256,16 @@ __device__ void enum_load(const BuildArgs& A, int b, EnumHdr& eh, const EnumView
     __syncwarp();
 }
 
+// The row's M largest composite keys (value desc, index asc) from the
+// slices' reports, on the combiner warp: every key at or above the largest
+// slice filter, cut to exactly M (composite keys are unique).  A slice
+// overflow, or more keys than the list holds, re-derives them from the row
+// itself.  `flags`, `theta` (the largest slice filter) and `cnt` (lane r:
+// slice r's key count) come from the headers.  Keys, unordered, to
+// list[0..return); 0 for a bad row.
+__device__ int merge_topm_w(const unsigned char* parts, int pb, int C, int M, uint32_t flags, uint64_t theta, int cnt,
+                            const float* qrow, int V, uint64_t* list);
+
 struct BuildOp {
     using Args = BuildArgs;
     using Smem = BuildSmem;
@@ -264,15 +273,12 @@ struct BuildOp {
     __device__ static int batch(const Args& A) { return A.B; }
     __device__ static bool tma(const Args& A) { return A.tma_q != 0; }
     __device__ static void init_smem(const Args&, const Geo&, Smem& sm) {
-        if (threadIdx.x == 0) {
-            topk_smem_init(sm.tk);
-            sm.tag = 0;
-        }
+        if (threadIdx.x == 0) topk_smem_init(sm.tk);
     }
     // the combiner's enumeration scratch sits after the ring
     __device__ static EnumView view(const Args& A, const Geo& G) {
         extern __shared__ __align__(128) unsigned char smem[];
-        const size_t off = Engine<BuildOp>::smem_bytes(G.C, G.own, G.part_bytes, G.stages);
+        const size_t off = Engine<BuildOp>::smem_bytes(G.C, G.own, G.part_bytes, G.stages, G.chunk);
         return enum_view(smem + ((off + 15) & ~static_cast<size_t>(15)), A.N, A.L);
     }
     __device__ static Job first(const Args& A, const Geo& G, int b, Smem& sm) {
@@ -297,7 +303,7 @@ struct BuildOp {
     }
     __device__ static StreamPlan plan(const Args& A, const Geo& G, const Job& j) {
         const float* qrow = A.q + static_cast<long long>(j.b) * A.q_bs + static_cast<long long>(j.row) * A.q_rs;
-        return plan_single(qrow, 4, slice_x0(G, G.rank), slice_x1(G, G.rank, A.V));
+        return plan_single(qrow, 4, slice_x0(G, G.rank), slice_x1(G, G.rank, A.V), G.chunk);
     }
     // consumers: this slice's top-M composite keys (value desc, index asc)
     __device__ static int consume(const Args& A, const Geo& G, const Pipe& P, uint32_t& seq, bool tma, const Job& j,
@@ -305,10 +311,8 @@ struct BuildOp {
         PartHdr* ph = reinterpret_cast<PartHdr*>(out);
         uint64_t* pk = reinterpret_cast<uint64_t*>(ph + 1);
         const int M = A.M;
-        if (threadIdx.x == 0) sm.tag = sm.tag + 1u;
-        csync();
         TopkHistFn<F32, false> fn;
-        fn.init(&sm.tk, M, 0u, sm.tag);
+        fn.init(&sm.tk, M, 0u, seq + 1u);   // every consumer holds the same seq
         if (!consume_row<F32>(P, seq, plan(A, G, j), tma, slice_x0(G, G.rank), fn)) return -1;
         uint64_t F;
         uint32_t oflow, bad;
@@ -418,41 +422,9 @@ struct BuildOp {
         }
         flags = __reduce_or_sync(0xffffffffu, flags);
         theta = warp_max_u64(theta);
+        const float* qrow = A.q + static_cast<long long>(b) * A.q_bs + static_cast<long long>(d - 1) * A.q_rs;
         uint64_t* list = sm.list;
-        int n = 0;
-        if (flags & kPfBad) {
-            n = 0;
-        } else if (flags & kPfOverflow) {
-            const float* qrow = A.q + static_cast<long long>(b) * A.q_bs + static_cast<long long>(d - 1) * A.q_rs;
-            n = fallback(qrow, A.V, M, list);
-        } else {
-            // every slice key at or above the largest slice filter, then the top M
-            const uint32_t lt = (1u << l) - 1u;
-            for (int r = 0; r < C; ++r) {
-                const int cr = __shfl_sync(0xffffffffu, cnt, r);
-                const uint64_t* keys = reinterpret_cast<const uint64_t*>(part_at(parts, pb, r) + 1);
-                for (int i0 = 0; i0 < cr; i0 += 32) {
-                    const int i = i0 + l;
-                    uint64_t key = 0;
-                    bool p = false;
-                    if (i < cr) { key = keys[i]; p = key >= theta; }
-                    const uint32_t bal = __ballot_sync(0xffffffffu, p);
-                    if (p) {
-                        const int pos = n + __popc(bal & lt);
-                        if (pos < kBuildList) list[pos] = key;
-                    }
-                    n += __popc(bal);
-                }
-            }
-            __syncwarp();
-            if (n > kBuildList) {
-                const float* qrow = A.q + static_cast<long long>(b) * A.q_bs + static_cast<long long>(d - 1) * A.q_rs;
-                n = fallback(qrow, A.V, M, list);
-            } else if (n > M) {
-                const uint64_t kth = kth_key_w(list, n, M);
-                n = compact_key_w(list, n, kth);   // exactly M: composite keys are unique
-            }
-        }
+        const int n = merge_topm_w(parts, pb, C, M, flags, theta, cnt, qrow, A.V, list);
         // the depth list in rank order (value desc, index asc)
         for (int i = l; i < n; i += 32) {
             const uint64_t key = list[i];
@@ -478,6 +450,132 @@ struct BuildOp {
     }
 };
 
+__device__ int merge_topm_w(const unsigned char* parts, int pb, int C, int M, uint32_t flags, uint64_t theta, int cnt,
+                            const float* qrow, int V, uint64_t* list) {
+    const int l = threadIdx.x & 31;
+    if (flags & kPfBad) return 0;
+    if (flags & kPfOverflow) return BuildOp::fallback(qrow, V, M, list);
+    const uint32_t lt = (1u << l) - 1u;
+    int n = 0;
+    for (int r = 0; r < C; ++r) {
+        const int cr = __shfl_sync(0xffffffffu, cnt, r);
+        const uint64_t* keys = reinterpret_cast<const uint64_t*>(part_at(parts, pb, r) + 1);
+        for (int i0 = 0; i0 < cr; i0 += 32) {
+            const int i = i0 + l;
+            uint64_t key = 0;
+            bool p = false;
+            if (i < cr) { key = keys[i]; p = key >= theta; }
+            const uint32_t bal = __ballot_sync(0xffffffffu, p);
+            if (p) {
+                const int pos = n + __popc(bal & lt);
+                if (pos < kBuildList) list[pos] = key;
+            }
+            n += __popc(bal);
+        }
+    }
+    __syncwarp();
+    if (n > kBuildList) return BuildOp::fallback(qrow, V, M, list);
+    if (n > M) {
+        const uint64_t kth = kth_key_w(list, n, M);
+        n = compact_key_w(list, n, kth);   // exactly M: composite keys are unique
+    }
+    return n;
+}
+
+// ---------------------------------------------------------------------------
+// EAGLE-2 expansion rows ([SD-survey] §4 "EAGLE-2"): every frontier node's
+// conditional draft row reduced to its K2 most probable tokens (probability
+// descending, lower id first), one engine unit per (request, frontier slot),
+// so that every row of the step streams in parallel.
+// ---------------------------------------------------------------------------
+size_t eagle_row_extra_bytes(int K2) { return sizeof(EagleRowHdr) + static_cast<size_t>(K2 > 0 ? K2 : 1) * 8; }
+
+struct EagleOp {
+    using Args = EagleArgs;
+    using Smem = BuildSmem;
+
+    __device__ static int batch(const Args& A) { return A.base.B * A.F; }
+    __device__ static bool tma(const Args& A) { return A.base.tma_q != 0; }
+    __device__ static void init_smem(const Args&, const Geo&, Smem& sm) {
+        if (threadIdx.x == 0) topk_smem_init(sm.tk);
+    }
+    __device__ static EagleRowHdr* row_hdr(const Args& A, int u) {
+        return reinterpret_cast<EagleRowHdr*>(A.base.E.W.extra + static_cast<size_t>(u) * A.base.E.W.extra_stride);
+    }
+    __device__ static Job first(const Args& A, const Geo&, int u, Smem&) {
+        const int b = u / A.F, f = u - b * A.F;
+        int nf = A.num_front_in[b];
+        nf = nf < 0 ? 0 : (nf > A.F ? A.F : nf);
+        int n = 0;
+        if (f >= nf) {
+            n = -1;
+        } else {
+            // node ids below the (valid) generated count
+            const int g = A.num_gen[b];
+            const int g0 = g < 1 ? 0 : (g > A.G ? A.G : g);
+            const int id = A.front_in[static_cast<long long>(b) * A.F + f];
+            if (id < 0 || id >= g0) n = -2;
+        }
+        if (n < 0) {
+            if ((threadIdx.x & 31) == 0) {
+                EagleRowHdr* h = row_hdr(A, u);
+                h->n = n;
+                h->bad = 0;
+            }
+            __syncwarp();
+            return job_done();
+        }
+        return make_job(b, f, 0, 0);
+    }
+    __device__ static StreamPlan plan(const Args& A, const Geo& G, const Job& j) { return BuildOp::plan(A.base, G, j); }
+    __device__ static int consume(const Args& A, const Geo& G, const Pipe& P, uint32_t& seq, bool tma, const Job& j,
+                                  Smem& sm, unsigned char* out) {
+        return BuildOp::consume(A.base, G, P, seq, tma, j, sm, out);
+    }
+    __device__ static Job combine(const Args& A, const Geo& G, const Job& j, const unsigned char* parts, Smem& sm) {
+        const int l = threadIdx.x & 31;
+        const int M = A.base.M, C = G.C, pb = G.part_bytes;
+        uint32_t flags = 0;
+        uint64_t theta = 0;
+        int cnt = 0;
+        if (l < C) {
+            const PartHdr* h = part_at(parts, pb, l);
+            flags = h->flags; theta = h->kth; cnt = h->cnt;
+        }
+        flags = __reduce_or_sync(0xffffffffu, flags);
+        theta = warp_max_u64(theta);
+        const float* qrow = A.base.q + static_cast<long long>(j.b) * A.base.q_bs +
+                            static_cast<long long>(j.row) * A.base.q_rs;
+        const int n = merge_topm_w(parts, pb, C, M, flags, theta, cnt, qrow, A.base.V, sm.list);
+        const int u = j.b * A.F + j.row;
+        EagleRowHdr* h = row_hdr(A, u);
+        int* tok = reinterpret_cast<int*>(h + 1);
+        float* prob = reinterpret_cast<float*>(tok + M);
+        for (int i = l; i < n; i += 32) {
+            const uint64_t key = sm.list[i];
+            int r = 0;
+            for (int q = 0; q < n; ++q) r += sm.list[q] > key;
+            tok[r] = ckey_idx(key);
+            prob[r] = ckey_val(key);
+        }
+        if (l == 0) {
+            h->n = n;
+            h->bad = (flags & kPfBad) ? 1 : 0;
+        }
+        __syncwarp();
+        return job_done();
+    }
+};
+
+__global__ void __launch_bounds__(kBlockThreads, 1) eagle_rows_kernel(const EagleArgs A) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    Engine<EagleOp>::run(A, A.base.E.W, make_geo(A.base.E), smem);
+}
+const void* eagle_rows_kernel_ptr() { return reinterpret_cast<const void*>(&eagle_rows_kernel); }
+size_t eagle_rows_smem(int C, int own, int part_bytes, int stages, int chunk) {
+    return Engine<EagleOp>::smem_bytes(C, own, part_bytes, stages, chunk);
+}
+
 __global__ void __launch_bounds__(kBlockThreads, 1) build_kernel(const BuildArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     Engine<BuildOp>::run(A, A.E.W, make_geo(A.E), smem);
@@ -485,8 +583,8 @@ __global__ void __launch_bounds__(kBlockThreads, 1) build_kernel(const BuildArgs
 
 const void* build_kernel_ptr() { return reinterpret_cast<const void*>(&build_kernel); }
 
-size_t build_smem(int C, int own, int part_bytes, int stages, int N, int L) {
-    return ((Engine<BuildOp>::smem_bytes(C, own, part_bytes, stages) + 15) & ~static_cast<size_t>(15)) +
+size_t build_smem(int C, int own, int part_bytes, int stages, int chunk, int N, int L) {
+    return ((Engine<BuildOp>::smem_bytes(C, own, part_bytes, stages, chunk) + 15) & ~static_cast<size_t>(15)) +
            enum_smem_bytes(N, L);
 }
 int build_part_bytes(int M) { return static_cast<int>(sizeof(PartHdr)) + ((M > 0 ? M : 1) * 8 + 15) / 16 * 16; }

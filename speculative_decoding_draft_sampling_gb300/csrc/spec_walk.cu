@@ -92,7 +92,7 @@ struct WalkOp {
     }
     __device__ static StreamPlan plan(const Args& A, const Geo& G, const Job& j) {
         return plan_single(walk_row<E, kTree>(A, j.b, j.row), E::kBytes, slice_x0(G, G.rank),
-                           slice_x1(G, G.rank, A.V));
+                           slice_x1(G, G.rank, A.V), G.chunk);
     }
     __device__ static int consume(const Args& A, const Geo& G, const Pipe& P, uint32_t& seq, bool tma, const Job& j,
                                   Smem& sm, unsigned char* out) {
@@ -170,8 +170,8 @@ const void* walk_kernel_ptr(int ldt, int mode) {
     return mode ? walk_fn<BF16, true>() : walk_fn<BF16, false>();
 }
 
-size_t walk_smem(int C, int own, int part_bytes, int stages) {
-    return Engine<WalkOp<F32, false>>::smem_bytes(C, own, part_bytes, stages);
+size_t walk_smem(int C, int own, int part_bytes, int stages, int chunk) {
+    return Engine<WalkOp<F32, false>>::smem_bytes(C, own, part_bytes, stages, chunk);
 }
 int walk_part_bytes() { return static_cast<int>(sizeof(PartHdr)); }
 

@@ -190,6 +190,30 @@ def test_tree_sample_top1_equals_greedy_walk_on_gpu():
 
 
 # ---------------------------------------------------------------------------
+# accepted-path KV compaction
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype,R,M", [(torch.bfloat16, 1024, 40), (torch.uint8, 37, 23), (torch.float32, 5, 17)])
+def test_kv_compact_matches_oracle(dtype, R, M):
+    """The KV rows of a real tree walk's accepted path, gathered into a
+    cache at per-request positions; byte for byte against the oracle (a
+    16-byte-aligned layout, and layouts that take 4-byte or byte copies)."""
+    t = workloads.make_tree("ddtree", device=DEV, B=8, L=6, V=3000, N=24)
+    g = sv.tree_build(t.q, t.budget)
+    tl = workloads.tree_target_logits(t, g.depth)
+    w = sv.verify_tree(tl, g.token, g.parent, g.num_nodes, 6)
+    P, B, N = 5, 8, 24
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(R)
+    src = torch.randint(0, 250, (P, B, N, R), generator=gen, device=DEV).to(dtype)
+    dst = torch.randint(0, 250, (P, B, M, R), generator=gen, device=DEV).to(dtype)
+    pos = torch.randint(0, M - 7 + 1, (B,), generator=gen, device=DEV, dtype=torch.int32)
+    want = oracle.kv_compact(host(src), host(dst), host(w.path_nodes), host(w.num_accepted), dst_pos=host(pos))
+    sv.kv_compact(src, dst, w.path_nodes, w.num_accepted, dst_pos=pos)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(dst), want)
+
+
+# ---------------------------------------------------------------------------
 # DSpark verify length + ragged chain verify
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("B,Kmax", [(512, 8), (3, 1), (1000, 16), (7, 0)])

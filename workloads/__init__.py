@@ -36,6 +36,8 @@ WORKLOADS = {
     "dspark": (4, "DSpark adaptive ragged verify B=512 Kmax=8 V=128256, bf16, T=1, top-k 50"),
     "dflash_vs": (5, "block-draft chain verify, DFlash shape, every row with its own logit scale "
                      "U[0.5, 6] and offset U[-20, 20], T=1, top-k 50"),
+    "eagle2": (6, "EAGLE-2 dynamic tree B=32 V=151936: 6 expansion steps, 10 children per node, "
+                  "frontier 10, budget 60; conditional draft rows softmax(N(0,3^2)) per path"),
 }
 
 DEFAULTS = {
@@ -46,6 +48,7 @@ DEFAULTS = {
     "dspark": dict(B=512, K=8, V=128256, dtype="bf16", sigma=3.0, T=1.0, top_k=50,
                    a=1.0, b=0.15),
     "dflash_vs": dict(B=256, K=8, V=151936, dtype="f32", sigma=3.0, T=1.0, top_k=50),
+    "eagle2": dict(B=32, V=151936, steps=6, K2=10, Fn=10, N=60, sigma=3.0),
 }
 
 
@@ -242,6 +245,32 @@ def tree_uniforms(tree: TreeInputs, max_depth: int, seed: Optional[int] = None) 
     dev = tree.q_logits.device
     g = _gen(dev, (seed_of(tree.name) + 4093) if seed is None else seed)
     return torch.rand((B, max_depth + 1), generator=g, device=dev).contiguous()
+
+
+def path_key(path) -> int:
+    """A stable 32-bit key of a token path (the draft's conditioning)."""
+    import zlib
+    import numpy as np
+    return zlib.crc32(np.asarray(path, dtype=np.int32).tobytes())
+
+
+def eagle2_rows(paths, V: int, seed: int, device="cpu", sigma: float = 3.0) -> torch.Tensor:
+    """Conditional draft rows for an EAGLE-2 step: paths[b][f] is the token
+    path of request b's frontier slot f (None: no row).  Row (b, f) is
+    softmax(N(0, sigma^2)) drawn from a generator seeded by (seed, b, path),
+    so the same node gets the same row whatever the step or the caller.
+    Returns [B, F, V] fp32 (absent rows zero)."""
+    B = len(paths)
+    F = max((len(p) for p in paths), default=1) or 1
+    out = torch.zeros((B, F, V), dtype=torch.float32, device=device)
+    for b in range(B):
+        for f, path in enumerate(paths[b]):
+            if path is None:
+                continue
+            g = _gen(device, (int(seed) * 1000003 + b * 7919 + path_key(path)) % (1 << 62))
+            z = torch.randn((V,), generator=g, device=device) * sigma
+            out[b, f] = torch.softmax(z, dim=-1)
+    return out
 
 
 def rotate_copies(fn, name: str, n: int, **kw):
