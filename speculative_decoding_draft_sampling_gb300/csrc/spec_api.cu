@@ -34,7 +34,7 @@ int g_tune_c = 0;        // CTAs per cluster (0 = automatic)
 int g_tune_spc = 0;      // slots per CTA (0 = automatic)
 
 constexpr int kDefaultC = 8;
-constexpr int kDefaultSpc = 2;
+constexpr int kDefaultSpc = 1;
 constexpr int kMinSliceElems = 2048;   // a slice holds at least this many elements (small rows use small clusters)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -137,15 +137,26 @@ spec_status make_plan_c(const char* who, const void* fn, int C, int V, int part_
 
 // The automatic cluster size also weighs how many SMs its clusters cover:
 // clusters must fit inside a GPC, so the largest size can leave SMs idle.
+// A smaller size of at least 4 CTAs is taken when it covers more SMs; 2-CTA
+// clusters only when, besides, the batch holds at least two requests per
+// cluster (rows then queue, and throughput, not the latency of one row,
+// sets the time).
 template <class SmemFn>
 spec_status make_plan(const char* who, const void* fn, int V, int part_bytes, int B, SmemFn smem_of, Plan& pl) {
     const int C = cluster_size_for(V);
     spec_status s = make_plan_c(who, fn, C, V, part_bytes, B, smem_of, pl);
-    if (s != SPEC_OK || g_tune_c > 0 || C < 4) return s;
-    Plan half;
-    if (make_plan_c(who, fn, C / 2, V, part_bytes, B, smem_of, half) != SPEC_OK) return s;
-    // compare the SMs each plan can keep busy (all resident clusters)
-    if (half.resident * (C / 2) > pl.resident * C * 21 / 20) pl = half;
+    if (s != SPEC_OK || g_tune_c > 0) return s;
+    int cur = C;
+    for (int c = C / 2; c >= 2; c /= 2) {
+        Plan p;
+        if (make_plan_c(who, fn, c, V, part_bytes, B, smem_of, p) != SPEC_OK) break;
+        const long long cov = static_cast<long long>(p.resident) * c;
+        const long long cov_cur = static_cast<long long>(pl.resident) * cur;
+        if (cov * 20 > cov_cur * 21 && (c >= 4 || B >= 2 * p.resident)) {
+            pl = p;
+            cur = c;
+        }
+    }
     return SPEC_OK;
 }
 

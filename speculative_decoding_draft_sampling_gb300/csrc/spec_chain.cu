@@ -146,13 +146,55 @@ __device__ __forceinline__ void chain_diag_R(const ChainArgs& A, int b, int i, f
 
 // The job that reads row `row` of request b (a bonus row when row == k_b;
 // in a tree walk every row is drawn from).
-__device__ __forceinline__ Job row_job(const ChainArgs& A, int b, int row, int st, uint32_t hint, int depth = 0) {
+// `y`: the row's drafted token when the caller already loaded it
+__device__ __forceinline__ Job row_job(const ChainArgs& A, int b, int row, int st, uint32_t hint, int depth = 0,
+                                       int y = kYUnknown) {
     Job j = make_job(b, row, A.top_k > 0 ? kTk : kSe, st);
     j.aux = (A.tree || row >= chain_k(A, b)) ? 1 : 0;
     j.hint = A.top_k > 0 ? hint : 0u;
     j.depth = depth;
+    j.y = y;
     return j;
 }
+
+// The drafted token of a draft row and its logit and q, loaded by the
+// combiner warp with loads issued where they stand (the values are used only
+// at the accept test, after the selection work).  `yn`: the next row's drafted
+// token, issued now for the next job of this request.
+// When the job does not carry y (a request's first row), y is loaded first
+// and the dependent loads wait until ready() (nothing before the accept test
+// waits on them).
+template <class E>
+struct DraftLoads {
+    int y, yn;
+    float ly, qy;
+    bool pend;
+    __device__ __forceinline__ void load_lq(const ChainArgs& A, int b, int row) {
+        ly = -kInf;
+        qy = 0.f;
+        if (y >= 0 && y < A.V) {
+            const unsigned char* lr = static_cast<const unsigned char*>(chain_lrow<E>(A, b, row));
+            if (E::kBytes == 4) ly = __uint_as_float(ldg_now_u32(lr + 4ll * y));
+            else ly = __uint_as_float(ldg_now_u16(lr + 2ll * y) << 16);
+            qy = __uint_as_float(ldg_now_u32(chain_qrow(A, b, row) + y));
+        }
+    }
+    __device__ __forceinline__ void issue(const ChainArgs& A, const Job& job, int kb) {
+        const int b = job.b, row = job.row;
+        const int* dr = A.draft + static_cast<long long>(b) * A.K;
+        yn = (row + 1 < kb) ? static_cast<int>(ldg_now_u32(dr + row + 1)) : kYUnknown;
+        pend = job.y == kYUnknown;
+        if (pend) {
+            y = static_cast<int>(ldg_now_u32(dr + row));
+        } else {
+            y = job.y;
+            load_lq(A, b, row);
+        }
+    }
+    __device__ __forceinline__ void ready(const ChainArgs& A, const Job& job) {
+        if (pend) load_lq(A, job.b, job.row);
+    }
+};
 
 // A row's draw x is known: the chain commits it; the tree walk looks it up
 // among the node's children and goes on there, or commits it as the bonus.
@@ -245,24 +287,6 @@ __device__ __forceinline__ int find_slice_w(int S, dfloat v, dfloat t, dfloat& b
 }
 __device__ __forceinline__ dfloat df_of(float2 v) { return dfloat{v.x, v.y}; }
 
-// the drafted token's logit and q, from the slice that holds it
-__device__ __forceinline__ void slice_y(const unsigned char* parts, int pb, int C, float& ly, float& qy) {
-    const int l = threadIdx.x & 31;
-    uint32_t has = 0;
-    float a = 0.f, q = 0.f;
-    if (l < C) {
-        const PartHdr* h = part_at(parts, pb, l);
-        has = h->hasy;
-        a = h->ly;
-        q = h->qy;
-    }
-    const uint32_t bal = __ballot_sync(0xffffffffu, has != 0);
-    const int src = bal ? __ffs(bal) - 1 : 0;
-    ly = __shfl_sync(0xffffffffu, a, src);
-    qy = __shfl_sync(0xffffffffu, q, src);
-    if (!bal) { ly = -kInf; qy = 0.f; }
-}
-
 // ---------------------------------------------------------------------------
 // combine of a top-k row.  Every slice reports its keys at or above its own
 // k-th value, sorted descending (composite keys: value, then lower id
@@ -311,7 +335,8 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
                                                               draw_uidx(A, job)]));
     const float ur = bonus ? 0.f : __uint_as_float(ldg_now_u32(&A.uniforms[static_cast<long long>(b) *
                                                                                 ((A.tree ? A.L : A.K) + 1) + row]));
-    const int yd = bonus ? -1 : static_cast<int>(ldg_now_u32(&A.draft[static_cast<long long>(b) * A.K + row]));
+    DraftLoads<E> dl;
+    if (!bonus) dl.issue(A, job, chain_k(A, b));
     // the slices' headers (value filters: the low key halves are zero)
     const uint32_t hb = smem_u32(parts) + static_cast<uint32_t>(l * pb);
     uint32_t flags = 0, vkey = 0, thk = 0;
@@ -337,14 +362,18 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
     // the prefix of each list at or above the largest slice filter holds
     // every member of S in that slice
     int mr = 0;
-    if (l < C && cnt > 0) {
-        const uint32_t lr = hb + static_cast<uint32_t>(sizeof(PartHdr));
-        int lo = 0, hi = cnt;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (hkey(lds_u64(lr + 8u * mid)) >= th) lo = mid + 1; else hi = mid;
+    {
+        // keys of list l at or above th: a power-of-two search over at most
+        // 512 keys (every lane runs it; lanes >= C count none)
+        const int cl = l < C ? cnt : 0;
+        const uint32_t lr = smem_u32(parts) + static_cast<uint32_t>((l < C ? l : 0) * pb + sizeof(PartHdr));
+#pragma unroll
+        for (int s = 256; s > 0; s >>= 1) {
+            const int np = mr + s;
+            const uint32_t hv = hkey(lds_u64(lr + 8u * static_cast<uint32_t>(max(min(np, cl), 1) - 1)));
+            mr = (np <= cl && hv >= th) ? np : mr;
         }
-        mr = lo;
+        if (cl >= 512 && mr == 511 && hkey(lds_u64(lr + 8u * 511u)) >= th) mr = 512;
     }
     int n;
     const int off = warp_exscan_i(mr, n);
@@ -387,33 +416,55 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
             o[q] = __shfl_sync(0xffffffffu, off, q);
             mq[q] = __shfl_sync(0xffffffffu, mr, q);
         }
+        // every load unconditional (indices clamped into a list that exists),
+        // so that each step's sixteen loads issue back to back
         uint64_t key[kRegKeys];
 #pragma unroll
         for (int j = 0; j < kRegKeys; ++j) {
-            const int f = l + 32 * j;
+            const int f = min(l + 32 * j, n - 1);
             const int r = (f >= o[1] ? 1 : 0) + (f >= o[2] ? 1 : 0) + (f >= o[3] ? 1 : 0);
             const int base = r == 0 ? 0 : (r == 1 ? o[1] : (r == 2 ? o[2] : o[3]));
-            key[j] = f < n ? lds_u64(kbase + static_cast<uint32_t>(r * pb + (f - base) * 8)) : 0ull;
+            const uint64_t v = lds_u64(kbase + static_cast<uint32_t>(r * pb + (f - base) * 8));
+            key[j] = l + 32 * j < n ? v : 0ull;
         }
         int pos[4][kRegKeys];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
             for (int j = 0; j < kRegKeys; ++j) pos[q][j] = 0;
+        uint32_t lbase[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) lbase[q] = kbase + static_cast<uint32_t>((q < C ? q : 0) * pb);
         for (int s = s0; s > 0; s >>= 1) {
+            uint64_t v[4][kRegKeys];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int j = 0; j < kRegKeys; ++j) {
+                    const int idx = max(min(pos[q][j] + s, mq[q]), 1) - 1;
+                    v[q][j] = lds_u64(lbase[q] + static_cast<uint32_t>(idx * 8));
+                }
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
                 for (int j = 0; j < kRegKeys; ++j) {
                     const int np = pos[q][j] + s;
-                    if (np <= mq[q] && lds_u64(kbase + static_cast<uint32_t>(q * pb + (np - 1) * 8)) > key[j])
-                        pos[q][j] = np;
+                    pos[q][j] = (np <= mq[q] && v[q][j] > key[j]) ? np : pos[q][j];
                 }
         }
+        // the one key of rank k - 1: its lane and slot by ballots
+        int jt = -1;
 #pragma unroll
         for (int j = 0; j < kRegKeys; ++j)
-            if (l + 32 * j < n && pos[0][j] + pos[1][j] + pos[2][j] + pos[3][j] == k - 1) tauc = key[j];
-        tauc = warp_max_u64(tauc);   // the one key of rank k - 1
+            if (l + 32 * j < n && pos[0][j] + pos[1][j] + pos[2][j] + pos[3][j] == k - 1) jt = j;
+        const uint32_t who = __ballot_sync(0xffffffffu, jt >= 0);
+        const int src = who ? __ffs(who) - 1 : 0;
+        uint64_t mine = 0;
+#pragma unroll
+        for (int j = 0; j < kRegKeys; ++j) mine = jt == j ? key[j] : mine;
+        const uint32_t tlo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(mine), src);
+        const uint32_t thi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(mine >> 32), src);
+        tauc = (static_cast<uint64_t>(thi) << 32) | tlo;
         tau_key = hkey(tauc);
 #pragma unroll
         for (int j = 0; j < kRegKeys; ++j) {
@@ -484,11 +535,11 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
     auto prob = [&](float e) { return static_cast<float>(static_cast<double>(e) / df_to_d(Z)); };   // diagnostics
     float ey = 0.f, qy = 0.f;
     if (!bonus) {
-        const int y = yd;
-        float ly;
-        slice_y(parts, pb, C, ly, qy);
+        dl.ready(A, job);
+        const int y = dl.y;
+        const float ly = dl.ly;
+        qy = dl.qy;
         ey = (y >= 0 && y < A.V && fkey(ly) >= tau_key) ? ex2((ly - m) * c2) : 0.f;
-        if (y < 0 || y >= A.V) qy = 0.f;
         const bool acc = chain_accept_z(A, y, ey, qy, Z, ur, st);
 #ifdef SPEC_TRACE
         SPEC_TRACE_T(tc3);
@@ -499,7 +550,7 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
 #endif
         if (acc) {
             if (A.diag) chain_diag(A, b, row, prob(ey), qy, Z.hi, 0.f);
-            return row_job(A, b, row + 1, st, hint);
+            return row_job(A, b, row + 1, st, hint, 0, dl.yn);
         }
     }
     // a draw on S (the residual at a rejection, p at the bonus row): S sorted
@@ -570,6 +621,7 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
 // ---------------------------------------------------------------------------
 // combine of a sum-exp row (untruncated, or masked at a known threshold)
 // ---------------------------------------------------------------------------
+template <class E>
 __device__ __noinline__ Job combine_se(const ChainArgs& A, const Geo& G, const Job job, const unsigned char* parts,
                                        ChainSmem& sm) {
     const int l = threadIdx.x & 31;
@@ -579,6 +631,8 @@ __device__ __noinline__ Job combine_se(const ChainArgs& A, const Geo& G, const J
     const uint32_t mask = job.hint;
     int st = job.st;
     const float c2 = A.c2;
+    DraftLoads<E> dl;
+    if (!bonus) dl.issue(A, job, chain_k(A, b));
     uint32_t flags = 0;
     float vm = -kInf;
     dfloat sv = df_make(0.f);
@@ -596,14 +650,13 @@ __device__ __noinline__ Job combine_se(const ChainArgs& A, const Geo& G, const J
     const dfloat Z = warp_sum_df(zv);
     const float uk = chain_u(A, b, draw_uidx(A, job));
     if (!bonus) {
-        const int y = A.draft[static_cast<long long>(b) * A.K + row];
-        float ly, qy;
-        slice_y(parts, pb, C, ly, qy);
+        dl.ready(A, job);
+        const int y = dl.y;
+        const float ly = dl.ly, qy = dl.qy;
         const float ey = (y >= 0 && y < A.V && fkey(ly) >= mask) ? ex2((ly - m) * c2) : 0.f;
-        if (y < 0 || y >= A.V) qy = 0.f;
         const bool acc = chain_accept_z(A, y, ey, qy, Z, chain_u(A, b, row), st);
         chain_diag(A, b, row, static_cast<float>(static_cast<double>(ey) / df_to_d(Z)), qy, Z.hi, 0.f);
-        if (acc) return row_job(A, b, row + 1, st, sm.last_hint);
+        if (acc) return row_job(A, b, row + 1, st, sm.last_hint, 0, dl.yn);
         // the residual pass: every slice's [p - q]_+ mass with this row's m and Z
         Job j = make_job(b, row, kResid, st);
         j.hint = mask;
@@ -836,16 +889,7 @@ struct ChainOp {
         }
         int nkeys = 0;
         if (j.kind == kTk || j.kind == kSe) {
-            // the drafted token: the thread 0 of the slice that holds it loads
-            // its logit and q at once (the loads overlap the stream)
-            int y = -1;
-            if (j.aux == 0) y = A.draft[static_cast<long long>(b) * A.K + row];
-            const bool owns = y >= x0 && y < x1;
-            float ly = -kInf, qy = 0.f;
-            if (owns && threadIdx.x == 0) {
-                ly = E::load(chain_lrow<E>(A, b, row), y);
-                qy = __ldg(chain_qrow(A, b, row) + y);
-            }
+            // (the drafted token's logit and q are the combiner's own loads)
             if (kTopk && j.kind == kTk) {
                 TopkHistFn<E, true> fn;
                 fn.init(&sm.tk, A.top_k, j.hint, seq + 1u);   // every consumer holds the same seq
@@ -891,7 +935,6 @@ struct ChainOp {
                     ph->cnt = n;
                     ph->kth = F;
                     ph->vmax = vm;
-                    if (owns) { ph->ly = ly; ph->qy = qy; ph->hasy = 1; }
                 }
             } else {
                 // sum-exp (masked at the job's threshold when it carries one)
@@ -921,8 +964,7 @@ struct ChainOp {
                         ph->flags = bad ? kPfBad : 0u;
                         ph->vmax = bad ? vx : ms;
                         ph->sum = make_float2(tot.hi, tot.lo);
-                        if (owns) { ph->ly = ly; ph->qy = qy; ph->hasy = 1; }
-                    }
+                        }
                     return true;
                 };
                 bool ok;
@@ -1002,7 +1044,7 @@ struct ChainOp {
     __device__ static Job combine(const Args& A, const Geo& G, const Job& j, const unsigned char* parts, Smem& sm) {
         switch (j.kind) {
             case kTk: return combine_topk<E>(A, G, j, parts, sm);
-            case kSe: return combine_se(A, G, j, parts, sm);
+            case kSe: return combine_se<E>(A, G, j, parts, sm);
             case kResid: return combine_resid(A, G, j, parts);
             case kRescan: return combine_rescan<E>(A, j, parts, G.part_bytes, sm.last_hint);
             default: return combine_radix(A, G, j, parts);

@@ -225,6 +225,11 @@ __device__ __forceinline__ uint32_t ldg_now_u32(const void* p) {
     asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
     return v;
 }
+__device__ __forceinline__ uint32_t ldg_now_u16(const void* p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
 __device__ __forceinline__ void st_cluster_v4(uint32_t a, const uint4& v) {
     asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};"
                  :: "r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");

@@ -112,17 +112,19 @@ struct Job {
     int aux, aux2;     // per kernel
     float f[4];        // per kernel
     int depth;         // tree walks: the depth of the node the job reads
-    int pad[3];
+    int y;             // chain: the row's drafted token when known (kYUnknown: not loaded yet)
+    int pad[2];
 };
 static_assert(sizeof(Job) == 64, "Job is 64 bytes");
 constexpr int kJobStop = -1;
 constexpr int kJobDone = -2;       // returned by a combine: the request finished
+constexpr int kYUnknown = -0x7fffffff;
 
 __device__ __forceinline__ Job make_job(int b, int row, int kind, int st) {
     Job j;
     j.b = b; j.row = row; j.kind = kind; j.target = -1; j.st = st; j.hint = 0; j.aux = 0; j.aux2 = 0;
     j.f[0] = j.f[1] = j.f[2] = j.f[3] = 0.f;
-    j.depth = 0; j.pad[0] = j.pad[1] = j.pad[2] = 0;
+    j.depth = 0; j.y = kYUnknown; j.pad[0] = j.pad[1] = 0;
     return j;
 }
 __device__ __forceinline__ Job job_done() { return make_job(kJobDone, 0, 0, 0); }
@@ -244,16 +246,23 @@ __device__ __forceinline__ bool mbar_try_cluster(const uint64_t* bar, uint32_t p
 
 // Wait for one mbarrier phase, up to kMbarLimitNs; gives up early when the
 // CTA aborted or another CTA raised the workspace error.  false: gave up.
+// The abort flag, the error word and the clock are looked at only every 64
+// tries: a global load of the error word after every try would delay the
+// next try by a memory round trip.
 template <bool kCluster = false>
 __device__ __forceinline__ bool wait_phase(const uint64_t* bar, uint32_t parity, volatile int* abort,
                                            const Ctrl* ctrl) {
     if (kCluster ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer_ns();
-    for (;;) {
+    unsigned long long t0 = 0;
+    for (uint32_t it = 1;; ++it) {
         if (kCluster ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
-        if (*abort) return false;
-        if (ld_relaxed(&ctrl->error) != 0u) return false;
-        if (globaltimer_ns() - t0 > kMbarLimitNs) return false;
+        if ((it & 63u) == 0u) {
+            if (*abort) return false;
+            if (ld_relaxed(&ctrl->error) != 0u) return false;
+            const unsigned long long now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > kMbarLimitNs) return false;
+        }
     }
 }
 
@@ -271,7 +280,7 @@ __device__ __forceinline__ bool poll_until(T test, volatile int* abort, const Ct
             if (t0 == 0) t0 = now;
             else if (now - t0 > kMbarLimitNs) return false;
         }
-        if (it >= 8u) nanosleep_ns(it >= 64u ? 256 : 64);
+        if (it >= 16u) nanosleep_ns(it >= 256u ? 128 : 32);
     }
 }
 __device__ __forceinline__ void raise_abort(volatile int* abort, Ctrl* ctrl) {
@@ -920,7 +929,7 @@ struct Engine {
                 job.b = vj->b; job.row = vj->row; job.kind = vj->kind; job.target = vj->target;
                 job.st = vj->st; job.hint = vj->hint; job.aux = vj->aux; job.aux2 = vj->aux2;
                 job.f[0] = vj->f[0]; job.f[1] = vj->f[1]; job.f[2] = vj->f[2]; job.f[3] = vj->f[3];
-                job.depth = vj->depth; job.pad[0] = job.pad[1] = job.pad[2] = 0;
+                job.depth = vj->depth; job.y = vj->y; job.pad[0] = job.pad[1] = 0;
             }
             if (job.b < 0) ++retired;
             // hand the job to the consumers

@@ -27,10 +27,11 @@ namespace spec {
 
 struct Ent {                 // a frontier entry or an emitted node
     double Q;
+    double pq;               // the parent's Q (a sibling's Q is pq times its probability)
     unsigned long long ph, pl;   // rank path, one byte per depth, depth 1 in the top byte
     int depth, parent, rank, pad;
 };
-static_assert(sizeof(Ent) == 40, "Ent is 40 bytes");
+static_assert(sizeof(Ent) == 48, "Ent is 48 bytes");
 
 struct EnumHdr {
     int count, npend, want, avail;
@@ -47,8 +48,25 @@ struct BuildSmem {
     int hist[64];
     uint32_t scratch[kWarps + 2];
     EnumHdr eh;              // combiner
+    uint32_t last_hint;      // combiner: value filter hint for the next row (0: none)
     alignas(16) uint64_t list[kBuildList];   // combiner: gathered keys
 };
+
+// Filter hints for top-M rows of probabilities: half of the last row's M-th
+// largest value (rows of one drafter differ little in it; a hint above a
+// row's M-th value costs a second pass over that row).  Kept across calls in
+// the workspace, tagged with V and M.
+constexpr uint32_t kPersistTagTopm = 0x5e1ec7eeu;
+__device__ __forceinline__ uint32_t topm_hint(float vM) { return vM > 0.f ? fkey(0.5f * vM) : 0u; }
+__device__ __forceinline__ uint32_t topm_hint_load(const Ctrl* ctrl, int V, int M) {
+    const uint4 ps = __ldcg(reinterpret_cast<const uint4*>(ctrl->persist + 4));
+    return (ps.x == kPersistTagTopm && ps.z == static_cast<uint32_t>(V) && ps.w == static_cast<uint32_t>(M)) ? ps.y
+                                                                                                           : 0u;
+}
+__device__ __forceinline__ void topm_hint_store(Ctrl* ctrl, uint32_t h, int V, int M) {
+    __stcg(reinterpret_cast<uint4*>(ctrl->persist + 4),
+           make_uint4(kPersistTagTopm, h, static_cast<uint32_t>(V), static_cast<uint32_t>(M)));
+}
 
 // per-request workspace: [EnumHdr][lists L*M (tok, prob bits)][nodes N][pending 2N+2]
 __host__ __device__ inline size_t build_lists_off() { return 128; }
@@ -91,7 +109,32 @@ struct EnumView {
     float* lprob;
     Ent* nodes;
     Ent* pend;
+    uint32_t a_lprob, a_nodes, a_pend;   // the same, as shared-window addresses
 };
+
+// Ent records through shared-window addresses (explicit shared loads and
+// stores: the enumeration's records are reached through struct members,
+// which would otherwise be generic accesses)
+__device__ __forceinline__ uint64_t ldsv_u64(uint32_t a) {
+    uint64_t v;
+    asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void stsv_u64(uint32_t a, uint64_t v) {
+    asm volatile("st.shared.u64 [%0], %1;" :: "r"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ Ent ld_ent(uint32_t a) {
+    Ent e;
+    uint64_t* w = reinterpret_cast<uint64_t*>(&e);
+#pragma unroll
+    for (int i = 0; i < static_cast<int>(sizeof(Ent) / 8); ++i) w[i] = ldsv_u64(a + 8u * i);
+    return e;
+}
+__device__ __forceinline__ void st_ent(uint32_t a, const Ent& e) {
+    const uint64_t* w = reinterpret_cast<const uint64_t*>(&e);
+#pragma unroll
+    for (int i = 0; i < static_cast<int>(sizeof(Ent) / 8); ++i) stsv_u64(a + 8u * i, w[i]);
+}
 __device__ __forceinline__ EnumView enum_view(unsigned char* base, int N, int L) {
     EnumView v;
     const int LM = L * (N - 1);
@@ -99,6 +142,9 @@ __device__ __forceinline__ EnumView enum_view(unsigned char* base, int N, int L)
     v.lprob = reinterpret_cast<float*>(base + static_cast<size_t>(LM) * 4);
     v.nodes = reinterpret_cast<Ent*>(base + ((static_cast<size_t>(LM) * 8 + 15) & ~static_cast<size_t>(15)));
     v.pend = v.nodes + N;
+    v.a_lprob = smem_u32(v.lprob);
+    v.a_nodes = smem_u32(v.nodes);
+    v.a_pend = smem_u32(v.pend);
     return v;
 }
 
@@ -142,19 +188,54 @@ __device__ void build_finalize(const BuildArgs& A, const EnumView& ev, int b, in
 }
 
 // warp-wide pop of the best frontier entry: its index in every lane
-__device__ __forceinline__ int best_pending_w(const Ent* pend, int np) {
+// The frontier's best entry (ent_before order) on the combiner warp, in two
+// parts: each lane's best over its slots (l, l + 32, ...), kept in registers
+// between pops and recomputed only by lanes whose slots changed; then the
+// warp reduction on an order-preserving 64-bit key of Q, and -- only among
+// exact ties -- on depth and on the rank path.
+struct LaneBest {
+    int j, d;
+    unsigned long long q, ph, pl;
+};
+__device__ __forceinline__ unsigned long long q_order_key(unsigned long long qb) {
+    if ((qb << 1) == 0ull) qb = 0ull;                              // -0 as +0
+    return (qb >> 63) ? ~qb : (qb | 0x8000000000000000ull);
+}
+__device__ __forceinline__ void lane_best(uint32_t a_pend, int np, LaneBest& b) {
     const int l = threadIdx.x & 31;
-    int best = -1;
-    for (int j = l; j < np; j += 32)
-        if (best < 0 || ent_before(pend[j], pend[best])) best = j;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const int other = __shfl_xor_sync(0xffffffffu, best, o);
-        if (other >= 0 && (best < 0 || ent_before(pend[other], pend[best]) ||
-                           (!ent_before(pend[best], pend[other]) && other < best)))
-            best = other;
+    b.j = -1; b.d = 0; b.q = 0; b.ph = 0; b.pl = 0;
+    for (int j = l; j < np; j += 32) {
+        const uint32_t a = a_pend + static_cast<uint32_t>(j * sizeof(Ent));
+        const unsigned long long q = q_order_key(ldsv_u64(a + offsetof(Ent, Q)));
+        const int d = static_cast<int>(static_cast<uint32_t>(ldsv_u64(a + offsetof(Ent, depth))));
+        const unsigned long long ph = ldsv_u64(a + offsetof(Ent, ph)), pl = ldsv_u64(a + offsetof(Ent, pl));
+        const bool take = b.j < 0 || q > b.q ||
+                          (q == b.q && (d < b.d || (d == b.d && (ph < b.ph || (ph == b.ph && pl < b.pl)))));
+        if (take) { b.j = j; b.q = q; b.d = d; b.ph = ph; b.pl = pl; }
     }
-    return best;
+}
+__device__ __forceinline__ int warp_best(const LaneBest& b) {
+    const int l = threadIdx.x & 31;
+    uint32_t cand = __ballot_sync(0xffffffffu, b.j >= 0);
+    if (!cand) return -1;
+    auto keep_max = [&](uint32_t v) {
+        const bool in = (cand >> l) & 1u;
+        const uint32_t m = __reduce_max_sync(0xffffffffu, in ? v : 0u);
+        cand = __ballot_sync(0xffffffffu, in && v == m);
+    };
+    auto keep_min = [&](uint32_t v) {
+        const bool in = (cand >> l) & 1u;
+        const uint32_t m = __reduce_min_sync(0xffffffffu, in ? v : 0xffffffffu);
+        cand = __ballot_sync(0xffffffffu, in && v == m);
+    };
+    keep_max(static_cast<uint32_t>(b.q >> 32));
+    if (__popc(cand) > 1) keep_max(static_cast<uint32_t>(b.q));
+    if (__popc(cand) > 1) keep_min(static_cast<uint32_t>(b.d));
+    if (__popc(cand) > 1) keep_min(static_cast<uint32_t>(b.ph >> 32));
+    if (__popc(cand) > 1) keep_min(static_cast<uint32_t>(b.ph));
+    if (__popc(cand) > 1) keep_min(static_cast<uint32_t>(b.pl >> 32));
+    if (__popc(cand) > 1) keep_min(static_cast<uint32_t>(b.pl));
+    return __shfl_sync(0xffffffffu, b.j, __ffs(cand) - 1);
 }
 
 // The best-first enumeration from the saved state in `eh` / `ev` (combiner
@@ -164,49 +245,111 @@ __device__ int enumerate_w(const BuildArgs& A, EnumHdr& eh, const EnumView& ev) 
     const int l = threadIdx.x & 31;
     const int N = A.N, M = A.M, L = A.L;
     int count = eh.count, np = eh.npend, want = eh.want;
+    const int avail = eh.avail;
+    const int lenl = l <= L ? eh.len[l] : 0;          // lane d: depth d's list length
     int need = 0;
-    while (count < N) {
-        if (want >= 0) {
-            const int dd = ev.nodes[want].depth + 1;
-            if (dd <= L) {
-                if (dd > eh.avail) { need = dd; break; }
-                if (eh.len[dd] > 0) {
-                    if (l == 0) {
-                        Ent c = ev.nodes[want];
-                        c.depth = dd; c.parent = want; c.rank = 0;
-                        path_set(c, dd, 0);
-                        c.Q = ev.nodes[want].Q * static_cast<double>(ev.lprob[(dd - 1) * M + 0]);
-                        ev.pend[np] = c;
-                    }
-                    ++np;
-                    __syncwarp();
+    constexpr uint32_t kE = static_cast<uint32_t>(sizeof(Ent));
+    // scalar copies: the explicit shared accesses below clobber memory, and a
+    // view reached through a reference would be reloaded after every one
+    const uint32_t a_lprob = ev.a_lprob, a_nodes = ev.a_nodes, a_pend = ev.a_pend;
+    auto lprob_at = [a_lprob](int i) { return __uint_as_float(lds_u32(a_lprob + 4u * static_cast<uint32_t>(i))); };
+#ifdef SPEC_TRACE
+    long long t_best = 0;
+    const long long t_all = clock64();
+#endif
+    // a node of an earlier call that still wants its first child
+    if (want >= 0 && count < N) {
+        const Ent w = ld_ent(a_nodes + kE * want);
+        const int dd = w.depth + 1;
+        if (dd <= L) {
+            if (dd > avail) {
+                need = dd;
+            } else if (__shfl_sync(0xffffffffu, lenl, dd) > 0) {
+                const double q0 = static_cast<double>(lprob_at((dd - 1) * M));
+                if (l == 0) {
+                    Ent c = w;
+                    c.depth = dd; c.parent = want; c.rank = 0;
+                    path_set(c, dd, 0);
+                    c.Q = w.Q * q0;
+                    c.pq = w.Q;
+                    st_ent(a_pend + kE * np, c);
                 }
+                ++np;
             }
-            want = -1;
         }
-        if (np == 0) break;
-        const int best = best_pending_w(ev.pend, np);
-        const Ent c = ev.pend[best];
+        if (!need) want = -1;
+    }
+    LaneBest lb;
+    lb.j = -1;
+    bool dirty = true;
+    while (!need && count < N && np > 0) {
         __syncwarp();
+#ifdef SPEC_TRACE
+        const long long tq0 = clock64();
+#endif
+        if (dirty) lane_best(a_pend, np, lb);
+        const int best = warp_best(lb);
+#ifdef SPEC_TRACE
+        t_best += clock64() - tq0;
+#endif
+        // the popped entry, the last entry (moves into its slot), and the
+        // probabilities of the popped entry's next sibling and first child:
+        // independent loads, independent products
+        const Ent c = ld_ent(a_pend + kE * best);
+        const Ent last = ld_ent(a_pend + kE * (np - 1));
+        const bool sib = c.rank + 1 < __shfl_sync(0xffffffffu, lenl, c.depth);
+        const int dd = c.depth + 1;
+        const bool deeper = dd <= L;
+        const bool have_list = deeper && dd <= avail && __shfl_sync(0xffffffffu, lenl, deeper ? dd : 0) > 0;
+        const float qs = lprob_at((c.depth - 1) * M + (sib ? c.rank + 1 : c.rank));
+        const float q0 = lprob_at(have_list ? (dd - 1) * M : 0);
+        const double sQ = c.pq * static_cast<double>(qs);
+        const double cQ = c.Q * static_cast<double>(q0);
+        __syncwarp();
+        const int nid = count++;
+        const int removed = np - 1;
         if (l == 0) {
-            ev.pend[best] = ev.pend[np - 1];
-            ev.nodes[count] = c;
+            st_ent(a_pend + kE * best, last);
+            st_ent(a_nodes + kE * nid, c);
         }
         --np;
-        const int nid = count++;
-        if (c.rank + 1 < eh.len[c.depth]) {
+        int slot_s = -1, slot_c = -1;
+        if (sib) {
+            // next sibling: same parent, next rank of the same depth list
             if (l == 0) {
                 Ent s2 = c;
                 s2.rank = c.rank + 1;
                 path_set(s2, c.depth, c.rank + 1);
-                s2.Q = ev.nodes[c.parent].Q * static_cast<double>(ev.lprob[(c.depth - 1) * M + c.rank + 1]);
-                ev.pend[np] = s2;
+                s2.Q = sQ;
+                st_ent(a_pend + kE * np, s2);
             }
-            ++np;
+            slot_s = np++;
         }
-        __syncwarp();
-        want = nid;
+        if (deeper && count < N) {
+            if (dd > avail) {
+                // the child needs a depth not read yet: stop, and resume here
+                want = nid;
+                need = dd;
+            } else if (have_list) {
+                if (l == 0) {
+                    Ent ch = c;
+                    ch.depth = dd; ch.parent = nid; ch.rank = 0;
+                    path_set(ch, dd, 0);
+                    ch.Q = cQ;
+                    ch.pq = c.Q;
+                    st_ent(a_pend + kE * np, ch);
+                }
+                slot_c = np++;
+            }
+        }
+        // lanes whose slots changed recompute their best
+        dirty = l == (best & 31) || l == (removed & 31) || (slot_s >= 0 && l == (slot_s & 31)) ||
+                (slot_c >= 0 && l == (slot_c & 31));
     }
+#ifdef SPEC_TRACE
+    if (l == 0) SPEC_TRACE_EV(16, static_cast<int>(t_best), static_cast<int>(clock64() - t_all), np);
+#endif
+    __syncwarp();
     if (l == 0) { eh.count = count; eh.npend = np; eh.want = want; }
     __syncwarp();
     return need;
@@ -220,10 +363,11 @@ __device__ void enum_save(const BuildArgs& A, int b, const EnumHdr& eh, const En
     unsigned char* ex = A.E.W.extra + static_cast<size_t>(b) * A.E.W.extra_stride;
     int* gl = reinterpret_cast<int*>(ex + build_lists_off());
     const int nc = eh.count, np = eh.npend;
-    for (int i = l; i < nc * 5; i += 32)
+    constexpr int kW = static_cast<int>(sizeof(Ent) / 8);
+    for (int i = l; i < nc * kW; i += 32)
         __stcg(reinterpret_cast<unsigned long long*>(ex + build_nodes_off(N, L)) + i,
                reinterpret_cast<const unsigned long long*>(ev.nodes)[i]);
-    for (int i = l; i < np * 5; i += 32)
+    for (int i = l; i < np * kW; i += 32)
         __stcg(reinterpret_cast<unsigned long long*>(ex + build_pend_off(N, L)) + i,
                reinterpret_cast<const unsigned long long*>(ev.pend)[i]);
     for (int i = first_list * M + l; i < eh.avail * M; i += 32) {
@@ -243,10 +387,11 @@ __device__ void enum_load(const BuildArgs& A, int b, EnumHdr& eh, const EnumView
         reinterpret_cast<int*>(&eh)[i] = __ldcg(reinterpret_cast<const int*>(ex) + i);
     __syncwarp();
     const int nc = eh.count, np = eh.npend;
-    for (int i = l; i < nc * 5; i += 32)
+    constexpr int kW = static_cast<int>(sizeof(Ent) / 8);
+    for (int i = l; i < nc * kW; i += 32)
         reinterpret_cast<unsigned long long*>(ev.nodes)[i] =
             __ldcg(reinterpret_cast<const unsigned long long*>(ex + build_nodes_off(N, L)) + i);
-    for (int i = l; i < np * 5; i += 32)
+    for (int i = l; i < np * kW; i += 32)
         reinterpret_cast<unsigned long long*>(ev.pend)[i] =
             __ldcg(reinterpret_cast<const unsigned long long*>(ex + build_pend_off(N, L)) + i);
     for (int i = l; i < eh.avail * M; i += 32) {
@@ -265,6 +410,7 @@ __device__ void enum_load(const BuildArgs& A, int b, EnumHdr& eh, const EnumView
 // list[0..return); 0 for a bad row.
 __device__ int merge_topm_w(const unsigned char* parts, int pb, int C, int M, uint32_t flags, uint64_t theta, int cnt,
                             const float* qrow, int V, uint64_t* list);
+__device__ int merge_sorted_topm_w(const unsigned char* parts, int pb, int C, int M, int cnt, int* tok, float* prob);
 
 struct BuildOp {
     using Args = BuildArgs;
@@ -272,8 +418,11 @@ struct BuildOp {
 
     __device__ static int batch(const Args& A) { return A.B; }
     __device__ static bool tma(const Args& A) { return A.tma_q != 0; }
-    __device__ static void init_smem(const Args&, const Geo&, Smem& sm) {
-        if (threadIdx.x == 0) topk_smem_init(sm.tk);
+    __device__ static void init_smem(const Args& A, const Geo&, Smem& sm) {
+        if (threadIdx.x == 0) {
+            topk_smem_init(sm.tk);
+            sm.last_hint = topm_hint_load(A.E.W.ctrl, A.V, A.M);
+        }
     }
     // the combiner's enumeration scratch sits after the ring
     __device__ static EnumView view(const Args& A, const Geo& G) {
@@ -298,8 +447,10 @@ struct BuildOp {
             build_finalize(A, ev, b, 1, 0);
             return job_done();
         }
-        enum_save(A, b, eh, ev, 0);
-        return make_job(b, 0, 0, 0);   // depth 1's row
+        if (G.own > 1) enum_save(A, b, eh, ev, 0);
+        Job j = make_job(b, 0, 0, 0);   // depth 1's row
+        j.hint = sm.last_hint;
+        return j;
     }
     __device__ static StreamPlan plan(const Args& A, const Geo& G, const Job& j) {
         const float* qrow = A.q + static_cast<long long>(j.b) * A.q_bs + static_cast<long long>(j.row) * A.q_rs;
@@ -312,7 +463,7 @@ struct BuildOp {
         uint64_t* pk = reinterpret_cast<uint64_t*>(ph + 1);
         const int M = A.M;
         TopkHistFn<F32, false> fn;
-        fn.init(&sm.tk, M, 0u, seq + 1u);   // every consumer holds the same seq
+        fn.init(&sm.tk, M, j.hint, seq + 1u);   // every consumer holds the same seq
         if (!consume_row<F32>(P, seq, plan(A, G, j), tma, slice_x0(G, G.rank), fn)) return -1;
         uint64_t F;
         uint32_t oflow, bad;
@@ -360,9 +511,18 @@ struct BuildOp {
         }
         if (bad || oflow) n = 0;
         csync();
-        for (int i = threadIdx.x; i < n; i += kThreads) pk[i] = list[i];
+        // the keys sorted descending (composite keys are unique: a key's
+        // position is the number of greater keys), so that the combine merges
+        // sorted lists
+        for (int i = threadIdx.x; i < n; i += kThreads) {
+            const uint64_t x = list[i];
+            int r = 0;
+#pragma unroll 8
+            for (int j = 0; j < n; ++j) r += list[j] > x ? 1 : 0;
+            pk[r] = x;
+        }
         if (threadIdx.x == 0) {
-            ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u);
+            ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u) | (j.hint ? kPfHinted : 0u);
             ph->cnt = n;
             ph->kth = F;
         }
@@ -406,13 +566,16 @@ struct BuildOp {
     }
 
     __device__ static Job combine(const Args& A, const Geo& G, const Job& j, const unsigned char* parts, Smem& sm) {
+        SPEC_TRACE_T(tb0);
         const int l = threadIdx.x & 31;
         const int M = A.M, C = G.C, pb = G.part_bytes;
         const int b = j.b;
         const int d = j.row + 1;
         const EnumView ev = view(A, G);
         EnumHdr& eh = sm.eh;
-        enum_load(A, b, eh, ev);
+        // a CTA that leads one slot keeps its request's enumeration in shared
+        // memory between jobs; with several slots it is saved in the workspace
+        if (G.own > 1) enum_load(A, b, eh, ev);
         uint32_t flags = 0;
         uint64_t theta = 0;
         int cnt = 0;
@@ -424,15 +587,32 @@ struct BuildOp {
         theta = warp_max_u64(theta);
         const float* qrow = A.q + static_cast<long long>(b) * A.q_bs + static_cast<long long>(d - 1) * A.q_rs;
         uint64_t* list = sm.list;
-        const int n = merge_topm_w(parts, pb, C, M, flags, theta, cnt, qrow, A.V, list);
-        // the depth list in rank order (value desc, index asc)
-        for (int i = l; i < n; i += 32) {
-            const uint64_t key = list[i];
-            int r = 0;
-            for (int q = 0; q < n; ++q) r += list[q] > key;
-            const int o = (d - 1) * M + r;
-            ev.ltok[o] = ckey_idx(key);
-            ev.lprob[o] = ckey_val(key);
+        int n;
+        if (!(flags & (kPfBad | kPfOverflow))) {
+            // the depth list in rank order (value desc, index asc) from the
+            // slices' sorted lists
+            n = merge_sorted_topm_w(parts, pb, C, M, cnt, ev.ltok + (d - 1) * M, ev.lprob + (d - 1) * M);
+        } else {
+            n = merge_topm_w(parts, pb, C, M, flags, theta, cnt, qrow, A.V, list);
+            for (int i = l; i < n; i += 32) {
+                const uint64_t key = list[i];
+                int r = 0;
+                for (int q = 0; q < n; ++q) r += list[q] > key;
+                const int o = (d - 1) * M + r;
+                ev.ltok[o] = ckey_idx(key);
+                ev.lprob[o] = ckey_val(key);
+            }
+        }
+        if ((flags & kPfHinted) && !(flags & kPfBad) && n < min(M, A.V)) {
+            // a hint above this row's M-th value: the row again, unhinted
+            return make_job(b, d - 1, 0, 0);
+        }
+        if (n > 0 && !(flags & kPfBad)) {
+            const uint32_t h = topm_hint(ev.lprob[(d - 1) * M + n - 1]);
+            if (l == 0) {
+                sm.last_hint = h;
+                topm_hint_store(A.E.W.ctrl, h, A.V, M);
+            }
         }
         if (l == 0) {
             eh.len[d] = n;
@@ -440,15 +620,85 @@ struct BuildOp {
             if (flags & kPfBad) eh.status |= 1;
         }
         __syncwarp();
+        SPEC_TRACE_T(tb1);
+#ifdef SPEC_TRACE
+        const int count0 = eh.count;
+#endif
         const int need = enumerate_w(A, eh, ev);
+#ifdef SPEC_TRACE
+        if (l == 0) SPEC_TRACE_EV(15, static_cast<int>(tb1 - tb0), static_cast<int>(clock64() - tb1), eh.count - count0);
+#endif
         if (need == 0) {
             build_finalize(A, ev, b, eh.count, eh.status);
             return job_done();
         }
-        enum_save(A, b, eh, ev, d - 1);
-        return make_job(b, need - 1, 0, 0);
+        if (G.own > 1) enum_save(A, b, eh, ev, d - 1);
+        Job nj = make_job(b, need - 1, 0, 0);
+        nj.hint = sm.last_hint;
+        return nj;
     }
 };
+
+// The row's top-M from the slices' sorted lists (combiner warp), written to
+// tok / prob in rank order: a key's merged rank is the number of greater keys
+// over all lists (binary searches, kRegKeys keys per lane at a time, every
+// load unconditional so that a step's loads issue together); the keys of
+// rank < M are the row's M largest.  `cnt`: lane r holds list r's length.
+// Returns min(total, M).
+constexpr int kMergeKeys = 4;
+__device__ int merge_sorted_topm_w(const unsigned char* parts, int pb, int C, int M, int cnt, int* tok,
+                                   float* prob) {
+    const int l = threadIdx.x & 31;
+    const int cl = l < C ? cnt : 0;
+    int tot;
+    const int off = warp_exscan_i(cl, tot);
+    if (tot == 0) return 0;
+    const uint32_t kb0 = smem_u32(parts) + static_cast<uint32_t>(sizeof(PartHdr));
+    const uint32_t mmax = warp_max_u32(static_cast<uint32_t>(cl));
+    const int s0 = 1 << (31 - __clz(mmax));
+    for (int f0 = 0; f0 < tot; f0 += 32 * kMergeKeys) {
+        uint64_t key[kMergeKeys];
+        int rank[kMergeKeys];
+#pragma unroll
+        for (int j = 0; j < kMergeKeys; ++j) {
+            const int f = min(f0 + l + 32 * j, tot - 1);
+            int r = 0;
+            for (int q = 1; q < C; ++q) r += __shfl_sync(0xffffffffu, off, q) <= f ? 1 : 0;
+            const int base = __shfl_sync(0xffffffffu, off, r);
+            key[j] = lds_u64(kb0 + static_cast<uint32_t>(r * pb + (f - base) * 8));
+            rank[j] = 0;
+        }
+        for (int q = 0; q < C; ++q) {
+            const int mq = __shfl_sync(0xffffffffu, cl, q);
+            const uint32_t lb = kb0 + static_cast<uint32_t>(q * pb);
+            int pos[kMergeKeys];
+#pragma unroll
+            for (int j = 0; j < kMergeKeys; ++j) pos[j] = 0;
+            for (int st = s0; st > 0; st >>= 1) {
+                uint64_t v[kMergeKeys];
+#pragma unroll
+                for (int j = 0; j < kMergeKeys; ++j)
+                    v[j] = lds_u64(lb + static_cast<uint32_t>((max(min(pos[j] + st, mq), 1) - 1) * 8));
+#pragma unroll
+                for (int j = 0; j < kMergeKeys; ++j) {
+                    const int np = pos[j] + st;
+                    pos[j] = (np <= mq && v[j] > key[j]) ? np : pos[j];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kMergeKeys; ++j) rank[j] += pos[j];
+        }
+#pragma unroll
+        for (int j = 0; j < kMergeKeys; ++j) {
+            if (f0 + l + 32 * j < tot && rank[j] < M) {
+                tok[rank[j]] = ckey_idx(key[j]);
+                prob[rank[j]] = ckey_val(key[j]);
+            }
+        }
+    }
+    __syncwarp();
+    return tot < M ? tot : M;
+}
 
 __device__ int merge_topm_w(const unsigned char* parts, int pb, int C, int M, uint32_t flags, uint64_t theta, int cnt,
                             const float* qrow, int V, uint64_t* list) {
@@ -496,13 +746,16 @@ struct EagleOp {
 
     __device__ static int batch(const Args& A) { return A.base.B * A.F; }
     __device__ static bool tma(const Args& A) { return A.base.tma_q != 0; }
-    __device__ static void init_smem(const Args&, const Geo&, Smem& sm) {
-        if (threadIdx.x == 0) topk_smem_init(sm.tk);
+    __device__ static void init_smem(const Args& A, const Geo&, Smem& sm) {
+        if (threadIdx.x == 0) {
+            topk_smem_init(sm.tk);
+            sm.last_hint = topm_hint_load(A.base.E.W.ctrl, A.base.V, A.base.M);
+        }
     }
     __device__ static EagleRowHdr* row_hdr(const Args& A, int u) {
         return reinterpret_cast<EagleRowHdr*>(A.base.E.W.extra + static_cast<size_t>(u) * A.base.E.W.extra_stride);
     }
-    __device__ static Job first(const Args& A, const Geo&, int u, Smem&) {
+    __device__ static Job first(const Args& A, const Geo&, int u, Smem& sm) {
         const int b = u / A.F, f = u - b * A.F;
         int nf = A.num_front_in[b];
         nf = nf < 0 ? 0 : (nf > A.F ? A.F : nf);
@@ -525,7 +778,9 @@ struct EagleOp {
             __syncwarp();
             return job_done();
         }
-        return make_job(b, f, 0, 0);
+        Job j = make_job(b, f, 0, 0);
+        j.hint = sm.last_hint;
+        return j;
     }
     __device__ static StreamPlan plan(const Args& A, const Geo& G, const Job& j) { return BuildOp::plan(A.base, G, j); }
     __device__ static int consume(const Args& A, const Geo& G, const Pipe& P, uint32_t& seq, bool tma, const Job& j,
@@ -546,17 +801,33 @@ struct EagleOp {
         theta = warp_max_u64(theta);
         const float* qrow = A.base.q + static_cast<long long>(j.b) * A.base.q_bs +
                             static_cast<long long>(j.row) * A.base.q_rs;
-        const int n = merge_topm_w(parts, pb, C, M, flags, theta, cnt, qrow, A.base.V, sm.list);
         const int u = j.b * A.F + j.row;
         EagleRowHdr* h = row_hdr(A, u);
         int* tok = reinterpret_cast<int*>(h + 1);
         float* prob = reinterpret_cast<float*>(tok + M);
-        for (int i = l; i < n; i += 32) {
-            const uint64_t key = sm.list[i];
-            int r = 0;
-            for (int q = 0; q < n; ++q) r += sm.list[q] > key;
-            tok[r] = ckey_idx(key);
-            prob[r] = ckey_val(key);
+        int n;
+        if (!(flags & (kPfBad | kPfOverflow))) {
+            n = merge_sorted_topm_w(parts, pb, C, M, cnt, tok, prob);
+            if ((flags & kPfHinted) && n < min(M, A.base.V)) {
+                // a hint above this row's K2-th value: the row again, unhinted
+                return make_job(j.b, j.row, 0, 0);
+            }
+            if (n > 0) {
+                const uint32_t hn = topm_hint(prob[n - 1]);
+                if (l == 0) {
+                    sm.last_hint = hn;
+                    topm_hint_store(A.base.E.W.ctrl, hn, A.base.V, M);
+                }
+            }
+        } else {
+            n = merge_topm_w(parts, pb, C, M, flags, theta, cnt, qrow, A.base.V, sm.list);
+            for (int i = l; i < n; i += 32) {
+                const uint64_t key = sm.list[i];
+                int r = 0;
+                for (int q = 0; q < n; ++q) r += sm.list[q] > key;
+                tok[r] = ckey_idx(key);
+                prob[r] = ckey_val(key);
+            }
         }
         if (l == 0) {
             h->n = n;
@@ -590,3 +861,18 @@ size_t build_smem(int C, int own, int part_bytes, int stages, int chunk, int N, 
 int build_part_bytes(int M) { return static_cast<int>(sizeof(PartHdr)) + ((M > 0 ? M : 1) * 8 + 15) / 16 * 16; }
 
 }  // namespace spec
+
+#ifdef SPEC_TRACE
+// development builds: this translation unit's event trace buffer
+extern "C" int spec_trace_setup_build(void* buf, unsigned cap) {
+    unsigned z = 0;
+    if (cudaMemcpyToSymbol(spec::g_trace, &buf, sizeof(buf)) != cudaSuccess) return 1;
+    if (cudaMemcpyToSymbol(spec::g_trace_cap, &cap, sizeof(cap)) != cudaSuccess) return 1;
+    return cudaMemcpyToSymbol(spec::g_trace_n, &z, sizeof(z)) != cudaSuccess;
+}
+extern "C" unsigned spec_trace_count_build(void) {
+    unsigned n = 0;
+    cudaMemcpyFromSymbol(&n, spec::g_trace_n, sizeof(n));
+    return n;
+}
+#endif

@@ -176,3 +176,18 @@ size_t walk_smem(int C, int own, int part_bytes, int stages, int chunk) {
 int walk_part_bytes() { return static_cast<int>(sizeof(PartHdr)); }
 
 }  // namespace spec
+
+#ifdef SPEC_TRACE
+// development builds: this translation unit's event trace buffer
+extern "C" int spec_trace_setup_walk(void* buf, unsigned cap) {
+    unsigned z = 0;
+    if (cudaMemcpyToSymbol(spec::g_trace, &buf, sizeof(buf)) != cudaSuccess) return 1;
+    if (cudaMemcpyToSymbol(spec::g_trace_cap, &cap, sizeof(cap)) != cudaSuccess) return 1;
+    return cudaMemcpyToSymbol(spec::g_trace_n, &z, sizeof(z)) != cudaSuccess;
+}
+extern "C" unsigned spec_trace_count_walk(void) {
+    unsigned n = 0;
+    cudaMemcpyFromSymbol(&n, spec::g_trace_n, sizeof(n));
+    return n;
+}
+#endif

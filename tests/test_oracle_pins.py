@@ -737,6 +737,20 @@ def test_adaptive_closed_forms():
     np.testing.assert_array_equal(zero["q_row_off"], [0, 0, 0, 0])
 
 
+def test_adaptive_exact_ties_go_to_the_smaller_k():
+    """c = 1 and cost a + b k with a = b = 1: E(k)/cost(k) = (1+k)/(1+k) = 1
+    exactly for every k, so the smaller-k tie rule picks k = 0; the same with
+    the cost table 1 + k, and a two-way tie at k = 2, 5 from a table."""
+    Kmax = 6
+    c = np.ones((2, Kmax), np.float32)
+    assert (oracle.adaptive_len(c, 1.0, 1.0)["k"] == 0).all()
+    assert (oracle.adaptive_len(c, 1.0, 0.0, cost=np.arange(1, Kmax + 2, dtype=np.float64))["k"] == 0).all()
+    # E = 1..7; cost chosen so that E/cost = 1.5 exactly at k = 2 and k = 5, 1 elsewhere
+    cost = np.array([1, 2, 2, 4, 5, 4, 7], np.float64)
+    o = oracle.adaptive_len(c, 1.0, 0.0, cost=cost)
+    assert (o["k"] == 2).all()
+
+
 def test_adaptive_hand_example():
     # c = 0.9, 0.8, 0.5, 0.5: s = .9, .72, .36, .18; E = 1.9, 2.62, 2.98, 3.16
     # E/(1+0.15k): 1.6522, 1.9407, 2.0552, 1.9750  -> k = 3
