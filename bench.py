@@ -54,13 +54,13 @@ NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
 
 
 def kernel_source_hash():
-    """Hash of the library's kernel and header sources (ties a profile to the code it measured)."""
-    import glob
+    """Hash of the chain kernel's sources -- its translation unit and the
+    headers it includes (ties a profile to the code it measured)."""
     import hashlib
     h = hashlib.sha256()
     pkg = os.path.join(ROOT, "speculative_decoding_draft_sampling_gb300", "csrc")
-    files = sorted(glob.glob(os.path.join(pkg, "*.cu")) + glob.glob(os.path.join(pkg, "*.cuh"))
-                   + glob.glob(os.path.join(ROOT, "include", "*.h")))
+    files = [os.path.join(pkg, f) for f in ("spec_chain.cu", "spec_chain.cuh", "spec_engine.cuh", "spec_common.cuh",
+                                             "spec_select.cuh")]
     for f in files:
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:

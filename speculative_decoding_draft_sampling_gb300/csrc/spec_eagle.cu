@@ -31,10 +31,18 @@ constexpr int kStTreeFull = 32;
 constexpr int kStBadNode = 64;
 
 struct SortEnt {
-    double s;
-    int d;        // depth (rerank) or 0 (grow)
-    int i;        // node index; 0x7fffffff: padding
+    unsigned long long s;   // order-preserving key of the score (larger first)
+    int d;                  // depth (rerank) or 0 (grow)
+    int i;                  // node index; 0x7fffffff: padding
 };
+
+// a double's order as an unsigned key (integer compares: the fp64 pipe is
+// narrow on this part); -0 and +0 share a key
+__device__ __forceinline__ unsigned long long score_key(double v) {
+    unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(v));
+    if ((b << 1) == 0ull) b = 0ull;
+    return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
+}
 
 // the order both sorts use: real entries first; score desc; depth asc; index asc
 __device__ __forceinline__ bool ent_first(const SortEnt& a, const SortEnt& b) {
@@ -69,7 +77,7 @@ __host__ __device__ __forceinline__ int pow2_at_least(int n) {
 }
 
 __global__ void __launch_bounds__(kGrowThreads) eagle_grow_kernel(const EagleGrowArgs A) {
-    __shared__ int s_off[65];
+    __shared__ int s_off[65], s_n[64], s_bad[64];
     __shared__ SortEnt s_ent[kGrowMax];
     __shared__ int s_st, s_g0, s_tot;
     const int b = blockIdx.x, tid = threadIdx.x;
@@ -77,17 +85,24 @@ __global__ void __launch_bounds__(kGrowThreads) eagle_grow_kernel(const EagleGro
     auto hdr = [&](int f) {
         return reinterpret_cast<const EagleRowHdr*>(A.rows + static_cast<long long>(b * F + f) * A.row_stride);
     };
+    // the row headers, one thread each, then the offsets on thread 0
+    if (tid < F) {
+        const EagleRowHdr* h = hdr(tid);
+        s_n[tid] = h->n;
+        s_bad[tid] = h->bad;
+    }
+    __syncthreads();
     if (tid == 0) {
         int st = 0;
         int g0 = A.num_gen[b];
         if (g0 < 1 || g0 > G) { st |= kStBadNode; g0 = g0 < 1 ? 0 : G; }
         int off = 0;
         for (int f = 0; f < F; ++f) {
-            const EagleRowHdr* h = hdr(f);
+            const int n = s_n[f];
             s_off[f] = off;
-            if (h->n == -2) st |= kStBadNode;
-            if (h->n >= 0 && h->bad) st |= 1;
-            if (h->n > 0) off += h->n;
+            if (n == -2) st |= kStBadNode;
+            if (n >= 0 && s_bad[f]) st |= 1;
+            if (n > 0) off += n;
         }
         s_off[F] = off;
         if (off > G - g0) st |= kStTreeFull;
@@ -99,7 +114,7 @@ __global__ void __launch_bounds__(kGrowThreads) eagle_grow_kernel(const EagleGro
     const int P = pow2_at_least(nc > 1 ? nc : 1);
     for (int c = tid; c < P; c += kGrowThreads) {
         SortEnt e;
-        e.s = 0.0; e.d = 0; e.i = 0x7fffffff;
+        e.s = 0ull; e.d = 0; e.i = 0x7fffffff;
         if (c < nc) {
             int f = 0;
             while (s_off[f + 1] <= c) ++f;           // the slot whose children cover c
@@ -115,7 +130,7 @@ __global__ void __launch_bounds__(kGrowThreads) eagle_grow_kernel(const EagleGro
             A.parent[nb + g] = u;
             A.depth[nb + g] = A.depth[nb + u] + 1;
             A.score[nb + g] = sc;
-            e.s = sc; e.i = g;
+            e.s = score_key(sc); e.i = g;
         }
         s_ent[c] = e;
     }
@@ -150,8 +165,8 @@ __global__ void __launch_bounds__(kRerankThreads) eagle_rerank_kernel(const Eagl
     const int g = s_g;
     for (int i = tid; i < P; i += kRerankThreads) {
         SortEnt e;
-        e.s = 0.0; e.d = 0; e.i = 0x7fffffff;
-        if (i + 1 < g) { e.s = A.score[nb + i + 1]; e.d = A.depth[nb + i + 1]; e.i = i + 1; }
+        e.s = 0ull; e.d = 0; e.i = 0x7fffffff;
+        if (i + 1 < g) { e.s = score_key(A.score[nb + i + 1]); e.d = A.depth[nb + i + 1]; e.i = i + 1; }
         ent[i] = e;
     }
     for (int i = tid; i < G; i += kRerankThreads) { pos[i] = 0; nid[i] = -1; }

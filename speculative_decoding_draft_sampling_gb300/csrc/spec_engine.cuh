@@ -913,12 +913,19 @@ struct Engine {
         bool dead = false;
         while (retired < G.R) {
             int s = -1;
+            // of the posted jobs, the deepest row first (a request's rows are
+            // sequential: its later rows are on the path that ends the call);
+            // equal rows in round-robin order
             dead = !poll_until([&]() {
+                int best_row = -1;
                 for (int k = 0; k < G.R; ++k) {
                     const int t = (s0 + k) % G.R;
-                    if (mbar_test_cluster(&es.jfull[t], (jph >> t) & 1u)) { s = t; return true; }
+                    if (mbar_test_cluster(&es.jfull[t], (jph >> t) & 1u)) {
+                        const int row = reinterpret_cast<const volatile Job*>(&es.jd[t])->row;
+                        if (row > best_row) { best_row = row; s = t; }
+                    }
                 }
-                return false;
+                return s >= 0;
             }, P.abort, W.ctrl);
             if (dead) break;
             s0 = s + 1 == G.R ? 0 : s + 1;
