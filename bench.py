@@ -13,6 +13,7 @@ A step is one pass of the verification hot path over one batch:
   chain_small    chain verify B=4 K=4 V=1000
   ddtree   DDTree build (B=32, L=16, budget 64, V=151936) + tree walk
   dspark   DSpark verify length + ragged chain verify (B=512, Kmax=8, V=128256 bf16)
+  eagle2   EAGLE-2 dynamic tree: six expansion steps + rerank (B=32, V=151936 fp32)
 
 Inputs are seeded synthetic tensors (see workloads/), resident in HBM before
 the timed region.  Successive steps rotate over 3 independently seeded input
@@ -22,9 +23,11 @@ rows read per step exceed the 126 MB L2 for dflash/dspark).
 The line also carries: `parity` -- every request of input copy 0 re-run on
 the float64 oracle (threads over requests on the host cores) and compared
 with the GPU's outputs; `cpu_baseline` -- that oracle timed on one thread and
-on every host core; `e2e` -- the same step through the public API with the
-inputs copied from pinned host buffers and the results copied back inside
-the timed region.
+on every host core; `e2e` -- the same step through the public API on
+inputs in pinned host memory, which the kernels read in place over the
+CPU-GPU link (only the rows the step needs cross it), with the results read
+back to the host inside the timed region; `e2e_copy_all` -- the same with
+every input copied to the device first.
 
 Multi-GPU (torchrun): every rank verifies its own batch (weak scaling, no
 collective on the data path); the time is the max over ranks.
@@ -206,19 +209,15 @@ def make_chain_case(name, dev, copies, greedy=False, over=None):
 
     def e2e():
         w = ws[0]
-        d_in = [w.logits, w.draft_greedy if greedy else w.draft]
-        if not greedy:
-            d_in += [w.uniforms, w.q]
-        d_in = [torch.empty_like(t) for t in d_in]
         h_in = [pinned(t) for t in ([w.logits, w.draft_greedy] if greedy else [w.logits, w.draft, w.uniforms, w.q])]
 
-        def call():
+        def call(x):
             if greedy:
-                r = sv.verify_greedy(d_in[0], d_in[1])
+                r = sv.verify_greedy(x[0], x[1])
             else:
-                r = sv.verify_chain(d_in[0], d_in[3], d_in[1], d_in[2], w.temperature, w.top_k)
+                r = sv.verify_chain(x[0], x[3], x[1], x[2], w.temperature, w.top_k)
             return [r.tokens, r.num_accepted, r.status]
-        return h_in, d_in, call
+        return h_in, call
 
     w0 = ws[0]
     cfg = dict(workload=name + ("_greedy" if greedy else ""), B=w0.B, K=w0.K, V=w0.V,
@@ -262,13 +261,12 @@ def make_tree_case(dev, copies):
     def e2e():
         t, tl = ts[0], tls[0]
         h_in = [pinned(t.q), pinned(tl)]
-        d_in = [torch.empty_like(t.q), torch.empty_like(tl)]
 
-        def call():
-            tr = sv.tree_build(d_in[0], t.budget)
-            wk = sv.verify_tree(d_in[1], tr.token, tr.parent, tr.num_nodes, L)
+        def call(x):
+            tr = sv.tree_build(x[0], t.budget)
+            wk = sv.verify_tree(x[1], tr.token, tr.parent, tr.num_nodes, L)
             return [wk.tokens, wk.num_accepted, wk.path_nodes, wk.status]
-        return h_in, d_in, call
+        return h_in, call
 
     B, L, V = ts[0].q.shape
     cfg = dict(workload="ddtree", B=B, L=L, V=V, budget=ts[0].budget, q_dtype="float32", target_dtype="bfloat16")
@@ -303,16 +301,14 @@ def make_dspark_case(dev, copies):
         # the target's rows arrive packed for the verify lengths the
         # confidences give (the same on the host and the device)
         w, (pl, pq) = ws[0], packs[0]
-        src = [w.conf, pl, pq, w.draft, w.uniforms]
-        h_in = [pinned(t) for t in src]
-        d_in = [torch.empty_like(t) for t in src]
+        h_in = [pinned(t) for t in (w.conf, pl, pq, w.draft, w.uniforms)]
 
-        def call():
-            a = sv.adaptive_len(d_in[0], 1.0, 0.15)
-            r = sv.verify_chain(d_in[1], d_in[2], d_in[3], d_in[4], w.temperature, w.top_k, k_per_req=a.k,
+        def call(x):
+            a = sv.adaptive_len(x[0], 1.0, 0.15)
+            r = sv.verify_chain(x[1], x[2], x[3], x[4], w.temperature, w.top_k, k_per_req=a.k,
                                 l_row_off=a.l_row_off, q_row_off=a.q_row_off)
             return [r.tokens, r.num_accepted, r.status, a.k]
-        return h_in, d_in, call
+        return h_in, call
 
     w0 = ws[0]
     cfg = dict(workload="dspark", B=w0.B, Kmax=w0.K, V=w0.V, logits_dtype="bfloat16", temperature=1.0,
@@ -391,16 +387,15 @@ def make_eagle_case(dev, copies):
 
     def e2e():
         h_in = [pinned(q) for q in qs]
-        d_in = [torch.empty_like(q) for q in qs]
 
-        def call():
+        def call(x):
             s2 = sv.eagle_state(B, G, dev)
             fr, n = fronts[0]
             for s in range(steps):
-                fr, n, _ = sv.eagle_expand(d_in[s], s2, fr, n, K2, Fn)
+                fr, n, _ = sv.eagle_expand(x[s], s2, fr, n, K2, Fn)
             t = sv.eagle_rerank(s2, N)
             return [t.token, t.parent, t.depth, t.num_nodes]
-        return h_in, d_in, call
+        return h_in, call
 
     ccfg = dict(workload="eagle2", B=B, V=V, steps=steps, children_per_node=K2, frontier=Fn, budget=N,
                 q_dtype="float32", node_capacity=G)
@@ -694,37 +689,60 @@ def run_reference(args, rank, world):
     return 0
 
 
-def run_e2e(case, steps):
-    """The same step through the public API from pinned host buffers: every
-    step copies its inputs host -> device and its results device -> host
-    inside the timed region."""
-    h_in, d_in, call = case["e2e"]()
-    outs = call()
+def run_e2e(case, steps, world=1):
+    """The same step through the public API on inputs in pinned host memory,
+    timed with its results read back to the host every step, two ways:
+
+    - zero-copy (the reported `e2e`): the host tensors go to the call as they
+      are and the kernels read them in place over the CPU-GPU link, so only
+      the rows the step needs cross it (rows past a rejection stay on the
+      host); `h2d_bytes_per_step` is the step's algorithmic bytes, the bytes
+      the kernels read;
+    - copy-all (`e2e_copy_all`): every input is first copied to device
+      memory, then the call runs there; its bytes are the whole inputs.
+    """
+    h_in, call = case["e2e"]()
+    d_in = [torch.empty_like(t, device=torch.device("cuda", torch.cuda.current_device())) for t in h_in]
+    outs = call(d_in)
     h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
     stream = torch.cuda.current_stream()
 
-    def one():
-        for h, d in zip(h_in, d_in):
-            d.copy_(h, non_blocking=True)
-        res = call()
+    def zero_copy():
+        res = call(h_in)
         for h, o in zip(h_out, res):
             h.copy_(o, non_blocking=True)
 
-    one()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
+    def copy_all():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        res = call(d_in)
+        for h, o in zip(h_out, res):
+            h.copy_(o, non_blocking=True)
+
+    def timed(one):
         one()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            one()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
     pos = case["positions"]
     pos0 = pos[0] if isinstance(pos, list) else pos
-    h2d = sum(t.numel() * t.element_size() for t in h_in)
     d2h = sum(t.numel() * t.element_size() for t in h_out)
-    return dict(value=pos0 / (ms / 1e3), unit=UNIT, h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h),
-                ms_per_step=ms)
+    ms_zc = max_over_ranks(timed(zero_copy), world)
+    ms_cp = max_over_ranks(timed(copy_all), world)
+    whole = sum(t.numel() * t.element_size() for t in h_in)
+    zc = dict(value=pos0 * world / (ms_zc / 1e3), unit=UNIT, h2d_bytes_per_step=int(case["bytes"][0]),
+              d2h_bytes_per_step=int(d2h), ms_per_step=ms_zc,
+              mode="zero-copy: the kernels read the pinned host inputs in place over NVLink-C2C; "
+                   "h2d bytes = the rows and values they read")
+    cp = dict(value=pos0 * world / (ms_cp / 1e3), unit=UNIT, h2d_bytes_per_step=int(whole), d2h_bytes_per_step=int(d2h),
+              ms_per_step=ms_cp, mode="copy-all: every input copied host -> device, then the call")
+    return zc, cp
 
 
 def main():
@@ -807,7 +825,7 @@ def main():
     peak, peak_kind = peaks()
     achieved = bytes_step / (statistics.mean(step_ms) / 1e3) / 1e9
 
-    e2e = run_e2e(case, args.e2e_steps) if args.e2e_steps > 0 else None
+    e2e, e2e_copy = run_e2e(case, args.e2e_steps, world) if args.e2e_steps > 0 else (None, None)
 
     cpu = parity = None
     if rank == 0 and not (args.no_cpu_baseline and args.no_parity):
@@ -829,7 +847,7 @@ def main():
                     roofline=dict(bound="hbm", achieved=achieved, peak=peak, unit="GB/s", frac=achieved / peak,
                                   traffic=profiled_traffic(args.workload, bytes_step), peak_kind=peak_kind,
                                   nominal_peak=NOMINAL_HBM_GBS, frac_of_nominal=achieved / NOMINAL_HBM_GBS),
-                    parity=parity, cpu_baseline=cpu, e2e=e2e,
+                    parity=parity, cpu_baseline=cpu, e2e=e2e, e2e_copy_all=e2e_copy,
                     gpu_launches=args.steps * case["launches_per_step"],
                     clocks=clocks, wall_s=wall)
         print(json.dumps(line), flush=True)

@@ -8,10 +8,18 @@
  *               DDTree and DSpark), chzhyang.github.io.
  *
  * Conventions for every call
- *   - All array pointers are DEVICE pointers owned by the caller.  The
- *     library never allocates device memory; scratch space comes from the
- *     caller's `ws` buffer, sized by the matching *_workspace_size() query.
- *     The workspace must not be shared by two calls in flight at once.
+ *   - Array pointers are owned by the caller and point to device memory or
+ *     to PINNED host memory (page-locked: cudaHostAlloc, cudaMallocHost or
+ *     cudaHostRegister).  Pinned host arrays are read and written in place
+ *     through their mapping into the device's address space -- on a Grace
+ *     host over the NVLink-C2C link -- so a call on host-resident inputs
+ *     moves only the bytes it reads (rows past a rejection never cross the
+ *     link).  Pageable host memory cannot be reached by the kernels and is
+ *     refused with SPEC_INVALID_ARG before anything is enqueued.
+ *   - The library never allocates device memory; scratch space comes from
+ *     the caller's `ws` buffer (device memory), sized by the matching
+ *     *_workspace_size() query.  The workspace must not be shared by two
+ *     calls in flight at once.
  *     One exception: spec_verify_greedy_static takes no `ws` and uses a
  *     fixed array the library reserves in device memory (described there).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
@@ -323,9 +331,9 @@ spec_status spec_verify_tree_sample(
  * num_accepted[b] (dst_pos NULL: rows 0 ..).  No other destination row is
  * written.  A gather bound by HBM bandwidth.
  *
- *   src      DEVICE, row (p, b, n) at src + p*src_plane_stride +
+ *   src      row (p, b, n) at src + p*src_plane_stride +
  *            b*src_batch_stride + n*src_row_stride (strides in BYTES), n < N.
- *   dst      DEVICE, row (p, b, m) at dst + p*dst_plane_stride +
+ *   dst      row (p, b, m) at dst + p*dst_plane_stride +
  *            b*dst_batch_stride + m*dst_row_stride (bytes).  The rows written
  *            must not overlap the rows read (copy from the tree's own buffer
  *            into the cache, not within one buffer).
@@ -365,7 +373,7 @@ spec_status spec_adaptive_len(
  * [SD-survey] §9 (DSpark in SGLang): the cost of verifying k positions comes
  * from a table profiled for the deployment rather than a formula.  As
  * spec_adaptive_len with the cost a + b*k replaced by cost[k]:
- *   cost   DEVICE pointer, [Kmax+1] fp64, every entry finite and > 0 (the
+ *   cost   [Kmax+1] fp64, every entry finite and > 0 (the
  *          caller's responsibility: the kernel divides by it).
  * Outputs as spec_adaptive_len.
  * ---------------------------------------------------------------------- */

@@ -8,6 +8,12 @@ current CUDA stream.  All computation runs in the library's sm_103a
 kernels; there is no CPU or PyTorch fallback.  Importing the package does
 not load the library; the first call does, and raises if it is missing.
 
+Inputs and outputs may be CUDA tensors or pinned host tensors
+(``tensor.pin_memory()``): the kernels read pinned host arrays in place over
+the CPU-GPU link, so a call on host-resident logits moves only the rows it
+reads (rows past a rejection stay on the host).  Outputs that the call
+allocates, and the workspace, are on the current CUDA device.
+
 Functions (same names as the C entry points, without the ``spec_`` prefix):
   verify_chain   chain speculative sampling (accept min(1,p/q), residual, bonus)
   verify_greedy  greedy argmax-match verification
@@ -117,11 +123,18 @@ def _stream(stream=None):
 
 
 def _cuda(t: torch.Tensor, name: str, dtype=None):
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise SpecError(f"{name} must be a CUDA tensor")
+    """A CUDA tensor, or a pinned host tensor that the kernels read (or write)
+    in place through its device mapping."""
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or (t.device.type == "cpu" and t.is_pinned())):
+        raise SpecError(f"{name} must be a CUDA tensor or a pinned host tensor")
     if dtype is not None and t.dtype != dtype:
         raise SpecError(f"{name} must be {dtype}, got {t.dtype}")
     return t
+
+
+def _dev(t: torch.Tensor) -> torch.device:
+    """The CUDA device a call on t runs on (the current one for host tensors)."""
+    return t.device if t.is_cuda else torch.device("cuda", torch.cuda.current_device())
 
 
 def _ldt(t: torch.Tensor) -> int:
@@ -222,7 +235,7 @@ def verify_chain(logits, q, draft, uniforms, temperature: float, top_k: int = 0,
             raise SpecError("dense q must be [B, K, V]")
         lbs, lrs = logits.stride(0), logits.stride(1)
         qbs, qrs = q.stride(0), q.stride(1)
-    dev = logits.device
+    dev = _dev(logits)
     if out is None:
         out = ChainResult(torch.empty((B, K + 1), dtype=torch.int32, device=dev),
                           torch.empty(B, dtype=torch.int32, device=dev),
@@ -279,7 +292,7 @@ def verify_greedy(logits, draft, *, k_per_req=None, l_row_off=None, out: Optiona
         if logits.dim() != 3 or logits.shape[:2] != (B, K + 1):
             raise SpecError("dense logits must be [B, K+1, V]")
         lbs, lrs = logits.stride(0), logits.stride(1)
-    dev = logits.device
+    dev = _dev(logits)
     if out is None:
         out = GreedyResult(torch.empty((B, K + 1), dtype=torch.int32, device=dev),
                            torch.empty(B, dtype=torch.int32, device=dev),
@@ -320,7 +333,7 @@ def tree_build(q, budget: int, *, out: Optional[Tree] = None, ws: Optional[torch
     B, L, V = q.shape
     N = int(budget)
     W = (N + 63) // 64
-    dev = q.device
+    dev = _dev(q)
     if out is None:
         out = Tree(torch.empty((B, N), dtype=torch.int32, device=dev),
                    torch.empty((B, N), dtype=torch.int32, device=dev),
@@ -383,7 +396,7 @@ def eagle_expand(q, state: EagleState, front, num_front, K2: int, Fn: int, *, fr
     _cuda(state.score, "score", torch.float64)
     if tuple(front.shape) != (B, F) or not front.is_contiguous():
         raise SpecError("front must be a contiguous [B, F] tensor")
-    dev = q.device
+    dev = _dev(q)
     if front_out is None:
         front_out = torch.empty((B, Fn), dtype=torch.int32, device=dev)
     if num_front_out is None:
@@ -408,7 +421,7 @@ def eagle_rerank(state: EagleState, budget: int, *, out: Optional[Tree] = None, 
     B, G = state.token.shape
     N = int(budget)
     W = (N + 63) // 64
-    dev = state.token.device
+    dev = _dev(state.token)
     if out is None:
         out = Tree(torch.empty((B, N), dtype=torch.int32, device=dev),
                    torch.empty((B, N), dtype=torch.int32, device=dev),
@@ -449,7 +462,7 @@ def verify_tree(logits, token, parent, num_nodes, max_depth: int, *, out: Option
     B, N = token.shape
     V = logits.shape[-1]
     Ld = int(max_depth)
-    dev = logits.device
+    dev = _dev(logits)
     if out is None:
         out = TreeWalk(torch.empty((B, Ld + 1), dtype=torch.int32, device=dev),
                        torch.empty((B, Ld + 1), dtype=torch.int32, device=dev),
@@ -487,7 +500,7 @@ def verify_tree_sample(logits, token, parent, num_nodes, uniforms, max_depth: in
     Ld = int(max_depth)
     if uniforms.shape != (B, Ld + 1) or not uniforms.is_contiguous():
         raise SpecError("uniforms must be a contiguous [B, max_depth+1] tensor")
-    dev = logits.device
+    dev = _dev(logits)
     if out is None:
         out = TreeWalk(torch.empty((B, Ld + 1), dtype=torch.int32, device=dev),
                        torch.empty((B, Ld + 1), dtype=torch.int32, device=dev),
@@ -558,7 +571,7 @@ def adaptive_len(conf, a: float, b: float, *, cost=None, out: Optional[AdaptiveL
     if conf.dim() != 2 or not conf.is_contiguous():
         raise SpecError("conf must be a contiguous [B, Kmax] tensor")
     B, Kmax = conf.shape
-    dev = conf.device
+    dev = _dev(conf)
     if out is None:
         out = AdaptiveLen(torch.empty(B, dtype=torch.int32, device=dev),
                           torch.empty((B, Kmax), dtype=torch.float64, device=dev),

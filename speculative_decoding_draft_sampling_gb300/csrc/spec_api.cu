@@ -43,6 +43,48 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool valid_dtype(spec_dtype d) { return d == SPEC_F32 || d == SPEC_BF16; }
 int esize_of(spec_dtype d) { return d == SPEC_F32 ? 4 : 2; }
 
+// Where an array lives.  Device (and managed) memory is used as it is;
+// pinned host memory is read and written in place through its mapping into
+// the device's address space (on a Grace host, over the NVLink-C2C link);
+// pageable host memory cannot be reached by the kernels and is refused.
+template <class T>
+spec_status map_ptr(const char* who, const char* name, T*& p) {
+    if (!p) return SPEC_OK;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SPEC_INVALID_ARG, "%s: %s is not memory the device can reach", who, name);
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return SPEC_OK;
+    if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+        p = static_cast<T*>(a.devicePointer);
+        return SPEC_OK;
+    }
+    return fail(SPEC_INVALID_ARG, "%s: %s is pageable host memory (pass device memory or pinned host memory)", who,
+                name);
+}
+#define SPEC_MAP(x)                                              \
+    do {                                                         \
+        const spec_status map_s_ = map_ptr(who, #x, x);          \
+        if (map_s_ != SPEC_OK) return map_s_;                    \
+    } while (0)
+
+// The workspace holds the kernels' queues, flags and partial results: it must
+// be device memory.
+spec_status ws_on_device(const char* who, const void* ws) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ws) != cudaSuccess || a.type != cudaMemoryTypeDevice) {
+        cudaGetLastError();
+        return fail(SPEC_INVALID_ARG, "%s: the workspace must be device memory", who);
+    }
+    return SPEC_OK;
+}
+#define SPEC_WS_DEVICE(w)                                        \
+    do {                                                         \
+        const spec_status ws_s_ = ws_on_device(who, w);          \
+        if (ws_s_ != SPEC_OK) return ws_s_;                      \
+    } while (0)
+
 // Bulk copies (TMA) need device memory: host memory mapped into the device's
 // address space is read with plain loads.
 bool device_memory(const void* p) {
@@ -331,6 +373,18 @@ spec_status spec_verify_chain(
     if (ws_bytes < ws_bytes_for(B, 0))
         return fail(SPEC_INVALID_ARG, "%s: workspace too small (%zu < %zu)", who, ws_bytes, ws_bytes_for(B, 0));
     if (!aligned16(ws)) return fail(SPEC_INVALID_ARG, "%s: workspace must be 16-byte aligned", who);
+    SPEC_MAP(logits);
+    SPEC_MAP(q);
+    SPEC_MAP(draft);
+    SPEC_MAP(uniforms);
+    SPEC_MAP(k_per_req);
+    SPEC_MAP(l_row_off);
+    SPEC_MAP(q_row_off);
+    SPEC_MAP(out_tokens);
+    SPEC_MAP(num_accepted);
+    SPEC_MAP(status);
+    SPEC_MAP(diag);
+    SPEC_WS_DEVICE(ws);
     const int es = esize_of(ldt);
     const bool topk = top_k > 0 && top_k < V;
     spec::ChainArgs A{};
@@ -387,6 +441,14 @@ spec_status spec_verify_greedy(
     if (ws_bytes < ws_bytes_for(B, 0))
         return fail(SPEC_INVALID_ARG, "%s: workspace too small (%zu < %zu)", who, ws_bytes, ws_bytes_for(B, 0));
     if (!aligned16(ws)) return fail(SPEC_INVALID_ARG, "%s: workspace must be 16-byte aligned", who);
+    SPEC_MAP(logits);
+    SPEC_MAP(draft);
+    SPEC_MAP(k_per_req);
+    SPEC_MAP(l_row_off);
+    SPEC_MAP(out_tokens);
+    SPEC_MAP(num_accepted);
+    SPEC_MAP(status);
+    SPEC_WS_DEVICE(ws);
     const int es = esize_of(ldt);
     spec::WalkArgs A{};
     A.logits = logits; A.l_bs = l_batch_stride; A.l_rs = l_row_stride;
@@ -431,6 +493,15 @@ spec_status spec_tree_build(
     const size_t need = ws_bytes_for(B, spec::build_extra_bytes(budget, L));
     if (ws_bytes < need) return fail(SPEC_INVALID_ARG, "%s: workspace too small (%zu < %zu)", who, ws_bytes, need);
     if (!aligned16(ws)) return fail(SPEC_INVALID_ARG, "%s: workspace must be 16-byte aligned", who);
+    SPEC_MAP(q);
+    SPEC_MAP(token);
+    SPEC_MAP(parent);
+    SPEC_MAP(depth);
+    SPEC_MAP(score);
+    SPEC_MAP(anc_mask);
+    SPEC_MAP(num_nodes);
+    SPEC_MAP(status);
+    SPEC_WS_DEVICE(ws);
     spec::BuildArgs A{};
     A.q = q; A.q_bs = q_batch_stride; A.q_rs = q_row_stride;
     A.B = B; A.L = L; A.V = V; A.N = budget; A.M = budget - 1;
@@ -480,6 +551,18 @@ spec_status spec_eagle_expand(
     const size_t need = ws_bytes_for(B * F, spec::eagle_row_extra_bytes(K2));
     if (ws_bytes < need) return fail(SPEC_INVALID_ARG, "%s: workspace too small (%zu < %zu)", who, ws_bytes, need);
     if (!aligned16(ws)) return fail(SPEC_INVALID_ARG, "%s: workspace must be 16-byte aligned", who);
+    SPEC_MAP(q);
+    SPEC_MAP(token);
+    SPEC_MAP(parent);
+    SPEC_MAP(depth);
+    SPEC_MAP(score);
+    SPEC_MAP(num_gen);
+    SPEC_MAP(front_in);
+    SPEC_MAP(num_front_in);
+    SPEC_MAP(front_out);
+    SPEC_MAP(num_front_out);
+    SPEC_MAP(status);
+    SPEC_WS_DEVICE(ws);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     spec::EagleArgs A{};
     A.base.q = q; A.base.q_bs = q_batch_stride; A.base.q_rs = q_row_stride;
@@ -523,6 +606,18 @@ spec_status spec_eagle_rerank(
     if (!token || !parent || !depth || !score || !num_gen || !out_token || !out_parent || !out_depth || !out_score ||
         !anc_mask || !num_nodes || !status)
         return fail(SPEC_INVALID_ARG, "%s: null pointer argument", who);
+    SPEC_MAP(token);
+    SPEC_MAP(parent);
+    SPEC_MAP(depth);
+    SPEC_MAP(score);
+    SPEC_MAP(num_gen);
+    SPEC_MAP(out_token);
+    SPEC_MAP(out_parent);
+    SPEC_MAP(out_depth);
+    SPEC_MAP(out_score);
+    SPEC_MAP(anc_mask);
+    SPEC_MAP(num_nodes);
+    SPEC_MAP(status);
     spec::EagleRerankArgs A{};
     A.token = token; A.parent = parent; A.depth = depth; A.score = score; A.num_gen = num_gen;
     A.B = B; A.G = G; A.N = budget;
@@ -559,6 +654,15 @@ spec_status spec_verify_tree(
     if (ws_bytes < ws_bytes_for(B, 0))
         return fail(SPEC_INVALID_ARG, "%s: workspace too small (%zu < %zu)", who, ws_bytes, ws_bytes_for(B, 0));
     if (!aligned16(ws)) return fail(SPEC_INVALID_ARG, "%s: workspace must be 16-byte aligned", who);
+    SPEC_MAP(logits);
+    SPEC_MAP(token);
+    SPEC_MAP(parent);
+    SPEC_MAP(num_nodes);
+    SPEC_MAP(path_nodes);
+    SPEC_MAP(out_tokens);
+    SPEC_MAP(num_accepted);
+    SPEC_MAP(status);
+    SPEC_WS_DEVICE(ws);
     const int es = esize_of(ldt);
     spec::WalkArgs A{};
     A.logits = logits; A.l_bs = l_batch_stride; A.l_rs = l_row_stride;
@@ -607,6 +711,16 @@ spec_status spec_verify_tree_sample(
     if (ws_bytes < ws_bytes_for(B, 0))
         return fail(SPEC_INVALID_ARG, "%s: workspace too small (%zu < %zu)", who, ws_bytes, ws_bytes_for(B, 0));
     if (!aligned16(ws)) return fail(SPEC_INVALID_ARG, "%s: workspace must be 16-byte aligned", who);
+    SPEC_MAP(logits);
+    SPEC_MAP(token);
+    SPEC_MAP(parent);
+    SPEC_MAP(num_nodes);
+    SPEC_MAP(uniforms);
+    SPEC_MAP(path_nodes);
+    SPEC_MAP(out_tokens);
+    SPEC_MAP(num_accepted);
+    SPEC_MAP(status);
+    SPEC_WS_DEVICE(ws);
     const int es = esize_of(ldt);
     const bool topk = top_k > 0 && top_k < V;
     spec::ChainArgs A{};
@@ -651,6 +765,11 @@ spec_status spec_kv_compact(
     if (src_row_stride < row_bytes || dst_row_stride < row_bytes || src_batch_stride < 0 || dst_batch_stride < 0 ||
         src_plane_stride < 0 || dst_plane_stride < 0)
         return fail(SPEC_INVALID_ARG, "%s: row strides must be >= row_bytes, other strides >= 0", who);
+    SPEC_MAP(src);
+    SPEC_MAP(dst);
+    SPEC_MAP(path_nodes);
+    SPEC_MAP(num_accepted);
+    SPEC_MAP(dst_pos);
     spec::KvArgs A{};
     A.src = static_cast<const unsigned char*>(src);
     A.s_plane = src_plane_stride; A.s_batch = src_batch_stride; A.s_row = src_row_stride;
@@ -687,6 +806,13 @@ spec_status spec_adaptive_len(
         return fail(SPEC_INVALID_ARG, "spec_adaptive_len: null pointer argument");
     if (static_cast<long long>(B) * (Kmax + 1) > 0x7fffffffLL)
         return fail(SPEC_UNSUPPORTED, "spec_adaptive_len: row offsets overflow int32");
+    const char* who = "spec_adaptive_len";
+    SPEC_MAP(conf);
+    SPEC_MAP(k_out);
+    SPEC_MAP(surv);
+    SPEC_MAP(exp_adv);
+    SPEC_MAP(l_row_off);
+    SPEC_MAP(q_row_off);
     cudaError_t e = spec::adaptive_run(conf, B, Kmax, a, b, nullptr, k_out, surv, exp_adv, l_row_off, q_row_off,
                                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "spec_adaptive_len: launch");
@@ -702,6 +828,14 @@ spec_status spec_adaptive_len_table(
         return fail(SPEC_INVALID_ARG, "spec_adaptive_len_table: null pointer argument");
     if (static_cast<long long>(B) * (Kmax + 1) > 0x7fffffffLL)
         return fail(SPEC_UNSUPPORTED, "spec_adaptive_len_table: row offsets overflow int32");
+    const char* who = "spec_adaptive_len_table";
+    SPEC_MAP(conf);
+    SPEC_MAP(cost);
+    SPEC_MAP(k_out);
+    SPEC_MAP(surv);
+    SPEC_MAP(exp_adv);
+    SPEC_MAP(l_row_off);
+    SPEC_MAP(q_row_off);
     cudaError_t e = spec::adaptive_run(conf, B, Kmax, 1.0f, 0.0f, cost, k_out, surv, exp_adv, l_row_off, q_row_off,
                                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "spec_adaptive_len_table: launch");

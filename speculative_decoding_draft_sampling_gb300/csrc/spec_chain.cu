@@ -323,6 +323,7 @@ __device__ __forceinline__ int list_of(int off, int C, int f) {
 template <class E>
 __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const Job job, const unsigned char* parts,
                                          ChainSmem& sm) {
+    if ((threadIdx.x & 31) == 0) SPEC_TRACE_EV(18, job.b, job.row, 0);
     SPEC_TRACE_T(tc0);
     const int l = threadIdx.x & 31;
     const int C = G.C, pb = G.part_bytes;
@@ -335,8 +336,10 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
                                                               draw_uidx(A, job)]));
     const float ur = bonus ? 0.f : __uint_as_float(ldg_now_u32(&A.uniforms[static_cast<long long>(b) *
                                                                                 ((A.tree ? A.L : A.K) + 1) + row]));
+    SPEC_TRACE_T(tcu);
     DraftLoads<E> dl;
     if (!bonus) dl.issue(A, job, chain_k(A, b));
+    SPEC_TRACE_T(tca);
     // the slices' headers (value filters: the low key halves are zero)
     const uint32_t hb = smem_u32(parts) + static_cast<uint32_t>(l * pb);
     uint32_t flags = 0, vkey = 0, thk = 0;
@@ -350,6 +353,7 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
     flags = __reduce_or_sync(0xffffffffu, flags);
     const float vmax = fkey_inv(__reduce_max_sync(0xffffffffu, vkey));
     const uint32_t th = __reduce_max_sync(0xffffffffu, thk);
+    SPEC_TRACE_T(tcb);
     if ((flags & kPfBad) || !(vmax > -kInf)) return finish_at(A, job, -1, st | 1);
     if (flags & kPfOverflow) {
         // massive ties: the exact k-th value by radix select
@@ -360,9 +364,12 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
         return j;
     }
     // the prefix of each list at or above the largest slice filter holds
-    // every member of S in that slice
+    // every member of S in that slice (two lists are merged whole: the split
+    // search below needs no common cut)
     int mr = 0;
-    {
+    if (C == 2) {
+        mr = l < C ? cnt : 0;
+    } else {
         // keys of list l at or above th: a power-of-two search over at most
         // 512 keys (every lane runs it; lanes >= C count none)
         const int cl = l < C ? cnt : 0;
@@ -375,8 +382,14 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
         }
         if (cl >= 512 && mr == 511 && hkey(lds_u64(lr + 8u * 511u)) >= th) mr = 512;
     }
-    int n;
-    const int off = warp_exscan_i(mr, n);
+    int n, off;
+    if (C == 2) {
+        const int c0 = __shfl_sync(0xffffffffu, mr, 0), c1 = __shfl_sync(0xffffffffu, mr, 1);
+        n = c0 + c1;
+        off = l == 0 ? 0 : (l == 1 ? c0 : n);
+    } else {
+        off = warp_exscan_i(mr, n);
+    }
     const uint32_t lt = (1u << l) - 1u;
     if (n < k) {
         // a hinted slice filter sat above the row's k-th value: stream the row
@@ -408,7 +421,52 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
     uint32_t tau_key;
     int keep = 0;
     dfloat zp = df_make(0.f);
-    if (C <= 4 && n <= 32 * kRegKeys) {
+    if (C == 2 && n <= 32 * kRegKeys) {
+        // two lists: the k largest keys are A[0, i) and B[0, k - i) for the
+        // one split i with A[i-1] > B[k-i] and B[k-i-1] > A[i] (where those
+        // entries exist; keys are distinct).  Every candidate split is tested
+        // at once, one per lane (adjacent entries: no bank conflicts), and
+        // the k-th largest key is the smaller of the two prefixes' last.
+        const int mA = __shfl_sync(0xffffffffu, mr, 0), mB = __shfl_sync(0xffffffffu, mr, 1);
+        uint64_t key[kRegKeys];
+#pragma unroll
+        for (int j = 0; j < kRegKeys; ++j) {
+            const int f = min(l + 32 * j, n - 1);
+            const uint32_t a = f < mA ? kbase + static_cast<uint32_t>(f * 8)
+                                      : kbase + static_cast<uint32_t>(pb + (f - mA) * 8);
+            const uint64_t v = lds_u64(a);
+            key[j] = l + 32 * j < n ? v : 0ull;
+        }
+        const int lo = max(0, k - mB), hi = min(k, mA);
+        const uint32_t la = kbase, lb = kbase + static_cast<uint32_t>(pb);
+        tauc = 0ull;
+        for (int i0 = lo; i0 <= hi; i0 += 32) {
+            const int i = min(i0 + l, hi), j = k - i;
+            const uint64_t a1 = lds_u64(la + 8u * static_cast<uint32_t>(max(i - 1, 0)));
+            const uint64_t a0 = lds_u64(la + 8u * static_cast<uint32_t>(min(i, max(mA - 1, 0))));
+            const uint64_t b1 = lds_u64(lb + 8u * static_cast<uint32_t>(max(j - 1, 0)));
+            const uint64_t b0 = lds_u64(lb + 8u * static_cast<uint32_t>(min(j, max(mB - 1, 0))));
+            const bool ok = i0 + l <= hi && (i == 0 || j == mB || a1 > b0) && (j == 0 || i == mA || b1 > a0);
+            const uint64_t cand = i == 0 ? b1 : (j == 0 ? a1 : (a1 < b1 ? a1 : b1));
+            const uint32_t who = __ballot_sync(0xffffffffu, ok);
+            if (who) {
+                const int src = __ffs(who) - 1;
+                const uint32_t tlo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(cand), src);
+                const uint32_t thi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(cand >> 32), src);
+                tauc = (static_cast<uint64_t>(thi) << 32) | tlo;
+                break;
+            }
+        }
+        tau_key = hkey(tauc);
+#pragma unroll
+        for (int j = 0; j < kRegKeys; ++j) {
+            const bool p = l + 32 * j < n && hkey(key[j]) >= tau_key;
+            if (p) zp = df_add(zp, ex2((ckey_val(key[j]) - m) * c2));
+            const uint32_t bal = __ballot_sync(0xffffffffu, p);
+            if (p) sm.list[keep + __popc(bal & lt)] = key[j];
+            keep += __popc(bal);
+        }
+    } else if (C <= 4 && n <= 32 * kRegKeys) {
         // every search of every key at once: lists q >= C are empty (offset n)
         int o[4], mq[4];
 #pragma unroll
@@ -546,10 +604,13 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
         if (l == 0) {
             SPEC_TRACE_EV(11, n, keep, static_cast<int>(tc1 - tc0));
             SPEC_TRACE_EV(12, static_cast<int>(tc2 - tc1), static_cast<int>(tc3 - tc2), 0);
+            SPEC_TRACE_EV(22, static_cast<int>(tca - tc0), static_cast<int>(tcb - tc0), static_cast<int>(tc1 - tc0));
+            SPEC_TRACE_EV(23, static_cast<int>(tcu - tc0), 0, 0);
         }
 #endif
         if (acc) {
             if (A.diag) chain_diag(A, b, row, prob(ey), qy, Z.hi, 0.f);
+            if (l == 0) SPEC_TRACE_EV(19, b, row, 0);
             return row_job(A, b, row + 1, st, hint, 0, dl.yn);
         }
     }

@@ -48,16 +48,7 @@ struct TraceRec {
 static __device__ TraceRec* g_trace;
 static __device__ unsigned g_trace_cap;
 static __device__ unsigned g_trace_n;
-__device__ __forceinline__ void trace_ev(int ev, int a, int b, int c) {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    const unsigned i = atomicAdd(&g_trace_n, 1u);
-    if (g_trace && i < g_trace_cap) {
-        TraceRec r;
-        r.t = t; r.cta = blockIdx.x; r.ev = ev; r.a = a; r.b = b; r.c = c; r.d = 0;
-        g_trace[i] = r;
-    }
-}
+static __device__ void trace_ev(int ev, int a, int b, int c);
 #define SPEC_TRACE_EV(ev, a, b, c) ::spec::trace_ev((ev), (a), (b), (c))
 #define SPEC_TRACE_T(v) const long long v = clock64()
 #else
@@ -211,8 +202,28 @@ struct EngSmem {
     Job cur[kMaxOwn];            // combiner: the job in flight of each own slot
     QEnt q[kQ];
     int abort;                   // a wait in this CTA gave up
-    int pad[3];
+    unsigned trace_n;            // development trace builds: this CTA's record count
+    int pad[2];
 };
+
+#ifdef SPEC_TRACE
+// every CTA appends to its own share of the buffer through a counter in its
+// shared memory (no global atomic on the traced path); unused records stay
+// zero.  The engine's shared block sits at the start of dynamic shared memory.
+extern __shared__ __align__(128) unsigned char spec_trace_dyn[];
+__device__ __forceinline__ void trace_reset_cta() { reinterpret_cast<EngSmem*>(spec_trace_dyn)->trace_n = 0; }
+static __device__ void trace_ev(int ev, int a, int b, int c) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    const unsigned per = g_trace_cap / gridDim.x;
+    const unsigned i = atomicAdd_block(&reinterpret_cast<EngSmem*>(spec_trace_dyn)->trace_n, 1u);
+    if (g_trace && i < per) {
+        TraceRec r;
+        r.t = t; r.cta = blockIdx.x; r.ev = ev; r.a = a; r.b = b; r.c = c; r.d = 0;
+        g_trace[static_cast<size_t>(blockIdx.x) * per + i] = r;
+    }
+}
+#endif
 
 // ---------------------------------------------------------------------------
 // bounded waits
@@ -392,6 +403,46 @@ struct FnHooks {
 
 static_assert(kChunkUnit % (4 * 16 * kThreads) == 0, "a full stage is whole groups of four rounds");
 
+// Plain-load mode (tma = false: pinned host memory read in place, or rows
+// whose layout a bulk copy cannot take).  The consumers copy the chunks into
+// the ring themselves with asynchronous 16-byte copies (global -> shared, no
+// registers held), one chunk ahead: while a chunk is processed the next one
+// is in flight, so a CTA keeps two chunks outstanding on the link.  Bytes
+// past the last 16-byte multiple of a range, and ranges whose start is not
+// 16-byte aligned, are copied element by element when their chunk is taken.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// the 16-byte part of n elements of es bytes at src, into dst (async)
+__device__ __forceinline__ void copy_async(unsigned char* dst, const unsigned char* src, int n, int es) {
+    if (reinterpret_cast<uintptr_t>(src) & 15u) return;
+    const int nv = (n * es) >> 4;
+    const uint32_t d = smem_u32(dst);
+    for (int v = threadIdx.x; v < nv; v += kThreads) cp_async16(d + 16u * static_cast<uint32_t>(v), src + 16ll * v);
+}
+// the rest of it (everything when src is not 16-byte aligned), loaded now
+__device__ __forceinline__ void copy_rest(unsigned char* dst, const unsigned char* src, int n, int es) {
+    const int done = (reinterpret_cast<uintptr_t>(src) & 15u) ? 0 : (((n * es) >> 4) << 4) / es;
+    if (es == 4) {
+        for (int i = done + threadIdx.x; i < n; i += kThreads)
+            reinterpret_cast<uint32_t*>(dst)[i] = __ldg(reinterpret_cast<const uint32_t*>(src) + i);
+    } else {
+        for (int i = done + threadIdx.x; i < n; i += kThreads)
+            reinterpret_cast<uint16_t*>(dst)[i] = __ldg(reinterpret_cast<const unsigned short*>(src) + i);
+    }
+}
+// chunk cc of plan p into dst, asynchronously; one commit group
+__device__ __forceinline__ void chunk_async(const StreamPlan& p, int cc, unsigned char* dst) {
+    const int nn = min(p.ce, p.n - cc * p.ce);
+    copy_async(dst, p.src0 + static_cast<long long>(cc) * p.ce * p.es0, nn, p.es0);
+    if (p.src1) copy_async(dst + p.ce * p.es0, p.src1 + static_cast<long long>(cc) * p.ce * 4, nn, 4);
+    cp_async_commit();
+}
+
 // Wait for chunk `seq` (every consumer thread).  With tma = false the
 // consumers copy it from global memory themselves (the producer issues
 // nothing in that mode).
@@ -407,20 +458,16 @@ __device__ __forceinline__ bool take_chunk(const Pipe& P, uint32_t seq, bool tma
     }
     const int ne = min(p.ce, p.n - c * p.ce);
     unsigned char* sm = P.slot(s);
-    csync();   // every consumer is done with this stage's previous chunk
-    const unsigned char* g0 = p.src0 + static_cast<long long>(c) * p.ce * p.es0;
-    if (p.es0 == 4) {
-        for (int i = threadIdx.x; i < ne; i += kThreads)
-            reinterpret_cast<uint32_t*>(sm)[i] = reinterpret_cast<const uint32_t*>(g0)[i];
-    } else {
-        for (int i = threadIdx.x; i < ne; i += kThreads)
-            reinterpret_cast<uint16_t*>(sm)[i] = reinterpret_cast<const uint16_t*>(g0)[i];
-    }
-    if (p.src1) {
-        const float* g1 = reinterpret_cast<const float*>(p.src1) + static_cast<long long>(c) * p.ce;
-        float* d1 = reinterpret_cast<float*>(sm + p.ce * p.es0);
-        for (int i = threadIdx.x; i < ne; i += kThreads) d1[i] = g1[i];
-    }
+    // every consumer is done with the chunks before this one, so this stage
+    // and the next (the ring has at least two) are free
+    csync();
+    if (c == 0) chunk_async(p, 0, sm);
+    const bool ahead = c + 1 < p.nch && P.stages >= 2;
+    if (ahead) chunk_async(p, c + 1, P.slot(P.stage(seq + 1)));
+    copy_rest(sm, p.src0 + static_cast<long long>(c) * p.ce * p.es0, ne, p.es0);
+    if (p.src1) copy_rest(sm + p.ce * p.es0, p.src1 + static_cast<long long>(c) * p.ce * 4, ne, 4);
+    if (ahead) cp_async_wait<1>();
+    else cp_async_wait<0>();
     csync();
     return true;
 }
@@ -757,9 +804,21 @@ struct Engine {
     using Args = typename Op::Args;
     using OSmem = typename Op::Smem;
 
-    // dynamic shared memory: EngSmem | Op::Smem | partials (own slots x C) |
-    // staging (one partial) | ring (stages x chunk bytes) | kernel extras
-    __host__ __device__ static size_t op_off() { return (sizeof(EngSmem) + 127) & ~size_t(127); }
+    // The combiner warp's copy of the arguments.  The combine steps are
+    // separate (non-inlined) functions that reach the arguments through a
+    // reference; a reference to the kernel's parameter block is a generic
+    // pointer whose loads are slow (each a memory round trip, on the
+    // critical path of every row), while one into shared memory is not.
+    struct ArgsCopy {
+        Args a;
+        Workspace w;
+        Geo g;
+    };
+    // dynamic shared memory: EngSmem | ArgsCopy | Op::Smem | partials (own
+    // slots x C) | staging (one partial) | ring (stages x chunk bytes) |
+    // kernel extras
+    __host__ __device__ static size_t args_off() { return (sizeof(EngSmem) + 127) & ~size_t(127); }
+    __host__ __device__ static size_t op_off() { return (args_off() + sizeof(ArgsCopy) + 127) & ~size_t(127); }
     __host__ __device__ static size_t part_off() { return (op_off() + sizeof(OSmem) + 127) & ~size_t(127); }
     __host__ __device__ static size_t stage_off(int C, int own, int part_bytes) {
         return part_off() + static_cast<size_t>(own) * C * part_bytes;
@@ -779,6 +838,9 @@ struct Engine {
         unsigned char* ring = smem + ring_off(G.C, G.own, G.part_bytes);
         const int C = G.C;
         if (threadIdx.x == 0) {
+#ifdef SPEC_TRACE
+            trace_reset_cta();
+#endif
             for (int s = 0; s < G.stages; ++s) {
                 mbar_init(&es.full[s], 1);
                 mbar_init(&es.empty[s], kWarps);
@@ -793,6 +855,11 @@ struct Engine {
             fence_mbar_init();
         }
         Op::init_smem(A, G, os);
+        ArgsCopy& ac = *reinterpret_cast<ArgsCopy*>(smem + args_off());
+        static_assert(sizeof(Args) % 4 == 0 && sizeof(Workspace) % 4 == 0 && sizeof(Geo) % 4 == 0, "word copies");
+        for (int i = threadIdx.x; i < static_cast<int>(sizeof(Args) / 4); i += blockDim.x)
+            reinterpret_cast<uint32_t*>(&ac.a)[i] = reinterpret_cast<const uint32_t*>(&A)[i];
+        if (threadIdx.x == 0) { ac.w = W; ac.g = G; }
         __syncthreads();
         // every CTA's barriers exist before any CTA posts to them
         cluster_sync();
@@ -803,7 +870,7 @@ struct Engine {
         P.chunk = G.chunk;
         const bool tma = Op::tma(A);
         if (threadIdx.x >= kCombiner0) {
-            combiner(A, W, G, es, os, parts);
+            combiner(ac.a, ac.w, ac.g, es, os, parts);
         } else if (threadIdx.x >= kThreads) {
             if (threadIdx.x == kProducer) producer(A, W, G, es, P, tma);
         } else {

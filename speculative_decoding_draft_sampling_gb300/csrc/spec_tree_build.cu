@@ -11,12 +11,15 @@
 // probable tokens of q_d, so each depth row is reduced to its sorted top-M
 // list: one job per depth, in which every CTA of the cluster finds its
 // slice's top-M composite keys and the slot's leader merges them.  The
-// best-first enumeration then runs on the leader's combiner warp: each pop is
-// a warp-wide arg-max over the frontier; the popped entry is emitted and its
-// next sibling (same parent, next rank) and first child (rank 0 of the next
-// depth) join the frontier.  Every emitted entry's successors score no
-// higher than it (q <= 1), so pops come out in non-increasing Q and the first
-// `budget` pops are the best prefixes.  When a first child needs a depth
+// best-first enumeration then runs on the leader's combiner warp.  The
+// frontier is kept per emitted node: every node carries the head of its
+// children not emitted yet (the next rank of the next depth's list, with its
+// Q), so the frontier is the set of heads, and each pop -- a warp-wide
+// arg-max over the nodes' heads -- emits one head as a new node, advances its
+// parent's head to the next rank and gives the new node its first head (rank
+// 0 of the next depth).  A node's successors score no higher than it (q <=
+// 1), so pops come out in non-increasing Q and the first `budget` pops are
+// the best prefixes.  When a first child needs a depth
 // whose list is not built yet, the enumeration saves its state to the
 // workspace and posts that depth's row job; depth rows past the last one the
 // enumeration consults are never read.
@@ -25,16 +28,17 @@
 
 namespace spec {
 
-struct Ent {                 // a frontier entry or an emitted node
+struct Ent {                 // an emitted node and the head of its children
     double Q;
-    double pq;               // the parent's Q (a sibling's Q is pq times its probability)
+    double hq;               // Q of its next child not emitted yet (< 0: none, or not known yet)
     unsigned long long ph, pl;   // rank path, one byte per depth, depth 1 in the top byte
-    int depth, parent, rank, pad;
+    int depth, parent, rank;
+    int next;                // the rank of that child in the next depth's list
 };
 static_assert(sizeof(Ent) == 48, "Ent is 48 bytes");
 
 struct EnumHdr {
-    int count, npend, want, avail;
+    int count, unused, want, avail;
     int status, pad[3];
     int len[24];             // list length per depth (index 1..L)
 };
@@ -68,37 +72,29 @@ __device__ __forceinline__ void topm_hint_store(Ctrl* ctrl, uint32_t h, int V, i
            make_uint4(kPersistTagTopm, h, static_cast<uint32_t>(V), static_cast<uint32_t>(M)));
 }
 
-// per-request workspace: [EnumHdr][lists L*M (tok, prob bits)][nodes N][pending 2N+2]
+// per-request workspace: [EnumHdr][lists L*M (tok, prob bits)][nodes N]
 __host__ __device__ inline size_t build_lists_off() { return 128; }
 __host__ __device__ inline size_t build_nodes_off(int N, int L) {
     return (build_lists_off() + static_cast<size_t>(L) * (N - 1) * 8 + 127) & ~static_cast<size_t>(127);
 }
-__host__ __device__ inline size_t build_pend_off(int N, int L) {
-    return build_nodes_off(N, L) + static_cast<size_t>(N) * sizeof(Ent);
-}
 size_t build_extra_bytes(int N, int L) {
-    return (build_pend_off(N, L) + static_cast<size_t>(2 * N + 2) * sizeof(Ent) + 127) & ~static_cast<size_t>(127);
+    return (build_nodes_off(N, L) + static_cast<size_t>(N) * sizeof(Ent) + 127) & ~static_cast<size_t>(127);
 }
-// combiner shared memory after the partial areas: depth lists, nodes and pending
+// combiner shared memory after the partial areas: depth lists and nodes
 __host__ __device__ inline size_t enum_smem_bytes(int N, int L) {
     return ((static_cast<size_t>(L) * (N - 1) * 8 + 15) & ~static_cast<size_t>(15)) +
-           static_cast<size_t>(3 * N + 2) * sizeof(Ent);
+           static_cast<size_t>(N) * sizeof(Ent);
 }
 
-__device__ __forceinline__ bool ent_before(const Ent& a, const Ent& b) {
-    if (a.Q != b.Q) return a.Q > b.Q;
-    if (a.depth != b.depth) return a.depth < b.depth;
-    if (a.ph != b.ph) return a.ph < b.ph;
-    return a.pl < b.pl;
-}
-__device__ __forceinline__ void path_set(Ent& e, int d, int r) {
+// rank path with byte d set to r (depth 1 in the top byte of ph)
+__device__ __forceinline__ void path_with(unsigned long long& ph, unsigned long long& pl, int d, int r) {
     const unsigned long long v = static_cast<unsigned long long>(r & 0xff);
     if (d <= 8) {
         const int sh = 8 * (8 - d);
-        e.ph = (e.ph & ~(0xffull << sh)) | (v << sh);
+        ph = (ph & ~(0xffull << sh)) | (v << sh);
     } else {
         const int sh = 8 * (16 - d);
-        e.pl = (e.pl & ~(0xffull << sh)) | (v << sh);
+        pl = (pl & ~(0xffull << sh)) | (v << sh);
     }
 }
 
@@ -108,8 +104,7 @@ struct EnumView {
     int* ltok;
     float* lprob;
     Ent* nodes;
-    Ent* pend;
-    uint32_t a_lprob, a_nodes, a_pend;   // the same, as shared-window addresses
+    uint32_t a_lprob, a_nodes;   // the same, as shared-window addresses
 };
 
 // Ent records through shared-window addresses (explicit shared loads and
@@ -123,28 +118,14 @@ __device__ __forceinline__ uint64_t ldsv_u64(uint32_t a) {
 __device__ __forceinline__ void stsv_u64(uint32_t a, uint64_t v) {
     asm volatile("st.shared.u64 [%0], %1;" :: "r"(a), "l"(v) : "memory");
 }
-__device__ __forceinline__ Ent ld_ent(uint32_t a) {
-    Ent e;
-    uint64_t* w = reinterpret_cast<uint64_t*>(&e);
-#pragma unroll
-    for (int i = 0; i < static_cast<int>(sizeof(Ent) / 8); ++i) w[i] = ldsv_u64(a + 8u * i);
-    return e;
-}
-__device__ __forceinline__ void st_ent(uint32_t a, const Ent& e) {
-    const uint64_t* w = reinterpret_cast<const uint64_t*>(&e);
-#pragma unroll
-    for (int i = 0; i < static_cast<int>(sizeof(Ent) / 8); ++i) stsv_u64(a + 8u * i, w[i]);
-}
 __device__ __forceinline__ EnumView enum_view(unsigned char* base, int N, int L) {
     EnumView v;
     const int LM = L * (N - 1);
     v.ltok = reinterpret_cast<int*>(base);
     v.lprob = reinterpret_cast<float*>(base + static_cast<size_t>(LM) * 4);
     v.nodes = reinterpret_cast<Ent*>(base + ((static_cast<size_t>(LM) * 8 + 15) & ~static_cast<size_t>(15)));
-    v.pend = v.nodes + N;
     v.a_lprob = smem_u32(v.lprob);
     v.a_nodes = smem_u32(v.nodes);
-    v.a_pend = smem_u32(v.pend);
     return v;
 }
 
@@ -187,55 +168,85 @@ __device__ void build_finalize(const BuildArgs& A, const EnumView& ev, int b, in
     __syncwarp();
 }
 
-// warp-wide pop of the best frontier entry: its index in every lane
-// The frontier's best entry (ent_before order) on the combiner warp, in two
-// parts: each lane's best over its slots (l, l + 32, ...), kept in registers
-// between pops and recomputed only by lanes whose slots changed; then the
-// warp reduction on an order-preserving 64-bit key of Q, and -- only among
-// exact ties -- on depth and on the rank path.
-struct LaneBest {
-    int j, d;
-    unsigned long long q, ph, pl;
-};
-__device__ __forceinline__ unsigned long long q_order_key(unsigned long long qb) {
+// The frontier's best head, on the combiner warp.  Node n belongs to lane
+// n % 32; each lane keeps the best head among its nodes in registers and
+// recomputes it only when one of its nodes changed.  Heads are ordered by Q
+// (descending), then by the child's depth (ascending), then by the child's
+// rank path (ascending); Q is compared through an order-preserving 64-bit key
+// of the double, and the rest only among exact ties.
+__device__ __forceinline__ unsigned long long q_order_key(double q) {
+    unsigned long long qb = static_cast<unsigned long long>(__double_as_longlong(q));
     if ((qb << 1) == 0ull) qb = 0ull;                              // -0 as +0
     return (qb >> 63) ? ~qb : (qb | 0x8000000000000000ull);
 }
-__device__ __forceinline__ void lane_best(uint32_t a_pend, int np, LaneBest& b) {
+// head key of a node: 0 when it has no head
+__device__ __forceinline__ unsigned long long head_key(uint32_t a_node) {
+    const double hq = __longlong_as_double(static_cast<long long>(ldsv_u64(a_node + offsetof(Ent, hq))));
+    return hq >= 0.0 ? q_order_key(hq) : 0ull;
+}
+// the child path and depth a head stands for
+__device__ __forceinline__ void head_path(uint32_t a_node, int& d, unsigned long long& ph, unsigned long long& pl) {
+    const uint64_t dp = ldsv_u64(a_node + offsetof(Ent, depth));     // depth, parent
+    const uint64_t rn = ldsv_u64(a_node + offsetof(Ent, rank));      // rank, next
+    ph = ldsv_u64(a_node + offsetof(Ent, ph));
+    pl = ldsv_u64(a_node + offsetof(Ent, pl));
+    d = static_cast<int>(static_cast<uint32_t>(dp)) + 1;
+    path_with(ph, pl, d, static_cast<int>(static_cast<uint32_t>(rn >> 32)));
+}
+// exact-tie order of two heads with equal Q keys: depth, then rank path
+__device__ __noinline__ bool head_before_tie(uint32_t a1, uint32_t a2) {
+    int d1, d2;
+    unsigned long long h1, l1, h2, l2;
+    head_path(a1, d1, h1, l1);
+    head_path(a2, d2, h2, l2);
+    if (d1 != d2) return d1 < d2;
+    if (h1 != h2) return h1 < h2;
+    return l1 < l2;
+}
+struct LaneBest {
+    int j;                   // node, -1: none
+    unsigned long long k;    // its head key
+};
+__device__ __forceinline__ void lane_best(uint32_t a_nodes, int count, LaneBest& b) {
     const int l = threadIdx.x & 31;
-    b.j = -1; b.d = 0; b.q = 0; b.ph = 0; b.pl = 0;
-    for (int j = l; j < np; j += 32) {
-        const uint32_t a = a_pend + static_cast<uint32_t>(j * sizeof(Ent));
-        const unsigned long long q = q_order_key(ldsv_u64(a + offsetof(Ent, Q)));
-        const int d = static_cast<int>(static_cast<uint32_t>(ldsv_u64(a + offsetof(Ent, depth))));
-        const unsigned long long ph = ldsv_u64(a + offsetof(Ent, ph)), pl = ldsv_u64(a + offsetof(Ent, pl));
-        const bool take = b.j < 0 || q > b.q ||
-                          (q == b.q && (d < b.d || (d == b.d && (ph < b.ph || (ph == b.ph && pl < b.pl)))));
-        if (take) { b.j = j; b.q = q; b.d = d; b.ph = ph; b.pl = pl; }
+    constexpr uint32_t kE = static_cast<uint32_t>(sizeof(Ent));
+    b.j = -1; b.k = 0;
+    for (int j = l; j < count; j += 32) {
+        const unsigned long long k = head_key(a_nodes + kE * j);
+        if (k == 0ull) continue;
+        if (b.j < 0 || k > b.k || (k == b.k && head_before_tie(a_nodes + kE * j, a_nodes + kE * b.j))) {
+            b.j = j;
+            b.k = k;
+        }
     }
 }
-__device__ __forceinline__ int warp_best(const LaneBest& b) {
+__device__ __forceinline__ int warp_best(const LaneBest& b, uint32_t a_nodes) {
     const int l = threadIdx.x & 31;
     uint32_t cand = __ballot_sync(0xffffffffu, b.j >= 0);
     if (!cand) return -1;
-    auto keep_max = [&](uint32_t v) {
+    {
+        const uint32_t hi = static_cast<uint32_t>(b.k >> 32);
+        const uint32_t m = __reduce_max_sync(0xffffffffu, b.j >= 0 ? hi : 0u);
+        cand = __ballot_sync(0xffffffffu, b.j >= 0 && hi == m);
+    }
+    if (__popc(cand) > 1) {
         const bool in = (cand >> l) & 1u;
-        const uint32_t m = __reduce_max_sync(0xffffffffu, in ? v : 0u);
-        cand = __ballot_sync(0xffffffffu, in && v == m);
-    };
-    auto keep_min = [&](uint32_t v) {
-        const bool in = (cand >> l) & 1u;
-        const uint32_t m = __reduce_min_sync(0xffffffffu, in ? v : 0xffffffffu);
-        cand = __ballot_sync(0xffffffffu, in && v == m);
-    };
-    keep_max(static_cast<uint32_t>(b.q >> 32));
-    if (__popc(cand) > 1) keep_max(static_cast<uint32_t>(b.q));
-    if (__popc(cand) > 1) keep_min(static_cast<uint32_t>(b.d));
-    if (__popc(cand) > 1) keep_min(static_cast<uint32_t>(b.ph >> 32));
-    if (__popc(cand) > 1) keep_min(static_cast<uint32_t>(b.ph));
-    if (__popc(cand) > 1) keep_min(static_cast<uint32_t>(b.pl >> 32));
-    if (__popc(cand) > 1) keep_min(static_cast<uint32_t>(b.pl));
-    return __shfl_sync(0xffffffffu, b.j, __ffs(cand) - 1);
+        const uint32_t lo = static_cast<uint32_t>(b.k);
+        const uint32_t m = __reduce_max_sync(0xffffffffu, in ? lo : 0u);
+        cand = __ballot_sync(0xffffffffu, in && lo == m);
+    }
+    int best = __shfl_sync(0xffffffffu, b.j, __ffs(cand) - 1);
+    if (__popc(cand) > 1) {
+        // exact ties in Q: the order on depth and rank path, over the tied lanes
+        constexpr uint32_t kE = static_cast<uint32_t>(sizeof(Ent));
+        cand &= cand - 1u;
+        while (cand) {
+            const int j = __shfl_sync(0xffffffffu, b.j, __ffs(cand) - 1);
+            if (head_before_tie(a_nodes + kE * j, a_nodes + kE * best)) best = j;
+            cand &= cand - 1u;
+        }
+    }
+    return best;
 }
 
 // The best-first enumeration from the saved state in `eh` / `ev` (combiner
@@ -244,113 +255,97 @@ __device__ __forceinline__ int warp_best(const LaneBest& b) {
 __device__ int enumerate_w(const BuildArgs& A, EnumHdr& eh, const EnumView& ev) {
     const int l = threadIdx.x & 31;
     const int N = A.N, M = A.M, L = A.L;
-    int count = eh.count, np = eh.npend, want = eh.want;
+    int count = eh.count, want = eh.want;
     const int avail = eh.avail;
     const int lenl = l <= L ? eh.len[l] : 0;          // lane d: depth d's list length
     int need = 0;
     constexpr uint32_t kE = static_cast<uint32_t>(sizeof(Ent));
     // scalar copies: the explicit shared accesses below clobber memory, and a
     // view reached through a reference would be reloaded after every one
-    const uint32_t a_lprob = ev.a_lprob, a_nodes = ev.a_nodes, a_pend = ev.a_pend;
+    const uint32_t a_lprob = ev.a_lprob, a_nodes = ev.a_nodes;
     auto lprob_at = [a_lprob](int i) { return __uint_as_float(lds_u32(a_lprob + 4u * static_cast<uint32_t>(i))); };
+    auto st_f64 = [](uint32_t a, double v) { stsv_u64(a, static_cast<uint64_t>(__double_as_longlong(v))); };
+    auto ld_f64 = [](uint32_t a) { return __longlong_as_double(static_cast<long long>(ldsv_u64(a))); };
 #ifdef SPEC_TRACE
     long long t_best = 0;
     const long long t_all = clock64();
 #endif
-    // a node of an earlier call that still wants its first child
+    // a node of an earlier call whose first head waited for its depth's list
     if (want >= 0 && count < N) {
-        const Ent w = ld_ent(a_nodes + kE * want);
-        const int dd = w.depth + 1;
+        const uint32_t aw = a_nodes + kE * want;
+        const int dd = static_cast<int>(static_cast<uint32_t>(ldsv_u64(aw + offsetof(Ent, depth)))) + 1;
         if (dd <= L) {
             if (dd > avail) {
                 need = dd;
-            } else if (__shfl_sync(0xffffffffu, lenl, dd) > 0) {
-                const double q0 = static_cast<double>(lprob_at((dd - 1) * M));
-                if (l == 0) {
-                    Ent c = w;
-                    c.depth = dd; c.parent = want; c.rank = 0;
-                    path_set(c, dd, 0);
-                    c.Q = w.Q * q0;
-                    c.pq = w.Q;
-                    st_ent(a_pend + kE * np, c);
-                }
-                ++np;
+            } else {
+                const bool has = __shfl_sync(0xffffffffu, lenl, dd) > 0;
+                const double hq = has ? ld_f64(aw + offsetof(Ent, Q)) * static_cast<double>(lprob_at((dd - 1) * M))
+                                      : -1.0;
+                if (l == (want & 31)) st_f64(aw + offsetof(Ent, hq), hq);
             }
         }
         if (!need) want = -1;
     }
+    __syncwarp();
     LaneBest lb;
-    lb.j = -1;
-    bool dirty = true;
-    while (!need && count < N && np > 0) {
-        __syncwarp();
+    lane_best(a_nodes, count, lb);
+    while (!need && count < N) {
 #ifdef SPEC_TRACE
         const long long tq0 = clock64();
 #endif
-        if (dirty) lane_best(a_pend, np, lb);
-        const int best = warp_best(lb);
+        const int v = warp_best(lb, a_nodes);
 #ifdef SPEC_TRACE
         t_best += clock64() - tq0;
 #endif
-        // the popped entry, the last entry (moves into its slot), and the
-        // probabilities of the popped entry's next sibling and first child:
-        // independent loads, independent products
-        const Ent c = ld_ent(a_pend + kE * best);
-        const Ent last = ld_ent(a_pend + kE * (np - 1));
-        const bool sib = c.rank + 1 < __shfl_sync(0xffffffffu, lenl, c.depth);
-        const int dd = c.depth + 1;
-        const bool deeper = dd <= L;
-        const bool have_list = deeper && dd <= avail && __shfl_sync(0xffffffffu, lenl, deeper ? dd : 0) > 0;
-        const float qs = lprob_at((c.depth - 1) * M + (sib ? c.rank + 1 : c.rank));
-        const float q0 = lprob_at(have_list ? (dd - 1) * M : 0);
-        const double sQ = c.pq * static_cast<double>(qs);
-        const double cQ = c.Q * static_cast<double>(q0);
-        __syncwarp();
+        if (v < 0) break;
+        // the head of v becomes node c: its Q, depth, rank and path; v's
+        // head moves to its next rank, c's first head is rank 0 of the next
+        // depth (independent loads, independent products)
+        const uint32_t av = a_nodes + kE * v;
+        const double Qv = ld_f64(av + offsetof(Ent, Q));
+        const double Qc = ld_f64(av + offsetof(Ent, hq));
+        const uint64_t dp = ldsv_u64(av + offsetof(Ent, depth));
+        const uint64_t rn = ldsv_u64(av + offsetof(Ent, rank));
+        unsigned long long ph = ldsv_u64(av + offsetof(Ent, ph)), pl = ldsv_u64(av + offsetof(Ent, pl));
+        const int d = static_cast<int>(static_cast<uint32_t>(dp)) + 1;
+        const int r = static_cast<int>(static_cast<uint32_t>(rn >> 32));
+        const bool sib = r + 1 < __shfl_sync(0xffffffffu, lenl, d);
+        const bool deeper = d + 1 <= L;
+        const bool have_list = deeper && d + 1 <= avail && __shfl_sync(0xffffffffu, lenl, deeper ? d + 1 : 0) > 0;
+        const float qs = lprob_at((d - 1) * M + (sib ? r + 1 : r));
+        const float q0 = lprob_at(have_list ? d * M : 0);
+        const double hv = sib ? Qv * static_cast<double>(qs) : -1.0;
+        const double hc = have_list ? Qc * static_cast<double>(q0) : -1.0;
+        path_with(ph, pl, d, r);
         const int nid = count++;
-        const int removed = np - 1;
-        if (l == 0) {
-            st_ent(a_pend + kE * best, last);
-            st_ent(a_nodes + kE * nid, c);
+        const uint32_t ac = a_nodes + kE * nid;
+        if (l == (v & 31)) {
+            st_f64(av + offsetof(Ent, hq), hv);
+            stsv_u64(av + offsetof(Ent, rank), (static_cast<uint64_t>(r + 1) << 32) | static_cast<uint32_t>(rn));
         }
-        --np;
-        int slot_s = -1, slot_c = -1;
-        if (sib) {
-            // next sibling: same parent, next rank of the same depth list
-            if (l == 0) {
-                Ent s2 = c;
-                s2.rank = c.rank + 1;
-                path_set(s2, c.depth, c.rank + 1);
-                s2.Q = sQ;
-                st_ent(a_pend + kE * np, s2);
-            }
-            slot_s = np++;
+        if (l == (nid & 31)) {
+            st_f64(ac + offsetof(Ent, Q), Qc);
+            st_f64(ac + offsetof(Ent, hq), hc);
+            stsv_u64(ac + offsetof(Ent, ph), ph);
+            stsv_u64(ac + offsetof(Ent, pl), pl);
+            stsv_u64(ac + offsetof(Ent, depth), (static_cast<uint64_t>(static_cast<uint32_t>(v)) << 32) |
+                                                    static_cast<uint32_t>(d));
+            stsv_u64(ac + offsetof(Ent, rank), static_cast<uint32_t>(r));   // next = 0
         }
-        if (deeper && count < N) {
-            if (dd > avail) {
-                // the child needs a depth not read yet: stop, and resume here
-                want = nid;
-                need = dd;
-            } else if (have_list) {
-                if (l == 0) {
-                    Ent ch = c;
-                    ch.depth = dd; ch.parent = nid; ch.rank = 0;
-                    path_set(ch, dd, 0);
-                    ch.Q = cQ;
-                    ch.pq = c.Q;
-                    st_ent(a_pend + kE * np, ch);
-                }
-                slot_c = np++;
-            }
+        if (deeper && count < N && d + 1 > avail) {
+            // c's first head needs a depth not read yet: stop, and resume here
+            want = nid;
+            need = d + 1;
         }
-        // lanes whose slots changed recompute their best
-        dirty = l == (best & 31) || l == (removed & 31) || (slot_s >= 0 && l == (slot_s & 31)) ||
-                (slot_c >= 0 && l == (slot_c & 31));
+        // the lanes whose nodes changed recompute their best
+        if (l == (v & 31) || l == (nid & 31)) lane_best(a_nodes, count, lb);
+        __syncwarp();
     }
 #ifdef SPEC_TRACE
-    if (l == 0) SPEC_TRACE_EV(16, static_cast<int>(t_best), static_cast<int>(clock64() - t_all), np);
+    if (l == 0) SPEC_TRACE_EV(16, static_cast<int>(t_best), static_cast<int>(clock64() - t_all), count);
 #endif
     __syncwarp();
-    if (l == 0) { eh.count = count; eh.npend = np; eh.want = want; }
+    if (l == 0) { eh.count = count; eh.want = want; }
     __syncwarp();
     return need;
 }
@@ -362,14 +357,11 @@ __device__ void enum_save(const BuildArgs& A, int b, const EnumHdr& eh, const En
     const int N = A.N, M = A.M, L = A.L;
     unsigned char* ex = A.E.W.extra + static_cast<size_t>(b) * A.E.W.extra_stride;
     int* gl = reinterpret_cast<int*>(ex + build_lists_off());
-    const int nc = eh.count, np = eh.npend;
+    const int nc = eh.count;
     constexpr int kW = static_cast<int>(sizeof(Ent) / 8);
     for (int i = l; i < nc * kW; i += 32)
         __stcg(reinterpret_cast<unsigned long long*>(ex + build_nodes_off(N, L)) + i,
                reinterpret_cast<const unsigned long long*>(ev.nodes)[i]);
-    for (int i = l; i < np * kW; i += 32)
-        __stcg(reinterpret_cast<unsigned long long*>(ex + build_pend_off(N, L)) + i,
-               reinterpret_cast<const unsigned long long*>(ev.pend)[i]);
     for (int i = first_list * M + l; i < eh.avail * M; i += 32) {
         __stcg(gl + 2 * i, ev.ltok[i]);
         __stcg(gl + 2 * i + 1, __float_as_int(ev.lprob[i]));
@@ -386,14 +378,11 @@ __device__ void enum_load(const BuildArgs& A, int b, EnumHdr& eh, const EnumView
     for (int i = l; i < static_cast<int>(sizeof(EnumHdr) / 4); i += 32)
         reinterpret_cast<int*>(&eh)[i] = __ldcg(reinterpret_cast<const int*>(ex) + i);
     __syncwarp();
-    const int nc = eh.count, np = eh.npend;
+    const int nc = eh.count;
     constexpr int kW = static_cast<int>(sizeof(Ent) / 8);
     for (int i = l; i < nc * kW; i += 32)
         reinterpret_cast<unsigned long long*>(ev.nodes)[i] =
             __ldcg(reinterpret_cast<const unsigned long long*>(ex + build_nodes_off(N, L)) + i);
-    for (int i = l; i < np * kW; i += 32)
-        reinterpret_cast<unsigned long long*>(ev.pend)[i] =
-            __ldcg(reinterpret_cast<const unsigned long long*>(ex + build_pend_off(N, L)) + i);
     for (int i = l; i < eh.avail * M; i += 32) {
         ev.ltok[i] = __ldcg(gl + 2 * i);
         ev.lprob[i] = __int_as_float(__ldcg(gl + 2 * i + 1));
@@ -436,10 +425,10 @@ struct BuildOp {
         EnumHdr& eh = sm.eh;
         if (l == 0) {
             EnumHdr h{};
-            h.count = 1; h.npend = 0; h.want = 0; h.avail = 0; h.status = 0;
+            h.count = 1; h.want = 0; h.avail = 0; h.status = 0;
             eh = h;
             Ent root{};
-            root.Q = 1.0; root.depth = 0; root.parent = -1; root.rank = -1;
+            root.Q = 1.0; root.hq = -1.0; root.depth = 0; root.parent = -1; root.rank = -1; root.next = 0;
             ev.nodes[0] = root;
         }
         __syncwarp();

@@ -101,3 +101,14 @@ def test_shape_limits_rejected_on_host(lib):
     assert lib.spec_verify_tree(1, 0, 0, 10, 1, 1, 1, 2, 8193, 10, 4, 1, 1, 1, 1, 16, 1 << 30, None) == 2
     assert b"N > 8192" in lib.spec_last_error()
     assert lib.spec_tree_build(1, 10, 10, 2, 4, 10, 257, 1, 1, 1, 1, 1, 1, 1, 16, 1 << 30, None) == 2
+
+
+def test_binding_refuses_unpinned_host_tensors(lib):
+    """Host tensors reach the kernels only when pinned (read in place through
+    the device mapping); an ordinary host tensor is refused before the call."""
+    import torch
+    t = torch.zeros(1, 1, 8)
+    with pytest.raises(sv.SpecError, match="pinned host tensor"):
+        sv.verify_chain(t, torch.zeros(1, 0, 8), torch.zeros(1, 0, dtype=torch.int32), torch.zeros(1, 1), 1.0, 0)
+    with pytest.raises(sv.SpecError, match="pinned host tensor"):
+        sv.tree_build(torch.zeros(1, 2, 8), 4)

@@ -67,7 +67,7 @@ CASES = [
 
 
 @pytest.mark.parametrize("name,over,seed_off", CASES)
-@pytest.mark.parametrize("slices", [0, 1, 3])
+@pytest.mark.parametrize("slices", [0, 1, 2, 3])
 def test_chain_parity(name, over, seed_off, slices):
     sv.set_tuning(slices, 0)
     w = workloads.make_chain(name, device=DEV, seed=workloads.seed_of(name) + 17 * seed_off, **over)
