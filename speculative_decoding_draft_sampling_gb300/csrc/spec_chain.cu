@@ -62,6 +62,8 @@ struct ChainSmem {
     float2 ws2[kWarps];
     uint32_t wb[kWarps];
     uint32_t last_hint;               // combiner: filter hint from this CTA's latest top-k row
+    float tau_prev;                   // combiner: the k-th value of that row
+    int tau_ok;                       // tau_prev holds one
     int nsel;                         // consumers: keys a slice reports
 };
 
@@ -580,13 +582,23 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
         j.depth = job.depth;
         return j;
     }
-    // the next rows' filter hint (and, persisted, the next call's)
-    const uint32_t hint = hint_from(tau, m, SPEC_HINT_MARGIN);
+    // the next rows' filter hint (and, persisted, the next call's) -- only
+    // while the rows keep their k-th value: this row's hint (if it had one)
+    // sat less than the row's max-to-tau gap below tau, else tau moved less
+    // than half that gap from the previous row this combiner saw.  Rows whose
+    // scale or offset moves from row to row get no hint (their slices start
+    // from a certified bound instead), so a stale hint costs no second pass.
+    const float gap = m - tau;
+    const bool steady = job.hint != 0u ? key_to_thr(job.hint) >= tau - gap
+                                       : (sm.tau_ok && fabsf(tau - sm.tau_prev) <= 0.5f * gap);
+    const uint32_t hint = steady ? hint_from(tau, m, SPEC_HINT_MARGIN) : 0u;
     if (l == 0) {
         sm.last_hint = hint;
+        sm.tau_prev = tau;
+        sm.tau_ok = tau == tau && tau > -kInf && m < kInf;
         // for the next call's first rows, with a wider margin (another call's
         // rows may sit lower); one 16-byte store
-        const uint32_t hw = hint_from(tau, m, 0.5f);
+        const uint32_t hw = steady ? hint_from(tau, m, 0.5f) : 0u;
         __stcg(reinterpret_cast<uint4*>(A.E.W.ctrl->persist),
                make_uint4(kPersistTag, hw, static_cast<uint32_t>(A.V), static_cast<uint32_t>(A.top_k)));
     }
@@ -893,6 +905,83 @@ __device__ int slice_sort_trim(const uint64_t* src, int n, uint64_t& F, int k, u
     return lo;
 }
 
+// The inverse CDF of a draw inside this CTA's slice (a RESCAN job; all
+// consumers): the smallest x with C(x) > t, C the inclusive prefix of the
+// weights in ascending x (residual [e / Z - q]_+ when aux2 == 1, else e), in
+// float-float; if rounding leaves no crossing, the last x with a positive
+// weight (or the slice start).  The slice streams through the ring like any
+// row; each chunk is scanned in shared memory with every thread on a run of
+// consecutive elements: the run's sum, a block exclusive scan, and the one
+// thread whose run crosses t walks it again.  Chunks after the crossing are
+// released unread.  Returns kIcdfDead when a chunk wait gave up.
+constexpr int kIcdfDead = -0x7ffffff0;
+template <class E>
+__device__ int consume_icdf(const ChainArgs& A, const Pipe& P, uint32_t& seq, const StreamPlan& p, bool tma, int x0,
+                            const Job& j, ChainSmem& sm) {
+    const float m = j.f[0], c2 = A.c2, invZ = j.f[1];
+    const float thr = j.hint ? key_to_thr(j.hint) : -kInf;
+    const dfloat t{j.f[2], j.f[3]};
+    const bool resid = j.aux2 == 1;
+    bool dead = false;
+    int found = 0x7fffffff, last_pos = -1;
+    dfloat base = df_make(0.f);
+    for (int c = 0; c < p.nch; ++c, ++seq) {
+        const bool have = take_chunk(P, seq, tma, dead, p, c);
+        // CTA-uniform (the barriers below): a warp whose wait gave up
+        // contributes nothing
+        if (found == 0x7fffffff) {
+            const unsigned char* sm_l = P.slot(P.stage(seq));
+            const float* sm_q = reinterpret_cast<const float*>(sm_l + p.ce * E::kBytes);
+            const int ne = min(p.ce, p.n - c * p.ce);
+            // bytes past the 16-byte-multiple prefix were not copied by TMA
+            const int l_in = tma ? ((ne * E::kBytes) & ~15) / E::kBytes : ne;
+            const int q_in = tma ? ((ne * 4) & ~15) / 4 : ne;
+            const float* gq = resid ? reinterpret_cast<const float*>(p.src1) + static_cast<long long>(c) * p.ce : nullptr;
+            auto weight = [&](int i) -> float {
+                const float lv = i < l_in ? E::load(sm_l, i) : E::load(p.src0, static_cast<long long>(c) * p.ce + i);
+                const float e = lv >= thr ? ex2((lv - m) * c2) : 0.f;
+                if (!resid) return e;
+                const float qv = i < q_in ? sm_q[i] : gq[i];
+                const float d = e * invZ - qv;
+                return d > 0.f ? d : 0.f;
+            };
+            const int per = (ne + kThreads - 1) / kThreads;
+            const int i0 = threadIdx.x * per, i1 = have ? min(ne, i0 + per) : i0;
+            dfloat loc = df_make(0.f);
+            int lp = -1;
+            for (int i = i0; i < i1; ++i) {
+                const float w = weight(i);
+                loc = df_add(loc, w);
+                if (w > 0.f) lp = i;
+            }
+            dfloat tot;
+            const dfloat c0 = df_add(base, block_exscan_df(loc, sm.red2, tot));
+            int mine = 0x7fffffff;
+            if (loc.hi > 0.f && df_gt(df_add(c0, loc), t)) {
+                dfloat cc = c0;
+                for (int i = i0; i < i1; ++i) {
+                    const float w = weight(i);
+                    cc = df_add(cc, w);
+                    if (w > 0.f && df_gt(cc, t)) { mine = i; break; }
+                }
+            }
+            if (threadIdx.x == 0) { sm.ired[0] = 0x7fffffff; sm.ired[1] = -1; }
+            csync();
+            if (mine != 0x7fffffff) atomicMin(&sm.ired[0], mine);
+            if (lp >= 0) atomicMax(&sm.ired[1], lp);
+            csync();
+            const int cx0 = x0 + c * p.ce;
+            if (sm.ired[0] != 0x7fffffff) found = cx0 + sm.ired[0];
+            if (sm.ired[1] >= 0) last_pos = cx0 + sm.ired[1];
+            base = df_add(base, tot);
+            csync();   // ired is read before the next chunk resets it
+        }
+        release_chunk(P, seq, tma, dead);
+    }
+    if (csync_or(dead)) return kIcdfDead;
+    return found != 0x7fffffff ? found : (last_pos >= 0 ? last_pos : x0);
+}
+
 // ---------------------------------------------------------------------------
 // the op
 // ---------------------------------------------------------------------------
@@ -917,6 +1006,8 @@ struct ChainOp {
                     h = ps.y;
             }
             sm.last_hint = h;
+            sm.tau_prev = 0.f;
+            sm.tau_ok = 0;
         }
     }
     __device__ static Job first(const Args& A, const Geo&, int b, Smem& sm) {
@@ -931,6 +1022,11 @@ struct ChainOp {
                 return plan_single(chain_lrow<E>(A, j.b, j.row), E::kBytes, x0, x1, G.chunk);
             case kResid:
                 return plan_dual(chain_lrow<E>(A, j.b, j.row), E::kBytes, chain_qrow(A, j.b, j.row), x0, x1, G.chunk);
+            case kRescan:
+                // the target CTA streams its slice (logits, and q for residual weights)
+                return j.aux2 == 1 ? plan_dual(chain_lrow<E>(A, j.b, j.row), E::kBytes, chain_qrow(A, j.b, j.row), x0,
+                                               x1, G.chunk)
+                                   : plan_single(chain_lrow<E>(A, j.b, j.row), E::kBytes, x0, x1, G.chunk);
             default:
                 return plan_none();
         }
@@ -1058,28 +1154,9 @@ struct ChainOp {
                 ph->sum2 = make_float2(psum.hi, psum.lo);
             }
         } else if (j.kind == kRescan) {
-            // the inverse CDF inside this slice, reading the row from global memory
-            const void* lrow = chain_lrow<E>(A, b, row);
-            const float m = j.f[0], c2 = A.c2, invZ = j.f[1];
-            const float thr = j.hint ? key_to_thr(j.hint) : -kInf;
-            const dfloat t{j.f[2], j.f[3]};
-            int x;
-            if (j.aux2 == 1) {
-                const float* qrow = chain_qrow(A, b, row);
-                auto wr = [&](int xx) -> float {
-                    const float lv = E::load(lrow, xx);
-                    const float w = lv >= thr ? ex2((lv - m) * c2) : 0.f;
-                    const float d = w * invZ - qrow[xx];
-                    return d > 0.f ? d : 0.f;
-                };
-                x = cta_icdf(x0, x1, t, wr, sm.red2, sm.ired);
-            } else {
-                auto wp = [&](int xx) -> float {
-                    const float lv = E::load(lrow, xx);
-                    return lv >= thr ? ex2((lv - m) * c2) : 0.f;
-                };
-                x = cta_icdf(x0, x1, t, wp, sm.red2, sm.ired);
-            }
+            // the inverse CDF inside this slice, streamed through the ring
+            const int x = consume_icdf<E>(A, P, seq, plan, tma, x0, j, sm);
+            if (x == kIcdfDead) return -1;
             if (threadIdx.x == 0) ph->tok = x;
         } else if (j.kind == kRadix) {
             for (int i = threadIdx.x; i < 256; i += kThreads) sm.bins[i] = 0;

@@ -640,69 +640,6 @@ __device__ bool consume_row2(const Pipe& P, uint32_t& seq, const StreamPlan& p, 
 }
 
 // ---------------------------------------------------------------------------
-// single-CTA passes over a global range (rescans and rare exact paths)
-// ---------------------------------------------------------------------------
-
-// Sum of w(x) over [x0, x1), float-float.
-template <class W>
-__device__ dfloat cta_sum(int x0, int x1, W& w, float2* red) {
-    dfloat acc = df_make(0.f);
-    for (int x = x0 + threadIdx.x; x < x1; x += kThreads) acc = df_add(acc, w(x));
-    return block_sum_df(acc, red);
-}
-
-// Inverse CDF over non-negative weights w(x), x ascending in [x0, x1): the
-// smallest x with C(x) > t.  Blocks of kThreads*16 consecutive elements; each
-// thread owns 16 consecutive elements, so every thread has 16 independent
-// loads in flight per block; prefixes in float-float.  If rounding leaves no
-// crossing, returns the last x with w(x) > 0 (or x0).
-template <class W>
-__device__ int cta_icdf(int x0, int x1, dfloat t, W& w, float2* red, int* ired) {
-    constexpr int PER = 16;
-    dfloat base = df_make(0.f);
-    int last_pos = -1;
-    for (int b0 = x0; b0 < x1; b0 += kThreads * PER) {
-        const int xs = b0 + threadIdx.x * PER;
-        float wv[PER];
-#pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int x = xs + j;
-            wv[j] = (x < x1) ? w(x) : 0.f;
-        }
-        dfloat loc = df_make(0.f);
-        int lp = -1;
-#pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            loc = df_add(loc, wv[j]);
-            if (wv[j] > 0.f) lp = xs + j;
-        }
-        dfloat tot;
-        const dfloat c0 = df_add(base, block_exscan_df(loc, red, tot));
-        int found = 0x7fffffff;
-        if (loc.hi > 0.f && df_gt(df_add(c0, loc), t)) {
-            dfloat c = c0;
-#pragma unroll
-            for (int j = 0; j < PER; ++j) {
-                c = df_add(c, wv[j]);
-                if (found == 0x7fffffff && wv[j] > 0.f && df_gt(c, t)) found = xs + j;
-            }
-        }
-        csync();
-        if (threadIdx.x == 0) { ired[0] = 0x7fffffff; ired[1] = -1; }
-        csync();
-        if (found != 0x7fffffff) atomicMin(&ired[0], found);
-        if (lp >= 0) atomicMax(&ired[1], lp);
-        csync();
-        const int fb = ired[0];
-        if (ired[1] > last_pos) last_pos = ired[1];
-        csync();
-        if (fb != 0x7fffffff) return fb;
-        base = df_add(base, tot);
-    }
-    return last_pos >= 0 ? last_pos : x0;
-}
-
-// ---------------------------------------------------------------------------
 // warp-level key selection over a shared-memory list (combiner warp)
 // ---------------------------------------------------------------------------
 // Keep list[i] with value key >= t, in place, order kept.

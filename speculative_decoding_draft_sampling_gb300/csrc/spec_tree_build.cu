@@ -53,6 +53,7 @@ struct BuildSmem {
     uint32_t scratch[kWarps + 2];
     EnumHdr eh;              // combiner
     uint32_t last_hint;      // combiner: value filter hint for the next row (0: none)
+    uint32_t depth_hint[17]; // DDTree: the hint for depth d's rows (index 1..16; 0: none)
     alignas(16) uint64_t list[kBuildList];   // combiner: gathered keys
 };
 
@@ -70,6 +71,24 @@ __device__ __forceinline__ uint32_t topm_hint_load(const Ctrl* ctrl, int V, int 
 __device__ __forceinline__ void topm_hint_store(Ctrl* ctrl, uint32_t h, int V, int M) {
     __stcg(reinterpret_cast<uint4*>(ctrl->persist + 4),
            make_uint4(kPersistTagTopm, h, static_cast<uint32_t>(V), static_cast<uint32_t>(M)));
+}
+// DDTree rows differ by depth (a drafter's position-d distributions are alike
+// across requests, not across depths): one hint per depth, from the last
+// depth-d row a CTA merged, and kept across calls (persist[8..10] tag, V, M;
+// persist[11 + d - 1] depth d's hint).
+constexpr uint32_t kPersistTagDepth = 0x5e1ec7efu;
+__device__ __forceinline__ void depth_hints_load(const Ctrl* ctrl, int V, int M, int L, uint32_t* dh) {
+    const bool ok = __ldcg(ctrl->persist + 8) == kPersistTagDepth &&
+                    __ldcg(ctrl->persist + 9) == static_cast<uint32_t>(V) &&
+                    __ldcg(ctrl->persist + 10) == static_cast<uint32_t>(M);
+    dh[0] = 0u;
+    for (int d = 1; d <= 16; ++d) dh[d] = (ok && d <= L) ? __ldcg(ctrl->persist + 10 + d) : 0u;
+}
+__device__ __forceinline__ void depth_hint_store(Ctrl* ctrl, int d, uint32_t h, int V, int M) {
+    __stcg(ctrl->persist + 8, kPersistTagDepth);
+    __stcg(ctrl->persist + 9, static_cast<uint32_t>(V));
+    __stcg(ctrl->persist + 10, static_cast<uint32_t>(M));
+    __stcg(ctrl->persist + 10 + d, h);
 }
 
 // per-request workspace: [EnumHdr][lists L*M (tok, prob bits)][nodes N]
@@ -174,15 +193,19 @@ __device__ void build_finalize(const BuildArgs& A, const EnumView& ev, int b, in
 // (descending), then by the child's depth (ascending), then by the child's
 // rank path (ascending); Q is compared through an order-preserving 64-bit key
 // of the double, and the rest only among exact ties.
-__device__ __forceinline__ unsigned long long q_order_key(double q) {
-    unsigned long long qb = static_cast<unsigned long long>(__double_as_longlong(q));
+__device__ __forceinline__ unsigned long long q_order_key(unsigned long long qb) {
     if ((qb << 1) == 0ull) qb = 0ull;                              // -0 as +0
     return (qb >> 63) ? ~qb : (qb | 0x8000000000000000ull);
 }
-// head key of a node: 0 when it has no head
+// a node without a head stores hq = -1.0
+constexpr unsigned long long kNoHead = 0xbff0000000000000ull;
+// head key of a node from its hq bits: 0 when it has no head (integer tests:
+// the fp64 pipe is narrow on this part)
+__device__ __forceinline__ unsigned long long head_key_bits(unsigned long long hb) {
+    return hb == kNoHead ? 0ull : q_order_key(hb);
+}
 __device__ __forceinline__ unsigned long long head_key(uint32_t a_node) {
-    const double hq = __longlong_as_double(static_cast<long long>(ldsv_u64(a_node + offsetof(Ent, hq))));
-    return hq >= 0.0 ? q_order_key(hq) : 0ull;
+    return head_key_bits(ldsv_u64(a_node + offsetof(Ent, hq)));
 }
 // the child path and depth a head stands for
 __device__ __forceinline__ void head_path(uint32_t a_node, int& d, unsigned long long& ph, unsigned long long& pl) {
@@ -222,12 +245,13 @@ __device__ __forceinline__ void lane_best(uint32_t a_nodes, int count, LaneBest&
 }
 __device__ __forceinline__ int warp_best(const LaneBest& b, uint32_t a_nodes) {
     const int l = threadIdx.x & 31;
-    uint32_t cand = __ballot_sync(0xffffffffu, b.j >= 0);
-    if (!cand) return -1;
+    uint32_t cand;
     {
-        const uint32_t hi = static_cast<uint32_t>(b.k >> 32);
-        const uint32_t m = __reduce_max_sync(0xffffffffu, b.j >= 0 ? hi : 0u);
-        cand = __ballot_sync(0xffffffffu, b.j >= 0 && hi == m);
+        // every head key has its top bit set: 0 stands for no head
+        const uint32_t hi = b.j >= 0 ? static_cast<uint32_t>(b.k >> 32) : 0u;
+        const uint32_t m = __reduce_max_sync(0xffffffffu, hi);
+        if (m == 0u) return -1;
+        cand = __ballot_sync(0xffffffffu, hi == m);
     }
     if (__popc(cand) > 1) {
         const bool in = (cand >> l) & 1u;
@@ -309,11 +333,15 @@ __device__ int enumerate_w(const BuildArgs& A, EnumHdr& eh, const EnumView& ev) 
         unsigned long long ph = ldsv_u64(av + offsetof(Ent, ph)), pl = ldsv_u64(av + offsetof(Ent, pl));
         const int d = static_cast<int>(static_cast<uint32_t>(dp)) + 1;
         const int r = static_cast<int>(static_cast<uint32_t>(rn >> 32));
-        const bool sib = r + 1 < __shfl_sync(0xffffffffu, lenl, d);
         const bool deeper = d + 1 <= L;
-        const bool have_list = deeper && d + 1 <= avail && __shfl_sync(0xffffffffu, lenl, deeper ? d + 1 : 0) > 0;
-        const float qs = lprob_at((d - 1) * M + (sib ? r + 1 : r));
-        const float q0 = lprob_at(have_list ? d * M : 0);
+        // the list lengths and both probabilities at once (clamped indices:
+        // the loads do not wait for the tests)
+        const int len_d = __shfl_sync(0xffffffffu, lenl, d);
+        const int len_n = __shfl_sync(0xffffffffu, lenl, deeper ? d + 1 : 0);
+        const float qs = lprob_at((d - 1) * M + min(r + 1, M - 1));
+        const float q0 = lprob_at(deeper ? d * M : 0);
+        const bool sib = r + 1 < len_d;
+        const bool have_list = deeper && d + 1 <= avail && len_n > 0;
         const double hv = sib ? Qv * static_cast<double>(qs) : -1.0;
         const double hc = have_list ? Qc * static_cast<double>(q0) : -1.0;
         path_with(ph, pl, d, r);
@@ -337,7 +365,8 @@ __device__ int enumerate_w(const BuildArgs& A, EnumHdr& eh, const EnumView& ev) 
             want = nid;
             need = d + 1;
         }
-        // the lanes whose nodes changed recompute their best
+        // the lanes whose nodes changed recompute their best (one branch for
+        // both, so that they run together)
         if (l == (v & 31) || l == (nid & 31)) lane_best(a_nodes, count, lb);
         __syncwarp();
     }
@@ -410,7 +439,8 @@ struct BuildOp {
     __device__ static void init_smem(const Args& A, const Geo&, Smem& sm) {
         if (threadIdx.x == 0) {
             topk_smem_init(sm.tk);
-            sm.last_hint = topm_hint_load(A.E.W.ctrl, A.V, A.M);
+            sm.last_hint = 0u;
+            depth_hints_load(A.E.W.ctrl, A.V, A.M, A.L, sm.depth_hint);
         }
     }
     // the combiner's enumeration scratch sits after the ring
@@ -438,7 +468,7 @@ struct BuildOp {
         }
         if (G.own > 1) enum_save(A, b, eh, ev, 0);
         Job j = make_job(b, 0, 0, 0);   // depth 1's row
-        j.hint = sm.last_hint;
+        j.hint = sm.depth_hint[1];
         return j;
     }
     __device__ static StreamPlan plan(const Args& A, const Geo& G, const Job& j) {
@@ -599,8 +629,8 @@ struct BuildOp {
         if (n > 0 && !(flags & kPfBad)) {
             const uint32_t h = topm_hint(ev.lprob[(d - 1) * M + n - 1]);
             if (l == 0) {
-                sm.last_hint = h;
-                topm_hint_store(A.E.W.ctrl, h, A.V, M);
+                sm.depth_hint[d] = h;
+                depth_hint_store(A.E.W.ctrl, d, h, A.V, M);
             }
         }
         if (l == 0) {
@@ -623,7 +653,7 @@ struct BuildOp {
         }
         if (G.own > 1) enum_save(A, b, eh, ev, d - 1);
         Job nj = make_job(b, need - 1, 0, 0);
-        nj.hint = sm.last_hint;
+        nj.hint = sm.depth_hint[need];
         return nj;
     }
 };
@@ -645,6 +675,59 @@ __device__ int merge_sorted_topm_w(const unsigned char* parts, int pb, int C, in
     const uint32_t kb0 = smem_u32(parts) + static_cast<uint32_t>(sizeof(PartHdr));
     const uint32_t mmax = warp_max_u32(static_cast<uint32_t>(cl));
     const int s0 = 1 << (31 - __clz(mmax));
+    if (C <= 4) {
+        // every search of every key at once (lists q >= C are empty): one
+        // step's loads for all lists and keys issue together, so a pass costs
+        // log2(list length) dependent steps instead of C times as many
+        int o[4], mq[4];
+        uint32_t lb[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            o[q] = q < C ? __shfl_sync(0xffffffffu, off, q) : tot;
+            mq[q] = __shfl_sync(0xffffffffu, cl, q);
+            lb[q] = kb0 + static_cast<uint32_t>((q < C ? q : 0) * pb);
+        }
+        for (int f0 = 0; f0 < tot; f0 += 32 * kMergeKeys) {
+            uint64_t key[kMergeKeys];
+#pragma unroll
+            for (int j = 0; j < kMergeKeys; ++j) {
+                const int f = min(f0 + l + 32 * j, tot - 1);
+                const int r = (f >= o[1] ? 1 : 0) + (f >= o[2] ? 1 : 0) + (f >= o[3] ? 1 : 0);
+                const int base = r == 0 ? 0 : (r == 1 ? o[1] : (r == 2 ? o[2] : o[3]));
+                key[j] = lds_u64(kb0 + static_cast<uint32_t>(r * pb + (f - base) * 8));
+            }
+            int pos[4][kMergeKeys];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int j = 0; j < kMergeKeys; ++j) pos[q][j] = 0;
+            for (int st = s0; st > 0; st >>= 1) {
+                uint64_t v[4][kMergeKeys];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int j = 0; j < kMergeKeys; ++j)
+                        v[q][j] = lds_u64(lb[q] + static_cast<uint32_t>((max(min(pos[q][j] + st, mq[q]), 1) - 1) * 8));
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int j = 0; j < kMergeKeys; ++j) {
+                        const int np = pos[q][j] + st;
+                        pos[q][j] = (np <= mq[q] && v[q][j] > key[j]) ? np : pos[q][j];
+                    }
+            }
+#pragma unroll
+            for (int j = 0; j < kMergeKeys; ++j) {
+                const int rank = pos[0][j] + pos[1][j] + pos[2][j] + pos[3][j];
+                if (f0 + l + 32 * j < tot && rank < M) {
+                    tok[rank] = ckey_idx(key[j]);
+                    prob[rank] = ckey_val(key[j]);
+                }
+            }
+        }
+        __syncwarp();
+        return tot < M ? tot : M;
+    }
     for (int f0 = 0; f0 < tot; f0 += 32 * kMergeKeys) {
         uint64_t key[kMergeKeys];
         int rank[kMergeKeys];
