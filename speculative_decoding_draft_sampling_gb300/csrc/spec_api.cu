@@ -570,6 +570,7 @@ spec_status spec_eagle_expand(
     A.base.cap_p = K2;
     A.base.tma_q = aligned16(q) && (q_row_stride * 4) % 16 == 0 && (q_batch_stride * 4) % 16 == 0 && device_memory(q);
     A.F = F; A.G = G; A.front_in = front_in; A.num_front_in = num_front_in; A.num_gen = num_gen;
+    A.score = score; A.depth = depth;
     const void* fn = spec::eagle_rows_kernel_ptr();
     Plan pl;
     spec_status s = make_plan(who, fn, V, spec::build_part_bytes(K2), B * F,

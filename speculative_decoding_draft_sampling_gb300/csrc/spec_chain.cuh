@@ -103,11 +103,16 @@ struct EagleArgs {
     const int* front_in;           // [B, F]
     const int* num_front_in;       // [B]
     const int* num_gen;            // [B]
+    const double* score;           // [B, G] node scores
+    const int* depth;              // [B, G] node depths
 };
 struct EagleRowHdr {
     int n;                         // children found; -1: no row (slot past the frontier); -2: bad node id
     int bad;                       // the row held a NaN or +inf
-    int pad[2];
+    int node;                      // the frontier node the row belongs to (n >= 0)
+    int depth;                     // that node's depth
+    double score;                  // and its score
+    double pad;
 };
 size_t eagle_row_extra_bytes(int K2);
 const void* eagle_rows_kernel_ptr();

@@ -77,24 +77,31 @@ __host__ __device__ __forceinline__ int pow2_at_least(int n) {
 }
 
 __global__ void __launch_bounds__(kGrowThreads) eagle_grow_kernel(const EagleGrowArgs A) {
-    __shared__ int s_off[65], s_n[64], s_bad[64];
+    __shared__ int s_off[65], s_n[64], s_bad[64], s_node[64], s_dep[64];
+    __shared__ double s_sc[64];
     __shared__ SortEnt s_ent[kGrowMax];
-    __shared__ int s_st, s_g0, s_tot;
+    __shared__ int s_st, s_g0, s_tot, s_ng;
     const int b = blockIdx.x, tid = threadIdx.x;
     const int F = A.F, K2 = A.K2, G = A.G;
     auto hdr = [&](int f) {
         return reinterpret_cast<const EagleRowHdr*>(A.rows + static_cast<long long>(b * F + f) * A.row_stride);
     };
-    // the row headers, one thread each, then the offsets on thread 0
+    // the row headers (each carries its frontier node, with the node's score
+    // and depth), one thread each, and the generated count: one round of
+    // independent loads; then the offsets on thread 0
     if (tid < F) {
         const EagleRowHdr* h = hdr(tid);
         s_n[tid] = h->n;
         s_bad[tid] = h->bad;
+        s_node[tid] = h->node;
+        s_dep[tid] = h->depth;
+        s_sc[tid] = h->score;
     }
+    if (tid == kGrowThreads - 1) s_ng = A.num_gen[b];
     __syncthreads();
     if (tid == 0) {
         int st = 0;
-        int g0 = A.num_gen[b];
+        int g0 = s_ng;
         if (g0 < 1 || g0 > G) { st |= kStBadNode; g0 = g0 < 1 ? 0 : G; }
         int off = 0;
         for (int f = 0; f < F; ++f) {
@@ -122,13 +129,12 @@ __global__ void __launch_bounds__(kGrowThreads) eagle_grow_kernel(const EagleGro
             const EagleRowHdr* h = hdr(f);
             const int* tok = reinterpret_cast<const int*>(h + 1);
             const float* prob = reinterpret_cast<const float*>(tok + K2);
-            const int u = A.front_in[static_cast<long long>(b) * F + f];
             const long long nb = static_cast<long long>(b) * G;
-            const double sc = A.score[nb + u] * static_cast<double>(prob[r]);
+            const double sc = s_sc[f] * static_cast<double>(prob[r]);
             const int g = g0 + c;
             A.token[nb + g] = tok[r];
-            A.parent[nb + g] = u;
-            A.depth[nb + g] = A.depth[nb + u] + 1;
+            A.parent[nb + g] = s_node[f];
+            A.depth[nb + g] = s_dep[f] + 1;
             A.score[nb + g] = sc;
             e.s = score_key(sc); e.i = g;
         }
@@ -222,12 +228,17 @@ __global__ void __launch_bounds__(kRerankThreads) eagle_rerank_kernel(const Eagl
         A.out_token[ob + n] = -1; A.out_parent[ob + n] = -1; A.out_depth[ob + n] = -1; A.out_score[ob + n] = 0.0;
     }
     __syncthreads();
-    // ancestor masks: node n sees itself and its ancestors
+    // ancestor masks: node n sees itself and its ancestors (each word built
+    // in a register from the parent chain in shared memory, then stored once)
     for (int n = tid; n < N; n += kRerankThreads) {
         unsigned long long* mk = A.anc_mask + (ob + n) * W;
-        for (int w = 0; w < W; ++w) mk[w] = 0ull;
-        if (n < cnt) {
-            for (int m = n; m >= 0; m = opar[m]) mk[m >> 6] |= 1ull << (m & 63);
+        for (int w = 0; w < W; ++w) {
+            unsigned long long word = 0ull;
+            if (n < cnt) {
+                for (int m = n; m >= 0; m = opar[m])
+                    if ((m >> 6) == w) word |= 1ull << (m & 63);
+            }
+            mk[w] = word;
         }
     }
     if (tid == 0) {

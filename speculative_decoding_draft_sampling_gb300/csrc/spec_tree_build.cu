@@ -852,6 +852,7 @@ struct EagleOp {
         }
         Job j = make_job(b, f, 0, 0);
         j.hint = sm.last_hint;
+        j.aux2 = A.front_in[static_cast<long long>(b) * A.F + f];   // the frontier node (checked above)
         return j;
     }
     __device__ static StreamPlan plan(const Args& A, const Geo& G, const Job& j) { return BuildOp::plan(A.base, G, j); }
@@ -875,6 +876,12 @@ struct EagleOp {
                             static_cast<long long>(j.row) * A.base.q_rs;
         const int u = j.b * A.F + j.row;
         EagleRowHdr* h = row_hdr(A, u);
+        // the frontier node's score and depth travel with the row's list, so
+        // that the grow step reads one header per slot (issued here, used at
+        // the end)
+        const long long nb = static_cast<long long>(j.b) * A.G + j.aux2;
+        const double psc = A.score[nb];
+        const int pdp = A.depth[nb];
         int* tok = reinterpret_cast<int*>(h + 1);
         float* prob = reinterpret_cast<float*>(tok + M);
         int n;
@@ -882,7 +889,9 @@ struct EagleOp {
             n = merge_sorted_topm_w(parts, pb, C, M, cnt, tok, prob);
             if ((flags & kPfHinted) && n < min(M, A.base.V)) {
                 // a hint above this row's K2-th value: the row again, unhinted
-                return make_job(j.b, j.row, 0, 0);
+                Job r = make_job(j.b, j.row, 0, 0);
+                r.aux2 = j.aux2;
+                return r;
             }
             if (n > 0) {
                 const uint32_t hn = topm_hint(prob[n - 1]);
@@ -904,6 +913,9 @@ struct EagleOp {
         if (l == 0) {
             h->n = n;
             h->bad = (flags & kPfBad) ? 1 : 0;
+            h->node = j.aux2;
+            h->depth = pdp;
+            h->score = psc;
         }
         __syncwarp();
         return job_done();
