@@ -166,11 +166,19 @@ __device__ __forceinline__ Job row_job(const ChainArgs& A, int b, int row, int s
 // When the job does not carry y (a request's first row), y is loaded first
 // and the dependent loads wait until ready() (nothing before the accept test
 // waits on them).
+// a chain job whose combine inputs the combiner loaded ahead (aux2; the
+// values in f[0..3], pad[0] and y)
+constexpr int kPrefetched = 0x7e1ec7;
+
 template <class E>
 struct DraftLoads {
     int y, yn;
     float ly, qy;
     bool pend;
+    __device__ __forceinline__ void from_job(const Job& job) {
+        y = job.y; yn = job.pad[0]; ly = job.f[2]; qy = job.f[3];
+        pend = false;
+    }
     __device__ __forceinline__ void load_lq(const ChainArgs& A, int b, int row) {
         ly = -kInf;
         qy = 0.f;
@@ -332,15 +340,23 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
     const int b = job.b, row = job.row, k = A.top_k;
     const bool bonus = job.aux != 0;
     int st = job.st;
-    // the request's global inputs this combine needs, issued first so that
-    // their latency overlaps the selection below
-    const float uk = __uint_as_float(ldg_now_u32(&A.uniforms[static_cast<long long>(b) * ((A.tree ? A.L : A.K) + 1) +
-                                                              draw_uidx(A, job)]));
-    const float ur = bonus ? 0.f : __uint_as_float(ldg_now_u32(&A.uniforms[static_cast<long long>(b) *
-                                                                                ((A.tree ? A.L : A.K) + 1) + row]));
-    SPEC_TRACE_T(tcu);
+    // the request's global inputs this combine needs: loaded by the combiner
+    // while the row streamed, else issued first so that their latency
+    // overlaps the selection below
+    float uk, ur;
     DraftLoads<E> dl;
-    if (!bonus) dl.issue(A, job, chain_k(A, b));
+    if (job.aux2 == kPrefetched) {
+        uk = job.f[0];
+        ur = job.f[1];
+        dl.from_job(job);
+    } else {
+        uk = __uint_as_float(ldg_now_u32(&A.uniforms[static_cast<long long>(b) * ((A.tree ? A.L : A.K) + 1) +
+                                                      draw_uidx(A, job)]));
+        ur = bonus ? 0.f : __uint_as_float(ldg_now_u32(&A.uniforms[static_cast<long long>(b) *
+                                                                    ((A.tree ? A.L : A.K) + 1) + row]));
+        if (!bonus) dl.issue(A, job, chain_k(A, b));
+    }
+    SPEC_TRACE_T(tcu);
     SPEC_TRACE_T(tca);
     // the slices' headers (value filters: the low key halves are zero)
     const uint32_t hb = smem_u32(parts) + static_cast<uint32_t>(l * pb);
@@ -704,8 +720,10 @@ __device__ __noinline__ Job combine_se(const ChainArgs& A, const Geo& G, const J
     const uint32_t mask = job.hint;
     int st = job.st;
     const float c2 = A.c2;
+    const bool pre = job.aux2 == kPrefetched;
     DraftLoads<E> dl;
-    if (!bonus) dl.issue(A, job, chain_k(A, b));
+    if (pre) dl.from_job(job);
+    else if (!bonus) dl.issue(A, job, chain_k(A, b));
     uint32_t flags = 0;
     float vm = -kInf;
     dfloat sv = df_make(0.f);
@@ -721,13 +739,13 @@ __device__ __noinline__ Job combine_se(const ChainArgs& A, const Geo& G, const J
     dfloat zv = df_make(0.f);
     if (l < C && sv.hi > 0.f) zv = df_mul(ex2((vm - m) * c2), sv);
     const dfloat Z = warp_sum_df(zv);
-    const float uk = chain_u(A, b, draw_uidx(A, job));
+    const float uk = pre ? job.f[0] : chain_u(A, b, draw_uidx(A, job));
     if (!bonus) {
         dl.ready(A, job);
         const int y = dl.y;
         const float ly = dl.ly, qy = dl.qy;
         const float ey = (y >= 0 && y < A.V && fkey(ly) >= mask) ? ex2((ly - m) * c2) : 0.f;
-        const bool acc = chain_accept_z(A, y, ey, qy, Z, chain_u(A, b, row), st);
+        const bool acc = chain_accept_z(A, y, ey, qy, Z, pre ? job.f[1] : chain_u(A, b, row), st);
         chain_diag(A, b, row, static_cast<float>(static_cast<double>(ey) / df_to_d(Z)), qy, Z.hi, 0.f);
         if (acc) return row_job(A, b, row + 1, st, sm.last_hint, 0, dl.yn);
         // the residual pass: every slice's [p - q]_+ mass with this row's m and Z
@@ -992,6 +1010,38 @@ struct ChainOp {
 
     __device__ static int batch(const Args& A) { return A.B; }
     __device__ static bool tma(const Args& A) { return A.tma_l && (kTopk || A.K == 0 || A.tma_q); }
+    // A chain row's combine inputs, loaded by the combiner while the row
+    // streams (right after the job was posted): the row's uniforms, its
+    // drafted token and the next row's, the token's logit and q.  They go to
+    // the combiner's own copy of the job (the posted copies are not touched),
+    // so the combine starts without a global load.
+    __device__ static void prefetch(const Args& A, const Geo&, Job& j) {
+        if (A.tree || j.b < 0 || (j.kind != kTk && j.kind != kSe)) return;
+        if ((threadIdx.x & 31) == 0) {
+            const int b = j.b, row = j.row;
+            const int kb = chain_k(A, b);
+            const long long ub = static_cast<long long>(b) * (A.K + 1);
+            const bool bonus = j.aux != 0;
+            const float uk = A.uniforms[ub + kb];
+            const float ur = bonus ? 0.f : A.uniforms[ub + row];
+            int y = kYUnknown, yn = kYUnknown;
+            float ly = -kInf, qy = 0.f;
+            if (!bonus) {
+                const int* dr = A.draft + static_cast<long long>(b) * A.K;
+                yn = row + 1 < kb ? dr[row + 1] : kYUnknown;
+                y = j.y != kYUnknown ? j.y : dr[row];
+                if (y >= 0 && y < A.V) {
+                    ly = E::load(chain_lrow<E>(A, b, row), y);
+                    qy = chain_qrow(A, b, row)[y];
+                }
+            }
+            j.f[0] = uk; j.f[1] = ur; j.f[2] = ly; j.f[3] = qy;
+            j.pad[0] = yn;
+            j.y = y;
+            j.aux2 = kPrefetched;
+        }
+        __syncwarp();
+    }
     __device__ static void init_smem(const Args& A, const Geo&, Smem& sm) {
         if (threadIdx.x == 0) {
             topk_smem_init(sm.tk);

@@ -78,6 +78,7 @@ struct WalkOp {
     using Args = WalkArgs;
     using Smem = WalkSmem;
 
+    __device__ static void prefetch(const Args&, const Geo&, Job&) {}
     __device__ static int batch(const Args& A) { return A.B; }
     __device__ static bool tma(const Args& A) { return A.tma_l != 0; }
     __device__ static void init_smem(const Args&, const Geo&, Smem&) {}
