@@ -291,7 +291,7 @@ __device__ int enumerate_w(const BuildArgs& A, EnumHdr& eh, const EnumView& ev) 
     auto st_f64 = [](uint32_t a, double v) { stsv_u64(a, static_cast<uint64_t>(__double_as_longlong(v))); };
     auto ld_f64 = [](uint32_t a) { return __longlong_as_double(static_cast<long long>(ldsv_u64(a))); };
 #ifdef SPEC_TRACE
-    long long t_best = 0;
+    long long t_best = 0, t_upd = 0, t_lb = 0;
     const long long t_all = clock64();
 #endif
     // a node of an earlier call whose first head waited for its depth's list
@@ -347,31 +347,39 @@ __device__ int enumerate_w(const BuildArgs& A, EnumHdr& eh, const EnumView& ev) 
         path_with(ph, pl, d, r);
         const int nid = count++;
         const uint32_t ac = a_nodes + kE * nid;
-        if (l == (v & 31)) {
-            st_f64(av + offsetof(Ent, hq), hv);
-            stsv_u64(av + offsetof(Ent, rank), (static_cast<uint64_t>(r + 1) << 32) | static_cast<uint32_t>(rn));
-        }
-        if (l == (nid & 31)) {
-            st_f64(ac + offsetof(Ent, Q), Qc);
-            st_f64(ac + offsetof(Ent, hq), hc);
-            stsv_u64(ac + offsetof(Ent, ph), ph);
-            stsv_u64(ac + offsetof(Ent, pl), pl);
-            stsv_u64(ac + offsetof(Ent, depth), (static_cast<uint64_t>(static_cast<uint32_t>(v)) << 32) |
-                                                    static_cast<uint32_t>(d));
-            stsv_u64(ac + offsetof(Ent, rank), static_cast<uint32_t>(r));   // next = 0
-        }
+        // every lane stores the same values (no divergent branch; a warp's
+        // stores of one value to one address are one write)
+        st_f64(av + offsetof(Ent, hq), hv);
+        stsv_u64(av + offsetof(Ent, rank), (static_cast<uint64_t>(r + 1) << 32) | static_cast<uint32_t>(rn));
+        st_f64(ac + offsetof(Ent, Q), Qc);
+        st_f64(ac + offsetof(Ent, hq), hc);
+        stsv_u64(ac + offsetof(Ent, ph), ph);
+        stsv_u64(ac + offsetof(Ent, pl), pl);
+        stsv_u64(ac + offsetof(Ent, depth), (static_cast<uint64_t>(static_cast<uint32_t>(v)) << 32) |
+                                                static_cast<uint32_t>(d));
+        stsv_u64(ac + offsetof(Ent, rank), static_cast<uint32_t>(r));   // next = 0
         if (deeper && count < N && d + 1 > avail) {
             // c's first head needs a depth not read yet: stop, and resume here
             want = nid;
             need = d + 1;
         }
-        // the lanes whose nodes changed recompute their best (one branch for
-        // both, so that they run together)
-        if (l == (v & 31) || l == (nid & 31)) lane_best(a_nodes, count, lb);
+#ifdef SPEC_TRACE
         __syncwarp();
+        const long long tq1 = clock64();
+        t_upd += tq1 - tq0;
+#endif
+        // every lane recomputes its best over its nodes (only the two lanes
+        // owning v and the new node find a change; running it everywhere
+        // keeps the warp converged)
+        __syncwarp();
+        lane_best(a_nodes, count, lb);
+#ifdef SPEC_TRACE
+        t_lb += clock64() - tq1;
+#endif
     }
 #ifdef SPEC_TRACE
     if (l == 0) SPEC_TRACE_EV(16, static_cast<int>(t_best), static_cast<int>(clock64() - t_all), count);
+    if (l == 0) SPEC_TRACE_EV(17, static_cast<int>(t_upd), static_cast<int>(t_lb), 0);
 #endif
     __syncwarp();
     if (l == 0) { eh.count = count; eh.want = want; }
