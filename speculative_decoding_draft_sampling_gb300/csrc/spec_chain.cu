@@ -1015,7 +1015,7 @@ struct ChainOp {
     // drafted token and the next row's, the token's logit and q.  They go to
     // the combiner's own copy of the job (the posted copies are not touched),
     // so the combine starts without a global load.
-    __device__ static void prefetch(const Args& A, const Geo&, Job& j) {
+    __device__ static void prefetch(const Args& A, const Geo&, Job& j, Smem&) {
         if (A.tree || j.b < 0 || (j.kind != kTk && j.kind != kSe)) return;
         if ((threadIdx.x & 31) == 0) {
             const int b = j.b, row = j.row;
@@ -1087,8 +1087,7 @@ struct ChainOp {
                                   Smem& sm, unsigned char* out) {
         PartHdr* ph = reinterpret_cast<PartHdr*>(out);
         uint64_t* pk = reinterpret_cast<uint64_t*>(ph + 1);
-        const int x0 = slice_x0(G, G.rank), x1 = slice_x1(G, G.rank, A.V);
-        const int b = j.b, row = j.row;
+        const int x0 = slice_x0(G, G.rank);
         const StreamPlan plan = ChainOp::plan(A, G, j);
         if (threadIdx.x == 0) {
             ph->flags = 0; ph->cnt = 0; ph->tok = -1; ph->kth = 0; ph->vmax = -kInf; ph->hasy = 0;

@@ -732,10 +732,11 @@ __device__ inline uint64_t kth_key_w(const uint64_t* list, int n, int k) {
 //                                           (header + payload) to `out`; returns
 //                                           its byte count (multiple of 16), or
 //                                           -1 when a wait gave up
-//   void prefetch(A, G, job)                combiner warp, right after the job
+//   void prefetch(A, G, job, sm)            combiner warp, right after the job
 //                                           was posted: load what its combine
 //                                           will read into the combiner's own
-//                                           copy of the job (no-op allowed)
+//                                           copy of the job or its shared
+//                                           memory (no-op allowed)
 //   Job  combine(A, G, job, parts, sm)      combiner warp of the slot's leader:
 //                                           parts = the C partials of the job;
 //                                           returns the slot's next job, or
@@ -868,7 +869,7 @@ struct Engine {
             if (!(g_test_drop_post && G.rank == 0 && i == 0 && blockIdx.x == 0))
 #endif
             post(G, es, s, j);
-            Op::prefetch(A, G, cur[i]);
+            Op::prefetch(A, G, cur[i], os);
             if (j.b >= 0) active |= 1 << i;
         }
         while (active) {
@@ -903,7 +904,7 @@ struct Engine {
             if ((threadIdx.x & 31) == 0) cur[i] = nx;
             SPEC_TRACE_T(tk2);
             post(G, es, s, nx);
-            Op::prefetch(A, G, cur[i]);
+            Op::prefetch(A, G, cur[i], os);
             if ((threadIdx.x & 31) == 0) {
                 SPEC_TRACE_EV(7, s, nx.b, nx.row);
                 SPEC_TRACE_EV(14, static_cast<int>(tk1 - tk0), static_cast<int>(tk2 - tk1),

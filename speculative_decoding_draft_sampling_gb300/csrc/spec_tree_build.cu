@@ -444,7 +444,7 @@ struct BuildOp {
 
     __device__ static int batch(const Args& A) { return A.B; }
     __device__ static bool tma(const Args& A) { return A.tma_q != 0; }
-    __device__ static void prefetch(const Args&, const Geo&, Job&) {}
+    __device__ static void prefetch(const Args&, const Geo&, Job&, Smem&) {}
     __device__ static void init_smem(const Args& A, const Geo&, Smem& sm) {
         if (threadIdx.x == 0) {
             topk_smem_init(sm.tk);
@@ -865,7 +865,7 @@ struct EagleOp {
         return j;
     }
     __device__ static StreamPlan plan(const Args& A, const Geo& G, const Job& j) { return BuildOp::plan(A.base, G, j); }
-    __device__ static void prefetch(const Args&, const Geo&, Job&) {}
+    __device__ static void prefetch(const Args&, const Geo&, Job&, Smem&) {}
     __device__ static int consume(const Args& A, const Geo& G, const Pipe& P, uint32_t& seq, bool tma, const Job& j,
                                   Smem& sm, unsigned char* out) {
         return BuildOp::consume(A.base, G, P, seq, tma, j, sm, out);

@@ -21,10 +21,18 @@
 
 namespace spec {
 
+// combiner: the children of the node a tree walk reads next (ascending id),
+// found while its row streams
+constexpr int kChildCache = 64;
 struct WalkSmem {
     uint64_t red[kWarps];
     uint32_t wb[kWarps];
+    int cb, cnode, cn;                 // request, node, children cached (-1: too many)
+    int cid[kChildCache];
+    int ctok[kChildCache];
 };
+// a greedy walk job whose combine inputs the combiner loaded ahead
+constexpr int kWalkPrefetched = 0x7e1ec8;
 
 template <class E, bool kTree>
 __device__ __forceinline__ const void* walk_row(const WalkArgs& A, int b, int i) {
@@ -78,10 +86,46 @@ struct WalkOp {
     using Args = WalkArgs;
     using Smem = WalkSmem;
 
-    __device__ static void prefetch(const Args&, const Geo&, Job&) {}
+    // What the combine reads, loaded by the combiner while the row streams:
+    // a greedy walk's draft length and drafted token (into its copy of the
+    // job); a tree walk's children of the node (into shared memory).
+    __device__ static void prefetch(const Args& A, const Geo&, Job& j, Smem& sm) {
+        if (j.b < 0) return;
+        const int l = threadIdx.x & 31;
+        const int b = j.b, row = j.row;
+        if (!kTree) {
+            if (l == 0) {
+                const int kb = A.k_per_req ? A.k_per_req[b] : A.K;
+                j.pad[0] = kb;
+                j.y = row < kb && row < A.K ? A.draft[static_cast<long long>(b) * A.K + row] : kYUnknown;
+                j.aux2 = kWalkPrefetched;
+            }
+            __syncwarp();
+            return;
+        }
+        int nn = A.num_nodes[b];
+        nn = nn < A.N ? nn : A.N;
+        const int* par = A.parent + static_cast<long long>(b) * A.N;
+        const int* tok = A.token + static_cast<long long>(b) * A.N;
+        const uint32_t lt = (1u << l) - 1u;
+        int n = 0;
+        for (int c0 = 0; c0 < nn; c0 += 32) {
+            const int c = c0 + l;
+            const bool is = c < nn && par[c] == row;
+            const int t = is ? tok[c] : 0;
+            const uint32_t bal = __ballot_sync(0xffffffffu, is);
+            const int pos = n + __popc(bal & lt);
+            if (is && pos < kChildCache) { sm.cid[pos] = c; sm.ctok[pos] = t; }
+            n += __popc(bal);
+        }
+        if (l == 0) { sm.cb = b; sm.cnode = row; sm.cn = n <= kChildCache ? n : -1; }
+        __syncwarp();
+    }
     __device__ static int batch(const Args& A) { return A.B; }
     __device__ static bool tma(const Args& A) { return A.tma_l != 0; }
-    __device__ static void init_smem(const Args&, const Geo&, Smem&) {}
+    __device__ static void init_smem(const Args&, const Geo&, Smem& sm) {
+        if (threadIdx.x == 0) { sm.cb = -1; sm.cnode = -1; sm.cn = -1; }
+    }
     __device__ static Job first(const Args& A, const Geo&, int b, Smem&) {
         if (!kTree) {
             const int kb = A.k_per_req ? A.k_per_req[b] : A.K;
@@ -115,7 +159,7 @@ struct WalkOp {
         }
         return static_cast<int>(sizeof(PartHdr));
     }
-    __device__ static Job combine(const Args& A, const Geo& G, const Job& j, const unsigned char* parts, Smem&) {
+    __device__ static Job combine(const Args& A, const Geo& G, const Job& j, const unsigned char* parts, Smem& sm) {
         const int l = threadIdx.x & 31;
         const int b = j.b, row = j.row;
         int st = j.st;
@@ -131,10 +175,11 @@ struct WalkOp {
         const bool bad_row = (flags & kPfBad) || !(ckey_val(best) > -kInf);
         const int am = ckey_idx(best);
         if (!kTree) {
-            const int kb = A.k_per_req ? A.k_per_req[b] : A.K;
+            const bool pre = j.aux2 == kWalkPrefetched;
+            const int kb = pre ? j.pad[0] : (A.k_per_req ? A.k_per_req[b] : A.K);
             if (bad_row) return greedy_finish(A, b, row, -1, st | 1);
             if (row == kb) return greedy_finish(A, b, row, am, st);
-            const int y = A.draft[static_cast<long long>(b) * A.K + row];
+            const int y = pre ? j.y : A.draft[static_cast<long long>(b) * A.K + row];
             if (y < 0 || y >= A.V) st |= 8;
             if (y != am) return greedy_finish(A, b, row, am, st);
             Job nj = make_job(b, row + 1, 0, st);
@@ -142,7 +187,19 @@ struct WalkOp {
         } else {
             const int acc = j.depth;
             if (bad_row) return tree_finish(A, b, acc, -1, st | 1);
-            const int child = find_child_w(A.token, A.parent, A.num_nodes, A.N, b, row, am);
+            int child;
+            if (sm.cb == b && sm.cnode == row && sm.cn >= 0) {
+                // the cached children, ascending id: the first one carrying am
+                uint32_t hit = 0;
+                for (int c0 = 0; c0 < sm.cn && !hit; c0 += 32) {
+                    const int c = c0 + l;
+                    hit = __ballot_sync(0xffffffffu, c < sm.cn && sm.ctok[c] == am);
+                    if (hit) child = sm.cid[c0 + __ffs(hit) - 1];
+                }
+                if (!hit) child = -1;
+            } else {
+                child = find_child_w(A.token, A.parent, A.num_nodes, A.N, b, row, am);
+            }
             if (child < 0 || acc >= A.L) return tree_finish(A, b, acc, am, st);
             if (l == 0) {
                 const int W = A.L + 1;
