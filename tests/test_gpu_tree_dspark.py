@@ -70,6 +70,24 @@ def test_tree_build_ties_and_uniform_rows():
     _assert_tree_equal(_tree_np(g), ref)
 
 
+def test_tree_build_stale_depth_hints():
+    """The per-depth filter hints persist in the workspace across calls.  A
+    call whose rows are much flatter at some depths and much sharper at
+    others than the previous call's makes those hints wrong (too high: the
+    row is read again unhinted; too low: many more candidates); the trees
+    must still equal the oracle's."""
+    B, L, V, N = 8, 6, 20011, 48
+    t1 = workloads.make_tree("ddtree", device=DEV, B=B, L=L, V=V, N=N, seed=7)
+    g1 = sv.tree_build(t1.q, N)
+    _assert_tree_equal(_tree_np(g1), oracle.tree_build(host(t1.q), N))
+    scale = torch.tensor([0.25, 2.5, 0.5, 2.0, 0.3, 3.0], device=DEV).view(1, L, 1)
+    q2 = torch.softmax(t1.q_logits * scale, dim=-1).float().contiguous()
+    for q in (q2, t1.q):                      # stale hints both ways, on the same workspace
+        g = sv.tree_build(q, N, ws=g1.ws)
+        _assert_tree_equal(_tree_np(g), oracle.tree_build(host(q), N))
+        assert sv.workspace_error(g.ws) == 0
+
+
 def test_tree_build_never_reads_past_needed_rows():
     t = workloads.make_tree("ddtree", device=DEV, B=8, L=16, V=20000, N=64)
     ref = oracle.tree_build(host(t.q), 64)
