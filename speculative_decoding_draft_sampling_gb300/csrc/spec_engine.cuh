@@ -842,12 +842,21 @@ struct Engine {
         }
         __syncwarp();
     }
-    // claim requests until one needs a row (or none are left: the stop job)
-    __device__ static Job claim(const Args& A, const Workspace& W, const Geo& G, OSmem& os) {
+    // Claim requests until one needs a row (or none are left: the stop job).
+    // The first request of every slot is assigned, not claimed: slot s of
+    // cluster c starts request s * clusters + c, so that a batch smaller
+    // than the slot count spreads over the clusters one request each before
+    // any cluster takes a second; later claims count on from there.
+    __device__ static Job claim(const Args& A, const Workspace& W, const Geo& G, OSmem& os, int assigned = -1) {
+        const int clusters = static_cast<int>(gridDim.x) / G.C;
+        const int base = min(Op::batch(A), clusters * G.R);
         for (;;) {
-            int b = 0;
-            if ((threadIdx.x & 31) == 0) b = static_cast<int>(atomicAdd(&W.ctrl->next, 1u));
-            b = __shfl_sync(0xffffffffu, b, 0);
+            int b = assigned;
+            assigned = -1;
+            if (b < 0) {
+                if ((threadIdx.x & 31) == 0) b = base + static_cast<int>(atomicAdd(&W.ctrl->next, 1u));
+                b = __shfl_sync(0xffffffffu, b, 0);
+            }
             Job j;
             if (b >= Op::batch(A)) return make_job(kJobStop, 0, 0, 0);
             j = Op::first(A, G, b, os);
@@ -860,9 +869,12 @@ struct Engine {
         Job* cur = es.cur;      // shared memory: a register array indexed by slot would live in local memory
         uint32_t phase = 0;     // bit i: parity of own slot i's next arrival phase
         int active = 0;
+        const int clusters = static_cast<int>(gridDim.x) / G.C;
+        const int cl = static_cast<int>(cluster_id_x());
         for (int i = 0; i < nown; ++i) {
             const int s = G.rank + i * G.C;
-            const Job j = claim(A, W, G, os);
+            const int first_b = s * clusters + cl;
+            const Job j = claim(A, W, G, os, first_b < Op::batch(A) ? first_b : -1);
             __syncwarp();
             if ((threadIdx.x & 31) == 0) cur[i] = j;
 #ifdef SPEC_TEST_HOOKS
