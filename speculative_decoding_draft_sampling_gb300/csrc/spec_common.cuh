@@ -246,6 +246,23 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr, uint3
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;"
                  :: "r"(cluster_addr), "r"(count) : "memory");
 }
+// Store 16 bytes into the shared memory of a CTA of the cluster (address
+// from mapa) and count them on that CTA's mbarrier `bar` (complete_tx): the
+// bytes are visible to a thread that observes the barrier's phase complete,
+// with no fence on the storing side.  Both addresses in the same CTA; `a`
+// 16-byte aligned.
+__device__ __forceinline__ void st_async_v4(uint32_t a, const uint4& v, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+                 :: "r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar) : "memory");
+}
+// One arrival on a barrier of any CTA of the cluster that also expects
+// `bytes` of st_async_v4 stores (from any thread of this CTA, before or after
+// the arrival): the phase completes once every arrival is in and the bytes
+// have landed.  Relaxed: it orders none of this thread's other accesses.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;"
+                 :: "r"(bar), "r"(bytes) : "memory");
+}
 // one non-blocking test of a phase completed by arrivals from other CTAs
 // (acquire at cluster scope: their writes before the arrive are visible)
 __device__ __forceinline__ bool mbar_test_cluster(const uint64_t* bar, uint32_t parity) {

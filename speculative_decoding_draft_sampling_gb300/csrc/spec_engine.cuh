@@ -11,7 +11,9 @@
 // leader's arrival mbarrier.  The leader's combiner warp takes the decision
 // and posts the slot's next *job* (the request's next row, a residual pass,
 // or the first row of a newly claimed request) to the mailbox of every CTA
-// of the cluster.  Every CTA streams the jobs of all slots interleaved, so
+// of the cluster.  Partials and jobs travel as asynchronous remote stores
+// (st.async) whose bytes complete the receiving barrier's transaction count,
+// so neither side pays a release fence at cluster scope.  Every CTA streams the jobs of all slots interleaved, so
 // one slot's combine overlaps the other slots' streaming; slot s is led by
 // CTA s mod C, so combines spread over the cluster.  Requests are claimed
 // from one global counter whenever a slot frees up; there is no grid-wide
@@ -833,12 +835,18 @@ struct Engine {
         __syncwarp();
         if (l < G.C) {
             const uint32_t a = mapa(smem_u32(&es.jd[s]), static_cast<uint32_t>(l));
+            const uint32_t bar = mapa(smem_u32(&es.jfull[s]), static_cast<uint32_t>(l));
             const uint4* v = reinterpret_cast<const uint4*>(&j);
-            st_cluster_v4(a, v[0]);
-            st_cluster_v4(a + 16, v[1]);
-            st_cluster_v4(a + 32, v[2]);
-            st_cluster_v4(a + 48, v[3]);
-            mbar_arrive_cluster(mapa(smem_u32(&es.jfull[s]), static_cast<uint32_t>(l)), 1u);
+            // the mailbox bytes are counted on the barrier as they land, so
+            // the arrival needs no release fence (a release at cluster scope
+            // would first wait for the outputs this warp just wrote to global
+            // memory: about 1300 cycles)
+            static_assert(sizeof(Job) == 64, "a job is four 16-byte stores");
+            st_async_v4(a, v[0], bar);
+            st_async_v4(a + 16, v[1], bar);
+            st_async_v4(a + 32, v[2], bar);
+            st_async_v4(a + 48, v[3], bar);
+            mbar_arrive_expect_tx_cluster(bar, static_cast<uint32_t>(sizeof(Job)));
         }
         __syncwarp();
     }
@@ -1031,15 +1039,23 @@ struct Engine {
             // the partial into the leader's slot area, then one counted arrival
             const uint32_t dst = mapa(smem_u32(parts + (static_cast<size_t>(oi) * G.C + G.rank) * G.part_bytes),
                                       static_cast<uint32_t>(leader));
+            SPEC_TRACE_T(tx0);
             csync();   // the staging partial is complete
+            SPEC_TRACE_T(tx1);
+            // each 16 bytes counted on the leader's barrier as they land; the
+            // barrier below only keeps the staging area until every thread
+            // has read its share (the next job rewrites it)
             for (int i = threadIdx.x; i < nb / 16; i += kThreads)
-                st_cluster_v4(dst + 16u * i, reinterpret_cast<const uint4*>(stage)[i]);
-            csync();   // every consumer's stores of the partial happen before the arrive
+                st_async_v4(dst + 16u * i, reinterpret_cast<const uint4*>(stage)[i], arr);
+            csync();
+            SPEC_TRACE_T(tx2);
             if (threadIdx.x == 0) {
-                // release at cluster scope: with the barrier above it makes
-                // every consumer's stores visible to the leader's acquire
-                mbar_arrive_cluster(arr, 1u);
+                // one arrival that expects the partial's bytes: the phase
+                // completes when every CTA has arrived and every byte landed
+                mbar_arrive_expect_tx_cluster(arr, static_cast<uint32_t>(nb & ~15));
                 SPEC_TRACE_EV(5, s, job.b, job.row);
+                SPEC_TRACE_EV(26, static_cast<int>(tx1 - tx0), static_cast<int>(tx2 - tx1),
+                              static_cast<int>(clock64() - tx2));
             }
         }
     }

@@ -493,10 +493,15 @@ struct BuildOp {
         TopkHistFn<F32, false> fn;
         fn.init(&sm.tk, M, j.hint, seq + 1u);   // every consumer holds the same seq
         if (!consume_row<F32>(P, seq, plan(A, G, j), tma, slice_x0(G, G.rank), fn)) return -1;
+        SPEC_TRACE_T(tf0);
         uint64_t F;
         uint32_t oflow, bad;
         float vm;
         int n = fn.finish(F, oflow, bad, vm);
+        SPEC_TRACE_T(tf1);
+#ifdef SPEC_TRACE
+        const int n_fin = n;
+#endif
         uint64_t* list = sm.tk.cand;
         if (n > A.cap_p && !bad && !oflow) {
             // the slice's exact M-th key: a certified value bound (repeated
@@ -538,6 +543,7 @@ struct BuildOp {
             }
         }
         if (bad || oflow) n = 0;
+        SPEC_TRACE_T(tf2);
         csync();
         // the keys sorted descending (composite keys are unique: a key's
         // position is the number of greater keys), so that the combine merges
@@ -553,6 +559,8 @@ struct BuildOp {
             ph->flags = (bad ? kPfBad : 0u) | (oflow ? kPfOverflow : 0u) | (j.hint ? kPfHinted : 0u);
             ph->cnt = n;
             ph->kth = F;
+            SPEC_TRACE_EV(24, static_cast<int>(tf1 - tf0), static_cast<int>(tf2 - tf1), static_cast<int>(clock64() - tf2));
+            SPEC_TRACE_EV(25, n_fin, n, 0);
         }
         return static_cast<int>(sizeof(PartHdr)) + ((n * 8 + 15) & ~15);
     }
