@@ -268,6 +268,12 @@ __device__ int warp_icdf_pairs(const int* tok, const float2* w, int n, dfloat t)
 // m: `margin` of the gap below tau (rows of one target differ little in tau;
 // a hint above the next row's tau costs a re-read of that row, one far below
 // it extra candidates).
+// The next call's first rows take a wider margin: 0.5 gave about 650
+// candidates per slice (13 k) on N(0, 3^2) rows of 151936, each costing a
+// slow row end; 0.25 ran faster both there and on rows whose scale varies.
+#ifndef SPEC_PERSIST_MARGIN
+#define SPEC_PERSIST_MARGIN 0.25f
+#endif
 #ifndef SPEC_HINT_MARGIN
 #define SPEC_HINT_MARGIN 0.08f
 #endif
@@ -614,7 +620,7 @@ __device__ __noinline__ Job combine_topk(const ChainArgs& A, const Geo& G, const
         sm.tau_ok = tau == tau && tau > -kInf && m < kInf;
         // for the next call's first rows, with a wider margin (another call's
         // rows may sit lower); one 16-byte store
-        const uint32_t hw = steady ? hint_from(tau, m, 0.5f) : 0u;
+        const uint32_t hw = steady ? hint_from(tau, m, SPEC_PERSIST_MARGIN) : 0u;
         __stcg(reinterpret_cast<uint4*>(A.E.W.ctrl->persist),
                make_uint4(kPersistTag, hw, static_cast<uint32_t>(A.V), static_cast<uint32_t>(A.top_k)));
     }
@@ -1100,6 +1106,7 @@ struct ChainOp {
                 TopkHistFn<E, true> fn;
                 fn.init(&sm.tk, A.top_k, j.hint, seq + 1u);   // every consumer holds the same seq
                 if (!consume_row<E>(P, seq, plan, tma, x0, fn)) return -1;
+                SPEC_TRACE_T(tp0);
                 fn.publish();
                 csync();
                 int tot;
@@ -1107,6 +1114,7 @@ struct ChainOp {
                 uint32_t fl;
                 float vm;
                 fn.summary(tot, F, fl, vm);
+                SPEC_TRACE_T(tp1);
                 const uint32_t bad = (fl >> 1) & 1u;
                 uint32_t oflow = fl & 1u;
                 int n = tot;
@@ -1133,6 +1141,7 @@ struct ChainOp {
                     if (n > A.cap_p) oflow = 1;   // ties at the k-th value: the combine takes the radix path
                     else src = list;
                 }
+                SPEC_TRACE_T(tp2);
                 if (oflow || bad) n = 0;
                 else n = slice_sort_trim(src, n, F, A.top_k, pk, &sm.nsel);
                 nkeys = n;
@@ -1141,6 +1150,9 @@ struct ChainOp {
                     ph->cnt = n;
                     ph->kth = F;
                     ph->vmax = vm;
+                    SPEC_TRACE_EV(27, static_cast<int>(tp1 - tp0), static_cast<int>(tp2 - tp1),
+                                  static_cast<int>(clock64() - tp2));
+                    SPEC_TRACE_EV(28, tot, n, static_cast<int>(j.hint));
                 }
             } else {
                 // sum-exp (masked at the job's threshold when it carries one)

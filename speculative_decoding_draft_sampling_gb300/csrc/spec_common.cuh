@@ -230,22 +230,6 @@ __device__ __forceinline__ uint32_t ldg_now_u16(const void* p) {
     asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t a, const uint4& v) {
-    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};"
-                 :: "r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
-}
-__device__ __forceinline__ void st_cluster_u32(uint32_t a, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" :: "r"(a), "r"(v) : "memory");
-}
-__device__ __forceinline__ void fence_acq_rel_cluster() {
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
-// arrive `count` times on an mbarrier of any CTA of the cluster (address from
-// mapa), releasing this thread's earlier writes at cluster scope
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr, uint32_t count) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;"
-                 :: "r"(cluster_addr), "r"(count) : "memory");
-}
 // Store 16 bytes into the shared memory of a CTA of the cluster (address
 // from mapa) and count them on that CTA's mbarrier `bar` (complete_tx): the
 // bytes are visible to a thread that observes the barrier's phase complete,

@@ -1029,7 +1029,7 @@ struct Engine {
             if (job.target >= 0 && job.target != G.rank) {
                 // not this CTA's job: acknowledge it (the leader posts the
                 // slot's next job only after every CTA has taken this one)
-                if (threadIdx.x == 0) mbar_arrive_cluster(arr, 1u);
+                if (threadIdx.x == 0) mbar_arrive_expect_tx_cluster(arr, 0u);   // no bytes: relaxed suffices
                 continue;
             }
             if (threadIdx.x == 0) SPEC_TRACE_EV(3, s, job.b, job.row);
