@@ -16,8 +16,9 @@
 // generated node by (score desc, depth asc, index asc) and keeps the root
 // and the best budget - 1; a parent always sorts before its children (its
 // score is no lower, its depth lower), so the kept set is a tree and is
-// emitted parents first.  Both orders are total, so a bitonic network over
-// shared memory gives them exactly.
+// emitted parents first.  Both orders are strict and total (indices are
+// distinct), so the grow places each child by its rank and the rerank sorts
+// with a bitonic network over shared memory, both exactly.
 #include "spec_chain.cuh"
 
 namespace spec {
@@ -118,33 +119,37 @@ __global__ void __launch_bounds__(kGrowThreads) eagle_grow_kernel(const EagleGro
     __syncthreads();
     const int g0 = s_g0, tot = s_tot;
     const int nc = tot < G - g0 ? tot : G - g0;   // children that fit, in (slot, rank) order
-    const int P = pow2_at_least(nc > 1 ? nc : 1);
-    for (int c = tid; c < P; c += kGrowThreads) {
+    for (int c = tid; c < nc; c += kGrowThreads) {
+        int f = 0;
+        while (s_off[f + 1] <= c) ++f;           // the slot whose children cover c
+        const int r = c - s_off[f];
+        const EagleRowHdr* h = hdr(f);
+        const int* tok = reinterpret_cast<const int*>(h + 1);
+        const float* prob = reinterpret_cast<const float*>(tok + K2);
+        const long long nb = static_cast<long long>(b) * G;
+        const double sc = s_sc[f] * static_cast<double>(prob[r]);
+        const int g = g0 + c;
+        A.token[nb + g] = tok[r];
+        A.parent[nb + g] = s_node[f];
+        A.depth[nb + g] = s_dep[f] + 1;
+        A.score[nb + g] = sc;
         SortEnt e;
-        e.s = 0ull; e.d = 0; e.i = 0x7fffffff;
-        if (c < nc) {
-            int f = 0;
-            while (s_off[f + 1] <= c) ++f;           // the slot whose children cover c
-            const int r = c - s_off[f];
-            const EagleRowHdr* h = hdr(f);
-            const int* tok = reinterpret_cast<const int*>(h + 1);
-            const float* prob = reinterpret_cast<const float*>(tok + K2);
-            const long long nb = static_cast<long long>(b) * G;
-            const double sc = s_sc[f] * static_cast<double>(prob[r]);
-            const int g = g0 + c;
-            A.token[nb + g] = tok[r];
-            A.parent[nb + g] = s_node[f];
-            A.depth[nb + g] = s_dep[f] + 1;
-            A.score[nb + g] = sc;
-            e.s = score_key(sc); e.i = g;
-        }
+        e.s = score_key(sc); e.d = 0; e.i = g;
         s_ent[c] = e;
     }
     __syncthreads();
-    bitonic_sort(s_ent, P);
+    // The next frontier: the Fn children first in that order, each placed
+    // by its rank (how many children sort before it; the order is strict, the
+    // indices being distinct).  One pass and no barrier: a sorting network
+    // spent most of this kernel in its per-stage barriers.
     const int nn = A.Fn < nc ? A.Fn : nc;
-    for (int j = tid; j < A.Fn; j += kGrowThreads)
-        A.front_out[static_cast<long long>(b) * A.Fn + j] = j < nn ? s_ent[j].i : -1;
+    for (int c = tid; c < nc; c += kGrowThreads) {
+        const SortEnt e = s_ent[c];
+        int r = 0;
+        for (int t = 0; t < nc; ++t) r += ent_first(s_ent[t], e) ? 1 : 0;
+        if (r < nn) A.front_out[static_cast<long long>(b) * A.Fn + r] = e.i;
+    }
+    for (int j = nn + tid; j < A.Fn; j += kGrowThreads) A.front_out[static_cast<long long>(b) * A.Fn + j] = -1;
     if (tid == 0) {
         A.num_front_out[b] = nn;
         A.num_gen[b] = g0 + nc;
