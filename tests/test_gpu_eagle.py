@@ -166,3 +166,29 @@ def test_eagle_rerank_ties_and_inconsistent_parents():
     assert list(ref["token"][0, :6]) == [-1, 3, 4, 5, 7, 6]
     g = sv.EagleState(*(torch.from_numpy(st[k]).to(DEV) for k in ("token", "parent", "depth", "score", "num_gen")))
     _tree_equal(sv.eagle_rerank(g, N), ref)
+
+
+@pytest.mark.parametrize("g", [1025, 1026, 3000])
+def test_eagle_rerank_large_node_counts(g):
+    """Rerank of random consistent trees of a thousand nodes and more (a
+    sorting network of 1024 to 4096 entries), with tied scores among
+    siblings; three node counts per case."""
+    B, G, N = 3, 4096, 200
+    rng = np.random.default_rng(g)
+    st = oracle.eagle_init(B, G)
+    for b in range(B):
+        par = np.zeros(g, np.int32)
+        dep = np.zeros(g, np.int32)
+        sc = np.ones(g, np.float64)
+        for i in range(1, g):
+            p = int(rng.integers(0, i))
+            par[i], dep[i] = p, dep[p] + 1
+            sc[i] = sc[p] * (0.5 if rng.random() < 0.2 else float(rng.uniform(0.05, 1.0)))
+        st["token"][b, 1:g] = rng.integers(0, 50000, g - 1)
+        st["parent"][b, 1:g] = par[1:]
+        st["depth"][b, 1:g] = dep[1:]
+        st["score"][b, 1:g] = sc[1:]
+        st["num_gen"][b] = g - b          # three sizes per case
+    ref = oracle.eagle_rerank(st, N)
+    gs = sv.EagleState(*(torch.from_numpy(st[k]).to(DEV) for k in ("token", "parent", "depth", "score", "num_gen")))
+    _tree_equal(sv.eagle_rerank(gs, N), ref)
